@@ -1,0 +1,386 @@
+"""Pins of the float64 oracle against things the pages and the mathematics fix.
+
+None of these compares the oracle with itself: each checks it against a value
+the pages print (tests/golden, cited there), a closed form, an independent
+library routine, a brute-force loop, or a hand-derived worked example, chosen so
+that a dropped term, a wrong sign or index, or a transposed operand fails one.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.stats
+import torch
+
+from oracle import ckv_oracle as O
+from oracle import layout as LY
+from compressed_kv_attention_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def _golden_kv(name):
+    return {row[0]: row[1:] for row in _golden_lines(name)}
+
+
+# ---------------------------------------------------------------- FWHT ----
+
+def _hadamard_closed_form(d):
+    i = np.arange(d)[:, None]
+    j = np.arange(d)[None, :]
+    pc = np.vectorize(lambda v: bin(int(v)).count("1"))(i & j)
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+@pytest.mark.parametrize("d", [1, 2, 4, 8, 16, 64, 128, 512])
+def test_fwht_equals_closed_form_hadamard(d):
+    # H[i, j] = (-1)^popcount(i & j) is the Sylvester matrix in natural order.
+    H = _hadamard_closed_form(d)
+    assert np.array_equal(O.fwht(np.eye(d)), H.T)
+    if d > 1:
+        assert np.array_equal(scipy.linalg.hadamard(d).astype(np.float64), H)
+
+
+@pytest.mark.parametrize("d", [2, 64, 512])
+def test_fwht_orthonormal_roundtrip_parseval(d):
+    rng = np.random.default_rng(d)
+    Hn = O.fwht_orthonormal(np.eye(d))
+    assert np.abs(Hn @ Hn.T - np.eye(d)).max() < 1e-14
+    x = rng.standard_normal((7, d))
+    s = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    back = s * O.fwht_orthonormal(O.fwht_orthonormal(s * x))
+    assert np.abs(back - x).max() < 1e-13
+    assert np.allclose(np.linalg.norm(O.fwht_orthonormal(x), axis=1), np.linalg.norm(x, axis=1),
+                       rtol=1e-14)
+
+
+# --------------------------------------------------------- Lloyd-Max -----
+
+def test_centroids_match_printed_table():
+    printed = np.array([float(r[0]) for r in _golden_lines("lloyd_max_3bit.txt")])
+    assert np.array_equal(printed, O.LLOYD_MAX_3BIT)
+
+
+def _gauss_cells():
+    c = O.LLOYD_MAX_3BIT
+    t = np.concatenate([[-np.inf], (c[1:] + c[:-1]) / 2, [np.inf]])
+    return c, t
+
+
+def test_lloyd_max_centroid_condition():
+    # Each centroid is the conditional mean of N(0,1) over its cell, whose edges
+    # are the midpoints: c_k = (phi(a) - phi(b)) / (Phi(b) - Phi(a)).
+    c, t = _gauss_cells()
+    a, b = t[:-1], t[1:]
+    cond_mean = (scipy.stats.norm.pdf(a) - scipy.stats.norm.pdf(b)) / \
+        (scipy.stats.norm.cdf(b) - scipy.stats.norm.cdf(a))
+    assert np.abs(cond_mean - c).max() < 5e-5
+
+
+def _lloyd_max_mse():
+    c, t = _gauss_cells()
+    total = 0.0
+    for k in range(8):
+        val, _ = scipy.integrate.quad(lambda u: (u - c[k]) ** 2 * scipy.stats.norm.pdf(u),
+                                      t[k], t[k + 1])
+        total += val
+    return total
+
+
+def test_lloyd_max_distortion_and_page_cosine():
+    D = _lloyd_max_mse()
+    assert abs(D - 0.034548) < 2e-5
+    # For a Lloyd-Max quantiser E[u c(u)] = E[c^2] = 1 - D, so the round-trip
+    # cosine tends to sqrt(1 - D); the PolyKV page prints 0.983.
+    page = float(_golden_lines("tbq3_roundtrip_cosine.txt")[0][0])
+    assert round(math.sqrt(1 - D), 3) == page
+
+
+def test_tbq3_montecarlo_cosine_matches_page():
+    page = float(_golden_lines("tbq3_roundtrip_cosine.txt")[0][0])
+    rng = np.random.default_rng(7)
+    d = 512
+    x = rng.standard_normal((3000, d)).astype(np.float16)
+    s = inputs.tbq_signs(d)
+    codes, n16, _ = O.tbq3_quantize(x, s)
+    xh = O.tbq3_dequantize(codes, n16, s)
+    xf = x.astype(np.float64)
+    cos = np.sum(xf * xh, 1) / (np.linalg.norm(xf, axis=1) * np.linalg.norm(xh, axis=1))
+    mean, sem = cos.mean(), cos.std() / math.sqrt(len(cos))
+    assert round(mean, 3) == page
+    assert abs(mean - math.sqrt(1 - _lloyd_max_mse())) < 4 * sem + 2e-4
+
+
+def test_code_frequencies_follow_gaussian_cells():
+    # Rotated, normalised coordinates of random vectors are close to N(0,1):
+    # code counts follow the Gaussian cell probabilities (chi-square test).
+    c, t = _gauss_cells()
+    probs = np.diff(scipy.stats.norm.cdf(t))
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((400, 512)).astype(np.float16)
+    codes, _, _ = O.tbq3_quantize(x, inputs.tbq_signs(512))
+    counts = np.bincount(codes.ravel(), minlength=8)
+    chi2, pval = scipy.stats.chisquare(counts, probs * counts.sum())
+    assert pval > 1e-4, (counts, probs * counts.sum())
+    assert np.allclose(probs[4:], [0.19166, 0.16147, 0.10663, 0.04024], atol=2e-4)
+
+
+def test_nearest_centroid_bruteforce_and_ties():
+    rng = np.random.default_rng(3)
+    u = rng.standard_normal(2000) * 1.5
+    got = O.nearest_centroid(u)
+    for ui, gi in zip(u, got):
+        dists = [abs(ui - ck) for ck in O.LLOYD_MAX_3BIT]
+        assert gi == int(np.argmin(dists))
+    c = O.LLOYD_MAX_3BIT
+    mids = (c[1:] + c[:-1]) / 2
+    # Exact midpoint ties go to the centroid of smaller magnitude; 0 goes to +0.2451.
+    expect = [1, 2, 3, 4, 4, 5, 6]
+    # Use the exact midpoint values the distance computation sees as ties.
+    for k, m in enumerate(mids):
+        if abs(m - c[k]) == abs(m - c[k + 1]):
+            assert O.nearest_centroid(np.array([m]))[0] == expect[k]
+    assert O.nearest_centroid(np.array([0.0]))[0] == 4
+    assert O.nearest_centroid(np.array([-0.0]))[0] == 4
+
+
+# ------------------------------------------------------------- TBQ3 ------
+
+def test_tbq3_worked_example_d4():
+    g = _golden_kv("tbq3_worked_d4.txt")
+    x = np.array([float(v) for v in g["x"]], dtype=np.float16)
+    s = np.array([int(v) for v in g["signs"]], dtype=np.int8)
+    codes, n16, u = O.tbq3_quantize(x, s)
+    assert list(codes) == [int(v) for v in g["codes"]]
+    assert float(n16) == float(g["norm16"][0])
+    assert np.allclose(u, [-2 / math.sqrt(30), 10 / math.sqrt(30), 0.0, -4 / math.sqrt(30)])
+
+
+def test_tbq3_zero_vector_and_idempotence():
+    d = 128
+    s = inputs.tbq_signs(d)
+    codes, n16, _ = O.tbq3_quantize(np.zeros((1, d), np.float16), s)
+    assert (codes == 4).all() and float(n16[0]) == 0.0
+    assert np.array_equal(O.tbq3_dequantize(codes, n16, s), np.zeros((1, d)))
+    # encode(decode(codes)) == codes on codes of random data: the decoded vector
+    # rotates back onto (a ~2 % scaled copy of) the centroids it came from.
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((50, d)).astype(np.float16)
+    c1, n1, _ = O.tbq3_quantize(x, s)
+    xh = O.tbq3_dequantize(c1, n1, s).astype(np.float16)
+    c2, _, _ = O.tbq3_quantize(xh, s)
+    assert np.array_equal(c1, c2)
+
+
+def test_tbq3_sign_then_transform_order_matters():
+    # Applying the sign diagonal after the transform instead of before gives a
+    # different code vector on the worked example (guards the step order).
+    g = _golden_kv("tbq3_worked_d4.txt")
+    x = np.array([float(v) for v in g["x"]])
+    s = np.array([int(v) for v in g["signs"]], dtype=np.float64)
+    wrong_u = s * O.fwht_orthonormal(x) * 2 / math.sqrt(30)
+    assert list(O.nearest_centroid(wrong_u)) != [int(v) for v in g["codes"]]
+
+
+def test_rotated_basis_accumulation_identity():
+    # sum_j p_j V_hat_j = s * H(sum_j p_j (n_j / sqrt d) c[code_j]) / sqrt(d):
+    # accumulating in the rotated basis and de-rotating once is exact.
+    d, T = 64, 50
+    rng = np.random.default_rng(9)
+    s = inputs.tbq_signs(d)
+    x = rng.standard_normal((T, d)).astype(np.float16)
+    codes, n16, _ = O.tbq3_quantize(x, s)
+    Vh = O.tbq3_dequantize(codes, n16, s)
+    p = rng.random(T)
+    direct = p @ Vh
+    rot = (p * n16.astype(np.float64) / math.sqrt(d)) @ O.LLOYD_MAX_3BIT[codes]
+    assert np.abs(direct - s * O.fwht_orthonormal(rot)).max() < 1e-12
+
+
+# ------------------------------------------------------------- q8_0 ------
+
+def test_q8_0_worked_blocks():
+    g = _golden_kv("q8_0_worked.txt")
+    x = np.array([float(v) for v in g["A_x"]], dtype=np.float16)
+    qs, d16 = O.q8_0_quantize(x)
+    assert float(d16[0]) == float(g["A_d16"][0])
+    assert list(qs) == [int(v) for v in g["A_q"]]
+    xb = np.zeros(32, np.float16)
+    xb[0] = float(g["B_amax"][0])
+    qs, d16 = O.q8_0_quantize(xb)
+    assert float(d16[0]) == float(g["B_d16"][0]) and qs[0] == 127
+
+
+def test_q8_0_bounds_and_special_blocks():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((500, 128)) * rng.choice([1e-2, 1.0, 30.0], (500, 1))).astype(np.float16)
+    x[3] = 0
+    qs, d16 = O.q8_0_quantize(x)
+    xb = x.astype(np.float64).reshape(500, 4, 32)
+    d = d16.astype(np.float64)[..., None]
+    err = np.abs(xb - qs.reshape(500, 4, 32) * d)
+    normal = d16.astype(np.float64) >= 6.103515625e-05
+    assert (err[normal] <= d[normal] / 2).all()
+    assert (np.abs(qs) <= 127).all()
+    # the largest element of every nonzero block maps to +/-127
+    amax_idx = np.abs(xb).argmax(-1)
+    top = np.take_along_axis(np.abs(qs.reshape(500, 4, 32)).astype(int), amax_idx[..., None], -1)[..., 0]
+    nz = d16.astype(np.float64) > 0
+    assert (top[nz & normal] == 127).all()
+    assert (qs[3] == 0).all() and (d16[3] == 0).all()
+
+
+def test_q8_0_fp32_and_fp64_decide_identically():
+    # Reading of the rounding precision: the CUDA packer divides in fp32, the
+    # oracle in fp64. For fp16 inputs both give the same fp16 scale for every
+    # possible amax, and the same codes.
+    amax = np.arange(1, 0x7C00, dtype=np.uint16).view(np.float16)
+    d64 = (amax.astype(np.float64) / 127.0).astype(np.float16)
+    d32 = (amax.astype(np.float32) / np.float32(127.0)).astype(np.float16)
+    assert np.array_equal(d64.view(np.uint16), d32.view(np.uint16))
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal((2000, 64)) * 3).astype(np.float16)
+    qs, d16 = O.q8_0_quantize(x)
+    r32 = x.astype(np.float32).reshape(2000, 2, 32) / d16.astype(np.float32)[..., None]
+    q32 = np.clip(np.sign(r32) * np.floor(np.abs(r32) + np.float32(0.5)), -127, 127)
+    assert np.array_equal(q32.reshape(2000, 64).astype(np.int8), qs)
+
+
+# -------------------------------------------------------- attention ------
+
+def test_attention_matches_torch_sdpa_float64():
+    rng = np.random.default_rng(4)
+    R, T, D = 6, 37, 32
+    q, k, v = rng.standard_normal((R, D)), rng.standard_normal((T, D)), rng.standard_normal((T, D))
+    scale = 1 / math.sqrt(D)
+    vis = rng.random((R, T)) < 0.7
+    vis[:, 0] = True
+    o, lse = O.attention(q, k, v, scale, visible=vis)
+    tq, tk, tv = (torch.from_numpy(a)[None, None] for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=torch.from_numpy(vis)[None, None], scale=scale)[0, 0].numpy()
+    assert np.abs(o - ref).max() < 1e-12
+    logits = torch.from_numpy(scale * q @ k.T).masked_fill(~torch.from_numpy(vis), -math.inf)
+    assert np.abs(lse - torch.logsumexp(logits, dim=1).numpy()).max() < 1e-12
+
+
+def test_attention_bruteforce_tiny():
+    rng = np.random.default_rng(6)
+    for T in (1, 2, 3, 4):
+        q, k, v = rng.standard_normal(5), rng.standard_normal((T, 5)), rng.standard_normal((T, 3))
+        logits = [0.7 * sum(q[a] * k[j][a] for a in range(5)) for j in range(T)]
+        w = [math.exp(l) for l in logits]
+        tot = sum(w)
+        expect = [sum(w[j] * v[j][c] for j in range(T)) / tot for c in range(3)]
+        o, lse = O.attention(q[None], k, v, 0.7)
+        assert np.allclose(o[0], expect, rtol=1e-13, atol=1e-14)
+        assert abs(lse[0] - math.log(tot)) < 1e-12
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(8)
+    k, v = rng.standard_normal((9, 4)), rng.standard_normal((9, 4))
+    o, lse = O.attention(rng.standard_normal((1, 4)), k[:1], v[:1], 0.5)
+    assert np.allclose(o[0], v[0])                      # one key -> its value
+    o, lse = O.attention(np.zeros((1, 4)), k, v, 0.5)
+    assert np.allclose(o[0], v.mean(0)) and abs(lse[0] - math.log(9)) < 1e-12  # q = 0 -> mean
+    o, _ = O.attention(rng.standard_normal((1, 4)), np.repeat(k[:1], 9, 0), v, 0.5)
+    assert np.allclose(o[0], v.mean(0))                 # identical keys -> mean
+    o, lse = O.attention(np.ones((2, 4)), k[:0], v[:0], 0.5)
+    assert (o == 0).all() and (lse == -np.inf).all()    # no key -> 0, -inf
+    vis = np.zeros((2, 9), bool)
+    vis[1, 3] = True
+    o, lse = O.attention(np.ones((2, 4)), k, v, 0.5, visible=vis)
+    assert (o[0] == 0).all() and lse[0] == -np.inf and np.allclose(o[1], v[3])
+
+
+def test_lse_merge_equals_single_pass_over_any_partition():
+    rng = np.random.default_rng(10)
+    R, T, D = 4, 60, 16
+    q, k, v = rng.standard_normal((R, D)), rng.standard_normal((T, D)), rng.standard_normal((T, D))
+    full_o, full_lse = O.attention(q, k, v, 0.3)
+    for trial in range(5):
+        cuts = np.sort(rng.integers(0, T + 1, size=4))
+        edges = [0, *cuts, T]
+        parts = [O.attention(q, k[a:b], v[a:b], 0.3) for a, b in zip(edges[:-1], edges[1:])]
+        o, lse = O.lse_merge([p[0] for p in parts], [p[1] for p in parts])
+        assert np.abs(o - full_o).max() < 1e-12 and np.abs(lse - full_lse).max() < 1e-12
+    # every partial empty -> 0, -inf
+    o, lse = O.lse_merge([np.zeros((2, 3))] * 3, [np.full(2, -np.inf)] * 3)
+    assert (o == 0).all() and (lse == -np.inf).all()
+
+
+def test_decode_and_prefill_reference_gqa_and_causality():
+    rng = np.random.default_rng(12)
+    Hq, Hkv, D, T = 4, 2, 16, 20
+    k, v = rng.standard_normal((Hkv, T, D)), rng.standard_normal((Hkv, T, D))
+    q = rng.standard_normal((3, Hq, D))
+    o, lse = O.decode_reference(q, k, v, 15, 0.25)
+    for h in range(Hq):
+        oh, lh = O.attention(q[:, h], k[h // 2, :15], v[h // 2, :15], 0.25)
+        assert np.array_equal(o[:, h], oh) and np.array_equal(lse[:, h], lh)
+    o, lse = O.prefill_reference(q, k[:, :13], v[:, :13], 10, 0.25)
+    for i in range(3):
+        for h in range(Hq):
+            oh, lh = O.attention(q[i:i + 1, h], k[h // 2, :11 + i], v[h // 2, :11 + i], 0.25)
+            assert np.allclose(o[i, h], oh[0], rtol=0, atol=1e-14)
+
+
+# ----------------------------------------------------------- layout ------
+
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
+def test_layout_is_a_bijection_and_roundtrips(D):
+    rec = LY.record_bytes(D)
+    kofs, sofs, nofs = LY.k_code_offsets(D), LY.k_scale_offsets(D), LY.v_norm_offsets(D)
+    vbits = LY.v_code_bits(D)
+    byte_owner = np.zeros(rec, int)
+    np.add.at(byte_owner, kofs.ravel(), 1)
+    np.add.at(byte_owner, sofs.ravel(), 1)
+    np.add.at(byte_owner, sofs.ravel() + 1, 1)
+    np.add.at(byte_owner, nofs, 1)
+    np.add.at(byte_owner, nofs + 1, 1)
+    vb = np.zeros(6 * D * 8, int)
+    np.add.at(vb, vbits.ravel() - 17 * D * 8, 1)
+    assert (vb == 1).all()                                   # every V bit used once
+    assert (byte_owner[:17 * D] == 1).all() and (byte_owner[23 * D:] == 1).all()
+    rng = np.random.default_rng(D)
+    T = 37
+    qs = rng.integers(-127, 128, (T, D)).astype(np.int8)
+    d16 = rng.standard_normal((T, D // 32)).astype(np.float16)
+    codes = rng.integers(0, 8, (T, D)).astype(np.uint8)
+    n16 = rng.random(T).astype(np.float16)
+    recs = LY.pack_records(qs, d16, codes, n16, 48)
+    back = LY.unpack_records(recs, T, D)
+    for a, b in zip((qs, d16, codes, n16), back):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+def test_layout_hand_offsets_and_sizes():
+    D = 512
+    # K code of position 9, dim 37: block 1, lane 4*(9%8) + (37%32)//8 = 4, half 1, byte 5.
+    assert LY.k_code_offsets(D)[9, 37] == (1 * 32 + 4) * 16 + 8 + 5
+    # V code bits of position 3, dim 70: G=64, g=1, u=6, lane 4+1=5, pair 4*3+0+0=12,
+    # first bit 6*12+3 = 75 -> stream byte 9 (bit 3), granule 16 -> offset (0*32+5)*16+9.
+    assert LY.v_code_bits(D)[3, 70, 0] == (17 * D + 5 * 16 + 9) * 8 + 3
+    # 738 bytes per token at d=512, 186 at d=128
+    assert LY.record_bytes(512) == 16 * 738 and LY.record_bytes(128) == 16 * 186
+    assert inputs.compressed_bytes_per_token(512) == 738
+
+
+def test_layout_code_bits_against_page_compression_ratio():
+    # K codes (8 bits) + V codes (3 bits) against fp16 K and V: 32 / 11 = 2.909,
+    # the page's 2.91x; 15 agents sharing one pooled copy gives ~15 x that.
+    g = _golden_kv("compression.txt")
+    D = 512
+    code_bytes = LY.k_code_offsets(D).size + LY.v_code_bits(D).size // 8
+    ratio = 16 * 2 * 2 * D / code_bytes
+    assert round(ratio, 2) == float(g["ratio"][0])
+    pooled = float(g["dense_gb"][0]) / float(g["pooled_gb"][0])
+    assert abs(pooled / (int(g["agents"][0]) * ratio) - 1) < 0.02
