@@ -1,0 +1,185 @@
+"""ctypes binding of libckv.so (include/ckv.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls, without the
+``ckv_`` prefix, takes torch tensors for device memory, passes their pointers
+and the current (or given) CUDA stream, and raises ``CkvError`` on a non-OK
+status. No computation happens in Python: every step of the path runs in the
+library's kernels. If the library is missing, loading it raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libckv.so")
+
+CKV_OK = 0
+STATUS_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "WORKSPACE", -4: "CUDA",
+                -5: "DEVICE_FLAG"}
+
+
+class CkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class CkvCacheStruct(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("capacity", ctypes.c_int64), ("data", ctypes.c_void_p),
+                ("v_signs", ctypes.c_void_p)]
+
+
+_lib = None
+
+_c_int, _c_i64, _c_size, _c_f, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+_cache_p = ctypes.POINTER(CkvCacheStruct)
+
+SIGNATURES = {
+    "ckv_version": (_c_int, []),
+    "ckv_last_error": (ctypes.c_char_p, []),
+    "ckv_cache_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_i64]),
+    "ckv_kv_pack": (_c_int, [_cache_p, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i64, _vp]),
+    "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
+    "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
+                                 _vp, _c_size, _vp]),
+    "ckv_attn_decode_f16_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
+    "ckv_attn_decode_f16": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
+                                     _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "ckv_lse_merge": (_c_int, [_c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _c_i64, _c_int, _vp, _vp,
+                               _vp]),
+    "ckv_attn_prefill_workspace": (_c_size, [_cache_p, _c_int, _c_int]),
+    "ckv_attn_prefill": (_c_int, [_cache_p, _c_i64, _vp, _c_int, _c_int, _vp, _vp, _c_f, _vp, _vp, _vp,
+                                  _c_size, _vp]),
+    "ckv_read_device_flag": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
+}
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libckv.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with compressed_kv_attention_gb300/build.py "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != CKV_OK:
+        raise CkvError(status, load().ckv_last_error().decode())
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+class PackedCache:
+    """A packed q8_0-K / TBQ3-V cache in device memory plus its geometry."""
+
+    def __init__(self, head_dim: int, n_kv_heads: int, batch: int, capacity: int, signs,
+                 device="cuda", data=None):
+        import torch
+        self.head_dim, self.n_kv_heads, self.batch, self.capacity = head_dim, n_kv_heads, batch, capacity
+        nbytes = cache_bytes(head_dim, n_kv_heads, batch, capacity)
+        if nbytes == 0:
+            raise CkvError(-1, "invalid cache geometry")
+        self.data = data if data is not None else torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        self.signs = torch.as_tensor(signs, dtype=torch.int8).to(device)
+        self.struct = CkvCacheStruct(head_dim, n_kv_heads, batch, 0, capacity, _ptr(self.data),
+                                     _ptr(self.signs))
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+def version() -> int:
+    return load().ckv_version()
+
+
+def cache_bytes(head_dim: int, n_kv_heads: int, batch: int, capacity: int) -> int:
+    return int(load().ckv_cache_bytes(head_dim, n_kv_heads, batch, capacity))
+
+
+def kv_pack(cache: PackedCache, tok_offset: int, k, v, stream=None):
+    """Pack fp16 K, V shaped [batch, n_tok, n_kv_heads, D] at positions [tok_offset, +n_tok)."""
+    n_tok = k.shape[1]
+    _check(load().ckv_kv_pack(cache.ref(), tok_offset, n_tok, _ptr(k), _ptr(v), k.stride(1), k.stride(0),
+                              _stream(stream)))
+
+
+def attn_decode_workspace(cache: PackedCache, max_seq_len: int, n_q: int, n_q_heads: int,
+                          n_split: int = 0) -> int:
+    return int(load().ckv_attn_decode_workspace(cache.ref(), max_seq_len, n_q, n_q_heads, n_split))
+
+
+def attn_decode(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,
+                n_split: int = 0, stream=None):
+    """q: fp16 [batch, n_q, n_q_heads, D]; out float32 like q; lse float32 [batch, n_q, n_q_heads]."""
+    _, n_q, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_decode(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
+                                  n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)))
+
+
+def attn_decode_f16_workspace(head_dim: int, n_kv_heads: int, batch: int, max_seq_len: int, n_q: int,
+                              n_q_heads: int, n_split: int = 0) -> int:
+    return int(load().ckv_attn_decode_f16_workspace(head_dim, n_kv_heads, batch, max_seq_len, n_q,
+                                                    n_q_heads, n_split))
+
+
+def attn_decode_f16(k, v, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,
+                    n_split: int = 0, stream=None):
+    """k, v: fp16 [batch, n_kv_heads, capacity, D]; q fp16 [batch, n_q, n_q_heads, D]."""
+    batch, n_kv_heads, capacity, D = k.shape
+    _, n_q, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_decode_f16(_ptr(k), _ptr(v), D, n_kv_heads, batch, capacity, _ptr(seq_len),
+                                      max_seq_len, _ptr(q), n_q, n_q_heads, scale, n_split, _ptr(out),
+                                      _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def lse_merge(o_parts, lse_parts, out, lse, stream=None):
+    """Merge partials: each o part float32 [n_rows, d], each lse part float32 [n_rows]."""
+    n = len(o_parts)
+    optrs = (_vp * n)(*[_ptr(o) for o in o_parts])
+    lptrs = (_vp * n)(*[_ptr(x) for x in lse_parts])
+    n_rows = lse_parts[0].numel()
+    d = o_parts[0].numel() // max(n_rows, 1)
+    _check(load().ckv_lse_merge(n, optrs, lptrs, n_rows, d, _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def attn_prefill_workspace(cache: PackedCache, n_new: int, n_q_heads: int) -> int:
+    return int(load().ckv_attn_prefill_workspace(cache.ref(), n_new, n_q_heads))
+
+
+def attn_prefill(cache: PackedCache, n_cached: int, q, k_new, v_new, scale: float, out, lse, workspace,
+                 stream=None):
+    """q: bf16 [batch, n_new, n_q_heads, D]; k_new, v_new fp16 [batch, n_new, n_kv_heads, D]."""
+    _, n_new, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_prefill(cache.ref(), n_cached, _ptr(q), n_new, n_q_heads, _ptr(k_new),
+                                   _ptr(v_new), scale, _ptr(out), _ptr(lse), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)))
+
+
+def read_device_flag(workspace, stream=None) -> int:
+    flag = ctypes.c_int32(0)
+    status = load().ckv_read_device_flag(_ptr(workspace), ctypes.byref(flag), _stream(stream))
+    if status not in (CKV_OK, -5):
+        _check(status)
+    return int(flag.value)

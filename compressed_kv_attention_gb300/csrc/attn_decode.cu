@@ -1,0 +1,374 @@
+// attn_decode.cu — split-K flash-decode over the packed q8_0-K / TBQ3-V cache,
+// and the split merge that applies the inverse transform once per output row.
+//
+// The pages' decode reads the compressed cache in-register inside the
+// attention kernel rather than materialising it (PolyKV page, "F5 M6 — PolyKV
+// (shared compressed KV pool)", section "S2 perf-path Level B": K and V read
+// in-register, the transform applied only to the small output; section "S2
+// perf-path — turbo-MMA verify kernel + scalar-K/turbo-V fused decode": K in
+// true space, V in the rotated basis, output inverse only). The design here:
+//
+//  * One CTA = one (sequence, kv head, row group of 8 query vectors, KV split).
+//    A producer warp streams the split's tile records (16 tokens each, one
+//    contiguous bulk copy per stage of NP records) into a 4-stage shared-memory
+//    ring guarded by mbarriers; 8 consumer warps take one record each.
+//  * S^T = K_hat Q^T on tensor cores (mma.sync m16n8k16): the int8 codes turn
+//    into exact fp16 integers with two byte permutes and a subtraction, each
+//    32-dim block is multiplied into its own accumulator and scaled by its fp16
+//    scale (so K_hat = q * d16 is exact, never rounded to fp16).
+//  * P'^T = exp2(S - m) * norm / (fp16) and O^T += C^T P'^T where C holds the
+//    Lloyd-Max centroids selected by the 3-bit codes: two codes (same dim, two
+//    adjacent positions) index a 64-entry fp16x2 table replicated per lane in
+//    shared memory, so every lookup is conflict-free.
+//  * The CTA merges its tile groups and writes one partial (m, l, O_rot) per
+//    row; the merge kernel combines the splits exactly (log-sum-exp), divides,
+//    runs one inverse Walsh-Hadamard transform and the sign flip per row.
+#include "ckv_kernels.cuh"
+#include "decode_common.cuh"
+
+namespace ckv {
+
+namespace {
+
+__constant__ float kCentroids[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
+                                 0.2451f,  0.7560f,  1.3439f,  2.1520f};
+
+template <int D>
+struct CDec : DecodeShape<D> {
+  using Sh = DecodeShape<D>;
+  static constexpr int REC = record_bytes(D);
+  static constexpr int STAGE = Sh::NP * REC;
+  static constexpr int NSTAGE = 4;
+  static constexpr int THREADS = (Sh::NCW + 1) * 32;
+  static constexpr int VW = 3 * Sh::MT_W / 4;   // V-code words per lane per warp
+  static constexpr int GR = v_granule(D);       // stream granule bytes
+  static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
+  static constexpr int RING = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
+  static constexpr int OFF_XCHG = (RING + 127) / 128 * 128;
+  static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
+  static constexpr int OFF_BAR = OFF_ML + Sh::NP * 16 * 4;
+  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 16;
+};
+
+// Load `n` bytes (4, 8 or 16) from shared memory into consecutive words.
+template <int N>
+__device__ __forceinline__ void lds_words(uint32_t* w, uint32_t addr) {
+  if constexpr (N == 16) {
+    const uint4 v = lds128(addr);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (N == 8) {
+    const uint2 v = lds64(addr);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    w[0] = lds32(addr);
+  }
+}
+
+// Bits [bit, bit + 6) of the little-endian word array, moved to bits [7, 13).
+template <int VW>
+__device__ __forceinline__ uint32_t field_x128(const uint32_t* w, int bit) {
+  const int wi = bit >> 5, sh = bit & 31;
+  uint32_t x;
+  if (sh < 7) {
+    x = w[wi] << (7 - sh);
+  } else if (sh <= 26) {
+    x = w[wi] >> (sh - 7);
+  } else {
+    x = __funnelshift_r(w[wi], (wi + 1 < VW) ? w[wi + 1] : 0u, sh - 7);
+  }
+  return x & 0x1F80u;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(DecodeArgs a) {
+  using C = CDec<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(16) uint32_t s_lut[64 * 32];
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, rg = blockIdx.y, bh = blockIdx.z;
+  const int b = bh / a.n_kv_heads, kvh = bh % a.n_kv_heads;
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int R = group_q * a.n_q;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::NSTAGE;
+  float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XCHG);
+  float* mlbuf = reinterpret_cast<float*>(smem + C::OFF_ML);
+
+  int seqlen = a.seq_len[b];
+  const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
+  if (seqlen < 0 || seqlen > lim) {
+    if (threadIdx.x == 0) raise_flag(a.flag, kFlagSeqLenRange);
+    seqlen = 0;
+  }
+  const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
+  const int64_t tile_begin = split * n_tiles / a.n_split;
+  const int64_t tile_end = (split + 1) * n_tiles / a.n_split;
+  const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+  const uint8_t* gbase = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) * C::REC;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NCW);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == C::NCW) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      int issued = 0;
+      for (int it = 0; it < n_iters; ++it) {
+        const int s = it % C::NSTAGE;
+        if (it >= C::NSTAGE && !*(volatile int*)&s_abort) {
+          if (!mbar_wait(&empty[s], ((it / C::NSTAGE) - 1) & 1)) {
+            *(volatile int*)&s_abort = 1;
+            raise_flag(a.flag, kFlagWaitTimeout);
+          }
+        }
+        if (*(volatile int*)&s_abort) break;
+        const int64_t first = tile_begin + (int64_t)it * C::NP;
+        const int64_t left = tile_end - first;
+        const uint32_t cnt = left < C::NP ? (uint32_t)left : (uint32_t)C::NP;
+        mbar_arrive_expect_tx(&full[s], cnt * C::REC);
+        bulk_g2s(smem + s * C::STAGE, gbase + first * C::REC, cnt * C::REC, &full[s]);
+        ++issued;
+      }
+      // Do not leave while a copy may still be landing in this CTA's memory.
+      const int k0 = issued > C::NSTAGE ? issued - C::NSTAGE : 0;
+      for (int k = k0; k < issued; ++k) {
+        if (!mbar_wait(&full[k % C::NSTAGE], (k / C::NSTAGE) & 1)) {
+          raise_flag(a.flag, kFlagWaitTimeout);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers --
+  const int tid = threadIdx.x;  // 0 .. 255
+  const int group = warp / C::WT, wh = warp % C::WT;
+  const int g = lane >> 2, t = lane & 3;
+
+  // Centroid-pair table: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
+  for (int e = tid; e < 64 * 32; e += C::NCW * 32) {
+    const int f = e >> 5;
+    const __half lo = __float2half_rn(kCentroids[f & 7]);
+    const __half hi = __float2half_rn(kCentroids[f >> 3]);
+    s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+
+  uint32_t qf[C::NB_W][4];
+  {
+    const int rr = rg * 8 + g;
+    int qi = 0, h = 0;
+    const bool ok = rr < R;
+    if (ok) row_to_query(rr, group_q, kvh, qi, h);
+    const __half* qrow = a.q + ((int64_t)(b * a.n_q + qi) * a.n_q_heads + h) * D;
+    load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
+  }
+  float acc[C::MT_W][4];
+#pragma unroll
+  for (int i = 0; i < C::MT_W; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  SoftmaxState st{-INFINITY, -INFINITY, 0.0f, 0.0f};
+  named_bar(1, C::NCW * 32);  // table ready
+
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t lut = smem_u32(s_lut) + (lane << 2);
+
+  for (int it = 0; it < n_iters; ++it) {
+    const int s = it % C::NSTAGE;
+    if (!*(volatile int*)&s_abort) {
+      if (!mbar_wait(&full[s], (it / C::NSTAGE) & 1)) {
+        *(volatile int*)&s_abort = 1;
+        raise_flag(a.flag, kFlagWaitTimeout);
+      }
+    }
+    const int64_t tile = tile_begin + (int64_t)it * C::NP + group;
+    if (tile < tile_end) {
+      const uint32_t rb = ring + s * C::STAGE + group * C::REC;
+      const int64_t tpos = tile * kTile;
+
+      // Scales of positions g and g+8 for this warp's blocks, and the V norms.
+      uint32_t sc0[C::NB_W / 2], sc1[C::NB_W / 2];
+      lds_words<C::NB_W * 2>(sc0, rb + k_scale_offset(D) + g * 2 * C::NB + wh * 2 * C::NB_W);
+      lds_words<C::NB_W * 2>(sc1, rb + k_scale_offset(D) + (g + 8) * 2 * C::NB + wh * 2 * C::NB_W);
+      const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * g)));
+      const float n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * (g + 8))));
+
+      // ---- S^T = K_hat Q^T, one accumulator per 32-dim block, scaled by d16 ----
+      float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int i = 0; i < C::NB_W; ++i) {
+        const int blk = wh * C::NB_W + i;
+        const uint4 kk = lds128(rb + (blk * 32 + lane) * 16);
+        uint32_t a0s0, a2s0, a0s1, a2s1, a1s0, a3s0, a1s1, a3s1;
+        i8x4_to_half2x2(kk.x, a0s0, a2s0);
+        i8x4_to_half2x2(kk.y, a0s1, a2s1);
+        i8x4_to_half2x2(kk.z, a1s0, a3s0);
+        i8x4_to_half2x2(kk.w, a1s1, a3s1);
+        float c[4];
+        mma16816_zc(c, a0s0, a1s0, a2s0, a3s0, qf[i][0], qf[i][1]);
+        mma16816(c, a0s1, a1s1, a2s1, a3s1, qf[i][2], qf[i][3]);
+        const __half2 d0h = *reinterpret_cast<const __half2*>(&sc0[i >> 1]);
+        const __half2 d1h = *reinterpret_cast<const __half2*>(&sc1[i >> 1]);
+        const float d0 = (i & 1) ? __high2float(d0h) : __low2float(d0h);
+        const float d1 = (i & 1) ? __high2float(d1h) : __low2float(d1h);
+        S[0] = fmaf(d0, c[0], S[0]);
+        S[1] = fmaf(d0, c[1], S[1]);
+        S[2] = fmaf(d1, c[2], S[2]);
+        S[3] = fmaf(d1, c[3], S[3]);
+      }
+      if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, it & 1, lane);
+
+      uint32_t pb0, pb1;
+      softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, n0, n1, st,
+                            acc, pb0, pb1);
+
+      // ---- O^T += C^T P'^T straight from the 3-bit codes ----
+      uint32_t vw[C::VW];
+#pragma unroll
+      for (int c3 = 0; c3 < 3; ++c3)
+        lds_words<C::GR>(vw + c3 * (C::GR / 4),
+                         rb + v_code_offset(D) + ((wh * 3 + c3) * 32 + lane) * C::GR);
+#pragma unroll
+      for (int i = 0; i < C::MT_W; ++i) {
+        uint32_t av[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) av[j] = lds32(lut + field_x128<C::VW>(vw, 6 * (4 * i + j)));
+        mma16816(acc[i], av[0], av[1], av[2], av[3], pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
+  float* part_out = a.part + ((gid * a.n_split + split) * 8) * D;
+  float* ml_out = a.ml + ((gid * a.n_split + split) * 8) * 2;
+  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, lane, tid,
+                              part_out, ml_out);
+}
+
+// --------------------------------------------------------------- merge --
+
+// One CTA per output row, one thread per dim: combine the splits exactly,
+// normalise, and (compressed cache) apply the inverse transform and sign flip:
+// O = s * H_D(O_rot) / D, where O_rot accumulated p * norm * centroid.
+template <int D, bool ROT>
+__global__ void __launch_bounds__(D) decode_merge_kernel(MergeArgs a) {
+  __shared__ float sx[D];
+  const int row = blockIdx.x;
+  const int64_t gid = row >> 3;
+  const int r = row & 7;
+  const int rgi = static_cast<int>(gid % a.n_row_groups);
+  const int bh = static_cast<int>(gid / a.n_row_groups);
+  const int b = bh / a.n_kv_heads, kvh = bh % a.n_kv_heads;
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int rr = rgi * 8 + r;
+  if (rr >= group_q * a.n_q) return;
+  int qi, h;
+  row_to_query(rr, group_q, kvh, qi, h);
+  const int d = threadIdx.x;
+
+  const float* mlp = a.ml + (gid * a.n_split * 8 + r) * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, mlp[s * 16]);
+  float L = 0.0f, acc = 0.0f;
+  const float* pp = a.part + (gid * a.n_split * 8 + r) * D + d;
+  if (M != -INFINITY) {
+    for (int s = 0; s < a.n_split; ++s) {
+      const float m = mlp[s * 16];
+      if (m == -INFINITY) continue;
+      const float w = exp2f(m - M);
+      L = fmaf(w, mlp[s * 16 + 1], L);
+      acc = fmaf(w, pp[(int64_t)s * 8 * D], acc);
+    }
+  }
+  const bool valid = L > 0.0f;
+  float v = valid ? acc / L : 0.0f;
+  if constexpr (ROT) {
+#pragma unroll
+    for (int hh = 1; hh < 32 && hh < D; hh <<= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, hh);
+      v = (d & hh) ? (o - v) : (v + o);
+    }
+#pragma unroll
+    for (int hh = 32; hh < D; hh <<= 1) {
+      sx[d] = v;
+      __syncthreads();
+      const float o = sx[d ^ hh];
+      __syncthreads();
+      v = (d & hh) ? (o - v) : (v + o);
+    }
+    v = (a.signs[d] < 0 ? -v : v) * (1.0f / D);
+  }
+  const int64_t orow = (int64_t)(b * a.n_q + qi) * a.n_q_heads + h;
+  a.out[orow * D + d] = v;
+  if (d == 0) a.lse[orow] = valid ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
+size_t decode_smem_bytes(int head_dim) {
+  switch (head_dim) {
+    case 64: return CDec<64>::SMEM;
+    case 128: return CDec<128>::SMEM;
+    case 256: return CDec<256>::SMEM;
+    case 512: return CDec<512>::SMEM;
+    default: return 0;
+  }
+}
+
+template <int D>
+static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
+  using C = CDec<D>;
+  static bool configured = false;  // per process; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
+  attn_decode_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.head_dim) {
+    case 64: return launch_decode_d<64>(a, stream);
+    case 128: return launch_decode_d<128>(a, stream);
+    case 256: return launch_decode_d<256>(a, stream);
+    case 512: return launch_decode_d<512>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int D>
+static cudaError_t launch_merge_d(const MergeArgs& a, cudaStream_t stream) {
+  const int64_t rows = (int64_t)a.batch * a.n_kv_heads * a.n_row_groups * 8;
+  if (a.signs)
+    decode_merge_kernel<D, true><<<static_cast<unsigned>(rows), D, 0, stream>>>(a);
+  else
+    decode_merge_kernel<D, false><<<static_cast<unsigned>(rows), D, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_merge(const MergeArgs& a, cudaStream_t stream) {
+  switch (a.head_dim) {
+    case 64: return launch_merge_d<64>(a, stream);
+    case 128: return launch_merge_d<128>(a, stream);
+    case 256: return launch_merge_d<256>(a, stream);
+    case 512: return launch_merge_d<512>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ckv

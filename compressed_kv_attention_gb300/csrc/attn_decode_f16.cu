@@ -1,0 +1,142 @@
+// attn_decode_f16.cu — split-K decode over a dense fp16 KV cache, emitting
+// (partial) outputs and log-sum-exps in the same form as the compressed
+// decode. It serves the private, uncompressed per-agent tails of a shared pool
+// (PolyKV page, "F5 M6 — PolyKV (shared compressed KV pool)", section "S1 —
+// SharedKVPool": one shared prefix plus a private suffix per agent; the
+// per-agent cost is just the suffix).
+//
+// Same warp formulation as the compressed decode (see decode_common.cuh); the
+// operands come straight from global memory as fp16 fragments (16-byte loads
+// per lane), so no staging ring and no producer warp.
+#include "ckv_kernels.cuh"
+#include "decode_common.cuh"
+
+namespace ckv {
+
+template <int D>
+struct FDec : DecodeShape<D> {
+  using Sh = DecodeShape<D>;
+  static constexpr int THREADS = Sh::NCW * 32;
+  static constexpr int OFF_XCHG = Sh::NP * Sh::RED_FLOATS * 4;
+  static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
+  static constexpr int SMEM = OFF_ML + Sh::NP * 16 * 4;
+};
+
+template <int D>
+__global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(DecodeArgs a) {
+  using C = FDec<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int split = blockIdx.x, rg = blockIdx.y, bh = blockIdx.z;
+  const int b = bh / a.n_kv_heads, kvh = bh % a.n_kv_heads;
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int R = group_q * a.n_q;
+  const int group = warp / C::WT, wh = warp % C::WT;
+  const int g = lane >> 2, t = lane & 3;
+  float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XCHG);
+  float* mlbuf = reinterpret_cast<float*>(smem + C::OFF_ML);
+
+  int seqlen = a.seq_len[b];
+  const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
+  if (seqlen < 0 || seqlen > lim) {
+    if (tid == 0) raise_flag(a.flag, kFlagSeqLenRange);
+    seqlen = 0;
+  }
+  const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
+  const int64_t tile_begin = split * n_tiles / a.n_split;
+  const int64_t tile_end = (split + 1) * n_tiles / a.n_split;
+  const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+  const __half* kb = a.k16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
+  const __half* vb = a.v16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
+
+  uint32_t qf[C::NB_W][4];
+  {
+    const int rr = rg * 8 + g;
+    int qi = 0, h = 0;
+    const bool ok = rr < R;
+    if (ok) row_to_query(rr, group_q, kvh, qi, h);
+    const __half* qrow = a.q + ((int64_t)(b * a.n_q + qi) * a.n_q_heads + h) * D;
+    load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
+  }
+  float acc[C::MT_W][4];
+#pragma unroll
+  for (int i = 0; i < C::MT_W; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  SoftmaxState st{-INFINITY, -INFINITY, 0.0f, 0.0f};
+  const int dbase = C::GD * g + 2 * wh * C::MT_W;  // first output dim of this lane's m-tiles
+
+  for (int it = 0; it < n_iters; ++it) {
+    const int64_t tile = tile_begin + (int64_t)it * C::NP + group;
+    if (tile >= tile_end) break;  // uniform across the warps of a group
+    const int64_t tpos = tile * kTile;
+    // ---- S^T = K Q^T ----
+    float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const __half* k0p = kb + (tpos + g) * D + 8 * t;
+    const __half* k1p = kb + (tpos + g + 8) * D + 8 * t;
+#pragma unroll
+    for (int i = 0; i < C::NB_W; ++i) {
+      const int blk = wh * C::NB_W + i;
+      const uint4 k0 = __ldg(reinterpret_cast<const uint4*>(k0p + blk * 32));
+      const uint4 k1 = __ldg(reinterpret_cast<const uint4*>(k1p + blk * 32));
+      mma16816(S, k0.x, k1.x, k0.y, k1.y, qf[i][0], qf[i][1]);
+      mma16816(S, k0.z, k1.z, k0.w, k1.w, qf[i][2], qf[i][3]);
+    }
+    if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, it & 1, lane);
+    uint32_t pb0, pb1;
+    softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, 1.0f, 1.0f,
+                          st, acc, pb0, pb1);
+    // ---- O^T += V^T P^T: lane reads positions 2t, 2t+1, 2t+8, 2t+9 ----
+    const __half* vp = vb + tpos * D + dbase;
+#pragma unroll
+    for (int c4 = 0; c4 < C::MT_W / 4; ++c4) {
+      const uint4 e0 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t) * D + c4 * 8));
+      const uint4 o0 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 1) * D + c4 * 8));
+      const uint4 e1 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 8) * D + c4 * 8));
+      const uint4 o1 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 9) * D + c4 * 8));
+      const uint32_t we[4] = {e0.x, e0.y, e0.z, e0.w}, wo[4] = {o0.x, o0.y, o0.z, o0.w};
+      const uint32_t xe[4] = {e1.x, e1.y, e1.z, e1.w}, xo[4] = {o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a0) : "r"(we[j]), "r"(wo[j]));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a1) : "r"(we[j]), "r"(wo[j]));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a2) : "r"(xe[j]), "r"(xo[j]));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a3) : "r"(xe[j]), "r"(xo[j]));
+        mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pb0, pb1);
+      }
+    }
+  }
+
+  const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
+  float* part_out = a.part + ((gid * a.n_split + split) * 8) * D;
+  float* ml_out = a.ml + ((gid * a.n_split + split) * 8) * 2;
+  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, lane, tid,
+                              part_out, ml_out);
+}
+
+template <int D>
+static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
+  using C = FDec<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_f16_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
+  attn_decode_f16_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.head_dim) {
+    case 64: return launch_f16_d<64>(a, stream);
+    case 128: return launch_f16_d<128>(a, stream);
+    case 256: return launch_f16_d<256>(a, stream);
+    case 512: return launch_f16_d<512>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ckv

@@ -1,0 +1,289 @@
+// ckv_api.cu — the extern "C" entry points declared in include/ckv.h: argument
+// checks, workspace sizing and kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/ckv.h"
+#include "ckv_kernels.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+ckv_status fail(ckv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ckv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(CKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+
+constexpr size_t kWsHeader = 256;  // device flag + padding
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+ckv_status check_cache(const ckv_cache* c) {
+  if (!c) return fail(CKV_ERR_INVALID_ARG, "cache is null");
+  if (!supported_dim(c->head_dim))
+    return fail(CKV_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256,512}", c->head_dim);
+  if (c->n_kv_heads <= 0 || c->batch <= 0 || c->reserved != 0)
+    return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive, reserved 0");
+  if (c->capacity <= 0 || c->capacity % 16)
+    return fail(CKV_ERR_INVALID_ARG, "capacity must be a positive multiple of 16");
+  if (!c->data || !aligned(c->data, 16)) return fail(CKV_ERR_INVALID_ARG, "cache data null or not 16-byte aligned");
+  if (!c->v_signs) return fail(CKV_ERR_INVALID_ARG, "v_signs is null");
+  return CKV_OK;
+}
+
+// Split count: enough CTAs to cover every SM once, no more splits than tiles.
+int auto_split(int64_t units, int64_t max_seq_len, int tiles_per_cta_iter) {
+  const int64_t tiles = (max_seq_len + 15) / 16;
+  if (tiles == 0) return 1;
+  const int sms = num_sms();
+  int64_t s = (sms + units - 1) / units;
+  const int64_t by_tiles = (tiles + tiles_per_cta_iter - 1) / tiles_per_cta_iter;
+  if (s > by_tiles) s = by_tiles;
+  if (s < 1) s = 1;
+  if (s > 65535) s = 65535;
+  return static_cast<int>(s);
+}
+
+size_t decode_ws_bytes(int D, int64_t groups, int n_split) {
+  return kWsHeader + static_cast<size_t>(groups) * n_split * 8 * (D + 2) * sizeof(float);
+}
+
+struct DecodePlan {
+  int n_row_groups, n_split;
+  int64_t groups;
+  size_t ws;
+};
+
+ckv_status plan_decode(int D, int n_kv_heads, int batch, int64_t max_seq_len, int n_q, int n_q_heads,
+                       int n_split, DecodePlan* p) {
+  if (n_q <= 0 || n_q_heads <= 0) return fail(CKV_ERR_INVALID_ARG, "n_q and n_q_heads must be positive");
+  if (n_q_heads % n_kv_heads)
+    return fail(CKV_ERR_UNSUPPORTED, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, n_kv_heads);
+  if (max_seq_len < 0) return fail(CKV_ERR_INVALID_ARG, "max_seq_len negative");
+  if (n_split < 0 || n_split > 65535) return fail(CKV_ERR_INVALID_ARG, "n_split out of range");
+  const int64_t rows = static_cast<int64_t>(n_q_heads / n_kv_heads) * n_q;
+  const int64_t nrg = (rows + 7) / 8;
+  if (nrg > 65535) return fail(CKV_ERR_UNSUPPORTED, "too many query rows per kv head");
+  p->n_row_groups = static_cast<int>(nrg);
+  p->groups = static_cast<int64_t>(batch) * n_kv_heads * nrg;
+  const int per_iter = (D == 512) ? 4 : 8;
+  p->n_split = n_split ? n_split : auto_split(p->groups, max_seq_len, per_iter);
+  p->ws = decode_ws_bytes(D, p->groups, p->n_split);
+  return CKV_OK;
+}
+
+ckv_status check_ws(void* ws, size_t have, size_t need) {
+  if (!ws || !aligned(ws, 256)) return fail(CKV_ERR_WORKSPACE, "workspace null or not 256-byte aligned");
+  if (have < need) return fail(CKV_ERR_WORKSPACE, "workspace %zu bytes, need %zu", have, need);
+  return CKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t ckv_version(void) { return 100; }
+
+const char* ckv_last_error(void) { return g_err; }
+
+size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity) {
+  if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0 || capacity <= 0 || capacity % 16)
+    return 0;
+  return static_cast<size_t>(batch) * n_kv_heads * (capacity / 16) * ckv::record_bytes(head_dim);
+}
+
+ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok, const void* k_f16,
+                       const void* v_f16, int64_t token_stride, int64_t batch_stride, void* stream) {
+  ckv_status s = check_cache(cache);
+  if (s != CKV_OK) return s;
+  if (n_tok < 0 || tok_offset < 0 || tok_offset + n_tok > cache->capacity)
+    return fail(CKV_ERR_INVALID_ARG, "token range [%lld, %lld) outside [0, %lld)", (long long)tok_offset,
+                (long long)(tok_offset + n_tok), (long long)cache->capacity);
+  if (n_tok == 0) return CKV_OK;
+  if (!k_f16 || !v_f16 || !aligned(k_f16, 16) || !aligned(v_f16, 16))
+    return fail(CKV_ERR_INVALID_ARG, "k/v null or not 16-byte aligned");
+  const int64_t row = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
+  if (token_stride < row || token_stride % 8 || batch_stride < 0 || batch_stride % 8 ||
+      (cache->batch > 1 && batch_stride < token_stride * n_tok))
+    return fail(CKV_ERR_INVALID_ARG, "bad strides (token %lld, batch %lld)", (long long)token_stride,
+                (long long)batch_stride);
+  const int64_t tiles = (tok_offset + n_tok - 1) / 16 - tok_offset / 16 + 1;
+  if (tiles > 0x7fffffffLL) return fail(CKV_ERR_UNSUPPORTED, "too many tiles in one pack");
+  ckv::PackArgs a{};
+  a.cache = static_cast<uint8_t*>(cache->data);
+  a.capacity = cache->capacity;
+  a.head_dim = cache->head_dim;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.batch = cache->batch;
+  a.tok_offset = tok_offset;
+  a.n_tok = n_tok;
+  a.k = static_cast<const __half*>(k_f16);
+  a.v = static_cast<const __half*>(v_f16);
+  a.token_stride = token_stride;
+  a.batch_stride = batch_stride;
+  a.signs = cache->v_signs;
+  cudaError_t e = ckv::launch_kv_pack(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_pack launch");
+  return CKV_OK;
+}
+
+size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q,
+                                 int32_t n_q_heads, int32_t n_split) {
+  if (check_cache(cache) != CKV_OK) return 0;
+  DecodePlan p;
+  if (plan_decode(cache->head_dim, cache->n_kv_heads, cache->batch, max_seq_len, n_q, n_q_heads, n_split,
+                  &p) != CKV_OK)
+    return 0;
+  return p.ws;
+}
+
+static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void* k16, const void* v16,
+                             int D, int Hkv, int B, int64_t capacity, const int32_t* seq_len,
+                             int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
+                             int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
+                             void* stream) {
+  DecodePlan p;
+  ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
+  if (s != CKV_OK) return s;
+  if (!seq_len || !q || !out || !lse) return fail(CKV_ERR_INVALID_ARG, "null seq_len/q/out/lse");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_len, 4))
+    return fail(CKV_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(CKV_ERR_INVALID_ARG, "scale not finite");
+  s = check_ws(ws, ws_bytes, p.ws);
+  if (s != CKV_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
+  if (e != cudaSuccess) return cuda_fail(e, "flag reset");
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  ckv::DecodeArgs a{};
+  a.cache = compressed ? static_cast<const uint8_t*>(cache->data) : nullptr;
+  a.k16 = static_cast<const __half*>(k16);
+  a.v16 = static_cast<const __half*>(v16);
+  a.capacity = capacity;
+  a.head_dim = D;
+  a.n_kv_heads = Hkv;
+  a.batch = B;
+  a.seq_len = seq_len;
+  a.max_seq_len = max_seq_len;
+  a.q = static_cast<const __half*>(q);
+  a.n_q = n_q;
+  a.n_q_heads = n_q_heads;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.n_split = p.n_split;
+  a.n_row_groups = p.n_row_groups;
+  a.part = reinterpret_cast<float*>(base + kWsHeader);
+  a.ml = a.part + static_cast<size_t>(p.groups) * p.n_split * 8 * D;
+  a.flag = reinterpret_cast<int32_t*>(base);
+  e = compressed ? ckv::launch_attn_decode(a, st) : ckv::launch_attn_decode_f16(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  ckv::MergeArgs m{};
+  m.part = a.part;
+  m.ml = a.ml;
+  m.signs = compressed ? cache->v_signs : nullptr;
+  m.head_dim = D;
+  m.n_kv_heads = Hkv;
+  m.batch = B;
+  m.n_q = n_q;
+  m.n_q_heads = n_q_heads;
+  m.n_split = p.n_split;
+  m.n_row_groups = p.n_row_groups;
+  m.out = out;
+  m.lse = lse;
+  e = ckv::launch_decode_merge(m, st);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return CKV_OK;
+}
+
+ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                           const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale, int32_t n_split,
+                           float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  ckv_status s = check_cache(cache);
+  if (s != CKV_OK) return s;
+  return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
+                    cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
+                    workspace, ws_bytes, stream);
+}
+
+size_t ckv_attn_decode_f16_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
+                                     int64_t max_seq_len, int32_t n_q, int32_t n_q_heads, int32_t n_split) {
+  if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0) return 0;
+  DecodePlan p;
+  if (plan_decode(head_dim, n_kv_heads, batch, max_seq_len, n_q, n_q_heads, n_split, &p) != CKV_OK) return 0;
+  return p.ws;
+}
+
+ckv_status ckv_attn_decode_f16(const void* k_f16, const void* v_f16, int32_t head_dim, int32_t n_kv_heads,
+                               int32_t batch, int64_t capacity, const int32_t* seq_len, int64_t max_seq_len,
+                               const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale,
+                               int32_t n_split, float* out, float* lse, void* workspace, size_t ws_bytes,
+                               void* stream) {
+  if (!supported_dim(head_dim))
+    return fail(CKV_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256,512}", head_dim);
+  if (n_kv_heads <= 0 || batch <= 0) return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive");
+  if (capacity <= 0 || capacity % 16) return fail(CKV_ERR_INVALID_ARG, "capacity must be a positive multiple of 16");
+  if (!k_f16 || !v_f16 || !aligned(k_f16, 16) || !aligned(v_f16, 16))
+    return fail(CKV_ERR_INVALID_ARG, "k/v null or not 16-byte aligned");
+  return run_decode(false, nullptr, k_f16, v_f16, head_dim, n_kv_heads, batch, capacity, seq_len, max_seq_len,
+                    q_f16, n_q, n_q_heads, scale, n_split, out, lse, workspace, ws_bytes, stream);
+}
+
+ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts, const float* const* lse_parts,
+                         int64_t n_rows, int32_t d, float* out, float* lse, void* stream) {
+  if (n_parts < 1 || n_parts > 16) return fail(CKV_ERR_INVALID_ARG, "n_parts must be in [1, 16]");
+  if (!o_parts || !lse_parts || !out || !lse) return fail(CKV_ERR_INVALID_ARG, "null pointer argument");
+  if (n_rows < 0 || n_rows > 0x7fffffffLL || d <= 0) return fail(CKV_ERR_INVALID_ARG, "bad n_rows or d");
+  ckv::LseMergeArgs a{};
+  for (int r = 0; r < n_parts; ++r) {
+    if (!o_parts[r] || !lse_parts[r]) return fail(CKV_ERR_INVALID_ARG, "part %d is null", r);
+    a.o[r] = o_parts[r];
+    a.l[r] = lse_parts[r];
+  }
+  a.n_parts = n_parts;
+  a.n_rows = n_rows;
+  a.d = d;
+  a.out = out;
+  a.lse = lse;
+  cudaError_t e = ckv::launch_lse_merge(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
+  return CKV_OK;
+}
+
+ckv_status ckv_read_device_flag(const void* workspace, int32_t* flag, void* stream) {
+  if (!workspace || !flag) return fail(CKV_ERR_INVALID_ARG, "null argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream sync");
+  e = cudaMemcpy(flag, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "flag read");
+  if (*flag != 0) return fail(CKV_ERR_DEVICE_FLAG, "device flag %d", *flag);
+  return CKV_OK;
+}
+
+}  // extern "C"

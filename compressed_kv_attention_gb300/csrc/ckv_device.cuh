@@ -1,0 +1,193 @@
+// ckv_device.cuh — device helpers shared by the kernels of the compressed-KV
+// attention library (sm_103a): shared-memory addresses, mbarriers with bounded
+// waits, bulk global->shared copies, warp-level tensor-core mma and movmatrix,
+// and the cache-record geometry.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace ckv {
+
+// ---------------------------------------------------------------- geometry --
+
+constexpr int kTile = 16;  // token positions per tile record
+
+__host__ __device__ constexpr int record_bytes(int D) { return 23 * D + 32; }
+__host__ __device__ constexpr int k_scale_offset(int D) { return 16 * D; }
+__host__ __device__ constexpr int v_code_offset(int D) { return 17 * D; }
+__host__ __device__ constexpr int v_norm_offset(int D) { return 23 * D; }
+// Bytes of one lane's V-code stream in a record, and the granule in which it is interleaved.
+__host__ __device__ constexpr int v_lane_bytes(int D) { return 3 * D / 16; }
+__host__ __device__ constexpr int v_granule(int D) {
+  return (v_lane_bytes(D) % 16 == 0) ? 16 : (v_lane_bytes(D) % 8 == 0) ? 8 : 4;
+}
+
+// Error codes written to the workspace flag word.
+enum DeviceFlag : int32_t {
+  kFlagNone = 0,
+  kFlagWaitTimeout = 1,   // a bounded mbarrier wait ran out
+  kFlagSeqLenRange = 2,   // seq_len[b] outside [0, min(capacity, max_seq_len)]
+};
+
+// ------------------------------------------------------------------- misc --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void raise_flag(int32_t* flag, int32_t code) {
+  if (flag) atomicCAS(flag, 0, code);
+}
+
+// Bound for every wait on an asynchronous event: 2 s of wall time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// --------------------------------------------------------------- mbarrier --
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; gives up after
+// kWaitLimitNs and returns false (the caller raises the device flag).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ------------------------------------------------------------ bulk copies --
+
+// One bulk copy global -> shared (16-byte aligned addresses, size multiple of 16)
+// completing on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------ shared loads --
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// --------------------------------------------------------- tensor-core mma --
+
+// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate.
+// Fragment ownership (lane = 4*g + t): a0 = A[g][2t..2t+1], a1 = A[g+8][2t..],
+// a2 = A[g][2t+8..2t+9], a3 = A[g+8][2t+8..]; b0 = B[2t..2t+1][g], b1 = B[2t+8..][g];
+// c0 = C[g][2t], c1 = C[g][2t+1], c2 = C[g+8][2t], c3 = C[g+8][2t+1].
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with a zero accumulator input.
+__device__ __forceinline__ void mma16816_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Transpose an 8x8 matrix of 16-bit values held one row-pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Pack two fp32 into fp16x2 (round to nearest even): lo -> bits 0..15, hi -> 16..31.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four int8 codes (one 32-bit word) -> two fp16x2 holding the same integers
+// exactly: byte b becomes fp16 (1024 + (b ^ 0x80)) - 1152 = b.
+__device__ __forceinline__ void i8x4_to_half2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t e = 0x64646464u;
+  uint32_t x0, x1;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(x0) : "r"(u), "r"(e));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(x1) : "r"(u), "r"(e));
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&x0), bias);
+  __half2 h1 = __hsub2(*reinterpret_cast<__half2*>(&x1), bias);
+  lo = *reinterpret_cast<uint32_t*>(&h0);
+  hi = *reinterpret_cast<uint32_t*>(&h1);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace ckv

@@ -1,0 +1,73 @@
+// ckv_kernels.cuh — argument blocks and launchers of the library's kernels.
+// Internal to the CUDA library: the public boundary is include/ckv.h.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "ckv_device.cuh"
+
+namespace ckv {
+
+struct PackArgs {
+  uint8_t* cache;
+  int64_t capacity;
+  int head_dim, n_kv_heads, batch;
+  int64_t tok_offset, n_tok;
+  const __half* k;
+  const __half* v;
+  int64_t token_stride, batch_stride;  // in elements
+  const int8_t* signs;
+};
+cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream);
+
+// Split-K decode. Rows of one (sequence, kv head) are the G * n_q query vectors
+// that read it, ordered (query token, head in group); they are processed in
+// groups of 8 ("row groups"). Partials go to the workspace:
+//   part[group][split][8][D]  float32, unnormalised rotated-basis accumulator
+//   ml  [group][split][8][2]  float32, (running max in log2 units, row sum)
+// group = (b * n_kv_heads + kv_head) * n_row_groups + row_group.
+struct DecodeArgs {
+  const uint8_t* cache;      // packed records (compressed decode) or nullptr
+  const __half* k16;         // dense fp16 keys (fp16 decode) or nullptr
+  const __half* v16;
+  int64_t capacity;
+  int head_dim, n_kv_heads, batch;
+  const int32_t* seq_len;
+  int64_t max_seq_len;
+  const __half* q;
+  int n_q, n_q_heads;
+  float scale_log2;          // logit scale * log2(e)
+  int n_split, n_row_groups;
+  float* part;
+  float* ml;
+  int32_t* flag;
+};
+
+struct MergeArgs {
+  const float* part;
+  const float* ml;
+  const int8_t* signs;       // nullptr: no inverse rotation (fp16 decode)
+  int head_dim, n_kv_heads, batch, n_q, n_q_heads, n_split, n_row_groups;
+  float* out;
+  float* lse;
+};
+
+cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_merge(const MergeArgs& a, cudaStream_t stream);
+
+struct LseMergeArgs {
+  const float* o[16];
+  const float* l[16];
+  int n_parts;
+  int64_t n_rows;
+  int d;
+  float* out;
+  float* lse;
+};
+cudaError_t launch_lse_merge(const LseMergeArgs& a, cudaStream_t stream);
+
+// Shared-memory bytes the compressed decode kernel needs for a head dim.
+size_t decode_smem_bytes(int head_dim);
+
+}  // namespace ckv

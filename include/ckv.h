@@ -1,0 +1,217 @@
+/*
+ * ckv.h — C ABI of the compressed-KV attention library for NVIDIA GB300 (sm_103a).
+ *
+ * The library runs attention directly over an asymmetrically compressed KV
+ * cache: keys are q8_0 (blocks of 32 int8 codes with one fp16 scale) and values
+ * are 3-bit TurboQuant-MSE ("TBQ3": a +/-1 sign diagonal, an orthonormal fast
+ * Walsh-Hadamard transform, one fp16 norm per vector, 3-bit Lloyd-Max codes).
+ * The scheme is the one on the PolyKV page ("F5 M6 — PolyKV (shared compressed
+ * KV pool)", section "What PolyKV is (reference)"); attention reads the packed
+ * bytes in-kernel rather than decompressing the cache first (same page,
+ * sections "S2 perf-path Level B" and "S2 perf-path — turbo-MMA verify kernel +
+ * scalar-K/turbo-V fused decode": K is read in true space, V in the rotated
+ * basis, and one inverse transform runs on the output).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates or frees memory. Scratch space ("workspace") is sized by
+ *    the matching *_workspace() query and passed in by the caller.
+ *  - Work is enqueued asynchronously on the caller's CUDA stream (`stream` is a
+ *    cudaStream_t; NULL means the legacy default stream). Arguments are checked
+ *    on the host before anything is launched; a failed check returns a status
+ *    and launches nothing. No call aborts or exits the process.
+ *  - ckv_last_error() returns a message for the last failure on this thread.
+ *  - Kernels that wait on asynchronous copies bound every wait; a wait that
+ *    runs out (or a device-side range check that fails) sets a flag in the first
+ *    4 bytes of the workspace instead of hanging. ckv_read_device_flag() reads
+ *    it after the stream has drained. Each call clears the flag when it starts.
+ *  - Head dims supported: 64, 128, 256, 512. The number of query heads must be
+ *    a multiple of the number of KV heads; query head h reads KV head
+ *    floor(h / G), G = n_q_heads / n_kv_heads (grouped-query attention, as the
+ *    Upstream Sync page's entry 0080 describes for Gemma-4: 16 heads, 2 KV heads).
+ *  - Outputs are float32: the normalised attention output and the natural-log
+ *    log-sum-exp of every query row, the "FA output packed with per-row LSE"
+ *    contract of the DCA page ("Feature — Gemma-4 A4B Dual Chunk Attention (DCA),
+ *    training-free 1M context", section "Implementation progress + Section-D
+ *    simplification"). A row that sees no key returns output 0 and lse -inf
+ *    (same page, section "Section C2b": empty regimes drop out of the merge).
+ */
+#ifndef CKV_H
+#define CKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CKV_API __attribute__((visibility("default")))
+#else
+#define CKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CKV_OK = 0,
+  CKV_ERR_INVALID_ARG = -1,  /* null pointer, misalignment, bad size or range   */
+  CKV_ERR_UNSUPPORTED = -2,  /* valid but not supported (head_dim, head ratio)  */
+  CKV_ERR_WORKSPACE = -3,    /* workspace pointer null or smaller than needed   */
+  CKV_ERR_CUDA = -4,         /* a CUDA call or launch failed (see last_error)   */
+  CKV_ERR_DEVICE_FLAG = -5   /* a kernel reported a bounded-wait or range fault */
+} ckv_status;
+
+/*
+ * The packed cache. One allocation of ckv_cache_bytes() bytes, 16-byte aligned.
+ *
+ * Each (sequence b, kv head h) owns capacity/16 consecutive "tile records";
+ * record t holds token positions [16 t, 16 t + 16) and starts at byte
+ * ((b * n_kv_heads + h) * (capacity / 16) + t) * (23 * D + 32). Inside a record
+ * (p = position in the tile, i = dim, D = head_dim):
+ *
+ *   [0, 16D)       K q8_0 codes (int8). (p, i) is at
+ *                  ((i/32)*32 + L)*16 + (p/8)*8 + (i%8), L = 4*(p%8) + (i%32)/8.
+ *   [16D, 17D)     K q8_0 scales (fp16), row-major [16][D/32].
+ *   [17D, 23D)     V TBQ3 codes, 3 bits each. With G = D/8, L = 4*(i/G) + (p%8)/2
+ *                  and pair index k = 4*((i%G)/2) + (i%G)%2 + 2*(p/8), the code of
+ *                  (p, i) is bits [6k + 3*(p%2), +3) (LSB first) of lane L's
+ *                  3D/16-byte stream; stream byte s of lane L is at
+ *                  17D + ((s/gr)*32 + L)*gr + s%gr, gr = the largest of 16, 8, 4
+ *                  that divides 3D/16. Codes index the ascending Lloyd-Max table
+ *                  (-2.1520, -1.3439, -0.7560, -0.2451, 0.2451, 0.7560, 1.3439, 2.1520).
+ *   [23D, 23D+32)  V norms (fp16), one per position.
+ *
+ * The layout puts every lane's share of a tile contiguous so that a tile moves
+ * into shared memory with one bulk copy and each lane's mma fragments come out
+ * of conflict-free 16-byte shared loads. Positions that were never packed hold
+ * whatever the allocation held; attention never reads past seq_len.
+ *
+ * v_signs: the +/-1 sign diagonal (int8, D entries, device), one vector shared
+ * by every head and token.
+ */
+typedef struct {
+  int32_t head_dim;      /* D */
+  int32_t n_kv_heads;    /* Hkv */
+  int32_t batch;         /* B sequences */
+  int32_t reserved;      /* must be 0 */
+  int64_t capacity;      /* token positions per sequence, multiple of 16 */
+  void* data;            /* device, ckv_cache_bytes(...) bytes, 16-byte aligned */
+  const int8_t* v_signs; /* device, head_dim entries of +1 / -1 */
+} ckv_cache;
+
+/* Bytes of the packed cache: batch * n_kv_heads * capacity/16 * (23*D + 32). 0 if invalid. */
+CKV_API size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity);
+
+/*
+ * kv_pack — quantise n_tok new K and V rows of every sequence into the cache at
+ * token positions [tok_offset, tok_offset + n_tok).
+ *
+ * K rows become q8_0 (PolyKV page, "What PolyKV is (reference)": K -> int8 q8_0):
+ * per block of 32, d16 = fp16(amax/127), q = x/d16 rounded half away from zero
+ * (fp32 division, correctly rounded), clamped to [-127, 127]; d16 == 0 stores 0.
+ * V rows become TBQ3 (same section: FWHT rotation, then Lloyd-Max; "Phase-0 fork
+ * recon": warp-shuffle group transform and bit-packed codes on write): y = s*x,
+ * u = H_D y / ||x|| (H_D the Sylvester Hadamard matrix; this equals the
+ * orthonormal transform times sqrt(D)/||x||), each u_i snapped to the nearest
+ * centroid (ties at midpoints to the smaller magnitude, u = 0 to +0.2451),
+ * n16 = fp16(||x||). A zero vector stores codes 4 and norm 0.
+ *
+ * k_f16, v_f16: fp16, element (b, j, h, i) of token j of sequence b at
+ *   b*batch_stride + j*token_stride + h*D + i (in elements). token_stride >= Hkv*D.
+ * Errors: INVALID_ARG for null/misaligned pointers (inputs 16-byte aligned,
+ * strides multiples of 8 elements), a range outside [0, capacity), or negative n_tok.
+ */
+CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok,
+                       const void* k_f16, const void* v_f16,
+                       int64_t token_stride, int64_t batch_stride, void* stream);
+
+/*
+ * attn_decode — attention of n_q query tokens per sequence over the packed
+ * cache, every query seeing cached positions [0, seq_len[b]).
+ *
+ * Split-K flash-decode: each CTA streams a contiguous range of tile records
+ * through shared memory, computes S = Q K_hat^T on tensor cores from the int8
+ * codes (scales applied per 32-block), runs the online softmax, and accumulates
+ * P V_hat in the rotated basis straight from the 3-bit codes. A second kernel
+ * merges the split partials with the exact log-sum-exp combine and applies the
+ * inverse transform and sign flip once per output row (valid because the
+ * rotation is linear and shared within a head: PolyKV page, "S2 perf-path Level
+ * B" — the transform runs only on the small FA output).
+ *
+ * seq_len: device int32 [batch], each in [0, min(capacity, max_seq_len)];
+ *   max_seq_len (host) sizes the split grid.
+ * q_f16: device fp16 [batch][n_q][n_q_heads][D].
+ * scale: logit scale (e.g. 1/sqrt(D)).
+ * n_split: KV splits per (sequence, kv head, row group); 0 picks one that fills
+ *   the GPU. out: float32 [batch][n_q][n_q_heads][D]; lse: float32 [batch][n_q][n_q_heads].
+ * workspace: ckv_attn_decode_workspace() bytes, 256-byte aligned.
+ */
+CKV_API size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q,
+                                 int32_t n_q_heads, int32_t n_split);
+CKV_API ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                           const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale,
+                           int32_t n_split, float* out, float* lse, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * attn_decode_f16 — the same decode over a dense fp16 KV cache (the private,
+ * uncompressed tails of the shared-pool fan-out: PolyKV page, section "S1 —
+ * SharedKVPool": one shared prefix plus a private suffix per agent).
+ * k_f16, v_f16: device fp16 [batch][n_kv_heads][capacity][D], 16-byte aligned.
+ * Other arguments as attn_decode.
+ */
+CKV_API size_t ckv_attn_decode_f16_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
+                                     int64_t max_seq_len, int32_t n_q, int32_t n_q_heads,
+                                     int32_t n_split);
+CKV_API ckv_status ckv_attn_decode_f16(const void* k_f16, const void* v_f16, int32_t head_dim,
+                               int32_t n_kv_heads, int32_t batch, int64_t capacity,
+                               const int32_t* seq_len, int64_t max_seq_len, const void* q_f16,
+                               int32_t n_q, int32_t n_q_heads, float scale, int32_t n_split,
+                               float* out, float* lse, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * lse_merge — exact merge of n_parts normalised partials computed over
+ * disjoint key sets (DCA page, "Implementation progress + Section-D
+ * simplification": M = max lse_r, w_r = exp(lse_r - M), O = sum w_r O_r / sum w_r,
+ * lse = M + ln sum w_r). Partials with lse = -inf weigh 0; all empty -> O = 0,
+ * lse = -inf.
+ * o_parts, lse_parts: HOST arrays of n_parts DEVICE pointers, each o part
+ * float32 [n_rows][d], each lse part float32 [n_rows]. 1 <= n_parts <= 16.
+ * out: float32 [n_rows][d]; lse: float32 [n_rows] (may alias a part).
+ */
+CKV_API ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts,
+                         const float* const* lse_parts, int64_t n_rows, int32_t d,
+                         float* out, float* lse, void* stream);
+
+/*
+ * attn_prefill — chunked prefill: pack n_new new K/V rows of every sequence at
+ * positions [n_cached, n_cached + n_new) (as kv_pack), then causal attention of
+ * the n_new queries over the packed cache: query i sees positions
+ * [0, n_cached + i] (the cache stores what the packer is handed and attention
+ * reads it back). S = Q K_hat^T and P V_hat run on tcgen05 tensor cores.
+ * q_bf16: device bf16 [batch][n_new][n_q_heads][D]. k_new_f16, v_new_f16: device
+ * fp16 [batch][n_new][n_kv_heads][D]. out: float32 [batch][n_new][n_q_heads][D];
+ * lse: float32 [batch][n_new][n_q_heads].
+ */
+CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads);
+CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16,
+                            int32_t n_new, int32_t n_q_heads, const void* k_new_f16,
+                            const void* v_new_f16, float scale, float* out, float* lse,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronously read the device flag (first 4 bytes of a workspace) after draining
+ * `stream`. *flag receives it; returns CKV_ERR_DEVICE_FLAG when it is nonzero. */
+CKV_API ckv_status ckv_read_device_flag(const void* workspace, int32_t* flag, void* stream);
+
+/* Message for the last failure on the calling thread ("" if none). */
+CKV_API const char* ckv_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+CKV_API int32_t ckv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CKV_H */

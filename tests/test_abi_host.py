@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+entry point include/ckv.h declares, and its argument checks return the
+documented status before anything reaches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_kv_attention_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from compressed_kv_attention_gb300 import build
+        build.build()
+    return B.load()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ckv.h")).read()
+    return sorted(set(re.findall(r"CKV_API\s+[\w\s\*]+?\b(ckv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    for required in ("ckv_kv_pack", "ckv_attn_decode", "ckv_attn_prefill", "ckv_lse_merge"):
+        assert required in names
+    assert len(names) >= 12
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in B.SIGNATURES, f"binding lacks {name}"
+
+
+def test_version_and_cache_bytes(lib):
+    assert lib.ckv_version() == 100
+    assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * (32768 // 16) * (23 * 512 + 32)
+    assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * 32768 * 738
+    assert lib.ckv_cache_bytes(128, 1, 1, 256) == 256 * 186
+    for bad in [(96, 1, 1, 16), (128, 0, 1, 16), (128, 1, 0, 16), (128, 1, 1, 20), (128, 1, 1, 0)]:
+        assert lib.ckv_cache_bytes(*bad) == 0
+
+
+def _fake_cache(D=128, Hkv=1, batch=1, cap=256, data=0x10000, signs=0x20000, reserved=0):
+    return B.CkvCacheStruct(D, Hkv, batch, reserved, cap, data, signs)
+
+
+def test_pack_argument_checks(lib):
+    fake = 0x7f0000000000  # 16-byte aligned, never dereferenced: checks fail first
+    c = _fake_cache()
+    assert lib.ckv_kv_pack(None, 0, 1, fake, fake, 128, 0, None) == -1
+    assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(D=96)), 0, 1, fake, fake, 128, 0, None) == -2
+    assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(cap=250)), 0, 1, fake, fake, 128, 0, None) == -1
+    assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(reserved=1)), 0, 1, fake, fake, 128, 0, None) == -1
+    assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(data=0x10008)), 0, 1, fake, fake, 128, 0, None) == -1
+    assert lib.ckv_kv_pack(ctypes.byref(c), 250, 10, fake, fake, 128, 0, None) == -1   # past capacity
+    assert lib.ckv_kv_pack(ctypes.byref(c), -1, 1, fake, fake, 128, 0, None) == -1
+    assert lib.ckv_kv_pack(ctypes.byref(c), 0, 4, None, fake, 128, 0, None) == -1
+    assert lib.ckv_kv_pack(ctypes.byref(c), 0, 4, fake + 2, fake, 128, 0, None) == -1  # misaligned
+    assert lib.ckv_kv_pack(ctypes.byref(c), 0, 4, fake, fake, 100, 0, None) == -1      # stride < row
+    assert lib.ckv_kv_pack(ctypes.byref(c), 0, 0, None, None, 0, 0, None) == 0         # empty: no-op
+    assert b"outside" in lib.ckv_last_error() or len(lib.ckv_last_error()) > 0
+
+
+def test_decode_argument_checks(lib):
+    fake = 0x7f0000000000
+    c = _fake_cache(D=512, Hkv=2, cap=4096)
+    need = lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 1, 16, 8)
+    assert need == 256 + 2 * 8 * 8 * (512 + 2) * 4
+    assert lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 1, 15, 8) == 0  # 15 % 2 != 0
+    args = lambda **kw: dict(dict(seq=fake, maxs=4096, q=fake, nq=1, hq=16, scale=0.04, ns=8, out=fake,
+                                  lse=fake, ws=fake, wsb=need), **kw)
+    def call(cache=c, **kw):
+        a = args(**kw)
+        return lib.ckv_attn_decode(ctypes.byref(cache), a["seq"], a["maxs"], a["q"], a["nq"], a["hq"],
+                                   a["scale"], a["ns"], a["out"], a["lse"], a["ws"], a["wsb"], None)
+    assert call(hq=15) == -2                      # 15 query heads over 2 kv heads
+    assert call(nq=0) == -1
+    assert call(seq=None) == -1
+    assert call(q=fake + 4) == -1
+    assert call(ws=None) == -3
+    assert call(wsb=need - 1) == -3
+    assert call(ws=fake + 16) == -3               # workspace must be 256-byte aligned
+    assert call(scale=float("nan")) == -1
+    assert call(ns=-1) == -1
+    assert call(cache=_fake_cache(D=100)) == -2
+
+
+def test_decode_f16_and_merge_argument_checks(lib):
+    fake = 0x7f0000000000
+    need = lib.ckv_attn_decode_f16_workspace(512, 2, 15, 512, 1, 16, 4)
+    assert need == 256 + 15 * 2 * 4 * 8 * 514 * 4
+    assert lib.ckv_attn_decode_f16(fake, fake, 512, 2, 15, 500, fake, 512, fake, 1, 16, 0.04, 4, fake, fake,
+                                   fake, need, None) == -1  # capacity not a multiple of 16
+    assert lib.ckv_attn_decode_f16(fake + 8, fake, 512, 2, 15, 512, fake, 512, fake, 1, 16, 0.04, 4, fake,
+                                   fake, fake, need, None) == -1
+    ptrs = (ctypes.c_void_p * 2)(fake, fake)
+    assert lib.ckv_lse_merge(0, ptrs, ptrs, 10, 512, fake, fake, None) == -1
+    assert lib.ckv_lse_merge(17, ptrs, ptrs, 10, 512, fake, fake, None) == -1
+    nul = (ctypes.c_void_p * 2)(fake, None)
+    assert lib.ckv_lse_merge(2, ptrs, nul, 10, 512, fake, fake, None) == -1
+    assert lib.ckv_lse_merge(2, ptrs, ptrs, 10, 0, fake, fake, None) == -1
+
+
+def test_read_device_flag_checks(lib):
+    flag = ctypes.c_int32(7)
+    assert lib.ckv_read_device_flag(None, ctypes.byref(flag), None) == -1
