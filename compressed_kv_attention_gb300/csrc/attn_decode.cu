@@ -254,66 +254,43 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
   float* part_out = a.part + ((gid * a.n_split + split) * 8) * D;
   float* ml_out = a.ml + ((gid * a.n_split + split) * 8) * 2;
-  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, lane, tid,
-                              part_out, ml_out);
+  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane, tid,
+                              a.signs, part_out, ml_out);
+  __shared__ int s_ok;
+  __shared__ float* s_out[8];
+  __shared__ float* s_lse[8];
+  decode_merge_tail<D>(a, split, rg, b, kvh, tid, reinterpret_cast<float*>(smem), &s_ok, s_out, s_lse);
 }
 
 // --------------------------------------------------------------- merge --
 
-// One CTA per output row, one thread per dim: combine the splits exactly,
-// normalise, and (compressed cache) apply the inverse transform and sign flip:
-// O = s * H_D(O_rot) / D, where O_rot accumulated p * norm * centroid.
-template <int D, bool ROT>
-__global__ void __launch_bounds__(D) decode_merge_kernel(MergeArgs a) {
-  __shared__ float sx[D];
-  const int row = blockIdx.x;
-  const int64_t gid = row >> 3;
-  const int r = row & 7;
-  const int rgi = static_cast<int>(gid % a.n_row_groups);
-  const int bh = static_cast<int>(gid / a.n_row_groups);
-  const int b = bh / a.n_kv_heads, kvh = bh % a.n_kv_heads;
-  const int group_q = a.n_q_heads / a.n_kv_heads;
-  const int rr = rgi * 8 + r;
-  if (rr >= group_q * a.n_q) return;
-  int qi, h;
-  row_to_query(rr, group_q, kvh, qi, h);
-  const int d = threadIdx.x;
-
-  const float* mlp = a.ml + (gid * a.n_split * 8 + r) * 2;
-  float M = -INFINITY;
-  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, mlp[s * 16]);
-  float L = 0.0f, acc = 0.0f;
-  const float* pp = a.part + (gid * a.n_split * 8 + r) * D + d;
-  if (M != -INFINITY) {
-    for (int s = 0; s < a.n_split; ++s) {
-      const float m = mlp[s * 16];
-      if (m == -INFINITY) continue;
-      const float w = exp2f(m - M);
-      L = fmaf(w, mlp[s * 16 + 1], L);
-      acc = fmaf(w, pp[(int64_t)s * 8 * D], acc);
-    }
+// Split merge as a separate kernel, for grids too large to be co-resident:
+// CTA (chunk, group) merges elements of the group's 8 x D output.
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(MergeArgs m) {
+  extern __shared__ __align__(16) float msm[];
+  __shared__ float* s_out[8];
+  __shared__ float* s_lse[8];
+  const int64_t gid = blockIdx.y;
+  const int rg = static_cast<int>(gid % m.n_row_groups);
+  const int bh = static_cast<int>(gid / m.n_row_groups);
+  const int b = bh / m.n_kv_heads, kvh = bh % m.n_kv_heads;
+  const int tid = threadIdx.x;
+  if (tid < 8) {
+    DecodeArgs a{};
+    a.n_q_heads = m.n_q_heads;
+    a.n_kv_heads = m.n_kv_heads;
+    a.n_q = m.n_q;
+    a.head_dim = D;
+    a.out = m.out;
+    a.lse = m.lse;
+    row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
   }
-  const bool valid = L > 0.0f;
-  float v = valid ? acc / L : 0.0f;
-  if constexpr (ROT) {
-#pragma unroll
-    for (int hh = 1; hh < 32 && hh < D; hh <<= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, v, hh);
-      v = (d & hh) ? (o - v) : (v + o);
-    }
-#pragma unroll
-    for (int hh = 32; hh < D; hh <<= 1) {
-      sx[d] = v;
-      __syncthreads();
-      const float o = sx[d ^ hh];
-      __syncthreads();
-      v = (d & hh) ? (o - v) : (v + o);
-    }
-    v = (a.signs[d] < 0 ? -v : v) * (1.0f / D);
-  }
-  const int64_t orow = (int64_t)(b * a.n_q + qi) * a.n_q_heads + h;
-  a.out[orow * D + d] = v;
-  if (d == 0) a.lse[orow] = valid ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  __syncthreads();
+  const int e0 = (int)((int64_t)blockIdx.x * 8 * D / gridDim.x);
+  const int e1 = (int)((int64_t)(blockIdx.x + 1) * 8 * D / gridDim.x);
+  merge_rows<D>(m.part + (size_t)gid * m.n_split * 8 * D, m.ml + (size_t)gid * m.n_split * 16, m.n_split,
+                e0, e1, tid, 256, msm, s_out, s_lse, blockIdx.x == 0, 1);
 }
 
 size_t decode_smem_bytes(int head_dim) {
@@ -327,37 +304,42 @@ size_t decode_smem_bytes(int head_dim) {
 }
 
 template <int D>
-static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
+static cudaError_t launch_decode_d(const DecodeArgs& a, bool cooperative, cudaStream_t stream) {
   using C = CDec<D>;
   static bool configured = false;  // per process; the attribute is per function
+  static int cap = 0;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
-  attn_decode_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(a);
-  return cudaGetLastError();
+  return launch_split_decode(attn_decode_kernel<D>, a, cooperative, C::THREADS, C::SMEM, &cap, stream);
 }
 
-cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stream) {
   switch (a.head_dim) {
-    case 64: return launch_decode_d<64>(a, stream);
-    case 128: return launch_decode_d<128>(a, stream);
-    case 256: return launch_decode_d<256>(a, stream);
-    case 512: return launch_decode_d<512>(a, stream);
+    case 64: return launch_decode_d<64>(a, cooperative, stream);
+    case 128: return launch_decode_d<128>(a, cooperative, stream);
+    case 256: return launch_decode_d<256>(a, cooperative, stream);
+    case 512: return launch_decode_d<512>(a, cooperative, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int D>
-static cudaError_t launch_merge_d(const MergeArgs& a, cudaStream_t stream) {
-  const int64_t rows = (int64_t)a.batch * a.n_kv_heads * a.n_row_groups * 8;
-  if (a.signs)
-    decode_merge_kernel<D, true><<<static_cast<unsigned>(rows), D, 0, stream>>>(a);
-  else
-    decode_merge_kernel<D, false><<<static_cast<unsigned>(rows), D, 0, stream>>>(a);
+static cudaError_t launch_merge_d(const MergeArgs& m, cudaStream_t stream) {
+  const int64_t groups = (int64_t)m.batch * m.n_kv_heads * m.n_row_groups;
+  const size_t smem = (size_t)(m.n_split * 8 + 16 + 256) * sizeof(float);
+  static size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  dim3 grid(8 * D / 256, static_cast<unsigned>(groups));
+  decode_merge_kernel<D><<<grid, 256, smem, stream>>>(m);
   return cudaGetLastError();
 }
 

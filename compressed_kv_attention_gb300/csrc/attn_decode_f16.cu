@@ -110,31 +110,34 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
   float* part_out = a.part + ((gid * a.n_split + split) * 8) * D;
   float* ml_out = a.ml + ((gid * a.n_split + split) * 8) * 2;
-  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, lane, tid,
-                              part_out, ml_out);
+  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane, tid,
+                              nullptr, part_out, ml_out);
+  __shared__ int s_ok;
+  __shared__ float* s_out[8];
+  __shared__ float* s_lse[8];
+  decode_merge_tail<D>(a, split, rg, b, kvh, tid, reinterpret_cast<float*>(smem), &s_ok, s_out, s_lse);
 }
 
 template <int D>
-static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
+static cudaError_t launch_f16_d(const DecodeArgs& a, bool cooperative, cudaStream_t stream) {
   using C = FDec<D>;
   static bool configured = false;
+  static int cap = 0;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_f16_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
-  attn_decode_f16_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(a);
-  return cudaGetLastError();
+  return launch_split_decode(attn_decode_f16_kernel<D>, a, cooperative, C::THREADS, C::SMEM, &cap, stream);
 }
 
-cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_attn_decode_f16(DecodeArgs a, bool cooperative, cudaStream_t stream) {
   switch (a.head_dim) {
-    case 64: return launch_f16_d<64>(a, stream);
-    case 128: return launch_f16_d<128>(a, stream);
-    case 256: return launch_f16_d<256>(a, stream);
-    case 512: return launch_f16_d<512>(a, stream);
+    case 64: return launch_f16_d<64>(a, cooperative, stream);
+    case 128: return launch_f16_d<128>(a, cooperative, stream);
+    case 256: return launch_f16_d<256>(a, cooperative, stream);
+    case 512: return launch_f16_d<512>(a, cooperative, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -30,7 +30,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool supported_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
-constexpr size_t kWsHeader = 256;  // device flag + padding
+// Workspace header: the device flag at byte 0, one split-merge counter per row
+// group from byte 64, rounded up to 256 bytes; both are cleared by every call.
+size_t ws_header_bytes(int64_t groups) { return (64 + 4 * static_cast<size_t>(groups) + 255) / 256 * 256; }
 
 int num_sms() {
   static int cached[64] = {0};
@@ -72,7 +74,7 @@ int auto_split(int64_t units, int64_t max_seq_len, int tiles_per_cta_iter) {
 }
 
 size_t decode_ws_bytes(int D, int64_t groups, int n_split) {
-  return kWsHeader + static_cast<size_t>(groups) * n_split * 8 * (D + 2) * sizeof(float);
+  return ws_header_bytes(groups) + static_cast<size_t>(groups) * n_split * 8 * (D + 2) * sizeof(float);
 }
 
 struct DecodePlan {
@@ -179,13 +181,15 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   s = check_ws(ws, ws_bytes, p.ws);
   if (s != CKV_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, 4, st);
-  if (e != cudaSuccess) return cuda_fail(e, "flag reset");
+  const size_t header = ws_header_bytes(p.groups);
+  cudaError_t e = cudaMemsetAsync(ws, 0, header, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
   uint8_t* base = static_cast<uint8_t*>(ws);
   ckv::DecodeArgs a{};
   a.cache = compressed ? static_cast<const uint8_t*>(cache->data) : nullptr;
   a.k16 = static_cast<const __half*>(k16);
   a.v16 = static_cast<const __half*>(v16);
+  a.signs = compressed ? cache->v_signs : nullptr;
   a.capacity = capacity;
   a.head_dim = D;
   a.n_kv_heads = Hkv;
@@ -198,26 +202,35 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_split = p.n_split;
   a.n_row_groups = p.n_row_groups;
-  a.part = reinterpret_cast<float*>(base + kWsHeader);
+  a.part = reinterpret_cast<float*>(base + header);
   a.ml = a.part + static_cast<size_t>(p.groups) * p.n_split * 8 * D;
   a.flag = reinterpret_cast<int32_t*>(base);
-  e = compressed ? ckv::launch_attn_decode(a, st) : ckv::launch_attn_decode_f16(a, st);
+  a.counters = reinterpret_cast<uint32_t*>(base + 64);
+  a.out = out;
+  a.lse = lse;
+  // One launch when every CTA can be resident at once (the CTAs of a row group
+  // merge their splits themselves); otherwise the decode plus a merge kernel.
+  e = compressed ? ckv::launch_attn_decode(a, true, st) : ckv::launch_attn_decode_f16(a, true, st);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    e = compressed ? ckv::launch_attn_decode(a, false, st) : ckv::launch_attn_decode_f16(a, false, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    ckv::MergeArgs m{};
+    m.part = a.part;
+    m.ml = a.ml;
+    m.head_dim = D;
+    m.n_kv_heads = Hkv;
+    m.batch = B;
+    m.n_q = n_q;
+    m.n_q_heads = n_q_heads;
+    m.n_split = p.n_split;
+    m.n_row_groups = p.n_row_groups;
+    m.out = out;
+    m.lse = lse;
+    e = ckv::launch_decode_merge(m, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return CKV_OK;
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  ckv::MergeArgs m{};
-  m.part = a.part;
-  m.ml = a.ml;
-  m.signs = compressed ? cache->v_signs : nullptr;
-  m.head_dim = D;
-  m.n_kv_heads = Hkv;
-  m.batch = B;
-  m.n_q = n_q;
-  m.n_q_heads = n_q_heads;
-  m.n_split = p.n_split;
-  m.n_row_groups = p.n_row_groups;
-  m.out = out;
-  m.lse = lse;
-  e = ckv::launch_decode_merge(m, st);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return CKV_OK;
 }
 

@@ -22,14 +22,18 @@ cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream);
 
 // Split-K decode. Rows of one (sequence, kv head) are the G * n_q query vectors
 // that read it, ordered (query token, head in group); they are processed in
-// groups of 8 ("row groups"). Partials go to the workspace:
-//   part[group][split][8][D]  float32, unnormalised rotated-basis accumulator
+// groups of 8 ("row groups"). Each CTA writes one partial to the workspace:
+//   part[group][split][8][D]  float32, sum_j p_j V_j in true space, relative to
+//                             the CTA's running max (unnormalised)
 //   ml  [group][split][8][2]  float32, (running max in log2 units, row sum)
-// group = (b * n_kv_heads + kv_head) * n_row_groups + row_group.
+// group = (b * n_kv_heads + kv_head) * n_row_groups + row_group. With a
+// cooperative launch the CTAs of a group then merge the splits themselves;
+// otherwise launch_decode_merge does it.
 struct DecodeArgs {
   const uint8_t* cache;      // packed records (compressed decode) or nullptr
   const __half* k16;         // dense fp16 keys (fp16 decode) or nullptr
   const __half* v16;
+  const int8_t* signs;       // sign diagonal (compressed decode) or nullptr
   int64_t capacity;
   int head_dim, n_kv_heads, batch;
   const int32_t* seq_len;
@@ -41,19 +45,28 @@ struct DecodeArgs {
   float* part;
   float* ml;
   int32_t* flag;
+  uint32_t* counters;        // [groups], zero at launch (cooperative merge)
+  int merge_in_kernel;       // 1: cooperative launch, CTAs merge their group
+  float* out;
+  float* lse;
 };
 
 struct MergeArgs {
   const float* part;
   const float* ml;
-  const int8_t* signs;       // nullptr: no inverse rotation (fp16 decode)
   int head_dim, n_kv_heads, batch, n_q, n_q_heads, n_split, n_row_groups;
   float* out;
   float* lse;
 };
 
-cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
-cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream);
+// Largest split count the in-kernel merge handles (its shared scratch).
+constexpr int kMaxInKernelSplits = 512;
+
+// Launch the decode kernel; `cooperative` requests the in-kernel merge (all
+// CTAs co-resident). Returns cudaErrorCooperativeLaunchTooLarge when the grid
+// cannot be co-resident, without launching.
+cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stream);
+cudaError_t launch_attn_decode_f16(DecodeArgs a, bool cooperative, cudaStream_t stream);
 cudaError_t launch_decode_merge(const MergeArgs& a, cudaStream_t stream);
 
 struct LseMergeArgs {

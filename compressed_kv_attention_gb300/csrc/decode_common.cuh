@@ -12,6 +12,7 @@
 #pragma once
 
 #include "ckv_device.cuh"
+#include "ckv_kernels.cuh"
 
 namespace ckv {
 
@@ -104,14 +105,21 @@ __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int grou
   S[3] += o.w;
 }
 
-// CTA epilogue: merge the NP tile groups' states and accumulators into one
-// partial and write it to the workspace. Runs on the 256 consumer threads
-// (named barrier 1). `red` must hold NP * RED_FLOATS floats (stage memory is
-// reused), `mlbuf` NP * 16 floats.
+// CTA epilogue. Merges the NP tile groups' softmax states and accumulators
+// into one partial per row, applies the inverse transform and sign flip (when
+// `signs` is set: the values were accumulated in the rotated basis), and
+// writes the partial to the workspace:
+//   part_out[8][D]  sum_j p_j V_j relative to the CTA's running max, true space
+//   ml_out[8][2]    (running max in log2 units, row sum)
+// De-rotating each partial here is exact: the transform is linear and the
+// split merge only forms per-row weighted sums of partials. Runs on the 256
+// consumer threads (named barrier 1). `red` holds NP * RED_FLOATS floats (stage
+// memory is reused), `mlbuf` NP * 16 floats.
 template <int D, int MTW>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
-                                                float* mlbuf, int group, int wh, int lane,
-                                                int tid, float* part_out, float* ml_out) {
+                                                float* mlbuf, int group, int wh, int warp, int lane,
+                                                int tid, const int8_t* signs, float* part_out,
+                                                float* ml_out) {
   using Sh = DecodeShape<D>;
   const int g = lane >> 2, t = lane & 3;
   // Reduce the row sums over the 8 lanes that share rows (2t, 2t+1).
@@ -147,20 +155,55 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
         make_float2(acc[i][2] * f0, acc[i][3] * f1);
   }
   named_bar(1, Sh::NCW * 32);
-  for (int d = tid; d < D; d += Sh::NCW * 32) {
-    float s[8];
+  // Warp r owns row r: lane holds dims [lane*E, lane*E + E), summed over groups.
+  constexpr int E = D / 32;
+  const int r = warp;
+  float v[E];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) s[r] = 0.0f;
+  for (int e = 0; e < E; ++e) {
+    const int d = lane * E + e;
+    float x = 0.0f;
 #pragma unroll
-    for (int q = 0; q < Sh::NP; ++q) {
-      const float* src = red + q * Sh::RED_FLOATS + d * 8 + 8 * (d / Sh::GD);
-      const float4 x = *reinterpret_cast<const float4*>(src);
-      const float4 y = *reinterpret_cast<const float4*>(src + 4);
-      s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
-      s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
+    for (int q = 0; q < Sh::NP; ++q) x += red[q * Sh::RED_FLOATS + d * 8 + 8 * (d / Sh::GD) + r];
+    v[e] = x;
+  }
+  if (signs) {
+    // Unnormalised Walsh-Hadamard transform of the row: stages inside the lane,
+    // then across lanes; then the sign flip and 1/D (one 1/sqrt(D) from the
+    // orthonormal inverse, one from the norm scaling folded into P').
+#pragma unroll
+    for (int hh = 1; hh < E; hh <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if ((e & hh) == 0) {
+          const float x0 = v[e], x1 = v[e + hh];
+          v[e] = x0 + x1;
+          v[e + hh] = x0 - x1;
+        }
+      }
     }
 #pragma unroll
-    for (int r = 0; r < 8; ++r) part_out[r * D + d] = s[r];
+    for (int hl = 1; hl < 32; hl <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
+        v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int d = lane * E + e;
+      v[e] = (signs[d] < 0 ? -v[e] : v[e]) * (1.0f / D);
+    }
+  }
+  float* prow = part_out + r * D + lane * E;
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < E; e += 4)
+      *reinterpret_cast<float4*>(prow + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; e += 2) *reinterpret_cast<float2*>(prow + e) = make_float2(v[e], v[e + 1]);
   }
   if (tid < 8) {
     float mc = -INFINITY;
@@ -175,6 +218,105 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
     ml_out[tid * 2 + 0] = mc;
     ml_out[tid * 2 + 1] = lc;
   }
+}
+
+// Exact merge of the n_split partials of one row group (8 rows x D):
+// M = max_s m_s, w_s = 2^(m_s - M), O = sum_s w_s part_s / sum_s w_s l_s,
+// lse = (M + log2 sum_s w_s l_s) ln 2; a row with no key gives O = 0, lse = -inf.
+// part: [n_split][8][D], ml: [n_split][8][2] of the group. This CTA produces
+// the elements [e0, e1) of the 8 x D output (row-major); threads tid < nthr take
+// part and synchronise on named barrier `bar_id`. `sm` provides
+// n_split * 8 + 16 + nthr floats. out_rows / lse_rows: where each row goes
+// (nullptr for padding rows); lse is written when write_lse.
+template <int D>
+__device__ __forceinline__ void merge_rows(const float* part, const float* ml, int n_split, int e0,
+                                           int e1, int tid, int nthr, float* sm, float* const* out_rows,
+                                           float* const* lse_rows, bool write_lse, int bar_id) {
+  float* w = sm;                  // [n_split][8] weights
+  float* ML = sm + n_split * 8;   // [8][2]: max, 1/sum (0 when empty)
+  float* red = ML + 16;           // [nthr] partial sums
+  for (int i = tid; i < n_split * 8; i += nthr) w[i] = __ldcg(ml + i * 2);
+  named_bar(bar_id, nthr);
+  if (tid < 8) {
+    float M = -INFINITY;
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, w[s * 8 + tid]);
+    ML[tid * 2] = M;
+  }
+  named_bar(bar_id, nthr);
+  for (int i = tid; i < n_split * 8; i += nthr) {
+    const float M = ML[(i & 7) * 2];
+    const float m = w[i];
+    w[i] = (m == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(m - M);
+  }
+  named_bar(bar_id, nthr);
+  if (tid < 8) {
+    float L = 0.0f;
+    for (int s = 0; s < n_split; ++s) L = fmaf(w[s * 8 + tid], __ldcg(ml + (s * 8 + tid) * 2 + 1), L);
+    const float M = ML[tid * 2];
+    ML[tid * 2 + 1] = (L > 0.0f) ? 1.0f / L : 0.0f;
+    if (write_lse && lse_rows[tid])
+      *lse_rows[tid] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  named_bar(bar_id, nthr);
+  const int ne = e1 - e0;
+  // k threads per element (each sums every k-th split) when the slice is small.
+  int k = 1;
+  while (k * 2 * ne <= nthr && k < 32) k *= 2;
+  const int cs = nthr / k;  // elements per pass
+  const int el_in = tid % cs, pk = tid / cs;
+  for (int base = 0; base < ne; base += cs) {
+    const int el = base + el_in;
+    const int e = e0 + el;
+    const int r = e / D, d = e % D;
+    float acc = 0.0f;
+    if (el < ne) {
+      const float* p = part + (size_t)r * D + d;
+#pragma unroll 8
+      for (int s = pk; s < n_split; s += k) acc = fmaf(w[s * 8 + r], __ldcg(p + (size_t)s * 8 * D), acc);
+    }
+    red[tid] = acc;
+    named_bar(bar_id, nthr);
+    if (pk == 0 && el < ne) {
+      float tot = 0.0f;
+      for (int j = 0; j < k; ++j) tot += red[el_in + j * cs];
+      if (out_rows[r]) out_rows[r][d] = tot * ML[r * 2 + 1];
+    }
+    named_bar(bar_id, nthr);
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Split-merge rendezvous of a cooperative launch: every CTA of the row group
+// has written its partial; the last of them to arrive releases the others.
+// The wait is bounded; on timeout the device flag is raised and false returned.
+__device__ __forceinline__ bool group_rendezvous(uint32_t* counter, uint32_t n_split, int tid, int nthr,
+                                                 int bar_id, int32_t* flag, int* s_ok) {
+  __threadfence();
+  named_bar(bar_id, nthr);
+  if (tid == 0) {
+    atomicAdd(counter, 1u);
+    int ok = 1;
+    if (ld_acquire_u32(counter) < n_split) {
+      const uint64_t t0 = global_timer_ns();
+      for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_u32(counter) >= n_split) break;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+          raise_flag(flag, kFlagWaitTimeout);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    *s_ok = ok;
+  }
+  named_bar(bar_id, nthr);
+  return *(volatile int*)s_ok != 0;
 }
 
 // Which query vector row `rr` (0 <= rr < G * n_q) of kv head `kvh` is: the
@@ -198,6 +340,76 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NBW][4], const __hal
     qf[i][2] = v.z;
     qf[i][3] = v.w;
   }
+}
+
+
+// Output pointers of the 8 rows of row group `rg` (nullptr for padding rows).
+__device__ __forceinline__ void row_outputs(const DecodeArgs& a, int b, int kvh, int rg, int r,
+                                            float** o, float** l) {
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int rr = rg * 8 + r;
+  if (rr >= group_q * a.n_q) {
+    *o = nullptr;
+    *l = nullptr;
+    return;
+  }
+  int qi, h;
+  row_to_query(rr, group_q, kvh, qi, h);
+  const int64_t orow = (int64_t)(b * a.n_q + qi) * a.n_q_heads + h;
+  *o = a.out + orow * a.head_dim;
+  *l = a.lse + orow;
+}
+
+// After the epilogue: when the launch is cooperative, meet the group's other
+// CTAs and merge this CTA's slice of the group's output (256 consumer threads).
+template <int D>
+__device__ __forceinline__ void decode_merge_tail(const DecodeArgs& a, int split, int rg, int b, int kvh,
+                                                  int tid, float* sm, int* s_ok, float** s_out,
+                                                  float** s_lse) {
+  if (!a.merge_in_kernel) return;
+  const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
+  if (!group_rendezvous(a.counters + gid, (uint32_t)a.n_split, tid, 256, 1, a.flag, s_ok)) return;
+  if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
+  named_bar(1, 256);
+  const int e0 = (int)((int64_t)split * 8 * D / a.n_split);
+  const int e1 = (int)((int64_t)(split + 1) * 8 * D / a.n_split);
+  merge_rows<D>(a.part + (size_t)gid * a.n_split * 8 * D, a.ml + (size_t)gid * a.n_split * 16, a.n_split,
+                e0, e1, tid, 256, sm, s_out, s_lse, split == 0, 1);
+}
+
+
+// ---------------------------------------------------------- host launch --
+
+// Blocks of `kernel` that can be resident at once on the current device.
+template <typename K>
+static inline int coresident_blocks(K kernel, int threads, size_t smem) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) return 0;
+  return sms * per_sm;
+}
+
+template <typename K>
+static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, bool cooperative, int threads, size_t smem,
+                                int* cap_cache, cudaStream_t stream) {
+  const int64_t grid_total = (int64_t)a.n_split * a.n_row_groups * a.batch * a.n_kv_heads;
+  if (cooperative) {
+    if (*cap_cache == 0) *cap_cache = coresident_blocks(kernel, threads, smem);
+    if (grid_total > *cap_cache || a.n_split > kMaxInKernelSplits) return cudaErrorCooperativeLaunchTooLarge;
+  }
+  a.merge_in_kernel = cooperative ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = cooperative ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace ckv
