@@ -45,6 +45,8 @@ SIGNATURES = {
     "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
                                  _vp, _c_size, _vp]),
+    "ckv_attn_decode_noalloc": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp,
+                                         _vp, _vp]),
     "ckv_attn_decode_f16_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode_f16": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
                                      _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
@@ -136,6 +138,16 @@ def attn_decode(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, 
     _check(load().ckv_attn_decode(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
                                   n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                   _stream(stream)))
+
+
+def attn_decode_noalloc(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse,
+                        n_split: int = 0, stream=None):
+    """attn_decode without a workspace: scratch lives in a fixed array inside the
+    library (for callers that cannot allocate device memory; calls must not
+    overlap on the GPU)."""
+    _, n_q, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_decode_noalloc(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads,
+                                          scale, n_split, _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def attn_decode_f16_workspace(head_dim: int, n_kv_heads: int, batch: int, max_seq_len: int, n_q: int,

@@ -1,0 +1,84 @@
+// attn_decode_noalloc.cu — compressed decode for callers that cannot allocate
+// device memory.
+//
+// ckv_attn_decode() needs a caller-provided workspace. Some callers have no way
+// to provide one: a host framework that owns all device memory and gives a
+// plug-in none of it, a latency-critical loop that must not call cudaMalloc
+// (which can block and synchronise the device), or a process whose memory
+// planner has already handed out the whole device. For them this entry point
+// runs the same two kernels (split-K decode and split merge) with their scratch
+// in a fixed array compiled into the library, so nothing is allocated at call
+// time.
+//
+// Limits and sharing:
+//  * The array holds kNoAllocScratchBytes (4 MiB) on every device that loads the
+//    library, for the life of the process. A call whose scratch would not fit
+//    (see ckv_attn_decode_workspace) is rejected with CKV_ERR_WORKSPACE.
+//  * All calls share the one array and it keeps the previous call's contents.
+//    The device flag word at its start is cleared by each call; the partials are
+//    fully rewritten by every call. Calls that overlap on the GPU (different
+//    streams, no ordering between them) race on the array and give wrong
+//    results: order them on one stream or with events.
+//  * The first call on a device looks up the array's device address on that
+//    device (cudaGetSymbolAddress, with the device current). Make that first
+//    call before any stream capture on the device.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/ckv.h"
+#include "ckv_kernels.cuh"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device (looked up once per device).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" CKV_API ckv_status ckv_attn_decode_noalloc(const ckv_cache* cache, const int32_t* seq_len,
+                                                      int64_t max_seq_len, const void* q_f16, int32_t n_q,
+                                                      int32_t n_q_heads, float scale, int32_t n_split,
+                                                      float* out, float* lse, void* stream) {
+  // Size the scratch exactly as ckv_attn_decode would, and refuse what does not fit.
+  const size_t need = ckv_attn_decode_workspace(cache, max_seq_len, n_q, n_q_heads, n_split);
+  if (need == 0) {
+    // Invalid geometry: let the regular entry point produce the precise status and message.
+    return ckv_attn_decode(cache, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
+                           nullptr, 0, stream);
+  }
+  if (need > kNoAllocScratchBytes)
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_WORKSPACE, "attn_decode_noalloc: needs %zu bytes of scratch, the built-in array holds %zu",
+        need, kNoAllocScratchBytes));
+  void* scratch = nullptr;
+  const cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess)
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_CUDA, "attn_decode_noalloc: scratch address lookup: %s", cudaGetErrorString(e)));
+  // ckv_attn_decode clears the flag word and rewrites every partial it reads.
+  return ckv_attn_decode(cache, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
+                         scratch, kNoAllocScratchBytes, stream);
+}

@@ -109,6 +109,16 @@ ckv_status check_ws(void* ws, size_t have, size_t need) {
 
 }  // namespace
 
+namespace ckv {
+int set_last_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return status;
+}
+}  // namespace ckv
+
 extern "C" {
 
 int32_t ckv_version(void) { return 100; }

@@ -83,4 +83,7 @@ cudaError_t launch_lse_merge(const LseMergeArgs& a, cudaStream_t stream);
 // Shared-memory bytes the compressed decode kernel needs for a head dim.
 size_t decode_smem_bytes(int head_dim);
 
+// Record a failure message for ckv_last_error() on this thread; returns `status`.
+int set_last_error(int status, const char* fmt, ...);
+
 }  // namespace ckv

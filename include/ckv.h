@@ -155,6 +155,29 @@ CKV_API ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_le
                            size_t ws_bytes, void* stream);
 
 /*
+ * attn_decode_noalloc — attn_decode for callers that cannot allocate device
+ * memory. The pages have no counterpart to this entry point; it exists for
+ * callers with no way to hand in a workspace: a host framework that owns all
+ * device memory and gives a plug-in none of it, a latency-critical loop that
+ * must not call cudaMalloc (it can block and synchronise the device), or a
+ * process whose memory planner has already handed out the whole device.
+ *
+ * Same arguments and results as attn_decode, without the workspace. The
+ * scratch is a 4 MiB array compiled into the library (held on every device that
+ * loads it until the process exits); a call whose scratch would exceed it (see
+ * ckv_attn_decode_workspace) returns CKV_ERR_WORKSPACE. Nothing is allocated.
+ * Every call shares that one array and it keeps the last call's contents: each
+ * call clears what must start at zero, but calls that overlap on the GPU race
+ * and give wrong results (order them on one stream or with events). The first
+ * call on a device looks up the array's address on that device; make that
+ * first call before any stream capture on the device.
+ */
+CKV_API ckv_status ckv_attn_decode_noalloc(const ckv_cache* cache, const int32_t* seq_len,
+                                           int64_t max_seq_len, const void* q_f16, int32_t n_q,
+                                           int32_t n_q_heads, float scale, int32_t n_split, float* out,
+                                           float* lse, void* stream);
+
+/*
  * attn_decode_f16 — the same decode over a dense fp16 KV cache (the private,
  * uncompressed tails of the shared-pool fan-out: PolyKV page, section "S1 —
  * SharedKVPool": one shared prefix plus a private suffix per agent).
