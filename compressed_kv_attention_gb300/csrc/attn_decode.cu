@@ -43,7 +43,9 @@ struct CDec : DecodeShape<D> {
   static constexpr int VW = 3 * Sh::MT_W / 4;   // V-code words per lane per warp
   static constexpr int GR = v_granule(D);       // stream granule bytes
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
-  static constexpr int RING = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
+  static constexpr int MERGE_BYTES = (2 * kMaxInKernelSplits * 8 + 16 + 256) * 4;
+  static constexpr int RING0 = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
+  static constexpr int RING = (RING0 > MERGE_BYTES) ? RING0 : MERGE_BYTES;
   static constexpr int OFF_XCHG = (RING + 127) / 128 * 128;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
   static constexpr int OFF_BAR = OFF_ML + Sh::NP * 16 * 4;
@@ -80,6 +82,58 @@ __device__ __forceinline__ uint32_t field_x128(const uint32_t* w, int bit) {
 }
 
 }  // namespace
+
+// S^T = K_hat Q^T for one tile record at shared address `rb`: this warp's
+// blocks, one accumulator per 32-dim block scaled by the block's fp16 scale.
+template <int D>
+__device__ __forceinline__ void qk_tile(uint32_t rb, int wh, int lane, const uint32_t (&qf)[CDec<D>::NB_W][4],
+                                        float (&S)[4]) {
+  using C = CDec<D>;
+  const int g = lane >> 2;
+  uint32_t sc0[C::NB_W / 2], sc1[C::NB_W / 2];
+  lds_words<C::NB_W * 2>(sc0, rb + k_scale_offset(D) + g * 2 * C::NB + wh * 2 * C::NB_W);
+  lds_words<C::NB_W * 2>(sc1, rb + k_scale_offset(D) + (g + 8) * 2 * C::NB + wh * 2 * C::NB_W);
+  S[0] = S[1] = S[2] = S[3] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < C::NB_W; ++i) {
+    const int blk = wh * C::NB_W + i;
+    const uint4 kk = lds128(rb + (blk * 32 + lane) * 16);
+    uint32_t a0s0, a2s0, a0s1, a2s1, a1s0, a3s0, a1s1, a3s1;
+    i8x4_to_half2x2(kk.x, a0s0, a2s0);
+    i8x4_to_half2x2(kk.y, a0s1, a2s1);
+    i8x4_to_half2x2(kk.z, a1s0, a3s0);
+    i8x4_to_half2x2(kk.w, a1s1, a3s1);
+    float c[4];
+    mma16816_zc(c, a0s0, a1s0, a2s0, a3s0, qf[i][0], qf[i][1]);
+    mma16816(c, a0s1, a1s1, a2s1, a3s1, qf[i][2], qf[i][3]);
+    const __half2 d0h = *reinterpret_cast<const __half2*>(&sc0[i >> 1]);
+    const __half2 d1h = *reinterpret_cast<const __half2*>(&sc1[i >> 1]);
+    const float d0 = (i & 1) ? __high2float(d0h) : __low2float(d0h);
+    const float d1 = (i & 1) ? __high2float(d1h) : __low2float(d1h);
+    S[0] = fmaf(d0, c[0], S[0]);
+    S[1] = fmaf(d0, c[1], S[1]);
+    S[2] = fmaf(d1, c[2], S[2]);
+    S[3] = fmaf(d1, c[3], S[3]);
+  }
+}
+
+// O^T += C^T P'^T for one tile record, straight from the 3-bit codes.
+template <int D>
+__device__ __forceinline__ void pv_tile(uint32_t rb, uint32_t lut, int wh, int lane, uint32_t pb0, uint32_t pb1,
+                                        float (&acc)[CDec<D>::MT_W][4]) {
+  using C = CDec<D>;
+  uint32_t vw[C::VW];
+#pragma unroll
+  for (int c3 = 0; c3 < 3; ++c3)
+    lds_words<C::GR>(vw + c3 * (C::GR / 4), rb + v_code_offset(D) + ((wh * 3 + c3) * 32 + lane) * C::GR);
+#pragma unroll
+  for (int i = 0; i < C::MT_W; ++i) {
+    uint32_t av[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) av[j] = lds32(lut + field_x128<C::VW>(vw, 6 * (4 * i + j)));
+    mma16816(acc[i], av[0], av[1], av[2], av[3], pb0, pb1);
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(DecodeArgs a) {
@@ -184,71 +238,66 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const uint32_t ring = smem_u32(smem);
   const uint32_t lut = smem_u32(s_lut) + (lane << 2);
 
-  for (int it = 0; it < n_iters; ++it) {
-    const int s = it % C::NSTAGE;
+  // Bounded wait for stage `it`; after a timeout every later wait is skipped
+  // (results are then flagged invalid) so that the CTA still finishes.
+  auto wait_stage = [&](int it) {
     if (!*(volatile int*)&s_abort) {
-      if (!mbar_wait(&full[s], (it / C::NSTAGE) & 1)) {
+      if (!mbar_wait(&full[it % C::NSTAGE], (it / C::NSTAGE) & 1)) {
         *(volatile int*)&s_abort = 1;
         raise_flag(a.flag, kFlagWaitTimeout);
       }
     }
-    const int64_t tile = tile_begin + (int64_t)it * C::NP + group;
-    if (tile < tile_end) {
-      const uint32_t rb = ring + s * C::STAGE + group * C::REC;
-      const int64_t tpos = tile * kTile;
+  };
+  auto record = [&](int it) { return ring + (it % C::NSTAGE) * C::STAGE + group * C::REC; };
 
-      // Scales of positions g and g+8 for this warp's blocks, and the V norms.
-      uint32_t sc0[C::NB_W / 2], sc1[C::NB_W / 2];
-      lds_words<C::NB_W * 2>(sc0, rb + k_scale_offset(D) + g * 2 * C::NB + wh * 2 * C::NB_W);
-      lds_words<C::NB_W * 2>(sc1, rb + k_scale_offset(D) + (g + 8) * 2 * C::NB + wh * 2 * C::NB_W);
+  // Software pipeline: while the softmax and P.V of tile `it` run, the
+  // S = K_hat Q^T of tile `it + 1` is already in flight. With two warps per
+  // tile, each warp's half of the next S goes to shared memory before the
+  // current P.V and is summed with the partner's half after it.
+  float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (n_iters > 0) {
+    wait_stage(0);
+    if (tile_begin + group < tile_end) {
+      qk_tile<D>(record(0), wh, lane, qf, S);
+      if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, 0, lane);
+    }
+  }
+  for (int it = 0; it < n_iters; ++it) {
+    const int64_t tile = tile_begin + (int64_t)it * C::NP + group;
+    const bool next = (it + 1 < n_iters) && (tile + C::NP < tile_end);
+    float Sn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (it + 1 < n_iters) wait_stage(it + 1);
+    if (next) {
+      qk_tile<D>(record(it + 1), wh, lane, qf, Sn);
+      if constexpr (C::WT == 2)
+        xbuf[((group * 2 + ((it + 1) & 1)) * 2 + wh) * 32 + lane] = make_float4(Sn[0], Sn[1], Sn[2], Sn[3]);
+    }
+    if (tile < tile_end) {
+      const uint32_t rb = record(it);
+      const int64_t tpos = tile * kTile;
       const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * g)));
       const float n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * (g + 8))));
-
-      // ---- S^T = K_hat Q^T, one accumulator per 32-dim block, scaled by d16 ----
-      float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int i = 0; i < C::NB_W; ++i) {
-        const int blk = wh * C::NB_W + i;
-        const uint4 kk = lds128(rb + (blk * 32 + lane) * 16);
-        uint32_t a0s0, a2s0, a0s1, a2s1, a1s0, a3s0, a1s1, a3s1;
-        i8x4_to_half2x2(kk.x, a0s0, a2s0);
-        i8x4_to_half2x2(kk.y, a0s1, a2s1);
-        i8x4_to_half2x2(kk.z, a1s0, a3s0);
-        i8x4_to_half2x2(kk.w, a1s1, a3s1);
-        float c[4];
-        mma16816_zc(c, a0s0, a1s0, a2s0, a3s0, qf[i][0], qf[i][1]);
-        mma16816(c, a0s1, a1s1, a2s1, a3s1, qf[i][2], qf[i][3]);
-        const __half2 d0h = *reinterpret_cast<const __half2*>(&sc0[i >> 1]);
-        const __half2 d1h = *reinterpret_cast<const __half2*>(&sc1[i >> 1]);
-        const float d0 = (i & 1) ? __high2float(d0h) : __low2float(d0h);
-        const float d1 = (i & 1) ? __high2float(d1h) : __low2float(d1h);
-        S[0] = fmaf(d0, c[0], S[0]);
-        S[1] = fmaf(d0, c[1], S[1]);
-        S[2] = fmaf(d1, c[2], S[2]);
-        S[3] = fmaf(d1, c[3], S[3]);
-      }
-      if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, it & 1, lane);
-
       uint32_t pb0, pb1;
-      softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, n0, n1, st,
-                            acc, pb0, pb1);
-
-      // ---- O^T += C^T P'^T straight from the 3-bit codes ----
-      uint32_t vw[C::VW];
-#pragma unroll
-      for (int c3 = 0; c3 < 3; ++c3)
-        lds_words<C::GR>(vw + c3 * (C::GR / 4),
-                         rb + v_code_offset(D) + ((wh * 3 + c3) * 32 + lane) * C::GR);
-#pragma unroll
-      for (int i = 0; i < C::MT_W; ++i) {
-        uint32_t av[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) av[j] = lds32(lut + field_x128<C::VW>(vw, 6 * (4 * i + j)));
-        mma16816(acc[i], av[0], av[1], av[2], av[3], pb0, pb1);
-      }
+      softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, n0, n1, st, acc, pb0,
+                            pb1);
+      pv_tile<D>(rb, lut, wh, lane, pb0, pb1, acc);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&empty[it % C::NSTAGE]);
+    if constexpr (C::WT == 2) {
+      if (next) {
+        named_bar(2 + group, 64);
+        const float4 o = xbuf[((group * 2 + ((it + 1) & 1)) * 2 + (1 - wh)) * 32 + lane];
+        Sn[0] += o.x;
+        Sn[1] += o.y;
+        Sn[2] += o.z;
+        Sn[3] += o.w;
+      }
+    }
+    S[0] = Sn[0];
+    S[1] = Sn[1];
+    S[2] = Sn[2];
+    S[3] = Sn[3];
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
@@ -260,6 +309,19 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   __shared__ float* s_out[8];
   __shared__ float* s_lse[8];
   decode_merge_tail<D>(a, split, rg, b, kvh, tid, reinterpret_cast<float*>(smem), &s_ok, s_out, s_lse);
+}
+
+// ------------------------------------------------------- header reset --
+
+// Clears the workspace header (device flag + split-merge counters) before a
+// decode. A one-block kernel: a memset node costs several times more.
+__global__ void __launch_bounds__(256) ws_reset_kernel(uint32_t* header, int words) {
+  for (int i = threadIdx.x; i < words; i += blockDim.x) header[i] = 0u;
+}
+
+cudaError_t launch_ws_reset(void* header, size_t bytes, cudaStream_t stream) {
+  ws_reset_kernel<<<1, 256, 0, stream>>>(static_cast<uint32_t*>(header), static_cast<int>(bytes / 4));
+  return cudaGetLastError();
 }
 
 // --------------------------------------------------------------- merge --
@@ -330,7 +392,7 @@ cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stre
 template <int D>
 static cudaError_t launch_merge_d(const MergeArgs& m, cudaStream_t stream) {
   const int64_t groups = (int64_t)m.batch * m.n_kv_heads * m.n_row_groups;
-  const size_t smem = (size_t)(m.n_split * 8 + 16 + 256) * sizeof(float);
+  const size_t smem = (size_t)(2 * m.n_split * 8 + 16 + 256) * sizeof(float);
   static size_t configured = 0;
   if (smem > 48 * 1024 && smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -192,7 +192,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   if (s != CKV_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t header = ws_header_bytes(p.groups);
-  cudaError_t e = cudaMemsetAsync(ws, 0, header, st);
+  cudaError_t e = ckv::launch_ws_reset(ws, header, st);
   if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
   uint8_t* base = static_cast<uint8_t*>(ws);
   ckv::DecodeArgs a{};

@@ -68,6 +68,8 @@ constexpr int kMaxInKernelSplits = 512;
 cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stream);
 cudaError_t launch_attn_decode_f16(DecodeArgs a, bool cooperative, cudaStream_t stream);
 cudaError_t launch_decode_merge(const MergeArgs& a, cudaStream_t stream);
+// Zero the first `bytes` (a multiple of 4) of a workspace.
+cudaError_t launch_ws_reset(void* header, size_t bytes, cudaStream_t stream);
 
 struct LseMergeArgs {
   const float* o[16];

@@ -26,7 +26,11 @@ struct DecodeShape {
   static constexpr int NB_W = NB / WT;              // blocks per warp (S)
   static constexpr int MT_W = MT / WT;              // m-tiles per warp (O)
   static constexpr int GD = D / 8;                  // output dims owned per lane row
-  static constexpr int RED_FLOATS = 8 * (D + 8);    // per-group reduction buffer
+  // Per-group reduction buffer [8 rows][RP]: dim d of row r at r*RP + d + d/GD.
+  // RP = D + 36 is = 4 (mod 32), which makes both the fragment-order writes and
+  // the row-order reads free of shared-memory bank conflicts.
+  static constexpr int RP = D + 36;
+  static constexpr int RED_FLOATS = 8 * RP;
   static constexpr int XCHG_BYTES = (WT == 2) ? NP * 2 * 2 * 32 * 16 : 0;
 };
 
@@ -148,29 +152,38 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
   float* myred = red + group * Sh::RED_FLOATS;
 #pragma unroll
   for (int i = 0; i < MTW; ++i) {
-    const int d0 = Sh::GD * g + 2 * (wh * MTW + i);
-    *reinterpret_cast<float2*>(myred + d0 * 8 + 8 * g + 2 * t) =
-        make_float2(acc[i][0] * f0, acc[i][1] * f1);
-    *reinterpret_cast<float2*>(myred + (d0 + 1) * 8 + 8 * g + 2 * t) =
-        make_float2(acc[i][2] * f0, acc[i][3] * f1);
+    const int d0 = Sh::GD * g + 2 * (wh * MTW + i) + g;  // padded index of dim d0 (d0 / GD == g)
+    myred[(2 * t) * Sh::RP + d0] = acc[i][0] * f0;
+    myred[(2 * t + 1) * Sh::RP + d0] = acc[i][1] * f1;
+    myred[(2 * t) * Sh::RP + d0 + 1] = acc[i][2] * f0;
+    myred[(2 * t + 1) * Sh::RP + d0 + 1] = acc[i][3] * f1;
   }
   named_bar(1, Sh::NCW * 32);
-  // Warp r owns row r: lane holds dims [lane*E, lane*E + E), summed over groups.
+  // Warp r owns row r: lane holds dims d = 32 e + lane (e < E), summed over groups.
   constexpr int E = D / 32;
   const int r = warp;
   float v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int d = lane * E + e;
+    const int d = 32 * e + lane;
     float x = 0.0f;
 #pragma unroll
-    for (int q = 0; q < Sh::NP; ++q) x += red[q * Sh::RED_FLOATS + d * 8 + 8 * (d / Sh::GD) + r];
+    for (int q = 0; q < Sh::NP; ++q) x += red[q * Sh::RED_FLOATS + r * Sh::RP + d + d / Sh::GD];
     v[e] = x;
   }
   if (signs) {
-    // Unnormalised Walsh-Hadamard transform of the row: stages inside the lane,
-    // then across lanes; then the sign flip and 1/D (one 1/sqrt(D) from the
-    // orthonormal inverse, one from the norm scaling folded into P').
+    // Unnormalised Walsh-Hadamard transform of the row: stages h < 32 pair
+    // lanes (shuffles), stages h >= 32 pair registers of the same lane; then the
+    // sign flip and 1/D (one 1/sqrt(D) from the orthonormal inverse, one from
+    // the norm scaling folded into P').
+#pragma unroll
+    for (int hl = 1; hl < 32; hl <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
+        v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+      }
+    }
 #pragma unroll
     for (int hh = 1; hh < E; hh <<= 1) {
 #pragma unroll
@@ -183,28 +196,14 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
       }
     }
 #pragma unroll
-    for (int hl = 1; hl < 32; hl <<= 1) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
-        v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
-      }
-    }
-#pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int d = lane * E + e;
+      const int d = 32 * e + lane;
       v[e] = (signs[d] < 0 ? -v[e] : v[e]) * (1.0f / D);
     }
   }
-  float* prow = part_out + r * D + lane * E;
-  if constexpr (E % 4 == 0) {
+  float* prow = part_out + r * D + lane;
 #pragma unroll
-    for (int e = 0; e < E; e += 4)
-      *reinterpret_cast<float4*>(prow + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; e += 2) *reinterpret_cast<float2*>(prow + e) = make_float2(v[e], v[e + 1]);
-  }
+  for (int e = 0; e < E; ++e) prow[32 * e] = v[e];
   if (tid < 8) {
     float mc = -INFINITY;
 #pragma unroll
@@ -224,38 +223,48 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
 // M = max_s m_s, w_s = 2^(m_s - M), O = sum_s w_s part_s / sum_s w_s l_s,
 // lse = (M + log2 sum_s w_s l_s) ln 2; a row with no key gives O = 0, lse = -inf.
 // part: [n_split][8][D], ml: [n_split][8][2] of the group. This CTA produces
-// the elements [e0, e1) of the 8 x D output (row-major); threads tid < nthr take
-// part and synchronise on named barrier `bar_id`. `sm` provides
-// n_split * 8 + 16 + nthr floats. out_rows / lse_rows: where each row goes
+// the elements [e0, e1) of the 8 x D output (row-major); threads tid < nthr
+// (nthr >= 256, 8 full warps) take part and synchronise on named barrier
+// `bar_id`. `sm` provides 2 * n_split * 8 + 16 + nthr floats. out_rows / lse_rows: where each row goes
 // (nullptr for padding rows); lse is written when write_lse.
 template <int D>
 __device__ __forceinline__ void merge_rows(const float* part, const float* ml, int n_split, int e0,
                                            int e1, int tid, int nthr, float* sm, float* const* out_rows,
                                            float* const* lse_rows, bool write_lse, int bar_id) {
-  float* w = sm;                  // [n_split][8] weights
+  float* w = sm;                  // [n_split][8] running maxima, then weights
   float* ML = sm + n_split * 8;   // [8][2]: max, 1/sum (0 when empty)
   float* red = ML + 16;           // [nthr] partial sums
-  for (int i = tid; i < n_split * 8; i += nthr) w[i] = __ldcg(ml + i * 2);
-  named_bar(bar_id, nthr);
-  if (tid < 8) {
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, w[s * 8 + tid]);
-    ML[tid * 2] = M;
-  }
-  named_bar(bar_id, nthr);
+  float* lsum = red + nthr;       // [n_split][8] row sums
+  const float2* ml2 = reinterpret_cast<const float2*>(ml);
   for (int i = tid; i < n_split * 8; i += nthr) {
-    const float M = ML[(i & 7) * 2];
-    const float m = w[i];
-    w[i] = (m == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(m - M);
+    const float2 x = __ldcg(ml2 + i);
+    w[i] = x.x;
+    lsum[i] = x.y;
   }
   named_bar(bar_id, nthr);
-  if (tid < 8) {
+  // Warp r (r < 8) reduces row r over the splits: max, weights, weighted sum.
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 8) {
+    const int r = warp;
+    float M = -INFINITY;
+    for (int s = lane; s < n_split; s += 32) M = fmaxf(M, w[s * 8 + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.0f;
-    for (int s = 0; s < n_split; ++s) L = fmaf(w[s * 8 + tid], __ldcg(ml + (s * 8 + tid) * 2 + 1), L);
-    const float M = ML[tid * 2];
-    ML[tid * 2 + 1] = (L > 0.0f) ? 1.0f / L : 0.0f;
-    if (write_lse && lse_rows[tid])
-      *lse_rows[tid] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    for (int s = lane; s < n_split; s += 32) {
+      const float m = w[s * 8 + r];
+      const float ws = (m == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(m - M);
+      w[s * 8 + r] = ws;
+      L = fmaf(ws, lsum[s * 8 + r], L);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) {
+      ML[r * 2] = M;
+      ML[r * 2 + 1] = (L > 0.0f) ? 1.0f / L : 0.0f;
+      if (write_lse && lse_rows[r])
+        *lse_rows[r] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
   }
   named_bar(bar_id, nthr);
   const int ne = e1 - e0;
@@ -271,8 +280,20 @@ __device__ __forceinline__ void merge_rows(const float* part, const float* ml, i
     float acc = 0.0f;
     if (el < ne) {
       const float* p = part + (size_t)r * D + d;
-#pragma unroll 8
-      for (int s = pk; s < n_split; s += k) acc = fmaf(w[s * 8 + r], __ldcg(p + (size_t)s * 8 * D), acc);
+      // Issue a batch of independent loads before using any of them.
+      for (int s0 = pk; s0 < n_split; s0 += 16 * k) {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int sj = s0 + j * k;
+          x[j] = (sj < n_split) ? __ldcg(p + (size_t)sj * 8 * D) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int sj = s0 + j * k;
+          if (sj < n_split) acc = fmaf(w[sj * 8 + r], x[j], acc);
+        }
+      }
     }
     red[tid] = acc;
     named_bar(bar_id, nthr);

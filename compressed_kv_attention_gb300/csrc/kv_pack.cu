@@ -174,6 +174,16 @@ cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream) {
   const int64_t t0 = a.tok_offset / kTile;
   const int64_t t1 = (a.tok_offset + a.n_tok - 1) / kTile;
   dim3 grid(static_cast<unsigned>(t1 - t0 + 1), static_cast<unsigned>(a.batch * a.n_kv_heads));
+  // Same shared-memory carveout as the decode kernels, so that an SM does not
+  // reconfigure its L1 / shared split between a pack and the decode after it.
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(kv_pack_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(kv_pack_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(kv_pack_kernel<256>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(kv_pack_kernel<512>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    configured = true;
+  }
   switch (a.head_dim) {
     case 64: kv_pack_kernel<64><<<grid, 512, 0, stream>>>(a); break;
     case 128: kv_pack_kernel<128><<<grid, 512, 0, stream>>>(a); break;
