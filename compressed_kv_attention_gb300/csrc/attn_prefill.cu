@@ -1,22 +1,524 @@
-// attn_prefill.cu — chunked causal prefill over the packed cache (tcgen05).
+// attn_prefill.cu — chunked causal prefill over the packed cache on tcgen05.
+//
+// PolyKV page ("F5 M6 — PolyKV (shared compressed KV pool)"), section "S2
+// perf-path Level B": large-n_q prefill over turbo KV is a tensor-core job
+// (the vector kernel is 2-3x slower than f16 MMA there). Here the n_new new
+// K/V rows are packed first (q8_0 / TBQ3, as kv_pack), then every query tile
+// attends over the packed cache through fifth-generation tensor cores.
+//
+// One CTA owns 128 query rows (128 / G query tokens x G heads of one kv head)
+// and walks the cache in 64-token steps:
+//   S  = Q K_hat^T        M = 128, N = 64, K = D, in TMEM columns [0, 64).
+//        K_hat = q * d16 has up to 18 significant bits, so it enters the tensor
+//        core as an exact fp16 pair hi + lo (two passes of MMAs into the same
+//        accumulator); Q is bf16, which converts to fp16 exactly.
+//   online softmax, one row per thread (warps 0-3), the running max moving
+//        only when it grows by more than 2^4 (O in TMEM is rescaled then);
+//        P' = p * norm as fp16 into shared memory.
+//   O += P' C             C = the Lloyd-Max centroids of the V codes (the
+//        rotated basis); dims [0, 448) accumulate in TMEM columns [64, 512); at
+//        D = 512 the last 64 dims go through columns [0, 64) each step and are
+//        summed in registers.
+// Operands live in shared memory in the 128-byte-swizzle K-major layout. The
+// output leaves the kernel normalised but still in the rotated basis; a
+// per-row kernel then applies the inverse Walsh-Hadamard transform and the
+// sign flip in place (the transform runs once per output row, never on the
+// cache).
 #include <cuda_runtime.h>
 
 #include "../../include/ckv.h"
 #include "ckv_kernels.cuh"
 
-extern "C" {
+namespace ckv {
 
-size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads) {
-  (void)cache; (void)n_new; (void)n_q_heads;
-  return 256;
+namespace {
+
+__constant__ float kPrefillCentroids[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
+                                           0.2451f,  0.7560f,  1.3439f,  2.1520f};
+
+struct PrefillArgs {
+  const uint8_t* cache;
+  int64_t capacity;
+  int n_kv_heads, batch;
+  int64_t n_cached;
+  int n_new, n_q_heads;
+  const __nv_bfloat16* q;  // [batch][n_new][n_q_heads][D]
+  float scale_log2;
+  float* out;              // [batch][n_new][n_q_heads][D]
+  float* lse;              // [batch][n_new][n_q_heads]
+  int32_t* flag;
+};
+
+template <int D>
+struct PCfg {
+  static constexpr int M = 128;                  // query rows per CTA
+  static constexpr int NKV = 64;                 // cached tokens per step
+  static constexpr int NB = D / 32;              // q8_0 blocks per vector
+  static constexpr int OT = D < 448 ? D : 448;   // output dims accumulated in TMEM
+  static constexpr int OR = D - OT;              // output dims summed in registers (0 or 64)
+  static constexpr int REC = record_bytes(D);
+  static constexpr int PIECES = NKV * NB;        // (token, 32-block) pieces of K per step
+  static constexpr int PPT = (PIECES + 255) / 256;  // pieces per thread
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = M * D * 2;                 // K_hat hi, then lo, then C^T
+  static constexpr int P_OFF = KV_OFF + NKV * D * 2;
+  static constexpr int NORM_OFF = P_OFF + M * NKV * 2;
+  static constexpr int BYTES = NORM_OFF + NKV * 4;
+  // At least half the SM's shared memory, so that one CTA (and its 512 TMEM
+  // columns) owns each SM.
+  static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);
+  static constexpr int THREADS = 256;
+};
+
+// TMEM column of output dim chunk c, and the chunks' (first dim, width, column):
+// dims [0, 256) -> column 64, dims [256, OT) -> column 320, dims [OT, D) -> column 0.
+struct OChunk {
+  int dim0, n, col;
+};
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
+  using C = PCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sQ = smem + C::Q_OFF;
+  uint8_t* sKV = smem + C::KV_OFF;
+  uint8_t* sP = smem + C::P_OFF;
+  float* sNorm = reinterpret_cast<float*>(smem + C::NORM_OFF);
+
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int QT = C::M / group_q;                   // query tokens per CTA
+  const int q0 = blockIdx.x * QT;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int last_q = min(q0 + QT, a.n_new) - 1;
+  const int64_t kv_end = a.n_cached + last_q + 1;  // keys any row of this tile can see
+  const int n_steps = static_cast<int>((kv_end + C::NKV - 1) / C::NKV);
+  const int64_t n_rec = a.capacity / kTile;
+  const uint8_t* stream = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * n_rec * C::REC;
+
+  if (warp == 0) tmem_alloc(&s_tmem, 512);
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+
+  // ---- Q tile: bf16 -> fp16 (exact in range), 128-byte swizzled K-major ----
+  for (int piece = tid; piece < C::M * (D / 8); piece += C::THREADS) {
+    const int r = piece / (D / 8), k0 = (piece % (D / 8)) * 8;
+    const int qi = q0 + r / group_q, h = kvh * group_q + r % group_q;
+    uint4 outv = make_uint4(0, 0, 0, 0);
+    if (qi < a.n_new) {
+      const uint4 v =
+          *reinterpret_cast<const uint4*>(a.q + (((int64_t)b * a.n_new + qi) * a.n_q_heads + h) * D + k0);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+        o[i] = pack_half2(__low2float(x), __high2float(x));
+      }
+      outv = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    *reinterpret_cast<uint4*>(sQ + sw128_offset(r, k0, C::M)) = outv;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+
+  // Per-row state (warps 0-3: thread = row).
+  const bool softmax_warp = warp < 4;
+  const int row = tid & 127;
+  const int row_qi = q0 + row / group_q;
+  const bool row_valid = row_qi < a.n_new;
+  const int64_t row_limit = a.n_cached + row_qi;  // last key this row sees
+  float m_used = -INFINITY, l_sum = 0.0f;
+  float otail[C::OR > 0 ? C::OR : 1];
+#pragma unroll
+  for (int i = 0; i < (C::OR > 0 ? C::OR : 1); ++i) otail[i] = 0.0f;
+  const uint32_t row_tmem = tmem + ((uint32_t)(warp & 3) * 32u << 16);
+
+  uint32_t phase = 0;
+  auto wait_mma = [&]() {
+    if (!*(volatile int*)&s_abort) {
+      if (!mbar_wait(&s_bar, phase & 1)) {
+        *(volatile int*)&s_abort = 1;
+        raise_flag(a.flag, kFlagWaitTimeout);
+      }
+    }
+    ++phase;
+    tc_fence_after();
+  };
+  auto sync_for_mma = [&]() {  // generic-proxy shared writes and TMEM stores -> tensor core
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  auto issue_s = [&]() {  // S (+)= Q K^T over D, from the K tile in sKV
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * (C::M * 128) + (ks & 3) * 32);
+      const uint64_t bd = umma_desc_sw128(kv_base + (ks >> 2) * (C::NKV * 128) + (ks & 3) * 32);
+      umma_f16(tmem, ad, bd, umma_idesc_f16_f32(C::M, C::NKV), true);
+    }
+  };
+  constexpr int NCH = (C::OT > 256 ? 2 : 1) + (C::OR > 0 ? 1 : 0);
+  const OChunk chunks[3] = {{0, C::OT < 256 ? C::OT : 256, 64},
+                            {256, C::OT > 256 ? C::OT - 256 : 0, 320},
+                            {C::OT, C::OR, 0}};
+
+  for (int step = 0; step < n_steps; ++step) {
+    const int64_t j0 = (int64_t)step * C::NKV;
+    // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
+    uint32_t lo_keep[C::PPT][4][4];
+#pragma unroll
+    for (int pc = 0; pc < C::PPT; ++pc) {
+      const int piece = tid + pc * C::THREADS;
+      const int p = piece / C::NB, blk = piece % C::NB;
+      const int64_t rec = (j0 + p) / kTile;
+      const int pp = p % kTile;
+      const bool in_tile = piece < C::PIECES;
+      const bool have = in_tile && rec < n_rec;
+      const uint8_t* rb = stream + rec * C::REC;
+      float d = 0.0f;
+      if (have) d = __half2float(*reinterpret_cast<const __half*>(rb + k_scale_offset(D) + 2 * (pp * C::NB + blk)));
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint2 w = make_uint2(0, 0);
+        if (have) w = *reinterpret_cast<const uint2*>(rb + (blk * 32 + 4 * (pp & 7) + t) * 16 + (pp >> 3) * 8);
+        uint32_t hi[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t word = e < 2 ? w.x : w.y;
+          const int sh = (e & 1) * 16;
+          const float k0v = (float)(int8_t)((word >> sh) & 0xFFu) * d;       // exact in fp32
+          const float k1v = (float)(int8_t)((word >> (sh + 8)) & 0xFFu) * d;
+          const __half h0 = __float2half_rn(k0v), h1 = __float2half_rn(k1v);
+          hi[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+          lo_keep[pc][t][e] = pack_half2(k0v - __half2float(h0), k1v - __half2float(h1));
+        }
+        if (in_tile)
+          *reinterpret_cast<uint4*>(sKV + sw128_offset(p, blk * 32 + 8 * t, C::NKV)) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+    }
+    // V norms of the step's tokens (positions past the cache read as 0).
+    if (tid < C::NKV) {
+      const int64_t rec = (j0 + tid) / kTile;
+      float n = 0.0f;
+      if (rec < n_rec)
+        n = __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D) + 2 * ((j0 + tid) % kTile)));
+      sNorm[tid] = n;
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      // First pass of S overwrites the accumulator (columns [0, 64)).
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * (C::M * 128) + (ks & 3) * 32);
+        const uint64_t bd = umma_desc_sw128(kv_base + (ks >> 2) * (C::NKV * 128) + (ks & 3) * 32);
+        umma_f16(tmem, ad, bd, umma_idesc_f16_f32(C::M, C::NKV), ks > 0);
+      }
+      umma_commit(&s_bar);
+    }
+    wait_mma();
+    // ---- lo pass ----
+#pragma unroll
+    for (int pc = 0; pc < C::PPT; ++pc) {
+      const int piece = tid + pc * C::THREADS;
+      const int p = piece / C::NB, blk = piece % C::NB;
+      if (piece < C::PIECES) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          *reinterpret_cast<uint4*>(sKV + sw128_offset(p, blk * 32 + 8 * t, C::NKV)) =
+              make_uint4(lo_keep[pc][t][0], lo_keep[pc][t][1], lo_keep[pc][t][2], lo_keep[pc][t][3]);
+      }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      issue_s();
+      umma_commit(&s_bar);
+    }
+    wait_mma();
+
+    if (softmax_warp) {
+      // ---- online softmax of this step's 64 columns, one row per thread ----
+      uint32_t sv[2][32];
+      tmem_ld32(row_tmem + 0, sv[0]);
+      tmem_ld32(row_tmem + 32, sv[1]);
+      tmem_ld_wait();
+      float x[C::NKV];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < C::NKV; ++j) {
+        const bool vis = row_valid && (j0 + j <= row_limit);
+        x[j] = vis ? __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, x[j]);
+      }
+      const float m_new = fmaxf(m_used, mt);
+      const bool need = (m_new > m_used + 4.0f);  // also true when m_used is -inf and a key is visible
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? ((m_used == -INFINITY) ? 0.0f : exp2f(m_used - m_new)) : 1.0f;
+        if (step > 0) {
+          // Rescale O in TMEM (initialised by the first P.V) and the register tail.
+#pragma unroll 1
+          for (int c0 = 64; c0 < 64 + C::OT; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(row_tmem + c0, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+            tmem_st32(row_tmem + c0, ov);
+          }
+          tmem_st_wait();
+        }
+#pragma unroll
+        for (int i = 0; i < C::OR; ++i) otail[i] *= f;
+        l_sum *= f;
+        if (need) m_used = m_new;
+      }
+      float ps = 0.0f;
+      uint32_t pw[C::NKV / 2];
+#pragma unroll
+      for (int j = 0; j < C::NKV; j += 2) {
+        const float p0 = (x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - m_used);
+        const float p1 = (x[j + 1] == -INFINITY) ? 0.0f : exp2f(x[j + 1] - m_used);
+        ps += p0 + p1;
+        pw[j / 2] = pack_half2(p0 * sNorm[j], p1 * sNorm[j + 1]);
+      }
+      l_sum += ps;
+#pragma unroll
+      for (int c = 0; c < C::NKV / 8; ++c)
+        *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * c, C::M)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+    } else {
+      // ---- C^T (centroids, rotated basis) for the step: rows = dims, K = tokens ----
+      // One (record, lane stream) per thread: 4 records x 32 lanes = 128 threads.
+      const int u = tid - 128;
+      const int r4 = u >> 5, L = u & 31;
+      const int64_t rec = j0 / kTile + r4;
+      constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D);
+      uint32_t sw[LB / 4];
+      if (rec < n_rec) {
+        const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
+#pragma unroll
+        for (int s4 = 0; s4 < LB / 4; ++s4) {
+          const int sbyte = s4 * 4;
+          sw[s4] = *reinterpret_cast<const uint32_t*>(vb + ((sbyte / GR) * 32 + L) * GR + (sbyte % GR));
+        }
+      } else {
+#pragma unroll
+        for (int s4 = 0; s4 < LB / 4; ++s4) sw[s4] = 0u;
+      }
+      const int g = L >> 2, tq = L & 3;
+#pragma unroll 4
+      for (int pi = 0; pi < 2 * G; ++pi) {
+        const int bit = 6 * pi;
+        const int wi = bit >> 5, sh = bit & 31;
+        uint32_t f = sw[wi] >> sh;
+        if (sh > 26 && wi + 1 < LB / 4) f |= sw[wi + 1] << (32 - sh);
+        const int ce = f & 7, co = (f >> 3) & 7;
+        const int mt = pi >> 2, rh = pi & 1, h2 = (pi >> 1) & 1;
+        const int dim = G * g + 2 * mt + rh;
+        const int tok = r4 * 16 + 2 * tq + 8 * h2;  // even position; the odd one follows it in K
+        const uint32_t val = pack_half2(kPrefillCentroids[ce], kPrefillCentroids[co]);
+        *reinterpret_cast<uint32_t*>(sKV + sw128_offset(dim, tok, D)) = val;
+      }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      // ---- O += P' C over the step's 64 tokens ----
+      for (int ks = 0; ks < C::NKV / 16; ++ks) {
+        const uint64_t ad = umma_desc_sw128(p_base + ks * 32);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          if (chunks[c].n == 0) continue;
+          const uint64_t bd = umma_desc_sw128(kv_base + chunks[c].dim0 * 128 + ks * 32);
+          const bool acc = (c == 2) ? (ks > 0) : (step > 0 || ks > 0);
+          umma_f16(tmem + chunks[c].col, ad, bd, umma_idesc_f16_f32(C::M, chunks[c].n), acc);
+        }
+      }
+      umma_commit(&s_bar);
+    }
+    wait_mma();
+    if (C::OR > 0 && softmax_warp) {
+      uint32_t tv[2][32];
+      tmem_ld32(row_tmem + 0, tv[0]);
+      tmem_ld32(row_tmem + 32, tv[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < C::OR; ++i) otail[i] += __uint_as_float(tv[i >> 5][i & 31]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+
+  // ---- normalise and write the rotated-basis rows; lse ----
+  if (softmax_warp) {
+    const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
+    const int h = kvh * group_q + row % group_q;
+    float* orow = a.out + (((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h) * D;
+#pragma unroll 1
+    for (int c0 = 0; c0 < C::OT; c0 += 32) {
+      uint32_t ov[32];
+      if (n_steps > 0) {
+        tmem_ld32(row_tmem + 64 + c0, ov);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+      }
+      if (row_valid) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(orow + c0 + i) =
+              make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                          __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+      }
+    }
+    if (row_valid) {
+#pragma unroll
+      for (int i = 0; i < C::OR; i += 4)
+        *reinterpret_cast<float4*>(orow + C::OT + i) =
+            make_float4(otail[i] * inv, otail[i + 1] * inv, otail[i + 2] * inv, otail[i + 3] * inv);
+      a.lse[((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h] =
+          l_sum > 0.0f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16, int32_t n_new,
-                            int32_t n_q_heads, const void* k_new_f16, const void* v_new_f16, float scale,
-                            float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
-  (void)cache; (void)n_cached; (void)q_bf16; (void)n_new; (void)n_q_heads; (void)k_new_f16;
-  (void)v_new_f16; (void)scale; (void)out; (void)lse; (void)workspace; (void)ws_bytes; (void)stream;
-  return CKV_ERR_UNSUPPORTED;
+// Inverse transform of prefill rows in place: row = s * H_D(row) / D.
+template <int D>
+__global__ void __launch_bounds__(256) derotate_rows_kernel(float* rows, int64_t n_rows, const int8_t* signs) {
+  constexpr int E = D / 32;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= n_rows) return;
+  float* p = rows + r * D;
+  float v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = p[32 * e + lane];
+#pragma unroll
+  for (int hl = 1; hl < 32; hl <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
+      v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+    }
+  }
+#pragma unroll
+  for (int hh = 1; hh < E; hh <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & hh) == 0) {
+        const float x0 = v[e], x1 = v[e + hh];
+        v[e] = x0 + x1;
+        v[e + hh] = x0 - x1;
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int d = 32 * e + lane;
+    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (1.0f / D);
+  }
+}
+
+template <int D>
+static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, cudaStream_t stream) {
+  using Cf = PCfg<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int qt = Cf::M / group_q;
+  dim3 grid((a.n_new + qt - 1) / qt, a.n_kv_heads, a.batch);
+  attn_prefill_kernel<D><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
+  derotate_rows_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(a.out, rows, signs);
+  return cudaGetLastError();
+}
+
+}  // namespace ckv
+
+extern "C" {
+
+CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads) {
+  (void)cache;
+  (void)n_new;
+  (void)n_q_heads;
+  return 256;  // the device flag word
+}
+
+CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16, int32_t n_new,
+                                    int32_t n_q_heads, const void* k_new_f16, const void* v_new_f16, float scale,
+                                    float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache) return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "cache is null"));
+  if (cache->head_dim != 512 && cache->head_dim != 256 && cache->head_dim != 128)
+    return static_cast<ckv_status>(
+        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill supports head_dim 128, 256, 512 (got %d)", cache->head_dim));
+  if (n_new < 0 || n_cached < 0 || n_cached + n_new > cache->capacity || cache->capacity % 16)
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "token range outside the cache"));
+  if (n_q_heads <= 0 || cache->n_kv_heads <= 0 || n_q_heads % cache->n_kv_heads ||
+      128 % (n_q_heads / cache->n_kv_heads))
+    return static_cast<ckv_status>(
+        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill needs n_q_heads / n_kv_heads dividing 128"));
+  if (!cache->data || !cache->v_signs || (reinterpret_cast<uintptr_t>(cache->data) & 15))
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "cache data / signs"));
+  if (n_new == 0) return CKV_OK;
+  if (!q_bf16 || !k_new_f16 || !v_new_f16 || !out || !lse || (reinterpret_cast<uintptr_t>(q_bf16) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(k_new_f16) & 15) ||
+      (reinterpret_cast<uintptr_t>(v_new_f16) & 15))
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "null or misaligned tensor"));
+  if (!workspace || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_WORKSPACE, "workspace needs 256 aligned bytes"));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = ckv::launch_ws_reset(workspace, 256, st);
+  if (e != cudaSuccess)
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_CUDA, "flag reset: %s", cudaGetErrorString(e)));
+  // Pack the new rows (same quantisers as kv_pack) at [n_cached, n_cached + n_new).
+  const int64_t row = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
+  const ckv_status ps = ckv_kv_pack(cache, n_cached, n_new, k_new_f16, v_new_f16, row, row * n_new, stream);
+  if (ps != CKV_OK) return ps;
+  ckv::PrefillArgs a{};
+  a.cache = static_cast<const uint8_t*>(cache->data);
+  a.capacity = cache->capacity;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.batch = cache->batch;
+  a.n_cached = n_cached;
+  a.n_new = n_new;
+  a.n_q_heads = n_q_heads;
+  a.q = static_cast<const __nv_bfloat16*>(q_bf16);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  a.lse = lse;
+  a.flag = static_cast<int32_t*>(workspace);
+  switch (cache->head_dim) {
+    case 128: e = ckv::launch_prefill_d<128>(a, cache->v_signs, st); break;
+    case 256: e = ckv::launch_prefill_d<256>(a, cache->v_signs, st); break;
+    default: e = ckv::launch_prefill_d<512>(a, cache->v_signs, st); break;
+  }
+  if (e != cudaSuccess)
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e)));
+  return CKV_OK;
 }
 
 }  // extern "C"

@@ -111,3 +111,21 @@ def test_decode_f16_and_merge_argument_checks(lib):
 def test_read_device_flag_checks(lib):
     flag = ctypes.c_int32(7)
     assert lib.ckv_read_device_flag(None, ctypes.byref(flag), None) == -1
+
+
+def test_prefill_argument_checks(lib):
+    fake = 0x7f0000000000
+    c = _fake_cache(D=512, Hkv=2, cap=4096)
+    ws = 256
+    call = lambda cache=c, n_cached=0, q=fake, n_new=16, hq=16, k=fake, v=fake, out=fake, lse=fake, w=fake, wb=ws: \
+        lib.ckv_attn_prefill(ctypes.byref(cache) if cache is not None else None, n_cached, q, n_new, hq, k, v,
+                             0.04, out, lse, w, wb, None)
+    assert call(cache=None) == -1
+    assert call(cache=_fake_cache(D=64)) == -2       # prefill head dims: 128, 256, 512
+    assert call(n_cached=4090) == -1                 # past capacity
+    assert call(hq=12) == -2                         # 6 heads per kv head does not divide 128
+    assert call(q=fake + 8) == -1
+    assert call(out=None) == -1
+    assert call(w=None) == -3
+    assert call(wb=128) == -3
+    assert call(n_new=0) == 0                        # nothing to do

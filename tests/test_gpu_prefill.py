@@ -1,0 +1,89 @@
+"""GPU parity of the chunked prefill (pack the new rows, then causal attention
+of the new queries over the packed cache on tcgen05) against the oracle:
+query i of the new chunk sees cached positions [0, n_cached + i], the new rows
+read back in packed form."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import compressed_kv_attention_gb300 as ckv  # noqa: E402
+from compressed_kv_attention_gb300 import inputs  # noqa: E402
+from oracle import ckv_oracle as O  # noqa: E402
+from tests import helpers as H  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(D, Hkv, Hq, B, n_cached, n_new, cap, seed):
+    outl = inputs.outlier_channels(D, max(1, round(0.01 * D)), seed)
+    T = n_cached + n_new
+    k = inputs.normal_tensor((B, T, Hkv, D), seed, "pf/k", outl)
+    v = inputs.normal_tensor((B, T, Hkv, D), seed, "pf/v", outl)
+    q = inputs.normal_tensor((B, n_new, Hq, D), seed, "pf/q", outl, dtype="bfloat16", torch_out=True)
+    signs = inputs.tbq_signs(D)
+    cache = ckv.PackedCache(D, Hkv, B, cap, signs)
+    kd, vd = torch.from_numpy(k).to(DEV), torch.from_numpy(v).to(DEV)
+    if n_cached:
+        ckv.kv_pack(cache, 0, kd[:, :n_cached].contiguous(), vd[:, :n_cached].contiguous())
+    out = torch.full((B, n_new, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    lse = torch.full((B, n_new, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.empty(ckv.attn_prefill_workspace(cache, n_new, Hq), dtype=torch.uint8, device=DEV)
+    ckv.attn_prefill(cache, n_cached, q.to(DEV), kd[:, n_cached:].contiguous(), vd[:, n_cached:].contiguous(),
+                     1.0 / math.sqrt(D), out, lse, ws)
+    torch.cuda.synchronize()
+    assert ckv.read_device_flag(ws) == 0
+    return k, v, q.float().numpy().astype(np.float64), signs, out.cpu().numpy(), lse.cpu().numpy()
+
+
+def _oracle(k, v, qf, signs, n_cached, b, rows=None):
+    D = k.shape[-1]
+    kt = np.ascontiguousarray(np.swapaxes(k[b], 0, 1))
+    vt = np.ascontiguousarray(np.swapaxes(v[b], 0, 1))
+    qs, d16, codes, n16, _ = H.oracle_quantize(kt, vt, signs)
+    kh = O.q8_0_dequantize(qs, d16)
+    vh = O.tbq3_dequantize(codes, n16, signs)
+    q = qf[b] if rows is None else qf[b][rows]
+    if rows is None:
+        return O.prefill_reference(q, kh, vh, n_cached, 1.0 / math.sqrt(D))
+    # Selected query tokens only: query index rows[i] sees [0, n_cached + rows[i]].
+    Hq, Hkv = q.shape[1], kh.shape[0]
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    for i, qi in enumerate(rows):
+        for h in range(Hq):
+            kv = O.kv_head_of(h, Hq, Hkv)
+            oo, ll = O.attention(q[i:i + 1, h], kh[kv, :n_cached + qi + 1], vh[kv, :n_cached + qi + 1],
+                                 1.0 / math.sqrt(D))
+            o[i, h], lse[i, h] = oo[0], ll[0]
+    return o, lse
+
+
+@pytest.mark.parametrize("D,Hkv,Hq,n_cached,n_new", [(128, 2, 16, 100, 37), (256, 1, 4, 64, 80),
+                                                     (512, 2, 16, 131, 45), (512, 1, 8, 0, 20)])
+def test_prefill_small(D, Hkv, Hq, n_cached, n_new):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B = 2
+    cap = ((n_cached + n_new + 15) // 16) * 16 + 16
+    k, v, qf, signs, out, lse = _case(D, Hkv, Hq, B, n_cached, n_new, cap, seed=40 + D + n_new)
+    for b in range(B):
+        o_ref, l_ref = _oracle(k, v, qf, signs, n_cached, b)
+        H.check_attention(out[b], lse[b], o_ref, l_ref, f"prefill D={D} b={b}")
+
+
+def test_chunked_prefill_workload_sampled():
+    """2048 new queries over 32768 cached tokens (Gemma-4 global-layer shapes):
+    query tokens sampled across every 128-row tile position and the last one."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = inputs.WORKLOADS["chunked_prefill"]
+    D, Hkv, Hq, nc, nn = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.n_new
+    k, v, qf, signs, out, lse = _case(D, Hkv, Hq, 1, nc, nn, nc + nn, seed=w.seed)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    rows = [0, 1, 15, 16, 17, 500, 1023, 1024, 1777, 2046, 2047]
+    o_ref, l_ref = _oracle(k, v, qf, signs, nc, 0, rows=rows)
+    H.check_attention(out[0][rows], lse[0][rows], o_ref, l_ref, "chunked prefill")
