@@ -63,7 +63,8 @@ struct PCfg {
   static constexpr int KV_OFF = M * D * 2;                 // K_hat hi, then lo, then C^T
   static constexpr int P_OFF = KV_OFF + NKV * D * 2;
   static constexpr int NORM_OFF = P_OFF + M * NKV * 2;
-  static constexpr int BYTES = NORM_OFF + NKV * 4;
+  static constexpr int LUT_OFF = NORM_OFF + NKV * 4;        // 64 centroid pairs x 32 lanes
+  static constexpr int BYTES = LUT_OFF + 64 * 32 * 4;
   // At least half the SM's shared memory, so that one CTA (and its 512 TMEM
   // columns) owns each SM.
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   uint8_t* sKV = smem + C::KV_OFF;
   uint8_t* sP = smem + C::P_OFF;
   float* sNorm = reinterpret_cast<float*>(smem + C::NORM_OFF);
+  uint32_t* sLut = reinterpret_cast<uint32_t*>(smem + C::LUT_OFF);
 
   const int group_q = a.n_q_heads / a.n_kv_heads;
   const int QT = C::M / group_q;                   // query tokens per CTA
@@ -129,6 +131,11 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       outv = make_uint4(o[0], o[1], o[2], o[3]);
     }
     *reinterpret_cast<uint4*>(sQ + sw128_offset(r, k0, C::M)) = outv;
+  }
+  // Centroid pairs: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
+  for (int e = tid; e < 64 * 32; e += C::THREADS) {
+    const int f = e >> 5;
+    sLut[e] = pack_half2(kPrefillCentroids[f & 7], kPrefillCentroids[f >> 3]);
   }
   tc_fence_before();
   __syncthreads();
@@ -180,36 +187,50 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   for (int step = 0; step < n_steps; ++step) {
     const int64_t j0 = (int64_t)step * C::NKV;
     // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
+    // q is an exact fp16 integer; hi = q*d rounded once (HMUL2 of exact fp16
+    // operands) and lo = fma(q, d, -hi), the exact residual (HFMA2).
     uint32_t lo_keep[C::PPT][4][4];
+    {
+      uint2 kw[C::PPT][4];
+      __half2 dd[C::PPT];
 #pragma unroll
-    for (int pc = 0; pc < C::PPT; ++pc) {
-      const int piece = tid + pc * C::THREADS;
-      const int p = piece / C::NB, blk = piece % C::NB;
-      const int64_t rec = (j0 + p) / kTile;
-      const int pp = p % kTile;
-      const bool in_tile = piece < C::PIECES;
-      const bool have = in_tile && rec < n_rec;
-      const uint8_t* rb = stream + rec * C::REC;
-      float d = 0.0f;
-      if (have) d = __half2float(*reinterpret_cast<const __half*>(rb + k_scale_offset(D) + 2 * (pp * C::NB + blk)));
+      for (int pc = 0; pc < C::PPT; ++pc) {  // issue every load of the step first
+        const int piece = tid + pc * C::THREADS;
+        const int p = piece / C::NB, blk = piece % C::NB;
+        const int64_t rec = (j0 + p) / kTile;
+        const int pp = p % kTile;
+        const bool have = piece < C::PIECES && rec < n_rec;
+        const uint8_t* rb = stream + rec * C::REC;
+        __half d = __ushort_as_half(0);
+        if (have) d = *reinterpret_cast<const __half*>(rb + k_scale_offset(D) + 2 * (pp * C::NB + blk));
+        dd[pc] = __halves2half2(d, d);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        uint2 w = make_uint2(0, 0);
-        if (have) w = *reinterpret_cast<const uint2*>(rb + (blk * 32 + 4 * (pp & 7) + t) * 16 + (pp >> 3) * 8);
-        uint32_t hi[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t word = e < 2 ? w.x : w.y;
-          const int sh = (e & 1) * 16;
-          const float k0v = (float)(int8_t)((word >> sh) & 0xFFu) * d;       // exact in fp32
-          const float k1v = (float)(int8_t)((word >> (sh + 8)) & 0xFFu) * d;
-          const __half h0 = __float2half_rn(k0v), h1 = __float2half_rn(k1v);
-          hi[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-          lo_keep[pc][t][e] = pack_half2(k0v - __half2float(h0), k1v - __half2float(h1));
+        for (int t = 0; t < 4; ++t) {
+          kw[pc][t] = make_uint2(0, 0);
+          if (have) kw[pc][t] = *reinterpret_cast<const uint2*>(rb + (blk * 32 + 4 * (pp & 7) + t) * 16 + (pp >> 3) * 8);
         }
-        if (in_tile)
-          *reinterpret_cast<uint4*>(sKV + sw128_offset(p, blk * 32 + 8 * t, C::NKV)) =
-              make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+#pragma unroll
+      for (int pc = 0; pc < C::PPT; ++pc) {
+        const int piece = tid + pc * C::THREADS;
+        const int p = piece / C::NB, blk = piece % C::NB;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          uint32_t qh[4], hi[4];
+          i8x4_to_half2x2(kw[pc][t].x, qh[0], qh[1]);
+          i8x4_to_half2x2(kw[pc][t].y, qh[2], qh[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 qv = *reinterpret_cast<const __half2*>(&qh[e]);
+            const __half2 h = __hmul2(qv, dd[pc]);
+            const __half2 l = __hfma2(qv, dd[pc], __hneg2(h));
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+            lo_keep[pc][t][e] = *reinterpret_cast<const uint32_t*>(&l);
+          }
+          if (piece < C::PIECES)
+            *reinterpret_cast<uint4*>(sKV + sw128_offset(p, blk * 32 + 8 * t, C::NKV)) =
+                make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
       }
     }
     // V norms of the step's tokens (positions past the cache read as 0).
@@ -303,35 +324,39 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     } else {
       // ---- C^T (centroids, rotated basis) for the step: rows = dims, K = tokens ----
       // One (record, lane stream) per thread: 4 records x 32 lanes = 128 threads.
+      // A 6-bit field pairs the codes of two adjacent positions of one dim,
+      // which is one fp16x2 word of C^T: one shared table load per field.
       const int u = tid - 128;
       const int r4 = u >> 5, L = u & 31;
       const int64_t rec = j0 / kTile + r4;
-      constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D);
-      uint32_t sw[LB / 4];
+      constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D), NW = LB / 4;
+      uint32_t sw[NW];
       if (rec < n_rec) {
         const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
 #pragma unroll
-        for (int s4 = 0; s4 < LB / 4; ++s4) {
+        for (int s4 = 0; s4 < NW; ++s4) {
           const int sbyte = s4 * 4;
           sw[s4] = *reinterpret_cast<const uint32_t*>(vb + ((sbyte / GR) * 32 + L) * GR + (sbyte % GR));
         }
       } else {
 #pragma unroll
-        for (int s4 = 0; s4 < LB / 4; ++s4) sw[s4] = 0u;
+        for (int s4 = 0; s4 < NW; ++s4) sw[s4] = 0u;
       }
       const int g = L >> 2, tq = L & 3;
-#pragma unroll 4
+      const uint32_t lut = smem_u32(sLut) + (uint32_t)(lane << 2);
+      const uint32_t kvb = smem_u32(sKV);
+      const int tok0 = r4 * 16 + 2 * tq;
+#pragma unroll
       for (int pi = 0; pi < 2 * G; ++pi) {
         const int bit = 6 * pi;
         const int wi = bit >> 5, sh = bit & 31;
         uint32_t f = sw[wi] >> sh;
-        if (sh > 26 && wi + 1 < LB / 4) f |= sw[wi + 1] << (32 - sh);
-        const int ce = f & 7, co = (f >> 3) & 7;
+        if (sh > 26 && wi + 1 < NW) f |= sw[wi + 1] << (32 - sh);
+        const uint32_t val = lds32(lut + ((f & 63u) << 7));
         const int mt = pi >> 2, rh = pi & 1, h2 = (pi >> 1) & 1;
         const int dim = G * g + 2 * mt + rh;
-        const int tok = r4 * 16 + 2 * tq + 8 * h2;  // even position; the odd one follows it in K
-        const uint32_t val = pack_half2(kPrefillCentroids[ce], kPrefillCentroids[co]);
-        *reinterpret_cast<uint32_t*>(sKV + sw128_offset(dim, tok, D)) = val;
+        const int tok = tok0 + 8 * h2;  // even position; the odd one follows it in K
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(kvb + sw128_offset(dim, tok, D)), "r"(val) : "memory");
       }
     }
     sync_for_mma();
