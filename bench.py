@@ -1,13 +1,23 @@
 #!/usr/bin/env python
-"""Benchmark: one decode step of the Gemma-4 global-layer workload over a packed
-q8_0-K / TBQ3-V cache on one GB300, printed as one JSON line.
+"""Benchmark of the compressed-KV attention hot path on one GB300: one JSON line.
 
-A step is the whole hot path for one new token: quantise and append the token's
-K and V rows into the cache (kv_pack), then attention of the 16 query heads over
-all 32768 cached tokens (attn_decode: split-K decode kernel + split merge with
-the inverse transform). Inputs are resident in HBM when the timed region starts.
-The packed cache (48.4 MB) is smaller than L2, so steps rotate over enough
-copies of it to exceed 4x the L2 size; every step reads its cache from HBM.
+Default workload (`gemma4_decode`): one decode step of a Gemma-4 global layer
+over a packed q8_0-K / TBQ3-V cache, one call of attn_decode_append: the decode
+kernel quantises the new token's K and V rows into the cache, then attends with
+the 16 query heads over all 32768 cached tokens (split-K decode, in-kernel split
+merge and inverse transform). Inputs are resident in HBM when the timed
+region starts. Caches smaller than L2 are rotated over enough copies to exceed
+4x the L2 size, so every step reads its cache from HBM.
+
+Other workloads (`--workload`), one line each:
+  long_decode      4 sequences x 262144 tokens, one decode step per sequence
+  fanout_decode    one 4096-token compressed prefix read by 15 agents (a
+                   120-row pass per kv head), a private 512-token fp16 tail per
+                   agent, the two partials merged by log-sum-exp
+  tiny_decode      1 kv head, 4 query heads, head_dim 128, 256 tokens
+  chunked_prefill  2048 new query tokens over 32768 cached ones (pack the new
+                   rows, causal attention on tcgen05); tensor roofline
+  kv_pack          packing 2048 tokens x 2 kv heads of fp16 K/V
 
 --impl reference times the float64 oracle (dequantise to dense, then softmax
 attention) on the host cores, on a bounded sample of the same workload.
@@ -30,12 +40,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "compressed-KV decode attn: tokens/s and effective HBM GB/s (% of GB300 peak)"
-WORKLOAD = "gemma4_decode"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM traffic of one attn_decode_kernel<512> launch on this workload, from the
-# ncu capture summarised in profiles/attn_decode_gemma4.md, valid for the source
-# hash below (null once the kernel source changes).
+# DRAM traffic of one decode-kernel launch on gemma4_decode from the ncu capture
+# summarised in profiles/attn_decode_gemma4.md, valid for the kernel sources
+# whose hash is recorded beside it (null once they change).
 NCU_TRAFFIC = {"bytes": None, "source_sha": None}
 
 
@@ -45,6 +55,9 @@ def _args():
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="gemma4_decode",
+                   choices=["gemma4_decode", "long_decode", "fanout_decode", "tiny_decode", "chunked_prefill",
+                            "kv_pack"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -54,9 +67,9 @@ def _peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def _decode_source_sha():
@@ -75,9 +88,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+        self.gpu, self.proc, self.path = gpu_index, None, None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -88,12 +99,8 @@ class ClockSampler:
                  "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        self.t0 = time.time()
 
-    def mark(self):
-        return time.time()
-
-    def stop(self, t_begin, t_end):
+    def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -109,8 +116,7 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.path)
-        # nvidia-smi lines carry no timestamps: keep the samples taken while the
-        # GPU was under load (clocks above idle), else all of them.
+
         def num(x):
             try:
                 return float(x)
@@ -124,18 +130,362 @@ class ClockSampler:
             for name, val in zip(names, r[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        # Lines carry no timestamps: keep the samples taken under load (clocks
+        # above half of the highest seen).
         loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(rows)}
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _timed(stream, fn, n):
+    """Run fn() n times on `stream`; elapsed ms from CUDA events recorded on that stream."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1)
+
+
+# -------------------------------------------------------------- workloads --
+
+class DecodeWork:
+    """Decode workloads: a step is attn_decode_append of one new token per sequence."""
+
+    graph = True
+
+    def __init__(self, name, dev, stream):
+        import torch
+        import compressed_kv_attention_gb300 as ckv
+        from compressed_kv_attention_gb300 import inputs
+        self.ckv, self.torch, self.stream = ckv, torch, stream
+        w = inputs.WORKLOADS[name]
+        self.w = w
+        D, Hkv, Hq, T, B = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.batch
+        self.D, self.T, self.B, self.Hq, self.Hkv = D, T, B, Hq, Hkv
+        outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
+        signs = inputs.tbq_signs(D)
+        self.scale = 1.0 / math.sqrt(D)
+        with torch.cuda.stream(stream):
+            k = inputs.normal_tensor((B, T, Hkv, D), w.seed, "k", outl, device=str(dev))
+            v = inputs.normal_tensor((B, T, Hkv, D), w.seed, "v", outl, device=str(dev))
+            self.q = inputs.normal_tensor((B, 1, Hq, D), w.seed, "q", outl, device=str(dev))
+            self.cache_bytes = ckv.cache_bytes(D, Hkv, B, T)
+            self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            self.n_rot = max(2, math.ceil(4 * self.l2 / self.cache_bytes))
+            self.caches = [ckv.PackedCache(D, Hkv, B, T, signs, device=dev) for _ in range(self.n_rot)]
+            for c in self.caches:
+                ckv.kv_pack(c, 0, k, v, stream=stream)
+            self.k_new, self.v_new = k[:, T - 1:T].clone(), v[:, T - 1:T].clone()
+            del k, v
+            self.out = torch.empty((B, 1, Hq, D), dtype=torch.float32, device=dev)
+            self.lse = torch.empty((B, 1, Hq), dtype=torch.float32, device=dev)
+            self.ws = torch.empty(ckv.attn_decode_workspace(self.caches[0], T, 1, Hq), dtype=torch.uint8,
+                                  device=dev)
+            self.seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+        stream.synchronize()
+        self.tokens_per_step = B
+        self.launches_per_step = 2  # workspace-header reset kernel, decode kernel (packs the new token)
+        self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D)
+
+    def step(self, i):
+        c = self.caches[i % self.n_rot]
+        self.ckv.attn_decode_append(c, self.seq, self.T, self.k_new, self.v_new, self.q, self.scale, self.out,
+                                    self.lse, self.ws, stream=self.stream)
+
+    kernel_call = step
+
+    def check(self):
+        assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [x.cpu().pin_memory() for x in (self.q, self.k_new, self.v_new)]
+        self.d_in = [t.empty_like(x) for x in (self.q, self.k_new, self.v_new)]
+        self.h_out = [t.empty(x.shape, dtype=x.dtype).pin_memory() for x in (self.out, self.lse)]
+        return (sum(x.numel() * x.element_size() for x in self.h_in),
+                sum(x.numel() * x.element_size() for x in self.h_out))
+
+    def e2e_step(self, i):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        c = self.caches[i % self.n_rot]
+        self.ckv.attn_decode_append(c, self.seq, self.T, self.d_in[1], self.d_in[2], self.d_in[0], self.scale,
+                                    self.out, self.lse, self.ws, stream=self.stream)
+        self.h_out[0].copy_(self.out, non_blocking=True)
+        self.h_out[1].copy_(self.lse, non_blocking=True)
+
+    def describe(self):
+        return {"workload": self.w.name, "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
+                "batch": self.B, "cached_tokens": self.T, "n_q": 1,
+                "step": "attn_decode_append (pack 1 new token per sequence in-kernel, then attend)",
+                "l2": f"rotating {self.n_rot} cache copies ({self.n_rot * self.cache_bytes / 1e6:.0f} MB > 4x L2 "
+                      f"{self.l2 / 1e6:.0f} MB)"}
+
+    def roofline(self, kernel_ms, peaks):
+        hbm, _, kind = peaks
+        achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
+        traffic = NCU_TRAFFIC["bytes"] if (self.w.name == "gemma4_decode" and
+                                           NCU_TRAFFIC["source_sha"] == _decode_source_sha()) else None
+        return {"bound": "hbm", "kernel": f"attn_decode_kernel<{self.D}> (append + split-K decode + in-kernel merge)",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_kind": kind, "traffic": traffic, "algorithmic_bytes": self.algo_bytes,
+                "launch_ms": round(kernel_ms, 6)}
+
+
+class FanoutWork:
+    """Shared-prefix fan-out: prefix decode (15 agents as 15 query tokens) + fp16 tails + LSE merge."""
+
+    graph = True
+
+    def __init__(self, dev, stream):
+        import torch
+        import compressed_kv_attention_gb300 as ckv
+        from compressed_kv_attention_gb300 import inputs
+        self.ckv, self.torch, self.stream = ckv, torch, stream
+        w = inputs.WORKLOADS["fanout_decode"]
+        self.w = w
+        D, Hkv, Hq, P, A, TL = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.n_agents, w.tail_len
+        self.D, self.Hkv, self.Hq, self.P, self.A, self.TL = D, Hkv, Hq, P, A, TL
+        outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
+        signs = inputs.tbq_signs(D)
+        self.scale = 1.0 / math.sqrt(D)
+        with torch.cuda.stream(stream):
+            k = inputs.normal_tensor((1, P, Hkv, D), w.seed, "prefix/k", outl, device=str(dev))
+            v = inputs.normal_tensor((1, P, Hkv, D), w.seed, "prefix/v", outl, device=str(dev))
+            self.qa = inputs.normal_tensor((A, Hq, D), w.seed, "agents/q", outl, device=str(dev))
+            self.per_copy = ckv.cache_bytes(D, Hkv, 1, P) + 2 * A * Hkv * TL * D * 2
+            self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            self.n_rot = max(2, math.ceil(4 * self.l2 / self.per_copy))
+            self.caches, self.tails = [], []
+            for _ in range(self.n_rot):
+                c = ckv.PackedCache(D, Hkv, 1, P, signs, device=dev)
+                ckv.kv_pack(c, 0, k, v, stream=stream)
+                self.caches.append(c)
+                kt = inputs.normal_tensor((A, Hkv, TL, D), w.seed, "tail/k", outl, device=str(dev))
+                vt = inputs.normal_tensor((A, Hkv, TL, D), w.seed, "tail/v", outl, device=str(dev))
+                self.tails.append((kt, vt))
+            self.o_pre = torch.empty((1, A, Hq, D), dtype=torch.float32, device=dev)
+            self.l_pre = torch.empty((1, A, Hq), dtype=torch.float32, device=dev)
+            self.o_t = torch.empty((A, 1, Hq, D), dtype=torch.float32, device=dev)
+            self.l_t = torch.empty((A, 1, Hq), dtype=torch.float32, device=dev)
+            self.out = torch.empty((A * Hq, D), dtype=torch.float32, device=dev)
+            self.lse = torch.empty(A * Hq, dtype=torch.float32, device=dev)
+            self.ws = torch.empty(ckv.attn_decode_workspace(self.caches[0], P, A, Hq), dtype=torch.uint8,
+                                  device=dev)
+            self.ws_t = torch.empty(ckv.attn_decode_f16_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8,
+                                    device=dev)
+            self.seq_p = torch.full((1,), P, dtype=torch.int32, device=dev)
+            self.seq_t = torch.full((A,), TL, dtype=torch.int32, device=dev)
+        stream.synchronize()
+        self.tokens_per_step = A
+        self.launches_per_step = 5  # 2 workspace-header resets, prefix decode, tail decode, merge
+        self.algo_bytes = Hkv * P * inputs.compressed_bytes_per_token(D) + 2 * A * Hkv * TL * D * 2
+
+    def _run(self, i, qa):
+        ckv, s = self.ckv, self.stream
+        c, (kt, vt) = self.caches[i % self.n_rot], self.tails[i % self.n_rot]
+        # The agents' queries as 15 query tokens of one sequence over the prefix,
+        # and as 15 sequences of one query token over their own tails.
+        ckv.attn_decode(c, self.seq_p, self.P, qa[None], self.scale, self.o_pre, self.l_pre, self.ws, stream=s)
+        ckv.attn_decode_f16(kt, vt, self.seq_t, self.TL, qa[:, None], self.scale, self.o_t, self.l_t, self.ws_t,
+                            stream=s)
+        ckv.lse_merge([self.o_pre.view(-1, self.D), self.o_t.view(-1, self.D)],
+                      [self.l_pre.view(-1), self.l_t.view(-1)], self.out, self.lse, stream=s)
+
+    def step(self, i):
+        self._run(i, self.qa)
+
+    kernel_call = step
+
+    def check(self):
+        assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
+        assert self.ckv.read_device_flag(self.ws_t, stream=self.stream) == 0
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_q = self.qa.cpu().pin_memory()
+        self.d_q = t.empty_like(self.qa)
+        self.h_out = [t.empty(x.shape, dtype=x.dtype).pin_memory() for x in (self.out, self.lse)]
+        return self.h_q.numel() * 2, sum(x.numel() * 4 for x in self.h_out)
+
+    def e2e_step(self, i):
+        self.d_q.copy_(self.h_q, non_blocking=True)
+        self._run(i, self.d_q)
+        self.h_out[0].copy_(self.out, non_blocking=True)
+        self.h_out[1].copy_(self.lse, non_blocking=True)
+
+    def describe(self):
+        return {"workload": "fanout_decode", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
+                "agents": self.A, "prefix_tokens": self.P, "tail_tokens": self.TL,
+                "step": "attn_decode(prefix, 15 agents) + attn_decode_f16(tails) + lse_merge",
+                "l2": f"rotating {self.n_rot} copies ({self.n_rot * self.per_copy / 1e6:.0f} MB > 4x L2)"}
+
+    def roofline(self, kernel_ms, peaks):
+        hbm, _, kind = peaks
+        achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "prefix decode + fp16 tail decode + lse merge (whole step)",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_kind": kind, "traffic": None, "algorithmic_bytes": self.algo_bytes,
+                "launch_ms": round(kernel_ms, 6)}
+
+
+class PrefillWork:
+    """Chunked prefill: attn_prefill packs 2048 new rows and attends causally (tcgen05)."""
+
+    graph = False  # long steps: launched eagerly, L2 flushed before each timed step
+
+    def __init__(self, dev, stream):
+        import torch
+        import compressed_kv_attention_gb300 as ckv
+        from compressed_kv_attention_gb300 import inputs
+        self.ckv, self.torch, self.stream = ckv, torch, stream
+        w = inputs.WORKLOADS["chunked_prefill"]
+        self.w = w
+        D, Hkv, Hq, nc, nn = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.n_new
+        self.D, self.Hkv, self.Hq, self.nc, self.nn = D, Hkv, Hq, nc, nn
+        outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
+        self.scale = 1.0 / math.sqrt(D)
+        with torch.cuda.stream(stream):
+            k = inputs.normal_tensor((1, nc + nn, Hkv, D), w.seed, "k", outl, device=str(dev))
+            v = inputs.normal_tensor((1, nc + nn, Hkv, D), w.seed, "v", outl, device=str(dev))
+            self.q = inputs.normal_tensor((1, nn, Hq, D), w.seed, "q", outl, device=str(dev), dtype="bfloat16")
+            self.cache = ckv.PackedCache(D, Hkv, 1, nc + nn, inputs.tbq_signs(D), device=dev)
+            ckv.kv_pack(self.cache, 0, k[:, :nc].contiguous(), v[:, :nc].contiguous(), stream=stream)
+            self.kn, self.vn = k[:, nc:].contiguous(), v[:, nc:].contiguous()
+            del k, v
+            self.out = torch.empty((1, nn, Hq, D), dtype=torch.float32, device=dev)
+            self.lse = torch.empty((1, nn, Hq), dtype=torch.float32, device=dev)
+            self.ws = torch.empty(ckv.attn_prefill_workspace(self.cache, nn, Hq), dtype=torch.uint8, device=dev)
+            self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            self.flush = torch.empty(2 * self.l2, dtype=torch.uint8, device=dev)
+        stream.synchronize()
+        self.tokens_per_step = nn
+        self.launches_per_step = 4  # header reset, pack, prefill, de-rotation
+        # QK^T and PV over the causal key range: query i sees nc + i + 1 keys.
+        self.flops = 2 * 2 * Hq * D * (nn * nc + nn * (nn + 1) // 2)
+
+    def step(self, i):
+        self.ckv.attn_prefill(self.cache, self.nc, self.q, self.kn, self.vn, self.scale, self.out, self.lse,
+                              self.ws, stream=self.stream)
+
+    kernel_call = step
+
+    def between(self):
+        with self.torch.cuda.stream(self.stream):
+            self.flush.fill_(1)
+
+    def check(self):
+        assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [x.cpu().pin_memory() for x in (self.q, self.kn, self.vn)]
+        self.d_in = [t.empty_like(x) for x in (self.q, self.kn, self.vn)]
+        self.h_out = [t.empty(x.shape, dtype=x.dtype).pin_memory() for x in (self.out, self.lse)]
+        return (sum(x.numel() * x.element_size() for x in self.h_in),
+                sum(x.numel() * x.element_size() for x in self.h_out))
+
+    def e2e_step(self, i):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        self.ckv.attn_prefill(self.cache, self.nc, self.d_in[0], self.d_in[1], self.d_in[2], self.scale,
+                              self.out, self.lse, self.ws, stream=self.stream)
+        self.h_out[0].copy_(self.out, non_blocking=True)
+        self.h_out[1].copy_(self.lse, non_blocking=True)
+
+    def describe(self):
+        return {"workload": "chunked_prefill", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
+                "cached_tokens": self.nc, "new_tokens": self.nn, "q_dtype": "bf16",
+                "step": "attn_prefill (pack 2048 rows + causal attention + de-rotation)",
+                "l2": f"flushed before each step ({2 * self.l2 / 1e6:.0f} MB write)"}
+
+    def roofline(self, kernel_ms, peaks):
+        _, tf, kind = peaks
+        achieved = self.flops / (kernel_ms / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": "attn_prefill_kernel<512> (+ pack, de-rotation) on tcgen05",
+                "achieved": round(achieved, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(achieved / tf, 4),
+                "peak_kind": kind + " bf16 dense (fp16 operands run at the same rate)", "traffic": None,
+                "algorithmic_flops": self.flops, "launch_ms": round(kernel_ms, 6)}
+
+
+class PackWork:
+    """kv_pack of 2048 tokens x 2 kv heads (the size of one prefill chunk)."""
+
+    graph = True
+
+    def __init__(self, dev, stream):
+        import torch
+        import compressed_kv_attention_gb300 as ckv
+        from compressed_kv_attention_gb300 import inputs
+        self.ckv, self.torch, self.stream = ckv, torch, stream
+        w = inputs.WORKLOADS["chunked_prefill"]
+        D, Hkv, n = w.head_dim, w.n_kv_heads, w.n_new
+        self.D, self.Hkv, self.n = D, Hkv, n
+        outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
+        with torch.cuda.stream(stream):
+            self.k = inputs.normal_tensor((1, n, Hkv, D), w.seed, "k", outl, device=str(dev))
+            self.v = inputs.normal_tensor((1, n, Hkv, D), w.seed, "v", outl, device=str(dev))
+            self.per = ckv.cache_bytes(D, Hkv, 1, n) + 2 * self.k.numel() * 2
+            self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            self.n_rot = max(2, math.ceil(4 * self.l2 / self.per))
+            self.caches = [ckv.PackedCache(D, Hkv, 1, n, inputs.tbq_signs(D), device=dev) for _ in range(self.n_rot)]
+            self.ins = [(self.k.clone(), self.v.clone()) for _ in range(self.n_rot)]
+        stream.synchronize()
+        self.tokens_per_step = n
+        self.launches_per_step = 1
+        self.algo_bytes = 2 * n * Hkv * D * 2 + n * Hkv * inputs.compressed_bytes_per_token(D)
+
+    def step(self, i):
+        k, v = self.ins[i % self.n_rot]
+        self.ckv.kv_pack(self.caches[i % self.n_rot], 0, k, v, stream=self.stream)
+
+    kernel_call = step
+
+    def check(self):
+        pass
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [x.cpu().pin_memory() for x in (self.k, self.v)]
+        self.d_in = [t.empty_like(x) for x in (self.k, self.v)]
+        return sum(x.numel() * 2 for x in self.h_in), 0
+
+    def e2e_step(self, i):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        self.ckv.kv_pack(self.caches[i % self.n_rot], 0, self.d_in[0], self.d_in[1], stream=self.stream)
+
+    def describe(self):
+        return {"workload": "kv_pack", "head_dim": self.D, "n_kv_heads": self.Hkv, "tokens": self.n,
+                "step": "kv_pack of 2048 tokens (q8_0 K + TBQ3 V)",
+                "l2": f"rotating {self.n_rot} input/cache copies ({self.n_rot * self.per / 1e6:.0f} MB > 4x L2)"}
+
+    def roofline(self, kernel_ms, peaks):
+        hbm, _, kind = peaks
+        achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": f"kv_pack_kernel<{self.D}>", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": kind,
+                "traffic": None, "algorithmic_bytes": self.algo_bytes, "launch_ms": round(kernel_ms, 6)}
+
+
+def _make_work(name, dev, stream):
+    if name in ("gemma4_decode", "long_decode", "tiny_decode"):
+        return DecodeWork(name, dev, stream)
+    if name == "fanout_decode":
+        return FanoutWork(dev, stream)
+    if name == "chunked_prefill":
+        return PrefillWork(dev, stream)
+    return PackWork(dev, stream)
 
 
 # --------------------------------------------------------------------- ours --
 
 def run_ours(args):
     import torch
-    import compressed_kv_attention_gb300 as ckv
-    from compressed_kv_attention_gb300 import inputs
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -147,64 +497,43 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(dev)
+    work = _make_work(args.workload, dev, stream)
+    n_rot = getattr(work, "n_rot", 1)
 
-    w = inputs.WORKLOADS[WORKLOAD]
-    D, Hkv, Hq, T = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len
-    outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
-    signs = inputs.tbq_signs(D)
-    scale = 1.0 / math.sqrt(D)
+    # Eager warm-up (configures kernel attributes before any capture).
     with torch.cuda.stream(stream):
-        k = inputs.normal_tensor((1, T, Hkv, D), w.seed, "k", outl, device=str(dev))
-        v = inputs.normal_tensor((1, T, Hkv, D), w.seed, "v", outl, device=str(dev))
-        q = inputs.normal_tensor((1, 1, Hq, D), w.seed, "q", outl, device=str(dev))
-        cache_b = ckv.cache_bytes(D, Hkv, 1, T)
-        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        n_rot = max(2, math.ceil(4 * l2 / cache_b))
-        caches = [ckv.PackedCache(D, Hkv, 1, T, signs, device=dev) for _ in range(n_rot)]
-        for c in caches:
-            ckv.kv_pack(c, 0, k, v, stream=stream)
-        k_new, v_new = k[:, T - 1:T].clone(), v[:, T - 1:T].clone()
-        out = torch.empty((1, 1, Hq, D), dtype=torch.float32, device=dev)
-        lse = torch.empty((1, 1, Hq), dtype=torch.float32, device=dev)
-        ws = torch.empty(ckv.attn_decode_workspace(caches[0], T, 1, Hq), dtype=torch.uint8, device=dev)
-        seq = torch.full((1,), T, dtype=torch.int32, device=dev)
+        for i in range(max(n_rot, 2)):
+            work.step(i)
     stream.synchronize()
+    work.check()
 
-    def step(c):
-        ckv.kv_pack(c, T - 1, k_new, v_new, stream=stream)
-        ckv.attn_decode(c, seq, T, q, scale, out, lse, ws, stream=stream)
+    if work.graph:
+        reps = max(1, 128 // n_rot)
+        per_big = reps * n_rot
+        big, single, kgraph = torch.cuda.CUDAGraph(), [], torch.cuda.CUDAGraph()
+        with torch.cuda.graph(big, stream=stream):
+            for i in range(per_big):
+                work.step(i)
+        for i in range(n_rot):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                work.step(i)
+            single.append(g)
+        with torch.cuda.graph(kgraph, stream=stream):
+            for i in range(per_big):
+                work.kernel_call(i)
 
-    def decode_only(c):
-        ckv.attn_decode(c, seq, T, q, scale, out, lse, ws, stream=stream)
-
-    # Eager warm-up (configures kernel attributes before capture), then graphs.
-    for c in caches:
-        step(c)
-    stream.synchronize()
-    assert ckv.read_device_flag(ws, stream=stream) == 0
-    reps = max(1, 128 // n_rot)
-    big, single, dec_graph = torch.cuda.CUDAGraph(), [], torch.cuda.CUDAGraph()
-    with torch.cuda.graph(big, stream=stream):
-        for _ in range(reps):
-            for c in caches:
-                step(c)
-    for c in caches:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(c)
-        single.append(g)
-    with torch.cuda.graph(dec_graph, stream=stream):
-        for _ in range(reps):
-            for c in caches:
-                decode_only(c)
-    per_big = reps * n_rot
-
-    def run_steps(n):
-        with torch.cuda.stream(stream):
-            for _ in range(n // per_big):
-                big.replay()
-            for i in range(n % per_big):
-                single[i % n_rot].replay()
+        def run_steps(n):
+            with torch.cuda.stream(stream):
+                for _ in range(n // per_big):
+                    big.replay()
+                for i in range(n % per_big):
+                    single[i % n_rot].replay()
+    else:
+        def run_steps(n):
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    work.step(i)
 
     run_steps(max(args.warmup, 3))
     stream.synchronize()
@@ -215,92 +544,66 @@ def run_ours(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_begin = time.time()
-    ev0.record(stream)
-    run_steps(args.steps)
-    ev1.record(stream)
+    if work.graph:
+        ms = _timed(stream, lambda: run_steps(args.steps), 1)
+    else:
+        ms = 0.0
+        for i in range(args.steps):
+            work.between()
+            ms += _timed(stream, lambda: work.step(i), 1)
     torch.cuda.synchronize(dev)
-    t_end = time.time()
-    ms = ev0.elapsed_time(ev1)
     if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
         dist.barrier()
 
-    # Dominant kernel alone: decode calls back to back (header reset + decode kernel).
-    n_dec = max(1, (2000 // per_big)) * per_big
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    # The dominant kernel call alone, back to back.
+    if work.graph:
+        n_k = max(1, 2000 // per_big) * per_big
+        k_ms = _timed(stream, kgraph.replay, n_k // per_big) / n_k
+    else:
+        k_ms = ms / args.steps
+    clocks = sampler.stop()
+    work.check()
+
+    # End to end through the public API with pinned host buffers, eager calls.
+    h2d, d2h = work.e2e_setup()
+    n_e2e = min(args.steps, 2000 if work.graph else 20)
     with torch.cuda.stream(stream):
-        for _ in range(n_dec // per_big):
-            dec_graph.replay()
-    e1.record(stream)
-    stream.synchronize()
-    dec_ms = e0.elapsed_time(e1) / n_dec
-    clocks = sampler.stop(t_begin, t_end)
-    assert ckv.read_device_flag(ws, stream=stream) == 0
-
-    # End to end through the public API with host buffers (pinned), eager calls.
-    q_h = q.cpu().pin_memory()
-    kn_h, vn_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, kn_d, vn_d = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    n_e2e = min(args.steps, 2000)
-
-    def e2e_step(i):
-        c = caches[i % n_rot]
-        q_d.copy_(q_h, non_blocking=True)
-        kn_d.copy_(kn_h, non_blocking=True)
-        vn_d.copy_(vn_h, non_blocking=True)
-        ckv.kv_pack(c, T - 1, kn_d, vn_d, stream=stream)
-        ckv.attn_decode(c, seq, T, q_d, scale, out, lse, ws, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for i in range(min(50, n_e2e)):
-            e2e_step(i)
+        for i in range(min(3, n_e2e)):
+            work.e2e_step(i)
         stream.synchronize()
         t0 = time.perf_counter()
         for i in range(n_e2e):
-            e2e_step(i)
+            work.e2e_step(i)
         stream.synchronize()
         e2e_s = time.perf_counter() - t0
-    h2d = (q.numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2)
-    d2h = out.numel() * 4 + lse.numel() * 4
 
-    tokens_per_step = 1  # one new token per sequence per step (batch 1)
-    value = world * tokens_per_step * args.steps / (ms / 1e3)
-    kv_bytes = Hkv * T * inputs.compressed_bytes_per_token(D)
-    peak, peak_kind = _peaks()
-    achieved = kv_bytes / (dec_ms / 1e3) / 1e9
-    traffic = NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["source_sha"] == _decode_source_sha() else None
+    peaks = _peaks()
+    value = world * work.tokens_per_step * args.steps / (ms / 1e3)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 mma, f32 accumulate (int8 / 3-bit storage)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "head_dim": D, "n_kv_heads": Hkv, "n_q_heads": Hq, "batch": 1,
-                   "cached_tokens": T, "n_q": 1, "step": "kv_pack(1 token) + attn_decode",
-                   "l2": f"rotating {n_rot} cache copies ({n_rot * cache_b / 1e6:.0f} MB > 4x L2 "
-                         f"{l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}",
-                   "timing": "CUDA graphs, events on the launching stream"},
-        "effective_gbs": round(kv_bytes * world * args.steps / (ms / 1e3) / 1e9, 1),
-        "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel<512> (split-K decode with in-kernel split merge)",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes": kv_bytes,
-                     "launch_ms": round(dec_ms, 6)},
-        "e2e": {"value": round(n_e2e / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": n_e2e, "api": "kv_pack + attn_decode, eager"},
-        "gpu_launches": 2 * args.steps,
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma, f32 accumulate (int8 / 3-bit storage)",
+        "data": "synthetic",
+        "config": dict(work.describe(), parallelism=f"replicas x{world}",
+                       timing="CUDA graphs, events on the launching stream" if work.graph else
+                       "events around each step on the launching stream"),
+        "roofline": work.roofline(k_ms, peaks),
+        "e2e": {"value": round(world * work.tokens_per_step * n_e2e / e2e_s, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                "api": "public Python API, eager"},
+        "gpu_launches": work.launches_per_step * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(min_seconds=10.0)
+    if hasattr(work, "algo_bytes"):
+        line["effective_gbs"] = round(work.algo_bytes * world * args.steps / (ms / 1e3) / 1e9, 1)
+    if hasattr(work, "flops"):
+        line["effective_tflops"] = round(work.flops * world * args.steps / (ms / 1e3) / 1e12, 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("gemma4_decode",
+                                                                                   "chunked_prefill"):
+        line["cpu_baseline"] = cpu_baseline(args.workload, min_seconds=10.0)
     if dist:
         dist.destroy_process_group()
     if rank == 0:
@@ -309,13 +612,14 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ oracle --
 
-def _oracle_setup(sample_tokens=None):
+def _oracle_setup(sample_tokens=None, workload="gemma4_decode"):
     import numpy as np
     from compressed_kv_attention_gb300 import inputs
     from tests import helpers as H
-    w = inputs.WORKLOADS[WORKLOAD]
-    D, Hkv, Hq, T = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len
-    Ts = T if sample_tokens is None else sample_tokens
+    w = inputs.WORKLOADS[workload]
+    D, Hkv, Hq = w.head_dim, w.n_kv_heads, w.n_q_heads
+    T = w.seq_len + w.n_new
+    Ts = T if sample_tokens is None else min(T, sample_tokens)
     outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
     k = inputs.normal_tensor((Ts, Hkv, D), w.seed, "bench-oracle/k", outl)
     v = inputs.normal_tensor((Ts, Hkv, D), w.seed, "bench-oracle/v", outl)
@@ -327,8 +631,9 @@ def _oracle_setup(sample_tokens=None):
 
 
 def _oracle_step(s):
-    """Oracle decode step: quantise the new token, dequantise the cache to dense
-    float64, softmax attention for every query head (decompress-then-attend)."""
+    """Oracle work for one query token: quantise the new token, dequantise the
+    cache to dense float64, softmax attention for every query head
+    (decompress-then-attend)."""
     from oracle import ckv_oracle as O
     O.q8_0_quantize(s["k_new"])
     O.tbq3_quantize(s["v_new"], s["signs"])
@@ -344,8 +649,11 @@ def _cores():
         return os.cpu_count()
 
 
-def cpu_baseline(min_seconds=10.0, max_seconds=30.0):
-    s = _oracle_setup()
+def cpu_baseline(workload="gemma4_decode", min_seconds=10.0, max_seconds=30.0):
+    """The oracle timed on the host cores. Decode: whole decode steps. Prefill:
+    one query token's work over the full key range (the last query's), in
+    query tokens per second."""
+    s = _oracle_setup(workload=workload)
     n, t0 = 0, time.perf_counter()
     while True:
         _oracle_step(s)
@@ -353,25 +661,31 @@ def cpu_baseline(min_seconds=10.0, max_seconds=30.0):
         el = time.perf_counter() - t0
         if el >= min_seconds or el * (n + 1) / n > max_seconds:
             break
-    return {"value": round(n / el, 4), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-            "sample": f"{n} full decode steps of {WORKLOAD} (dequantise {s['T']} tokens x {s['Hkv']} kv "
-                      f"heads to float64, attend 16 heads), numpy float64"}
+    rate = n / el
+    if workload == "chunked_prefill":
+        sample = (f"{n} query tokens of chunked_prefill, each attending over {s['Ts']} dequantised tokens "
+                  "(the last query's key range), numpy float64")
+    else:
+        sample = (f"{n} full decode steps of {workload} (dequantise {s['T']} tokens x {s['Hkv']} kv heads to "
+                  "float64, attend 16 heads), numpy float64")
+    return {"value": round(rate, 4), "unit": "tokens/s", "cores": _cores(), "kind": "oracle", "sample": sample}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    workload = args.workload if args.workload in ("gemma4_decode", "chunked_prefill") else "gemma4_decode"
     # Size each step's sample so that warm-up + timed steps take about 2 minutes:
     # a step attends over the first Ts tokens of the cache and its time is
     # scaled by T / Ts to a full step.
-    cal = _oracle_setup(sample_tokens=1024)
+    cal = _oracle_setup(sample_tokens=1024, workload=workload)
     t0 = time.perf_counter()
     _oracle_step(cal)
     full_est = (time.perf_counter() - t0) * cal["T"] / cal["Ts"]
     per_step = 120.0 / max(1, args.steps + args.warmup)
     Ts = int(min(cal["T"], max(16, (cal["T"] * per_step / full_est) // 16 * 16)))
-    s = _oracle_setup(sample_tokens=Ts)
+    s = _oracle_setup(sample_tokens=Ts, workload=workload)
     frac = s["Ts"] / s["T"]
     for _ in range(max(args.warmup, 0)):
         _oracle_step(s)
@@ -380,13 +694,13 @@ def run_reference(args):
         _oracle_step(s)
     el = (time.perf_counter() - t0) / frac
     value = args.steps / el
-    sample = (f"each step: oracle decode (dequantise to float64 + attend 16 heads) over {s['Ts']} of "
-              f"{s['T']} tokens of {WORKLOAD}, time scaled by {1 / frac:.2f}")
+    sample = (f"each step: oracle work for one query token (dequantise to float64 + attend 16 heads) over "
+              f"{s['Ts']} of {s['T']} tokens of {workload}, time scaled by {1 / frac:.2f}")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / max(args.steps, 1) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "data": "synthetic", "config": {"workload": workload, "sample": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

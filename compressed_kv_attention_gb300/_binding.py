@@ -45,6 +45,8 @@ SIGNATURES = {
     "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
                                  _vp, _c_size, _vp]),
+    "ckv_attn_decode_append": (_c_int, [_cache_p, _vp, _c_i64, _vp, _vp, _c_int, _c_i64, _c_i64, _vp, _c_int,
+                                        _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_attn_decode_noalloc": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp,
                                          _vp, _vp]),
     "ckv_attn_decode_f16_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
@@ -138,6 +140,18 @@ def attn_decode(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, 
     _check(load().ckv_attn_decode(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
                                   n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                   _stream(stream)))
+
+
+def attn_decode_append(cache: PackedCache, seq_len, max_seq_len: int, k_new, v_new, q, scale: float, out, lse,
+                       workspace, n_split: int = 0, stream=None):
+    """One decode step: pack k_new / v_new (fp16 [batch, n_new, n_kv_heads, D]) at positions
+    [seq_len - n_new, seq_len) of every sequence, then attn_decode over [0, seq_len)."""
+    _, n_q, n_q_heads, _ = q.shape
+    n_new = k_new.shape[1]
+    _check(load().ckv_attn_decode_append(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(k_new), _ptr(v_new), n_new,
+                                         k_new.stride(1), k_new.stride(0), _ptr(q), n_q, n_q_heads, scale, n_split,
+                                         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                         _stream(stream)))
 
 
 def attn_decode_noalloc(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse,

@@ -25,13 +25,20 @@
 //    runs one inverse Walsh-Hadamard transform and the sign flip per row.
 #include "ckv_kernels.cuh"
 #include "decode_common.cuh"
+#include "pack_common.cuh"
 
 namespace ckv {
 
 namespace {
 
-__constant__ float kCentroids[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
-                                 0.2451f,  0.7560f,  1.3439f,  2.1520f};
+// Lloyd-Max centroid of code k (0..7): -2.1520, -1.3439, -0.7560, -0.2451,
+// +0.2451, +0.7560, +1.3439, +2.1520. Selects on immediates, so the table fill
+// at kernel start reads no memory.
+__device__ __forceinline__ float centroid(int k) {
+  const int m = (k >= 4) ? k - 4 : 3 - k;
+  const float mag = (m == 0) ? 0.2451f : (m == 1) ? 0.7560f : (m == 2) ? 1.3439f : 2.1520f;
+  return (k >= 4) ? mag : -mag;
+}
 
 template <int D>
 struct CDec : DecodeShape<D> {
@@ -43,12 +50,13 @@ struct CDec : DecodeShape<D> {
   static constexpr int VW = 3 * Sh::MT_W / 4;   // V-code words per lane per warp
   static constexpr int GR = v_granule(D);       // stream granule bytes
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
-  static constexpr int MERGE_BYTES = (2 * kMaxInKernelSplits * 8 + 16 + 256) * 4;
+  static constexpr int MERGE_BYTES = merge_scratch_floats(kMaxInKernelSplits, 256) * 4;
   static constexpr int RING0 = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
   static constexpr int RING = (RING0 > MERGE_BYTES) ? RING0 : MERGE_BYTES;
   static constexpr int OFF_XCHG = (RING + 127) / 128 * 128;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
-  static constexpr int OFF_BAR = OFF_ML + Sh::NP * 16 * 4;
+  static constexpr int OFF_QB = OFF_ML + Sh::NP * 16 * 4;          // [NCW][NB_W][4][2] query-block biases
+  static constexpr int OFF_BAR = OFF_QB + Sh::NCW * Sh::NB_W * 4 * 2 * 4;
   static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 16;
 };
 
@@ -85,9 +93,13 @@ __device__ __forceinline__ uint32_t field_x128(const uint32_t* w, int bit) {
 
 // S^T = K_hat Q^T for one tile record at shared address `rb`: this warp's
 // blocks, one accumulator per 32-dim block scaled by the block's fp16 scale.
+// The codes enter the tensor core as fp16 subnormals (q + 128) * 2^-24, the
+// accumulator starts at qbias = -2^-17 * (block sum of the query row), so each
+// block product is 2^-24 q.Q exactly up to fp32 accumulation; the 2^24 goes
+// into the softmax scale.
 template <int D>
 __device__ __forceinline__ void qk_tile(uint32_t rb, int wh, int lane, const uint32_t (&qf)[CDec<D>::NB_W][4],
-                                        float (&S)[4]) {
+                                        uint32_t qb, float (&S)[4]) {
   using C = CDec<D>;
   const int g = lane >> 2;
   uint32_t sc0[C::NB_W / 2], sc1[C::NB_W / 2];
@@ -99,12 +111,13 @@ __device__ __forceinline__ void qk_tile(uint32_t rb, int wh, int lane, const uin
     const int blk = wh * C::NB_W + i;
     const uint4 kk = lds128(rb + (blk * 32 + lane) * 16);
     uint32_t a0s0, a2s0, a0s1, a2s1, a1s0, a3s0, a1s1, a3s1;
-    i8x4_to_half2x2(kk.x, a0s0, a2s0);
-    i8x4_to_half2x2(kk.y, a0s1, a2s1);
-    i8x4_to_half2x2(kk.z, a1s0, a3s0);
-    i8x4_to_half2x2(kk.w, a1s1, a3s1);
-    float c[4];
-    mma16816_zc(c, a0s0, a1s0, a2s0, a3s0, qf[i][0], qf[i][1]);
+    i8x4_to_sub_half2x2(kk.x, a0s0, a2s0);
+    i8x4_to_sub_half2x2(kk.y, a0s1, a2s1);
+    i8x4_to_sub_half2x2(kk.z, a1s0, a3s0);
+    i8x4_to_sub_half2x2(kk.w, a1s1, a3s1);
+    const uint2 bq = lds64(qb + i * 32);
+    float c[4] = {__uint_as_float(bq.x), __uint_as_float(bq.y), __uint_as_float(bq.x), __uint_as_float(bq.y)};
+    mma16816(c, a0s0, a1s0, a2s0, a3s0, qf[i][0], qf[i][1]);
     mma16816(c, a0s1, a1s1, a2s1, a3s1, qf[i][2], qf[i][3]);
     const __half2 d0h = *reinterpret_cast<const __half2*>(&sc0[i >> 1]);
     const __half2 d1h = *reinterpret_cast<const __half2*>(&sc1[i >> 1]);
@@ -117,10 +130,39 @@ __device__ __forceinline__ void qk_tile(uint32_t rb, int wh, int lane, const uin
   }
 }
 
-// O^T += C^T P'^T for one tile record, straight from the 3-bit codes.
+// Bias of the subnormal code encoding for rows 2t, 2t+1 of each of the warp's
+// blocks: -2^-17 times the sum of the block's query values. Each lane sums its
+// B fragments, the four lanes of a row reduce, and lanes 0..3 (t = lane) store
+// the pair for rows 2t, 2t+1 at qb[i][t] (shared, [NBW][4] float2).
+template <int NBW>
+__device__ __forceinline__ void q_block_bias(const uint32_t (&qf)[NBW][4], int lane, float* qb) {
+  const int t = lane & 3;
+#pragma unroll
+  for (int i = 0; i < NBW; ++i) {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qf[i][j]));
+      s += f.x + f.y;
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    const float r0 = __shfl_sync(0xffffffffu, s, 8 * t);
+    const float r1 = __shfl_sync(0xffffffffu, s, 8 * t + 4);
+    if (lane < 4) {
+      qb[(i * 4 + t) * 2] = -r0 * 7.62939453125e-06f;  // 2^-17
+      qb[(i * 4 + t) * 2 + 1] = -r1 * 7.62939453125e-06f;
+    }
+  }
+  __syncwarp();
+}
+
+// O^T += C^T P'^T for one tile record, straight from the 3-bit codes. `lut`
+// is the shared centroid-pair table; entry f of lane l sits at byte f * 128 + 4 l,
+// so the address is one AND-OR of the shifted field with the lane offset.
 template <int D>
-__device__ __forceinline__ void pv_tile(uint32_t rb, uint32_t lut, int wh, int lane, uint32_t pb0, uint32_t pb1,
-                                        float (&acc)[CDec<D>::MT_W][4]) {
+__device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_t lane4, int wh, int lane,
+                                        uint32_t pb0, uint32_t pb1, float (&acc)[CDec<D>::MT_W][4]) {
   using C = CDec<D>;
   uint32_t vw[C::VW];
 #pragma unroll
@@ -130,7 +172,8 @@ __device__ __forceinline__ void pv_tile(uint32_t rb, uint32_t lut, int wh, int l
   for (int i = 0; i < C::MT_W; ++i) {
     uint32_t av[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) av[j] = lds32(lut + field_x128<C::VW>(vw, 6 * (4 * i + j)));
+    for (int j = 0; j < 4; ++j)
+      av[j] = *reinterpret_cast<const uint32_t*>(lut + (field_x128<C::VW>(vw, 6 * (4 * i + j)) | lane4));
     mma16816(acc[i], av[0], av[1], av[2], av[3], pb0, pb1);
   }
 }
@@ -153,17 +196,30 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XCHG);
   float* mlbuf = reinterpret_cast<float*>(smem + C::OFF_ML);
 
-  int seqlen = a.seq_len[b];
+  // The split boundaries come from the host-side bound min(capacity,
+  // max_seq_len), so the producer can start streaming before the sequence's
+  // length has arrived from memory; tiles past the length are masked (and not
+  // fetched once the length is known).
+  const int seq_raw = a.seq_len[b];
   const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
-  if (seqlen < 0 || seqlen > lim) {
-    if (threadIdx.x == 0) raise_flag(a.flag, kFlagSeqLenRange);
-    seqlen = 0;
-  }
-  const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
-  const int64_t tile_begin = split * n_tiles / a.n_split;
-  const int64_t tile_end = (split + 1) * n_tiles / a.n_split;
-  const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+  const int64_t n_tiles_max = (lim + kTile - 1) / kTile;
+  const int64_t tile_begin = split * n_tiles_max / a.n_split;
+  const int64_t tile_end_max = (split + 1) * n_tiles_max / a.n_split;
+  const int n_iters_max = static_cast<int>((tile_end_max - tile_begin + C::NP - 1) / C::NP);
   const uint8_t* gbase = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) * C::REC;
+
+  // Query fragments first: issued before the producer starts its bulk copies,
+  // these small loads do not queue behind them.
+  uint32_t qf[C::NB_W][4];
+  if (warp < C::NCW) {
+    const int g = lane >> 2, t = lane & 3, wh = warp % C::WT;
+    const int rr = rg * 8 + g;
+    int qi = 0, h = 0;
+    const bool ok = rr < R;
+    if (ok) row_to_query(rr, group_q, kvh, qi, h);
+    const __half* qrow = a.q + ((int64_t)(b * a.n_q + qi) * a.n_q_heads + h) * D;
+    load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -177,9 +233,60 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
 
   if (warp == C::NCW) {
     // ------------------------------------------------------------ producer --
+    int issued = 0;  // lane 0
+    auto issue = [&](int it, int64_t end) {
+      const int s = it % C::NSTAGE;
+      const int64_t first = tile_begin + (int64_t)it * C::NP;
+      const int64_t left = end - first;
+      const uint32_t cnt = left < C::NP ? (uint32_t)left : (uint32_t)C::NP;
+      mbar_arrive_expect_tx(&full[s], cnt * C::REC);
+      bulk_g2s(smem + s * C::STAGE, gbase + first * C::REC, cnt * C::REC, &full[s]);
+      ++issued;
+    };
+    int pre = 0;
+    if (a.n_new == 0) {
+      pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
+      if (lane == 0)
+        for (int it = 0; it < pre; ++it) issue(it, tile_end_max);
+    }
+    const int64_t sl = (seq_raw < 0 || seq_raw > lim) ? 0 : seq_raw;  // first use of the length
+    const int64_t nt = (sl + kTile - 1) / kTile;
+    const int64_t tile_end = nt < tile_end_max ? (nt > tile_begin ? nt : tile_begin) : tile_end_max;
+    const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+    if (a.n_new > 0) {
+      // New positions inside this CTA's tiles. Stages before the first of them
+      // stream meanwhile; the rest is issued once the rows are in the cache.
+      int64_t n0 = sl - a.n_new, n1 = sl;
+      if (n0 < tile_begin * kTile) n0 = tile_begin * kTile;
+      if (n1 > tile_end * kTile) n1 = tile_end * kTile;
+      if (sl < a.n_new) {
+        if (lane == 0) raise_flag(a.flag, kFlagSeqLenRange);
+        n1 = n0;
+      }
+      const int it_new = (n0 < n1) ? static_cast<int>((n0 / kTile - tile_begin) / C::NP) : n_iters;
+      pre = it_new < n_iters ? it_new : n_iters;
+      if (pre > C::NSTAGE) pre = C::NSTAGE;
+      if (lane == 0)
+        for (int it = 0; it < pre; ++it) issue(it, tile_end);
+      for (int64_t pos = n0; pos < n1; ++pos) {
+        const int64_t j = pos - (sl - a.n_new);
+        const __half* krow = a.k_new + b * a.new_batch_stride + j * a.new_token_stride + (int64_t)kvh * D;
+        const __half* vrow = a.v_new + b * a.new_batch_stride + j * a.new_token_stride + (int64_t)kvh * D;
+        uint8_t* grec = a.cache_w + ((int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) + pos / kTile) * C::REC;
+        pack::PositionCodes<D> pc;
+        pack::quantise_position<D>(krow, vrow, a.signs, static_cast<int>(pos % kTile), lane, pc);
+        pack::store_position_global<D>(grec, static_cast<int>(pos % kTile), lane, pc);
+      }
+      if (n0 < n1) {
+        // The rows were written through the generic proxy; the bulk copies that
+        // read them back run in the async proxy.
+        __threadfence();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+      }
+    }
     if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < n_iters; ++it) {
+      for (int it = pre; it < n_iters; ++it) {
         const int s = it % C::NSTAGE;
         if (it >= C::NSTAGE && !*(volatile int*)&s_abort) {
           if (!mbar_wait(&empty[s], ((it / C::NSTAGE) - 1) & 1)) {
@@ -188,12 +295,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
           }
         }
         if (*(volatile int*)&s_abort) break;
-        const int64_t first = tile_begin + (int64_t)it * C::NP;
-        const int64_t left = tile_end - first;
-        const uint32_t cnt = left < C::NP ? (uint32_t)left : (uint32_t)C::NP;
-        mbar_arrive_expect_tx(&full[s], cnt * C::REC);
-        bulk_g2s(smem + s * C::STAGE, gbase + first * C::REC, cnt * C::REC, &full[s]);
-        ++issued;
+        issue(it, tile_end);
       }
       // Do not leave while a copy may still be landing in this CTA's memory.
       const int k0 = issued > C::NSTAGE ? issued - C::NSTAGE : 0;
@@ -207,28 +309,32 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     return;
   }
 
+  int seqlen = seq_raw;
+  if (seqlen < 0 || seqlen > lim) {
+    if (threadIdx.x == 0) raise_flag(a.flag, kFlagSeqLenRange);
+    seqlen = 0;
+  }
+  const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
+  const int64_t tile_end = n_tiles < tile_end_max ? (n_tiles > tile_begin ? n_tiles : tile_begin) : tile_end_max;
+  const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+
   // -------------------------------------------------------------- consumers --
   const int tid = threadIdx.x;  // 0 .. 255
   const int group = warp / C::WT, wh = warp % C::WT;
-  const int g = lane >> 2, t = lane & 3;
+  const int g = lane >> 2;
 
   // Centroid-pair table: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
   for (int e = tid; e < 64 * 32; e += C::NCW * 32) {
     const int f = e >> 5;
-    const __half lo = __float2half_rn(kCentroids[f & 7]);
-    const __half hi = __float2half_rn(kCentroids[f >> 3]);
+    const __half lo = __float2half_rn(centroid(f & 7));
+    const __half hi = __float2half_rn(centroid(f >> 3));
     s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
   }
 
-  uint32_t qf[C::NB_W][4];
-  {
-    const int rr = rg * 8 + g;
-    int qi = 0, h = 0;
-    const bool ok = rr < R;
-    if (ok) row_to_query(rr, group_q, kvh, qi, h);
-    const __half* qrow = a.q + ((int64_t)(b * a.n_q + qi) * a.n_q_heads + h) * D;
-    load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
-  }
+  float* qb_warp = reinterpret_cast<float*>(smem + C::OFF_QB) + warp * C::NB_W * 8;
+  q_block_bias<C::NB_W>(qf, lane, qb_warp);
+  const uint32_t qb = smem_u32(qb_warp) + (lane & 3) * 8;
+  const float scale_log2 = a.scale_log2 * 16777216.0f;  // S carries 2^-24
   float acc[C::MT_W][4];
 #pragma unroll
   for (int i = 0; i < C::MT_W; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
@@ -236,7 +342,8 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   named_bar(1, C::NCW * 32);  // table ready
 
   const uint32_t ring = smem_u32(smem);
-  const uint32_t lut = smem_u32(s_lut) + (lane << 2);
+  const uint8_t* lut_bytes = reinterpret_cast<const uint8_t*>(s_lut);
+  const uint32_t lane4 = (uint32_t)lane << 2;
 
   // Bounded wait for stage `it`; after a timeout every later wait is skipped
   // (results are then flagged invalid) so that the CTA still finishes.
@@ -258,7 +365,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   if (n_iters > 0) {
     wait_stage(0);
     if (tile_begin + group < tile_end) {
-      qk_tile<D>(record(0), wh, lane, qf, S);
+      qk_tile<D>(record(0), wh, lane, qf, qb, S);
       if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, 0, lane);
     }
   }
@@ -268,7 +375,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     float Sn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (it + 1 < n_iters) wait_stage(it + 1);
     if (next) {
-      qk_tile<D>(record(it + 1), wh, lane, qf, Sn);
+      qk_tile<D>(record(it + 1), wh, lane, qf, qb, Sn);
       if constexpr (C::WT == 2)
         xbuf[((group * 2 + ((it + 1) & 1)) * 2 + wh) * 32 + lane] = make_float4(Sn[0], Sn[1], Sn[2], Sn[3]);
     }
@@ -278,9 +385,9 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
       const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * g)));
       const float n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * (g + 8))));
       uint32_t pb0, pb1;
-      softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, n0, n1, st, acc, pb0,
+      softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, scale_log2, n0, n1, st, acc, pb0,
                             pb1);
-      pv_tile<D>(rb, lut, wh, lane, pb0, pb1, acc);
+      pv_tile<D>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[it % C::NSTAGE]);
@@ -298,6 +405,14 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     S[1] = Sn[1];
     S[2] = Sn[2];
     S[3] = Sn[3];
+  }
+
+  // The epilogue reuses the ring. Stages the producer issued before the length
+  // was known but that hold none of this CTA's tiles may still be landing:
+  // wait for them first.
+  if (a.n_new == 0) {
+    const int pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
+    for (int it = n_iters; it < pre; ++it) wait_stage(it);
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
@@ -349,10 +464,10 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(MergeArgs m) {
     row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
   }
   __syncthreads();
-  const int e0 = (int)((int64_t)blockIdx.x * 8 * D / gridDim.x);
-  const int e1 = (int)((int64_t)(blockIdx.x + 1) * 8 * D / gridDim.x);
+  const int u0 = (int)((int64_t)blockIdx.x * 2 * D / gridDim.x);
+  const int u1 = (int)((int64_t)(blockIdx.x + 1) * 2 * D / gridDim.x);
   merge_rows<D>(m.part + (size_t)gid * m.n_split * 8 * D, m.ml + (size_t)gid * m.n_split * 16, m.n_split,
-                e0, e1, tid, 256, msm, s_out, s_lse, blockIdx.x == 0, 1);
+                u0, u1, tid, 256, msm, s_out, s_lse, blockIdx.x == 0, 1);
 }
 
 size_t decode_smem_bytes(int head_dim) {
@@ -392,7 +507,7 @@ cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stre
 template <int D>
 static cudaError_t launch_merge_d(const MergeArgs& m, cudaStream_t stream) {
   const int64_t groups = (int64_t)m.batch * m.n_kv_heads * m.n_row_groups;
-  const size_t smem = (size_t)(2 * m.n_split * 8 + 16 + 256) * sizeof(float);
+  const size_t smem = (size_t)merge_scratch_floats(m.n_split, 256) * sizeof(float);
   static size_t configured = 0;
   if (smem > 48 * 1024 && smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

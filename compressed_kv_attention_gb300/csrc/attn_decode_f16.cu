@@ -18,7 +18,7 @@ struct FDec : DecodeShape<D> {
   using Sh = DecodeShape<D>;
   static constexpr int THREADS = Sh::NCW * 32;
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
-  static constexpr int MERGE_BYTES = (2 * kMaxInKernelSplits * 8 + 16 + 256) * 4;
+  static constexpr int MERGE_BYTES = merge_scratch_floats(kMaxInKernelSplits, 256) * 4;
   static constexpr int OFF_XCHG = (RED_BYTES > MERGE_BYTES) ? RED_BYTES : MERGE_BYTES;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
   static constexpr int SMEM = OFF_ML + Sh::NP * 16 * 4;

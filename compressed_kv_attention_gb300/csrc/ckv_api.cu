@@ -176,14 +176,36 @@ size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, in
   return p.ws;
 }
 
+// New rows appended by the decode kernel itself (ckv_attn_decode_append).
+struct AppendRows {
+  const void* k;
+  const void* v;
+  int n_new;
+  int64_t token_stride, batch_stride;
+};
+
 static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void* k16, const void* v16,
                              int D, int Hkv, int B, int64_t capacity, const int32_t* seq_len,
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
-                             void* stream) {
+                             void* stream, const AppendRows* app = nullptr) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
   if (s != CKV_OK) return s;
+  if (app) {
+    if (p.n_row_groups != 1)
+      return fail(CKV_ERR_UNSUPPORTED, "append needs at most 8 query rows per kv head (n_q * group = %d)",
+                  (n_q_heads / Hkv) * n_q);
+    if (app->n_new < 1 || app->n_new > 16) return fail(CKV_ERR_INVALID_ARG, "n_new must be in [1, 16]");
+    if (app->n_new > max_seq_len) return fail(CKV_ERR_INVALID_ARG, "n_new exceeds max_seq_len");
+    if (!app->k || !app->v || !aligned(app->k, 16) || !aligned(app->v, 16))
+      return fail(CKV_ERR_INVALID_ARG, "k_new/v_new null or not 16-byte aligned");
+    const int64_t row = static_cast<int64_t>(Hkv) * D;
+    if (app->token_stride < row || app->token_stride % 8 || app->batch_stride < 0 || app->batch_stride % 8 ||
+        (B > 1 && app->batch_stride < app->token_stride * app->n_new))
+      return fail(CKV_ERR_INVALID_ARG, "bad strides (token %lld, batch %lld)", (long long)app->token_stride,
+                  (long long)app->batch_stride);
+  }
   if (!seq_len || !q || !out || !lse) return fail(CKV_ERR_INVALID_ARG, "null seq_len/q/out/lse");
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_len, 4))
     return fail(CKV_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
@@ -218,6 +240,14 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.counters = reinterpret_cast<uint32_t*>(base + 64);
   a.out = out;
   a.lse = lse;
+  if (app) {
+    a.n_new = app->n_new;
+    a.cache_w = static_cast<uint8_t*>(cache->data);
+    a.k_new = static_cast<const __half*>(app->k);
+    a.v_new = static_cast<const __half*>(app->v);
+    a.new_token_stride = app->token_stride;
+    a.new_batch_stride = app->batch_stride;
+  }
   // One launch when every CTA can be resident at once (the CTAs of a row group
   // merge their splits themselves); otherwise the decode plus a merge kernel.
   e = compressed ? ckv::launch_attn_decode(a, true, st) : ckv::launch_attn_decode_f16(a, true, st);
@@ -252,6 +282,19 @@ ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64
   return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
                     cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
                     workspace, ws_bytes, stream);
+}
+
+ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                                  const void* k_new_f16, const void* v_new_f16, int32_t n_new,
+                                  int64_t token_stride, int64_t batch_stride, const void* q_f16, int32_t n_q,
+                                  int32_t n_q_heads, float scale, int32_t n_split, float* out, float* lse,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  ckv_status s = check_cache(cache);
+  if (s != CKV_OK) return s;
+  const AppendRows app{k_new_f16, v_new_f16, n_new, token_stride, batch_stride};
+  return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
+                    cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
+                    workspace, ws_bytes, stream, &app);
 }
 
 size_t ckv_attn_decode_f16_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,

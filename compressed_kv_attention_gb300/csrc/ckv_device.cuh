@@ -184,6 +184,17 @@ __device__ __forceinline__ void i8x4_to_half2x2(uint32_t w, uint32_t& lo, uint32
   hi = *reinterpret_cast<uint32_t*>(&h1);
 }
 
+// Four int8 codes (one 32-bit word) -> two fp16x2 holding (q + 128) * 2^-24:
+// after flipping the sign bit each byte is q + 128 in [1, 255], and a byte in
+// the low half of an fp16 with a zero high half is exactly that many units of
+// the smallest subnormal. The constant 128 * 2^-24 per code is removed by
+// starting the accumulator at -2^-17 times the sum of the other operand.
+__device__ __forceinline__ void i8x4_to_sub_half2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0u));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -49,6 +49,14 @@ struct DecodeArgs {
   int merge_in_kernel;       // 1: cooperative launch, CTAs merge their group
   float* out;
   float* lse;
+  // Append (compressed decode, one row group): before its tiles are read, the
+  // CTA that owns positions [seq_len - n_new, seq_len) of a sequence and kv
+  // head quantises those rows of k_new / v_new into the cache.
+  int n_new;                 // 0: plain decode
+  uint8_t* cache_w;          // the same cache, writable
+  const __half* k_new;       // [batch][n_new][n_kv_heads][D] with the strides below
+  const __half* v_new;
+  int64_t new_token_stride, new_batch_stride;  // in elements
 };
 
 struct MergeArgs {

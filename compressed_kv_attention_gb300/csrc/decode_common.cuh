@@ -219,90 +219,156 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
   }
 }
 
+// Floats of shared scratch that merge_rows needs.
+__host__ __device__ constexpr int merge_scratch_floats(int n_split, int nthr) {
+  return 8 * n_split + 16 * (nthr / 32);
+}
+
 // Exact merge of the n_split partials of one row group (8 rows x D):
 // M = max_s m_s, w_s = 2^(m_s - M), O = sum_s w_s part_s / sum_s w_s l_s,
 // lse = (M + log2 sum_s w_s l_s) ln 2; a row with no key gives O = 0, lse = -inf.
 // part: [n_split][8][D], ml: [n_split][8][2] of the group. This CTA produces
-// the elements [e0, e1) of the 8 x D output (row-major); threads tid < nthr
-// (nthr >= 256, 8 full warps) take part and synchronise on named barrier
-// `bar_id`. `sm` provides 2 * n_split * 8 + 16 + nthr floats. out_rows / lse_rows: where each row goes
-// (nullptr for padding rows); lse is written when write_lse.
+// the float4 units [u0, u1) of the 8 x D output (unit u: row u / (D/4), dims
+// 4 (u % (D/4)) .. +4). Threads tid < nthr (nthr a multiple of 32, >= 256)
+// take part and synchronise on named barrier `bar_id`; `sm` provides
+// merge_scratch_floats(n_split, nthr) floats. out_rows / lse_rows: where each
+// row goes (nullptr for padding rows); lse is written when write_lse.
+//
+// The partials sit in L2, so the cost is dependent round trips and barriers:
+// every thread issues its (m, l) loads and its first batch of partial loads
+// before it waits on any of them; row maxima and sums are reduced by all
+// threads at once (the (m, l) entries a thread holds all belong to row tid % 8);
+// each output unit is summed by k consecutive lanes and reduced with shuffles.
 template <int D>
-__device__ __forceinline__ void merge_rows(const float* part, const float* ml, int n_split, int e0,
-                                           int e1, int tid, int nthr, float* sm, float* const* out_rows,
+__device__ __forceinline__ void merge_rows(const float* part, const float* ml, int n_split, int u0, int u1,
+                                           int tid, int nthr, float* sm, float* const* out_rows,
                                            float* const* lse_rows, bool write_lse, int bar_id) {
-  float* w = sm;                  // [n_split][8] running maxima, then weights
-  float* ML = sm + n_split * 8;   // [8][2]: max, 1/sum (0 when empty)
-  float* red = ML + 16;           // [nthr] partial sums
-  float* lsum = red + nthr;       // [n_split][8] row sums
+  constexpr int U = D / 4;        // float4 units per row
+  constexpr int MLR = 4;          // (m, l) pairs per thread held in registers
+  constexpr int PB = 8;           // partial loads per thread per batch
+  const int nw = nthr >> 5;
+  float* w = sm;                  // [n_split][8] weights
+  float* wmax = w + n_split * 8;  // [nw][8] per-warp row maxima
+  float* wsum = wmax + nw * 8;    // [nw][8] per-warp row sums
   const float2* ml2 = reinterpret_cast<const float2*>(ml);
-  for (int i = tid; i < n_split * 8; i += nthr) {
-    const float2 x = __ldcg(ml2 + i);
-    w[i] = x.x;
-    lsum[i] = x.y;
-  }
-  named_bar(bar_id, nthr);
-  // Warp r (r < 8) reduces row r over the splits: max, weights, weighted sum.
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp < 8) {
-    const int r = warp;
-    float M = -INFINITY;
-    for (int s = lane; s < n_split; s += 32) M = fmaxf(M, w[s * 8 + r]);
+  const float4* part4 = reinterpret_cast<const float4*>(part);
+  const int n_ml = n_split * 8;
+  const int nu = u1 - u0;
+  const int lane = tid & 31, warp = tid >> 5;
+  int k = 1;  // lanes per unit: a power of two, so a unit's lanes share a warp
+  while (k < 32 && 2 * k * nu <= nthr) k *= 2;
+  const int cs = nthr / k;
+  const int ui = tid / k, sub = tid % k;
+
+  // 1. Loads in flight together.
+  float2 mlv[MLR];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  for (int j = 0; j < MLR; ++j) {
+    const int i = tid + j * nthr;
+    mlv[j] = (i < n_ml) ? __ldcg(ml2 + i) : make_float2(-INFINITY, 0.0f);
+  }
+  float4 x[PB];
+#pragma unroll
+  for (int j = 0; j < PB; ++j) {
+    const int s = sub + j * k;
+    x[j] = (ui < nu && s < n_split) ? __ldcg(part4 + (size_t)s * 8 * U + u0 + ui)
+                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  // 2. Row maxima.
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < MLR; ++j) m = fmaxf(m, mlv[j].x);
+  for (int i = tid + MLR * nthr; i < n_ml; i += nthr) m = fmaxf(m, __ldcg(ml2 + i).x);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  if (lane < 8) wmax[warp * 8 + lane] = m;
+  named_bar(bar_id, nthr);
+  float M = -INFINITY;
+  for (int ww = 0; ww < nw; ++ww) M = fmaxf(M, wmax[ww * 8 + (tid & 7)]);
+  // 3. Weights and row sums.
+  float Ls = 0.0f;
+#pragma unroll
+  for (int j = 0; j < MLR; ++j) {
+    const int i = tid + j * nthr;
+    if (i < n_ml) {
+      const float ws = (mlv[j].x == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mlv[j].x - M);
+      w[i] = ws;
+      Ls = fmaf(ws, mlv[j].y, Ls);
+    }
+  }
+  for (int i = tid + MLR * nthr; i < n_ml; i += nthr) {
+    const float2 v = __ldcg(ml2 + i);
+    const float ws = (v.x == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(v.x - M);
+    w[i] = ws;
+    Ls = fmaf(ws, v.y, Ls);
+  }
+  Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
+  Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
+  if (lane < 8) wsum[warp * 8 + lane] = Ls;
+  named_bar(bar_id, nthr);
+  if (write_lse && tid < 8 && lse_rows[tid]) {
     float L = 0.0f;
-    for (int s = lane; s < n_split; s += 32) {
-      const float m = w[s * 8 + r];
-      const float ws = (m == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(m - M);
-      w[s * 8 + r] = ws;
-      L = fmaf(ws, lsum[s * 8 + r], L);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) {
-      ML[r * 2] = M;
-      ML[r * 2 + 1] = (L > 0.0f) ? 1.0f / L : 0.0f;
-      if (write_lse && lse_rows[r])
-        *lse_rows[r] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-    }
+    for (int ww = 0; ww < nw; ++ww) L += wsum[ww * 8 + tid];
+    *lse_rows[tid] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
-  named_bar(bar_id, nthr);
-  const int ne = e1 - e0;
-  // k threads per element (each sums every k-th split) when the slice is small.
-  int k = 1;
-  while (k * 2 * ne <= nthr && k < 32) k *= 2;
-  const int cs = nthr / k;  // elements per pass
-  const int el_in = tid % cs, pk = tid / cs;
-  for (int base = 0; base < ne; base += cs) {
-    const int el = base + el_in;
-    const int e = e0 + el;
-    const int r = e / D, d = e % D;
-    float acc = 0.0f;
-    if (el < ne) {
-      const float* p = part + (size_t)r * D + d;
-      // Issue a batch of independent loads before using any of them.
-      for (int s0 = pk; s0 < n_split; s0 += 16 * k) {
-        float x[16];
+  // 4. Weighted sums, reduced over each unit's k lanes.
+  for (int base = 0; base < nu; base += cs) {
+    const int el = base + ui;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int r = 0;
+    if (el < nu) {
+      const int u = u0 + el;
+      r = u / U;
+      int s0 = sub;
+      if (base == 0) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int sj = s0 + j * k;
-          x[j] = (sj < n_split) ? __ldcg(p + (size_t)sj * 8 * D) : 0.0f;
+        for (int j = 0; j < PB; ++j) {
+          const int s = sub + j * k;
+          if (s < n_split) {
+            const float ws = w[s * 8 + r];
+            acc.x = fmaf(ws, x[j].x, acc.x);
+            acc.y = fmaf(ws, x[j].y, acc.y);
+            acc.z = fmaf(ws, x[j].z, acc.z);
+            acc.w = fmaf(ws, x[j].w, acc.w);
+          }
+        }
+        s0 = sub + PB * k;
+      }
+      for (; s0 < n_split; s0 += PB * k) {
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+          const int s = s0 + j * k;
+          x[j] = (s < n_split) ? __ldcg(part4 + (size_t)s * 8 * U + u) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int sj = s0 + j * k;
-          if (sj < n_split) acc = fmaf(w[sj * 8 + r], x[j], acc);
+        for (int j = 0; j < PB; ++j) {
+          const int s = s0 + j * k;
+          if (s < n_split) {
+            const float ws = w[s * 8 + r];
+            acc.x = fmaf(ws, x[j].x, acc.x);
+            acc.y = fmaf(ws, x[j].y, acc.y);
+            acc.z = fmaf(ws, x[j].z, acc.z);
+            acc.w = fmaf(ws, x[j].w, acc.w);
+          }
         }
       }
     }
-    red[tid] = acc;
-    named_bar(bar_id, nthr);
-    if (pk == 0 && el < ne) {
-      float tot = 0.0f;
-      for (int j = 0; j < k; ++j) tot += red[el_in + j * cs];
-      if (out_rows[r]) out_rows[r][d] = tot * ML[r * 2 + 1];
+    for (int off = 1; off < k; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
     }
-    named_bar(bar_id, nthr);
+    if (sub == 0 && el < nu && out_rows[r]) {
+      float L = 0.0f;
+      for (int ww = 0; ww < nw; ++ww) L += wsum[ww * 8 + r];
+      const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+      float* o = out_rows[r] + 4 * ((u0 + el) % U);
+      o[0] = acc.x * inv;
+      o[1] = acc.y * inv;
+      o[2] = acc.z * inv;
+      o[3] = acc.w * inv;
+    }
   }
 }
 
@@ -392,10 +458,10 @@ __device__ __forceinline__ void decode_merge_tail(const DecodeArgs& a, int split
   if (!group_rendezvous(a.counters + gid, (uint32_t)a.n_split, tid, 256, 1, a.flag, s_ok)) return;
   if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
   named_bar(1, 256);
-  const int e0 = (int)((int64_t)split * 8 * D / a.n_split);
-  const int e1 = (int)((int64_t)(split + 1) * 8 * D / a.n_split);
+  const int u0 = (int)((int64_t)split * 2 * D / a.n_split);
+  const int u1 = (int)((int64_t)(split + 1) * 2 * D / a.n_split);
   merge_rows<D>(a.part + (size_t)gid * a.n_split * 8 * D, a.ml + (size_t)gid * a.n_split * 16, a.n_split,
-                e0, e1, tid, 256, sm, s_out, s_lse, split == 0, 1);
+                u0, u1, tid, 256, sm, s_out, s_lse, split == 0, 1);
 }
 
 

@@ -133,14 +133,17 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
  * Split-K flash-decode: each CTA streams a contiguous range of tile records
  * through shared memory, computes S = Q K_hat^T on tensor cores from the int8
  * codes (scales applied per 32-block), runs the online softmax, and accumulates
- * P V_hat in the rotated basis straight from the 3-bit codes. A second kernel
- * merges the split partials with the exact log-sum-exp combine and applies the
- * inverse transform and sign flip once per output row (valid because the
+ * P V_hat in the rotated basis straight from the 3-bit codes. Each CTA applies
+ * the inverse transform and sign flip to its own partial (valid because the
  * rotation is linear and shared within a head: PolyKV page, "S2 perf-path Level
- * B" — the transform runs only on the small FA output).
+ * B" — the transform runs only on the small FA output); the CTAs of a row group
+ * then merge their partials with the exact log-sum-exp combine (a separate
+ * merge kernel when the grid cannot be co-resident).
  *
- * seq_len: device int32 [batch], each in [0, min(capacity, max_seq_len)];
- *   max_seq_len (host) sizes the split grid.
+ * seq_len: device int32 [batch], each in [0, min(capacity, max_seq_len)]; a
+ *   value outside that range raises the device flag and counts as 0.
+ *   max_seq_len (host) sizes the split grid: the splits divide
+ *   [0, min(capacity, max_seq_len)), and tiles past seq_len are skipped.
  * q_f16: device fp16 [batch][n_q][n_q_heads][D].
  * scale: logit scale (e.g. 1/sqrt(D)).
  * n_split: KV splits per (sequence, kv head, row group); 0 picks one that fills
@@ -153,6 +156,30 @@ CKV_API ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_le
                            const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale,
                            int32_t n_split, float* out, float* lse, void* workspace,
                            size_t ws_bytes, void* stream);
+
+/*
+ * attn_decode_append — one decode step: quantise n_new new K/V rows of every
+ * sequence into the cache at positions [seq_len[b] - n_new, seq_len[b]) (the
+ * same bytes ckv_kv_pack writes), then attend as attn_decode over
+ * [0, seq_len[b]). The rows are packed inside the decode kernel by the CTA whose
+ * KV range holds them, before it reads those tiles, so the step is a single
+ * kernel. seq_len is the length after the append.
+ *
+ * k_new_f16, v_new_f16: fp16, element (b, j, h, i) of new row j at
+ *   b*batch_stride + j*token_stride + h*D + i (elements), 16-byte aligned,
+ *   strides multiples of 8. n_new in [1, 16], <= max_seq_len.
+ * Other arguments and the workspace as attn_decode.
+ * Errors: as attn_decode and ckv_kv_pack; UNSUPPORTED when a kv head has more
+ * than 8 query rows (n_q * n_q_heads / n_kv_heads > 8): use ckv_kv_pack then
+ * ckv_attn_decode. A seq_len[b] below n_new raises the device flag (nothing is
+ * written for that sequence).
+ */
+CKV_API ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t* seq_len,
+                                          int64_t max_seq_len, const void* k_new_f16, const void* v_new_f16,
+                                          int32_t n_new, int64_t token_stride, int64_t batch_stride,
+                                          const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale,
+                                          int32_t n_split, float* out, float* lse, void* workspace,
+                                          size_t ws_bytes, void* stream);
 
 /*
  * attn_decode_noalloc — attn_decode for callers that cannot allocate device

@@ -129,3 +129,22 @@ def test_prefill_argument_checks(lib):
     assert call(w=None) == -3
     assert call(wb=128) == -3
     assert call(n_new=0) == 0                        # nothing to do
+
+
+def test_decode_append_argument_checks(lib):
+    fake = 0x7f0000000000
+    c = _fake_cache(D=512, Hkv=2, cap=4096)
+    need = lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 1, 16, 8)
+
+    def call(nq=1, hq=16, k=fake, v=fake, n_new=1, ts=1024, bs=0, wsb=need):
+        return lib.ckv_attn_decode_append(ctypes.byref(c), fake, 4096, k, v, n_new, ts, bs, fake, nq, hq, 0.04, 8,
+                                          fake, fake, fake, wsb, None)
+    assert call(nq=2) == -2          # 16 query rows per kv head: more than one row group
+    assert call(n_new=0) == -1
+    assert call(n_new=17) == -1
+    assert call(k=None) == -1
+    assert call(v=fake + 8) == -1    # not 16-byte aligned
+    assert call(ts=1000) == -1       # token stride below one row of all kv heads
+    assert call(ts=1028) == -1       # not a multiple of 8 elements
+    assert call(bs=-8) == -1
+    assert call(wsb=need - 1) == -3
