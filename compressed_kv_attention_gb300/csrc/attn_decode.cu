@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   // max_seq_len), so the producer can start streaming before the sequence's
   // length has arrived from memory; tiles past the length are masked (and not
   // fetched once the length is known).
-  const int seq_raw = a.seq_len[b];
+  __shared__ int s_seq;
   const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
   const int64_t n_tiles_max = (lim + kTile - 1) / kTile;
   const int64_t tile_begin = split * n_tiles_max / a.n_split;
@@ -209,7 +209,17 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const uint8_t* gbase = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) * C::REC;
 
   // Query fragments first: issued before the producer starts its bulk copies,
-  // these small loads do not queue behind them.
+  // these small loads do not queue behind them. The sequence length is read by
+  // one thread per CTA (every CTA of the grid reads the same few words) and
+  // shared; for an append the producer warp also fetches the newest row now.
+  if (threadIdx.x == 0) s_seq = a.seq_len[b];
+  pack::PositionInput<D> new_row;
+  if (warp == C::NCW && a.n_new > 0) {
+    const int64_t j = a.n_new - 1;
+    pack::load_position<D>(a.k_new + b * a.new_batch_stride + j * a.new_token_stride + (int64_t)kvh * D,
+                           a.v_new + b * a.new_batch_stride + j * a.new_token_stride + (int64_t)kvh * D, a.signs,
+                           lane, new_row);
+  }
   uint32_t qf[C::NB_W][4];
   if (warp < C::NCW) {
     const int g = lane >> 2, t = lane & 3, wh = warp % C::WT;
@@ -221,35 +231,49 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
   }
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NCW);
-    }
-    s_abort = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-
+  // The producer lane sets up the barriers and, for a plain decode, issues the
+  // first stages before the CTA-wide barrier; the consumers meanwhile load Q
+  // and fill the centroid table.
+  int issued = 0;  // producer lane
+  auto issue = [&](int it, int64_t end) {
+    const int s = it % C::NSTAGE;
+    const int64_t first = tile_begin + (int64_t)it * C::NP;
+    const int64_t left = end - first;
+    const uint32_t cnt = left < C::NP ? (uint32_t)left : (uint32_t)C::NP;
+    mbar_arrive_expect_tx(&full[s], cnt * C::REC);
+    bulk_g2s(smem + s * C::STAGE, gbase + first * C::REC, cnt * C::REC, &full[s]);
+    ++issued;
+  };
+  int pre = 0;
   if (warp == C::NCW) {
-    // ------------------------------------------------------------ producer --
-    int issued = 0;  // lane 0
-    auto issue = [&](int it, int64_t end) {
-      const int s = it % C::NSTAGE;
-      const int64_t first = tile_begin + (int64_t)it * C::NP;
-      const int64_t left = end - first;
-      const uint32_t cnt = left < C::NP ? (uint32_t)left : (uint32_t)C::NP;
-      mbar_arrive_expect_tx(&full[s], cnt * C::REC);
-      bulk_g2s(smem + s * C::STAGE, gbase + first * C::REC, cnt * C::REC, &full[s]);
-      ++issued;
-    };
-    int pre = 0;
+    if (lane == 0) {
+      for (int s = 0; s < C::NSTAGE; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], C::NCW);
+      }
+      s_abort = 0;
+      fence_barrier_init();
+    }
     if (a.n_new == 0) {
       pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
       if (lane == 0)
         for (int it = 0; it < pre; ++it) issue(it, tile_end_max);
     }
-    const int64_t sl = (seq_raw < 0 || seq_raw > lim) ? 0 : seq_raw;  // first use of the length
+  } else {
+    // Centroid-pair table: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
+    for (int e = threadIdx.x; e < 64 * 32; e += C::NCW * 32) {
+      const int f = e >> 5;
+      const __half lo = __float2half_rn(centroid(f & 7));
+      const __half hi = __float2half_rn(centroid(f >> 3));
+      s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+  }
+  __syncthreads();
+
+  if (warp == C::NCW) {
+    // ------------------------------------------------------------ producer --
+    const int seq_raw = s_seq;
+    const int64_t sl = (seq_raw < 0 || seq_raw > lim) ? 0 : seq_raw;
     const int64_t nt = (sl + kTile - 1) / kTile;
     const int64_t tile_end = nt < tile_end_max ? (nt > tile_begin ? nt : tile_begin) : tile_end_max;
     const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
@@ -274,7 +298,11 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
         const __half* vrow = a.v_new + b * a.new_batch_stride + j * a.new_token_stride + (int64_t)kvh * D;
         uint8_t* grec = a.cache_w + ((int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) + pos / kTile) * C::REC;
         pack::PositionCodes<D> pc;
-        pack::quantise_position<D>(krow, vrow, a.signs, static_cast<int>(pos % kTile), lane, pc);
+        if (pos == sl - 1) {
+          pack::quantise_loaded<D>(new_row, static_cast<int>(pos % kTile), lane, pc);
+        } else {
+          pack::quantise_position<D>(krow, vrow, a.signs, static_cast<int>(pos % kTile), lane, pc);
+        }
         pack::store_position_global<D>(grec, static_cast<int>(pos % kTile), lane, pc);
       }
       if (n0 < n1) {
@@ -309,7 +337,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     return;
   }
 
-  int seqlen = seq_raw;
+  int seqlen = s_seq;
   if (seqlen < 0 || seqlen > lim) {
     if (threadIdx.x == 0) raise_flag(a.flag, kFlagSeqLenRange);
     seqlen = 0;
@@ -323,14 +351,6 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const int group = warp / C::WT, wh = warp % C::WT;
   const int g = lane >> 2;
 
-  // Centroid-pair table: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
-  for (int e = tid; e < 64 * 32; e += C::NCW * 32) {
-    const int f = e >> 5;
-    const __half lo = __float2half_rn(centroid(f & 7));
-    const __half hi = __float2half_rn(centroid(f >> 3));
-    s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-  }
-
   float* qb_warp = reinterpret_cast<float*>(smem + C::OFF_QB) + warp * C::NB_W * 8;
   q_block_bias<C::NB_W>(qf, lane, qb_warp);
   const uint32_t qb = smem_u32(qb_warp) + (lane & 3) * 8;
@@ -339,7 +359,6 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
 #pragma unroll
   for (int i = 0; i < C::MT_W; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
   SoftmaxState st{-INFINITY, -INFINITY, 0.0f, 0.0f};
-  named_bar(1, C::NCW * 32);  // table ready
 
   const uint32_t ring = smem_u32(smem);
   const uint8_t* lut_bytes = reinterpret_cast<const uint8_t*>(s_lut);

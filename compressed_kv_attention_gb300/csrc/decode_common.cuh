@@ -26,10 +26,13 @@ struct DecodeShape {
   static constexpr int NB_W = NB / WT;              // blocks per warp (S)
   static constexpr int MT_W = MT / WT;              // m-tiles per warp (O)
   static constexpr int GD = D / 8;                  // output dims owned per lane row
-  // Per-group reduction buffer [8 rows][RP]: dim d of row r at r*RP + d + d/GD.
-  // RP = D + 36 is = 4 (mod 32), which makes both the fragment-order writes and
-  // the row-order reads free of shared-memory bank conflicts.
-  static constexpr int RP = D + 36;
+  // Per-group reduction buffer [8 rows][RP]: dim d of row r at
+  // r*RP + d + 2*PS*(d / GD). Dims are written and read in pairs (float2). With
+  // PS = (1 - GD/2) mod 16 and RP = 4 (mod 16) the fragment-order pair writes
+  // of a half-warp fall on 16 different bank pairs.
+  static constexpr int PS = ((1 - GD / 2) % 16 + 16) % 16;
+  static constexpr int RP0 = D + 14 * PS + 2;
+  static constexpr int RP = RP0 + ((4 - RP0 % 16) + 16) % 16;
   static constexpr int RED_FLOATS = 8 * RP;
   static constexpr int XCHG_BYTES = (WT == 2) ? NP * 2 * 2 * 32 * 16 : 0;
 };
@@ -118,7 +121,9 @@ __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int grou
 // De-rotating each partial here is exact: the transform is linear and the
 // split merge only forms per-row weighted sums of partials. Runs on the 256
 // consumer threads (named barrier 1). `red` holds NP * RED_FLOATS floats (stage
-// memory is reused), `mlbuf` NP * 16 floats.
+// memory is reused), `mlbuf` NP * 16 floats. Each group stores its unscaled
+// accumulators with its own (m, l); the warp that owns a row rescales the
+// groups while summing them.
 template <int D, int MTW>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
                                                 float* mlbuf, int group, int wh, int warp, int lane,
@@ -140,83 +145,90 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
     mlbuf[group * 16 + (2 * t + 1) * 2 + 0] = st.m1;
     mlbuf[group * 16 + (2 * t + 1) * 2 + 1] = st.l1;
   }
-  named_bar(1, Sh::NCW * 32);
-  float mc0 = -INFINITY, mc1 = -INFINITY;
-#pragma unroll
-  for (int q = 0; q < Sh::NP; ++q) {
-    mc0 = fmaxf(mc0, mlbuf[q * 16 + (2 * t) * 2]);
-    mc1 = fmaxf(mc1, mlbuf[q * 16 + (2 * t + 1) * 2]);
-  }
-  const float f0 = (st.m0 == -INFINITY) ? 0.0f : exp2f(st.m0 - mc0);
-  const float f1 = (st.m1 == -INFINITY) ? 0.0f : exp2f(st.m1 - mc1);
   float* myred = red + group * Sh::RED_FLOATS;
 #pragma unroll
   for (int i = 0; i < MTW; ++i) {
-    const int d0 = Sh::GD * g + 2 * (wh * MTW + i) + g;  // padded index of dim d0 (d0 / GD == g)
-    myred[(2 * t) * Sh::RP + d0] = acc[i][0] * f0;
-    myred[(2 * t + 1) * Sh::RP + d0] = acc[i][1] * f1;
-    myred[(2 * t) * Sh::RP + d0 + 1] = acc[i][2] * f0;
-    myred[(2 * t + 1) * Sh::RP + d0 + 1] = acc[i][3] * f1;
+    const int pd = Sh::GD * g + 2 * (wh * MTW + i) + 2 * Sh::PS * g;  // dim pair d, d+1 with d / GD == g
+    *reinterpret_cast<float2*>(myred + (2 * t) * Sh::RP + pd) = make_float2(acc[i][0], acc[i][2]);
+    *reinterpret_cast<float2*>(myred + (2 * t + 1) * Sh::RP + pd) = make_float2(acc[i][1], acc[i][3]);
   }
   named_bar(1, Sh::NCW * 32);
-  // Warp r owns row r: lane holds dims d = 32 e + lane (e < E), summed over groups.
-  constexpr int E = D / 32;
+  // Warp r owns row r: lane holds dims d = 64 e + 2 lane + c (e < D/64, c < 2).
   const int r = warp;
-  float v[E];
+  float mq[Sh::NP], mc = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int d = 32 * e + lane;
-    float x = 0.0f;
+  for (int q = 0; q < Sh::NP; ++q) {
+    mq[q] = mlbuf[q * 16 + r * 2];
+    mc = fmaxf(mc, mq[q]);
+  }
+  float fq[Sh::NP], lc = 0.0f;
 #pragma unroll
-    for (int q = 0; q < Sh::NP; ++q) x += red[q * Sh::RED_FLOATS + r * Sh::RP + d + d / Sh::GD];
+  for (int q = 0; q < Sh::NP; ++q) {
+    fq[q] = (mq[q] == -INFINITY) ? 0.0f : exp2f(mq[q] - mc);
+    lc = fmaf(fq[q], mlbuf[q * 16 + r * 2 + 1], lc);
+  }
+  constexpr int E2 = D / 64;
+  float2 v[E2];
+#pragma unroll
+  for (int e = 0; e < E2; ++e) {
+    const int d = 64 * e + 2 * lane;
+    const int pd = d + 2 * Sh::PS * (d / Sh::GD);
+    float2 x = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < Sh::NP; ++q) {
+      const float2 y = *reinterpret_cast<const float2*>(red + q * Sh::RED_FLOATS + r * Sh::RP + pd);
+      x.x = fmaf(fq[q], y.x, x.x);
+      x.y = fmaf(fq[q], y.y, x.y);
+    }
     v[e] = x;
   }
   if (signs) {
-    // Unnormalised Walsh-Hadamard transform of the row: stages h < 32 pair
-    // lanes (shuffles), stages h >= 32 pair registers of the same lane; then the
-    // sign flip and 1/D (one 1/sqrt(D) from the orthonormal inverse, one from
-    // the norm scaling folded into P').
+    // Unnormalised Walsh-Hadamard transform of the row: the stage on dim bit 0
+    // pairs the two values of a float2, bits 1..5 pair lanes (shuffles), bits
+    // 6.. pair registers; then the sign flip and 1/D (one 1/sqrt(D) from the
+    // orthonormal inverse, one from the norm scaling folded into P').
+#pragma unroll
+    for (int e = 0; e < E2; ++e) {
+      const float a0 = v[e].x, a1 = v[e].y;
+      v[e] = make_float2(a0 + a1, a0 - a1);
+    }
 #pragma unroll
     for (int hl = 1; hl < 32; hl <<= 1) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
-        v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+      for (int e = 0; e < E2; ++e) {
+        const float ox = __shfl_xor_sync(0xffffffffu, v[e].x, hl);
+        const float oy = __shfl_xor_sync(0xffffffffu, v[e].y, hl);
+        v[e].x = (lane & hl) ? (ox - v[e].x) : (v[e].x + ox);
+        v[e].y = (lane & hl) ? (oy - v[e].y) : (v[e].y + oy);
       }
     }
 #pragma unroll
-    for (int hh = 1; hh < E; hh <<= 1) {
+    for (int hh = 1; hh < E2; hh <<= 1) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
+      for (int e = 0; e < E2; ++e) {
         if ((e & hh) == 0) {
-          const float x0 = v[e], x1 = v[e + hh];
-          v[e] = x0 + x1;
-          v[e + hh] = x0 - x1;
+          const float2 x0 = v[e], x1 = v[e + hh];
+          v[e] = make_float2(x0.x + x1.x, x0.y + x1.y);
+          v[e + hh] = make_float2(x0.x - x1.x, x0.y - x1.y);
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int d = 32 * e + lane;
-      v[e] = (signs[d] < 0 ? -v[e] : v[e]) * (1.0f / D);
+    for (int e = 0; e < E2; ++e) {
+      const int d = 64 * e + 2 * lane;
+      const char2 sg = *reinterpret_cast<const char2*>(signs + d);
+      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (1.0f / D);
+      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (1.0f / D);
     }
   }
-  float* prow = part_out + r * D + lane;
+  float2* prow = reinterpret_cast<float2*>(part_out + r * D) + lane;
 #pragma unroll
-  for (int e = 0; e < E; ++e) prow[32 * e] = v[e];
-  if (tid < 8) {
-    float mc = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < Sh::NP; ++q) mc = fmaxf(mc, mlbuf[q * 16 + tid * 2]);
-    float lc = 0.0f;
-#pragma unroll
-    for (int q = 0; q < Sh::NP; ++q) {
-      const float mq = mlbuf[q * 16 + tid * 2];
-      if (mq != -INFINITY) lc += exp2f(mq - mc) * mlbuf[q * 16 + tid * 2 + 1];
-    }
-    ml_out[tid * 2 + 0] = mc;
-    ml_out[tid * 2 + 1] = lc;
+  for (int e = 0; e < E2; ++e) prow[32 * e] = v[e];
+  if (lane == 0) {
+    ml_out[r * 2 + 0] = mc;
+    ml_out[r * 2 + 1] = lc;
   }
+  (void)tid;
 }
 
 // Floats of shared scratch that merge_rows needs.

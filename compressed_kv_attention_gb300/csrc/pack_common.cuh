@@ -73,15 +73,31 @@ struct PositionCodes {
   int L;               // lane stream
 };
 
+// This lane's values of one K row and one V row, and its sign entries.
 template <int D>
-__device__ __forceinline__ void quantise_position(const __half* krow, const __half* vrow, const int8_t* signs,
-                                                  int p, int lane, PositionCodes<D>& pc) {
+struct PositionInput {
+  static constexpr int E = D / 32;
+  float kx[E], vx[E];
+  int8_t sg[E];
+};
+
+template <int D>
+__device__ __forceinline__ void load_position(const __half* krow, const __half* vrow, const int8_t* signs,
+                                              int lane, PositionInput<D>& in) {
+  constexpr int E = D / 32;
+  load_row<E>(krow + lane * E, in.kx);
+  load_row<E>(vrow + lane * E, in.vx);
+#pragma unroll
+  for (int e = 0; e < E; ++e) in.sg[e] = signs[lane * E + e];
+}
+
+template <int D>
+__device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int p, int lane, PositionCodes<D>& pc) {
   constexpr int E = D / 32;            // values per lane
   constexpr int LPB = 32 / E;          // lanes per q8_0 block
   using PC = PositionCodes<D>;
-  float kx[E], vx[E];
-  load_row<E>(krow + lane * E, kx);
-  load_row<E>(vrow + lane * E, vx);
+  const float (&kx)[E] = in.kx;
+  const float (&vx)[E] = in.vx;
 
   // ---- K: q8_0 ----
   float amax = 0.0f;
@@ -105,11 +121,10 @@ __device__ __forceinline__ void quantise_position(const __half* krow, const __ha
   // ---- V: TBQ3 ----
   float ss = 0.0f;
   float z[E];
-  const int8_t* sg = signs + lane * E;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     ss = fmaf(vx[e], vx[e], ss);
-    z[e] = sg[e] < 0 ? -vx[e] : vx[e];
+    z[e] = in.sg[e] < 0 ? -vx[e] : vx[e];
   }
   // Butterfly stages inside the lane (pairs closer than E apart).
 #pragma unroll
@@ -169,6 +184,14 @@ __device__ __forceinline__ void quantise_position(const __half* krow, const __ha
     pc.val[w] = __funnelshift_l(lo_v, cv[w], sh);
     pc.mask[w] = __funnelshift_l(lo_m, cm[w], sh);
   }
+}
+
+template <int D>
+__device__ __forceinline__ void quantise_position(const __half* krow, const __half* vrow, const int8_t* signs,
+                                                  int p, int lane, PositionCodes<D>& pc) {
+  PositionInput<D> in;
+  load_position<D>(krow, vrow, signs, lane, in);
+  quantise_loaded<D>(in, p, lane, pc);
 }
 
 // Byte offset inside a record of the 8-byte K-code chunk that holds dims
