@@ -46,7 +46,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one decode-kernel launch on gemma4_decode from the ncu capture
 # summarised in profiles/attn_decode_gemma4.md, valid for the kernel sources
 # whose hash is recorded beside it (null once they change).
-NCU_TRAFFIC = {"bytes": None, "source_sha": None}
+NCU_TRAFFIC = {"bytes": 49526784, "source_sha": "e1011a1113edb3ff"}
 
 
 def _args():
@@ -74,7 +74,7 @@ def _peaks():
 
 def _decode_source_sha():
     h = hashlib.sha256()
-    for name in ("attn_decode.cu", "decode_common.cuh", "ckv_device.cuh"):
+    for name in ("attn_decode.cu", "decode_common.cuh", "ckv_device.cuh", "pack_common.cuh"):
         with open(os.path.join(ROOT, "compressed_kv_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
