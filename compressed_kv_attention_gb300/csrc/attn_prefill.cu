@@ -57,8 +57,6 @@ struct PCfg {
   static constexpr int OT = D < 448 ? D : 448;   // output dims accumulated in TMEM
   static constexpr int OR = D - OT;              // output dims summed in registers (0 or 64)
   static constexpr int REC = record_bytes(D);
-  static constexpr int PIECES = NKV * NB;        // (token, 32-block) pieces of K per step
-  static constexpr int PPT = (PIECES + 255) / 256;  // pieces per thread
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = M * D * 2;                 // K_hat hi, then lo, then C^T
   static constexpr int P_OFF = KV_OFF + NKV * D * 2;
@@ -179,68 +177,97 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       umma_f16(tmem, ad, bd, umma_idesc_f16_f32(C::M, C::NKV), true);
     }
   };
-  constexpr int NCH = (C::OT > 256 ? 2 : 1) + (C::OR > 0 ? 1 : 0);
   const OChunk chunks[3] = {{0, C::OT < 256 ? C::OT : 256, 64},
                             {256, C::OT > 256 ? C::OT - 256 : 0, 320},
                             {C::OT, C::OR, 0}};
+
+  // Codes of a step are fetched into registers one step ahead, so their
+  // global-memory latency overlaps the previous step's MMAs and softmax.
+  //  K: thread t owns token kp = t % NKV and the 32-dim blocks kb0 + KBS * c;
+  //     a warp covers 32 consecutive tokens of one block, so its fp16 stores
+  //     into the swizzled tile fall on distinct bank groups.
+  //  V: threads 128..255; warp w takes lane streams [8w, 8w + 8) of the
+  //     step's 4 records (lane = 8 * record + stream), which spreads one
+  //     store instruction over 16 banks.
+  constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D), NW = LB / 4;
+  constexpr int KBS = C::THREADS / C::NKV;  // blocks between a thread's pieces
+  constexpr int KPT = C::NB / KBS;          // blocks (pieces) per thread
+  const int kp = tid % C::NKV, kb0 = tid / C::NKV;
+  const int vu = tid - 128, vr4 = (vu & 31) >> 3, vL = 8 * (vu >> 5) + (vu & 7);
+  uint2 kw[KPT][4];
+  __half kd[KPT];
+  uint32_t vw[NW];
+  float nrm = 0.0f;
+  auto fetch = [&](int step) {
+    const int64_t j0 = (int64_t)step * C::NKV;
+    {
+      const int64_t tpos = j0 + kp;
+      const int64_t rec = tpos / kTile;
+      const int pp = static_cast<int>(tpos % kTile);
+      const bool have = rec < n_rec;
+      const uint8_t* rb = stream + rec * C::REC;
+#pragma unroll
+      for (int c = 0; c < KPT; ++c) {
+        const int blk = kb0 + KBS * c;
+        kd[c] = have ? *reinterpret_cast<const __half*>(rb + k_scale_offset(D) + 2 * (pp * C::NB + blk))
+                     : __ushort_as_half(0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          kw[c][t] = have ? *reinterpret_cast<const uint2*>(rb + (blk * 32 + 4 * (pp & 7) + t) * 16 + (pp >> 3) * 8)
+                          : make_uint2(0, 0);
+      }
+    }
+    if (!softmax_warp) {
+      const int64_t rec = j0 / kTile + vr4;
+      const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
+#pragma unroll
+      for (int s4 = 0; s4 < NW; ++s4) {
+        const int sbyte = s4 * 4;
+        vw[s4] = (rec < n_rec) ? *reinterpret_cast<const uint32_t*>(vb + ((sbyte / GR) * 32 + vL) * GR + (sbyte % GR))
+                               : 0u;
+      }
+    }
+    if (tid < C::NKV) {
+      const int64_t rec = (j0 + tid) / kTile;
+      nrm = (rec < n_rec) ? __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D) +
+                                                                          2 * ((j0 + tid) % kTile)))
+                          : 0.0f;
+    }
+  };
+  if (n_steps > 0) fetch(0);
 
   for (int step = 0; step < n_steps; ++step) {
     const int64_t j0 = (int64_t)step * C::NKV;
     // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
     // q is an exact fp16 integer; hi = q*d rounded once (HMUL2 of exact fp16
     // operands) and lo = fma(q, d, -hi), the exact residual (HFMA2).
-    uint32_t lo_keep[C::PPT][4][4];
-    {
-      uint2 kw[C::PPT][4];
-      __half2 dd[C::PPT];
+    uint32_t lo_keep[KPT][4][4];
 #pragma unroll
-      for (int pc = 0; pc < C::PPT; ++pc) {  // issue every load of the step first
-        const int piece = tid + pc * C::THREADS;
-        const int p = piece / C::NB, blk = piece % C::NB;
-        const int64_t rec = (j0 + p) / kTile;
-        const int pp = p % kTile;
-        const bool have = piece < C::PIECES && rec < n_rec;
-        const uint8_t* rb = stream + rec * C::REC;
-        __half d = __ushort_as_half(0);
-        if (have) d = *reinterpret_cast<const __half*>(rb + k_scale_offset(D) + 2 * (pp * C::NB + blk));
-        dd[pc] = __halves2half2(d, d);
+    for (int c = 0; c < KPT; ++c) {
+      const int blk = kb0 + KBS * c;
+      const __half2 dd = __halves2half2(kd[c], kd[c]);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          kw[pc][t] = make_uint2(0, 0);
-          if (have) kw[pc][t] = *reinterpret_cast<const uint2*>(rb + (blk * 32 + 4 * (pp & 7) + t) * 16 + (pp >> 3) * 8);
+      for (int t = 0; t < 4; ++t) {
+        uint32_t qh[4], hi[4];
+        i8x4_to_half2x2(kw[c][t].x, qh[0], qh[1]);
+        i8x4_to_half2x2(kw[c][t].y, qh[2], qh[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half2 qv = *reinterpret_cast<const __half2*>(&qh[e]);
+          const __half2 h = __hmul2(qv, dd);
+          const __half2 l = __hfma2(qv, dd, __hneg2(h));
+          hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+          lo_keep[c][t][e] = *reinterpret_cast<const uint32_t*>(&l);
         }
-      }
-#pragma unroll
-      for (int pc = 0; pc < C::PPT; ++pc) {
-        const int piece = tid + pc * C::THREADS;
-        const int p = piece / C::NB, blk = piece % C::NB;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          uint32_t qh[4], hi[4];
-          i8x4_to_half2x2(kw[pc][t].x, qh[0], qh[1]);
-          i8x4_to_half2x2(kw[pc][t].y, qh[2], qh[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 qv = *reinterpret_cast<const __half2*>(&qh[e]);
-            const __half2 h = __hmul2(qv, dd[pc]);
-            const __half2 l = __hfma2(qv, dd[pc], __hneg2(h));
-            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-            lo_keep[pc][t][e] = *reinterpret_cast<const uint32_t*>(&l);
-          }
-          if (piece < C::PIECES)
-            *reinterpret_cast<uint4*>(sKV + sw128_offset(p, blk * 32 + 8 * t, C::NKV)) =
-                make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        }
+        *reinterpret_cast<uint4*>(sKV + sw128_offset(kp, blk * 32 + 8 * t, C::NKV)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
     }
-    // V norms of the step's tokens (positions past the cache read as 0).
-    if (tid < C::NKV) {
-      const int64_t rec = (j0 + tid) / kTile;
-      float n = 0.0f;
-      if (rec < n_rec)
-        n = __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D) + 2 * ((j0 + tid) % kTile)));
-      sNorm[tid] = n;
-    }
+    if (tid < C::NKV) sNorm[tid] = nrm;
+    uint32_t vcur[NW];
+#pragma unroll
+    for (int s4 = 0; s4 < NW; ++s4) vcur[s4] = vw[s4];
+    if (step + 1 < n_steps) fetch(step + 1);
     sync_for_mma();
     if (tid == 0) {
       // First pass of S overwrites the accumulator (columns [0, 64)).
@@ -254,15 +281,12 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     wait_mma();
     // ---- lo pass ----
 #pragma unroll
-    for (int pc = 0; pc < C::PPT; ++pc) {
-      const int piece = tid + pc * C::THREADS;
-      const int p = piece / C::NB, blk = piece % C::NB;
-      if (piece < C::PIECES) {
+    for (int c = 0; c < KPT; ++c) {
+      const int blk = kb0 + KBS * c;
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          *reinterpret_cast<uint4*>(sKV + sw128_offset(p, blk * 32 + 8 * t, C::NKV)) =
-              make_uint4(lo_keep[pc][t][0], lo_keep[pc][t][1], lo_keep[pc][t][2], lo_keep[pc][t][3]);
-      }
+      for (int t = 0; t < 4; ++t)
+        *reinterpret_cast<uint4*>(sKV + sw128_offset(kp, blk * 32 + 8 * t, C::NKV)) =
+            make_uint4(lo_keep[c][t][0], lo_keep[c][t][1], lo_keep[c][t][2], lo_keep[c][t][3]);
     }
     sync_for_mma();
     if (tid == 0) {
@@ -323,35 +347,18 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
             make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
     } else {
       // ---- C^T (centroids, rotated basis) for the step: rows = dims, K = tokens ----
-      // One (record, lane stream) per thread: 4 records x 32 lanes = 128 threads.
       // A 6-bit field pairs the codes of two adjacent positions of one dim,
       // which is one fp16x2 word of C^T: one shared table load per field.
-      const int u = tid - 128;
-      const int r4 = u >> 5, L = u & 31;
-      const int64_t rec = j0 / kTile + r4;
-      constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D), NW = LB / 4;
-      uint32_t sw[NW];
-      if (rec < n_rec) {
-        const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
-#pragma unroll
-        for (int s4 = 0; s4 < NW; ++s4) {
-          const int sbyte = s4 * 4;
-          sw[s4] = *reinterpret_cast<const uint32_t*>(vb + ((sbyte / GR) * 32 + L) * GR + (sbyte % GR));
-        }
-      } else {
-#pragma unroll
-        for (int s4 = 0; s4 < NW; ++s4) sw[s4] = 0u;
-      }
-      const int g = L >> 2, tq = L & 3;
+      const int g = vL >> 2, tq = vL & 3;
       const uint32_t lut = smem_u32(sLut) + (uint32_t)(lane << 2);
       const uint32_t kvb = smem_u32(sKV);
-      const int tok0 = r4 * 16 + 2 * tq;
+      const int tok0 = vr4 * 16 + 2 * tq;
 #pragma unroll
       for (int pi = 0; pi < 2 * G; ++pi) {
         const int bit = 6 * pi;
         const int wi = bit >> 5, sh = bit & 31;
-        uint32_t f = sw[wi] >> sh;
-        if (sh > 26 && wi + 1 < NW) f |= sw[wi + 1] << (32 - sh);
+        uint32_t f = vcur[wi] >> sh;
+        if (sh > 26 && wi + 1 < NW) f |= vcur[wi + 1] << (32 - sh);
         const uint32_t val = lds32(lut + ((f & 63u) << 7));
         const int mt = pi >> 2, rh = pi & 1, h2 = (pi >> 1) & 1;
         const int dim = G * g + 2 * mt + rh;

@@ -60,12 +60,13 @@ ckv_status check_cache(const ckv_cache* c) {
   return CKV_OK;
 }
 
-// Split count: enough CTAs to cover every SM once, no more splits than tiles.
+// Split count: as many CTAs as fit on the SMs at once (one each), so the grid
+// stays co-resident and merges its splits in-kernel; no more splits than tiles.
 int auto_split(int64_t units, int64_t max_seq_len, int tiles_per_cta_iter) {
   const int64_t tiles = (max_seq_len + 15) / 16;
   if (tiles == 0) return 1;
   const int sms = num_sms();
-  int64_t s = (sms + units - 1) / units;
+  int64_t s = sms / units;
   const int64_t by_tiles = (tiles + tiles_per_cta_iter - 1) / tiles_per_cta_iter;
   if (s > by_tiles) s = by_tiles;
   if (s < 1) s = 1;
