@@ -28,6 +28,7 @@
 
 #include "../../include/ckv.h"
 #include "ckv_kernels.cuh"
+#include "prefill_common.cuh"
 
 namespace ckv {
 
@@ -35,19 +36,6 @@ namespace {
 
 __constant__ float kPrefillCentroids[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
                                            0.2451f,  0.7560f,  1.3439f,  2.1520f};
-
-struct PrefillArgs {
-  const uint8_t* cache;
-  int64_t capacity;
-  int n_kv_heads, batch;
-  int64_t n_cached;
-  int n_new, n_q_heads;
-  const __nv_bfloat16* q;  // [batch][n_new][n_q_heads][D]
-  float scale_log2;
-  float* out;              // [batch][n_new][n_q_heads][D]
-  float* lse;              // [batch][n_new][n_q_heads]
-  int32_t* flag;
-};
 
 template <int D>
 struct PCfg {
@@ -301,18 +289,22 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       tmem_ld32(row_tmem + 0, sv[0]);
       tmem_ld32(row_tmem + 32, sv[1]);
       tmem_ld_wait();
+      // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
+      const int64_t rel = row_valid ? row_limit - j0 + 1 : 0;
+      const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
+      const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
       float x[C::NKV];
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < C::NKV; ++j) {
-        const bool vis = row_valid && (j0 + j <= row_limit);
-        x[j] = vis ? __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2 : -INFINITY;
+        const float v = __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2;
+        x[j] = (all_vis || j < nvis) ? v : -INFINITY;
         mt = fmaxf(mt, x[j]);
       }
       const float m_new = fmaxf(m_used, mt);
       const bool need = (m_new > m_used + 4.0f);  // also true when m_used is -inf and a key is visible
       if (__any_sync(0xffffffffu, need)) {
-        const float f = need ? ((m_used == -INFINITY) ? 0.0f : exp2f(m_used - m_new)) : 1.0f;
+        const float f = need ? ((m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - m_new)) : 1.0f;
         if (step > 0) {
           // Rescale O in TMEM (initialised by the first P.V) and the register tail.
 #pragma unroll 1
@@ -331,14 +323,19 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         l_sum *= f;
         if (need) m_used = m_new;
       }
+      // With no visible key so far m_used is -inf and every x is -inf: all p are 0.
+      const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
       float ps = 0.0f;
       uint32_t pw[C::NKV / 2];
+      const float4* n4 = reinterpret_cast<const float4*>(sNorm);
 #pragma unroll
-      for (int j = 0; j < C::NKV; j += 2) {
-        const float p0 = (x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - m_used);
-        const float p1 = (x[j + 1] == -INFINITY) ? 0.0f : exp2f(x[j + 1] - m_used);
-        ps += p0 + p1;
-        pw[j / 2] = pack_half2(p0 * sNorm[j], p1 * sNorm[j + 1]);
+      for (int j = 0; j < C::NKV; j += 4) {
+        const float4 nn = n4[j / 4];
+        const float p0 = fast_exp2(x[j] - mref), p1 = fast_exp2(x[j + 1] - mref);
+        const float p2 = fast_exp2(x[j + 2] - mref), p3 = fast_exp2(x[j + 3] - mref);
+        ps += (p0 + p1) + (p2 + p3);
+        pw[j / 2] = pack_half2(p0 * nn.x, p1 * nn.y);
+        pw[j / 2 + 1] = pack_half2(p2 * nn.z, p3 * nn.w);
       }
       l_sum += ps;
 #pragma unroll

@@ -50,6 +50,11 @@ __device__ __forceinline__ void raise_flag(int32_t* flag, int32_t code) {
 // Bound for every wait on an asynchronous event: 2 s of wall time.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Barrier over `threads` threads (whole warps) of the CTA, id 1..15.
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // --------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

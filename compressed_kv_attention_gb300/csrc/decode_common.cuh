@@ -93,10 +93,6 @@ __device__ __forceinline__ void softmax_tile(const float (&S)[4], bool valid0, b
   pb1 = movmatrix_trans(X1);
 }
 
-__device__ __forceinline__ void named_bar(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // Sum the two warps' partial S of a shared tile (D = 512). Both warps end
 // with the same values (IEEE addition is commutative).
 __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int group, int wh,
