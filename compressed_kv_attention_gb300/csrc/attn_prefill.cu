@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
                             {C::OT, C::OR, 0}};
 
   // Codes of a step are fetched into registers one step ahead, so their
-  // global-memory latency overlaps the previous step's MMAs and softmax.
+  // global-memory latency overlaps the rest of the previous step.
   //  K: thread t owns token kp = t % NKV and the 32-dim blocks kb0 + KBS * c;
   //     a warp covers 32 consecutive tokens of one block, so its fp16 stores
   //     into the swizzled tile fall on distinct bank groups.
@@ -224,6 +224,25 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   };
   if (n_steps > 0) fetch(0);
 
+  // C^T (centroids, rotated basis): rows = dims, K = tokens. A 6-bit field
+  // pairs the codes of two adjacent positions of one dim, which is one fp16x2
+  // word of C^T: one shared table load per field (v_field), one store (v_store).
+  const uint32_t v_lut = smem_u32(sLut) + (uint32_t)(lane << 2);
+  const int v_g = vL >> 2, v_tok0 = vr4 * 16 + 2 * (vL & 3);
+  auto v_field = [&](const uint32_t (&vc)[NW], int pi) -> uint32_t {
+    const int bit = 6 * pi;
+    const int wi = bit >> 5, sh = bit & 31;
+    uint32_t f = vc[wi] >> sh;
+    if (sh > 26 && wi + 1 < NW) f |= vc[wi + 1] << (32 - sh);
+    return lds32(v_lut + ((f & 63u) << 7));
+  };
+  auto v_store = [&](int pi, uint32_t val) {
+    const int mt = pi >> 2, rh = pi & 1, h2 = (pi >> 1) & 1;
+    const int dim = G * v_g + 2 * mt + rh;
+    const int tok = v_tok0 + 8 * h2;  // even position; the odd one follows it in K
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(sKV) + sw128_offset(dim, tok, D)), "r"(val));
+  };
+
   for (int step = 0; step < n_steps; ++step) {
     const int64_t j0 = (int64_t)step * C::NKV;
     // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
@@ -255,7 +274,6 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     uint32_t vcur[NW];
 #pragma unroll
     for (int s4 = 0; s4 < NW; ++s4) vcur[s4] = vw[s4];
-    if (step + 1 < n_steps) fetch(step + 1);
     sync_for_mma();
     if (tid == 0) {
       // First pass of S overwrites the accumulator (columns [0, 64)).
@@ -266,6 +284,10 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       }
       umma_commit(&s_bar);
     }
+    // The next step's loads are issued while the tensor core runs this pass;
+    // warp 0, whose MMA issue blocks until the pass drains, loads during the
+    // second pass instead (its softmax has slack against the value build).
+    if (warp != 0 && step + 1 < n_steps) fetch(step + 1);
     wait_mma();
     // ---- lo pass ----
 #pragma unroll
@@ -281,6 +303,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       issue_s();
       umma_commit(&s_bar);
     }
+    if (warp == 0 && step + 1 < n_steps) fetch(step + 1);
     wait_mma();
 
     if (softmax_warp) {
@@ -343,24 +366,17 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * c, C::M)) =
             make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
     } else {
-      // ---- C^T (centroids, rotated basis) for the step: rows = dims, K = tokens ----
-      // A 6-bit field pairs the codes of two adjacent positions of one dim,
-      // which is one fp16x2 word of C^T: one shared table load per field.
-      const int g = vL >> 2, tq = vL & 3;
-      const uint32_t lut = smem_u32(sLut) + (uint32_t)(lane << 2);
-      const uint32_t kvb = smem_u32(sKV);
-      const int tok0 = vr4 * 16 + 2 * tq;
+      // ---- C^T for the step ----
+      // Table loads are issued in batches ahead of their stores, so one
+      // shared-memory latency is exposed per batch rather than per field.
+      constexpr int VB = 16;
 #pragma unroll
-      for (int pi = 0; pi < 2 * G; ++pi) {
-        const int bit = 6 * pi;
-        const int wi = bit >> 5, sh = bit & 31;
-        uint32_t f = vcur[wi] >> sh;
-        if (sh > 26 && wi + 1 < NW) f |= vcur[wi + 1] << (32 - sh);
-        const uint32_t val = lds32(lut + ((f & 63u) << 7));
-        const int mt = pi >> 2, rh = pi & 1, h2 = (pi >> 1) & 1;
-        const int dim = G * g + 2 * mt + rh;
-        const int tok = tok0 + 8 * h2;  // even position; the odd one follows it in K
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(kvb + sw128_offset(dim, tok, D)), "r"(val) : "memory");
+      for (int pb = 0; pb < 2 * G; pb += VB) {
+        uint32_t val[VB];
+#pragma unroll
+        for (int u = 0; u < VB; ++u) val[u] = v_field(vcur, pb + u);
+#pragma unroll
+        for (int u = 0; u < VB; ++u) v_store(pb + u, val[u]);
       }
     }
     sync_for_mma();
