@@ -26,6 +26,8 @@
 // cache).
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "../../include/ckv.h"
 #include "ckv_kernels.cuh"
 #include "prefill_common.cuh"
@@ -50,7 +52,8 @@ struct PCfg {
   static constexpr int P_OFF = KV_OFF + NKV * D * 2;
   static constexpr int NORM_OFF = P_OFF + M * NKV * 2;
   static constexpr int LUT_OFF = NORM_OFF + NKV * 4;        // 64 centroid pairs x 32 lanes
-  static constexpr int BYTES = LUT_OFF + 64 * 32 * 4;
+  static constexpr int SCALE_OFF = LUT_OFF + 64 * 32 * 4; // two steps' q8_0 scales
+  static constexpr int BYTES = SCALE_OFF + 2 * NKV * NB * 2;
   // At least half the SM's shared memory, so that one CTA (and its 512 TMEM
   // columns) owns each SM.
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);
@@ -81,6 +84,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   uint8_t* sP = smem + C::P_OFF;
   float* sNorm = reinterpret_cast<float*>(smem + C::NORM_OFF);
   uint32_t* sLut = reinterpret_cast<uint32_t*>(smem + C::LUT_OFF);
+  __half* sScale = reinterpret_cast<__half*>(smem + C::SCALE_OFF);
 
   const int group_q = a.n_q_heads / a.n_kv_heads;
   const int QT = C::M / group_q;                   // query tokens per CTA
@@ -135,10 +139,6 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   const int row_qi = q0 + row / group_q;
   const bool row_valid = row_qi < a.n_new;
   const int64_t row_limit = a.n_cached + row_qi;  // last key this row sees
-  float m_used = -INFINITY, l_sum = 0.0f;
-  float otail[C::OR > 0 ? C::OR : 1];
-#pragma unroll
-  for (int i = 0; i < (C::OR > 0 ? C::OR : 1); ++i) otail[i] = 0.0f;
   const uint32_t row_tmem = tmem + ((uint32_t)(warp & 3) * 32u << 16);
 
   uint32_t phase = 0;
@@ -171,58 +171,85 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
 
   // Codes of a step are fetched into registers one step ahead, so their
   // global-memory latency overlaps the rest of the previous step.
-  //  K: thread t owns token kp = t % NKV and the 32-dim blocks kb0 + KBS * c;
-  //     a warp covers 32 consecutive tokens of one block, so its fp16 stores
-  //     into the swizzled tile fall on distinct bank groups.
+  //  K: the step's 4 records hold 4D 16-byte code chunks; round r of warp w
+  //     loads chunks [256r + 32w, +32), one (record, 32-dim block) with its
+  //     32 lanes L, 512 contiguous bytes. Lane l takes L = 4 (l & 7) + (l >> 3):
+  //     the chunk holds 8 dims of tokens l & 7 and (l & 7) + 8, and a quarter
+  //     warp (fixed l >> 3) then stores 8 rows of one swizzle column, which
+  //     land on distinct bank groups. The scales go to shared memory.
   //  V: threads 128..255; warp w takes lane streams [8w, 8w + 8) of the
   //     step's 4 records (lane = 8 * record + stream), which spreads one
   //     store instruction over 16 banks.
   constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D), NW = LB / 4;
-  constexpr int KBS = C::THREADS / C::NKV;  // blocks between a thread's pieces
-  constexpr int KPT = C::NB / KBS;          // blocks (pieces) per thread
-  const int kp = tid % C::NKV, kb0 = tid / C::NKV;
+  constexpr int KR = 4 * D / C::THREADS;    // code chunks per thread per step
+  constexpr int NSW = C::NKV * C::NB / 4;   // 8-byte scale words per step
+  static_assert(NSW <= C::THREADS, "one scale word per thread");
+  const int kq = lane >> 3, kpp = lane & 7;
   const int vu = tid - 128, vr4 = (vu & 31) >> 3, vL = 8 * (vu >> 5) + (vu & 7);
-  uint2 kw[KPT][4];
-  __half kd[KPT];
-  uint32_t vw[NW];
+  uint4 kw[KR];
+  uint2 ksc = make_uint2(0, 0);
   float nrm = 0.0f;
   auto fetch = [&](int step) {
-    const int64_t j0 = (int64_t)step * C::NKV;
-    {
-      const int64_t tpos = j0 + kp;
-      const int64_t rec = tpos / kTile;
-      const int pp = static_cast<int>(tpos % kTile);
-      const bool have = rec < n_rec;
-      const uint8_t* rb = stream + rec * C::REC;
+    const int64_t rec0 = (int64_t)step * (C::NKV / kTile);
 #pragma unroll
-      for (int c = 0; c < KPT; ++c) {
-        const int blk = kb0 + KBS * c;
-        kd[c] = have ? *reinterpret_cast<const __half*>(rb + k_scale_offset(D) + 2 * (pp * C::NB + blk))
-                     : __ushort_as_half(0);
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          kw[c][t] = have ? *reinterpret_cast<const uint2*>(rb + (blk * 32 + 4 * (pp & 7) + t) * 16 + (pp >> 3) * 8)
-                          : make_uint2(0, 0);
-      }
+    for (int r = 0; r < KR; ++r) {
+      const int g = r * C::THREADS + warp * 32;
+      const int64_t rec = rec0 + g / D;
+      const int blk = (g % D) / 32;
+      kw[r] = rec < n_rec ? *reinterpret_cast<const uint4*>(stream + rec * C::REC + (blk * 32 + 4 * kpp + kq) * 16)
+                          : make_uint4(0, 0, 0, 0);
     }
-    if (!softmax_warp) {
-      const int64_t rec = j0 / kTile + vr4;
-      const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
-#pragma unroll
-      for (int s4 = 0; s4 < NW; ++s4) {
-        const int sbyte = s4 * 4;
-        vw[s4] = (rec < n_rec) ? *reinterpret_cast<const uint32_t*>(vb + ((sbyte / GR) * 32 + vL) * GR + (sbyte % GR))
-                               : 0u;
-      }
+    if (tid < NSW) {
+      const int h0 = tid * 4;  // first of the word's 4 scales, [record][token][block] order
+      const int64_t rec = rec0 + h0 / (kTile * C::NB);
+      ksc = rec < n_rec ? *reinterpret_cast<const uint2*>(stream + rec * C::REC + k_scale_offset(D) +
+                                                          2 * (h0 % (kTile * C::NB)))
+                        : make_uint2(0, 0);
     }
     if (tid < C::NKV) {
-      const int64_t rec = (j0 + tid) / kTile;
+      const int64_t rec = rec0 + tid / kTile;
       nrm = (rec < n_rec) ? __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D) +
-                                                                          2 * ((j0 + tid) % kTile)))
+                                                                          2 * (tid % kTile)))
                           : 0.0f;
     }
   };
-  if (n_steps > 0) fetch(0);
+  // V codes of a step (value warps), loaded once the previous step's build
+  // has consumed them.
+  auto fetch_v = [&](uint32_t (&vw)[NW], int step) {
+    const int64_t rec0 = (int64_t)step * (C::NKV / kTile);
+    {
+      const int64_t rec = rec0 + vr4;
+      const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
+      if constexpr (GR == 16) {
+#pragma unroll
+        for (int k = 0; k < NW / 4; ++k) {
+          const uint4 v = (rec < n_rec) ? *reinterpret_cast<const uint4*>(vb + (k * 32 + vL) * 16)
+                                        : make_uint4(0, 0, 0, 0);
+          vw[4 * k] = v.x;
+          vw[4 * k + 1] = v.y;
+          vw[4 * k + 2] = v.z;
+          vw[4 * k + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int s4 = 0; s4 < NW; ++s4) {
+          const int sbyte = s4 * 4;
+          vw[s4] = (rec < n_rec)
+                       ? *reinterpret_cast<const uint32_t*>(vb + ((sbyte / GR) * 32 + vL) * GR + (sbyte % GR))
+                       : 0u;
+        }
+      }
+    }
+  };
+  // Scales of a fetched step into buffer `buf` (read after the next barrier).
+  auto put_scales = [&](int buf) {
+    if (tid < NSW) *reinterpret_cast<uint2*>(sScale + buf * C::NKV * C::NB + tid * 4) = ksc;
+  };
+  if (n_steps > 0) {
+    fetch(0);
+    put_scales(0);
+  }
+  __syncthreads();
 
   // C^T (centroids, rotated basis): rows = dims, K = tokens. A 6-bit field
   // pairs the codes of two adjacent positions of one dim, which is one fp16x2
@@ -243,203 +270,227 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(sKV) + sw128_offset(dim, tok, D)), "r"(val));
   };
 
-  for (int step = 0; step < n_steps; ++step) {
-    const int64_t j0 = (int64_t)step * C::NKV;
-    // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
-    // q is an exact fp16 integer; hi = q*d rounded once (HMUL2 of exact fp16
-    // operands) and lo = fma(q, d, -hi), the exact residual (HFMA2).
-    uint32_t lo_keep[KPT][4][4];
+  // The two roles run the same barriers and MMA waits; each role's state
+  // (the softmax rows' running max, sum and register tail; the value warps'
+  // code words) exists only on its own path.
+  auto role_loop = [&](auto role) {
+    constexpr bool SM = decltype(role)::value;  // softmax warps (rows) or value warps
+    float m_used = -INFINITY, l_sum = 0.0f;
+    float otail[SM && C::OR > 0 ? C::OR : 1];
 #pragma unroll
-    for (int c = 0; c < KPT; ++c) {
-      const int blk = kb0 + KBS * c;
-      const __half2 dd = __halves2half2(kd[c], kd[c]);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        uint32_t qh[4], hi[4];
-        i8x4_to_half2x2(kw[c][t].x, qh[0], qh[1]);
-        i8x4_to_half2x2(kw[c][t].y, qh[2], qh[3]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half2 qv = *reinterpret_cast<const __half2*>(&qh[e]);
-          const __half2 h = __hmul2(qv, dd);
-          const __half2 l = __hfma2(qv, dd, __hneg2(h));
-          hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-          lo_keep[c][t][e] = *reinterpret_cast<const uint32_t*>(&l);
-        }
-        *reinterpret_cast<uint4*>(sKV + sw128_offset(kp, blk * 32 + 8 * t, C::NKV)) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      }
+    for (int i = 0; i < (SM && C::OR > 0 ? C::OR : 1); ++i) otail[i] = 0.0f;
+    uint32_t vw[SM ? 1 : NW];
+    if constexpr (!SM) {
+      if (n_steps > 0) fetch_v(vw, 0);
     }
-    if (tid < C::NKV) sNorm[tid] = nrm;
-    uint32_t vcur[NW];
-#pragma unroll
-    for (int s4 = 0; s4 < NW; ++s4) vcur[s4] = vw[s4];
-    sync_for_mma();
-    if (tid == 0) {
-      // First pass of S overwrites the accumulator (columns [0, 64)).
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * (C::M * 128) + (ks & 3) * 32);
-        const uint64_t bd = umma_desc_sw128(kv_base + (ks >> 2) * (C::NKV * 128) + (ks & 3) * 32);
-        umma_f16(tmem, ad, bd, umma_idesc_f16_f32(C::M, C::NKV), ks > 0);
-      }
-      umma_commit(&s_bar);
-    }
-    // The next step's loads are issued while the tensor core runs this pass;
-    // warp 0, whose MMA issue blocks until the pass drains, loads during the
-    // second pass instead (its softmax has slack against the value build).
-    if (warp != 0 && step + 1 < n_steps) fetch(step + 1);
-    wait_mma();
-    // ---- lo pass ----
-#pragma unroll
-    for (int c = 0; c < KPT; ++c) {
-      const int blk = kb0 + KBS * c;
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        *reinterpret_cast<uint4*>(sKV + sw128_offset(kp, blk * 32 + 8 * t, C::NKV)) =
-            make_uint4(lo_keep[c][t][0], lo_keep[c][t][1], lo_keep[c][t][2], lo_keep[c][t][3]);
-    }
-    sync_for_mma();
-    if (tid == 0) {
-      issue_s();
-      umma_commit(&s_bar);
-    }
-    if (warp == 0 && step + 1 < n_steps) fetch(step + 1);
-    wait_mma();
-
-    if (softmax_warp) {
-      // ---- online softmax of this step's 64 columns, one row per thread ----
-      uint32_t sv[2][32];
-      tmem_ld32(row_tmem + 0, sv[0]);
-      tmem_ld32(row_tmem + 32, sv[1]);
-      tmem_ld_wait();
-      // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
-      const int64_t rel = row_valid ? row_limit - j0 + 1 : 0;
-      const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
-      const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
-      float x[C::NKV];
-      float mt = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < C::NKV; ++j) {
-        const float v = __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2;
-        x[j] = (all_vis || j < nvis) ? v : -INFINITY;
-        mt = fmaxf(mt, x[j]);
-      }
-      const float m_new = fmaxf(m_used, mt);
-      const bool need = (m_new > m_used + 4.0f);  // also true when m_used is -inf and a key is visible
-      if (__any_sync(0xffffffffu, need)) {
-        const float f = need ? ((m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - m_new)) : 1.0f;
-        if (step > 0) {
-          // Rescale O in TMEM (initialised by the first P.V) and the register tail.
-#pragma unroll 1
-          for (int c0 = 64; c0 < 64 + C::OT; c0 += 32) {
-            uint32_t ov[32];
-            tmem_ld32(row_tmem + c0, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-            tmem_st32(row_tmem + c0, ov);
+    for (int step = 0; step < n_steps; ++step) {
+      const int64_t j0 = (int64_t)step * C::NKV;
+      // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
+      // q is an exact fp16 integer; hi = q*d rounded once (HMUL2 of exact fp16
+      // operands) and lo = fma(q, d, -hi), the exact residual (HFMA2).
+      uint32_t lo_keep[KR][8];
+      const __half* scb = sScale + (step & 1) * C::NKV * C::NB;
+  #pragma unroll
+      for (int r = 0; r < KR; ++r) {
+        const int g = r * C::THREADS + warp * 32;
+        const int blk = (g % D) / 32;
+        const int row0 = (g / D) * kTile + kpp;  // tokens row0 and row0 + 8 of the step
+        const uint32_t w[4] = {kw[r].x, kw[r].y, kw[r].z, kw[r].w};
+  #pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const __half d = scb[(row0 + 8 * hs) * C::NB + blk];
+          const __half2 dd = __halves2half2(d, d);
+          uint32_t qh[4], hi[4];
+          i8x4_to_half2x2(w[2 * hs], qh[0], qh[1]);
+          i8x4_to_half2x2(w[2 * hs + 1], qh[2], qh[3]);
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 qv = *reinterpret_cast<const __half2*>(&qh[e]);
+            const __half2 h = __hmul2(qv, dd);
+            const __half2 l = __hfma2(qv, dd, __hneg2(h));
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+            lo_keep[r][4 * hs + e] = *reinterpret_cast<const uint32_t*>(&l);
           }
-          tmem_st_wait();
-        }
-#pragma unroll
-        for (int i = 0; i < C::OR; ++i) otail[i] *= f;
-        l_sum *= f;
-        if (need) m_used = m_new;
-      }
-      // With no visible key so far m_used is -inf and every x is -inf: all p are 0.
-      const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
-      float ps = 0.0f;
-      uint32_t pw[C::NKV / 2];
-      const float4* n4 = reinterpret_cast<const float4*>(sNorm);
-#pragma unroll
-      for (int j = 0; j < C::NKV; j += 4) {
-        const float4 nn = n4[j / 4];
-        const float p0 = fast_exp2(x[j] - mref), p1 = fast_exp2(x[j + 1] - mref);
-        const float p2 = fast_exp2(x[j + 2] - mref), p3 = fast_exp2(x[j + 3] - mref);
-        ps += (p0 + p1) + (p2 + p3);
-        pw[j / 2] = pack_half2(p0 * nn.x, p1 * nn.y);
-        pw[j / 2 + 1] = pack_half2(p2 * nn.z, p3 * nn.w);
-      }
-      l_sum += ps;
-#pragma unroll
-      for (int c = 0; c < C::NKV / 8; ++c)
-        *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * c, C::M)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-    } else {
-      // ---- C^T for the step ----
-      // Table loads are issued in batches ahead of their stores, so one
-      // shared-memory latency is exposed per batch rather than per field.
-      constexpr int VB = 16;
-#pragma unroll
-      for (int pb = 0; pb < 2 * G; pb += VB) {
-        uint32_t val[VB];
-#pragma unroll
-        for (int u = 0; u < VB; ++u) val[u] = v_field(vcur, pb + u);
-#pragma unroll
-        for (int u = 0; u < VB; ++u) v_store(pb + u, val[u]);
-      }
-    }
-    sync_for_mma();
-    if (tid == 0) {
-      // ---- O += P' C over the step's 64 tokens ----
-      for (int ks = 0; ks < C::NKV / 16; ++ks) {
-        const uint64_t ad = umma_desc_sw128(p_base + ks * 32);
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          if (chunks[c].n == 0) continue;
-          const uint64_t bd = umma_desc_sw128(kv_base + chunks[c].dim0 * 128 + ks * 32);
-          const bool acc = (c == 2) ? (ks > 0) : (step > 0 || ks > 0);
-          umma_f16(tmem + chunks[c].col, ad, bd, umma_idesc_f16_f32(C::M, chunks[c].n), acc);
+          *reinterpret_cast<uint4*>(sKV + sw128_offset(row0 + 8 * hs, blk * 32 + 8 * kq, C::NKV)) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
       }
-      umma_commit(&s_bar);
-    }
-    wait_mma();
-    if (C::OR > 0 && softmax_warp) {
-      uint32_t tv[2][32];
-      tmem_ld32(row_tmem + 0, tv[0]);
-      tmem_ld32(row_tmem + 32, tv[1]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < C::OR; ++i) otail[i] += __uint_as_float(tv[i >> 5][i & 31]);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  }
+      if (tid < C::NKV) sNorm[tid] = nrm;
+      sync_for_mma();
+      if (SM && tid == 0) {
+        // First pass of S overwrites the accumulator (columns [0, 64)).
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * (C::M * 128) + (ks & 3) * 32);
+          const uint64_t bd = umma_desc_sw128(kv_base + (ks >> 2) * (C::NKV * 128) + (ks & 3) * 32);
+          umma_f16(tmem, ad, bd, umma_idesc_f16_f32(C::M, C::NKV), ks > 0);
+        }
+        umma_commit(&s_bar);
+      }
+      // The next step's loads are issued while the tensor core runs this pass;
+      // warp 0, whose MMA issue blocks until the pass drains, loads during the
+      // second pass instead (its softmax has slack against the value build).
+      if (warp != 0 && step + 1 < n_steps) fetch(step + 1);
+      wait_mma();
+      // ---- lo pass ----
+  #pragma unroll
+      for (int r = 0; r < KR; ++r) {
+        const int g = r * C::THREADS + warp * 32;
+        const int blk = (g % D) / 32;
+        const int row0 = (g / D) * kTile + kpp;
+  #pragma unroll
+        for (int hs = 0; hs < 2; ++hs)
+          *reinterpret_cast<uint4*>(sKV + sw128_offset(row0 + 8 * hs, blk * 32 + 8 * kq, C::NKV)) =
+              make_uint4(lo_keep[r][4 * hs], lo_keep[r][4 * hs + 1], lo_keep[r][4 * hs + 2], lo_keep[r][4 * hs + 3]);
+      }
+      sync_for_mma();
+      if (SM && tid == 0) {
+        issue_s();
+        umma_commit(&s_bar);
+      }
+      if (warp == 0 && step + 1 < n_steps) fetch(step + 1);
+      wait_mma();
+      if (step + 1 < n_steps) put_scales((step + 1) & 1);  // read after this step's last barrier
 
-  // ---- normalise and write the rotated-basis rows; lse ----
-  if (softmax_warp) {
-    const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
-    const int h = kvh * group_q + row % group_q;
-    float* orow = a.out + (((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h) * D;
-#pragma unroll 1
-    for (int c0 = 0; c0 < C::OT; c0 += 32) {
-      uint32_t ov[32];
-      if (n_steps > 0) {
-        tmem_ld32(row_tmem + 64 + c0, ov);
+      if constexpr (SM) {
+        // ---- online softmax of this step's 64 columns, one row per thread ----
+        uint32_t sv[2][32];
+        tmem_ld32(row_tmem + 0, sv[0]);
+        tmem_ld32(row_tmem + 32, sv[1]);
         tmem_ld_wait();
+        // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
+        const int64_t rel = row_valid ? row_limit - j0 + 1 : 0;
+        const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
+        const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
+        float x[C::NKV];
+        float mt = -INFINITY;
+  #pragma unroll
+        for (int j = 0; j < C::NKV; ++j) {
+          const float v = __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2;
+          x[j] = (all_vis || j < nvis) ? v : -INFINITY;
+          mt = fmaxf(mt, x[j]);
+        }
+        const float m_new = fmaxf(m_used, mt);
+        const bool need = (m_new > m_used + 4.0f);  // also true when m_used is -inf and a key is visible
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? ((m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - m_new)) : 1.0f;
+          if (step > 0) {
+            // Rescale O in TMEM (initialised by the first P.V) and the register tail.
+  #pragma unroll 1
+            for (int c0 = 64; c0 < 64 + C::OT; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld32(row_tmem + c0, ov);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+              tmem_st32(row_tmem + c0, ov);
+            }
+            tmem_st_wait();
+          }
+  #pragma unroll
+          for (int i = 0; i < C::OR; ++i) otail[i] *= f;
+          l_sum *= f;
+          if (need) m_used = m_new;
+        }
+        // With no visible key so far m_used is -inf and every x is -inf: all p are 0.
+        const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
+        float ps = 0.0f;
+        uint32_t pw[C::NKV / 2];
+        const float4* n4 = reinterpret_cast<const float4*>(sNorm);
+  #pragma unroll
+        for (int j = 0; j < C::NKV; j += 4) {
+          const float4 nn = n4[j / 4];
+          const float p0 = fast_exp2(x[j] - mref), p1 = fast_exp2(x[j + 1] - mref);
+          const float p2 = fast_exp2(x[j + 2] - mref), p3 = fast_exp2(x[j + 3] - mref);
+          ps += (p0 + p1) + (p2 + p3);
+          pw[j / 2] = pack_half2(p0 * nn.x, p1 * nn.y);
+          pw[j / 2 + 1] = pack_half2(p2 * nn.z, p3 * nn.w);
+        }
+        l_sum += ps;
+  #pragma unroll
+        for (int c = 0; c < C::NKV / 8; ++c)
+          *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * c, C::M)) =
+              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        // ---- C^T for the step ----
+        // Table loads are issued in batches ahead of their stores, so one
+        // shared-memory latency is exposed per batch rather than per field.
+        constexpr int VB = 16;
+  #pragma unroll
+        for (int pb = 0; pb < 2 * G; pb += VB) {
+          uint32_t val[VB];
+  #pragma unroll
+          for (int u = 0; u < VB; ++u) val[u] = v_field(vw, pb + u);
+  #pragma unroll
+          for (int u = 0; u < VB; ++u) v_store(pb + u, val[u]);
+        }
+        if (step + 1 < n_steps) fetch_v(vw, step + 1);
+      }
+      sync_for_mma();
+      if (SM && tid == 0) {
+        // ---- O += P' C over the step's 64 tokens ----
+        for (int ks = 0; ks < C::NKV / 16; ++ks) {
+          const uint64_t ad = umma_desc_sw128(p_base + ks * 32);
+  #pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            if (chunks[c].n == 0) continue;
+            const uint64_t bd = umma_desc_sw128(kv_base + chunks[c].dim0 * 128 + ks * 32);
+            const bool acc = (c == 2) ? (ks > 0) : (step > 0 || ks > 0);
+            umma_f16(tmem + chunks[c].col, ad, bd, umma_idesc_f16_f32(C::M, chunks[c].n), acc);
+          }
+        }
+        umma_commit(&s_bar);
+      }
+      wait_mma();
+      if constexpr (SM && C::OR > 0) {
+        uint32_t tv[2][32];
+        tmem_ld32(row_tmem + 0, tv[0]);
+        tmem_ld32(row_tmem + 32, tv[1]);
+        tmem_ld_wait();
+  #pragma unroll
+        for (int i = 0; i < C::OR; ++i) otail[i] += __uint_as_float(tv[i >> 5][i & 31]);
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+
+    // ---- normalise and write the rotated-basis rows; lse ----
+    if constexpr (SM) {
+      const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
+      const int h = kvh * group_q + row % group_q;
+      float* orow = a.out + (((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h) * D;
+  #pragma unroll 1
+      for (int c0 = 0; c0 < C::OT; c0 += 32) {
+        uint32_t ov[32];
+        if (n_steps > 0) {
+          tmem_ld32(row_tmem + 64 + c0, ov);
+          tmem_ld_wait();
+        } else {
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
+        if (row_valid) {
+  #pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(orow + c0 + i) =
+                make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                            __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+        }
       }
       if (row_valid) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(orow + c0 + i) =
-              make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                          __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+  #pragma unroll
+        for (int i = 0; i < C::OR; i += 4)
+          *reinterpret_cast<float4*>(orow + C::OT + i) =
+              make_float4(otail[i] * inv, otail[i + 1] * inv, otail[i + 2] * inv, otail[i + 3] * inv);
+        a.lse[((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h] =
+            l_sum > 0.0f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
       }
     }
-    if (row_valid) {
-#pragma unroll
-      for (int i = 0; i < C::OR; i += 4)
-        *reinterpret_cast<float4*>(orow + C::OT + i) =
-            make_float4(otail[i] * inv, otail[i + 1] * inv, otail[i + 2] * inv, otail[i + 3] * inv);
-      a.lse[((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h] =
-          l_sum > 0.0f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
-    }
-  }
+  };
+  if (softmax_warp)
+    role_loop(std::true_type{});
+  else
+    role_loop(std::false_type{});
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
