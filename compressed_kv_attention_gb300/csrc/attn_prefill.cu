@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D), NW = LB / 4;
   constexpr int KR = 4 * D / C::THREADS;    // code chunks per thread per step
   constexpr int NSW = C::NKV * C::NB / 4;   // 8-byte scale words per step
+  constexpr int VPRE = G;                   // value fields whose table loads overlap the second S pass
   static_assert(NSW <= C::THREADS, "one scale word per thread");
   const int kq = lane >> 3, kpp = lane & 7;
   const int vu = tid - 128, vr4 = (vu & 31) >> 3, vL = 8 * (vu >> 5) + (vu & 7);
@@ -348,6 +349,13 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         umma_commit(&s_bar);
       }
       if (warp == 0 && step + 1 < n_steps) fetch(step + 1);
+      // While the second pass runs, the value warps load the table entries of
+      // their first VPRE fields (the stores wait for the K tile to free).
+      uint32_t vpre[SM ? 1 : VPRE];
+      if constexpr (!SM) {
+#pragma unroll
+        for (int u = 0; u < VPRE; ++u) vpre[u] = v_field(vw, u);
+      }
       wait_mma();
       if (step + 1 < n_steps) put_scales((step + 1) & 1);  // read after this step's last barrier
 
@@ -411,12 +419,14 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
           *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * c, C::M)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       } else {
-        // ---- C^T for the step ----
+        // ---- C^T for the step: the prefetched fields, then the rest ----
+#pragma unroll
+        for (int u = 0; u < VPRE; ++u) v_store(u, vpre[u]);
         // Table loads are issued in batches ahead of their stores, so one
         // shared-memory latency is exposed per batch rather than per field.
-        constexpr int VB = 16;
+        constexpr int VB = G < 16 ? G : 16;  // divides the G fields left
   #pragma unroll
-        for (int pb = 0; pb < 2 * G; pb += VB) {
+        for (int pb = VPRE; pb < 2 * G; pb += VB) {
           uint32_t val[VB];
   #pragma unroll
           for (int u = 0; u < VB; ++u) val[u] = v_field(vw, pb + u);
@@ -568,11 +578,12 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
                                     int32_t n_q_heads, const void* k_new_f16, const void* v_new_f16, float scale,
                                     float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
   if (!cache) return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "cache is null"));
-  if (cache->head_dim != 512 && cache->head_dim != 256 && cache->head_dim != 128)
-    return static_cast<ckv_status>(
-        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill supports head_dim 128, 256, 512 (got %d)", cache->head_dim));
   if (n_new < 0 || n_cached < 0 || n_cached + n_new > cache->capacity || cache->capacity % 16)
     return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "token range outside the cache"));
+  if (cache->head_dim != 64 && cache->head_dim != 128 && cache->head_dim != 256 && cache->head_dim != 512)
+    return static_cast<ckv_status>(
+        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill supports head_dim 64, 128, 256, 512 (got %d)",
+                            static_cast<int>(cache->head_dim)));
   if (n_q_heads <= 0 || cache->n_kv_heads <= 0 || n_q_heads % cache->n_kv_heads ||
       128 % (n_q_heads / cache->n_kv_heads))
     return static_cast<ckv_status>(
@@ -608,9 +619,13 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
   a.lse = lse;
   a.flag = static_cast<int32_t*>(workspace);
   switch (cache->head_dim) {
+    case 64: e = ckv::launch_prefill_d<64>(a, cache->v_signs, st); break;
     case 128: e = ckv::launch_prefill_d<128>(a, cache->v_signs, st); break;
     case 256: e = ckv::launch_prefill_d<256>(a, cache->v_signs, st); break;
-    default: e = ckv::launch_prefill_d<512>(a, cache->v_signs, st); break;
+    case 512: e = ckv::launch_prefill_d<512>(a, cache->v_signs, st); break;
+    default:
+      return static_cast<ckv_status>(
+          ckv::set_last_error(CKV_ERR_UNSUPPORTED, "head_dim %d", static_cast<int>(cache->head_dim)));
   }
   if (e != cudaSuccess)
     return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e)));

@@ -121,7 +121,7 @@ def test_prefill_argument_checks(lib):
         lib.ckv_attn_prefill(ctypes.byref(cache) if cache is not None else None, n_cached, q, n_new, hq, k, v,
                              0.04, out, lse, w, wb, None)
     assert call(cache=None) == -1
-    assert call(cache=_fake_cache(D=64)) == -2       # prefill head dims: 128, 256, 512
+    assert call(cache=_fake_cache(D=32)) == -2       # prefill head dims: 64, 128, 256, 512
     assert call(n_cached=4090) == -1                 # past capacity
     assert call(hq=12) == -2                         # 6 heads per kv head does not divide 128
     assert call(q=fake + 8) == -1

@@ -63,7 +63,8 @@ def _oracle(k, v, qf, signs, n_cached, b, rows=None):
 
 
 @pytest.mark.parametrize("D,Hkv,Hq,n_cached,n_new", [(128, 2, 16, 100, 37), (256, 1, 4, 64, 80),
-                                                     (512, 2, 16, 131, 45), (512, 1, 8, 0, 20)])
+                                                     (512, 2, 16, 131, 45), (512, 1, 8, 0, 20),
+                                                     (64, 1, 4, 50, 33)])
 def test_prefill_small(D, Hkv, Hq, n_cached, n_new):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
