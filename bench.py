@@ -183,12 +183,12 @@ class DecodeWork:
             del k, v
             self.out = torch.empty((B, 1, Hq, D), dtype=torch.float32, device=dev)
             self.lse = torch.empty((B, 1, Hq), dtype=torch.float32, device=dev)
-            self.ws = torch.empty(ckv.attn_decode_workspace(self.caches[0], T, 1, Hq), dtype=torch.uint8,
+            self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], T, 1, Hq), dtype=torch.uint8,
                                   device=dev)
             self.seq = torch.full((B,), T, dtype=torch.int32, device=dev)
         stream.synchronize()
         self.tokens_per_step = B
-        self.launches_per_step = 2  # workspace-header reset kernel, decode kernel (packs the new token)
+        self.launches_per_step = 1  # the decode kernel (packs the new token, merges its splits)
         self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D)
 
     def step(self, i):
@@ -274,15 +274,15 @@ class FanoutWork:
             self.l_t = torch.empty((A, 1, Hq), dtype=torch.float32, device=dev)
             self.out = torch.empty((A * Hq, D), dtype=torch.float32, device=dev)
             self.lse = torch.empty(A * Hq, dtype=torch.float32, device=dev)
-            self.ws = torch.empty(ckv.attn_decode_workspace(self.caches[0], P, A, Hq), dtype=torch.uint8,
+            self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], P, A, Hq), dtype=torch.uint8,
                                   device=dev)
-            self.ws_t = torch.empty(ckv.attn_decode_f16_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8,
+            self.ws_t = torch.zeros(ckv.attn_decode_f16_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8,
                                     device=dev)
             self.seq_p = torch.full((1,), P, dtype=torch.int32, device=dev)
             self.seq_t = torch.full((A,), TL, dtype=torch.int32, device=dev)
         stream.synchronize()
         self.tokens_per_step = A
-        self.launches_per_step = 5  # 2 workspace-header resets, prefix decode, tail decode, merge
+        self.launches_per_step = 3  # prefix decode, tail decode, merge
         self.algo_bytes = Hkv * P * inputs.compressed_bytes_per_token(D) + 2 * A * Hkv * TL * D * 2
 
     def _run(self, i, qa):
@@ -359,12 +359,12 @@ class PrefillWork:
             del k, v
             self.out = torch.empty((1, nn, Hq, D), dtype=torch.float32, device=dev)
             self.lse = torch.empty((1, nn, Hq), dtype=torch.float32, device=dev)
-            self.ws = torch.empty(ckv.attn_prefill_workspace(self.cache, nn, Hq), dtype=torch.uint8, device=dev)
+            self.ws = torch.zeros(ckv.attn_prefill_workspace(self.cache, nn, Hq), dtype=torch.uint8, device=dev)
             self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
             self.flush = torch.empty(2 * self.l2, dtype=torch.uint8, device=dev)
         stream.synchronize()
         self.tokens_per_step = nn
-        self.launches_per_step = 4  # header reset, pack, prefill, de-rotation
+        self.launches_per_step = 3  # pack, prefill, de-rotation
         # QK^T and PV over the causal key range: query i sees nc + i + 1 keys.
         self.flops = 2 * 2 * Hq * D * (nn * nc + nn * (nn + 1) // 2)
 

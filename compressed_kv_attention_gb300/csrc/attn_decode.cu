@@ -50,9 +50,7 @@ struct CDec : DecodeShape<D> {
   static constexpr int VW = 3 * Sh::MT_W / 4;   // V-code words per lane per warp
   static constexpr int GR = v_granule(D);       // stream granule bytes
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
-  static constexpr int MERGE_BYTES = merge_scratch_floats(kMaxInKernelSplits, 256) * 4;
-  static constexpr int RING0 = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
-  static constexpr int RING = (RING0 > MERGE_BYTES) ? RING0 : MERGE_BYTES;
+  static constexpr int RING = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
   static constexpr int OFF_XCHG = (RING + 127) / 128 * 128;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
   static constexpr int OFF_QB = OFF_ML + Sh::NP * 16 * 4;          // [NCW][NB_W][4][2] query-block biases
@@ -208,6 +206,30 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const int n_iters_max = static_cast<int>((tile_end_max - tile_begin + C::NP - 1) / C::NP);
   const uint8_t* gbase = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) * C::REC;
 
+  // Setup that reads no global memory runs while the previous grid on the
+  // stream may still be finishing: the producer lane sets up the barriers,
+  // the consumers fill the centroid-pair table (entry f (6 bits) =
+  // fp16x2(c[f & 7], c[f >> 3]), one copy per lane).
+  griddep_launch_dependents();
+  if (warp == C::NCW) {
+    if (lane == 0) {
+      for (int s = 0; s < C::NSTAGE; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], C::NCW);
+      }
+      s_abort = 0;
+      fence_barrier_init();
+    }
+  } else {
+    for (int e = threadIdx.x; e < 64 * 32; e += C::NCW * 32) {
+      const int f = e >> 5;
+      const __half lo = __float2half_rn(centroid(f & 7));
+      const __half hi = __float2half_rn(centroid(f >> 3));
+      s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+  }
+  griddep_wait();
+
   // Query fragments first: issued before the producer starts its bulk copies,
   // these small loads do not queue behind them. The sequence length is read by
   // one thread per CTA (every CTA of the grid reads the same few words) and
@@ -231,9 +253,8 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
   }
 
-  // The producer lane sets up the barriers and, for a plain decode, issues the
-  // first stages before the CTA-wide barrier; the consumers meanwhile load Q
-  // and fill the centroid table.
+  // For a plain decode the producer lane issues the first stages before the
+  // CTA-wide barrier; the consumers meanwhile load Q.
   int issued = 0;  // producer lane
   auto issue = [&](int it, int64_t end) {
     const int s = it % C::NSTAGE;
@@ -245,28 +266,10 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     ++issued;
   };
   int pre = 0;
-  if (warp == C::NCW) {
-    if (lane == 0) {
-      for (int s = 0; s < C::NSTAGE; ++s) {
-        mbar_init(&full[s], 1);
-        mbar_init(&empty[s], C::NCW);
-      }
-      s_abort = 0;
-      fence_barrier_init();
-    }
-    if (a.n_new == 0) {
-      pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
-      if (lane == 0)
-        for (int it = 0; it < pre; ++it) issue(it, tile_end_max);
-    }
-  } else {
-    // Centroid-pair table: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
-    for (int e = threadIdx.x; e < 64 * 32; e += C::NCW * 32) {
-      const int f = e >> 5;
-      const __half lo = __float2half_rn(centroid(f & 7));
-      const __half hi = __float2half_rn(centroid(f >> 3));
-      s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-    }
+  if (warp == C::NCW && a.n_new == 0) {
+    pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
+    if (lane == 0)
+      for (int it = 0; it < pre; ++it) issue(it, tile_end_max);
   }
   __syncthreads();
 
@@ -435,72 +438,13 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  float* part_out = a.part + ((gid * a.n_split + split) * 8) * D;
-  float* ml_out = a.ml + ((gid * a.n_split + split) * 8) * 2;
-  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane, tid,
-                              a.signs, part_out, ml_out);
-  __shared__ int s_ok;
-  __shared__ float* s_out[8];
-  __shared__ float* s_lse[8];
-  decode_merge_tail<D>(a, split, rg, b, kvh, tid, reinterpret_cast<float*>(smem), &s_ok, s_out, s_lse);
-}
-
-// ------------------------------------------------------- header reset --
-
-// Clears the workspace header (device flag + split-merge counters) before a
-// decode. A one-block kernel: a memset node costs several times more.
-__global__ void __launch_bounds__(256) ws_reset_kernel(uint32_t* header, int words) {
-  for (int i = threadIdx.x; i < words; i += blockDim.x) header[i] = 0u;
-}
-
-cudaError_t launch_ws_reset(void* header, size_t bytes, cudaStream_t stream) {
-  ws_reset_kernel<<<1, 256, 0, stream>>>(static_cast<uint32_t*>(header), static_cast<int>(bytes / 4));
-  return cudaGetLastError();
-}
-
-// --------------------------------------------------------------- merge --
-
-// Split merge as a separate kernel, for grids too large to be co-resident:
-// CTA (chunk, group) merges elements of the group's 8 x D output.
-template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(MergeArgs m) {
-  extern __shared__ __align__(16) float msm[];
-  __shared__ float* s_out[8];
-  __shared__ float* s_lse[8];
-  const int64_t gid = blockIdx.y;
-  const int rg = static_cast<int>(gid % m.n_row_groups);
-  const int bh = static_cast<int>(gid / m.n_row_groups);
-  const int b = bh / m.n_kv_heads, kvh = bh % m.n_kv_heads;
-  const int tid = threadIdx.x;
-  if (tid < 8) {
-    DecodeArgs a{};
-    a.n_q_heads = m.n_q_heads;
-    a.n_kv_heads = m.n_kv_heads;
-    a.n_q = m.n_q;
-    a.head_dim = D;
-    a.out = m.out;
-    a.lse = m.lse;
-    row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
-  }
-  __syncthreads();
-  const int u0 = (int)((int64_t)blockIdx.x * 2 * D / gridDim.x);
-  const int u1 = (int)((int64_t)(blockIdx.x + 1) * 2 * D / gridDim.x);
-  merge_rows<D>(m.part + (size_t)gid * m.n_split * 8 * D, m.ml + (size_t)gid * m.n_split * 16, m.n_split,
-                u0, u1, tid, 256, msm, s_out, s_lse, blockIdx.x == 0, 1);
-}
-
-size_t decode_smem_bytes(int head_dim) {
-  switch (head_dim) {
-    case 64: return CDec<64>::SMEM;
-    case 128: return CDec<128>::SMEM;
-    case 256: return CDec<256>::SMEM;
-    case 512: return CDec<512>::SMEM;
-    default: return 0;
-  }
+  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
+                              a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
+  decode_split_tail<D, C::RING>(a, split, gid, b, kvh, rg, tid, smem);
 }
 
 template <int D>
-static cudaError_t launch_decode_d(const DecodeArgs& a, bool cooperative, cudaStream_t stream) {
+static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = CDec<D>;
   static bool configured = false;  // per process; the attribute is per function
   static int cap = 0;
@@ -510,41 +454,15 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, bool cooperative, cudaSt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_split_decode(attn_decode_kernel<D>, a, cooperative, C::THREADS, C::SMEM, &cap, stream);
+  return launch_split_decode(attn_decode_kernel<D>, a, C::THREADS, C::SMEM, &cap, stream);
 }
 
-cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stream) {
+cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
-    case 64: return launch_decode_d<64>(a, cooperative, stream);
-    case 128: return launch_decode_d<128>(a, cooperative, stream);
-    case 256: return launch_decode_d<256>(a, cooperative, stream);
-    case 512: return launch_decode_d<512>(a, cooperative, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int D>
-static cudaError_t launch_merge_d(const MergeArgs& m, cudaStream_t stream) {
-  const int64_t groups = (int64_t)m.batch * m.n_kv_heads * m.n_row_groups;
-  const size_t smem = (size_t)merge_scratch_floats(m.n_split, 256) * sizeof(float);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  dim3 grid(8 * D / 256, static_cast<unsigned>(groups));
-  decode_merge_kernel<D><<<grid, 256, smem, stream>>>(m);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_decode_merge(const MergeArgs& a, cudaStream_t stream) {
-  switch (a.head_dim) {
-    case 64: return launch_merge_d<64>(a, stream);
-    case 128: return launch_merge_d<128>(a, stream);
-    case 256: return launch_merge_d<256>(a, stream);
-    case 512: return launch_merge_d<512>(a, stream);
+    case 64: return launch_decode_d<64>(a, stream);
+    case 128: return launch_decode_d<128>(a, stream);
+    case 256: return launch_decode_d<256>(a, stream);
+    case 512: return launch_decode_d<512>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -18,8 +18,7 @@ struct FDec : DecodeShape<D> {
   using Sh = DecodeShape<D>;
   static constexpr int THREADS = Sh::NCW * 32;
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
-  static constexpr int MERGE_BYTES = merge_scratch_floats(kMaxInKernelSplits, 256) * 4;
-  static constexpr int OFF_XCHG = (RED_BYTES > MERGE_BYTES) ? RED_BYTES : MERGE_BYTES;
+  static constexpr int OFF_XCHG = (RED_BYTES + 127) / 128 * 128;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
   static constexpr int SMEM = OFF_ML + Sh::NP * 16 * 4;
 };
@@ -39,6 +38,8 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XCHG);
   float* mlbuf = reinterpret_cast<float*>(smem + C::OFF_ML);
 
+  griddep_launch_dependents();
+  griddep_wait();  // the previous grid on the stream is complete
   int seqlen = a.seq_len[b];
   const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
   if (seqlen < 0 || seqlen > lim) {
@@ -110,18 +111,13 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  float* part_out = a.part + ((gid * a.n_split + split) * 8) * D;
-  float* ml_out = a.ml + ((gid * a.n_split + split) * 8) * 2;
-  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane, tid,
-                              nullptr, part_out, ml_out);
-  __shared__ int s_ok;
-  __shared__ float* s_out[8];
-  __shared__ float* s_lse[8];
-  decode_merge_tail<D>(a, split, rg, b, kvh, tid, reinterpret_cast<float*>(smem), &s_ok, s_out, s_lse);
+  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
+                              nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
+  decode_split_tail<D, C::RED_BYTES>(a, split, gid, b, kvh, rg, tid, smem);
 }
 
 template <int D>
-static cudaError_t launch_f16_d(const DecodeArgs& a, bool cooperative, cudaStream_t stream) {
+static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = FDec<D>;
   static bool configured = false;
   static int cap = 0;
@@ -131,15 +127,15 @@ static cudaError_t launch_f16_d(const DecodeArgs& a, bool cooperative, cudaStrea
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_split_decode(attn_decode_f16_kernel<D>, a, cooperative, C::THREADS, C::SMEM, &cap, stream);
+  return launch_split_decode(attn_decode_f16_kernel<D>, a, C::THREADS, C::SMEM, &cap, stream);
 }
 
-cudaError_t launch_attn_decode_f16(DecodeArgs a, bool cooperative, cudaStream_t stream) {
+cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
-    case 64: return launch_f16_d<64>(a, cooperative, stream);
-    case 128: return launch_f16_d<128>(a, cooperative, stream);
-    case 256: return launch_f16_d<256>(a, cooperative, stream);
-    case 512: return launch_f16_d<512>(a, cooperative, stream);
+    case 64: return launch_f16_d<64>(a, stream);
+    case 128: return launch_f16_d<128>(a, stream);
+    case 256: return launch_f16_d<256>(a, stream);
+    case 512: return launch_f16_d<512>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -15,8 +15,9 @@
 //    library, for the life of the process. A call whose scratch would not fit
 //    (see ckv_attn_decode_workspace) is rejected with CKV_ERR_WORKSPACE.
 //  * All calls share the one array and it keeps the previous call's contents.
-//    The device flag word at its start is cleared by each call; the partials are
-//    fully rewritten by every call. Calls that overlap on the GPU (different
+//    It is zero when the library loads; every call puts the split-merge
+//    counters back to zero and rewrites every partial it reads (the device
+//    flag word keeps any error). Calls that overlap on the GPU (different
 //    streams, no ordering between them) race on the array and give wrong
 //    results: order them on one stream or with events.
 //  * The first call on a device looks up the array's device address on that
@@ -78,7 +79,7 @@ extern "C" CKV_API ckv_status ckv_attn_decode_noalloc(const ckv_cache* cache, co
   if (e != cudaSuccess)
     return static_cast<ckv_status>(ckv::set_last_error(
         CKV_ERR_CUDA, "attn_decode_noalloc: scratch address lookup: %s", cudaGetErrorString(e)));
-  // ckv_attn_decode clears the flag word and rewrites every partial it reads.
+  // ckv_attn_decode leaves the counters at zero and rewrites every partial it reads.
   return ckv_attn_decode(cache, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
                          scratch, kNoAllocScratchBytes, stream);
 }

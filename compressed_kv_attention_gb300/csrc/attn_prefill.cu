@@ -598,9 +598,7 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
   if (!workspace || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_WORKSPACE, "workspace needs 256 aligned bytes"));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = ckv::launch_ws_reset(workspace, 256, st);
-  if (e != cudaSuccess)
-    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_CUDA, "flag reset: %s", cudaGetErrorString(e)));
+  cudaError_t e = cudaSuccess;
   // Pack the new rows (same quantisers as kv_pack) at [n_cached, n_cached + n_new).
   const int64_t row = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
   const ckv_status ps = ckv_kv_pack(cache, n_cached, n_new, k_new_f16, v_new_f16, row, row * n_new, stream);

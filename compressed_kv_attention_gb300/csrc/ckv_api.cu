@@ -32,7 +32,16 @@ bool supported_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; 
 
 // Workspace header: the device flag at byte 0, one split-merge counter per row
 // group from byte 64, rounded up to 256 bytes; both are cleared by every call.
-size_t ws_header_bytes(int64_t groups) { return (64 + 4 * static_cast<size_t>(groups) + 255) / 256 * 256; }
+// Decode workspace: the device flag (bytes 0..3), the merge-tree counters from
+// byte 64, then the partial slots and the leaf slots (decode_common.cuh).
+// Counter words per group: two for the rendezvous merge, nl + 1 for the tree.
+int ctr_stride(int n_split) {
+  const int t = ckv::merge_tree(n_split).nl + 1;
+  return t > 2 ? t : 2;
+}
+size_t ws_header_bytes(int64_t groups, int n_split) {
+  return (64 + 4 * static_cast<size_t>(groups) * ctr_stride(n_split) + 255) / 256 * 256;
+}
 
 int num_sms() {
   static int cached[64] = {0};
@@ -60,8 +69,8 @@ ckv_status check_cache(const ckv_cache* c) {
   return CKV_OK;
 }
 
-// Split count: as many CTAs as fit on the SMs at once (one each), so the grid
-// stays co-resident and merges its splits in-kernel; no more splits than tiles.
+// Split count: one CTA per SM in a single wave (measured best: a CTA streams
+// its splits' tiles through the whole kernel); no more splits than tiles.
 int auto_split(int64_t units, int64_t max_seq_len, int tiles_per_cta_iter) {
   const int64_t tiles = (max_seq_len + 15) / 16;
   if (tiles == 0) return 1;
@@ -70,12 +79,14 @@ int auto_split(int64_t units, int64_t max_seq_len, int tiles_per_cta_iter) {
   const int64_t by_tiles = (tiles + tiles_per_cta_iter - 1) / tiles_per_cta_iter;
   if (s > by_tiles) s = by_tiles;
   if (s < 1) s = 1;
-  if (s > 65535) s = 65535;
+  if (s > ckv::kMaxSplits) s = ckv::kMaxSplits;
   return static_cast<int>(s);
 }
 
 size_t decode_ws_bytes(int D, int64_t groups, int n_split) {
-  return ws_header_bytes(groups) + static_cast<size_t>(groups) * n_split * 8 * (D + 2) * sizeof(float);
+  const ckv::MergeTree tr = ckv::merge_tree(n_split);
+  return ws_header_bytes(groups, n_split) +
+         static_cast<size_t>(groups) * (n_split + tr.nl) * ckv::merge_slot_floats(D) * sizeof(float);
 }
 
 struct DecodePlan {
@@ -90,7 +101,7 @@ ckv_status plan_decode(int D, int n_kv_heads, int batch, int64_t max_seq_len, in
   if (n_q_heads % n_kv_heads)
     return fail(CKV_ERR_UNSUPPORTED, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, n_kv_heads);
   if (max_seq_len < 0) return fail(CKV_ERR_INVALID_ARG, "max_seq_len negative");
-  if (n_split < 0 || n_split > 65535) return fail(CKV_ERR_INVALID_ARG, "n_split out of range");
+  if (n_split < 0 || n_split > ckv::kMaxSplits) return fail(CKV_ERR_INVALID_ARG, "n_split out of range");
   const int64_t rows = static_cast<int64_t>(n_q_heads / n_kv_heads) * n_q;
   const int64_t nrg = (rows + 7) / 8;
   if (nrg > 65535) return fail(CKV_ERR_UNSUPPORTED, "too many query rows per kv head");
@@ -214,9 +225,8 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   s = check_ws(ws, ws_bytes, p.ws);
   if (s != CKV_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t header = ws_header_bytes(p.groups);
-  cudaError_t e = ckv::launch_ws_reset(ws, header, st);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
+  const size_t header = ws_header_bytes(p.groups, p.n_split);
+  const ckv::MergeTree tr = ckv::merge_tree(p.n_split);
   uint8_t* base = static_cast<uint8_t*>(ws);
   ckv::DecodeArgs a{};
   a.cache = compressed ? static_cast<const uint8_t*>(cache->data) : nullptr;
@@ -236,7 +246,10 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.n_split = p.n_split;
   a.n_row_groups = p.n_row_groups;
   a.part = reinterpret_cast<float*>(base + header);
-  a.ml = a.part + static_cast<size_t>(p.groups) * p.n_split * 8 * D;
+  a.sub = a.part + static_cast<size_t>(p.groups) * p.n_split * ckv::merge_slot_floats(D);
+  a.merge_ls = tr.ls;
+  a.merge_nl = tr.nl;
+  a.ctr_stride = ctr_stride(p.n_split);
   a.flag = reinterpret_cast<int32_t*>(base);
   a.counters = reinterpret_cast<uint32_t*>(base + 64);
   a.out = out;
@@ -249,28 +262,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
     a.new_token_stride = app->token_stride;
     a.new_batch_stride = app->batch_stride;
   }
-  // One launch when every CTA can be resident at once (the CTAs of a row group
-  // merge their splits themselves); otherwise the decode plus a merge kernel.
-  e = compressed ? ckv::launch_attn_decode(a, true, st) : ckv::launch_attn_decode_f16(a, true, st);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
-    e = compressed ? ckv::launch_attn_decode(a, false, st) : ckv::launch_attn_decode_f16(a, false, st);
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    ckv::MergeArgs m{};
-    m.part = a.part;
-    m.ml = a.ml;
-    m.head_dim = D;
-    m.n_kv_heads = Hkv;
-    m.batch = B;
-    m.n_q = n_q;
-    m.n_q_heads = n_q_heads;
-    m.n_split = p.n_split;
-    m.n_row_groups = p.n_row_groups;
-    m.out = out;
-    m.lse = lse;
-    e = ckv::launch_decode_merge(m, st);
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-    return CKV_OK;
-  }
+  const cudaError_t e = compressed ? ckv::launch_attn_decode(a, st) : ckv::launch_attn_decode_f16(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return CKV_OK;
 }
@@ -349,7 +341,11 @@ ckv_status ckv_read_device_flag(const void* workspace, int32_t* flag, void* stre
   if (e != cudaSuccess) return cuda_fail(e, "stream sync");
   e = cudaMemcpy(flag, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "flag read");
-  if (*flag != 0) return fail(CKV_ERR_DEVICE_FLAG, "device flag %d", *flag);
+  if (*flag != 0) {
+    e = cudaMemset(const_cast<void*>(workspace), 0, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "flag clear");
+    return fail(CKV_ERR_DEVICE_FLAG, "device flag %d", *flag);
+  }
   return CKV_OK;
 }
 

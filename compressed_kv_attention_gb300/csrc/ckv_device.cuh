@@ -112,6 +112,23 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// ------------------------------------------------- programmatic launch --
+
+// With programmatic stream serialisation a grid may start while the grid
+// before it on the stream is still running. griddep_wait returns once that
+// grid has completed and its memory operations are visible (at once when the
+// launch had no such dependency); nothing before it may read or write global
+// memory that another kernel touches. griddep_launch_dependents lets the next
+// grid on the stream begin its own launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Order this thread's generic-proxy accesses (global data acquired from other
+// CTAs, shared memory it used) before its later async-proxy (bulk copy) ones.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // ------------------------------------------------------------ shared loads --
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

@@ -22,13 +22,14 @@ cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream);
 
 // Split-K decode. Rows of one (sequence, kv head) are the G * n_q query vectors
 // that read it, ordered (query token, head in group); they are processed in
-// groups of 8 ("row groups"). Each CTA writes one partial to the workspace:
-//   part[group][split][8][D]  float32, sum_j p_j V_j in true space, relative to
-//                             the CTA's running max (unnormalised)
-//   ml  [group][split][8][2]  float32, (running max in log2 units, row sum)
-// group = (b * n_kv_heads + kv_head) * n_row_groups + row_group. With a
-// cooperative launch the CTAs of a group then merge the splits themselves;
-// otherwise launch_decode_merge does it.
+// groups of 8 ("row groups"). Each CTA writes its partial to a workspace slot
+// and the CTAs that finish last merge them (decode_common.cuh, split merge
+// tree). Workspace regions (floats, slot = 8 D + 16 floats):
+//   part[group][split][slot]   one partial per CTA
+//   sub [group][leaf][slot]    one merged partial per leaf of splits
+//   counters[group][stride]    u32: rendezvous arrivals and departures, or
+//                              the tree's leaf and root counters
+// group = (b * n_kv_heads + kv_head) * n_row_groups + row_group.
 struct DecodeArgs {
   const uint8_t* cache;      // packed records (compressed decode) or nullptr
   const __half* k16;         // dense fp16 keys (fp16 decode) or nullptr
@@ -43,10 +44,12 @@ struct DecodeArgs {
   float scale_log2;          // logit scale * log2(e)
   int n_split, n_row_groups;
   float* part;
-  float* ml;
+  float* sub;
+  int merge_ls, merge_nl;    // leaf size and leaf count of the merge tree
+  int rendezvous;            // 1: every CTA resident at once, merge by rendezvous
   int32_t* flag;
-  uint32_t* counters;        // [groups], zero at launch (cooperative merge)
-  int merge_in_kernel;       // 1: cooperative launch, CTAs merge their group
+  uint32_t* counters;        // ctr_stride words per group, zero between calls
+  int ctr_stride;
   float* out;
   float* lse;
   // Append (compressed decode, one row group): before its tiles are read, the
@@ -59,25 +62,26 @@ struct DecodeArgs {
   int64_t new_token_stride, new_batch_stride;  // in elements
 };
 
-struct MergeArgs {
-  const float* part;
-  const float* ml;
-  int head_dim, n_kv_heads, batch, n_q, n_q_heads, n_split, n_row_groups;
-  float* out;
-  float* lse;
+// Largest split count: the merge tree merges at most 32 slots at a time.
+constexpr int kMaxSplits = 1024;
+
+// Floats of one slot: [8][D] accumulators, then 8 maxima and 8 row sums.
+__host__ __device__ constexpr int64_t merge_slot_floats(int D) { return 8 * (int64_t)D + 16; }
+
+// The tree shape for n_split partials: leaves of ls splits (the last may be
+// shorter), nl leaves, ls = ceil(sqrt(n_split)).
+struct MergeTree {
+  int ls, nl;
 };
+__host__ __device__ inline MergeTree merge_tree(int n_split) {
+  int ls = 1;
+  while (ls * ls < n_split) ++ls;
+  return MergeTree{ls, (n_split + ls - 1) / ls};
+}
 
-// Largest split count the in-kernel merge handles (its shared scratch).
-constexpr int kMaxInKernelSplits = 512;
 
-// Launch the decode kernel; `cooperative` requests the in-kernel merge (all
-// CTAs co-resident). Returns cudaErrorCooperativeLaunchTooLarge when the grid
-// cannot be co-resident, without launching.
-cudaError_t launch_attn_decode(DecodeArgs a, bool cooperative, cudaStream_t stream);
-cudaError_t launch_attn_decode_f16(DecodeArgs a, bool cooperative, cudaStream_t stream);
-cudaError_t launch_decode_merge(const MergeArgs& a, cudaStream_t stream);
-// Zero the first `bytes` (a multiple of 4) of a workspace.
-cudaError_t launch_ws_reset(void* header, size_t bytes, cudaStream_t stream);
+cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream);
 
 struct LseMergeArgs {
   const float* o[16];

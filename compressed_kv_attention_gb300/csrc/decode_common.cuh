@@ -108,23 +108,76 @@ __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int grou
   S[3] += o.w;
 }
 
+// Inverse rotation of one output row held by a warp (lane: dims 64 e + 2 lane
+// + c, c < 2), then the sign flip and 1/D, stored to `orow`: the unnormalised
+// Walsh-Hadamard transform pairs the two values of a float2 (dim bit 0), lanes
+// (bits 1..5, shuffles) and registers (bits 6..); one 1/sqrt(D) comes from the
+// orthonormal inverse, one from the norm scaling folded into P'. Without
+// `signs` (dense values) the row is stored as is.
+template <int D>
+__device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane, const int8_t* signs,
+                                                   float* orow) {
+  constexpr int E2 = D / 64;
+  if (signs) {
+#pragma unroll
+    for (int e = 0; e < E2; ++e) {
+      const float a0 = v[e].x, a1 = v[e].y;
+      v[e] = make_float2(a0 + a1, a0 - a1);
+    }
+#pragma unroll
+    for (int hl = 1; hl < 32; hl <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E2; ++e) {
+        const float ox = __shfl_xor_sync(0xffffffffu, v[e].x, hl);
+        const float oy = __shfl_xor_sync(0xffffffffu, v[e].y, hl);
+        v[e].x = (lane & hl) ? (ox - v[e].x) : (v[e].x + ox);
+        v[e].y = (lane & hl) ? (oy - v[e].y) : (v[e].y + oy);
+      }
+    }
+#pragma unroll
+    for (int hh = 1; hh < E2; hh <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E2; ++e) {
+        if ((e & hh) == 0) {
+          const float2 x0 = v[e], x1 = v[e + hh];
+          v[e] = make_float2(x0.x + x1.x, x0.y + x1.y);
+          v[e + hh] = make_float2(x0.x - x1.x, x0.y - x1.y);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E2; ++e) {
+      const int d = 64 * e + 2 * lane;
+      const char2 sg = *reinterpret_cast<const char2*>(signs + d);
+      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (1.0f / D);
+      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (1.0f / D);
+    }
+  }
+  if (orow) {
+    float2* o2 = reinterpret_cast<float2*>(orow) + lane;
+#pragma unroll
+    for (int e = 0; e < E2; ++e) o2[32 * e] = v[e];
+  }
+}
+
 // CTA epilogue. Merges the NP tile groups' softmax states and accumulators
 // into one partial per row, applies the inverse transform and sign flip (when
 // `signs` is set: the values were accumulated in the rotated basis), and
-// writes the partial to the workspace:
-//   part_out[8][D]  sum_j p_j V_j relative to the CTA's running max, true space
-//   ml_out[8][2]    (running max in log2 units, row sum)
+// writes the partial to the CTA's workspace slot:
+//   slot[r * D + d]   sum_j p_j V_j of row r relative to the CTA's running
+//                     max, true space
+//   slot[8 D + r]     running max of row r in log2 units
+//   slot[8 D + 8 + r] row sum of row r
 // De-rotating each partial here is exact: the transform is linear and the
-// split merge only forms per-row weighted sums of partials. Runs on the 256
-// consumer threads (named barrier 1). `red` holds NP * RED_FLOATS floats (stage
-// memory is reused), `mlbuf` NP * 16 floats. Each group stores its unscaled
-// accumulators with its own (m, l); the warp that owns a row rescales the
-// groups while summing them.
+// split merge only forms per-row weighted sums of partials.
+// Runs on the 256 consumer threads (named barrier 1). `red` holds
+// NP * RED_FLOATS floats (stage memory is reused), `mlbuf` NP * 16 floats.
+// Each group stores its unscaled accumulators with its own (m, l); the warp
+// that owns a row rescales the groups while summing them.
 template <int D, int MTW>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
                                                 float* mlbuf, int group, int wh, int warp, int lane,
-                                                int tid, const int8_t* signs, float* part_out,
-                                                float* ml_out) {
+                                                const int8_t* signs, float* slot) {
   using Sh = DecodeShape<D>;
   const int g = lane >> 2, t = lane & 3;
   // Reduce the row sums over the 8 lanes that share rows (2t, 2t+1).
@@ -178,241 +231,13 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
     }
     v[e] = x;
   }
-  if (signs) {
-    // Unnormalised Walsh-Hadamard transform of the row: the stage on dim bit 0
-    // pairs the two values of a float2, bits 1..5 pair lanes (shuffles), bits
-    // 6.. pair registers; then the sign flip and 1/D (one 1/sqrt(D) from the
-    // orthonormal inverse, one from the norm scaling folded into P').
-#pragma unroll
-    for (int e = 0; e < E2; ++e) {
-      const float a0 = v[e].x, a1 = v[e].y;
-      v[e] = make_float2(a0 + a1, a0 - a1);
-    }
-#pragma unroll
-    for (int hl = 1; hl < 32; hl <<= 1) {
-#pragma unroll
-      for (int e = 0; e < E2; ++e) {
-        const float ox = __shfl_xor_sync(0xffffffffu, v[e].x, hl);
-        const float oy = __shfl_xor_sync(0xffffffffu, v[e].y, hl);
-        v[e].x = (lane & hl) ? (ox - v[e].x) : (v[e].x + ox);
-        v[e].y = (lane & hl) ? (oy - v[e].y) : (v[e].y + oy);
-      }
-    }
-#pragma unroll
-    for (int hh = 1; hh < E2; hh <<= 1) {
-#pragma unroll
-      for (int e = 0; e < E2; ++e) {
-        if ((e & hh) == 0) {
-          const float2 x0 = v[e], x1 = v[e + hh];
-          v[e] = make_float2(x0.x + x1.x, x0.y + x1.y);
-          v[e + hh] = make_float2(x0.x - x1.x, x0.y - x1.y);
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < E2; ++e) {
-      const int d = 64 * e + 2 * lane;
-      const char2 sg = *reinterpret_cast<const char2*>(signs + d);
-      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (1.0f / D);
-      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (1.0f / D);
-    }
-  }
-  float2* prow = reinterpret_cast<float2*>(part_out + r * D) + lane;
-#pragma unroll
-  for (int e = 0; e < E2; ++e) prow[32 * e] = v[e];
+  derotate_store_row<D>(v, lane, signs, slot + r * D);
   if (lane == 0) {
-    ml_out[r * 2 + 0] = mc;
-    ml_out[r * 2 + 1] = lc;
-  }
-  (void)tid;
-}
-
-// Floats of shared scratch that merge_rows needs.
-__host__ __device__ constexpr int merge_scratch_floats(int n_split, int nthr) {
-  return 8 * n_split + 16 * (nthr / 32);
-}
-
-// Exact merge of the n_split partials of one row group (8 rows x D):
-// M = max_s m_s, w_s = 2^(m_s - M), O = sum_s w_s part_s / sum_s w_s l_s,
-// lse = (M + log2 sum_s w_s l_s) ln 2; a row with no key gives O = 0, lse = -inf.
-// part: [n_split][8][D], ml: [n_split][8][2] of the group. This CTA produces
-// the float4 units [u0, u1) of the 8 x D output (unit u: row u / (D/4), dims
-// 4 (u % (D/4)) .. +4). Threads tid < nthr (nthr a multiple of 32, >= 256)
-// take part and synchronise on named barrier `bar_id`; `sm` provides
-// merge_scratch_floats(n_split, nthr) floats. out_rows / lse_rows: where each
-// row goes (nullptr for padding rows); lse is written when write_lse.
-//
-// The partials sit in L2, so the cost is dependent round trips and barriers:
-// every thread issues its (m, l) loads and its first batch of partial loads
-// before it waits on any of them; row maxima and sums are reduced by all
-// threads at once (the (m, l) entries a thread holds all belong to row tid % 8);
-// each output unit is summed by k consecutive lanes and reduced with shuffles.
-template <int D>
-__device__ __forceinline__ void merge_rows(const float* part, const float* ml, int n_split, int u0, int u1,
-                                           int tid, int nthr, float* sm, float* const* out_rows,
-                                           float* const* lse_rows, bool write_lse, int bar_id) {
-  constexpr int U = D / 4;        // float4 units per row
-  constexpr int MLR = 4;          // (m, l) pairs per thread held in registers
-  constexpr int PB = 8;           // partial loads per thread per batch
-  const int nw = nthr >> 5;
-  float* w = sm;                  // [n_split][8] weights
-  float* wmax = w + n_split * 8;  // [nw][8] per-warp row maxima
-  float* wsum = wmax + nw * 8;    // [nw][8] per-warp row sums
-  const float2* ml2 = reinterpret_cast<const float2*>(ml);
-  const float4* part4 = reinterpret_cast<const float4*>(part);
-  const int n_ml = n_split * 8;
-  const int nu = u1 - u0;
-  const int lane = tid & 31, warp = tid >> 5;
-  int k = 1;  // lanes per unit: a power of two, so a unit's lanes share a warp
-  while (k < 32 && 2 * k * nu <= nthr) k *= 2;
-  const int cs = nthr / k;
-  const int ui = tid / k, sub = tid % k;
-
-  // 1. Loads in flight together.
-  float2 mlv[MLR];
-#pragma unroll
-  for (int j = 0; j < MLR; ++j) {
-    const int i = tid + j * nthr;
-    mlv[j] = (i < n_ml) ? __ldcg(ml2 + i) : make_float2(-INFINITY, 0.0f);
-  }
-  float4 x[PB];
-#pragma unroll
-  for (int j = 0; j < PB; ++j) {
-    const int s = sub + j * k;
-    x[j] = (ui < nu && s < n_split) ? __ldcg(part4 + (size_t)s * 8 * U + u0 + ui)
-                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  }
-  // 2. Row maxima.
-  float m = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < MLR; ++j) m = fmaxf(m, mlv[j].x);
-  for (int i = tid + MLR * nthr; i < n_ml; i += nthr) m = fmaxf(m, __ldcg(ml2 + i).x);
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-  if (lane < 8) wmax[warp * 8 + lane] = m;
-  named_bar(bar_id, nthr);
-  float M = -INFINITY;
-  for (int ww = 0; ww < nw; ++ww) M = fmaxf(M, wmax[ww * 8 + (tid & 7)]);
-  // 3. Weights and row sums.
-  float Ls = 0.0f;
-#pragma unroll
-  for (int j = 0; j < MLR; ++j) {
-    const int i = tid + j * nthr;
-    if (i < n_ml) {
-      const float ws = (mlv[j].x == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mlv[j].x - M);
-      w[i] = ws;
-      Ls = fmaf(ws, mlv[j].y, Ls);
-    }
-  }
-  for (int i = tid + MLR * nthr; i < n_ml; i += nthr) {
-    const float2 v = __ldcg(ml2 + i);
-    const float ws = (v.x == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(v.x - M);
-    w[i] = ws;
-    Ls = fmaf(ws, v.y, Ls);
-  }
-  Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
-  Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
-  if (lane < 8) wsum[warp * 8 + lane] = Ls;
-  named_bar(bar_id, nthr);
-  if (write_lse && tid < 8 && lse_rows[tid]) {
-    float L = 0.0f;
-    for (int ww = 0; ww < nw; ++ww) L += wsum[ww * 8 + tid];
-    *lse_rows[tid] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-  }
-  // 4. Weighted sums, reduced over each unit's k lanes.
-  for (int base = 0; base < nu; base += cs) {
-    const int el = base + ui;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    int r = 0;
-    if (el < nu) {
-      const int u = u0 + el;
-      r = u / U;
-      int s0 = sub;
-      if (base == 0) {
-#pragma unroll
-        for (int j = 0; j < PB; ++j) {
-          const int s = sub + j * k;
-          if (s < n_split) {
-            const float ws = w[s * 8 + r];
-            acc.x = fmaf(ws, x[j].x, acc.x);
-            acc.y = fmaf(ws, x[j].y, acc.y);
-            acc.z = fmaf(ws, x[j].z, acc.z);
-            acc.w = fmaf(ws, x[j].w, acc.w);
-          }
-        }
-        s0 = sub + PB * k;
-      }
-      for (; s0 < n_split; s0 += PB * k) {
-#pragma unroll
-        for (int j = 0; j < PB; ++j) {
-          const int s = s0 + j * k;
-          x[j] = (s < n_split) ? __ldcg(part4 + (size_t)s * 8 * U + u) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        }
-#pragma unroll
-        for (int j = 0; j < PB; ++j) {
-          const int s = s0 + j * k;
-          if (s < n_split) {
-            const float ws = w[s * 8 + r];
-            acc.x = fmaf(ws, x[j].x, acc.x);
-            acc.y = fmaf(ws, x[j].y, acc.y);
-            acc.z = fmaf(ws, x[j].z, acc.z);
-            acc.w = fmaf(ws, x[j].w, acc.w);
-          }
-        }
-      }
-    }
-    for (int off = 1; off < k; off <<= 1) {
-      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
-    }
-    if (sub == 0 && el < nu && out_rows[r]) {
-      float L = 0.0f;
-      for (int ww = 0; ww < nw; ++ww) L += wsum[ww * 8 + r];
-      const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-      float* o = out_rows[r] + 4 * ((u0 + el) % U);
-      o[0] = acc.x * inv;
-      o[1] = acc.y * inv;
-      o[2] = acc.z * inv;
-      o[3] = acc.w * inv;
-    }
+    slot[8 * D + r] = mc;
+    slot[8 * D + 8 + r] = lc;
   }
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Split-merge rendezvous of a cooperative launch: every CTA of the row group
-// has written its partial; the last of them to arrive releases the others.
-// The wait is bounded; on timeout the device flag is raised and false returned.
-__device__ __forceinline__ bool group_rendezvous(uint32_t* counter, uint32_t n_split, int tid, int nthr,
-                                                 int bar_id, int32_t* flag, int* s_ok) {
-  __threadfence();
-  named_bar(bar_id, nthr);
-  if (tid == 0) {
-    atomicAdd(counter, 1u);
-    int ok = 1;
-    if (ld_acquire_u32(counter) < n_split) {
-      const uint64_t t0 = global_timer_ns();
-      for (uint32_t it = 1;; ++it) {
-        if (ld_acquire_u32(counter) >= n_split) break;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
-          raise_flag(flag, kFlagWaitTimeout);
-          ok = 0;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    *s_ok = ok;
-  }
-  named_bar(bar_id, nthr);
-  return *(volatile int*)s_ok != 0;
-}
 
 // Which query vector row `rr` (0 <= rr < G * n_q) of kv head `kvh` is: the
 // query token and the query head.
@@ -455,25 +280,407 @@ __device__ __forceinline__ void row_outputs(const DecodeArgs& a, int b, int kvh,
   *l = a.lse + orow;
 }
 
-// After the epilogue: when the launch is cooperative, meet the group's other
-// CTAs and merge this CTA's slice of the group's output (256 consumer threads).
-template <int D>
-__device__ __forceinline__ void decode_merge_tail(const DecodeArgs& a, int split, int rg, int b, int kvh,
-                                                  int tid, float* sm, int* s_ok, float** s_out,
-                                                  float** s_lse) {
-  if (!a.merge_in_kernel) return;
-  const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  if (!group_rendezvous(a.counters + gid, (uint32_t)a.n_split, tid, 256, 1, a.flag, s_ok)) return;
-  if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
+// ------------------------------------------------------------ split merge --
+//
+// Merging is exact: with M = max_s m_s and w_s = 2^(m_s - M), the merge of
+// slots s is (sum_s w_s O_s, M, L = sum_s w_s l_s); the output is O / L and
+// lse = (M + log2 L) ln 2, and a row with no key gives O = 0, lse = -inf.
+// Two ways to get there, both leaving the group's counters at zero:
+//  * Rendezvous (every CTA of the grid resident at once, the host checks
+//    occupancy): the CTAs of a group meet on a counter, then each merges a
+//    slice of the group's 8 x D output, all slices at once. A second counter
+//    counts departures; the last CTA to leave zeroes both.
+//  * Tree (any grid): the splits form NL leaves of up to LS consecutive
+//    splits. A CTA counts itself into its leaf; the CTA that completes a leaf
+//    merges the leaf's slots into a leaf slot and counts the leaf into the
+//    group's root; the CTA that completes the root merges the leaf slots and
+//    writes the output rows. No CTA waits for another; each merger zeroes the
+//    counter it completed.
+
+// Merge `cnt` slots (slot s at src + s * merge_slot_floats(D)), cnt <= 32.
+// The accumulators arrive through bulk copies, at most SCR / (32 D) slots at
+// a time, into `scratch` (SCR bytes of shared memory no longer in use). On
+// return unit u = tid + 256 k (u < 2 D: row u / (D/4), dims 4 (u % (D/4)) ..)
+// of the weighted sum is in acc[k]; s_M / s_L hold the row maxima and sums.
+// 256 threads, named barrier 1. False when a copy wait ran out (the device
+// flag is raised; the sums are then incomplete).
+template <int D, int SCR>
+__device__ __forceinline__ bool merge_slots(const float* src, int cnt, uint8_t* scratch, uint64_t* mbar,
+                                            uint32_t& mphase, int tid, float* s_w, float* s_M, float* s_L,
+                                            int32_t* flag, float4 (&acc)[(2 * D + 255) / 256]) {
+  constexpr int64_t SLOT = merge_slot_floats(D);
+  constexpr int NK = (2 * D + 255) / 256;
+  constexpr int KC = SCR / (32 * D);
+  static_assert(KC >= 1, "merge scratch holds at least one slot");
+  // Maxima and sums of every slot and row, then the weights.
+  if (tid < cnt * 8) {
+    const float* ml = src + (tid >> 3) * SLOT + 8 * D;
+    s_w[tid] = __ldcg(ml + (tid & 7));
+    s_w[256 + tid] = __ldcg(ml + 8 + (tid & 7));
+  }
   named_bar(1, 256);
-  const int u0 = (int)((int64_t)split * 2 * D / a.n_split);
-  const int u1 = (int)((int64_t)(split + 1) * 2 * D / a.n_split);
-  merge_rows<D>(a.part + (size_t)gid * a.n_split * 8 * D, a.ml + (size_t)gid * a.n_split * 16, a.n_split,
-                u0, u1, tid, 256, sm, s_out, s_lse, split == 0, 1);
+  if (tid < 8) {
+    float M = -INFINITY;
+    for (int q = 0; q < cnt; ++q) M = fmaxf(M, s_w[q * 8 + tid]);
+    float L = 0.0f;
+    for (int q = 0; q < cnt; ++q) {
+      const float m = s_w[q * 8 + tid];
+      const float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+      s_w[q * 8 + tid] = w;
+      L = fmaf(w, s_w[256 + q * 8 + tid], L);
+    }
+    s_M[tid] = M;
+    s_L[tid] = L;
+  }
+#pragma unroll
+  for (int k = 0; k < NK; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  bool ok = true;
+  for (int c0 = 0; c0 < cnt; c0 += KC) {
+    const int kc = (cnt - c0 < KC) ? cnt - c0 : KC;
+    fence_proxy_async_all();  // this thread's reads of the scratch precede the copies into it
+    named_bar(1, 256);        // weights written; the previous chunk fully read
+    if (tid == 0) {
+      fence_proxy_async_all();
+      mbar_arrive_expect_tx(mbar, (uint32_t)kc * 32u * D);
+      for (int q = 0; q < kc; ++q) bulk_g2s(scratch + q * 32 * D, src + (c0 + q) * SLOT, 32u * D, mbar);
+    }
+    if (!mbar_wait(mbar, mphase & 1)) {
+      ok = false;
+      if (tid == 0) raise_flag(flag, kFlagWaitTimeout);
+      mbar_wait(mbar, mphase & 1);  // a second bounded wait for copies still landing
+    }
+    ++mphase;
+    const float4* chunk = reinterpret_cast<const float4*>(scratch);
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+      const int u = tid + 256 * k;
+      if (u < 2 * D) {
+        const int row = u / (D / 4);
+        for (int q = 0; q < kc; ++q) {
+          const float w = s_w[(c0 + q) * 8 + row];
+          const float4 x = chunk[q * 2 * D + u];
+          acc[k].x = fmaf(w, x.x, acc[k].x);
+          acc[k].y = fmaf(w, x.y, acc[k].y);
+          acc[k].z = fmaf(w, x.z, acc[k].z);
+          acc[k].w = fmaf(w, x.w, acc[k].w);
+        }
+      }
+    }
+  }
+  named_bar(1, 256);  // every thread is done with the scratch and the weights
+  return ok;
 }
 
+// Tree merge, after the epilogue has written this CTA's slot: count into the
+// leaf and, when this CTA completes the leaf (and then the root), merge. 256
+// consumer threads, named barrier 1. `scratch` (SCR bytes) is the stage memory.
+template <int D, int SCR>
+__device__ __forceinline__ void tree_merge_tail(const DecodeArgs& a, int split, int64_t gid, int b, int kvh,
+                                                int rg, int tid, uint8_t* scratch) {
+  constexpr int64_t SLOT = merge_slot_floats(D);
+  constexpr int NK = (2 * D + 255) / 256;
+  __shared__ __align__(8) uint64_t s_mbar;
+  __shared__ float s_w[512], s_M[8], s_L[8];
+  __shared__ int s_last;
+  __shared__ float* s_out[8];
+  __shared__ float* s_lse[8];
+  const MergeTree tr{a.merge_ls, a.merge_nl};
+  const int leaf = split / tr.ls;
+  const int leaf_cnt = (leaf + 1 < tr.nl) ? tr.ls : a.n_split - leaf * tr.ls;
+  uint32_t* ctr = a.counters + gid * a.ctr_stride;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // 1. Count into the leaf (the slot stores are released first; mergers read
+  //    them back through bulk copies).
+  fence_proxy_async_all();
+  __threadfence();
+  named_bar(1, 256);
+  if (tid == 0) {
+    const uint32_t t = atomicAdd(ctr + leaf, 1u);
+    s_last = (t + 1 == (uint32_t)leaf_cnt);
+    if (s_last) {
+      ctr[leaf] = 0u;
+      __threadfence();  // acquire: the leaf's slots are complete
+      mbar_init(&s_mbar, 1);
+      fence_barrier_init();
+    }
+  }
+  named_bar(1, 256);
+  if (!s_last) return;
+  uint32_t mphase = 0;
+  float4 acc[NK];
+  const float* leaf_src = a.part + (gid * a.n_split + (int64_t)leaf * tr.ls) * SLOT;
+  merge_slots<D, SCR>(leaf_src, leaf_cnt, scratch, &s_mbar, mphase, tid, s_w, s_M, s_L, a.flag, acc);
+
+  // 2. Write the leaf slot and count it into the root.
+  float* lslot = a.sub + (gid * tr.nl + leaf) * SLOT;
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    const int u = tid + 256 * k;
+    if (u < 2 * D) reinterpret_cast<float4*>(lslot)[u] = acc[k];
+  }
+  if (tid < 8) {
+    lslot[8 * D + tid] = s_M[tid];
+    lslot[8 * D + 8 + tid] = s_L[tid];
+  }
+  fence_proxy_async_all();
+  __threadfence();
+  named_bar(1, 256);
+  if (tid == 0) {
+    const uint32_t t = atomicAdd(ctr + tr.nl, 1u);
+    s_last = (t + 1 == (uint32_t)tr.nl);
+    if (s_last) {
+      ctr[tr.nl] = 0u;
+      __threadfence();
+    }
+  }
+  if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
+  named_bar(1, 256);
+  if (!s_last) return;
+
+  // 3. Merge the leaves; normalise; rows through shared memory to the warp
+  //    that stores each.
+  merge_slots<D, SCR>(a.sub + gid * tr.nl * SLOT, tr.nl, scratch, &s_mbar, mphase, tid, s_w, s_M, s_L, a.flag,
+                      acc);
+  float* rows = reinterpret_cast<float*>(scratch);
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    const int u = tid + 256 * k;
+    if (u < 2 * D) {
+      const float L = s_L[u / (D / 4)];
+      const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+      reinterpret_cast<float4*>(rows)[u] =
+          make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+    }
+  }
+  named_bar(1, 256);
+  {
+    const int r = warp;  // 8 warps, 8 rows
+    float2 v[D / 64];
+#pragma unroll
+    for (int e = 0; e < D / 64; ++e) v[e] = reinterpret_cast<const float2*>(rows + r * D)[32 * e + lane];
+    derotate_store_row<D>(v, lane, nullptr, s_out[r]);
+    if (lane == 0 && s_lse[r]) {
+      const float L = s_L[r];
+      *s_lse[r] = (L > 0.0f) ? (s_M[r] + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+}
 
 // ---------------------------------------------------------- host launch --
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Rendezvous merge of one slice of the group's output: floats units [u0, u1)
+// of the 8 x D rows (unit u: row u / (D/4), dims 4 (u % (D/4)) .. +4), from the
+// n_split slots at `slots`. Threads tid < nthr (a multiple of 32, >= 256) take
+// part and synchronise on named barrier `bar_id`; `sm` holds
+// 8 n_split + 16 nthr / 32 floats. The partials sit in L2, so the cost is
+// dependent round trips: every thread issues its (m, l) loads and its first
+// batch of partial loads before it waits on any; row maxima and sums are
+// reduced by all threads at once (the (m, l) entries a thread holds all belong
+// to row tid % 8); each output unit is summed by k consecutive lanes and
+// reduced with shuffles.
+template <int D>
+__device__ __forceinline__ void merge_slice(const float* slots, int n_split, int u0, int u1, int tid, int nthr,
+                                            float* sm, float* const* out_rows, float* const* lse_rows,
+                                            bool write_lse, int bar_id) {
+  constexpr int U = D / 4;                               // float4 units per row
+  constexpr int64_t SLOT = merge_slot_floats(D);
+  constexpr int64_t SLOT4 = SLOT / 4;
+  constexpr int MLR = 4;                                 // (m, l) pairs per thread in registers
+  constexpr int PB = 8;                                  // partial loads per thread per batch
+  const int nw = nthr >> 5;
+  float* w = sm;                   // [n_split][8] weights
+  float* wmax = w + n_split * 8;   // [nw][8] per-warp row maxima
+  float* wsum = wmax + nw * 8;     // [nw][8] per-warp row sums
+  const float4* part4 = reinterpret_cast<const float4*>(slots);
+  const int n_ml = n_split * 8;
+  const int nu = u1 - u0;
+  const int lane = tid & 31, warp = tid >> 5;
+  int k = 1;  // lanes per unit: a power of two, so a unit's lanes share a warp
+  while (k < 32 && 2 * k * nu <= nthr) k *= 2;
+  const int cs = nthr / k;
+  const int ui = tid / k, sub = tid % k;
+  auto ml_at = [&](int i) {  // (max, sum) of entry i = slot * 8 + row
+    const float* p = slots + (int64_t)(i >> 3) * SLOT + 8 * D + (i & 7);
+    return make_float2(__ldcg(p), __ldcg(p + 8));
+  };
+
+  // 1. Loads in flight together.
+  float2 mlv[MLR];
+#pragma unroll
+  for (int j = 0; j < MLR; ++j) {
+    const int i = tid + j * nthr;
+    mlv[j] = (i < n_ml) ? ml_at(i) : make_float2(-INFINITY, 0.0f);
+  }
+  float4 x[PB];
+#pragma unroll
+  for (int j = 0; j < PB; ++j) {
+    const int s = sub + j * k;
+    x[j] = (ui < nu && s < n_split) ? __ldcg(part4 + s * SLOT4 + u0 + ui) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  // 2. Row maxima.
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < MLR; ++j) m = fmaxf(m, mlv[j].x);
+  for (int i = tid + MLR * nthr; i < n_ml; i += nthr) m = fmaxf(m, ml_at(i).x);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  if (lane < 8) wmax[warp * 8 + lane] = m;
+  named_bar(bar_id, nthr);
+  float M = -INFINITY;
+  for (int ww = 0; ww < nw; ++ww) M = fmaxf(M, wmax[ww * 8 + (tid & 7)]);
+  // 3. Weights and row sums.
+  float Ls = 0.0f;
+#pragma unroll
+  for (int j = 0; j < MLR; ++j) {
+    const int i = tid + j * nthr;
+    if (i < n_ml) {
+      const float ws = (mlv[j].x == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(mlv[j].x - M);
+      w[i] = ws;
+      Ls = fmaf(ws, mlv[j].y, Ls);
+    }
+  }
+  for (int i = tid + MLR * nthr; i < n_ml; i += nthr) {
+    const float2 v = ml_at(i);
+    const float ws = (v.x == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(v.x - M);
+    w[i] = ws;
+    Ls = fmaf(ws, v.y, Ls);
+  }
+  Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
+  Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
+  if (lane < 8) wsum[warp * 8 + lane] = Ls;
+  named_bar(bar_id, nthr);
+  if (write_lse && tid < 8 && lse_rows[tid]) {
+    float L = 0.0f;
+    for (int ww = 0; ww < nw; ++ww) L += wsum[ww * 8 + tid];
+    *lse_rows[tid] = (L > 0.0f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  // 4. Weighted sums, reduced over each unit's k lanes.
+  for (int base = 0; base < nu; base += cs) {
+    const int el = base + ui;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int r = 0;
+    if (el < nu) {
+      const int u = u0 + el;
+      r = u / U;
+      int s0 = sub;
+      if (base == 0) {
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+          const int s = sub + j * k;
+          if (s < n_split) {
+            const float ws = w[s * 8 + r];
+            acc.x = fmaf(ws, x[j].x, acc.x);
+            acc.y = fmaf(ws, x[j].y, acc.y);
+            acc.z = fmaf(ws, x[j].z, acc.z);
+            acc.w = fmaf(ws, x[j].w, acc.w);
+          }
+        }
+        s0 = sub + PB * k;
+      }
+      for (; s0 < n_split; s0 += PB * k) {
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+          const int s = s0 + j * k;
+          x[j] = (s < n_split) ? __ldcg(part4 + s * SLOT4 + u) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+          const int s = s0 + j * k;
+          if (s < n_split) {
+            const float ws = w[s * 8 + r];
+            acc.x = fmaf(ws, x[j].x, acc.x);
+            acc.y = fmaf(ws, x[j].y, acc.y);
+            acc.z = fmaf(ws, x[j].z, acc.z);
+            acc.w = fmaf(ws, x[j].w, acc.w);
+          }
+        }
+      }
+    }
+    for (int off = 1; off < k; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if (sub == 0 && el < nu && out_rows[r]) {
+      float L = 0.0f;
+      for (int ww = 0; ww < nw; ++ww) L += wsum[ww * 8 + r];
+      const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+      float* o = out_rows[r] + 4 * ((u0 + el) % U);
+      o[0] = acc.x * inv;
+      o[1] = acc.y * inv;
+      o[2] = acc.z * inv;
+      o[3] = acc.w * inv;
+    }
+  }
+}
+
+// Rendezvous merge, after the epilogue has written this CTA's slot (256
+// consumer threads, named barrier 1, `scratch` holds the merge's shared
+// floats). The wait is bounded: on timeout the device flag is raised and the
+// CTA leaves without merging (the counters are then left non-zero: a
+// workspace whose flag was raised is zeroed before reuse).
+template <int D>
+__device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int split, int64_t gid, int b, int kvh,
+                                                      int rg, int tid, float* scratch) {
+  __shared__ int s_ok;
+  __shared__ float* s_out[8];
+  __shared__ float* s_lse[8];
+  uint32_t* arrive = a.counters + gid * a.ctr_stride;
+  uint32_t* depart = arrive + 1;
+  const uint32_t n = (uint32_t)a.n_split;
+  __threadfence();  // this CTA's slot, released to the group
+  named_bar(1, 256);
+  uint32_t dep = 0;
+  if (tid == 0) {
+    atomicAdd(arrive, 1u);
+    int ok = 1;
+    if (ld_acquire_u32(arrive) < n) {
+      const uint64_t t0 = global_timer_ns();
+      for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_u32(arrive) >= n) break;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+          raise_flag(a.flag, kFlagWaitTimeout);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    // Departure count; its result is needed only at the end.
+    if (ok) dep = atomicAdd(depart, 1u);
+    s_ok = ok;
+  }
+  if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
+  named_bar(1, 256);
+  if (!s_ok) return;
+  const int u0 = (int)((int64_t)split * 2 * D / a.n_split);
+  const int u1 = (int)((int64_t)(split + 1) * 2 * D / a.n_split);
+  merge_slice<D>(a.part + gid * a.n_split * merge_slot_floats(D), a.n_split, u0, u1, tid, 256, scratch, s_out,
+                 s_lse, split == 0, 1);
+  if (tid == 0 && dep + 1 == n) {  // the last CTA to leave: nobody reads the counters any more
+    *arrive = 0u;
+    *depart = 0u;
+  }
+}
+
+// The split merge after the epilogue: rendezvous when the host found the grid
+// co-resident, else the tree.
+template <int D, int SCR>
+__device__ __forceinline__ void decode_split_tail(const DecodeArgs& a, int split, int64_t gid, int b, int kvh,
+                                                  int rg, int tid, uint8_t* scratch) {
+  if (a.rendezvous)
+    rendezvous_merge_tail<D>(a, split, gid, b, kvh, rg, tid, reinterpret_cast<float*>(scratch));
+  else
+    tree_merge_tail<D, SCR>(a, split, gid, b, kvh, rg, tid, scratch);
+}
 
 // Blocks of `kernel` that can be resident at once on the current device.
 template <typename K>
@@ -485,23 +692,26 @@ static inline int coresident_blocks(K kernel, int threads, size_t smem) {
   return sms * per_sm;
 }
 
+// Launch a split decode kernel. The splits merge by rendezvous when the whole
+// grid fits on the device at once, else by the tree. With programmatic stream
+// serialisation the grid may begin while the previous grid on the stream
+// finishes; the kernel waits for it (griddep_wait) before touching global
+// memory, and every one of this grid's CTAs has started before the next grid
+// can begin, so the rendezvous never waits on a CTA that cannot run.
 template <typename K>
-static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, bool cooperative, int threads, size_t smem,
-                                int* cap_cache, cudaStream_t stream) {
+static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, int threads, size_t smem, int* cap_cache,
+                                              cudaStream_t stream) {
   const int64_t grid_total = (int64_t)a.n_split * a.n_row_groups * a.batch * a.n_kv_heads;
-  if (cooperative) {
-    if (*cap_cache == 0) *cap_cache = coresident_blocks(kernel, threads, smem);
-    if (grid_total > *cap_cache || a.n_split > kMaxInKernelSplits) return cudaErrorCooperativeLaunchTooLarge;
-  }
-  a.merge_in_kernel = cooperative ? 1 : 0;
+  if (*cap_cache == 0) *cap_cache = coresident_blocks(kernel, threads, smem);
+  a.rendezvous = (grid_total <= *cap_cache) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = cooperative ? 1 : 0;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, a);

@@ -16,7 +16,9 @@
  * ---------------------------------------
  *  - All tensor pointers are DEVICE pointers owned by the caller. The library
  *    never allocates or frees memory. Scratch space ("workspace") is sized by
- *    the matching *_workspace() query and passed in by the caller.
+ *    the matching *_workspace() query and passed in by the caller, zero-filled
+ *    once before its first use (e.g. cudaMemsetAsync); calls leave its header
+ *    as they found it, so it is reused without clearing.
  *  - Work is enqueued asynchronously on the caller's CUDA stream (`stream` is a
  *    cudaStream_t; NULL means the legacy default stream). Arguments are checked
  *    on the host before anything is launched; a failed check returns a status
@@ -24,8 +26,9 @@
  *  - ckv_last_error() returns a message for the last failure on this thread.
  *  - Kernels that wait on asynchronous copies bound every wait; a wait that
  *    runs out (or a device-side range check that fails) sets a flag in the first
- *    4 bytes of the workspace instead of hanging. ckv_read_device_flag() reads
- *    it after the stream has drained. Each call clears the flag when it starts.
+ *    4 bytes of the workspace instead of hanging. The flag keeps the first
+ *    error of any call since it was last read: ckv_read_device_flag() reads it
+ *    after the stream has drained and clears it.
  *  - Head dims supported: 64, 128, 256, 512. The number of query heads must be
  *    a multiple of the number of KV heads; query head h reads KV head
  *    floor(h / G), G = n_q_heads / n_kv_heads (grouped-query attention, as the
@@ -133,12 +136,14 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
  * Split-K flash-decode: each CTA streams a contiguous range of tile records
  * through shared memory, computes S = Q K_hat^T on tensor cores from the int8
  * codes (scales applied per 32-block), runs the online softmax, and accumulates
- * P V_hat in the rotated basis straight from the 3-bit codes. Each CTA applies
- * the inverse transform and sign flip to its own partial (valid because the
- * rotation is linear and shared within a head: PolyKV page, "S2 perf-path Level
- * B" — the transform runs only on the small FA output); the CTAs of a row group
- * then merge their partials with the exact log-sum-exp combine (a separate
- * merge kernel when the grid cannot be co-resident).
+ * P V_hat in the rotated basis straight from the 3-bit codes. Each CTA writes
+ * its partial to the workspace; the CTAs that finish last merge the partials
+ * of their row group with the exact log-sum-exp combine (a two-level tree,
+ * no CTA waiting for another) and apply the inverse transform and sign flip
+ * once per output row (valid because the rotation is linear and shared within
+ * a head: PolyKV page, "S2 perf-path Level B" — the transform runs only on the
+ * small FA output). One kernel launch; it may begin while the previous kernel
+ * on the stream finishes, and waits for it before touching global memory.
  *
  * seq_len: device int32 [batch], each in [0, min(capacity, max_seq_len)]; a
  *   value outside that range raises the device flag and counts as 0.
@@ -146,9 +151,11 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
  *   [0, min(capacity, max_seq_len)), and tiles past seq_len are skipped.
  * q_f16: device fp16 [batch][n_q][n_q_heads][D].
  * scale: logit scale (e.g. 1/sqrt(D)).
- * n_split: KV splits per (sequence, kv head, row group); 0 picks one that fills
- *   the GPU. out: float32 [batch][n_q][n_q_heads][D]; lse: float32 [batch][n_q][n_q_heads].
- * workspace: ckv_attn_decode_workspace() bytes, 256-byte aligned.
+ * n_split: KV splits per (sequence, kv head, row group), at most 1024; 0 picks
+ *   one that fills the GPU. out: float32 [batch][n_q][n_q_heads][D]; lse:
+ *   float32 [batch][n_q][n_q_heads].
+ * workspace: ckv_attn_decode_workspace() bytes, 256-byte aligned, zero-filled
+ *   before first use; its merge counters are back at zero after every call.
  */
 CKV_API size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q,
                                  int32_t n_q_heads, int32_t n_split);
@@ -193,9 +200,10 @@ CKV_API ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t*
  * scratch is a 4 MiB array compiled into the library (held on every device that
  * loads it until the process exits); a call whose scratch would exceed it (see
  * ckv_attn_decode_workspace) returns CKV_ERR_WORKSPACE. Nothing is allocated.
- * Every call shares that one array and it keeps the last call's contents: each
- * call clears what must start at zero, but calls that overlap on the GPU race
- * and give wrong results (order them on one stream or with events). The first
+ * Every call shares that one array (zero when the library loads; every call
+ * leaves its header at zero, except the device flag after an error); calls
+ * that overlap on the GPU race and give wrong results (order them on one
+ * stream or with events). The first
  * call on a device looks up the array's address on that device; make that
  * first call before any stream capture on the device.
  */
@@ -253,7 +261,8 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
                             void* workspace, size_t ws_bytes, void* stream);
 
 /* Synchronously read the device flag (first 4 bytes of a workspace) after draining
- * `stream`. *flag receives it; returns CKV_ERR_DEVICE_FLAG when it is nonzero. */
+ * `stream`. *flag receives it; when it is nonzero the flag is cleared and
+ * CKV_ERR_DEVICE_FLAG returned. */
 CKV_API ckv_status ckv_read_device_flag(const void* workspace, int32_t* flag, void* stream);
 
 /* Message for the last failure on the calling thread ("" if none). */

@@ -72,7 +72,9 @@ def test_decode_argument_checks(lib):
     fake = 0x7f0000000000
     c = _fake_cache(D=512, Hkv=2, cap=4096)
     need = lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 1, 16, 8)
-    assert need == 256 + 2 * 8 * 8 * (512 + 2) * 4
+    # header (flag, 2 groups x (3 leaves + root) counters) in 256 bytes; per group
+    # 8 partial slots + 3 leaf slots (leaves of ceil(sqrt(8)) = 3 splits) of 8 x 512 + 16 floats
+    assert need == 256 + 2 * (8 + 3) * (8 * 512 + 16) * 4
     assert lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 1, 15, 8) == 0  # 15 % 2 != 0
     args = lambda **kw: dict(dict(seq=fake, maxs=4096, q=fake, nq=1, hq=16, scale=0.04, ns=8, out=fake,
                                   lse=fake, ws=fake, wsb=need), **kw)
@@ -89,13 +91,15 @@ def test_decode_argument_checks(lib):
     assert call(ws=fake + 16) == -3               # workspace must be 256-byte aligned
     assert call(scale=float("nan")) == -1
     assert call(ns=-1) == -1
+    assert call(ns=1025) == -1                    # at most 1024 splits
     assert call(cache=_fake_cache(D=100)) == -2
 
 
 def test_decode_f16_and_merge_argument_checks(lib):
     fake = 0x7f0000000000
     need = lib.ckv_attn_decode_f16_workspace(512, 2, 15, 512, 1, 16, 4)
-    assert need == 256 + 15 * 2 * 4 * 8 * 514 * 4
+    # 30 groups: counters 64 + 30 x 3 x 4 bytes -> 512; 4 partial + 2 leaf slots each
+    assert need == 512 + 15 * 2 * (4 + 2) * (8 * 512 + 16) * 4
     assert lib.ckv_attn_decode_f16(fake, fake, 512, 2, 15, 500, fake, 512, fake, 1, 16, 0.04, 4, fake, fake,
                                    fake, need, None) == -1  # capacity not a multiple of 16
     assert lib.ckv_attn_decode_f16(fake + 8, fake, 512, 2, 15, 512, fake, 512, fake, 1, 16, 0.04, 4, fake,

@@ -59,7 +59,7 @@ def _run(D, Hkv, Hq, lens, n_new, cap, n_split, seed):
     for kind, cache in (("append", fused), ("decode", ref)):
         out = torch.full((B, 1, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
         lse = torch.full((B, 1, Hq), float("nan"), dtype=torch.float32, device=DEV)
-        ws = torch.empty(ckv.attn_decode_workspace(cache, maxs, 1, Hq, n_split), dtype=torch.uint8, device=DEV)
+        ws = torch.zeros(ckv.attn_decode_workspace(cache, maxs, 1, Hq, n_split), dtype=torch.uint8, device=DEV)
         if kind == "append":
             ckv.attn_decode_append(cache, seq, maxs, k_new, v_new, q, scale, out, lse, ws, n_split=n_split)
         else:

@@ -70,7 +70,7 @@ def run_decode(cache, q, seq_lens, max_seq_len, n_split=0):
     qd = to_dev(q)
     out = torch.empty((B, n_q, Hq, D), dtype=torch.float32, device=DEV)
     lse = torch.empty((B, n_q, Hq), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ckv.attn_decode_workspace(cache, max_seq_len, n_q, Hq, n_split), dtype=torch.uint8,
+    ws = torch.zeros(ckv.attn_decode_workspace(cache, max_seq_len, n_q, Hq, n_split), dtype=torch.uint8,
                      device=DEV)
     sl = torch.tensor(seq_lens, dtype=torch.int32, device=DEV)
     ckv.attn_decode(cache, sl, max_seq_len, qd, 1.0 / math.sqrt(D), out, lse, ws, n_split=n_split)
@@ -146,7 +146,9 @@ def test_tiny_decode_workload():
 
 @pytest.mark.parametrize("D,Hkv,Hq,n_q", [(64, 2, 4, 1), (128, 1, 4, 2), (128, 2, 16, 1), (256, 2, 8, 3),
                                           (512, 2, 16, 1), (512, 1, 8, 2), (512, 2, 4, 1)])
-@pytest.mark.parametrize("n_split", [0, 1, 5])
+# 40 and 300 splits exceed the 13-14 tiles (empty partials) and give merge
+# trees of 7 and 18-slot leaves (several bulk-copy chunks per merge).
+@pytest.mark.parametrize("n_split", [0, 1, 5, 40, 300])
 def test_decode_shapes_ragged(D, Hkv, Hq, n_q, n_split):
     _need_gpu()
     B, T, cap = 3, 203, 224
@@ -167,16 +169,19 @@ def test_decode_seq_len_out_of_range_sets_flag():
     k, v, outl = make_kv(D, 1, 1, T, seed=3, n_out=1)
     q = inputs.normal_tensor((1, 1, 4, D), 3, "q", outl)
     cache = gpu_pack(k, v, inputs.tbq_signs(D), T)
-    ws = torch.empty(ckv.attn_decode_workspace(cache, T, 1, 4), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ckv.attn_decode_workspace(cache, T, 1, 4), dtype=torch.uint8, device=DEV)
     out = torch.empty((1, 1, 4, D), dtype=torch.float32, device=DEV)
     lse = torch.empty((1, 1, 4), dtype=torch.float32, device=DEV)
     sl = torch.tensor([T + 16], dtype=torch.int32, device=DEV)   # beyond max_seq_len
     ckv.attn_decode(cache, sl, T, to_dev(q), 0.1, out, lse, ws)
-    assert ckv.read_device_flag(ws) == 2
+    assert ckv.read_device_flag(ws) == 2                             # reading clears it
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))   # treated as empty, no read past the end
+    assert ckv.read_device_flag(ws) == 0
     sl.fill_(T)
     ckv.attn_decode(cache, sl, T, to_dev(q), 0.1, out, lse, ws)
-    assert ckv.read_device_flag(ws) == 0                             # cleared by the next call
+    assert ckv.read_device_flag(ws) == 0
+    ckv.attn_decode(cache, sl, T, to_dev(q), 0.1, out, lse, ws)    # the workspace is reused as is
+    assert ckv.read_device_flag(ws) == 0
 
 
 # ----------------------------------------------------------- fp16 decode ----
@@ -185,7 +190,7 @@ def run_decode_f16(k16, v16, q, seq_lens, max_seq_len, n_split=0):
     B, n_q, Hq, D = q.shape
     out = torch.empty((B, n_q, Hq, D), dtype=torch.float32, device=DEV)
     lse = torch.empty((B, n_q, Hq), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ckv.attn_decode_f16_workspace(D, k16.shape[1], B, max_seq_len, n_q, Hq, n_split),
+    ws = torch.zeros(ckv.attn_decode_f16_workspace(D, k16.shape[1], B, max_seq_len, n_q, Hq, n_split),
                      dtype=torch.uint8, device=DEV)
     sl = torch.tensor(seq_lens, dtype=torch.int32, device=DEV)
     ckv.attn_decode_f16(k16, v16, sl, max_seq_len, to_dev(q), 1.0 / math.sqrt(D), out, lse, ws,
@@ -195,7 +200,8 @@ def run_decode_f16(k16, v16, q, seq_lens, max_seq_len, n_split=0):
 
 
 @pytest.mark.parametrize("D,Hkv,Hq,n_q", [(64, 1, 2, 1), (128, 2, 8, 2), (256, 1, 8, 1), (512, 2, 16, 1)])
-def test_decode_f16_matches_oracle(D, Hkv, Hq, n_q):
+@pytest.mark.parametrize("n_split", [0, 37])
+def test_decode_f16_matches_oracle(D, Hkv, Hq, n_q, n_split):
     _need_gpu()
     B, cap = 3, 144
     seq_lens = [144, 77, 0]
@@ -208,8 +214,8 @@ def test_decode_f16_matches_oracle(D, Hkv, Hq, n_q):
     for b in range(B):
         o_ref[b], lse_ref[b] = O.decode_reference(q[b], k[b].astype(np.float64), v[b].astype(np.float64),
                                                   seq_lens[b], 1.0 / math.sqrt(D))
-    o, l = run_decode_f16(to_dev(k), to_dev(v), q, seq_lens, cap)
-    H.check_attention(o, l, o_ref, lse_ref, f"f16 D={D}")
+    o, l = run_decode_f16(to_dev(k), to_dev(v), q, seq_lens, cap, n_split=n_split)
+    H.check_attention(o, l, o_ref, lse_ref, f"f16 D={D} n_split={n_split}")
 
 
 # -------------------------------------------------------------- lse_merge ---

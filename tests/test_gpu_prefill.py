@@ -31,7 +31,7 @@ def _case(D, Hkv, Hq, B, n_cached, n_new, cap, seed):
         ckv.kv_pack(cache, 0, kd[:, :n_cached].contiguous(), vd[:, :n_cached].contiguous())
     out = torch.full((B, n_new, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
     lse = torch.full((B, n_new, Hq), float("nan"), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ckv.attn_prefill_workspace(cache, n_new, Hq), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ckv.attn_prefill_workspace(cache, n_new, Hq), dtype=torch.uint8, device=DEV)
     ckv.attn_prefill(cache, n_cached, q.to(DEV), kd[:, n_cached:].contiguous(), vd[:, n_cached:].contiguous(),
                      1.0 / math.sqrt(D), out, lse, ws)
     torch.cuda.synchronize()

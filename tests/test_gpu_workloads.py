@@ -74,7 +74,7 @@ def test_fanout_decode_full():
     qd = to_dev(qa[:, None])
     o_t = torch.empty((A, 1, Hq, D), dtype=torch.float32, device=DEV)
     l_t = torch.empty((A, 1, Hq), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ckv.attn_decode_f16_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ckv.attn_decode_f16_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8, device=DEV)
     ckv.attn_decode_f16(to_dev(kt), to_dev(vt), torch.full((A,), TL, dtype=torch.int32, device=DEV), TL,
                         qd, scale, o_t, l_t, ws)
     out = torch.empty((A * Hq, D), dtype=torch.float32, device=DEV)
@@ -109,7 +109,7 @@ def test_long_decode_sampled():
     ckv.kv_pack(cache, 0, k, v)
     out = torch.empty((B, 1, Hq, D), dtype=torch.float32, device=DEV)
     lse = torch.empty((B, 1, Hq), dtype=torch.float32, device=DEV)
-    ws = torch.empty(ckv.attn_decode_workspace(cache, T, 1, Hq), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ckv.attn_decode_workspace(cache, T, 1, Hq), dtype=torch.uint8, device=DEV)
     sl = torch.full((B,), T, dtype=torch.int32, device=DEV)
     ckv.attn_decode(cache, sl, T, q, 1.0 / math.sqrt(D), out, lse, ws)
     assert ckv.read_device_flag(ws) == 0

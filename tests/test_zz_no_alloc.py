@@ -43,7 +43,7 @@ def _both(cache, q, sl, max_len):
     scale = 1.0 / math.sqrt(D)
     out_a = torch.empty((B, n_q, Hq, D), dtype=torch.float32, device="cuda")
     lse_a = torch.empty((B, n_q, Hq), dtype=torch.float32, device="cuda")
-    ws = torch.empty(ckv.attn_decode_workspace(cache, max_len, n_q, Hq), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ckv.attn_decode_workspace(cache, max_len, n_q, Hq), dtype=torch.uint8, device="cuda")
     ckv.attn_decode(cache, sl, max_len, q, scale, out_a, lse_a, ws)
     out_b = torch.full_like(out_a, float("nan"))
     lse_b = torch.full_like(lse_a, float("nan"))
