@@ -49,6 +49,7 @@ struct CDec : DecodeShape<D> {
   static constexpr int THREADS = (Sh::NCW + 1) * 32;
   static constexpr int VW = 3 * Sh::MT_W / 4;   // V-code words per lane per warp
   static constexpr int GR = v_granule(D);       // stream granule bytes
+  static constexpr bool PSPLIT = D <= 128;      // P' as an fp16 hi + lo pair
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
   static constexpr int RING = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
   static constexpr int OFF_XCHG = (RING + 127) / 128 * 128;
@@ -160,7 +161,8 @@ __device__ __forceinline__ void q_block_bias(const uint32_t (&qf)[NBW][4], int l
 // so the address is one AND-OR of the shifted field with the lane offset.
 template <int D>
 __device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_t lane4, int wh, int lane,
-                                        uint32_t pb0, uint32_t pb1, float (&acc)[CDec<D>::MT_W][4]) {
+                                        uint32_t pb0, uint32_t pb1, const uint32_t (&pl)[2],
+                                        float (&acc)[CDec<D>::MT_W][4]) {
   using C = CDec<D>;
   uint32_t vw[C::VW];
 #pragma unroll
@@ -173,6 +175,7 @@ __device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_
     for (int j = 0; j < 4; ++j)
       av[j] = *reinterpret_cast<const uint32_t*>(lut + (field_x128<C::VW>(vw, 6 * (4 * i + j)) | lane4));
     mma16816(acc[i], av[0], av[1], av[2], av[3], pb0, pb1);
+    if constexpr (CDec<D>::PSPLIT) mma16816(acc[i], av[0], av[1], av[2], av[3], pl[0], pl[1]);
   }
 }
 
@@ -223,8 +226,8 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   } else {
     for (int e = threadIdx.x; e < 64 * 32; e += C::NCW * 32) {
       const int f = e >> 5;
-      const __half lo = __float2half_rn(centroid(f & 7));
-      const __half hi = __float2half_rn(centroid(f >> 3));
+      const __half lo = __float2half_rn(centroid(f & 7) * (1.0f / kCentroidScale));
+      const __half hi = __float2half_rn(centroid(f >> 3) * (1.0f / kCentroidScale));
       s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
   }
@@ -406,10 +409,10 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
       const int64_t tpos = tile * kTile;
       const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * g)));
       const float n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * (g + 8))));
-      uint32_t pb0, pb1;
-      softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, scale_log2, n0, n1, st, acc, pb0,
-                            pb1);
-      pv_tile<D>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, acc);
+      uint32_t pb0, pb1, pl[2] = {0u, 0u};
+      softmax_tile<C::MT_W, C::PSPLIT>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, scale_log2, n0, n1, st, acc,
+                                       pb0, pb1, pl);
+      pv_tile<D>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, pl, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[it % C::NSTAGE]);

@@ -17,6 +17,7 @@ template <int D>
 struct FDec : DecodeShape<D> {
   using Sh = DecodeShape<D>;
   static constexpr int THREADS = Sh::NCW * 32;
+  static constexpr bool PSPLIT = D <= 128;  // P' as an fp16 hi + lo pair
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
   static constexpr int OFF_XCHG = (RED_BYTES + 127) / 128 * 128;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
@@ -85,9 +86,9 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
       mma16816(S, k0.z, k1.z, k0.w, k1.w, qf[i][2], qf[i][3]);
     }
     if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, it & 1, lane);
-    uint32_t pb0, pb1;
-    softmax_tile<C::MT_W>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, 1.0f, 1.0f,
-                          st, acc, pb0, pb1);
+    uint32_t pb0, pb1, pl[2] = {0u, 0u};
+    softmax_tile<C::MT_W, C::PSPLIT>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, a.scale_log2, 1.0f, 1.0f,
+                                     st, acc, pb0, pb1, pl);
     // ---- O^T += V^T P^T: lane reads positions 2t, 2t+1, 2t+8, 2t+9 ----
     const __half* vp = vb + tpos * D + dbase;
 #pragma unroll
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
         asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a2) : "r"(xe[j]), "r"(xo[j]));
         asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a3) : "r"(xe[j]), "r"(xo[j]));
         mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pb0, pb1);
+        if constexpr (C::PSPLIT) mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pl[0], pl[1]);
       }
     }
   }

@@ -26,15 +26,38 @@
 // cache).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "../../include/ckv.h"
 #include "ckv_kernels.cuh"
-#include "prefill_common.cuh"
 
 namespace ckv {
 
 namespace {
+
+struct PrefillArgs {
+  const uint8_t* cache;
+  int64_t capacity;
+  int n_kv_heads, batch;
+  int64_t n_cached;
+  int n_new, n_q_heads;
+  const __nv_bfloat16* q;  // [batch][n_new][n_q_heads][D]
+  float scale_log2;
+  float* out;              // [batch][n_new][n_q_heads][D]
+  float* lse;              // [batch][n_new][n_q_heads]
+  int32_t* flag;
+  // Stream-K schedule (stream_k = 1): CTA c takes the 64-key steps
+  // [c W / grid, (c + 1) W / grid) of all tiles laid end to end (tile
+  // t = (b * n_kv_heads + kv_head) * n_q_tiles + q_tile); a tile is cut at
+  // most once. The part before a cut at CTA c goes to slot 2c, the part after
+  // it to slot 2c + 1 (slot: [128 rows][D] normalised rotated-basis rows, then
+  // [128] lse), and tile_split[t] = c; whole tiles write their rows to `out`
+  // and tile_split[t] = -1. Otherwise (stream_k = 0) CTA t runs tile t.
+  int stream_k;
+  float* part;
+  int32_t* tile_split;
+};
 
 __constant__ float kPrefillCentroids[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
                                            0.2451f,  0.7560f,  1.3439f,  2.1520f};
@@ -53,7 +76,12 @@ struct PCfg {
   static constexpr int NORM_OFF = P_OFF + M * NKV * 2;
   static constexpr int LUT_OFF = NORM_OFF + NKV * 4;        // 64 centroid pairs x 32 lanes
   static constexpr int SCALE_OFF = LUT_OFF + 64 * 32 * 4; // two steps' q8_0 scales
-  static constexpr int BYTES = SCALE_OFF + 2 * NKV * NB * 2;
+  // Up to head dim 128, P' enters the P.V product as the fp16 pair hi (P_OFF)
+  // + lo (P_LO_OFF): fp16 rounding of P' alone costs up to 2.7e-3 of |o|_inf
+  // at head dim 64 over long rows (2.1e-3 at 128; 1.4e-3 at 256, 8e-4 at 512).
+  static constexpr bool PSPLIT = D <= 128;
+  static constexpr int P_LO_OFF = (SCALE_OFF + 2 * NKV * NB * 2 + 1023) / 1024 * 1024;
+  static constexpr int BYTES = PSPLIT ? P_LO_OFF + M * NKV * 2 : SCALE_OFF + 2 * NKV * NB * 2;
   // At least half the SM's shared memory, so that one CTA (and its 512 TMEM
   // columns) owns each SM.
   static constexpr int SMEM = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);
@@ -87,14 +115,20 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   __half* sScale = reinterpret_cast<__half*>(smem + C::SCALE_OFF);
 
   const int group_q = a.n_q_heads / a.n_kv_heads;
-  const int QT = C::M / group_q;                   // query tokens per CTA
-  const int q0 = blockIdx.x * QT;
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int last_q = min(q0 + QT, a.n_new) - 1;
-  const int64_t kv_end = a.n_cached + last_q + 1;  // keys any row of this tile can see
-  const int n_steps = static_cast<int>((kv_end + C::NKV - 1) / C::NKV);
+  const int QT = C::M / group_q;  // query tokens per tile
+  const int n_qt = (a.n_new + QT - 1) / QT;
   const int64_t n_rec = a.capacity / kTile;
-  const uint8_t* stream = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * n_rec * C::REC;
+  // 64-key steps of query tile qt: its rows see keys [0, n_cached + last row].
+  auto steps_of = [&](int qt) {
+    const int64_t kv_end = a.n_cached + min((qt + 1) * QT, a.n_new);
+    return static_cast<int>((kv_end + C::NKV - 1) / C::NKV);
+  };
+
+  // The tile being run, set per segment (CTA-uniform, kept in shared memory
+  // so that the step loop does not hold it in registers).
+  __shared__ int s_q0, s_kvh, s_b, s_s0;
+  __shared__ const uint8_t* s_stream;
+  __shared__ float* s_slot;  // nullptr: rows to `out`
 
   if (warp == 0) tmem_alloc(&s_tmem, 512);
   if (tid == 0) {
@@ -102,15 +136,28 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     s_abort = 0;
     fence_barrier_init();
   }
+  // Centroid pairs: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]) / kCentroidScale,
+  // one copy per lane (the de-rotation multiplies the scale back).
+  for (int e = tid; e < 64 * 32; e += C::THREADS) {
+    const int f = e >> 5;
+    sLut[e] = pack_half2(kPrefillCentroids[f & 7] * (1.0f / kCentroidScale),
+                         kPrefillCentroids[f >> 3] * (1.0f / kCentroidScale));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
 
   // ---- Q tile: bf16 -> fp16 (exact in range), 128-byte swizzled K-major ----
+  auto load_q = [&]() {
   for (int piece = tid; piece < C::M * (D / 8); piece += C::THREADS) {
     const int r = piece / (D / 8), k0 = (piece % (D / 8)) * 8;
-    const int qi = q0 + r / group_q, h = kvh * group_q + r % group_q;
+    const int qi = s_q0 + r / group_q, h = s_kvh * group_q + r % group_q;
     uint4 outv = make_uint4(0, 0, 0, 0);
     if (qi < a.n_new) {
       const uint4 v =
-          *reinterpret_cast<const uint4*>(a.q + (((int64_t)b * a.n_new + qi) * a.n_q_heads + h) * D + k0);
+          *reinterpret_cast<const uint4*>(a.q + (((int64_t)s_b * a.n_new + qi) * a.n_q_heads + h) * D + k0);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t o[4];
 #pragma unroll
@@ -122,23 +169,11 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     }
     *reinterpret_cast<uint4*>(sQ + sw128_offset(r, k0, C::M)) = outv;
   }
-  // Centroid pairs: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]), one copy per lane.
-  for (int e = tid; e < 64 * 32; e += C::THREADS) {
-    const int f = e >> 5;
-    sLut[e] = pack_half2(kPrefillCentroids[f & 7], kPrefillCentroids[f >> 3]);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+  };
 
-  // Per-row state (warps 0-3: thread = row).
+  // Rows: warps 0-3, thread = row (query token s_q0 + row / G, head row % G).
   const bool softmax_warp = warp < 4;
   const int row = tid & 127;
-  const int row_qi = q0 + row / group_q;
-  const bool row_valid = row_qi < a.n_new;
-  const int64_t row_limit = a.n_cached + row_qi;  // last key this row sees
   const uint32_t row_tmem = tmem + ((uint32_t)(warp & 3) * 32u << 16);
 
   uint32_t phase = 0;
@@ -191,6 +226,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   uint2 ksc = make_uint2(0, 0);
   float nrm = 0.0f;
   auto fetch = [&](int step) {
+    const uint8_t* stream = s_stream;
     const int64_t rec0 = (int64_t)step * (C::NKV / kTile);
 #pragma unroll
     for (int r = 0; r < KR; ++r) {
@@ -217,6 +253,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   // V codes of a step (value warps), loaded once the previous step's build
   // has consumed them.
   auto fetch_v = [&](uint32_t (&vw)[NW], int step) {
+    const uint8_t* stream = s_stream;
     const int64_t rec0 = (int64_t)step * (C::NKV / kTile);
     {
       const int64_t rec = rec0 + vr4;
@@ -246,11 +283,6 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   auto put_scales = [&](int buf) {
     if (tid < NSW) *reinterpret_cast<uint2*>(sScale + buf * C::NKV * C::NB + tid * 4) = ksc;
   };
-  if (n_steps > 0) {
-    fetch(0);
-    put_scales(0);
-  }
-  __syncthreads();
 
   // C^T (centroids, rotated basis): rows = dims, K = tokens. A 6-bit field
   // pairs the codes of two adjacent positions of one dim, which is one fp16x2
@@ -274,7 +306,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   // The two roles run the same barriers and MMA waits; each role's state
   // (the softmax rows' running max, sum and register tail; the value warps'
   // code words) exists only on its own path.
-  auto role_loop = [&](auto role) {
+  // Steps [s_s0, s1) of the current tile; the rows go to `out` (s_slot
+  // nullptr) or to a partial slot of the stream-K schedule.
+  auto role_loop = [&](auto role, int s1) {
     constexpr bool SM = decltype(role)::value;  // softmax warps (rows) or value warps
     float m_used = -INFINITY, l_sum = 0.0f;
     float otail[SM && C::OR > 0 ? C::OR : 1];
@@ -282,29 +316,29 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     for (int i = 0; i < (SM && C::OR > 0 ? C::OR : 1); ++i) otail[i] = 0.0f;
     uint32_t vw[SM ? 1 : NW];
     if constexpr (!SM) {
-      if (n_steps > 0) fetch_v(vw, 0);
+      if (s_s0 < s1) fetch_v(vw, s_s0);
     }
-    for (int step = 0; step < n_steps; ++step) {
+    for (int step = s_s0; step < s1; ++step) {
       const int64_t j0 = (int64_t)step * C::NKV;
       // ---- K_hat = q * d16 split into fp16 hi (to shared memory) + lo (kept) ----
       // q is an exact fp16 integer; hi = q*d rounded once (HMUL2 of exact fp16
       // operands) and lo = fma(q, d, -hi), the exact residual (HFMA2).
       uint32_t lo_keep[KR][8];
       const __half* scb = sScale + (step & 1) * C::NKV * C::NB;
-  #pragma unroll
+#pragma unroll
       for (int r = 0; r < KR; ++r) {
         const int g = r * C::THREADS + warp * 32;
         const int blk = (g % D) / 32;
         const int row0 = (g / D) * kTile + kpp;  // tokens row0 and row0 + 8 of the step
         const uint32_t w[4] = {kw[r].x, kw[r].y, kw[r].z, kw[r].w};
-  #pragma unroll
+#pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
           const __half d = scb[(row0 + 8 * hs) * C::NB + blk];
           const __half2 dd = __halves2half2(d, d);
           uint32_t qh[4], hi[4];
           i8x4_to_half2x2(w[2 * hs], qh[0], qh[1]);
           i8x4_to_half2x2(w[2 * hs + 1], qh[2], qh[3]);
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 4; ++e) {
             const __half2 qv = *reinterpret_cast<const __half2*>(&qh[e]);
             const __half2 h = __hmul2(qv, dd);
@@ -330,15 +364,15 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       // The next step's loads are issued while the tensor core runs this pass;
       // warp 0, whose MMA issue blocks until the pass drains, loads during the
       // second pass instead (its softmax has slack against the value build).
-      if (warp != 0 && step + 1 < n_steps) fetch(step + 1);
+      if (warp != 0 && step + 1 < s1) fetch(step + 1);
       wait_mma();
       // ---- lo pass ----
-  #pragma unroll
+#pragma unroll
       for (int r = 0; r < KR; ++r) {
         const int g = r * C::THREADS + warp * 32;
         const int blk = (g % D) / 32;
         const int row0 = (g / D) * kTile + kpp;
-  #pragma unroll
+#pragma unroll
         for (int hs = 0; hs < 2; ++hs)
           *reinterpret_cast<uint4*>(sKV + sw128_offset(row0 + 8 * hs, blk * 32 + 8 * kq, C::NKV)) =
               make_uint4(lo_keep[r][4 * hs], lo_keep[r][4 * hs + 1], lo_keep[r][4 * hs + 2], lo_keep[r][4 * hs + 3]);
@@ -348,7 +382,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         issue_s();
         umma_commit(&s_bar);
       }
-      if (warp == 0 && step + 1 < n_steps) fetch(step + 1);
+      if (warp == 0 && step + 1 < s1) fetch(step + 1);
       // While the second pass runs, the value warps load the table entries of
       // their first VPRE fields (the stores wait for the K tile to free).
       uint32_t vpre[SM ? 1 : VPRE];
@@ -357,7 +391,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         for (int u = 0; u < VPRE; ++u) vpre[u] = v_field(vw, u);
       }
       wait_mma();
-      if (step + 1 < n_steps) put_scales((step + 1) & 1);  // read after this step's last barrier
+      if (step + 1 < s1) put_scales((step + 1) & 1);  // read after this step's last barrier
 
       if constexpr (SM) {
         // ---- online softmax of this step's 64 columns, one row per thread ----
@@ -366,12 +400,13 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         tmem_ld32(row_tmem + 32, sv[1]);
         tmem_ld_wait();
         // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
-        const int64_t rel = row_valid ? row_limit - j0 + 1 : 0;
+        const int row_qi = s_q0 + row / group_q;
+        const int64_t rel = row_qi < a.n_new ? a.n_cached + row_qi - j0 + 1 : 0;
         const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
         const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
         float x[C::NKV];
         float mt = -INFINITY;
-  #pragma unroll
+#pragma unroll
         for (int j = 0; j < C::NKV; ++j) {
           const float v = __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2;
           x[j] = (all_vis || j < nvis) ? v : -INFINITY;
@@ -381,20 +416,20 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         const bool need = (m_new > m_used + 4.0f);  // also true when m_used is -inf and a key is visible
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? ((m_used == -INFINITY) ? 0.0f : fast_exp2(m_used - m_new)) : 1.0f;
-          if (step > 0) {
+          if (step > s_s0) {
             // Rescale O in TMEM (initialised by the first P.V) and the register tail.
-  #pragma unroll 1
+#pragma unroll 1
             for (int c0 = 64; c0 < 64 + C::OT; c0 += 32) {
               uint32_t ov[32];
               tmem_ld32(row_tmem + c0, ov);
               tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
               tmem_st32(row_tmem + c0, ov);
             }
             tmem_st_wait();
           }
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < C::OR; ++i) otail[i] *= f;
           l_sum *= f;
           if (need) m_used = m_new;
@@ -403,21 +438,33 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
         float ps = 0.0f;
         uint32_t pw[C::NKV / 2];
+        uint32_t pwl[C::PSPLIT ? C::NKV / 2 : 1];
         const float4* n4 = reinterpret_cast<const float4*>(sNorm);
-  #pragma unroll
+        auto pack_p = [&](int i, float y0, float y1) {  // P' pair i: fp16 hi, and lo when split
+          pw[i] = pack_half2(y0, y1);
+          if constexpr (C::PSPLIT) {
+            const __half2 h = *reinterpret_cast<const __half2*>(&pw[i]);
+            pwl[i] = pack_half2(y0 - __low2float(h), y1 - __high2float(h));
+          }
+        };
+#pragma unroll
         for (int j = 0; j < C::NKV; j += 4) {
           const float4 nn = n4[j / 4];
           const float p0 = fast_exp2(x[j] - mref), p1 = fast_exp2(x[j + 1] - mref);
           const float p2 = fast_exp2(x[j + 2] - mref), p3 = fast_exp2(x[j + 3] - mref);
           ps += (p0 + p1) + (p2 + p3);
-          pw[j / 2] = pack_half2(p0 * nn.x, p1 * nn.y);
-          pw[j / 2 + 1] = pack_half2(p2 * nn.z, p3 * nn.w);
+          pack_p(j / 2, p0 * nn.x, p1 * nn.y);
+          pack_p(j / 2 + 1, p2 * nn.z, p3 * nn.w);
         }
         l_sum += ps;
-  #pragma unroll
-        for (int c = 0; c < C::NKV / 8; ++c)
+#pragma unroll
+        for (int c = 0; c < C::NKV / 8; ++c) {
           *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * c, C::M)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+          if constexpr (C::PSPLIT)
+            *reinterpret_cast<uint4*>(smem + C::P_LO_OFF + sw128_offset(row, 8 * c, C::M)) =
+                make_uint4(pwl[4 * c], pwl[4 * c + 1], pwl[4 * c + 2], pwl[4 * c + 3]);
+        }
       } else {
         // ---- C^T for the step: the prefetched fields, then the rest ----
 #pragma unroll
@@ -425,27 +472,30 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         // Table loads are issued in batches ahead of their stores, so one
         // shared-memory latency is exposed per batch rather than per field.
         constexpr int VB = G < 16 ? G : 16;  // divides the G fields left
-  #pragma unroll
+#pragma unroll
         for (int pb = VPRE; pb < 2 * G; pb += VB) {
           uint32_t val[VB];
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < VB; ++u) val[u] = v_field(vw, pb + u);
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < VB; ++u) v_store(pb + u, val[u]);
         }
-        if (step + 1 < n_steps) fetch_v(vw, step + 1);
+        if (step + 1 < s1) fetch_v(vw, step + 1);
       }
       sync_for_mma();
       if (SM && tid == 0) {
         // ---- O += P' C over the step's 64 tokens ----
         for (int ks = 0; ks < C::NKV / 16; ++ks) {
           const uint64_t ad = umma_desc_sw128(p_base + ks * 32);
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 3; ++c) {
             if (chunks[c].n == 0) continue;
             const uint64_t bd = umma_desc_sw128(kv_base + chunks[c].dim0 * 128 + ks * 32);
-            const bool acc = (c == 2) ? (ks > 0) : (step > 0 || ks > 0);
+            const bool acc = (c == 2) ? (ks > 0) : (step > s_s0 || ks > 0);
             umma_f16(tmem + chunks[c].col, ad, bd, umma_idesc_f16_f32(C::M, chunks[c].n), acc);
+            if constexpr (C::PSPLIT)  // the lo half of P' into the same accumulator
+              umma_f16(tmem + chunks[c].col, umma_desc_sw128(smem_u32(smem + C::P_LO_OFF) + ks * 32), bd,
+                       umma_idesc_f16_f32(C::M, chunks[c].n), true);
           }
         }
         umma_commit(&s_bar);
@@ -456,7 +506,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         tmem_ld32(row_tmem + 0, tv[0]);
         tmem_ld32(row_tmem + 32, tv[1]);
         tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < C::OR; ++i) otail[i] += __uint_as_float(tv[i >> 5][i & 31]);
       }
       tc_fence_before();
@@ -467,56 +517,172 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     // ---- normalise and write the rotated-basis rows; lse ----
     if constexpr (SM) {
       const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
-      const int h = kvh * group_q + row % group_q;
-      float* orow = a.out + (((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h) * D;
-  #pragma unroll 1
+      float* const slot = s_slot;
+      const int h = s_kvh * group_q + row % group_q;
+      const int row_qi = s_q0 + row / group_q;
+      const bool wr = slot ? true : row_qi < a.n_new;
+      const int64_t orow_i = ((int64_t)s_b * a.n_new + row_qi) * a.n_q_heads + h;
+      float* orow = slot ? slot + (int64_t)row * D : a.out + orow_i * D;
+      float* olse = slot ? slot + (int64_t)C::M * D + row : a.lse + orow_i;
+#pragma unroll 1
       for (int c0 = 0; c0 < C::OT; c0 += 32) {
         uint32_t ov[32];
-        if (n_steps > 0) {
+        if (s_s0 < s1) {
           tmem_ld32(row_tmem + 64 + c0, ov);
           tmem_ld_wait();
         } else {
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = 0u;
         }
-        if (row_valid) {
-  #pragma unroll
+        if (wr) {
+#pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(orow + c0 + i) =
                 make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
                             __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
         }
       }
-      if (row_valid) {
-  #pragma unroll
+      if (wr) {
+#pragma unroll
         for (int i = 0; i < C::OR; i += 4)
           *reinterpret_cast<float4*>(orow + C::OT + i) =
               make_float4(otail[i] * inv, otail[i + 1] * inv, otail[i + 2] * inv, otail[i + 3] * inv);
-        a.lse[((int64_t)b * a.n_new + row_qi) * a.n_q_heads + h] =
-            l_sum > 0.0f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+        *olse = l_sum > 0.0f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
       }
     }
   };
-  if (softmax_warp)
-    role_loop(std::true_type{});
-  else
-    role_loop(std::false_type{});
+
+  // ---- the CTA's step range, walked tile by tile ----
+  // The walk state is uniform over the CTA and kept in shared memory (thread
+  // 0 advances it), so the step loop does not carry it in registers.
+  __shared__ long long s_walk[4];  // steps left, (sequence, kv head), query tile, first step
+  if (tid == 0) {
+    int64_t S_bh = 0;  // steps of all query tiles of one (sequence, kv head)
+    for (int q = 0; q < n_qt; ++q) S_bh += steps_of(q);
+    const int64_t n_bh = (int64_t)a.batch * a.n_kv_heads;
+    if (a.stream_k) {
+      const int64_t W = n_bh * S_bh;
+      const int64_t w0 = (int64_t)blockIdx.x * W / gridDim.x;
+      const int64_t w1 = (int64_t)(blockIdx.x + 1) * W / gridDim.x;
+      const int64_t bh0 = S_bh > 0 ? w0 / S_bh : n_bh;
+      int64_t rem = w0 - bh0 * S_bh;
+      int q = 0;
+      while (q < n_qt && rem >= steps_of(q)) rem -= steps_of(q++);
+      s_walk[0] = w1 - w0;
+      s_walk[1] = bh0;
+      s_walk[2] = q;
+      s_walk[3] = rem;
+    } else {
+      s_walk[0] = steps_of(static_cast<int>(blockIdx.x % n_qt));
+      s_walk[1] = blockIdx.x / n_qt;
+      s_walk[2] = blockIdx.x % n_qt;
+      s_walk[3] = 0;
+    }
+  }
+  __syncthreads();
+  const int64_t n_bh = (int64_t)a.batch * a.n_kv_heads;
+  while (true) {
+    const int64_t left = s_walk[0], bh = s_walk[1];
+    const int qt = static_cast<int>(s_walk[2]), s0 = static_cast<int>(s_walk[3]);
+    if (left <= 0 || bh >= n_bh) break;
+    const int n_steps = steps_of(qt);
+    const int s1 = (s0 + left < n_steps) ? static_cast<int>(s0 + left) : n_steps;
+    const int64_t t = bh * n_qt + qt;
+    float* slot = nullptr;  // this segment's rows: `out`, or a partial slot
+    if (s0 > 0 || s1 < n_steps) {
+      // Cut tile: the head part before the cut at CTA blockIdx + 1, the tail
+      // part after the cut at this CTA.
+      const int cut = (s0 == 0) ? blockIdx.x + 1 : blockIdx.x;
+      if (!a.stream_k || (s0 > 0 && s1 < n_steps)) {
+        if (tid == 0) raise_flag(a.flag, kFlagInternal);
+        break;
+      }
+      slot = a.part + (int64_t)(2 * cut + (s0 == 0 ? 0 : 1)) * (C::M * (D + 1));
+      if (tid == 0) a.tile_split[t] = cut;
+    } else if (a.tile_split && tid == 0) {
+      a.tile_split[t] = -1;
+    }
+    if (tid == 0) {
+      s_b = static_cast<int>(bh / a.n_kv_heads);
+      s_kvh = static_cast<int>(bh % a.n_kv_heads);
+      s_q0 = qt * QT;
+      s_s0 = s0;
+      s_stream = a.cache + bh * n_rec * C::REC;
+      s_slot = slot;
+    }
+    __syncthreads();
+    load_q();
+    if (s0 < s1) {
+      fetch(s0);
+      put_scales(s0 & 1);
+    }
+    __syncthreads();  // also: every thread has read the walk state
+    if (tid == 0) {
+      s_walk[0] = left - (s1 - s0);
+      s_walk[3] = 0;
+      if (qt + 1 == n_qt) {
+        s_walk[2] = 0;
+        s_walk[1] = bh + 1;
+      } else {
+        s_walk[2] = qt + 1;
+      }
+    }
+    if (softmax_warp)
+      role_loop(std::true_type{}, s1);
+    else
+      role_loop(std::false_type{}, s1);
+    tc_fence_before();
+    __syncthreads();  // TMEM read and Q tile free before the next segment
+    tc_fence_after();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Inverse transform of prefill rows in place: row = s * H_D(row) / D.
+// Inverse transform of the prefill output rows in place:
+// row = s * H_D(row) * kCentroidScale / D.
+// Rows of a tile cut by the stream-K schedule are first merged from the two
+// partial slots (exact log-sum-exp combine), and their lse written.
 template <int D>
-__global__ void __launch_bounds__(256) derotate_rows_kernel(float* rows, int64_t n_rows, const int8_t* signs) {
+__global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const int8_t* signs, int QT) {
   constexpr int E = D / 32;
+  const int64_t n_rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= n_rows) return;
-  float* p = rows + r * D;
+  float* p = a.out + r * D;
   float v[E];
+  int cut = -1, rin = 0;
+  if (a.stream_k) {
+    const int group_q = a.n_q_heads / a.n_kv_heads;
+    const int h = static_cast<int>(r % a.n_q_heads);
+    const int64_t bq = r / a.n_q_heads;
+    const int qi = static_cast<int>(bq % a.n_new);
+    const int64_t b = bq / a.n_new;
+    const int n_qt = (a.n_new + QT - 1) / QT;
+    const int64_t t = (b * a.n_kv_heads + h / group_q) * n_qt + qi / QT;
+    cut = a.tile_split[t];
+    rin = (qi % QT) * group_q + h % group_q;
+  }
+  if (cut < 0) {
 #pragma unroll
-  for (int e = 0; e < E; ++e) v[e] = p[32 * e + lane];
+    for (int e = 0; e < E; ++e) v[e] = p[32 * e + lane];
+  } else {
+    constexpr int64_t SLOT = 128 * (int64_t)(D + 1);
+    const float* s0 = a.part + (2 * (int64_t)cut) * SLOT;
+    const float* s1 = s0 + SLOT;
+    const float l0 = s0[128 * D + rin], l1 = s1[128 * D + rin];
+    const float M = fmaxf(l0, l1);
+    const float w0 = (l0 == -INFINITY) ? 0.0f : __expf(l0 - M);
+    const float w1 = (l1 == -INFINITY) ? 0.0f : __expf(l1 - M);
+    const float L = w0 + w1;
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      v[e] = (w0 * s0[(int64_t)rin * D + 32 * e + lane] + w1 * s1[(int64_t)rin * D + 32 * e + lane]) * inv;
+    if (lane == 0) a.lse[r] = L > 0.0f ? M + logf(L) : -INFINITY;
+  }
 #pragma unroll
   for (int hl = 1; hl < 32; hl <<= 1) {
 #pragma unroll
@@ -539,8 +705,60 @@ __global__ void __launch_bounds__(256) derotate_rows_kernel(float* rows, int64_t
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int d = 32 * e + lane;
-    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (1.0f / D);
+    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (kCentroidScale / D);
   }
+}
+
+// SMs of the current device (cached per device).
+static int device_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Work layout of one prefill call: query tiles of qt tokens (128 rows), 64-key
+// steps per tile, and whether the stream-K schedule runs (more tiles than SMs,
+// and every CTA's step range at least as long as any tile, so a tile is cut at
+// most once).
+struct PrefillPlan {
+  int qt, n_qt;
+  int64_t n_tiles;
+  int grid;
+  int stream_k;
+};
+static PrefillPlan plan_prefill(int batch, int n_kv_heads, int n_q_heads, int64_t n_cached, int n_new) {
+  PrefillPlan p{};
+  p.qt = 128 / (n_q_heads / n_kv_heads);
+  p.n_qt = (n_new + p.qt - 1) / p.qt;
+  p.n_tiles = (int64_t)batch * n_kv_heads * p.n_qt;
+  p.grid = device_sms();
+  int64_t s_bh = 0, max_steps = 0;
+  for (int t = 0; t < p.n_qt; ++t) {
+    const int64_t kv_end = n_cached + std::min((t + 1) * p.qt, n_new);
+    const int64_t st = (kv_end + 63) / 64;
+    s_bh += st;
+    max_steps = std::max(max_steps, st);
+  }
+  const int64_t W = (int64_t)batch * n_kv_heads * s_bh;
+  p.stream_k = (p.n_tiles > p.grid && W / p.grid >= max_steps) ? 1 : 0;
+  return p;
+}
+
+// Workspace bytes: the device flag, tile_split, and (when the schedule may be
+// stream-K) two partial slots per CTA.
+static size_t prefill_ws_bytes(int D, int batch, int n_kv_heads, int n_q_heads, int n_new) {
+  const int qt = 128 / (n_q_heads / n_kv_heads);
+  const int64_t n_tiles = (int64_t)batch * n_kv_heads * ((n_new + qt - 1) / qt);
+  size_t bytes = 256 + (4 * static_cast<size_t>(n_tiles) + 255) / 256 * 256;
+  const int sms = device_sms();
+  if (n_tiles > sms) bytes += 2 * static_cast<size_t>(sms) * 128 * (D + 1) * sizeof(float);
+  return bytes;
 }
 
 template <int D>
@@ -552,14 +770,15 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int group_q = a.n_q_heads / a.n_kv_heads;
-  const int qt = Cf::M / group_q;
-  dim3 grid((a.n_new + qt - 1) / qt, a.n_kv_heads, a.batch);
-  attn_prefill_kernel<D><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(a);
+  const PrefillPlan pl = plan_prefill(a.batch, a.n_kv_heads, a.n_q_heads, a.n_cached, a.n_new);
+  PrefillArgs k = a;
+  k.stream_k = pl.stream_k;
+  const unsigned grid = static_cast<unsigned>(pl.stream_k ? pl.grid : pl.n_tiles);
+  attn_prefill_kernel<D><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
-  derotate_rows_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(a.out, rows, signs);
+  derotate_rows_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(k, signs, pl.qt);
   return cudaGetLastError();
 }
 
@@ -568,10 +787,10 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
 extern "C" {
 
 CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads) {
-  (void)cache;
-  (void)n_new;
-  (void)n_q_heads;
-  return 256;  // the device flag word
+  if (!cache || n_new < 0 || cache->n_kv_heads <= 0 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads ||
+      128 % (n_q_heads / cache->n_kv_heads))
+    return 256;
+  return ckv::prefill_ws_bytes(cache->head_dim, cache->batch, cache->n_kv_heads, n_q_heads, n_new);
 }
 
 CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16, int32_t n_new,
@@ -595,8 +814,10 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
       (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(k_new_f16) & 15) ||
       (reinterpret_cast<uintptr_t>(v_new_f16) & 15))
     return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "null or misaligned tensor"));
-  if (!workspace || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255))
-    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_WORKSPACE, "workspace needs 256 aligned bytes"));
+  const size_t need = ckv::prefill_ws_bytes(cache->head_dim, cache->batch, cache->n_kv_heads, n_q_heads, n_new);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   // Pack the new rows (same quantisers as kv_pack) at [n_cached, n_cached + n_new).
@@ -616,6 +837,13 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
   a.out = out;
   a.lse = lse;
   a.flag = static_cast<int32_t*>(workspace);
+  {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int qt = 128 / (n_q_heads / cache->n_kv_heads);
+    const int64_t n_tiles = (int64_t)cache->batch * cache->n_kv_heads * ((n_new + qt - 1) / qt);
+    a.tile_split = reinterpret_cast<int32_t*>(ws + 256);
+    a.part = reinterpret_cast<float*>(ws + 256 + (4 * n_tiles + 255) / 256 * 256);
+  }
   switch (cache->head_dim) {
     case 64: e = ckv::launch_prefill_d<64>(a, cache->v_signs, st); break;
     case 128: e = ckv::launch_prefill_d<128>(a, cache->v_signs, st); break;

@@ -52,12 +52,16 @@ __device__ __forceinline__ float warp_max_over_gid(float x) {
 // One tile of the online softmax. S holds the logits of positions (g, g+8) x
 // rows (2t, 2t+1) in the mma C layout; n0/n1 multiply the probabilities of
 // positions g / g+8 (the V norms; 1 for dense values). Rescales acc when the
-// running max grows and returns the two B-operand registers of P'.
-template <int MTW>
+// running max grows and returns the two B-operand registers of P'. With
+// SPLIT, P' is the exact-to-2^-22 pair hi + lo of fp16 values (hi in pb,
+// lo in pl) and the caller multiplies both: rounding P' to fp16 alone costs up
+// to 2.7e-3 of |o|_inf at head dim 64 over long rows (2.1e-3 at 128, 1.4e-3 at
+// 256, 8e-4 at 512), so the kernels split at head dims up to 128.
+template <int MTW, bool SPLIT = false>
 __device__ __forceinline__ void softmax_tile(const float (&S)[4], bool valid0, bool valid1,
                                              float scale_log2, float n0, float n1,
                                              SoftmaxState& st, float (&acc)[MTW][4],
-                                             uint32_t& pb0, uint32_t& pb1) {
+                                             uint32_t& pb0, uint32_t& pb1, uint32_t* pl = nullptr) {
   const float ninf = -INFINITY;
   const float x0 = valid0 ? S[0] * scale_log2 : ninf;
   const float x1 = valid0 ? S[1] * scale_log2 : ninf;
@@ -87,10 +91,18 @@ __device__ __forceinline__ void softmax_tile(const float (&S)[4], bool valid0, b
   const float p3 = valid1 ? fast_exp2(x3 - st.m1) : 0.0f;
   st.l0 += p0 + p2;
   st.l1 += p1 + p3;
-  const uint32_t X0 = pack_half2(valid0 ? p0 * n0 : 0.0f, valid0 ? p1 * n0 : 0.0f);
-  const uint32_t X1 = pack_half2(valid1 ? p2 * n1 : 0.0f, valid1 ? p3 * n1 : 0.0f);
+  const float y0 = valid0 ? p0 * n0 : 0.0f, y1 = valid0 ? p1 * n0 : 0.0f;
+  const float y2 = valid1 ? p2 * n1 : 0.0f, y3 = valid1 ? p3 * n1 : 0.0f;
+  const uint32_t X0 = pack_half2(y0, y1);
+  const uint32_t X1 = pack_half2(y2, y3);
   pb0 = movmatrix_trans(X0);
   pb1 = movmatrix_trans(X1);
+  if constexpr (SPLIT) {
+    const __half2 h0 = *reinterpret_cast<const __half2*>(&X0);
+    const __half2 h1 = *reinterpret_cast<const __half2*>(&X1);
+    pl[0] = movmatrix_trans(pack_half2(y0 - __low2float(h0), y1 - __high2float(h0)));
+    pl[1] = movmatrix_trans(pack_half2(y2 - __low2float(h1), y3 - __high2float(h1)));
+  }
 }
 
 // Sum the two warps' partial S of a shared tile (D = 512). Both warps end
@@ -109,10 +121,11 @@ __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int grou
 }
 
 // Inverse rotation of one output row held by a warp (lane: dims 64 e + 2 lane
-// + c, c < 2), then the sign flip and 1/D, stored to `orow`: the unnormalised
-// Walsh-Hadamard transform pairs the two values of a float2 (dim bit 0), lanes
-// (bits 1..5, shuffles) and registers (bits 6..); one 1/sqrt(D) comes from the
-// orthonormal inverse, one from the norm scaling folded into P'. Without
+// + c, c < 2), then the sign flip and kCentroidScale / D, stored to `orow`:
+// the unnormalised Walsh-Hadamard transform pairs the two values of a float2
+// (dim bit 0), lanes (bits 1..5, shuffles) and registers (bits 6..); one
+// 1/sqrt(D) comes from the orthonormal inverse, one from the norm scaling
+// folded into P', and kCentroidScale undoes the centroid table's scale. Without
 // `signs` (dense values) the row is stored as is.
 template <int D>
 __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane, const int8_t* signs,
@@ -149,8 +162,8 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
     for (int e = 0; e < E2; ++e) {
       const int d = 64 * e + 2 * lane;
       const char2 sg = *reinterpret_cast<const char2*>(signs + d);
-      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (1.0f / D);
-      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (1.0f / D);
+      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (kCentroidScale / D);
+      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (kCentroidScale / D);
     }
   }
   if (orow) {

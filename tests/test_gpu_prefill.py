@@ -88,3 +88,18 @@ def test_chunked_prefill_workload_sampled():
     rows = [0, 1, 15, 16, 17, 500, 1023, 1024, 1777, 2046, 2047]
     o_ref, l_ref = _oracle(k, v, qf, signs, nc, 0, rows=rows)
     H.check_attention(out[0][rows], lse[0][rows], o_ref, l_ref, "chunked prefill")
+
+
+def test_prefill_stream_k_schedule():
+    """More 128-row tiles than SMs, each CTA taking an equal run of 64-key steps:
+    tiles cut between two CTAs are merged from two partials. Every row of both
+    sequences is checked (head_dim 64 keeps the oracle quick)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    D, Hkv, Hq, B, nc, nn = 64, 2, 16, 2, 64, 2560   # 2 x 2 x 160 tiles of 16 tokens x 8 heads
+    cap = nc + nn + 16
+    k, v, qf, signs, out, lse = _case(D, Hkv, Hq, B, nc, nn, cap, seed=77)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    for b in range(B):
+        o_ref, l_ref = _oracle(k, v, qf, signs, nc, b)
+        H.check_attention(out[b], lse[b], o_ref, l_ref, f"stream-K prefill b={b}")
