@@ -43,10 +43,10 @@ METRIC = "compressed-KV decode attn: tokens/s and effective HBM GB/s (% of GB300
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM traffic of one decode-kernel launch on gemma4_decode from the ncu capture
-# summarised in profiles/attn_decode_gemma4.md, valid for the kernel sources
-# whose hash is recorded beside it (null once they change).
-NCU_TRAFFIC = {"bytes": 49526784, "source_sha": "e1011a1113edb3ff"}
+# DRAM traffic (read + write) of one decode-kernel launch on gemma4_decode from
+# one ncu capture, valid for the kernel sources whose hash is recorded beside it
+# (null once they change).
+NCU_TRAFFIC = {"bytes": 48503808, "source_sha": "a578922ecfd5a0b6"}
 
 
 def _args():
@@ -74,7 +74,7 @@ def _peaks():
 
 def _decode_source_sha():
     h = hashlib.sha256()
-    for name in ("attn_decode.cu", "decode_common.cuh", "ckv_device.cuh", "pack_common.cuh"):
+    for name in ("attn_decode.cu", "decode_common.cuh", "ckv_device.cuh", "ckv_kernels.cuh", "pack_common.cuh"):
         with open(os.path.join(ROOT, "compressed_kv_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
