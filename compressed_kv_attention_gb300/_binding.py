@@ -45,6 +45,8 @@ SIGNATURES = {
     "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
                                  _vp, _c_size, _vp]),
+    "ckv_attn_decode_verify": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
+                                        _vp, _c_size, _vp]),
     "ckv_attn_decode_append": (_c_int, [_cache_p, _vp, _c_i64, _vp, _vp, _c_int, _c_i64, _c_i64, _vp, _c_int,
                                         _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_attn_decode_noalloc": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp,
@@ -140,6 +142,16 @@ def attn_decode(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, 
     _check(load().ckv_attn_decode(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
                                   n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                   _stream(stream)))
+
+
+def attn_decode_verify(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,
+                       n_split: int = 0, stream=None):
+    """Verify batch: q fp16 [batch, n_q, n_q_heads, D] are the last n_q positions of each
+    sequence; query token i sees [0, seq_len - n_q + i]. Outputs as attn_decode."""
+    _, n_q, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_decode_verify(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
+                                         n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                         _stream(stream)))
 
 
 def attn_decode_append(cache: PackedCache, seq_len, max_seq_len: int, k_new, v_new, q, scale: float, out, lse,

@@ -356,6 +356,9 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const int tid = threadIdx.x;  // 0 .. 255
   const int group = warp / C::WT, wh = warp % C::WT;
   const int g = lane >> 2;
+  // Key limits of this lane's two rows (2t, 2t + 1) of the row group.
+  const int lim0 = row_key_limit(a, rg * 8 + 2 * (lane & 3), seqlen);
+  const int lim1 = row_key_limit(a, rg * 8 + 2 * (lane & 3) + 1, seqlen);
 
   float* qb_warp = reinterpret_cast<float*>(smem + C::OFF_QB) + warp * C::NB_W * 8;
   q_block_bias<C::NB_W>(qf, lane, qb_warp);
@@ -410,8 +413,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
       const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * g)));
       const float n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * (g + 8))));
       uint32_t pb0, pb1, pl[2] = {0u, 0u};
-      softmax_tile<C::MT_W, C::PSPLIT>(S, tpos + g < seqlen, tpos + g + 8 < seqlen, scale_log2, n0, n1, st, acc,
-                                       pb0, pb1, pl);
+      softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lim0, lim1, scale_log2, n0, n1, st, acc, pb0, pb1, pl);
       pv_tile<D>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, pl, acc);
     }
     __syncwarp();

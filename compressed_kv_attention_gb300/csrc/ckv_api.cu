@@ -133,7 +133,7 @@ int set_last_error(int status, const char* fmt, ...) {
 
 extern "C" {
 
-int32_t ckv_version(void) { return 100; }
+int32_t ckv_version(void) { return 101; }
 
 const char* ckv_last_error(void) { return g_err; }
 
@@ -200,7 +200,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int D, int Hkv, int B, int64_t capacity, const int32_t* seq_len,
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
-                             void* stream, const AppendRows* app = nullptr) {
+                             void* stream, const AppendRows* app = nullptr, int causal_q = 0) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
   if (s != CKV_OK) return s;
@@ -242,6 +242,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.q = static_cast<const __half*>(q);
   a.n_q = n_q;
   a.n_q_heads = n_q_heads;
+  a.causal_q = causal_q;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_split = p.n_split;
   a.n_row_groups = p.n_row_groups;
@@ -275,6 +276,16 @@ ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64
   return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
                     cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
                     workspace, ws_bytes, stream);
+}
+
+ckv_status ckv_attn_decode_verify(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                                  const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale, int32_t n_split,
+                                  float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  ckv_status s = check_cache(cache);
+  if (s != CKV_OK) return s;
+  return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
+                    cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
+                    workspace, ws_bytes, stream, nullptr, 1);
 }
 
 ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,

@@ -41,6 +41,7 @@ struct DecodeArgs {
   int64_t max_seq_len;
   const __half* q;
   int n_q, n_q_heads;
+  int causal_q;              // 1: query token qi sees [0, seq_len - n_q + qi + 1) (verify batch)
   float scale_log2;          // logit scale * log2(e)
   int n_split, n_row_groups;
   float* part;

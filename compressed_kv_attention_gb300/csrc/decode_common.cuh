@@ -50,23 +50,27 @@ __device__ __forceinline__ float warp_max_over_gid(float x) {
 }
 
 // One tile of the online softmax. S holds the logits of positions (g, g+8) x
-// rows (2t, 2t+1) in the mma C layout; n0/n1 multiply the probabilities of
-// positions g / g+8 (the V norms; 1 for dense values). Rescales acc when the
+// rows (2t, 2t+1) in the mma C layout; position p is visible to row 2t when
+// p < lim0 and to row 2t+1 when p < lim1 (tpos: the tile's first position);
+// n0/n1 multiply the probabilities of positions g / g+8 (the V norms; 1 for
+// dense values). Rescales acc when the
 // running max grows and returns the two B-operand registers of P'. With
 // SPLIT, P' is the exact-to-2^-22 pair hi + lo of fp16 values (hi in pb,
 // lo in pl) and the caller multiplies both: rounding P' to fp16 alone costs up
 // to 2.7e-3 of |o|_inf at head dim 64 over long rows (2.1e-3 at 128, 1.4e-3 at
 // 256, 8e-4 at 512), so the kernels split at head dims up to 128.
 template <int MTW, bool SPLIT = false>
-__device__ __forceinline__ void softmax_tile(const float (&S)[4], bool valid0, bool valid1,
+__device__ __forceinline__ void softmax_tile(const float (&S)[4], int64_t tpos, int g, int lim0, int lim1,
                                              float scale_log2, float n0, float n1,
                                              SoftmaxState& st, float (&acc)[MTW][4],
                                              uint32_t& pb0, uint32_t& pb1, uint32_t* pl = nullptr) {
   const float ninf = -INFINITY;
-  const float x0 = valid0 ? S[0] * scale_log2 : ninf;
-  const float x1 = valid0 ? S[1] * scale_log2 : ninf;
-  const float x2 = valid1 ? S[2] * scale_log2 : ninf;
-  const float x3 = valid1 ? S[3] * scale_log2 : ninf;
+  const bool v0 = tpos + g < lim0, v1 = tpos + g < lim1;          // position g, rows 2t / 2t+1
+  const bool v2 = tpos + g + 8 < lim0, v3 = tpos + g + 8 < lim1;  // position g + 8
+  const float x0 = v0 ? S[0] * scale_log2 : ninf;
+  const float x1 = v1 ? S[1] * scale_log2 : ninf;
+  const float x2 = v2 ? S[2] * scale_log2 : ninf;
+  const float x3 = v3 ? S[3] * scale_log2 : ninf;
   const float t0 = warp_max_over_gid(fmaxf(x0, x2));
   const float t1 = warp_max_over_gid(fmaxf(x1, x3));
   const float mn0 = fmaxf(st.m0, t0), mn1 = fmaxf(st.m1, t1);
@@ -85,14 +89,14 @@ __device__ __forceinline__ void softmax_tile(const float (&S)[4], bool valid0, b
     st.m0 = mn0;
     st.m1 = mn1;
   }
-  const float p0 = valid0 ? fast_exp2(x0 - st.m0) : 0.0f;
-  const float p1 = valid0 ? fast_exp2(x1 - st.m1) : 0.0f;
-  const float p2 = valid1 ? fast_exp2(x2 - st.m0) : 0.0f;
-  const float p3 = valid1 ? fast_exp2(x3 - st.m1) : 0.0f;
+  const float p0 = v0 ? fast_exp2(x0 - st.m0) : 0.0f;
+  const float p1 = v1 ? fast_exp2(x1 - st.m1) : 0.0f;
+  const float p2 = v2 ? fast_exp2(x2 - st.m0) : 0.0f;
+  const float p3 = v3 ? fast_exp2(x3 - st.m1) : 0.0f;
   st.l0 += p0 + p2;
   st.l1 += p1 + p3;
-  const float y0 = valid0 ? p0 * n0 : 0.0f, y1 = valid0 ? p1 * n0 : 0.0f;
-  const float y2 = valid1 ? p2 * n1 : 0.0f, y3 = valid1 ? p3 * n1 : 0.0f;
+  const float y0 = v0 ? p0 * n0 : 0.0f, y1 = v1 ? p1 * n0 : 0.0f;
+  const float y2 = v2 ? p2 * n1 : 0.0f, y3 = v3 ? p3 * n1 : 0.0f;
   const uint32_t X0 = pack_half2(y0, y1);
   const uint32_t X1 = pack_half2(y2, y3);
   pb0 = movmatrix_trans(X0);
@@ -251,6 +255,16 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
   }
 }
 
+
+// Keys visible to row `rr` of a row group: [0, seq_len), or with causal_q
+// (a verify batch: the n_q query tokens are the last n_q positions) query
+// token qi sees [0, seq_len - n_q + qi + 1).
+__device__ __forceinline__ int row_key_limit(const DecodeArgs& a, int rr, int seqlen) {
+  if (!a.causal_q) return seqlen;
+  const int qi = rr / (a.n_q_heads / a.n_kv_heads);
+  const int lim = seqlen - a.n_q + qi + 1;
+  return lim < 0 ? 0 : lim;
+}
 
 // Which query vector row `rr` (0 <= rr < G * n_q) of kv head `kvh` is: the
 // query token and the query head.

@@ -113,6 +113,7 @@ class Workload:
     n_agents: int = 0     # shared-prefix fan-out: agents reading one prefix
     tail_len: int = 0     # shared-prefix fan-out: private fp16 tail per agent
     n_new: int = 0        # prefill: new tokens appended and attended causally
+    n_q: int = 1          # decode: query tokens per sequence (a verify batch when > 1)
     q_dtype: str = "float16"
 
     @property
@@ -126,7 +127,8 @@ def _one_percent(d: int) -> int:
 
 # The five workloads: a tiny decode that the oracle finishes in well under a
 # second, the Gemma-4 global-layer decode, the shared-prefix fan-out decode, the
-# long-context decode and the chunked prefill.
+# long-context decode and the chunked prefill; and a verify batch of 4 drafted
+# tokens over the Gemma-4 global-layer cache (multi-query decode).
 WORKLOADS = {
     "tiny_decode": Workload("tiny_decode", head_dim=128, n_kv_heads=1, n_q_heads=4, batch=1,
                             seq_len=256, seed=0, n_outliers=2),
@@ -137,6 +139,8 @@ WORKLOADS = {
                               n_agents=15, tail_len=512),
     "long_decode": Workload("long_decode", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=4,
                             seq_len=262144, seed=3, n_outliers=_one_percent(512)),
+    "verify_decode": Workload("verify_decode", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=1,
+                              seq_len=32768, seed=5, n_outliers=_one_percent(512), n_q=4),
     "chunked_prefill": Workload("chunked_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16,
                                 batch=1, seq_len=32768, seed=4, n_outliers=_one_percent(512),
                                 n_new=2048, q_dtype="bfloat16"),

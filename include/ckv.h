@@ -165,6 +165,21 @@ CKV_API ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_le
                            size_t ws_bytes, void* stream);
 
 /*
+ * attn_decode_verify — attention of a verify batch: the n_q query tokens of a
+ * sequence are its last n_q positions, so query token i sees cached positions
+ * [0, seq_len[b] - n_q + i] (causal among the batch; a token whose range is
+ * empty gets O = 0 and lse = -inf). This is the multi-query decode that checks
+ * n_q drafted tokens at once (PolyKV page, section "WorkStream-1": the
+ * "turbo-MMA verify (n_q>1)" path for MTP verify batches). The drafts' K/V rows
+ * must already be in the cache (ckv_kv_pack). Arguments, workspace and errors
+ * as attn_decode; the same kernel runs with per-row key limits.
+ */
+CKV_API ckv_status ckv_attn_decode_verify(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                                          const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale,
+                                          int32_t n_split, float* out, float* lse, void* workspace,
+                                          size_t ws_bytes, void* stream);
+
+/*
  * attn_decode_append — one decode step: quantise n_new new K/V rows of every
  * sequence into the cache at positions [seq_len[b] - n_new, seq_len[b]) (the
  * same bytes ckv_kv_pack writes), then attend as attn_decode over

@@ -284,6 +284,29 @@ def decode_reference(q, k_hat, v_hat, seq_len, scale: float):
     return o, lse
 
 
+def verify_decode_reference(q, k_hat, v_hat, seq_len, scale: float):
+    """Attention of a verify batch for one sequence.
+
+    ``q [n_q, Hq, D]`` are the last n_q positions of the sequence (the drafted
+    tokens, whose K/V rows are the last n_q cached rows); query token i sees
+    cached tokens [0, seq_len - n_q + i] (causal among the batch, as the PolyKV
+    page's "turbo-MMA verify (n_q>1)" batches check drafted tokens; section
+    "WorkStream-1"). A token whose range is empty returns o = 0, lse = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n_q, Hq, D = q.shape
+    Hkv = k_hat.shape[0]
+    vis = np.arange(seq_len)[None, :] <= (seq_len - n_q + np.arange(n_q))[:, None]
+    o = np.zeros((n_q, Hq, v_hat.shape[-1]))
+    lse = np.zeros((n_q, Hq))
+    for h in range(Hq):
+        kh = kv_head_of(h, Hq, Hkv)
+        oh, lh = attention(q[:, h, :], k_hat[kh, :seq_len], v_hat[kh, :seq_len], scale, visible=vis)
+        o[:, h, :] = oh
+        lse[:, h] = lh
+    return o, lse
+
+
 def prefill_reference(q, k_hat, v_hat, n_cached: int, scale: float):
     """Causal chunked prefill for one sequence.
 

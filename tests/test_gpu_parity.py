@@ -163,6 +163,36 @@ def test_decode_shapes_ragged(D, Hkv, Hq, n_q, n_split):
     H.check_attention(o, l, o_ref, lse_ref, f"D={D} Hq={Hq} n_q={n_q} split={n_split}")
 
 
+@pytest.mark.parametrize("D,Hkv,Hq,n_q,n_split", [(128, 2, 16, 4, 0), (512, 2, 16, 2, 0), (512, 2, 16, 8, 0),
+                                                  (512, 1, 4, 5, 3), (128, 2, 2, 16, 0), (64, 1, 1, 3, 200)])
+def test_verify_decode_is_causal_among_the_batch(D, Hkv, Hq, n_q, n_split):
+    """Verify batch: query token i of n_q sees [0, seq_len - n_q + i]; rows of
+    a group of 8 mix tokens when the head ratio is below 8; a sequence shorter
+    than the batch leaves its first tokens with nothing to see."""
+    _need_gpu()
+    B, T, cap = 3, 203, 224
+    seq_lens = [203, 3, 150]
+    k, v, outl = make_kv(D, Hkv, B, T, seed=31 + D + Hq + n_q, n_out=max(1, round(0.01 * D)))
+    q = inputs.normal_tensor((B, n_q, Hq, D), 31 + D, "qv", outl)
+    signs = inputs.tbq_signs(D)
+    qs, d16, codes, n16, u = oracle_cache(k, v, signs)
+    o_ref = np.zeros((B, n_q, Hq, D))
+    lse_ref = np.zeros((B, n_q, Hq))
+    for b in range(B):
+        T_b = seq_lens[b]
+        kh = O.q8_0_dequantize(qs[b, :, :T_b], d16[b, :, :T_b])
+        vh = O.tbq3_dequantize(codes[b, :, :T_b], n16[b, :, :T_b], signs)
+        o_ref[b], lse_ref[b] = O.verify_decode_reference(q[b], kh, vh, T_b, 1.0 / math.sqrt(D))
+    cache = gpu_pack(k, v, signs, cap)
+    out = torch.empty((B, n_q, Hq, D), dtype=torch.float32, device=DEV)
+    lse = torch.empty((B, n_q, Hq), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(ckv.attn_decode_workspace(cache, T, n_q, Hq, n_split), dtype=torch.uint8, device=DEV)
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device=DEV)
+    ckv.attn_decode_verify(cache, sl, T, to_dev(q), 1.0 / math.sqrt(D), out, lse, ws, n_split=n_split)
+    assert ckv.read_device_flag(ws) == 0
+    H.check_attention(out.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"verify D={D} Hq={Hq} n_q={n_q}")
+
+
 def test_decode_seq_len_out_of_range_sets_flag():
     _need_gpu()
     D, T = 128, 64

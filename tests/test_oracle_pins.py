@@ -333,6 +333,32 @@ def test_decode_and_prefill_reference_gqa_and_causality():
             assert np.allclose(o[i, h], oh[0], rtol=0, atol=1e-14)
 
 
+def test_verify_decode_reference_is_causal_among_the_batch():
+    """Query token i of a verify batch equals a single-token decode over the
+    first seq_len - n_q + i + 1 keys; the last token equals the plain decode;
+    tokens whose range is empty give 0 / -inf."""
+    rng = np.random.default_rng(13)
+    Hq, Hkv, D, T = 4, 2, 16, 24
+    k, v = rng.standard_normal((Hkv, T, D)), rng.standard_normal((Hkv, T, D))
+    n_q, seq_len = 5, 18
+    q = rng.standard_normal((n_q, Hq, D))
+    o, lse = O.verify_decode_reference(q, k, v, seq_len, 0.25)
+    for i in range(n_q):
+        oi, li = O.decode_reference(q[i:i + 1], k, v, seq_len - n_q + i + 1, 0.25)
+        assert np.allclose(o[i], oi[0], rtol=0, atol=1e-13) and np.allclose(lse[i], li[0], rtol=0, atol=1e-13)
+    od, ld = O.decode_reference(q[-1:], k, v, seq_len, 0.25)
+    assert np.allclose(o[-1], od[0], rtol=0, atol=1e-13)
+    # brute force for one head and token: softmax over the visible logits
+    i, h = 2, 3
+    n_vis = seq_len - n_q + i + 1
+    lg = 0.25 * k[h // 2, :n_vis] @ q[i, h]
+    w = np.exp(lg - lg.max())
+    assert np.allclose(o[i, h], (w[:, None] * v[h // 2, :n_vis]).sum(0) / w.sum(), rtol=0, atol=1e-13)
+    # a batch longer than the sequence: the first tokens see nothing
+    o, lse = O.verify_decode_reference(q, k, v, 3, 0.25)
+    assert (o[:2] == 0).all() and (lse[:2] == -np.inf).all() and np.isfinite(lse[2:]).all()
+
+
 # ----------------------------------------------------------- layout ------
 
 @pytest.mark.parametrize("D", [64, 128, 256, 512])
