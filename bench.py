@@ -57,7 +57,7 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="gemma4_decode",
                    choices=["gemma4_decode", "long_decode", "fanout_decode", "tiny_decode", "chunked_prefill",
-                            "kv_pack", "verify_decode"])
+                            "kv_pack", "verify_decode", "dca_decode"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -168,13 +168,15 @@ class DecodeWork:
         D, Hkv, Hq, T, B = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.batch
         self.D, self.T, self.B, self.Hq, self.Hkv = D, T, B, Hq, Hkv
         self.n_q = w.n_q
+        self.dca = w.dca_chunk  # dual chunk attention: three regime queries, one output token
         outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
         signs = inputs.tbq_signs(D)
         self.scale = 1.0 / math.sqrt(D)
         with torch.cuda.stream(stream):
             k = inputs.normal_tensor((B, T, Hkv, D), w.seed, "k", outl, device=str(dev))
             v = inputs.normal_tensor((B, T, Hkv, D), w.seed, "v", outl, device=str(dev))
-            self.q = inputs.normal_tensor((B, self.n_q, Hq, D), w.seed, "q", outl, device=str(dev))
+            self.q = inputs.normal_tensor((B, 3 if self.dca else self.n_q, Hq, D), w.seed, "q", outl,
+                                          device=str(dev))
             self.cache_bytes = ckv.cache_bytes(D, Hkv, B, T)
             self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
             self.n_rot = max(2, math.ceil(4 * self.l2 / self.cache_bytes))
@@ -185,17 +187,22 @@ class DecodeWork:
             del k, v
             self.out = torch.empty((B, self.n_q, Hq, D), dtype=torch.float32, device=dev)
             self.lse = torch.empty((B, self.n_q, Hq), dtype=torch.float32, device=dev)
-            self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], T, self.n_q, Hq), dtype=torch.uint8,
-                                  device=dev)
+            ws_bytes = (ckv.attn_decode_dca_workspace(self.caches[0], T, Hq) if self.dca else
+                        ckv.attn_decode_workspace(self.caches[0], T, self.n_q, Hq))
+            self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
             self.seq = torch.full((B,), T, dtype=torch.int32, device=dev)
         stream.synchronize()
         self.tokens_per_step = B * self.n_q
-        self.launches_per_step = 1  # the decode kernel (packs the new token or runs the batch, merges splits)
+        # the decode kernel (packs the new token or runs the batch, merges splits); DCA adds the regime merge
+        self.launches_per_step = 2 if self.dca else 1
         self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D)
 
     def step(self, i):
         c = self.caches[i % self.n_rot]
-        if self.n_q > 1:
+        if self.dca:
+            self.ckv.attn_decode_dca(c, self.seq, self.T, self.dca, self.q, self.scale, self.out, self.lse, self.ws,
+                                     stream=self.stream)
+        elif self.n_q > 1:
             self.ckv.attn_decode_verify(c, self.seq, self.T, self.q, self.scale, self.out, self.lse, self.ws,
                                         stream=self.stream)
         else:
@@ -209,7 +216,8 @@ class DecodeWork:
 
     def e2e_setup(self):
         t = self.torch
-        ins = (self.q,) if self.n_q > 1 else (self.q, self.k_new, self.v_new)  # a verify batch sends only Q
+        # a verify batch or a DCA step sends only Q
+        ins = (self.q,) if (self.n_q > 1 or self.dca) else (self.q, self.k_new, self.v_new)
         self.h_in = [x.cpu().pin_memory() for x in ins]
         self.d_in = [t.empty_like(x) for x in ins]
         self.h_out = [t.empty(x.shape, dtype=x.dtype).pin_memory() for x in (self.out, self.lse)]
@@ -220,7 +228,10 @@ class DecodeWork:
         for h, d in zip(self.h_in, self.d_in):
             d.copy_(h, non_blocking=True)
         c = self.caches[i % self.n_rot]
-        if self.n_q > 1:
+        if self.dca:
+            self.ckv.attn_decode_dca(c, self.seq, self.T, self.dca, self.d_in[0], self.scale, self.out, self.lse,
+                                     self.ws, stream=self.stream)
+        elif self.n_q > 1:
             self.ckv.attn_decode_verify(c, self.seq, self.T, self.d_in[0], self.scale, self.out, self.lse, self.ws,
                                         stream=self.stream)
         else:
@@ -232,7 +243,9 @@ class DecodeWork:
     def describe(self):
         return {"workload": self.w.name, "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
                 "batch": self.B, "cached_tokens": self.T, "n_q": self.n_q,
-                "step": ("attn_decode_verify (a batch of n_q drafted tokens, causal among them)" if self.n_q > 1
+                "step": (f"attn_decode_dca (chunk {self.dca}: intra, successive and inter regimes + merge)"
+                         if self.dca else
+                         "attn_decode_verify (a batch of n_q drafted tokens, causal among them)" if self.n_q > 1
                          else "attn_decode_append (pack 1 new token per sequence in-kernel, then attend)"),
                 "l2": f"rotating {self.n_rot} cache copies ({self.n_rot * self.cache_bytes / 1e6:.0f} MB > 4x L2 "
                       f"{self.l2 / 1e6:.0f} MB)"}
@@ -242,7 +255,8 @@ class DecodeWork:
         achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
         traffic = NCU_TRAFFIC["bytes"] if (self.w.name == "gemma4_decode" and
                                            NCU_TRAFFIC["source_sha"] == _decode_source_sha()) else None
-        what = "verify batch, per-row causal limits" if self.n_q > 1 else "append"
+        what = ("DCA regimes as three query rows" if self.dca else
+                "verify batch, per-row causal limits" if self.n_q > 1 else "append")
         return {"bound": "hbm", "kernel": f"attn_decode_kernel<{self.D}> ({what} + split-K decode + in-kernel merge)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_kind": kind, "traffic": traffic, "algorithmic_bytes": self.algo_bytes,
@@ -486,7 +500,7 @@ class PackWork:
 
 
 def _make_work(name, dev, stream):
-    if name in ("gemma4_decode", "long_decode", "tiny_decode", "verify_decode"):
+    if name in ("gemma4_decode", "long_decode", "tiny_decode", "verify_decode", "dca_decode"):
         return DecodeWork(name, dev, stream)
     if name == "fanout_decode":
         return FanoutWork(dev, stream)

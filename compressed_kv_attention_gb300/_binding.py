@@ -45,6 +45,9 @@ SIGNATURES = {
     "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
                                  _vp, _c_size, _vp]),
+    "ckv_attn_decode_dca_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int]),
+    "ckv_attn_decode_dca": (_c_int, [_cache_p, _vp, _c_i64, _c_int, _vp, _c_int, _c_f, _c_int, _vp, _vp, _vp,
+                                     _c_size, _vp]),
     "ckv_attn_decode_verify": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
                                         _vp, _c_size, _vp]),
     "ckv_attn_decode_append": (_c_int, [_cache_p, _vp, _c_i64, _vp, _vp, _c_int, _c_i64, _c_i64, _vp, _c_int,
@@ -142,6 +145,23 @@ def attn_decode(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, 
     _check(load().ckv_attn_decode(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
                                   n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                   _stream(stream)))
+
+
+def attn_decode_dca_workspace(cache: PackedCache, max_seq_len: int, n_q_heads: int, n_split: int = 0) -> int:
+    return int(load().ckv_attn_decode_dca_workspace(cache.ref(), max_seq_len, n_q_heads, n_split))
+
+
+def attn_decode_dca(cache: PackedCache, seq_len, max_seq_len: int, chunk: int, q, scale: float, out, lse,
+                    workspace, n_split: int = 0, stream=None):
+    """Dual chunk attention: q fp16 [batch, 3, n_q_heads, D] holds the intra, successive and inter
+    regime queries of the token at position seq_len - 1; out float32 [batch, n_q_heads, D], lse
+    float32 [batch, n_q_heads]."""
+    _, n_r, n_q_heads, _ = q.shape
+    if n_r != 3:
+        raise ValueError("q must hold the three regime queries on its second axis")
+    _check(load().ckv_attn_decode_dca(cache.ref(), _ptr(seq_len), max_seq_len, chunk, _ptr(q), n_q_heads, scale,
+                                      n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                      _stream(stream)))
 
 
 def attn_decode_verify(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,

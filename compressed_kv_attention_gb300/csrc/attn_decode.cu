@@ -179,7 +179,9 @@ __device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_
   }
 }
 
-template <int D>
+// DCA: built with the regime key ranges' lower limits and tile narrowing
+// (the other decodes compile without them).
+template <int D, bool DCA>
 __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(DecodeArgs a) {
   using C = CDec<D>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -205,6 +207,10 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
   const int64_t n_tiles_max = (lim + kTile - 1) / kTile;
   const int64_t tile_begin = split * n_tiles_max / a.n_split;
+  // Without an append or a DCA regime the first stages are issued before the
+  // length is known; otherwise the tile range depends on it.
+  const bool defer = a.n_new > 0 || DCA;
+  int64_t tb = tile_begin;  // first tile actually run (DCA: at or after the regime's first key)
   const int64_t tile_end_max = (split + 1) * n_tiles_max / a.n_split;
   const int n_iters_max = static_cast<int>((tile_end_max - tile_begin + C::NP - 1) / C::NP);
   const uint8_t* gbase = a.cache + (int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) * C::REC;
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   int issued = 0;  // producer lane
   auto issue = [&](int it, int64_t end) {
     const int s = it % C::NSTAGE;
-    const int64_t first = tile_begin + (int64_t)it * C::NP;
+    const int64_t first = tb + (int64_t)it * C::NP;
     const int64_t left = end - first;
     const uint32_t cnt = left < C::NP ? (uint32_t)left : (uint32_t)C::NP;
     mbar_arrive_expect_tx(&full[s], cnt * C::REC);
@@ -269,7 +275,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     ++issued;
   };
   int pre = 0;
-  if (warp == C::NCW && a.n_new == 0) {
+  if (warp == C::NCW && !defer) {
     pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
     if (lane == 0)
       for (int it = 0; it < pre; ++it) issue(it, tile_end_max);
@@ -281,8 +287,9 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     const int seq_raw = s_seq;
     const int64_t sl = (seq_raw < 0 || seq_raw > lim) ? 0 : seq_raw;
     const int64_t nt = (sl + kTile - 1) / kTile;
-    const int64_t tile_end = nt < tile_end_max ? (nt > tile_begin ? nt : tile_begin) : tile_end_max;
-    const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+    int64_t tile_end = nt < tile_end_max ? (nt > tile_begin ? nt : tile_begin) : tile_end_max;
+    if constexpr (DCA) dca_tiles(a, rg, static_cast<int>(sl), split, tb, tile_end);
+    const int n_iters = static_cast<int>((tile_end - tb + C::NP - 1) / C::NP);
     if (a.n_new > 0) {
       // New positions inside this CTA's tiles. Stages before the first of them
       // stream meanwhile; the rest is issued once the rows are in the cache.
@@ -349,16 +356,18 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
     seqlen = 0;
   }
   const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
-  const int64_t tile_end = n_tiles < tile_end_max ? (n_tiles > tile_begin ? n_tiles : tile_begin) : tile_end_max;
-  const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+  int64_t tile_end = n_tiles < tile_end_max ? (n_tiles > tile_begin ? n_tiles : tile_begin) : tile_end_max;
+  if constexpr (DCA) dca_tiles(a, rg, seqlen, split, tb, tile_end);
+  const int n_iters = static_cast<int>((tile_end - tb + C::NP - 1) / C::NP);
 
   // -------------------------------------------------------------- consumers --
   const int tid = threadIdx.x;  // 0 .. 255
   const int group = warp / C::WT, wh = warp % C::WT;
   const int g = lane >> 2;
-  // Key limits of this lane's two rows (2t, 2t + 1) of the row group.
-  const int lim0 = row_key_limit(a, rg * 8 + 2 * (lane & 3), seqlen);
-  const int lim1 = row_key_limit(a, rg * 8 + 2 * (lane & 3) + 1, seqlen);
+  // Key ranges of this lane's two rows (2t, 2t + 1) of the row group.
+  int lo0, lim0, lo1, lim1;
+  row_key_range(a, rg * 8 + 2 * (lane & 3), seqlen, lo0, lim0);
+  row_key_range(a, rg * 8 + 2 * (lane & 3) + 1, seqlen, lo1, lim1);
 
   float* qb_warp = reinterpret_cast<float*>(smem + C::OFF_QB) + warp * C::NB_W * 8;
   q_block_bias<C::NB_W>(qf, lane, qb_warp);
@@ -392,13 +401,13 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   if (n_iters > 0) {
     wait_stage(0);
-    if (tile_begin + group < tile_end) {
+    if (tb + group < tile_end) {
       qk_tile<D>(record(0), wh, lane, qf, qb, S);
       if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, 0, lane);
     }
   }
   for (int it = 0; it < n_iters; ++it) {
-    const int64_t tile = tile_begin + (int64_t)it * C::NP + group;
+    const int64_t tile = tb + (int64_t)it * C::NP + group;
     const bool next = (it + 1 < n_iters) && (tile + C::NP < tile_end);
     float Sn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (it + 1 < n_iters) wait_stage(it + 1);
@@ -413,7 +422,8 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
       const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * g)));
       const float n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D) + 2 * (g + 8))));
       uint32_t pb0, pb1, pl[2] = {0u, 0u};
-      softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lim0, lim1, scale_log2, n0, n1, st, acc, pb0, pb1, pl);
+      softmax_tile<C::MT_W, C::PSPLIT, DCA>(S, tpos, g, lo0, lim0, lo1, lim1, scale_log2, n0, n1, st, acc, pb0,
+                                            pb1, pl);
       pv_tile<D>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, pl, acc);
     }
     __syncwarp();
@@ -437,7 +447,7 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   // The epilogue reuses the ring. Stages the producer issued before the length
   // was known but that hold none of this CTA's tiles may still be landing:
   // wait for them first.
-  if (a.n_new == 0) {
+  if (!defer) {
     const int pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
     for (int it = n_iters; it < pre; ++it) wait_stage(it);
   }
@@ -448,26 +458,31 @@ __global__ void __launch_bounds__(CDec<D>::THREADS, 1) attn_decode_kernel(Decode
   decode_split_tail<D, C::RING>(a, split, gid, b, kvh, rg, tid, smem);
 }
 
-template <int D>
+template <int D, bool DCA>
 static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = CDec<D>;
   static bool configured = false;  // per process; the attribute is per function
   static int cap = 0;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, DCA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_split_decode(attn_decode_kernel<D>, a, C::THREADS, C::SMEM, &cap, stream);
+  return launch_split_decode(attn_decode_kernel<D, DCA>, a, C::THREADS, C::SMEM, &cap, stream);
+}
+
+template <int D>
+static cudaError_t launch_decode_dim(const DecodeArgs& a, cudaStream_t stream) {
+  return a.dca_chunk > 0 ? launch_decode_d<D, true>(a, stream) : launch_decode_d<D, false>(a, stream);
 }
 
 cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
-    case 64: return launch_decode_d<64>(a, stream);
-    case 128: return launch_decode_d<128>(a, stream);
-    case 256: return launch_decode_d<256>(a, stream);
-    case 512: return launch_decode_d<512>(a, stream);
+    case 64: return launch_decode_dim<64>(a, stream);
+    case 128: return launch_decode_dim<128>(a, stream);
+    case 256: return launch_decode_dim<256>(a, stream);
+    case 512: return launch_decode_dim<512>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -47,8 +47,9 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     if (tid == 0) raise_flag(a.flag, kFlagSeqLenRange);
     seqlen = 0;
   }
-  const int lim0 = row_key_limit(a, rg * 8 + 2 * t, seqlen);  // this lane's rows 2t, 2t + 1
-  const int lim1 = row_key_limit(a, rg * 8 + 2 * t + 1, seqlen);
+  int lo0, lim0, lo1, lim1;  // key ranges of this lane's rows 2t, 2t + 1
+  row_key_range(a, rg * 8 + 2 * t, seqlen, lo0, lim0);
+  row_key_range(a, rg * 8 + 2 * t + 1, seqlen, lo1, lim1);
   const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
   const int64_t tile_begin = split * n_tiles / a.n_split;
   const int64_t tile_end = (split + 1) * n_tiles / a.n_split;
@@ -89,7 +90,8 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     }
     if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, it & 1, lane);
     uint32_t pb0, pb1, pl[2] = {0u, 0u};
-    softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lim0, lim1, a.scale_log2, 1.0f, 1.0f, st, acc, pb0, pb1, pl);
+    softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lo0, lim0, lo1, lim1, a.scale_log2, 1.0f, 1.0f, st, acc, pb0,
+                                     pb1, pl);
     // ---- O^T += V^T P^T: lane reads positions 2t, 2t+1, 2t+8, 2t+9 ----
     const __half* vp = vb + tpos * D + dbase;
 #pragma unroll

@@ -200,7 +200,8 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int D, int Hkv, int B, int64_t capacity, const int32_t* seq_len,
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
-                             void* stream, const AppendRows* app = nullptr, int causal_q = 0) {
+                             void* stream, const AppendRows* app = nullptr, int causal_q = 0,
+                             int dca_chunk = 0) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
   if (s != CKV_OK) return s;
@@ -243,6 +244,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.n_q = n_q;
   a.n_q_heads = n_q_heads;
   a.causal_q = causal_q;
+  a.dca_chunk = dca_chunk;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_split = p.n_split;
   a.n_row_groups = p.n_row_groups;
@@ -276,6 +278,69 @@ ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64
   return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
                     cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
                     workspace, ws_bytes, stream);
+}
+
+// DCA decode workspace: the decode's (3 query rows per query head), then the
+// three regimes' partial outputs [batch][3][n_q_heads][D] and lse values.
+static size_t dca_ws_parts(const ckv_cache* cache, int n_q_heads, size_t* o_off, size_t* l_off) {
+  const size_t rows = static_cast<size_t>(cache->batch) * 3 * n_q_heads;
+  *o_off = 0;
+  *l_off = (rows * cache->head_dim * sizeof(float) + 255) / 256 * 256;
+  return *l_off + (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t ckv_attn_decode_dca_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q_heads,
+                                     int32_t n_split) {
+  const size_t dec = ckv_attn_decode_workspace(cache, max_seq_len, 3, n_q_heads, n_split);
+  if (dec == 0) return 0;
+  size_t o_off, l_off;
+  return (dec + 255) / 256 * 256 + dca_ws_parts(cache, n_q_heads, &o_off, &l_off);
+}
+
+ckv_status ckv_attn_decode_dca(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                               int32_t chunk, const void* q_f16, int32_t n_q_heads, float scale, int32_t n_split,
+                               float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  ckv_status s = check_cache(cache);
+  if (s != CKV_OK) return s;
+  if (chunk < 1) return fail(CKV_ERR_INVALID_ARG, "chunk must be positive (got %d)", chunk);
+  if (!out || !lse) return fail(CKV_ERR_INVALID_ARG, "null out/lse");
+  const size_t dec = ckv_attn_decode_workspace(cache, max_seq_len, 3, n_q_heads, n_split);
+  if (dec == 0) {
+    // Invalid geometry: the decode's own checks give the status and message.
+    return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
+                      cache->capacity, seq_len, max_seq_len, q_f16, 3, n_q_heads, scale, n_split, out, lse,
+                      workspace, ws_bytes, stream, nullptr, 0, chunk);
+  }
+  const size_t need = ckv_attn_decode_dca_workspace(cache, max_seq_len, n_q_heads, n_split);
+  s = check_ws(workspace, ws_bytes, need);
+  if (s != CKV_OK) return s;
+  size_t o_off, l_off;
+  dca_ws_parts(cache, n_q_heads, &o_off, &l_off);
+  uint8_t* parts = static_cast<uint8_t*>(workspace) + (dec + 255) / 256 * 256;
+  float* po = reinterpret_cast<float*>(parts + o_off);
+  float* pl = reinterpret_cast<float*>(parts + l_off);
+  // The three regimes as the three query tokens of one decode.
+  s = run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
+                 cache->capacity, seq_len, max_seq_len, q_f16, 3, n_q_heads, scale, n_split, po, pl, workspace,
+                 dec, stream, nullptr, 0, chunk);
+  if (s != CKV_OK) return s;
+  const int D = cache->head_dim;
+  ckv::LseMergeArgs m{};
+  for (int r = 0; r < 3; ++r) {
+    m.o[r] = po + static_cast<size_t>(r) * n_q_heads * D;
+    m.l[r] = pl + static_cast<size_t>(r) * n_q_heads;
+  }
+  m.n_parts = 3;
+  m.n_rows = static_cast<int64_t>(cache->batch) * n_q_heads;
+  m.d = D;
+  m.rows_per_group = n_q_heads;
+  m.o_group_stride = 3LL * n_q_heads * D;
+  m.l_group_stride = 3LL * n_q_heads;
+  m.out = out;
+  m.lse = lse;
+  const cudaError_t e = ckv::launch_lse_merge(m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
+  return CKV_OK;
 }
 
 ckv_status ckv_attn_decode_verify(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
@@ -338,6 +403,7 @@ ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts, const flo
   a.n_parts = n_parts;
   a.n_rows = n_rows;
   a.d = d;
+  a.rows_per_group = n_rows > 0 ? n_rows : 1;
   a.out = out;
   a.lse = lse;
   cudaError_t e = ckv::launch_lse_merge(a, static_cast<cudaStream_t>(stream));

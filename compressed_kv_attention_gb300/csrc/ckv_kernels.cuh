@@ -42,6 +42,7 @@ struct DecodeArgs {
   const __half* q;
   int n_q, n_q_heads;
   int causal_q;              // 1: query token qi sees [0, seq_len - n_q + qi + 1) (verify batch)
+  int dca_chunk;             // > 0: the n_q = 3 query tokens are the DCA regimes (decode_common.cuh)
   float scale_log2;          // logit scale * log2(e)
   int n_split, n_row_groups;
   float* part;
@@ -90,6 +91,10 @@ struct LseMergeArgs {
   int n_parts;
   int64_t n_rows;
   int d;
+  // Row i of part r is o[r] + (i / rows_per_group) * o_group_stride +
+  // (i % rows_per_group) * d (lse likewise with l_group_stride and 1); the
+  // output row i is out + i * d. One group of n_rows rows: contiguous parts.
+  int64_t rows_per_group, o_group_stride, l_group_stride;
   float* out;
   float* lse;
 };

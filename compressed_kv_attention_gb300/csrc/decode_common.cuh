@@ -51,7 +51,8 @@ __device__ __forceinline__ float warp_max_over_gid(float x) {
 
 // One tile of the online softmax. S holds the logits of positions (g, g+8) x
 // rows (2t, 2t+1) in the mma C layout; position p is visible to row 2t when
-// p < lim0 and to row 2t+1 when p < lim1 (tpos: the tile's first position);
+// lo0 <= p < lim0 and to row 2t+1 when lo1 <= p < lim1 (tpos: the tile's first
+// position);
 // n0/n1 multiply the probabilities of positions g / g+8 (the V norms; 1 for
 // dense values). Rescales acc when the
 // running max grows and returns the two B-operand registers of P'. With
@@ -59,14 +60,22 @@ __device__ __forceinline__ float warp_max_over_gid(float x) {
 // lo in pl) and the caller multiplies both: rounding P' to fp16 alone costs up
 // to 2.7e-3 of |o|_inf at head dim 64 over long rows (2.1e-3 at 128, 1.4e-3 at
 // 256, 8e-4 at 512), so the kernels split at head dims up to 128.
-template <int MTW, bool SPLIT = false>
-__device__ __forceinline__ void softmax_tile(const float (&S)[4], int64_t tpos, int g, int lim0, int lim1,
-                                             float scale_log2, float n0, float n1,
+template <int MTW, bool SPLIT = false, bool LOWER = false>
+__device__ __forceinline__ void softmax_tile(const float (&S)[4], int64_t tpos, int g, int lo0, int lim0, int lo1,
+                                             int lim1, float scale_log2, float n0, float n1,
                                              SoftmaxState& st, float (&acc)[MTW][4],
                                              uint32_t& pb0, uint32_t& pb1, uint32_t* pl = nullptr) {
   const float ninf = -INFINITY;
-  const bool v0 = tpos + g < lim0, v1 = tpos + g < lim1;          // position g, rows 2t / 2t+1
-  const bool v2 = tpos + g + 8 < lim0, v3 = tpos + g + 8 < lim1;  // position g + 8
+  // Position g for rows 2t / 2t+1 (v0, v1), position g + 8 (v2, v3); the
+  // lower limits are checked only in the kernels built for them (LOWER).
+  const int64_t pos_g = tpos + g, pos_g8 = tpos + g + 8;
+  bool v0 = pos_g < lim0, v1 = pos_g < lim1, v2 = pos_g8 < lim0, v3 = pos_g8 < lim1;
+  if constexpr (LOWER) {
+    v0 = v0 && pos_g >= lo0;
+    v1 = v1 && pos_g >= lo1;
+    v2 = v2 && pos_g8 >= lo0;
+    v3 = v3 && pos_g8 >= lo1;
+  }
   const float x0 = v0 ? S[0] * scale_log2 : ninf;
   const float x1 = v1 ? S[1] * scale_log2 : ninf;
   const float x2 = v2 ? S[2] * scale_log2 : ninf;
@@ -256,14 +265,62 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
 }
 
 
-// Keys visible to row `rr` of a row group: [0, seq_len), or with causal_q
-// (a verify batch: the n_q query tokens are the last n_q positions) query
-// token qi sees [0, seq_len - n_q + qi + 1).
-__device__ __forceinline__ int row_key_limit(const DecodeArgs& a, int rr, int seqlen) {
-  if (!a.causal_q) return seqlen;
+// Keys [lo, hi) visible to row `rr` (query token qi = rr / G) of a sequence
+// of length seqlen:
+//  * plain decode: [0, seqlen);
+//  * causal_q (a verify batch: the n_q tokens are the last n_q positions):
+//    [0, seqlen - n_q + qi + 1);
+//  * dca_chunk = c (dual chunk attention of the query at position
+//    i = seqlen - 1, chunk k = i / c; token qi is the regime): intra
+//    [k c, seqlen), successive [(k - 1) c, k c), inter [0, (k - 1) c) — the
+//    three partition [0, seqlen) (DCA page, "Section C design").
+__device__ __forceinline__ void row_key_range(const DecodeArgs& a, int rr, int seqlen, int& lo, int& hi) {
   const int qi = rr / (a.n_q_heads / a.n_kv_heads);
-  const int lim = seqlen - a.n_q + qi + 1;
-  return lim < 0 ? 0 : lim;
+  lo = 0;
+  hi = seqlen;
+  if (a.causal_q) {
+    hi = seqlen - a.n_q + qi + 1;
+    if (hi < 0) hi = 0;
+  } else if (a.dca_chunk > 0) {
+    if (seqlen == 0) return;
+    const int c = a.dca_chunk, k = (seqlen - 1) / c;
+    if (qi == 0) {
+      lo = k * c;
+    } else if (qi == 1) {
+      lo = k >= 1 ? (k - 1) * c : 0;
+      hi = k >= 1 ? k * c : 0;
+    } else {
+      hi = k >= 2 ? (k - 1) * c : 0;
+    }
+  }
+}
+
+// Union of the key ranges of the row group's real rows (tiles outside it are
+// neither fetched nor read): [glo, ghi), empty when glo >= ghi.
+__device__ __forceinline__ void group_key_range(const DecodeArgs& a, int rg, int seqlen, int& glo, int& ghi) {
+  const int R = (a.n_q_heads / a.n_kv_heads) * a.n_q;
+  glo = seqlen;
+  ghi = 0;
+  for (int r = 0; r < 8 && rg * 8 + r < R; ++r) {
+    int lo, hi;
+    row_key_range(a, rg * 8 + r, seqlen, lo, hi);
+    if (lo < hi) {
+      glo = lo < glo ? lo : glo;
+      ghi = hi > ghi ? hi : ghi;
+    }
+  }
+}
+
+// DCA: the n_split CTAs of a row group divide its regime's key range (not
+// the whole cache), so every CTA of every regime streams: tiles [tb, te).
+__device__ __forceinline__ void dca_tiles(const DecodeArgs& a, int rg, int seqlen, int split, int64_t& tb,
+                                          int64_t& te) {
+  int glo, ghi;
+  group_key_range(a, rg, seqlen, glo, ghi);
+  const int64_t lo_t = glo / kTile, hi_t = ghi > glo ? (ghi + kTile - 1) / kTile : lo_t;
+  const int64_t n = hi_t - lo_t;
+  tb = lo_t + (int64_t)split * n / a.n_split;
+  te = lo_t + (int64_t)(split + 1) * n / a.n_split;
 }
 
 // Which query vector row `rr` (0 <= rr < G * n_q) of kv head `kvh` is: the

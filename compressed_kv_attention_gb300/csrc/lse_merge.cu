@@ -11,15 +11,17 @@ namespace ckv {
 // One CTA per row; threads stride over the d columns (float4 where possible).
 __global__ void __launch_bounds__(128) lse_merge_kernel(LseMergeArgs a) {
   const int64_t row = blockIdx.x;
+  const int64_t grp = row / a.rows_per_group, j = row % a.rows_per_group;
+  const int64_t orow = grp * a.o_group_stride + j * a.d, lrow = grp * a.l_group_stride + j;
   float M = -INFINITY;
-  for (int r = 0; r < a.n_parts; ++r) M = fmaxf(M, a.l[r][row]);
+  for (int r = 0; r < a.n_parts; ++r) M = fmaxf(M, a.l[r][lrow]);
   float w[16];
   float W = 0.0f;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     w[r] = 0.0f;
     if (r < a.n_parts && M != -INFINITY) {
-      const float lr = a.l[r][row];
+      const float lr = a.l[r][lrow];
       w[r] = (lr == -INFINITY) ? 0.0f : expf(lr - M);
       W += w[r];
     }
@@ -29,7 +31,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(LseMergeArgs a) {
     float s = 0.0f;
 #pragma unroll
     for (int r = 0; r < 16; ++r)
-      if (r < a.n_parts && w[r] != 0.0f) s = fmaf(w[r], a.o[r][row * a.d + c], s);
+      if (r < a.n_parts && w[r] != 0.0f) s = fmaf(w[r], a.o[r][orow + c], s);
     a.out[row * a.d + c] = s * inv;
   }
   __syncthreads();  // every read of the lse parts is done before lse may be overwritten

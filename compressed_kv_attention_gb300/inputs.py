@@ -114,6 +114,7 @@ class Workload:
     tail_len: int = 0     # shared-prefix fan-out: private fp16 tail per agent
     n_new: int = 0        # prefill: new tokens appended and attended causally
     n_q: int = 1          # decode: query tokens per sequence (a verify batch when > 1)
+    dca_chunk: int = 0    # decode: dual chunk attention with this chunk (three regime queries)
     q_dtype: str = "float16"
 
     @property
@@ -128,7 +129,8 @@ def _one_percent(d: int) -> int:
 # The five workloads: a tiny decode that the oracle finishes in well under a
 # second, the Gemma-4 global-layer decode, the shared-prefix fan-out decode, the
 # long-context decode and the chunked prefill; and a verify batch of 4 drafted
-# tokens over the Gemma-4 global-layer cache (multi-query decode).
+# tokens over the Gemma-4 global-layer cache (multi-query decode), and dual
+# chunk attention of one token over it with 8192-token chunks.
 WORKLOADS = {
     "tiny_decode": Workload("tiny_decode", head_dim=128, n_kv_heads=1, n_q_heads=4, batch=1,
                             seq_len=256, seed=0, n_outliers=2),
@@ -141,6 +143,8 @@ WORKLOADS = {
                             seq_len=262144, seed=3, n_outliers=_one_percent(512)),
     "verify_decode": Workload("verify_decode", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=1,
                               seq_len=32768, seed=5, n_outliers=_one_percent(512), n_q=4),
+    "dca_decode": Workload("dca_decode", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=1,
+                           seq_len=32768, seed=6, n_outliers=_one_percent(512), dca_chunk=8192),
     "chunked_prefill": Workload("chunked_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16,
                                 batch=1, seq_len=32768, seed=4, n_outliers=_one_percent(512),
                                 n_new=2048, q_dtype="bfloat16"),

@@ -180,6 +180,30 @@ CKV_API ckv_status ckv_attn_decode_verify(const ckv_cache* cache, const int32_t*
                                           size_t ws_bytes, void* stream);
 
 /*
+ * attn_decode_dca — dual chunk attention of one query token per sequence (the
+ * token at position i = seq_len[b] - 1) over the packed cache. DCA page
+ * ("Feature — Gemma-4 A4B Dual Chunk Attention (DCA), training-free 1M
+ * context"), section "Section C design": with chunk c and k = i / c, three
+ * regimes partition the keys [0, seq_len[b]):
+ *   intra       [k c, seq_len)        query q_f16[b][0]
+ *   successive  [(k - 1) c, k c)      query q_f16[b][1]
+ *   inter       [0, (k - 1) c)        query q_f16[b][2]
+ * (each query roped for its regime by the caller; the keys are cached as
+ * roped once), and their softmaxes are merged exactly by log-sum-exp.
+ * q_f16: fp16 [batch][3][n_q_heads][D]; out: float32 [batch][n_q_heads][D];
+ * lse: float32 [batch][n_q_heads]. chunk >= 1. Two launches: the decode
+ * kernel with the regimes as its three query rows (each row group reads only
+ * its regime's tiles) and the merge. workspace:
+ * ckv_attn_decode_dca_workspace() bytes, zero-filled before first use.
+ */
+CKV_API size_t ckv_attn_decode_dca_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q_heads,
+                                             int32_t n_split);
+CKV_API ckv_status ckv_attn_decode_dca(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                                       int32_t chunk, const void* q_f16, int32_t n_q_heads, float scale,
+                                       int32_t n_split, float* out, float* lse, void* workspace,
+                                       size_t ws_bytes, void* stream);
+
+/*
  * attn_decode_append — one decode step: quantise n_new new K/V rows of every
  * sequence into the cache at positions [seq_len[b] - n_new, seq_len[b]) (the
  * same bytes ckv_kv_pack writes), then attend as attn_decode over

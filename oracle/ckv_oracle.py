@@ -307,6 +307,46 @@ def verify_decode_reference(q, k_hat, v_hat, seq_len, scale: float):
     return o, lse
 
 
+def dca_ranges(seq_len: int, chunk: int):
+    """Key ranges [lo, hi) of the three DCA regimes for the query at position
+    i = seq_len - 1 with chunk size c: the [DCA] page's "Section C design"
+    keep-masks (chunk of a position = floor(pos / c), causal j <= i) are
+    intra: chunk(j) == chunk(i); successive: chunk(j) == chunk(i) - 1;
+    inter: chunk(j) < chunk(i) - 1. With k = chunk(i) they are the ranges
+    [k c, i + 1), [(k - 1) c, k c) and [0, (k - 1) c), clipped at 0.
+    """
+    if seq_len <= 0:
+        return [(0, 0)] * 3
+    k = (seq_len - 1) // chunk
+    intra = (k * chunk, seq_len)
+    succ = ((k - 1) * chunk, k * chunk) if k >= 1 else (0, 0)
+    inter = (0, (k - 1) * chunk) if k >= 2 else (0, 0)
+    return [intra, succ, inter]
+
+
+def dca_decode_reference(q, k_hat, v_hat, seq_len: int, chunk: int, scale: float):
+    """Dual chunk attention of the token at position seq_len - 1 for one sequence.
+
+    ``q [3, Hq, D]`` holds the query of each regime (intra, successive, inter;
+    roped for its regime by the caller, [DCA] "rope-K-once, rope-Q-thrice");
+    every regime attends over its key range (``dca_ranges``) and the three
+    softmaxes are merged by ``lse_merge`` (step 4 of the page's graph body).
+    Returns ``o [Hq, D]`` and ``lse [Hq]``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    _, Hq, D = q.shape
+    Hkv = k_hat.shape[0]
+    o = np.zeros((Hq, v_hat.shape[-1]))
+    lse = np.zeros(Hq)
+    for h in range(Hq):
+        kh = kv_head_of(h, Hq, Hkv)
+        parts = [attention(q[r:r + 1, h, :], k_hat[kh, lo:hi], v_hat[kh, lo:hi], scale)
+                 for r, (lo, hi) in enumerate(dca_ranges(seq_len, chunk))]
+        oh, lh = lse_merge([p[0] for p in parts], [p[1] for p in parts])
+        o[h], lse[h] = oh[0], lh[0]
+    return o, lse
+
+
 def prefill_reference(q, k_hat, v_hat, n_cached: int, scale: float):
     """Causal chunked prefill for one sequence.
 

@@ -95,6 +95,22 @@ def test_decode_argument_checks(lib):
     assert call(cache=_fake_cache(D=100)) == -2
 
 
+def test_dca_and_verify_argument_checks(lib):
+    fake = 0x7f0000000000
+    c = _fake_cache(D=512, Hkv=2, cap=4096)
+    need = lib.ckv_attn_decode_dca_workspace(ctypes.byref(c), 4096, 16, 8)
+    dec = lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 3, 16, 8)
+    assert need > dec > 0                           # the decode's workspace plus the three regimes' partials
+    call = lambda chunk=64, hq=16, ws=fake, wsb=need: lib.ckv_attn_decode_dca(
+        ctypes.byref(c), fake, 4096, chunk, fake, hq, 0.04, 8, fake, fake, ws, wsb, None)
+    assert call(chunk=0) == -1
+    assert call(hq=15) == -2
+    assert call(wsb=need - 1) == -3
+    assert call(ws=None) == -3
+    assert lib.ckv_attn_decode_verify(ctypes.byref(c), fake, 4096, fake, 4, 15, 0.04, 8, fake, fake, fake,
+                                      need, None) == -2
+
+
 def test_decode_f16_and_merge_argument_checks(lib):
     fake = 0x7f0000000000
     need = lib.ckv_attn_decode_f16_workspace(512, 2, 15, 512, 1, 16, 4)

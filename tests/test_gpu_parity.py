@@ -193,6 +193,37 @@ def test_verify_decode_is_causal_among_the_batch(D, Hkv, Hq, n_q, n_split):
     H.check_attention(out.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"verify D={D} Hq={Hq} n_q={n_q}")
 
 
+@pytest.mark.parametrize("D,Hkv,Hq,chunk,n_split", [(128, 2, 16, 64, 0), (512, 2, 16, 50, 0), (512, 1, 4, 16, 7),
+                                                    (64, 1, 2, 300, 0), (128, 2, 8, 1, 0), (512, 2, 16, 32, 400)])
+def test_dca_decode_matches_oracle(D, Hkv, Hq, chunk, n_split):
+    """Dual chunk attention: three regime queries over the intra, successive and
+    inter key ranges of the last position, merged by log-sum-exp. Head ratios
+    below 8 put several regimes in one group of 8 rows; chunk 1 and a chunk
+    longer than the sequence are the degenerate cases."""
+    _need_gpu()
+    B, T, cap = 3, 203, 224
+    seq_lens = [203, 0, 150]
+    k, v, outl = make_kv(D, Hkv, B, T, seed=41 + D + Hq + chunk, n_out=max(1, round(0.01 * D)))
+    q = inputs.normal_tensor((B, 3, Hq, D), 41 + D, "qdca", outl)
+    signs = inputs.tbq_signs(D)
+    qs, d16, codes, n16, u = oracle_cache(k, v, signs)
+    o_ref = np.zeros((B, Hq, D))
+    lse_ref = np.zeros((B, Hq))
+    for b in range(B):
+        T_b = seq_lens[b]
+        kh = O.q8_0_dequantize(qs[b, :, :T_b], d16[b, :, :T_b])
+        vh = O.tbq3_dequantize(codes[b, :, :T_b], n16[b, :, :T_b], signs)
+        o_ref[b], lse_ref[b] = O.dca_decode_reference(q[b], kh, vh, T_b, chunk, 1.0 / math.sqrt(D))
+    cache = gpu_pack(k, v, signs, cap)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(ckv.attn_decode_dca_workspace(cache, T, Hq, n_split), dtype=torch.uint8, device=DEV)
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device=DEV)
+    ckv.attn_decode_dca(cache, sl, T, chunk, to_dev(q), 1.0 / math.sqrt(D), out, lse, ws, n_split=n_split)
+    assert ckv.read_device_flag(ws) == 0
+    H.check_attention(out.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"dca D={D} Hq={Hq} chunk={chunk}")
+
+
 def test_decode_seq_len_out_of_range_sets_flag():
     _need_gpu()
     D, T = 128, 64

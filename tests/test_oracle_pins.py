@@ -359,6 +359,48 @@ def test_verify_decode_reference_is_causal_among_the_batch():
     assert (o[:2] == 0).all() and (lse[:2] == -np.inf).all() and np.isfinite(lse[2:]).all()
 
 
+@pytest.mark.parametrize("seq_len,chunk", [(1, 4), (4, 4), (5, 4), (9, 4), (17, 4), (23, 5), (40, 7), (12, 100)])
+def test_dca_ranges_partition_the_causal_row(seq_len, chunk):
+    """The three regimes cover [0, seq_len) exactly once, each within its chunk
+    relation to the query's chunk (the page's keep-masks written out)."""
+    rs = O.dca_ranges(seq_len, chunk)
+    cover = np.zeros(seq_len, int)
+    i = seq_len - 1
+    for r, (lo, hi) in enumerate(rs):
+        cover[lo:hi] += 1
+        for j in range(lo, hi):
+            if r == 0:
+                assert j // chunk == i // chunk
+            elif r == 1:
+                assert j // chunk == i // chunk - 1
+            else:
+                assert j // chunk < i // chunk - 1
+    assert (cover == 1).all()
+
+
+def test_dca_reference_reduces_to_attention_and_brute_force():
+    """With the same query in all three regimes DCA is plain attention over
+    [0, seq_len); with different queries it matches a brute-force softmax per
+    regime merged by hand."""
+    rng = np.random.default_rng(14)
+    Hq, Hkv, D, T = 4, 2, 16, 40
+    k, v = rng.standard_normal((Hkv, T, D)), rng.standard_normal((Hkv, T, D))
+    q1 = rng.standard_normal((1, Hq, D))
+    o, lse = O.dca_decode_reference(np.repeat(q1, 3, axis=0), k, v, 37, 8, 0.25)
+    od, ld = O.decode_reference(q1, k, v, 37, 0.25)
+    assert np.abs(o - od[0]).max() < 1e-12 and np.abs(lse - ld[0]).max() < 1e-12
+    q3 = rng.standard_normal((3, Hq, D))
+    o, lse = O.dca_decode_reference(q3, k, v, 37, 8, 0.25)
+    h = 1
+    num, den = np.zeros(D), 0.0
+    for r, (lo, hi) in enumerate([(32, 37), (24, 32), (0, 24)]):
+        for j in range(lo, hi):
+            w = np.exp(0.25 * q3[r, h] @ k[0, j])
+            num += w * v[0, j]
+            den += w
+    assert np.allclose(o[h], num / den, rtol=0, atol=1e-12) and abs(lse[h] - np.log(den)) < 1e-12
+
+
 # ----------------------------------------------------------- layout ------
 
 @pytest.mark.parametrize("D", [64, 128, 256, 512])
