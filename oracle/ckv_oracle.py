@@ -140,6 +140,67 @@ def fwht_orthonormal(y) -> np.ndarray:
     return fwht(y) / np.sqrt(d)
 
 
+def lloyd_max_gaussian(levels: int) -> np.ndarray:
+    """Centroids of the minimum-MSE quantiser of N(0,1) with ``levels`` levels, by
+    Lloyd's iteration: thresholds are the midpoints of neighbouring centroids and
+    each centroid is the conditional mean of its cell,
+    c_k = (phi(t_k) - phi(t_{k+1})) / (Phi(t_{k+1}) - Phi(t_k)), with phi and Phi
+    the normal density and distribution function (closed forms via erf). Starts
+    from the equal-probability cell centres and stops when no centroid moves by
+    1e-15. [PolyKV] section "S2 perf-path Level B" runs the same scheme at 2, 3
+    and 4 bits (turbo2 / turbo3 / turbo4).
+    """
+    import math
+    from scipy.special import erfinv
+
+    def pdf(x):
+        return 0.0 if not np.isfinite(x) else math.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
+
+    def cdf(x):
+        if not np.isfinite(x):
+            return 1.0 if x > 0 else 0.0
+        return 0.5 * (1.0 + math.erf(x / math.sqrt(2.0)))
+
+    c = np.array([math.sqrt(2.0) * erfinv(2.0 * (k + 0.5) / levels - 1.0) for k in range(levels)])
+    for _ in range(100000):
+        t = np.concatenate([[-np.inf], 0.5 * (c[:-1] + c[1:]), [np.inf]])
+        new = np.array([(pdf(t[k]) - pdf(t[k + 1])) / (cdf(t[k + 1]) - cdf(t[k])) for k in range(levels)])
+        moved = np.abs(new - c).max()
+        c = new
+        if moved < 1e-15:
+            break
+    return c
+
+
+#: Value bit widths the cache supports: 2, 3 or 4 bits per coordinate.
+TBQ_BITS = (2, 3, 4)
+
+
+def tbq_centroids(bits: int) -> np.ndarray:
+    """Ascending centroid table of the ``bits``-bit quantiser: the printed 3-bit
+    table (north of the method), and at 2 and 4 bits the Lloyd-Max centroids of
+    N(0,1) rounded to 4 decimals like the printed one."""
+    if bits == 3:
+        return LLOYD_MAX_3BIT
+    if bits not in TBQ_BITS:
+        raise ValueError("bits must be 2, 3 or 4")
+    return np.round(lloyd_max_gaussian(1 << bits), 4)
+
+
+def nearest_centroid_bits(u, bits: int) -> np.ndarray:
+    """Index (ascending centroids) of the nearest ``bits``-bit centroid; an exact
+    tie goes to the neighbour of smaller magnitude and u == 0 to the smallest
+    positive centroid (index 2^(bits-1)), as at 3 bits."""
+    table = tbq_centroids(bits)
+    u = np.asarray(u, dtype=np.float64)
+    dist = np.abs(u[..., None] - table)
+    best = dist.min(axis=-1, keepdims=True)
+    tied = dist == best
+    rank = np.abs(table) * 4.0 - (table > 0)
+    score = np.where(tied, rank, np.inf)
+    return score.argmin(axis=-1).astype(np.uint8)
+
+
 def nearest_centroid(u) -> np.ndarray:
     """Index (0..7, ascending centroids) of the Lloyd-Max centroid nearest to each u.
 
@@ -186,10 +247,31 @@ def tbq3_quantize(x, signs):
 
 def tbq3_dequantize(codes, n16, signs) -> np.ndarray:
     """Dense float64 values: V_hat = s * H_d^T ((n16 / sqrt(d)) * c[code]) / sqrt(d)."""
+    return tbq_dequantize(codes, n16, signs, 3)
+
+
+def tbq_quantize(x, signs, bits: int = 3):
+    """TBQ quantisation at ``bits`` bits per coordinate: the steps of
+    :func:`tbq3_quantize` with the ``bits``-bit centroid table (a zero vector
+    stores the smallest positive centroid's index everywhere and norm 0)."""
+    if bits == 3:
+        return tbq3_quantize(x, signs)
+    x = np.asarray(x, dtype=np.float16).astype(np.float64)
+    s = np.asarray(signs).astype(np.float64)
+    d = x.shape[-1]
+    z = fwht_orthonormal(s * x)
+    r = np.sqrt(np.sum(x * x, axis=-1))
+    safe_r = np.where(r == 0.0, 1.0, r)
+    u = np.where(r[..., None] == 0.0, 0.0, z * np.sqrt(d) / safe_r[..., None])
+    return nearest_centroid_bits(u, bits), to_fp16(r), u
+
+
+def tbq_dequantize(codes, n16, signs, bits: int = 3) -> np.ndarray:
+    """Dense float64 values: V_hat = s * H_d^T ((n16 / sqrt(d)) * c_bits[code]) / sqrt(d)."""
     codes = np.asarray(codes)
     d = codes.shape[-1]
     n = np.asarray(n16, dtype=np.float16).astype(np.float64)
-    w = (n / np.sqrt(d))[..., None] * LLOYD_MAX_3BIT[codes]
+    w = (n / np.sqrt(d))[..., None] * tbq_centroids(bits)[codes]
     return np.asarray(signs).astype(np.float64) * fwht_orthonormal(w)
 
 

@@ -7,20 +7,22 @@ written here from its definition, independently of the CUDA packer, so that
 the packer's bytes can be compared with the oracle's.
 
 Definition. Each (sequence, kv-head) owns T_cap / 16 tile records; tile t covers
-token positions [16 t, 16 t + 16). A record is 23 D + 32 bytes (D = head_dim):
+token positions [16 t, 16 t + 16). With b bits per V code (b = 2, 3 or 4; 3 is
+the method's TBQ3) a record is 17 D + 2 b D + 32 bytes (D = head_dim; 23 D + 32
+at b = 3):
 
   [0, 16D)      K codes. Element (p, i) (p = position in tile, i = dim) sits at
                 ((i // 32) * 32 + L) * 16 + (p // 8) * 8 + (i % 8),
                 with lane L = 4 * (p % 8) + (i % 32) // 8.
   [16D, 17D)    K scales, fp16, [16][D/32] row-major: (p, block) at 16D + 2 (p D/32 + block).
-  [17D, 23D)    V codes, 3 bits each. Lane L owns a stream of 3D/16 bytes. With
+  [17D, 17D + 2bD)  V codes, b bits each. Lane L owns a stream of b D/16 bytes. With
                 G = D/8, g = i // G, u = i % G, L = 4 g + (p % 8) // 2 and
                 pair index pi = 4 (u // 2) + (u % 2) + 2 (p // 8), the code of (p, i)
-                occupies stream bits [6 pi + 3 (p % 2), 6 pi + 3 (p % 2) + 3), least
-                significant bit first (stream bit b is bit b % 8 of stream byte b // 8).
+                occupies stream bits [2b pi + b (p % 2), 2b pi + b (p % 2) + b), least
+                significant bit first (stream bit x is bit x % 8 of stream byte x // 8).
                 Stream byte s of lane L is stored at 17D + ((s // gr) * 32 + L) * gr + s % gr,
-                gr = 16, 8 or 4: the largest of those dividing 3D/16.
-  [23D, 23D+32) V norms, fp16, one per position: p at 23D + 2 p.
+                gr = 16, 8 or 4: the largest of those dividing b D/16.
+  [17D + 2bD, +32)  V norms, fp16, one per position: p at 17D + 2bD + 2 p.
 """
 from __future__ import annotations
 
@@ -29,12 +31,12 @@ import numpy as np
 TILE = 16
 
 
-def record_bytes(D: int) -> int:
-    return 23 * D + 32
+def record_bytes(D: int, bits: int = 3) -> int:
+    return 17 * D + 2 * bits * D + 32
 
 
-def _granule(D: int) -> int:
-    per_lane = 3 * D // 16
+def _granule(D: int, bits: int = 3) -> int:
+    per_lane = bits * D // 16
     for gr in (16, 8, 4):
         if per_lane % gr == 0:
             return gr
@@ -56,41 +58,41 @@ def k_scale_offsets(D: int) -> np.ndarray:
     return 16 * D + 2 * (p * (D // 32) + b)
 
 
-def v_code_bits(D: int) -> np.ndarray:
-    """[16, D, 3] absolute bit index (byte * 8 + bit) of each V code bit inside a record."""
+def v_code_bits(D: int, bits: int = 3) -> np.ndarray:
+    """[16, D, bits] absolute bit index (byte * 8 + bit) of each V code bit inside a record."""
     G = D // 8
-    gr = _granule(D)
+    gr = _granule(D, bits)
     p = np.arange(TILE)[:, None]
     i = np.arange(D)[None, :]
     g, u = i // G, i % G
     lane = 4 * g + (p % 8) // 2
     pair = 4 * (u // 2) + (u % 2) + 2 * (p // 8)
-    first = 6 * pair + 3 * (p % 2)
-    bits = first[..., None] + np.arange(3)[None, None, :]
-    stream_byte = bits // 8
+    first = 2 * bits * pair + bits * (p % 2)
+    sbit = first[..., None] + np.arange(bits)[None, None, :]
+    stream_byte = sbit // 8
     byte = 17 * D + ((stream_byte // gr) * 32 + lane[..., None]) * gr + stream_byte % gr
-    return byte * 8 + bits % 8
+    return byte * 8 + sbit % 8
 
 
-def v_norm_offsets(D: int) -> np.ndarray:
-    return 23 * D + 2 * np.arange(TILE)
+def v_norm_offsets(D: int, bits: int = 3) -> np.ndarray:
+    return 17 * D + 2 * bits * D + 2 * np.arange(TILE)
 
 
-def pack_records(qs, d16, codes, n16, capacity: int) -> np.ndarray:
+def pack_records(qs, d16, codes, n16, capacity: int, bits: int = 3) -> np.ndarray:
     """Lay out one (sequence, kv-head) stream of T tokens as capacity/16 records.
 
-    ``qs int8 [T, D]``, ``d16 fp16 [T, D/32]``, ``codes uint8 [T, D]`` (0..7),
+    ``qs int8 [T, D]``, ``d16 fp16 [T, D/32]``, ``codes uint8 [T, D]`` (0..2^bits - 1),
     ``n16 fp16 [T]``. Positions >= T are left zero. Returns uint8
-    ``[capacity/16, record_bytes(D)]``.
+    ``[capacity/16, record_bytes(D, bits)]``.
     """
     qs = np.asarray(qs, dtype=np.int8)
     T, D = qs.shape
     if capacity % TILE or T > capacity:
         raise ValueError("capacity must be a multiple of 16 and hold every token")
     n_tiles = capacity // TILE
-    out = np.zeros((n_tiles, record_bytes(D)), dtype=np.uint8)
+    out = np.zeros((n_tiles, record_bytes(D, bits)), dtype=np.uint8)
     kofs, sofs = k_code_offsets(D), k_scale_offsets(D)
-    vbits, nofs = v_code_bits(D), v_norm_offsets(D)
+    vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits)
     qs_u8 = qs.view(np.uint8)
     d16_u8 = np.asarray(d16, dtype=np.float16).view(np.uint8).reshape(T, D // 32, 2)
     n16_u8 = np.asarray(n16, dtype=np.float16).view(np.uint8).reshape(T, 2)
@@ -103,18 +105,18 @@ def pack_records(qs, d16, codes, n16, capacity: int) -> np.ndarray:
         rec[sofs[p] + 1] = d16_u8[t, :, 1]
         rec[nofs[p]] = n16_u8[t, 0]
         rec[nofs[p] + 1] = n16_u8[t, 1]
-        for k in range(3):
+        for k in range(bits):
             bit = vbits[p, :, k]
             val = (codes[t] >> k) & 1
             np.bitwise_or.at(rec, bit // 8, (val << (bit % 8)).astype(np.uint8))
     return out
 
 
-def unpack_records(records, T: int, D: int):
+def unpack_records(records, T: int, D: int, bits: int = 3):
     """Inverse of :func:`pack_records` for the first T positions."""
     records = np.asarray(records, dtype=np.uint8)
     kofs, sofs = k_code_offsets(D), k_scale_offsets(D)
-    vbits, nofs = v_code_bits(D), v_norm_offsets(D)
+    vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits)
     qs = np.zeros((T, D), dtype=np.int8)
     d16 = np.zeros((T, D // 32), dtype=np.float16)
     codes = np.zeros((T, D), dtype=np.uint8)
@@ -126,7 +128,7 @@ def unpack_records(records, T: int, D: int):
         d16[t] = (rec[sofs[p]].astype(np.uint16) | (rec[sofs[p] + 1].astype(np.uint16) << 8)).view(np.float16)
         n16[t] = np.array([rec[nofs[p]] | (rec[nofs[p] + 1].astype(np.uint16) << 8)], dtype=np.uint16).view(np.float16)[0]
         c = np.zeros(D, dtype=np.uint8)
-        for k in range(3):
+        for k in range(bits):
             bit = vbits[p, :, k]
             c |= (((rec[bit // 8] >> (bit % 8)) & 1) << k).astype(np.uint8)
         codes[t] = c

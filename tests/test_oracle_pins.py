@@ -132,6 +132,105 @@ def test_code_frequencies_follow_gaussian_cells():
     assert np.allclose(probs[4:], [0.19166, 0.16147, 0.10663, 0.04024], atol=2e-4)
 
 
+# ------------------------------------------- other bit widths (TBQ2, TBQ4) --
+
+def _cells(c):
+    return np.concatenate([[-np.inf], (c[1:] + c[:-1]) / 2, [np.inf]])
+
+
+def _mse(c):
+    t = _cells(c)
+    return sum(scipy.integrate.quad(lambda u: (u - c[k]) ** 2 * scipy.stats.norm.pdf(u), t[k], t[k + 1])[0]
+               for k in range(len(c)))
+
+
+def test_lloyd_iteration_reproduces_the_printed_3bit_table():
+    # The iteration is pinned by the 3-bit table the method prints (its outer
+    # value 2.1520 is the classic 2.152, given to 3 decimals: the iterate is 2.15195).
+    assert np.abs(O.lloyd_max_gaussian(8) - O.LLOYD_MAX_3BIT).max() < 6e-5
+    assert np.array_equal(O.tbq_centroids(3), O.LLOYD_MAX_3BIT)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_tbq_tables_are_lloyd_max_fixed_points(bits):
+    c = O.tbq_centroids(bits)
+    assert len(c) == 1 << bits and np.all(np.diff(c) > 0)
+    assert np.array_equal(c, -c[::-1])                          # symmetric
+    t = _cells(c)
+    a, b = t[:-1], t[1:]
+    cond_mean = (scipy.stats.norm.pdf(a) - scipy.stats.norm.pdf(b)) / \
+        (scipy.stats.norm.cdf(b) - scipy.stats.norm.cdf(a))
+    assert np.abs(cond_mean - c).max() < 5e-5                   # centroid condition
+    # Any perturbation of one centroid raises the distortion (local optimum).
+    base = _mse(c)
+    for k in range(len(c) // 2, len(c)):
+        for e in (-0.01, 0.01):
+            cp = c.copy()
+            cp[k] += e
+            assert _mse(np.sort(cp)) > base
+
+
+def test_tbq_distortions_against_known_values():
+    # Minimum mean-square error of N(0,1) at 4, 8 and 16 levels: 0.1175, 0.03455,
+    # 0.009497 (the classic Lloyd-Max figures); 2-level would be 1 - 2/pi.
+    assert abs(_mse(O.tbq_centroids(2)) - 0.1175) < 1e-4
+    assert abs(_mse(O.tbq_centroids(3)) - 0.03455) < 2e-5
+    assert abs(_mse(O.tbq_centroids(4)) - 0.009497) < 5e-6
+    c1 = O.lloyd_max_gaussian(2)
+    assert abs(c1[1] - math.sqrt(2 / math.pi)) < 1e-12 and abs(_mse(c1) - (1 - 2 / math.pi)) < 1e-9
+    # 2-bit thresholds: 0 and +-0.9816; the outer cells hold 2 (1 - Phi(0.9816)) = 0.3263.
+    t2 = _cells(O.tbq_centroids(2))
+    assert abs(t2[3] - 0.9816) < 1e-4
+    assert abs(2 * scipy.stats.norm.sf(t2[3]) - 0.3263) < 1e-4
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_nearest_centroid_bits_bruteforce_and_ties(bits):
+    c = O.tbq_centroids(bits)
+    rng = np.random.default_rng(bits)
+    u = rng.standard_normal(4000) * 1.5
+    got = O.nearest_centroid_bits(u, bits)
+    for ui, gi in zip(u, got):
+        assert gi == int(np.argmin(np.abs(ui - c)))
+    half = len(c) // 2
+    for k in range(len(c) - 1):
+        m = (c[k] + c[k + 1]) / 2
+        if m == 0.0:
+            continue
+        if abs(m - c[k]) == abs(m - c[k + 1]):   # an exact tie -> smaller magnitude
+            assert O.nearest_centroid_bits(np.array([m]), bits)[0] == (k + 1 if m < 0 else k)
+        lo, hi = np.nextafter(m, -np.inf), np.nextafter(m, np.inf)
+        assert O.nearest_centroid_bits(np.array([lo, hi]), bits).tolist() in ([k, k + 1], [k, k], [k + 1, k + 1])
+        assert O.nearest_centroid_bits(np.array([m - 1e-9, m + 1e-9]), bits).tolist() == [k, k + 1]
+    assert O.nearest_centroid_bits(np.array([0.0, -0.0]), bits).tolist() == [half, half]
+    # At 3 bits the general rule is the 3-bit one.
+    u3 = rng.standard_normal(2000) * 1.5
+    assert np.array_equal(O.nearest_centroid_bits(u3, 3), O.nearest_centroid(u3))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_tbq_roundtrip_cosine_tracks_distortion(bits):
+    # For a Lloyd-Max quantiser the round-trip cosine of a long random vector
+    # tends to sqrt(1 - D_b); at 3 bits the same estimate gives the page's 0.983.
+    rng = np.random.default_rng(20 + bits)
+    d = 512
+    x = rng.standard_normal((1500, d)).astype(np.float16)
+    s = inputs.tbq_signs(d)
+    codes, n16, _ = O.tbq_quantize(x, s, bits)
+    assert codes.max() == (1 << bits) - 1 and codes.min() == 0
+    xh = O.tbq_dequantize(codes, n16, s, bits)
+    xf = x.astype(np.float64)
+    cos = np.sum(xf * xh, 1) / (np.linalg.norm(xf, axis=1) * np.linalg.norm(xh, axis=1))
+    assert abs(cos.mean() - math.sqrt(1 - _mse(O.tbq_centroids(bits)))) < 4 * cos.std() / math.sqrt(len(cos)) + 2e-4
+    # the zero vector: norm 0, the smallest positive centroid's index everywhere
+    zc, zn, _ = O.tbq_quantize(np.zeros((1, d), np.float16), s, bits)
+    assert zn[0] == 0 and (zc == 1 << (bits - 1)).all()
+    # bits=3 through the general entry point is TBQ3
+    c3, n3, _ = O.tbq_quantize(x[:50], s, 3)
+    r3, m3, _ = O.tbq3_quantize(x[:50], s)
+    assert np.array_equal(c3, r3) and np.array_equal(n3.view(np.uint16), m3.view(np.uint16))
+
+
 def test_nearest_centroid_bruteforce_and_ties():
     rng = np.random.default_rng(3)
     u = rng.standard_normal(2000) * 1.5
@@ -403,29 +502,32 @@ def test_dca_reference_reduces_to_attention_and_brute_force():
 
 # ----------------------------------------------------------- layout ------
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("D", [64, 128, 256, 512])
-def test_layout_is_a_bijection_and_roundtrips(D):
-    rec = LY.record_bytes(D)
-    kofs, sofs, nofs = LY.k_code_offsets(D), LY.k_scale_offsets(D), LY.v_norm_offsets(D)
-    vbits = LY.v_code_bits(D)
+def test_layout_is_a_bijection_and_roundtrips(D, bits):
+    rec = LY.record_bytes(D, bits)
+    kofs, sofs, nofs = LY.k_code_offsets(D), LY.k_scale_offsets(D), LY.v_norm_offsets(D, bits)
+    vbits = LY.v_code_bits(D, bits)
     byte_owner = np.zeros(rec, int)
     np.add.at(byte_owner, kofs.ravel(), 1)
     np.add.at(byte_owner, sofs.ravel(), 1)
     np.add.at(byte_owner, sofs.ravel() + 1, 1)
     np.add.at(byte_owner, nofs, 1)
     np.add.at(byte_owner, nofs + 1, 1)
-    vb = np.zeros(6 * D * 8, int)
+    vb = np.zeros(2 * bits * D * 8, int)
     np.add.at(vb, vbits.ravel() - 17 * D * 8, 1)
     assert (vb == 1).all()                                   # every V bit used once
-    assert (byte_owner[:17 * D] == 1).all() and (byte_owner[23 * D:] == 1).all()
+    v_end = 17 * D + 2 * bits * D
+    assert (byte_owner[:17 * D] == 1).all() and (byte_owner[v_end:] == 1).all()
+    assert rec == v_end + 32
     rng = np.random.default_rng(D)
     T = 37
     qs = rng.integers(-127, 128, (T, D)).astype(np.int8)
     d16 = rng.standard_normal((T, D // 32)).astype(np.float16)
-    codes = rng.integers(0, 8, (T, D)).astype(np.uint8)
+    codes = rng.integers(0, 1 << bits, (T, D)).astype(np.uint8)
     n16 = rng.random(T).astype(np.float16)
-    recs = LY.pack_records(qs, d16, codes, n16, 48)
-    back = LY.unpack_records(recs, T, D)
+    recs = LY.pack_records(qs, d16, codes, n16, 48, bits)
+    back = LY.unpack_records(recs, T, D, bits)
     for a, b in zip((qs, d16, codes, n16), back):
         assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
@@ -452,3 +554,20 @@ def test_layout_code_bits_against_page_compression_ratio():
     assert round(ratio, 2) == float(g["ratio"][0])
     pooled = float(g["dense_gb"][0]) / float(g["pooled_gb"][0])
     assert abs(pooled / (int(g["agents"][0]) * ratio) - 1) < 0.02
+
+
+def test_layout_v_bytes_per_value_against_page_tier_table():
+    # One fp16 norm per 128-value vector plus b-bit codes: (b + 16/128) / 8 bytes
+    # per value at head_dim 128, as printed for turbo2 and turbo3.
+    D = 128
+    for mode, bits, bpv in _golden_lines("tier_bpv.txt"):
+        bits = int(bits)
+        v_bytes = (LY.record_bytes(D, bits) - LY.record_bytes(D, bits) + LY.v_code_bits(D, bits).size // 8
+                   + LY.v_norm_offsets(D, bits).size * 2)
+        assert round(v_bytes / (16 * D), 3) == float(bpv), mode
+    # 2-bit hand offset: position 3, dim 70 at D=512 -> lane 5, pair 12,
+    # first bit 4*12 + 2 = 50 -> stream byte 6 (bit 2); lane stream 64 bytes, granule 16.
+    assert LY.v_code_bits(512, 2)[3, 70, 0] == (17 * 512 + 5 * 16 + 6) * 8 + 2
+    # 4-bit: first bit 8*12 + 4 = 100 -> stream byte 12 (bit 4); stream 128 bytes, granule 16.
+    assert LY.v_code_bits(512, 4)[3, 70, 0] == (17 * 512 + 5 * 16 + 12) * 8 + 4
+    assert LY.record_bytes(512, 2) == 16 * 674 and LY.record_bytes(512, 4) == 16 * 802
