@@ -57,7 +57,7 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="gemma4_decode",
                    choices=["gemma4_decode", "long_decode", "fanout_decode", "tiny_decode", "chunked_prefill",
-                            "kv_pack", "verify_decode", "dca_decode"])
+                            "kv_pack", "verify_decode", "dca_decode", "long_decode_tbq2", "long_decode_tbq4"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -74,7 +74,8 @@ def _peaks():
 
 def _decode_source_sha():
     h = hashlib.sha256()
-    for name in ("attn_decode.cu", "decode_common.cuh", "ckv_device.cuh", "ckv_kernels.cuh", "pack_common.cuh"):
+    for name in ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh", "ckv_kernels.cuh",
+                 "pack_common.cuh"):
         with open(os.path.join(ROOT, "compressed_kv_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -169,6 +170,8 @@ class DecodeWork:
         self.D, self.T, self.B, self.Hq, self.Hkv = D, T, B, Hq, Hkv
         self.n_q = w.n_q
         self.dca = w.dca_chunk  # dual chunk attention: three regime queries, one output token
+        self.v_bits = w.v_bits
+        self.dtype = f"f16 mma, f32 accumulate (int8 / {w.v_bits}-bit storage)"
         outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
         signs = inputs.tbq_signs(D)
         self.scale = 1.0 / math.sqrt(D)
@@ -177,10 +180,11 @@ class DecodeWork:
             v = inputs.normal_tensor((B, T, Hkv, D), w.seed, "v", outl, device=str(dev))
             self.q = inputs.normal_tensor((B, 3 if self.dca else self.n_q, Hq, D), w.seed, "q", outl,
                                           device=str(dev))
-            self.cache_bytes = ckv.cache_bytes(D, Hkv, B, T)
+            self.cache_bytes = ckv.cache_bytes(D, Hkv, B, T, w.v_bits)
             self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
             self.n_rot = max(2, math.ceil(4 * self.l2 / self.cache_bytes))
-            self.caches = [ckv.PackedCache(D, Hkv, B, T, signs, device=dev) for _ in range(self.n_rot)]
+            self.caches = [ckv.PackedCache(D, Hkv, B, T, signs, device=dev, v_bits=w.v_bits)
+                           for _ in range(self.n_rot)]
             for c in self.caches:
                 ckv.kv_pack(c, 0, k, v, stream=stream)
             self.k_new, self.v_new = k[:, T - 1:T].clone(), v[:, T - 1:T].clone()
@@ -195,7 +199,7 @@ class DecodeWork:
         self.tokens_per_step = B * self.n_q
         # the decode kernel (packs the new token or runs the batch, merges splits); DCA adds the regime merge
         self.launches_per_step = 2 if self.dca else 1
-        self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D)
+        self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D, w.v_bits)
 
     def step(self, i):
         c = self.caches[i % self.n_rot]
@@ -242,7 +246,7 @@ class DecodeWork:
 
     def describe(self):
         return {"workload": self.w.name, "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
-                "batch": self.B, "cached_tokens": self.T, "n_q": self.n_q,
+                "batch": self.B, "cached_tokens": self.T, "n_q": self.n_q, "v_bits": self.v_bits,
                 "step": (f"attn_decode_dca (chunk {self.dca}: intra, successive and inter regimes + merge)"
                          if self.dca else
                          "attn_decode_verify (a batch of n_q drafted tokens, causal among them)" if self.n_q > 1
@@ -257,7 +261,8 @@ class DecodeWork:
                                            NCU_TRAFFIC["source_sha"] == _decode_source_sha()) else None
         what = ("DCA regimes as three query rows" if self.dca else
                 "verify batch, per-row causal limits" if self.n_q > 1 else "append")
-        return {"bound": "hbm", "kernel": f"attn_decode_kernel<{self.D}> ({what} + split-K decode + in-kernel merge)",
+        return {"bound": "hbm",
+                "kernel": f"attn_decode_kernel<{self.D}, {self.v_bits}> ({what} + split-K decode + in-kernel merge)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_kind": kind, "traffic": traffic, "algorithmic_bytes": self.algo_bytes,
                 "launch_ms": round(kernel_ms, 6)}
@@ -500,7 +505,8 @@ class PackWork:
 
 
 def _make_work(name, dev, stream):
-    if name in ("gemma4_decode", "long_decode", "tiny_decode", "verify_decode", "dca_decode"):
+    if name in ("gemma4_decode", "long_decode", "tiny_decode", "verify_decode", "dca_decode", "long_decode_tbq2",
+                "long_decode_tbq4"):
         return DecodeWork(name, dev, stream)
     if name == "fanout_decode":
         return FanoutWork(dev, stream)
@@ -612,7 +618,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma, f32 accumulate (int8 / 3-bit storage)",
+        "scaling": "weak", "vs_baseline": None, "dtype": getattr(work, "dtype", "f16 mma, f32 accumulate (int8 / 3-bit storage)"),
         "data": "synthetic",
         "config": dict(work.describe(), parallelism=f"replicas x{world}",
                        timing="CUDA graphs, events on the launching stream" if work.graph else

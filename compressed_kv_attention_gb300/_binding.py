@@ -27,7 +27,7 @@ class CkvError(RuntimeError):
 
 class CkvCacheStruct(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
-                ("batch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("v_bits", ctypes.c_int32),
                 ("capacity", ctypes.c_int64), ("data", ctypes.c_void_p),
                 ("v_signs", ctypes.c_void_p)]
 
@@ -41,6 +41,7 @@ SIGNATURES = {
     "ckv_version": (_c_int, []),
     "ckv_last_error": (ctypes.c_char_p, []),
     "ckv_cache_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_i64]),
+    "ckv_cache_bytes_v": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int]),
     "ckv_kv_pack": (_c_int, [_cache_p, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i64, _vp]),
     "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
@@ -100,18 +101,20 @@ def _stream(stream) -> int:
 
 
 class PackedCache:
-    """A packed q8_0-K / TBQ3-V cache in device memory plus its geometry."""
+    """A packed q8_0-K / TBQ-V cache in device memory plus its geometry
+    (``v_bits`` bits per V code: 3 is TBQ3, 2 and 4 the neighbouring tiers)."""
 
     def __init__(self, head_dim: int, n_kv_heads: int, batch: int, capacity: int, signs,
-                 device="cuda", data=None):
+                 device="cuda", data=None, v_bits: int = 3):
         import torch
         self.head_dim, self.n_kv_heads, self.batch, self.capacity = head_dim, n_kv_heads, batch, capacity
-        nbytes = cache_bytes(head_dim, n_kv_heads, batch, capacity)
+        self.v_bits = v_bits
+        nbytes = cache_bytes(head_dim, n_kv_heads, batch, capacity, v_bits)
         if nbytes == 0:
             raise CkvError(-1, "invalid cache geometry")
         self.data = data if data is not None else torch.zeros(nbytes, dtype=torch.uint8, device=device)
         self.signs = torch.as_tensor(signs, dtype=torch.int8).to(device)
-        self.struct = CkvCacheStruct(head_dim, n_kv_heads, batch, 0, capacity, _ptr(self.data),
+        self.struct = CkvCacheStruct(head_dim, n_kv_heads, batch, v_bits, capacity, _ptr(self.data),
                                      _ptr(self.signs))
 
     def ref(self):
@@ -122,8 +125,8 @@ def version() -> int:
     return load().ckv_version()
 
 
-def cache_bytes(head_dim: int, n_kv_heads: int, batch: int, capacity: int) -> int:
-    return int(load().ckv_cache_bytes(head_dim, n_kv_heads, batch, capacity))
+def cache_bytes(head_dim: int, n_kv_heads: int, batch: int, capacity: int, v_bits: int = 3) -> int:
+    return int(load().ckv_cache_bytes_v(head_dim, n_kv_heads, batch, capacity, v_bits))
 
 
 def kv_pack(cache: PackedCache, tok_offset: int, k, v, stream=None):

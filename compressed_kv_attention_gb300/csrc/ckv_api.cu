@@ -56,12 +56,16 @@ int num_sms() {
   return cached[dev];
 }
 
+int cache_v_bits(const ckv_cache* c) { return c->v_bits == 0 ? 3 : c->v_bits; }
+
 ckv_status check_cache(const ckv_cache* c) {
   if (!c) return fail(CKV_ERR_INVALID_ARG, "cache is null");
   if (!supported_dim(c->head_dim))
     return fail(CKV_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256,512}", c->head_dim);
-  if (c->n_kv_heads <= 0 || c->batch <= 0 || c->reserved != 0)
-    return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive, reserved 0");
+  if (c->n_kv_heads <= 0 || c->batch <= 0)
+    return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive");
+  if (c->v_bits != 0 && (c->v_bits < 2 || c->v_bits > 4))
+    return fail(CKV_ERR_INVALID_ARG, "v_bits must be 2, 3 or 4 (or 0 for 3), got %d", c->v_bits);
   if (c->capacity <= 0 || c->capacity % 16)
     return fail(CKV_ERR_INVALID_ARG, "capacity must be a positive multiple of 16");
   if (!c->data || !aligned(c->data, 16)) return fail(CKV_ERR_INVALID_ARG, "cache data null or not 16-byte aligned");
@@ -137,10 +141,16 @@ int32_t ckv_version(void) { return 101; }
 
 const char* ckv_last_error(void) { return g_err; }
 
-size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity) {
-  if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0 || capacity <= 0 || capacity % 16)
+size_t ckv_cache_bytes_v(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity,
+                         int32_t v_bits) {
+  if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0 || capacity <= 0 || capacity % 16 ||
+      v_bits < 2 || v_bits > 4)
     return 0;
-  return static_cast<size_t>(batch) * n_kv_heads * (capacity / 16) * ckv::record_bytes(head_dim);
+  return static_cast<size_t>(batch) * n_kv_heads * (capacity / 16) * ckv::record_bytes(head_dim, v_bits);
+}
+
+size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity) {
+  return ckv_cache_bytes_v(head_dim, n_kv_heads, batch, capacity, 3);
 }
 
 ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok, const void* k_f16,
@@ -166,6 +176,7 @@ ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok
   a.head_dim = cache->head_dim;
   a.n_kv_heads = cache->n_kv_heads;
   a.batch = cache->batch;
+  a.v_bits = cache_v_bits(cache);
   a.tok_offset = tok_offset;
   a.n_tok = n_tok;
   a.k = static_cast<const __half*>(k_f16);
@@ -238,6 +249,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.head_dim = D;
   a.n_kv_heads = Hkv;
   a.batch = B;
+  a.v_bits = compressed ? cache_v_bits(cache) : 0;
   a.seq_len = seq_len;
   a.max_seq_len = max_seq_len;
   a.q = static_cast<const __half*>(q);

@@ -14,21 +14,50 @@ namespace ckv {
 
 constexpr int kTile = 16;  // token positions per tile record
 
-__host__ __device__ constexpr int record_bytes(int D) { return 23 * D + 32; }
+// A record holds 16 positions: K codes [0, 16D), K scales [16D, 17D), V codes
+// at B bits per value [17D, 17D + 2BD), V norms (32 bytes). B = 3 is TBQ3;
+// 2 and 4 are the neighbouring tiers of the same quantiser.
+__host__ __device__ constexpr int record_bytes(int D, int B = 3) { return 17 * D + 2 * B * D + 32; }
 __host__ __device__ constexpr int k_scale_offset(int D) { return 16 * D; }
 __host__ __device__ constexpr int v_code_offset(int D) { return 17 * D; }
-__host__ __device__ constexpr int v_norm_offset(int D) { return 23 * D; }
+__host__ __device__ constexpr int v_norm_offset(int D, int B = 3) { return 17 * D + 2 * B * D; }
 // Bytes of one lane's V-code stream in a record, and the granule in which it is interleaved.
-__host__ __device__ constexpr int v_lane_bytes(int D) { return 3 * D / 16; }
-__host__ __device__ constexpr int v_granule(int D) {
-  return (v_lane_bytes(D) % 16 == 0) ? 16 : (v_lane_bytes(D) % 8 == 0) ? 8 : 4;
+__host__ __device__ constexpr int v_lane_bytes(int D, int B = 3) { return B * D / 16; }
+__host__ __device__ constexpr int v_granule(int D, int B = 3) {
+  return (v_lane_bytes(D, B) % 16 == 0) ? 16 : (v_lane_bytes(D, B) % 8 == 0) ? 8 : 4;
 }
 
-// The centroids enter the tensor cores as fp16 values of c / kCentroidScale
-// and the output is multiplied back by kCentroidScale: with this scale all four
+// The centroids enter the tensor cores as fp16 values of c / scale and the
+// output is multiplied back by the scale. 3 bits: with 1.7475121 all four
 // centroid magnitudes lie within 1.6e-5 (relative) of an fp16 value, where
-// plain fp16 rounding of 0.7560 is off by 1.9e-4.
+// plain fp16 rounding of 0.7560 is off by 1.9e-4. 2 bits: 0.4528 / 1.6384 and
+// 1.5104 / 1.6384 are exact fp16 values (283/1024, 944/1024). 4 bits: with
+// 1.251395 the eight magnitudes lie within 9.3e-5 of fp16 values (plain
+// rounding: 3.1e-4).
 constexpr float kCentroidScale = 1.7475121f;
+__host__ __device__ constexpr float centroid_scale(int B) {
+  return B == 2 ? 1.6384f : B == 4 ? 1.251395f : kCentroidScale;
+}
+
+// Ascending Lloyd-Max centroids of N(0,1) for B-bit codes k (selects on
+// immediates, no memory): 2 bits +/-0.4528, +/-1.5104; 3 bits +/-0.2451,
+// +/-0.7560, +/-1.3439, +/-2.1520; 4 bits +/-0.1284, +/-0.3880, +/-0.6568,
+// +/-0.9423, +/-1.2562, +/-1.6180, +/-2.0690, +/-2.7326.
+template <int B>
+__host__ __device__ __forceinline__ float tbq_centroid(int k) {
+  constexpr int H = 1 << (B - 1);
+  const int m = (k >= H) ? k - H : H - 1 - k;  // magnitude rank
+  float mag;
+  if constexpr (B == 2) {
+    mag = (m == 0) ? 0.4528f : 1.5104f;
+  } else if constexpr (B == 3) {
+    mag = (m == 0) ? 0.2451f : (m == 1) ? 0.7560f : (m == 2) ? 1.3439f : 2.1520f;
+  } else {
+    mag = (m == 0) ? 0.1284f : (m == 1) ? 0.3880f : (m == 2) ? 0.6568f : (m == 3) ? 0.9423f
+        : (m == 4) ? 1.2562f : (m == 5) ? 1.6180f : (m == 6) ? 2.0690f : 2.7326f;
+  }
+  return (k >= H) ? mag : -mag;
+}
 
 // Error codes written to the workspace flag word.
 enum DeviceFlag : int32_t {

@@ -12,6 +12,7 @@ struct PackArgs {
   uint8_t* cache;
   int64_t capacity;
   int head_dim, n_kv_heads, batch;
+  int v_bits;                          // bits per V code: 2, 3 or 4
   int64_t tok_offset, n_tok;
   const __half* k;
   const __half* v;
@@ -37,6 +38,7 @@ struct DecodeArgs {
   const int8_t* signs;       // sign diagonal (compressed decode) or nullptr
   int64_t capacity;
   int head_dim, n_kv_heads, batch;
+  int v_bits;                // bits per V code of the compressed cache: 2, 3 or 4
   const int32_t* seq_len;
   int64_t max_seq_len;
   const __half* q;
@@ -82,7 +84,9 @@ __host__ __device__ inline MergeTree merge_tree(int n_split) {
 }
 
 
-cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);       // dispatches on v_bits
+cudaError_t launch_attn_decode_tbq2(const DecodeArgs& a, cudaStream_t stream);  // v_bits 2
+cudaError_t launch_attn_decode_tbq4(const DecodeArgs& a, cudaStream_t stream);  // v_bits 4
 cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream);
 
 struct LseMergeArgs {
@@ -99,9 +103,6 @@ struct LseMergeArgs {
   float* lse;
 };
 cudaError_t launch_lse_merge(const LseMergeArgs& a, cudaStream_t stream);
-
-// Shared-memory bytes the compressed decode kernel needs for a head dim.
-size_t decode_smem_bytes(int head_dim);
 
 // Record a failure message for ckv_last_error() on this thread; returns `status`.
 int set_last_error(int status, const char* fmt, ...);

@@ -134,15 +134,15 @@ __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int grou
 }
 
 // Inverse rotation of one output row held by a warp (lane: dims 64 e + 2 lane
-// + c, c < 2), then the sign flip and kCentroidScale / D, stored to `orow`:
+// + c, c < 2), then the sign flip and vscale / D, stored to `orow`:
 // the unnormalised Walsh-Hadamard transform pairs the two values of a float2
 // (dim bit 0), lanes (bits 1..5, shuffles) and registers (bits 6..); one
 // 1/sqrt(D) comes from the orthonormal inverse, one from the norm scaling
-// folded into P', and kCentroidScale undoes the centroid table's scale. Without
-// `signs` (dense values) the row is stored as is.
+// folded into P', and vscale (the centroid table's scale) undoes the
+// table's scaling. Without `signs` (dense values) the row is stored as is.
 template <int D>
 __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane, const int8_t* signs,
-                                                   float* orow) {
+                                                   float* orow, float vscale = kCentroidScale) {
   constexpr int E2 = D / 64;
   if (signs) {
 #pragma unroll
@@ -175,8 +175,8 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
     for (int e = 0; e < E2; ++e) {
       const int d = 64 * e + 2 * lane;
       const char2 sg = *reinterpret_cast<const char2*>(signs + d);
-      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (kCentroidScale / D);
-      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (kCentroidScale / D);
+      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (vscale / D);
+      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (vscale / D);
     }
   }
   if (orow) {
@@ -203,7 +203,8 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
 template <int D, int MTW>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
                                                 float* mlbuf, int group, int wh, int warp, int lane,
-                                                const int8_t* signs, float* slot) {
+                                                const int8_t* signs, float* slot,
+                                                float vscale = kCentroidScale) {
   using Sh = DecodeShape<D>;
   const int g = lane >> 2, t = lane & 3;
   // Reduce the row sums over the 8 lanes that share rows (2t, 2t+1).
@@ -257,7 +258,7 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
     }
     v[e] = x;
   }
-  derotate_store_row<D>(v, lane, signs, slot + r * D);
+  derotate_store_row<D>(v, lane, signs, slot + r * D, vscale);
   if (lane == 0) {
     slot[8 * D + r] = mc;
     slot[8 * D + 8 + r] = lc;

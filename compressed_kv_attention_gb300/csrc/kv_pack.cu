@@ -2,16 +2,17 @@
 //
 // K: q8_0 (PolyKV page, "F5 M6 — PolyKV (shared compressed KV pool)", section
 // "What PolyKV is (reference)": K -> int8 q8_0, blocks of 32 with one fp16 scale).
-// V: 3-bit TurboQuant-MSE (same section: FWHT rotation then Lloyd-Max; section
-// "Phase-0 fork recon": the writer does the group transform with warp shuffles
-// and bit-packs the codes). One warp owns one token position (pack_common.cuh).
+// V: B-bit TurboQuant-MSE, B = 3 by default and 2 or 4 for the other tiers
+// (same section: FWHT rotation then Lloyd-Max; section "Phase-0 fork recon":
+// the writer does the group transform with warp shuffles and bit-packs the
+// codes). One warp owns one token position (pack_common.cuh).
 //
 // Two ways to write a position, chosen per tile record (CTA-uniform):
 //  * a record whose 16 positions are all new is assembled in shared memory and
 //    written back with coalesced 16-byte stores (bulk packing, prefill);
 //  * a record that is only partly rewritten (the decode append of one token,
 //    the ragged ends of a range) is updated in place: the position's K codes,
-//    scale and norm are plain stores, and its 3-bit V fields, which share
+//    scale and norm are plain stores, and its B-bit V fields, which share
 //    32-bit words with the other positions of the record, are cleared and set
 //    with word-wide atomic AND / OR on global memory. Positions own disjoint
 //    bits, so concurrent writers of one record cannot disturb each other.
@@ -20,12 +21,12 @@
 
 namespace ckv {
 
-template <int D>
+template <int D, int B>
 __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
-  constexpr int REC = record_bytes(D);
+  constexpr int REC = record_bytes(D, B);
   constexpr int E = D / 32;
   constexpr int LPB = 32 / E;
-  using PC = pack::PositionCodes<D>;
+  using PC = pack::PositionCodes<D, B>;
   __shared__ __align__(16) uint8_t rec[REC];
 
   const int bh = blockIdx.y;
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
   if (full) {
     // Every byte of the record is rewritten: only the V code region, which is
     // OR-ed together from the 16 positions, starts from zero.
-    for (int ofs = v_code_offset(D) + threadIdx.x * 16; ofs < v_norm_offset(D); ofs += blockDim.x * 16)
+    for (int ofs = v_code_offset(D) + threadIdx.x * 16; ofs < v_norm_offset(D, B); ofs += blockDim.x * 16)
       *reinterpret_cast<uint4*>(rec + ofs) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     {
@@ -53,14 +54,15 @@ __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
       const __half* krow = a.k + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
       const __half* vrow = a.v + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
       PC pc;
-      pack::quantise_position<D>(krow, vrow, a.signs, p, lane, pc);
+      pack::quantise_position<D, B>(krow, vrow, a.signs, p, lane, pc);
       pack::store_k_codes<E>(rec, p, lane, pc.q);
       if (lane % LPB == 0)
         *reinterpret_cast<__half*>(rec + k_scale_offset(D) + 2 * (p * (D / 32) + lane / LPB)) = pc.d16;
-      if (lane == 0) *reinterpret_cast<__half*>(rec + v_norm_offset(D) + 2 * p) = pc.n16;
+      if (lane == 0) *reinterpret_cast<__half*>(rec + v_norm_offset(D, B) + 2 * p) = pc.n16;
 #pragma unroll
       for (int w = 0; w < PC::NW; ++w)
-        if (pc.mask[w]) atomicOr(reinterpret_cast<uint32_t*>(rec + pack::v_word_offset<D>(pc.L, pc.w0 + w)), pc.val[w]);
+        if (pc.mask[w])
+          atomicOr(reinterpret_cast<uint32_t*>(rec + pack::v_word_offset<D, B>(pc.L, pc.w0 + w)), pc.val[w]);
     }
     __syncthreads();
     for (int ofs = threadIdx.x * 16; ofs < REC; ofs += blockDim.x * 16)
@@ -74,8 +76,31 @@ __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
   const __half* krow = a.k + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
   const __half* vrow = a.v + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
   PC pc;
-  pack::quantise_position<D>(krow, vrow, a.signs, p, lane, pc);
-  pack::store_position_global<D>(grec, p, lane, pc);
+  pack::quantise_position<D, B>(krow, vrow, a.signs, p, lane, pc);
+  pack::store_position_global<D, B>(grec, p, lane, pc);
+}
+
+template <int D, int B>
+static cudaError_t launch_pack_db(const PackArgs& a, dim3 grid, cudaStream_t stream) {
+  // Same shared-memory carveout as the decode kernels, so that an SM does not
+  // reconfigure its L1 / shared split between a pack and the decode after it.
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(kv_pack_kernel<D, B>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    configured = true;
+  }
+  kv_pack_kernel<D, B><<<grid, 512, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_pack_d(const PackArgs& a, dim3 grid, cudaStream_t stream) {
+  switch (a.v_bits) {
+    case 2: return launch_pack_db<D, 2>(a, grid, stream);
+    case 3: return launch_pack_db<D, 3>(a, grid, stream);
+    case 4: return launch_pack_db<D, 4>(a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream) {
@@ -83,24 +108,13 @@ cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream) {
   const int64_t t0 = a.tok_offset / kTile;
   const int64_t t1 = (a.tok_offset + a.n_tok - 1) / kTile;
   dim3 grid(static_cast<unsigned>(t1 - t0 + 1), static_cast<unsigned>(a.batch * a.n_kv_heads));
-  // Same shared-memory carveout as the decode kernels, so that an SM does not
-  // reconfigure its L1 / shared split between a pack and the decode after it.
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(kv_pack_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(kv_pack_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(kv_pack_kernel<256>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(kv_pack_kernel<512>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    configured = true;
-  }
   switch (a.head_dim) {
-    case 64: kv_pack_kernel<64><<<grid, 512, 0, stream>>>(a); break;
-    case 128: kv_pack_kernel<128><<<grid, 512, 0, stream>>>(a); break;
-    case 256: kv_pack_kernel<256><<<grid, 512, 0, stream>>>(a); break;
-    case 512: kv_pack_kernel<512><<<grid, 512, 0, stream>>>(a); break;
+    case 64: return launch_pack_d<64>(a, grid, stream);
+    case 128: return launch_pack_d<128>(a, grid, stream);
+    case 256: return launch_pack_d<256>(a, grid, stream);
+    case 512: return launch_pack_d<512>(a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace ckv

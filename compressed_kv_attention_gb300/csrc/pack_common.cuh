@@ -3,9 +3,10 @@
 //
 // K: q8_0 (PolyKV page, "F5 M6 — PolyKV (shared compressed KV pool)", section
 // "What PolyKV is (reference)": K -> int8 q8_0, blocks of 32 with one fp16 scale).
-// V: 3-bit TurboQuant-MSE (same section: FWHT rotation then Lloyd-Max; section
-// "Phase-0 fork recon": the writer does the group transform with warp shuffles
-// and bit-packs the codes). Each lane holds D/32 consecutive values; the
+// V: B-bit TurboQuant-MSE, B = 3 the method's TBQ3 (same section: FWHT rotation
+// then Lloyd-Max; section "Phase-0 fork recon": the writer does the group
+// transform with warp shuffles and bit-packs the codes; section "S2 — TurboQuant
+// tier family": the same scheme at other bit widths, B = 2 and 4 here). Each lane holds D/32 consecutive values; the
 // transform runs its first stages in registers and the rest across lanes with
 // shuffles.
 #pragma once
@@ -23,6 +24,27 @@ __device__ __forceinline__ uint32_t tbq3_code(float u) {
     return 4u + (u > t1) + (u > t2) + (u > t3);
   }
   return 3u - (u < -t1) - (u < -t2) - (u < -t3);
+}
+
+// Code of u at B bits: the index of the nearest centroid of the ascending
+// B-bit table (tbq_centroid), comparing against the fp32 midpoints; ties go
+// to the smaller magnitude and u = 0 to the smallest positive centroid.
+template <int B>
+__device__ __forceinline__ uint32_t tbq_code(float u) {
+  if constexpr (B == 3) {
+    return tbq3_code(u);
+  } else if constexpr (B == 2) {
+    constexpr float t1 = 0.9816f;  // (0.4528 + 1.5104) / 2
+    if (u >= 0.0f) return 2u + (u > t1);
+    return 1u - (u < -t1);
+  } else {
+    // (0.1284 + 0.3880) / 2, ..., (2.0690 + 2.7326) / 2
+    constexpr float t1 = 0.2582f, t2 = 0.5224f, t3 = 0.79955f, t4 = 1.09925f, t5 = 1.4371f,
+                    t6 = 1.8435f, t7 = 2.4008f;
+    if (u >= 0.0f)
+      return 8u + (u > t1) + (u > t2) + (u > t3) + (u > t4) + (u > t5) + (u > t6) + (u > t7);
+    return 7u - (u < -t1) - (u < -t2) - (u < -t3) - (u < -t4) - (u < -t5) - (u < -t6) - (u < -t7);
+  }
 }
 
 // Load E consecutive fp16 values as floats (16-byte loads where E allows).
@@ -51,19 +73,19 @@ __device__ __forceinline__ void load_row(const __half* p, float (&x)[E]) {
 }
 
 // Stream word w of lane stream L: its byte offset inside a record.
-template <int D>
+template <int D, int B = 3>
 __device__ __forceinline__ int v_word_offset(int L, int w) {
-  constexpr int GR = v_granule(D);
+  constexpr int GR = v_granule(D, B);
   const int s = 4 * w;
   return v_code_offset(D) + ((s / GR) * 32 + L) * GR + (s % GR);
 }
 
 // Quantised forms of one position, per lane (values [E*lane, E*lane + E)).
-template <int D>
+template <int D, int B = 3>
 struct PositionCodes {
   static constexpr int E = D / 32;
-  // Window words: the compact bits span [0, 12E - 15), shifted by up to 31.
-  static constexpr int NW = (12 * E + 16 + 31) / 32;
+  // Window words: the compact bits span [0, 4BE - 5B), shifted by up to 31.
+  static constexpr int NW = (4 * B * E - 5 * B + 31 + 31) / 32;
   uint8_t q[E];        // q8_0 codes
   __half d16;          // scale of this lane's block
   __half n16;          // fp16 norm (same in every lane)
@@ -91,11 +113,12 @@ __device__ __forceinline__ void load_position(const __half* krow, const __half* 
   for (int e = 0; e < E; ++e) in.sg[e] = signs[lane * E + e];
 }
 
-template <int D>
-__device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int p, int lane, PositionCodes<D>& pc) {
+template <int D, int B = 3>
+__device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int p, int lane,
+                                                PositionCodes<D, B>& pc) {
   constexpr int E = D / 32;            // values per lane
   constexpr int LPB = 32 / E;          // lanes per q8_0 block
-  using PC = PositionCodes<D>;
+  using PC = PositionCodes<D, B>;
   const float (&kx)[E] = in.kx;
   const float (&vx)[E] = in.vx;
 
@@ -118,7 +141,7 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
     pc.q[e] = static_cast<uint8_t>(static_cast<int8_t>(q));
   }
 
-  // ---- V: TBQ3 ----
+  // ---- V: B-bit TBQ ----
   float ss = 0.0f;
   float z[E];
 #pragma unroll
@@ -155,11 +178,11 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
   // Bit positions. The lane's values i = E*lane + e all fall in the lane stream
   // L = 4 (i / G) + (p % 8) / 2 (G = D / 8 = 4 E), at pair field
   // k = 4 (u / 2) + u % 2 + 2 (p / 8) with u = i % G = E m + e (m = lane % 4),
-  // bits [6 k + 3 (p % 2), +3). Relative to the lane's window start 12 E m:
-  // 24 (e / 2) + 6 (e % 2) + 12 (p / 8) + 3 (p % 2).
+  // bits [2B k + B (p % 2), +B). Relative to the lane's window start 4BE m:
+  // 8B (e / 2) + 2B (e % 2) + 4B (p / 8) + B (p % 2).
   const int m = lane & 3;
   pc.L = 4 * (lane >> 2) + ((p & 7) >> 1);
-  const int start = 12 * E * m + 12 * (p >> 3) + 3 * (p & 1);
+  const int start = 4 * B * E * m + 4 * B * (p >> 3) + B * (p & 1);
   pc.w0 = start >> 5;
   const int sh = start & 31;
   // Compact form (shift 0), then one multiword shift by sh.
@@ -168,14 +191,15 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
   for (int w = 0; w < PC::NW; ++w) cv[w] = cm[w] = 0u;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const uint32_t code = (r > 0.0f) ? tbq3_code(z[e] / r) : 4u;
-    const int pos = 24 * (e >> 1) + 6 * (e & 1);  // compile-time
+    constexpr uint32_t kMask = (1u << B) - 1u;
+    const uint32_t code = (r > 0.0f) ? tbq_code<B>(z[e] / r) : (1u << (B - 1));
+    const int pos = 8 * B * (e >> 1) + 2 * B * (e & 1);  // compile-time
     const int wi = pos >> 5, bi = pos & 31;
     cv[wi] |= code << bi;
-    cm[wi] |= 7u << bi;
-    if (bi > 29) {
+    cm[wi] |= kMask << bi;
+    if (bi > 32 - B) {
       cv[wi + 1] |= code >> (32 - bi);
-      cm[wi + 1] |= 7u >> (32 - bi);
+      cm[wi + 1] |= kMask >> (32 - bi);
     }
   }
 #pragma unroll
@@ -186,12 +210,12 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
   }
 }
 
-template <int D>
+template <int D, int B = 3>
 __device__ __forceinline__ void quantise_position(const __half* krow, const __half* vrow, const int8_t* signs,
-                                                  int p, int lane, PositionCodes<D>& pc) {
+                                                  int p, int lane, PositionCodes<D, B>& pc) {
   PositionInput<D> in;
   load_position<D>(krow, vrow, signs, lane, in);
-  quantise_loaded<D>(in, p, lane, pc);
+  quantise_loaded<D, B>(in, p, lane, pc);
 }
 
 // Byte offset inside a record of the 8-byte K-code chunk that holds dims
@@ -233,19 +257,20 @@ __device__ __forceinline__ void store_k_codes(uint8_t* rec, int p, int lane, con
 // stores for its K codes, scale and norm; word-wide atomic AND then OR for its
 // V fields, whose words it shares with the other positions of the record.
 // Positions own disjoint bits, so concurrent writers of one record commute.
-template <int D>
-__device__ __forceinline__ void store_position_global(uint8_t* grec, int p, int lane, const PositionCodes<D>& pc) {
+template <int D, int B = 3>
+__device__ __forceinline__ void store_position_global(uint8_t* grec, int p, int lane,
+                                                      const PositionCodes<D, B>& pc) {
   constexpr int E = D / 32;
   constexpr int LPB = 32 / E;
-  using PC = PositionCodes<D>;
+  using PC = PositionCodes<D, B>;
   store_k_codes<E>(grec, p, lane, pc.q);
   if (lane % LPB == 0)
     *reinterpret_cast<__half*>(grec + k_scale_offset(D) + 2 * (p * (D / 32) + lane / LPB)) = pc.d16;
-  if (lane == 0) *reinterpret_cast<__half*>(grec + v_norm_offset(D) + 2 * p) = pc.n16;
+  if (lane == 0) *reinterpret_cast<__half*>(grec + v_norm_offset(D, B) + 2 * p) = pc.n16;
 #pragma unroll
   for (int w = 0; w < PC::NW; ++w) {
     if (pc.mask[w]) {
-      uint32_t* word = reinterpret_cast<uint32_t*>(grec + v_word_offset<D>(pc.L, pc.w0 + w));
+      uint32_t* word = reinterpret_cast<uint32_t*>(grec + v_word_offset<D, B>(pc.L, pc.w0 + w));
       atomicAnd(word, ~pc.mask[w]);
       atomicOr(word, pc.val[w]);
     }

@@ -107,7 +107,6 @@ class Workload:
     n_q_heads: int
     batch: int
     seq_len: int          # cached tokens per sequence (decode) / already cached (prefill)
-    n_q: int = 1          # query tokens per sequence
     seed: int = 0
     n_outliers: int = 0
     n_agents: int = 0     # shared-prefix fan-out: agents reading one prefix
@@ -116,6 +115,7 @@ class Workload:
     n_q: int = 1          # decode: query tokens per sequence (a verify batch when > 1)
     dca_chunk: int = 0    # decode: dual chunk attention with this chunk (three regime queries)
     q_dtype: str = "float16"
+    v_bits: int = 3       # bits per V code (3: TBQ3; 2 and 4: the neighbouring tiers)
 
     @property
     def group(self) -> int:
@@ -129,8 +129,9 @@ def _one_percent(d: int) -> int:
 # The five workloads: a tiny decode that the oracle finishes in well under a
 # second, the Gemma-4 global-layer decode, the shared-prefix fan-out decode, the
 # long-context decode and the chunked prefill; and a verify batch of 4 drafted
-# tokens over the Gemma-4 global-layer cache (multi-query decode), and dual
-# chunk attention of one token over it with 8192-token chunks.
+# tokens over the Gemma-4 global-layer cache (multi-query decode), dual chunk
+# attention of one token over it with 8192-token chunks, and the long-context
+# decode over caches whose V codes have 2 or 4 bits.
 WORKLOADS = {
     "tiny_decode": Workload("tiny_decode", head_dim=128, n_kv_heads=1, n_q_heads=4, batch=1,
                             seq_len=256, seed=0, n_outliers=2),
@@ -145,13 +146,17 @@ WORKLOADS = {
                               seq_len=32768, seed=5, n_outliers=_one_percent(512), n_q=4),
     "dca_decode": Workload("dca_decode", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=1,
                            seq_len=32768, seed=6, n_outliers=_one_percent(512), dca_chunk=8192),
+    "long_decode_tbq2": Workload("long_decode_tbq2", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=4,
+                                 seq_len=262144, seed=7, n_outliers=_one_percent(512), v_bits=2),
+    "long_decode_tbq4": Workload("long_decode_tbq4", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=4,
+                                 seq_len=262144, seed=8, n_outliers=_one_percent(512), v_bits=4),
     "chunked_prefill": Workload("chunked_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16,
                                 batch=1, seq_len=32768, seed=4, n_outliers=_one_percent(512),
                                 n_new=2048, q_dtype="bfloat16"),
 }
 
 
-def compressed_bytes_per_token(head_dim: int) -> int:
-    """Packed bytes per (token, kv-head): q8_0 K (D int8 + D/32 fp16 scales) and TBQ3 V
-    (3 bits per value + one fp16 norm)."""
-    return head_dim + 2 * (head_dim // 32) + 3 * head_dim // 8 + 2
+def compressed_bytes_per_token(head_dim: int, v_bits: int = 3) -> int:
+    """Packed bytes per (token, kv-head): q8_0 K (D int8 + D/32 fp16 scales) and TBQ V
+    (v_bits bits per value + one fp16 norm)."""
+    return head_dim + 2 * (head_dim // 32) + v_bits * head_dim // 8 + 2

@@ -68,22 +68,30 @@ typedef enum {
 /*
  * The packed cache. One allocation of ckv_cache_bytes() bytes, 16-byte aligned.
  *
+ * V codes have b = v_bits bits (3: TBQ3, the default; 2 and 4: the neighbouring
+ * TurboQuant tiers, PolyKV page section "S2 — TurboQuant tier family": the same
+ * rotation and Lloyd-Max scheme at another bit width). A record is
+ * R = 17*D + 2*b*D + 32 bytes (23*D + 32 at b = 3).
+ *
  * Each (sequence b, kv head h) owns capacity/16 consecutive "tile records";
  * record t holds token positions [16 t, 16 t + 16) and starts at byte
- * ((b * n_kv_heads + h) * (capacity / 16) + t) * (23 * D + 32). Inside a record
+ * ((b * n_kv_heads + h) * (capacity / 16) + t) * R. Inside a record
  * (p = position in the tile, i = dim, D = head_dim):
  *
  *   [0, 16D)       K q8_0 codes (int8). (p, i) is at
  *                  ((i/32)*32 + L)*16 + (p/8)*8 + (i%8), L = 4*(p%8) + (i%32)/8.
  *   [16D, 17D)     K q8_0 scales (fp16), row-major [16][D/32].
- *   [17D, 23D)     V TBQ3 codes, 3 bits each. With G = D/8, L = 4*(i/G) + (p%8)/2
+ *   [17D, 17D+2bD) V codes, b bits each. With G = D/8, L = 4*(i/G) + (p%8)/2
  *                  and pair index k = 4*((i%G)/2) + (i%G)%2 + 2*(p/8), the code of
- *                  (p, i) is bits [6k + 3*(p%2), +3) (LSB first) of lane L's
- *                  3D/16-byte stream; stream byte s of lane L is at
+ *                  (p, i) is bits [2bk + b*(p%2), +b) (LSB first) of lane L's
+ *                  bD/16-byte stream; stream byte s of lane L is at
  *                  17D + ((s/gr)*32 + L)*gr + s%gr, gr = the largest of 16, 8, 4
- *                  that divides 3D/16. Codes index the ascending Lloyd-Max table
- *                  (-2.1520, -1.3439, -0.7560, -0.2451, 0.2451, 0.7560, 1.3439, 2.1520).
- *   [23D, 23D+32)  V norms (fp16), one per position.
+ *                  that divides bD/16. Codes index the ascending Lloyd-Max table
+ *                  of N(0,1) with 2^b levels; b = 3:
+ *                  (-2.1520, -1.3439, -0.7560, -0.2451, 0.2451, 0.7560, 1.3439, 2.1520),
+ *                  b = 2: (-1.5104, -0.4528, 0.4528, 1.5104), b = 4: +/-(0.1284,
+ *                  0.3880, 0.6568, 0.9423, 1.2562, 1.6180, 2.0690, 2.7326).
+ *   [17D+2bD, R)   V norms (fp16), one per position.
  *
  * The layout puts every lane's share of a tile contiguous so that a tile moves
  * into shared memory with one bulk copy and each lane's mma fragments come out
@@ -97,14 +105,18 @@ typedef struct {
   int32_t head_dim;      /* D */
   int32_t n_kv_heads;    /* Hkv */
   int32_t batch;         /* B sequences */
-  int32_t reserved;      /* must be 0 */
+  int32_t v_bits;        /* bits per V code: 2, 3 or 4; 0 means 3 */
   int64_t capacity;      /* token positions per sequence, multiple of 16 */
   void* data;            /* device, ckv_cache_bytes(...) bytes, 16-byte aligned */
   const int8_t* v_signs; /* device, head_dim entries of +1 / -1 */
 } ckv_cache;
 
-/* Bytes of the packed cache: batch * n_kv_heads * capacity/16 * (23*D + 32). 0 if invalid. */
+/* Bytes of the packed cache at 3 bits per V code: batch * n_kv_heads * capacity/16 * (23*D + 32).
+ * 0 if invalid. */
 CKV_API size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity);
+/* The same at v_bits (2, 3 or 4) bits per V code: ... * (17*D + 2*v_bits*D + 32). 0 if invalid. */
+CKV_API size_t ckv_cache_bytes_v(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity,
+                                 int32_t v_bits);
 
 /*
  * kv_pack — quantise n_tok new K and V rows of every sequence into the cache at
@@ -118,7 +130,9 @@ CKV_API size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t bat
  * u = H_D y / ||x|| (H_D the Sylvester Hadamard matrix; this equals the
  * orthonormal transform times sqrt(D)/||x||), each u_i snapped to the nearest
  * centroid (ties at midpoints to the smaller magnitude, u = 0 to +0.2451),
- * n16 = fp16(||x||). A zero vector stores codes 4 and norm 0.
+ * n16 = fp16(||x||). A zero vector stores codes 4 and norm 0. With v_bits 2 or
+ * 4 the same steps use that tier's table (u = 0 and the zero vector take code
+ * 2^(b-1), the smallest positive centroid).
  *
  * k_f16, v_f16: fp16, element (b, j, h, i) of token j of sequence b at
  *   b*batch_stride + j*token_stride + h*D + i (in elements). token_stride >= Hkv*D.
@@ -136,7 +150,7 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
  * Split-K flash-decode: each CTA streams a contiguous range of tile records
  * through shared memory, computes S = Q K_hat^T on tensor cores from the int8
  * codes (scales applied per 32-block), runs the online softmax, and accumulates
- * P V_hat in the rotated basis straight from the 3-bit codes. Each CTA writes
+ * P V_hat in the rotated basis straight from the b-bit codes. Each CTA writes
  * its partial to the workspace; the CTAs that finish last merge the partials
  * of their row group with the exact log-sum-exp combine (a two-level tree,
  * no CTA waiting for another) and apply the inverse transform and sign flip
@@ -291,7 +305,8 @@ CKV_API ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts,
  * q_bf16: device bf16 [batch][n_new][n_q_heads][D]. k_new_f16, v_new_f16: device
  * fp16 [batch][n_new][n_kv_heads][D]. out: float32 [batch][n_new][n_q_heads][D];
  * lse: float32 [batch][n_new][n_q_heads]. head_dim 64, 128, 256 or 512; the
- * query-to-kv head ratio must divide 128 (else CKV_ERR_UNSUPPORTED).
+ * query-to-kv head ratio must divide 128, and the cache must hold 3-bit V
+ * codes (v_bits 0 or 3): else CKV_ERR_UNSUPPORTED.
  */
 CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads);
 CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16,

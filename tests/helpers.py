@@ -17,23 +17,29 @@ from oracle import layout as LY
 ATOL_REL = 2e-3
 #: lse acceptance (natural log units): |lse_gpu - lse_ref| <= LSE_ATOL + LSE_RTOL * |lse_ref|.
 LSE_ATOL, LSE_RTOL = 2e-3, 1e-5
-#: A TBQ3 code may differ from the oracle's only when the oracle's normalised
+#: A TBQ code may differ from the oracle's only when the oracle's normalised
 #: coordinate lies within this distance of a centroid midpoint.
 TIE_WINDOW = 1e-6
 MIDPOINTS = (O.LLOYD_MAX_3BIT[1:] + O.LLOYD_MAX_3BIT[:-1]) / 2
 
+
+def midpoints(bits: int = 3):
+    c = O.tbq_centroids(bits)
+    return (c[1:] + c[:-1]) / 2
+
 CHUNK = 4096  # tokens per oracle chunk
 
 
-def oracle_quantize(k, v, signs):
-    """Oracle q8_0 / TBQ3 of fp16 K, V [..., T, D] (leading dims kept), chunked over T."""
+def oracle_quantize(k, v, signs, bits: int = 3):
+    """Oracle q8_0 / TBQ (``bits`` per V code) of fp16 K, V [..., T, D] (leading
+    dims kept), chunked over T."""
     k = np.asarray(k, np.float16)
     v = np.asarray(v, np.float16)
     T = k.shape[-2]
     qs, d16, codes, n16, u = [], [], [], [], []
     for a in range(0, T, CHUNK):
         q_, d_ = O.q8_0_quantize(k[..., a:a + CHUNK, :])
-        c_, n_, u_ = O.tbq3_quantize(v[..., a:a + CHUNK, :], signs)
+        c_, n_, u_ = O.tbq_quantize(v[..., a:a + CHUNK, :], signs, bits)
         qs.append(q_); d16.append(d_); codes.append(c_); n16.append(n_); u.append(u_.astype(np.float32))
     return (np.concatenate(qs, -2), np.concatenate(d16, -2), np.concatenate(codes, -2),
             np.concatenate(n16, -1), np.concatenate(u, -2))
@@ -87,49 +93,49 @@ def check_attention(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
 
 # ------------------------------------------------------------- packed bytes --
 
-def oracle_records(qs, d16, codes, n16, capacity):
+def oracle_records(qs, d16, codes, n16, capacity, bits: int = 3):
     """Oracle byte layout of a whole cache: qs etc. shaped [B, Hkv, T, ...] -> uint8
     [B, Hkv, capacity/16, record]."""
     B, H = qs.shape[:2]
     D = qs.shape[-1]
-    out = np.zeros((B, H, capacity // 16, LY.record_bytes(D)), np.uint8)
+    out = np.zeros((B, H, capacity // 16, LY.record_bytes(D, bits)), np.uint8)
     for b in range(B):
         for h in range(H):
-            out[b, h] = LY.pack_records(qs[b, h], d16[b, h], codes[b, h], n16[b, h], capacity)
+            out[b, h] = LY.pack_records(qs[b, h], d16[b, h], codes[b, h], n16[b, h], capacity, bits)
     return out
 
 
-def read_fields(records, D, T):
+def read_fields(records, D, T, bits: int = 3):
     """Read the fields of the first T positions out of one stream's records
     (uint8 [n_tiles, record]) using the layout's index maps. Returns
     (qs int8 [T, D], d16 uint16 [T, D/32], codes uint8 [T, D], n16 uint16 [T])."""
-    kofs, sofs, nofs = LY.k_code_offsets(D), LY.k_scale_offsets(D), LY.v_norm_offsets(D)
-    vbits = LY.v_code_bits(D)
+    kofs, sofs, nofs = LY.k_code_offsets(D), LY.k_scale_offsets(D), LY.v_norm_offsets(D, bits)
+    vbits = LY.v_code_bits(D, bits)
     n_tiles = (T + 15) // 16
     rec = records[:n_tiles]
     qs = rec[:, kofs].view(np.int8).reshape(n_tiles * 16, D)[:T]
     sc = (rec[:, sofs].astype(np.uint16) | (rec[:, sofs + 1].astype(np.uint16) << 8)).reshape(-1, D // 32)[:T]
     nm = (rec[:, nofs].astype(np.uint16) | (rec[:, nofs + 1].astype(np.uint16) << 8)).reshape(-1)[:T]
     codes = np.zeros((n_tiles, 16, D), np.uint8)
-    for k in range(3):
-        bits = vbits[..., k]
-        codes |= (((rec[:, bits // 8] >> (bits % 8)) & 1) << k).astype(np.uint8)
+    for k in range(bits):
+        bit = vbits[..., k]
+        codes |= (((rec[:, bit // 8] >> (bit % 8)) & 1) << k).astype(np.uint8)
     return qs, sc, codes.reshape(-1, D)[:T], nm
 
 
-def compare_pack(gpu_records, qs, d16, codes, n16, u, T):
+def compare_pack(gpu_records, qs, d16, codes, n16, u, T, bits: int = 3):
     """Compare one stream's GPU records with the oracle's fields. q8_0 bytes and
     scales must match bit for bit; V codes may differ only at centroid-midpoint
     ties (|u - t| < TIE_WINDOW), fp16 norms by at most one ulp. Returns counts."""
     D = qs.shape[-1]
-    gq, gs, gc, gn = read_fields(gpu_records, D, T)
+    gq, gs, gc, gn = read_fields(gpu_records, D, T, bits)
     assert np.array_equal(gq, qs[:T]), "q8_0 codes differ"
     assert np.array_equal(gs, d16[:T].view(np.uint16)), "q8_0 scales differ"
     mism = gc != codes[:T]
     n_mism = int(mism.sum())
     if n_mism:
         uu = u[:T][mism].astype(np.float64)
-        dist = np.abs(uu[:, None] - MIDPOINTS[None, :]).min(axis=1)
+        dist = np.abs(uu[:, None] - midpoints(bits)[None, :]).min(axis=1)
         assert np.all(dist < TIE_WINDOW), f"{n_mism} code mismatches, worst distance to a midpoint {dist.max():.3e}"
         assert np.all(np.abs(gc[mism].astype(int) - codes[:T][mism].astype(int)) == 1)
     on = n16[:T].view(np.uint16).astype(np.int64)

@@ -45,10 +45,17 @@ def test_version_and_cache_bytes(lib):
     assert lib.ckv_cache_bytes(128, 1, 1, 256) == 256 * 186
     for bad in [(96, 1, 1, 16), (128, 0, 1, 16), (128, 1, 0, 16), (128, 1, 1, 20), (128, 1, 1, 0)]:
         assert lib.ckv_cache_bytes(*bad) == 0
+    # other V bit widths: 17 D + 2 b D + 32 bytes per 16 positions
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 3) == lib.ckv_cache_bytes(512, 2, 1, 32768)
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 2) == 2 * 32768 * 674
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 4) == 2 * 32768 * 802
+    assert lib.ckv_cache_bytes_v(64, 1, 1, 16, 2) == 17 * 64 + 4 * 64 + 32
+    for bits in (0, 1, 5, 8):
+        assert lib.ckv_cache_bytes_v(128, 1, 1, 256, bits) == 0
 
 
-def _fake_cache(D=128, Hkv=1, batch=1, cap=256, data=0x10000, signs=0x20000, reserved=0):
-    return B.CkvCacheStruct(D, Hkv, batch, reserved, cap, data, signs)
+def _fake_cache(D=128, Hkv=1, batch=1, cap=256, data=0x10000, signs=0x20000, v_bits=0):
+    return B.CkvCacheStruct(D, Hkv, batch, v_bits, cap, data, signs)
 
 
 def test_pack_argument_checks(lib):
@@ -57,7 +64,9 @@ def test_pack_argument_checks(lib):
     assert lib.ckv_kv_pack(None, 0, 1, fake, fake, 128, 0, None) == -1
     assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(D=96)), 0, 1, fake, fake, 128, 0, None) == -2
     assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(cap=250)), 0, 1, fake, fake, 128, 0, None) == -1
-    assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(reserved=1)), 0, 1, fake, fake, 128, 0, None) == -1
+    for bits in (1, 5, -1):
+        assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(v_bits=bits)), 0, 1, fake, fake, 128, 0, None) == -1
+    assert b"v_bits" in lib.ckv_last_error()
     assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(data=0x10008)), 0, 1, fake, fake, 128, 0, None) == -1
     assert lib.ckv_kv_pack(ctypes.byref(c), 250, 10, fake, fake, 128, 0, None) == -1   # past capacity
     assert lib.ckv_kv_pack(ctypes.byref(c), -1, 1, fake, fake, 128, 0, None) == -1
@@ -144,6 +153,9 @@ def test_prefill_argument_checks(lib):
     assert call(cache=_fake_cache(D=32)) == -2       # prefill head dims: 64, 128, 256, 512
     assert call(n_cached=4090) == -1                 # past capacity
     assert call(hq=12) == -2                         # 6 heads per kv head does not divide 128
+    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=2)) == -2   # prefill reads 3-bit V only
+    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=4)) == -2
+    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=3)) == -3   # 3 passes (then the workspace)
     assert call(q=fake + 8) == -1
     assert call(out=None) == -1
     assert call(w=None) == -3
