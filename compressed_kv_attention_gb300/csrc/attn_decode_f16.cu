@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
       mma16816(S, k0.x, k1.x, k0.y, k1.y, qf[i][0], qf[i][1]);
       mma16816(S, k0.z, k1.z, k0.w, k1.w, qf[i][2], qf[i][3]);
     }
-    if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, it & 1, lane);
+    if constexpr (C::WT >= 2) exchange_S<C::WT>(S, xbuf, group, wh, it & 1, lane);
     uint32_t pb0, pb1, pl[2] = {0u, 0u};
     softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lo0, lim0, lo1, lim1, a.scale_log2, 1.0f, 1.0f, st, acc, pb0,
                                      pb1, pl);
@@ -116,9 +116,9 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
-                              nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
-  decode_split_tail<D, C::RED_BYTES>(a, split, gid, b, kvh, rg, tid, smem);
+  decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
+                                           nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
+  decode_split_tail<D, C::RED_BYTES, C::THREADS>(a, split, gid, b, kvh, rg, tid, smem);
 }
 
 template <int D>

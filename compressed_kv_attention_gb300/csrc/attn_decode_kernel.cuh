@@ -44,6 +44,10 @@ struct CDec : DecodeShape<D> {
   static constexpr int REC = record_bytes(D, B);
   static constexpr int STAGE = Sh::NP * REC;
   static constexpr int NSTAGE = 4;
+  // Stages issued at once at the start; each later first-round stage waits
+  // until the stage EARLY before it has landed, so that the first data of
+  // every CTA does not queue behind the other CTAs' later stages.
+  static constexpr int EARLY = 2;
   static constexpr int THREADS = (Sh::NCW + 1) * 32;
   static constexpr int VW = B * Sh::MT_W / 4;   // V-code words per lane per warp
   static constexpr int GR = v_granule(D, B);    // stream granule bytes
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
   };
   int pre = 0;
   if (warp == C::NCW && !defer) {
-    pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
+    pre = n_iters_max < C::EARLY ? n_iters_max : C::EARLY;
     if (lane == 0)
       for (int it = 0; it < pre; ++it) issue(it, tile_end_max);
   }
@@ -314,21 +318,34 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
     int64_t tile_end = nt < tile_end_max ? (nt > tile_begin ? nt : tile_begin) : tile_end_max;
     if constexpr (DCA) dca_tiles(a, rg, static_cast<int>(sl), split, tb, tile_end);
     const int n_iters = static_cast<int>((tile_end - tb + C::NP - 1) / C::NP);
-    if (a.n_new > 0) {
-      // New positions inside this CTA's tiles. Stages before the first of them
-      // stream meanwhile; the rest is issued once the rows are in the cache.
-      int64_t n0 = sl - a.n_new, n1 = sl;
-      if (n0 < tile_begin * kTile) n0 = tile_begin * kTile;
-      if (n1 > tile_end * kTile) n1 = tile_end * kTile;
-      if (sl < a.n_new) {
-        if (lane == 0) raise_flag(a.flag, kFlagSeqLenRange);
-        n1 = n0;
+    // Later first-round stages wait for an earlier one to land (EARLY), except
+    // in the CTA that appends: it issues every stage before its new rows at
+    // once and quantises while they stream.
+    bool hold = true;
+    if (defer) {
+      int64_t n0 = 0, n1 = 0;
+      if (a.n_new > 0) {
+        n0 = sl - a.n_new;
+        n1 = sl;
+        if (n0 < tile_begin * kTile) n0 = tile_begin * kTile;
+        if (n1 > tile_end * kTile) n1 = tile_end * kTile;
+        if (sl < a.n_new) {
+          if (lane == 0) raise_flag(a.flag, kFlagSeqLenRange);
+          n1 = n0;
+        }
       }
-      const int it_new = (n0 < n1) ? static_cast<int>((n0 / kTile - tile_begin) / C::NP) : n_iters;
-      pre = it_new < n_iters ? it_new : n_iters;
-      if (pre > C::NSTAGE) pre = C::NSTAGE;
+      if (n0 < n1) {
+        hold = false;
+        const int it_new = static_cast<int>((n0 / kTile - tile_begin) / C::NP);
+        pre = it_new < n_iters ? it_new : n_iters;
+        if (pre > C::NSTAGE) pre = C::NSTAGE;
+      } else {
+        pre = n_iters < C::EARLY ? n_iters : C::EARLY;
+      }
       if (lane == 0)
         for (int it = 0; it < pre; ++it) issue(it, tile_end);
+      // New positions inside this CTA's tiles, written into the cache before
+      // the stages holding them are issued.
       for (int64_t pos = n0; pos < n1; ++pos) {
         const int64_t j = pos - (sl - a.n_new);
         const __half* krow = a.k_new + b * a.new_batch_stride + j * a.new_token_stride + (int64_t)kvh * D;
@@ -355,6 +372,11 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
         const int s = it % C::NSTAGE;
         if (it >= C::NSTAGE && !*(volatile int*)&s_abort) {
           if (!mbar_wait(&empty[s], ((it / C::NSTAGE) - 1) & 1)) {
+            *(volatile int*)&s_abort = 1;
+            raise_flag(a.flag, kFlagWaitTimeout);
+          }
+        } else if (hold && it >= C::EARLY && !*(volatile int*)&s_abort) {
+          if (!mbar_wait(&full[it - C::EARLY], 0)) {
             *(volatile int*)&s_abort = 1;
             raise_flag(a.flag, kFlagWaitTimeout);
           }
@@ -427,7 +449,7 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
     wait_stage(0);
     if (tb + group < tile_end) {
       qk_tile<D>(record(0), wh, lane, qf, qb, S);
-      if constexpr (C::WT == 2) exchange_S(S, xbuf, group, wh, 0, lane);
+      if constexpr (C::WT == 2) exchange_S<2>(S, xbuf, group, wh, 0, lane);
     }
   }
   for (int it = 0; it < n_iters; ++it) {
@@ -473,15 +495,15 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
   // was known but that hold none of this CTA's tiles may still be landing:
   // wait for them first.
   if (!defer) {
-    const int pre = n_iters_max < C::NSTAGE ? n_iters_max : C::NSTAGE;
+    const int pre = n_iters_max < C::EARLY ? n_iters_max : C::EARLY;
     for (int it = n_iters; it < pre; ++it) wait_stage(it);
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  decode_epilogue<D, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
-                              a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
-                              centroid_scale(B));
-  decode_split_tail<D, C::RING>(a, split, gid, b, kvh, rg, tid, smem);
+  decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
+                                           a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
+                                           centroid_scale(B));
+  decode_split_tail<D, C::RING, 256>(a, split, gid, b, kvh, rg, tid, smem);
 }
 
 template <int D, int B, bool DCA>

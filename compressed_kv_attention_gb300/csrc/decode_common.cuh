@@ -6,9 +6,9 @@
 //   O^T[D x 8]  += V_hat^T[D x 16] * P'^T[16 x 8]          (V as A, P' as B)
 // The softmax probabilities leave the S^T accumulator as fp16 pairs and become
 // the B operand of the second product through one movmatrix transpose per
-// 8x8 block. With D = 512 two warps share a tile: each multiplies half of the
-// 32-dim blocks for S and owns half of the output dims for O, and the two
-// partial S are summed through shared memory.
+// 8x8 block. WT warps may share a tile: each multiplies 1/WT of the 32-dim
+// blocks for S and owns 1/WT of the output dims for O, and the partial S are
+// summed through shared memory.
 #pragma once
 
 #include "ckv_device.cuh"
@@ -16,12 +16,13 @@
 
 namespace ckv {
 
-template <int D>
+template <int D, int NCW_ = 8, int WT_ = (D == 512) ? 2 : 1>
 struct DecodeShape {
+  static constexpr int DIM = D;
   static constexpr int NB = D / 32;                 // q8_0 blocks per vector
   static constexpr int MT = D / 16;                 // 16-dim m-tiles of O^T
-  static constexpr int WT = (D == 512) ? 2 : 1;     // warps sharing one tile
-  static constexpr int NCW = 8;                     // consumer warps per CTA
+  static constexpr int WT = WT_;                    // warps sharing one tile
+  static constexpr int NCW = NCW_;                  // consumer warps per CTA
   static constexpr int NP = NCW / WT;               // tiles in flight per CTA
   static constexpr int NB_W = NB / WT;              // blocks per warp (S)
   static constexpr int MT_W = MT / WT;              // m-tiles per warp (O)
@@ -34,7 +35,7 @@ struct DecodeShape {
   static constexpr int RP0 = D + 14 * PS + 2;
   static constexpr int RP = RP0 + ((4 - RP0 % 16) + 16) % 16;
   static constexpr int RED_FLOATS = 8 * RP;
-  static constexpr int XCHG_BYTES = (WT == 2) ? NP * 2 * 2 * 32 * 16 : 0;
+  static constexpr int XCHG_BYTES = (WT >= 2) ? NP * 2 * WT * 32 * 16 : 0;  // [NP][2][WT][32] float4
 };
 
 // Per-row online-softmax state of one lane: rows 2t and 2t+1 of the row group.
@@ -118,19 +119,40 @@ __device__ __forceinline__ void softmax_tile(const float (&S)[4], int64_t tpos, 
   }
 }
 
-// Sum the two warps' partial S of a shared tile (D = 512). Both warps end
-// with the same values (IEEE addition is commutative).
-__device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int group, int wh,
-                                           int parity, int lane) {
-  float4* mine = xbuf + ((group * 2 + parity) * 2 + wh) * 32 + lane;
-  const float4* other = xbuf + ((group * 2 + parity) * 2 + (1 - wh)) * 32 + lane;
-  *mine = make_float4(S[0], S[1], S[2], S[3]);
-  named_bar(2 + group, 64);
-  const float4 o = *other;
-  S[0] += o.x;
-  S[1] += o.y;
-  S[2] += o.z;
-  S[3] += o.w;
+// Partial S of a tile shared by WT warps: each warp stores its float4 into
+// slot [group][parity][wh] (xchg_put), then after the group's named barrier
+// every warp sums the WT slots in the same order (xchg_get), so all of them
+// hold bit-identical S. Parity alternates per tile so that a warp that runs
+// ahead never overwrites a slot a partner is still reading.
+template <int WT>
+__device__ __forceinline__ void xchg_put(const float (&S)[4], float4* xbuf, int group, int wh, int parity,
+                                         int lane) {
+  xbuf[((group * 2 + parity) * WT + wh) * 32 + lane] = make_float4(S[0], S[1], S[2], S[3]);
+}
+
+template <int WT>
+__device__ __forceinline__ void xchg_get(float (&S)[4], const float4* xbuf, int group, int parity, int lane) {
+  named_bar(2 + group, 32 * WT);
+  const float4* p = xbuf + ((group * 2 + parity) * WT) * 32 + lane;
+  float4 v = p[0];
+#pragma unroll
+  for (int w = 1; w < WT; ++w) {
+    const float4 o = p[w * 32];
+    v.x += o.x;
+    v.y += o.y;
+    v.z += o.z;
+    v.w += o.w;
+  }
+  S[0] = v.x;
+  S[1] = v.y;
+  S[2] = v.z;
+  S[3] = v.w;
+}
+
+template <int WT>
+__device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int group, int wh, int parity, int lane) {
+  xchg_put<WT>(S, xbuf, group, wh, parity, lane);
+  xchg_get<WT>(S, xbuf, group, parity, lane);
 }
 
 // Inverse rotation of one output row held by a warp (lane: dims 64 e + 2 lane
@@ -196,16 +218,17 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
 //   slot[8 D + 8 + r] row sum of row r
 // De-rotating each partial here is exact: the transform is linear and the
 // split merge only forms per-row weighted sums of partials.
-// Runs on the 256 consumer threads (named barrier 1). `red` holds
+// Runs on the Sh::NCW consumer warps (named barrier 1). `red` holds
 // NP * RED_FLOATS floats (stage memory is reused), `mlbuf` NP * 16 floats.
-// Each group stores its unscaled accumulators with its own (m, l); the warp
-// that owns a row rescales the groups while summing them.
-template <int D, int MTW>
+// Each group stores its unscaled accumulators with its own (m, l); warp r < 8
+// owns row r and rescales the groups while summing them (other warps are done
+// after the second barrier).
+template <typename Sh, int MTW>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
                                                 float* mlbuf, int group, int wh, int warp, int lane,
                                                 const int8_t* signs, float* slot,
                                                 float vscale = kCentroidScale) {
-  using Sh = DecodeShape<D>;
+  constexpr int D = Sh::DIM;
   const int g = lane >> 2, t = lane & 3;
   // Reduce the row sums over the 8 lanes that share rows (2t, 2t+1).
   st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 4);
@@ -229,6 +252,7 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
     *reinterpret_cast<float2*>(myred + (2 * t + 1) * Sh::RP + pd) = make_float2(acc[i][1], acc[i][3]);
   }
   named_bar(1, Sh::NCW * 32);
+  if (warp >= 8) return;
   // Warp r owns row r: lane holds dims d = 64 e + 2 lane + c (e < D/64, c < 2).
   const int r = warp;
   float mq[Sh::NP], mc = -INFINITY;
@@ -707,12 +731,12 @@ __device__ __forceinline__ void merge_slice(const float* slots, int n_split, int
   }
 }
 
-// Rendezvous merge, after the epilogue has written this CTA's slot (256
-// consumer threads, named barrier 1, `scratch` holds the merge's shared
-// floats). The wait is bounded: on timeout the device flag is raised and the
-// CTA leaves without merging (the counters are then left non-zero: a
+// Rendezvous merge, after the epilogue has written this CTA's slot (NT
+// consumer threads, NT >= 256, named barrier 1, `scratch` holds the merge's
+// shared floats). The wait is bounded: on timeout the device flag is raised
+// and the CTA leaves without merging (the counters are then left non-zero: a
 // workspace whose flag was raised is zeroed before reuse).
-template <int D>
+template <int D, int NT>
 __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int split, int64_t gid, int b, int kvh,
                                                       int rg, int tid, float* scratch) {
   __shared__ int s_ok;
@@ -722,7 +746,7 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
   uint32_t* depart = arrive + 1;
   const uint32_t n = (uint32_t)a.n_split;
   __threadfence();  // this CTA's slot, released to the group
-  named_bar(1, 256);
+  named_bar(1, NT);
   uint32_t dep = 0;
   if (tid == 0) {
     atomicAdd(arrive, 1u);
@@ -744,11 +768,11 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
     s_ok = ok;
   }
   if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
-  named_bar(1, 256);
+  named_bar(1, NT);
   if (!s_ok) return;
   const int u0 = (int)((int64_t)split * 2 * D / a.n_split);
   const int u1 = (int)((int64_t)(split + 1) * 2 * D / a.n_split);
-  merge_slice<D>(a.part + gid * a.n_split * merge_slot_floats(D), a.n_split, u0, u1, tid, 256, scratch, s_out,
+  merge_slice<D>(a.part + gid * a.n_split * merge_slot_floats(D), a.n_split, u0, u1, tid, NT, scratch, s_out,
                  s_lse, split == 0, 1);
   if (tid == 0 && dep + 1 == n) {  // the last CTA to leave: nobody reads the counters any more
     *arrive = 0u;
@@ -757,14 +781,16 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
 }
 
 // The split merge after the epilogue: rendezvous when the host found the grid
-// co-resident, else the tree.
-template <int D, int SCR>
+// co-resident (on all NT consumer threads), else the tree (on threads < 256;
+// the others leave).
+template <int D, int SCR, int NT>
 __device__ __forceinline__ void decode_split_tail(const DecodeArgs& a, int split, int64_t gid, int b, int kvh,
                                                   int rg, int tid, uint8_t* scratch) {
-  if (a.rendezvous)
-    rendezvous_merge_tail<D>(a, split, gid, b, kvh, rg, tid, reinterpret_cast<float*>(scratch));
-  else
+  if (a.rendezvous) {
+    rendezvous_merge_tail<D, NT>(a, split, gid, b, kvh, rg, tid, reinterpret_cast<float*>(scratch));
+  } else if (tid < 256) {
     tree_merge_tail<D, SCR>(a, split, gid, b, kvh, rg, tid, scratch);
+  }
 }
 
 // Blocks of `kernel` that can be resident at once on the current device.
