@@ -275,6 +275,56 @@ def tbq_dequantize(codes, n16, signs, bits: int = 3) -> np.ndarray:
     return np.asarray(signs).astype(np.float64) * fwht_orthonormal(w)
 
 
+#: Dims per rotation group of the block-diagonal variant.
+ROT_GROUP = 128
+
+
+def tbq_quantize_blocked(x, signs1, signs2, bits: int = 3, group: int = ROT_GROUP):
+    """The block-diagonal, two-sign rotation variant of the TBQ quantiser.
+
+    [PolyKV] section "S2 perf-path Level B" (the GGML_OP_TURBO_WHT forward
+    direction: first sign diagonal, the WHT, then 1/sqrt(G) times the second
+    sign diagonal); section "S2 perf-path D=512 fused turbo-vec" (the transform
+    is block-diagonal over 128-dim groups, so D = 512 is four independent
+    groups); section "S2 tier-family overview" (one norm per 128 values).
+    Steps for every group g of G consecutive dims:
+      y_g = s2_g * H_G (s1_g * x_g) / sqrt(G);  r_g = ||x_g||_2;
+      u_g = y_g * sqrt(G) / r_g;  codes = nearest centroid;  n16_g = fp16(r_g).
+    A zero group stores u = 0 (code 2^(bits-1)) and norm 0.
+
+    Returns ``(codes uint8 [..., D], n16 float16 [..., D / G], u float64 [..., D])``.
+    """
+    x = np.asarray(x, dtype=np.float16).astype(np.float64)
+    d = x.shape[-1]
+    if d % group:
+        raise ValueError("head dim must be a multiple of the rotation group")
+    s1 = np.asarray(signs1).astype(np.float64)
+    s2 = np.asarray(signs2).astype(np.float64)
+    xg = x.reshape(x.shape[:-1] + (d // group, group))
+    yg = s2.reshape(d // group, group) * fwht_orthonormal(s1.reshape(d // group, group) * xg)
+    r = np.sqrt(np.sum(xg * xg, axis=-1))
+    safe_r = np.where(r == 0.0, 1.0, r)
+    u = np.where(r[..., None] == 0.0, 0.0, yg * np.sqrt(group) / safe_r[..., None])
+    u = u.reshape(x.shape)
+    return nearest_centroid_bits(u, bits), to_fp16(r), u
+
+
+def tbq_dequantize_blocked(codes, n16, signs1, signs2, bits: int = 3, group: int = ROT_GROUP) -> np.ndarray:
+    """Dense float64 values of the block-diagonal variant. [PolyKV] section "S2
+    perf-path Level A" gives the inverse order per 128-dim group: the second
+    sign diagonal, the butterfly, then 1/sqrt(G) and the first diagonal:
+      V_hat_g = s1_g * H_G (s2_g * (n16_g / sqrt(G)) * c[code_g]) / sqrt(G)."""
+    codes = np.asarray(codes)
+    d = codes.shape[-1]
+    ng = d // group
+    n = np.asarray(n16, dtype=np.float16).astype(np.float64)
+    c = tbq_centroids(bits)[codes].reshape(codes.shape[:-1] + (ng, group))
+    w = (n / np.sqrt(group))[..., None] * c
+    s1 = np.asarray(signs1).astype(np.float64).reshape(ng, group)
+    s2 = np.asarray(signs2).astype(np.float64).reshape(ng, group)
+    return (s1 * fwht_orthonormal(s2 * w)).reshape(codes.shape)
+
+
 # ---------------------------------------------------------------------------
 # Attention and the (output, lse) merge
 # ---------------------------------------------------------------------------

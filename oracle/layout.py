@@ -23,6 +23,9 @@ at b = 3):
                 Stream byte s of lane L is stored at 17D + ((s // gr) * 32 + L) * gr + s % gr,
                 gr = 16, 8 or 4: the largest of those dividing b D/16.
   [17D + 2bD, +32)  V norms, fp16, one per position: p at 17D + 2bD + 2 p.
+                With the block-diagonal rotation (one norm per 128-dim group, G' =
+                D / 128 groups) the norm region is 32 G' bytes, group-major: norm
+                (p, j) at 17D + 2bD + 2 (16 j + p).
 """
 from __future__ import annotations
 
@@ -31,8 +34,10 @@ import numpy as np
 TILE = 16
 
 
-def record_bytes(D: int, bits: int = 3) -> int:
-    return 17 * D + 2 * bits * D + 32
+def record_bytes(D: int, bits: int = 3, groups: int = 1) -> int:
+    """Bytes of one 16-position record: ``groups`` fp16 V norms per position (1
+    for the full transform, D / 128 for the block-diagonal variant)."""
+    return 17 * D + 2 * bits * D + 32 * groups
 
 
 def _granule(D: int, bits: int = 3) -> int:
@@ -74,28 +79,34 @@ def v_code_bits(D: int, bits: int = 3) -> np.ndarray:
     return byte * 8 + sbit % 8
 
 
-def v_norm_offsets(D: int, bits: int = 3) -> np.ndarray:
-    return 17 * D + 2 * bits * D + 2 * np.arange(TILE)
+def v_norm_offsets(D: int, bits: int = 3, groups: int = 1) -> np.ndarray:
+    """Byte offset of the norm of position p (and group j): group-major,
+    17 D + 2 b D + 2 (16 j + p). Shape [16] for one group, else [16, groups]."""
+    p = np.arange(TILE)
+    if groups == 1:
+        return 17 * D + 2 * bits * D + 2 * p
+    j = np.arange(groups)
+    return 17 * D + 2 * bits * D + 2 * (TILE * j[None, :] + p[:, None])
 
 
-def pack_records(qs, d16, codes, n16, capacity: int, bits: int = 3) -> np.ndarray:
+def pack_records(qs, d16, codes, n16, capacity: int, bits: int = 3, groups: int = 1) -> np.ndarray:
     """Lay out one (sequence, kv-head) stream of T tokens as capacity/16 records.
 
     ``qs int8 [T, D]``, ``d16 fp16 [T, D/32]``, ``codes uint8 [T, D]`` (0..2^bits - 1),
-    ``n16 fp16 [T]``. Positions >= T are left zero. Returns uint8
-    ``[capacity/16, record_bytes(D, bits)]``.
+    ``n16 fp16 [T]`` (``[T, groups]`` for several norm groups). Positions >= T
+    are left zero. Returns uint8 ``[capacity/16, record_bytes(D, bits, groups)]``.
     """
     qs = np.asarray(qs, dtype=np.int8)
     T, D = qs.shape
     if capacity % TILE or T > capacity:
         raise ValueError("capacity must be a multiple of 16 and hold every token")
     n_tiles = capacity // TILE
-    out = np.zeros((n_tiles, record_bytes(D, bits)), dtype=np.uint8)
+    out = np.zeros((n_tiles, record_bytes(D, bits, groups)), dtype=np.uint8)
     kofs, sofs = k_code_offsets(D), k_scale_offsets(D)
-    vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits)
+    vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits, groups).reshape(TILE, groups)
     qs_u8 = qs.view(np.uint8)
     d16_u8 = np.asarray(d16, dtype=np.float16).view(np.uint8).reshape(T, D // 32, 2)
-    n16_u8 = np.asarray(n16, dtype=np.float16).view(np.uint8).reshape(T, 2)
+    n16_u8 = np.asarray(n16, dtype=np.float16).view(np.uint8).reshape(T, groups, 2)
     codes = np.asarray(codes, dtype=np.uint8)
     for t in range(T):
         tile, p = divmod(t, TILE)
@@ -103,8 +114,8 @@ def pack_records(qs, d16, codes, n16, capacity: int, bits: int = 3) -> np.ndarra
         rec[kofs[p]] = qs_u8[t]
         rec[sofs[p]] = d16_u8[t, :, 0]
         rec[sofs[p] + 1] = d16_u8[t, :, 1]
-        rec[nofs[p]] = n16_u8[t, 0]
-        rec[nofs[p] + 1] = n16_u8[t, 1]
+        rec[nofs[p]] = n16_u8[t, :, 0]
+        rec[nofs[p] + 1] = n16_u8[t, :, 1]
         for k in range(bits):
             bit = vbits[p, :, k]
             val = (codes[t] >> k) & 1
@@ -112,24 +123,24 @@ def pack_records(qs, d16, codes, n16, capacity: int, bits: int = 3) -> np.ndarra
     return out
 
 
-def unpack_records(records, T: int, D: int, bits: int = 3):
+def unpack_records(records, T: int, D: int, bits: int = 3, groups: int = 1):
     """Inverse of :func:`pack_records` for the first T positions."""
     records = np.asarray(records, dtype=np.uint8)
     kofs, sofs = k_code_offsets(D), k_scale_offsets(D)
-    vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits)
+    vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits, groups).reshape(TILE, groups)
     qs = np.zeros((T, D), dtype=np.int8)
     d16 = np.zeros((T, D // 32), dtype=np.float16)
     codes = np.zeros((T, D), dtype=np.uint8)
-    n16 = np.zeros(T, dtype=np.float16)
+    n16 = np.zeros((T, groups), dtype=np.float16)
     for t in range(T):
         tile, p = divmod(t, TILE)
         rec = records[tile]
         qs[t] = rec[kofs[p]].view(np.int8)
         d16[t] = (rec[sofs[p]].astype(np.uint16) | (rec[sofs[p] + 1].astype(np.uint16) << 8)).view(np.float16)
-        n16[t] = np.array([rec[nofs[p]] | (rec[nofs[p] + 1].astype(np.uint16) << 8)], dtype=np.uint16).view(np.float16)[0]
+        n16[t] = (rec[nofs[p]].astype(np.uint16) | (rec[nofs[p] + 1].astype(np.uint16) << 8)).view(np.float16)
         c = np.zeros(D, dtype=np.uint8)
         for k in range(bits):
             bit = vbits[p, :, k]
             c |= (((rec[bit // 8] >> (bit % 8)) & 1) << k).astype(np.uint8)
         codes[t] = c
-    return qs, d16, codes, n16
+    return qs, d16, codes, (n16[:, 0] if groups == 1 else n16)

@@ -571,3 +571,128 @@ def test_layout_v_bytes_per_value_against_page_tier_table():
     # 4-bit: first bit 8*12 + 4 = 100 -> stream byte 12 (bit 4); stream 128 bytes, granule 16.
     assert LY.v_code_bits(512, 4)[3, 70, 0] == (17 * 512 + 5 * 16 + 12) * 8 + 4
     assert LY.record_bytes(512, 2) == 16 * 674 and LY.record_bytes(512, 4) == 16 * 802
+
+
+# ------------------------------------- block-diagonal two-sign rotation ----
+
+def _rot_matrix_blocked(d, s1, s2, group=128):
+    """Forward rotation of the blocked variant as a matrix, column by column."""
+    cols = []
+    for k in range(d):
+        e = np.zeros(d)
+        e[k] = 1.0
+        x = e
+        xg = x.reshape(d // group, group)
+        y = s2.reshape(d // group, group) * O.fwht_orthonormal(s1.reshape(d // group, group) * xg)
+        cols.append(y.reshape(d))
+    return np.stack(cols, axis=1)
+
+
+def test_blocked_rotation_is_orthonormal_and_block_diagonal():
+    d = 512
+    s1, s2 = inputs.tbq_signs(d), inputs.tbq_signs(d, seed=43)
+    R = _rot_matrix_blocked(d, s1.astype(np.float64), s2.astype(np.float64))
+    assert np.allclose(R @ R.T, np.eye(d), atol=1e-12)
+    for a in range(4):                       # nothing couples two 128-dim groups
+        for b in range(4):
+            if a != b:
+                assert np.all(R[128 * a:128 * a + 128, 128 * b:128 * b + 128] == 0.0)
+    # Each block is s2 H s1 / sqrt(128) with the Sylvester H (closed form).
+    blk = R[:128, :128]
+    i = np.arange(128)[:, None]
+    j = np.arange(128)[None, :]
+    H = np.array([[(-1) ** bin(int(a) & int(b)).count("1") for b in range(128)] for a in range(128)], float)
+    assert np.allclose(blk, s2[:128, None] * H * s1[None, :128] / math.sqrt(128), atol=1e-14)
+    del i, j
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_blocked_reduces_to_full_transform_at_one_group(bits):
+    # D = 128 and s2 = +1: one group, and the variant is the full transform.
+    d = 128
+    rng = np.random.default_rng(31 + bits)
+    x = rng.standard_normal((200, d)).astype(np.float16)
+    s1 = inputs.tbq_signs(d)
+    c_b, n_b, u_b = O.tbq_quantize_blocked(x, s1, np.ones(d, np.int8), bits)
+    c_f, n_f, u_f = O.tbq_quantize(x, s1, bits)
+    assert np.array_equal(c_b, c_f) and np.array_equal(n_b[:, 0].view(np.uint16), n_f.view(np.uint16))
+    assert np.allclose(u_b, u_f, atol=1e-12)
+    assert np.allclose(O.tbq_dequantize_blocked(c_b, n_b, s1, np.ones(d, np.int8), bits),
+                       O.tbq_dequantize(c_f, n_f, s1, bits), atol=1e-12)
+
+
+def test_blocked_groups_are_independent_quantisers():
+    d = 512
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((50, d)).astype(np.float16)
+    x[3, 128:256] = 0.0                      # a zero group: its own norm 0, codes 4
+    s1, s2 = inputs.tbq_signs(d), inputs.tbq_signs(d, seed=43)
+    codes, n16, _ = O.tbq_quantize_blocked(x, s1, s2, 3)
+    assert n16.shape == (50, 4) and n16[3, 1] == 0 and np.all(codes[3, 128:256] == 4)
+    for g in range(4):
+        sl = slice(128 * g, 128 * g + 128)
+        cg, ng, _ = O.tbq_quantize_blocked(x[:, sl], s1[sl], s2[sl], 3)
+        assert np.array_equal(cg, codes[:, sl]) and np.array_equal(ng[:, 0], n16[:, g])
+    # the norm of each group is that group's own Euclidean norm
+    xf = x.astype(np.float64).reshape(50, 4, 128)
+    assert np.allclose(n16.astype(np.float64), np.linalg.norm(xf, axis=-1), rtol=1e-3)
+
+
+def test_blocked_inverse_order_recovers_the_input_exactly():
+    # Dequantising the unquantised coordinates u (instead of centroids) must give
+    # back x: the inverse order s2 -> butterfly -> 1/sqrt(G) s1 undoes the forward
+    # s1 -> butterfly -> 1/sqrt(G) s2.
+    d = 256
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((20, d)).astype(np.float16).astype(np.float64)
+    s1, s2 = inputs.tbq_signs(d).astype(np.float64), inputs.tbq_signs(d, seed=43).astype(np.float64)
+    _, n16, u = O.tbq_quantize_blocked(x, s1, s2, 3)
+    r = np.linalg.norm(x.reshape(20, 2, 128), axis=-1)
+    ug = u.reshape(20, 2, 128)
+    w = (r / math.sqrt(128))[..., None] * ug
+    back = (s1.reshape(2, 128) * O.fwht_orthonormal(s2.reshape(2, 128) * w)).reshape(20, d)
+    assert np.allclose(back, x, atol=1e-12)
+    # Applying the signs in the other order (a plausible slip) does not.
+    wrong = (s2.reshape(2, 128) * O.fwht_orthonormal(s1.reshape(2, 128) * w)).reshape(20, d)
+    assert not np.allclose(wrong, x, atol=1e-3)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_blocked_roundtrip_cosine_tracks_distortion(bits):
+    rng = np.random.default_rng(40 + bits)
+    d = 512
+    x = rng.standard_normal((1200, d)).astype(np.float16)
+    s1, s2 = inputs.tbq_signs(d), inputs.tbq_signs(d, seed=43)
+    codes, n16, _ = O.tbq_quantize_blocked(x, s1, s2, bits)
+    xh = O.tbq_dequantize_blocked(codes, n16, s1, s2, bits)
+    xf = x.astype(np.float64)
+    cos = np.sum(xf * xh, 1) / (np.linalg.norm(xf, axis=1) * np.linalg.norm(xh, axis=1))
+    # Within 128-dim groups the normalised coordinates lie on a sphere of radius
+    # sqrt(128): slightly lighter-tailed than N(0,1), so the cosine may sit up to
+    # ~1e-3 above the large-dimension value sqrt(1 - D_b), never far below it.
+    gap = cos.mean() - math.sqrt(1 - _mse(O.tbq_centroids(bits)))
+    assert -4 * cos.std() / math.sqrt(len(cos)) - 2e-4 < gap < 2.5e-3
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_blocked_layout_roundtrips_and_matches_page_bytes_per_value(D, bits):
+    g = D // 128
+    rec = LY.record_bytes(D, bits, g)
+    nofs = LY.v_norm_offsets(D, bits, g).reshape(16, g)
+    assert nofs.min() == 17 * D + 2 * bits * D and nofs.max() + 2 == rec
+    assert len(np.unique(nofs)) == 16 * g
+    rng = np.random.default_rng(D + bits)
+    T = 21
+    qs = rng.integers(-127, 128, (T, D)).astype(np.int8)
+    d16 = rng.standard_normal((T, D // 32)).astype(np.float16)
+    codes = rng.integers(0, 1 << bits, (T, D)).astype(np.uint8)
+    n16 = rng.random((T, g)).astype(np.float16)
+    back = LY.unpack_records(LY.pack_records(qs, d16, codes, n16, 32, bits, g), T, D, bits, g)
+    for a, b in zip((qs, d16, codes, n16), back):
+        assert np.array_equal(np.asarray(a).view(np.uint8).ravel(), np.asarray(b).view(np.uint8).ravel())
+    # one fp16 norm per 128 values at every head dim: (b + 16/128) / 8 bytes per value
+    v_bytes = LY.v_code_bits(D, bits).size // 8 + 2 * nofs.size
+    page = {int(r[1]): float(r[2]) for r in _golden_lines("tier_bpv.txt")}
+    if bits in page:
+        assert round(v_bytes / (16 * D), 3) == page[bits]
