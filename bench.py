@@ -57,7 +57,8 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="gemma4_decode",
                    choices=["gemma4_decode", "long_decode", "fanout_decode", "tiny_decode", "chunked_prefill",
-                            "kv_pack", "verify_decode", "dca_decode", "long_decode_tbq2", "long_decode_tbq4"])
+                            "kv_pack", "verify_decode", "dca_decode", "long_decode_tbq2", "long_decode_tbq4",
+                            "long_decode_rot"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -172,6 +173,7 @@ class DecodeWork:
         self.dca = w.dca_chunk  # dual chunk attention: three regime queries, one output token
         self.v_bits = w.v_bits
         self.dtype = f"f16 mma, f32 accumulate (int8 / {w.v_bits}-bit storage)"
+        self.rot = w.rot_group
         outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
         signs = inputs.tbq_signs(D)
         self.scale = 1.0 / math.sqrt(D)
@@ -180,10 +182,11 @@ class DecodeWork:
             v = inputs.normal_tensor((B, T, Hkv, D), w.seed, "v", outl, device=str(dev))
             self.q = inputs.normal_tensor((B, 3 if self.dca else self.n_q, Hq, D), w.seed, "q", outl,
                                           device=str(dev))
-            self.cache_bytes = ckv.cache_bytes(D, Hkv, B, T, w.v_bits)
+            self.cache_bytes = ckv.cache_bytes(D, Hkv, B, T, w.v_bits, w.rot_group)
+            signs2 = inputs.tbq_signs(D, seed=43) if w.rot_group else None
             self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
             self.n_rot = max(2, math.ceil(4 * self.l2 / self.cache_bytes))
-            self.caches = [ckv.PackedCache(D, Hkv, B, T, signs, device=dev, v_bits=w.v_bits)
+            self.caches = [ckv.PackedCache(D, Hkv, B, T, signs, device=dev, v_bits=w.v_bits, signs2=signs2)
                            for _ in range(self.n_rot)]
             for c in self.caches:
                 ckv.kv_pack(c, 0, k, v, stream=stream)
@@ -199,7 +202,7 @@ class DecodeWork:
         self.tokens_per_step = B * self.n_q
         # the decode kernel (packs the new token or runs the batch, merges splits); DCA adds the regime merge
         self.launches_per_step = 2 if self.dca else 1
-        self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D, w.v_bits)
+        self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D, w.v_bits, w.rot_group)
 
     def step(self, i):
         c = self.caches[i % self.n_rot]
@@ -247,6 +250,7 @@ class DecodeWork:
     def describe(self):
         return {"workload": self.w.name, "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
                 "batch": self.B, "cached_tokens": self.T, "n_q": self.n_q, "v_bits": self.v_bits,
+                "rotation": "128-dim groups, two sign diagonals" if self.rot else "full D-point, one sign diagonal",
                 "step": (f"attn_decode_dca (chunk {self.dca}: intra, successive and inter regimes + merge)"
                          if self.dca else
                          "attn_decode_verify (a batch of n_q drafted tokens, causal among them)" if self.n_q > 1
@@ -506,7 +510,7 @@ class PackWork:
 
 def _make_work(name, dev, stream):
     if name in ("gemma4_decode", "long_decode", "tiny_decode", "verify_decode", "dca_decode", "long_decode_tbq2",
-                "long_decode_tbq4"):
+                "long_decode_tbq4", "long_decode_rot"):
         return DecodeWork(name, dev, stream)
     if name == "fanout_decode":
         return FanoutWork(dev, stream)

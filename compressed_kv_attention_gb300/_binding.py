@@ -29,7 +29,7 @@ class CkvCacheStruct(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("v_bits", ctypes.c_int32),
                 ("capacity", ctypes.c_int64), ("data", ctypes.c_void_p),
-                ("v_signs", ctypes.c_void_p)]
+                ("v_signs", ctypes.c_void_p), ("v_signs2", ctypes.c_void_p)]
 
 
 _lib = None
@@ -41,7 +41,7 @@ SIGNATURES = {
     "ckv_version": (_c_int, []),
     "ckv_last_error": (ctypes.c_char_p, []),
     "ckv_cache_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_i64]),
-    "ckv_cache_bytes_v": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int]),
+    "ckv_cache_bytes_v": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int]),
     "ckv_kv_pack": (_c_int, [_cache_p, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i64, _vp]),
     "ckv_attn_decode_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp, _vp,
@@ -102,20 +102,24 @@ def _stream(stream) -> int:
 
 class PackedCache:
     """A packed q8_0-K / TBQ-V cache in device memory plus its geometry
-    (``v_bits`` bits per V code: 3 is TBQ3, 2 and 4 the neighbouring tiers)."""
+    (``v_bits`` bits per V code: 3 is TBQ3, 2 and 4 the neighbouring tiers;
+    ``signs2`` given: the block-diagonal rotation over 128-dim groups with
+    ``signs`` before and ``signs2`` after the transform)."""
 
     def __init__(self, head_dim: int, n_kv_heads: int, batch: int, capacity: int, signs,
-                 device="cuda", data=None, v_bits: int = 3):
+                 device="cuda", data=None, v_bits: int = 3, signs2=None):
         import torch
         self.head_dim, self.n_kv_heads, self.batch, self.capacity = head_dim, n_kv_heads, batch, capacity
         self.v_bits = v_bits
-        nbytes = cache_bytes(head_dim, n_kv_heads, batch, capacity, v_bits)
+        self.rot_group = 128 if signs2 is not None else 0
+        nbytes = cache_bytes(head_dim, n_kv_heads, batch, capacity, v_bits, self.rot_group)
         if nbytes == 0:
             raise CkvError(-1, "invalid cache geometry")
         self.data = data if data is not None else torch.zeros(nbytes, dtype=torch.uint8, device=device)
         self.signs = torch.as_tensor(signs, dtype=torch.int8).to(device)
+        self.signs2 = None if signs2 is None else torch.as_tensor(signs2, dtype=torch.int8).to(device)
         self.struct = CkvCacheStruct(head_dim, n_kv_heads, batch, v_bits, capacity, _ptr(self.data),
-                                     _ptr(self.signs))
+                                     _ptr(self.signs), _ptr(self.signs2))
 
     def ref(self):
         return ctypes.byref(self.struct)
@@ -125,8 +129,9 @@ def version() -> int:
     return load().ckv_version()
 
 
-def cache_bytes(head_dim: int, n_kv_heads: int, batch: int, capacity: int, v_bits: int = 3) -> int:
-    return int(load().ckv_cache_bytes_v(head_dim, n_kv_heads, batch, capacity, v_bits))
+def cache_bytes(head_dim: int, n_kv_heads: int, batch: int, capacity: int, v_bits: int = 3,
+                rot_group: int = 0) -> int:
+    return int(load().ckv_cache_bytes_v(head_dim, n_kv_heads, batch, capacity, v_bits, rot_group))
 
 
 def kv_pack(cache: PackedCache, tok_offset: int, k, v, stream=None):

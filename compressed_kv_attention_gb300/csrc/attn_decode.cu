@@ -6,6 +6,14 @@
 namespace ckv {
 
 cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.rot) {
+    switch (a.v_bits) {
+      case 2: return launch_attn_decode_rot2(a, stream);
+      case 3: return launch_attn_decode_rot3(a, stream);
+      case 4: return launch_attn_decode_rot4(a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.v_bits) {
     case 2: return launch_attn_decode_tbq2(a, stream);
     case 3: return launch_decode_bits<3>(a, stream);

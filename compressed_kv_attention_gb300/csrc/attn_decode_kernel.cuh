@@ -38,10 +38,15 @@ namespace ckv {
 
 namespace {
 
-template <int D, int B>
+// ROT = 1: the block-diagonal rotation (128-dim groups, two sign diagonals,
+// one norm per group). The group norms then scale V's fp16 pairs on the
+// A side (a lane's dims all lie in one group), P' carries no norm and is split
+// into hi + lo up to head dim 256.
+template <int D, int B, int ROT = 0>
 struct CDec : DecodeShape<D> {
   using Sh = DecodeShape<D>;
-  static constexpr int REC = record_bytes(D, B);
+  static constexpr int NGRP = ROT ? D / kRotGroup : 1;  // V norms per position
+  static constexpr int REC = record_bytes(D, B, NGRP);
   static constexpr int STAGE = Sh::NP * REC;
   static constexpr int NSTAGE = 4;
   // Stages issued at once at the start; each later first-round stage waits
@@ -53,7 +58,7 @@ struct CDec : DecodeShape<D> {
   static constexpr int GR = v_granule(D, B);    // stream granule bytes
   static constexpr int NG = VW * 4 / GR;        // granules per lane per warp
   static constexpr int LUT = (B == 3) ? 64 : 16;  // table entries (each replicated per lane)
-  static constexpr bool PSPLIT = D <= 128;      // P' as an fp16 hi + lo pair
+  static constexpr bool PSPLIT = ROT ? D <= 256 : D <= 128;  // P' as an fp16 hi + lo pair
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
   static constexpr int RING = (NSTAGE * STAGE > RED_BYTES) ? NSTAGE * STAGE : RED_BYTES;
   static constexpr int OFF_XCHG = (RING + 127) / 128 * 128;
@@ -173,11 +178,13 @@ __device__ __forceinline__ void q_block_bias(const uint32_t (&qf)[NBW][4], int l
 // so the address is one AND-OR of the shifted field with the lane offset.
 // Pair field k (2B bits, codes of two adjacent positions, same dim) feeds
 // A-fragment register k % 4 of m-tile k / 4.
-template <int D, int B>
+// ROT: nA / nB are the lane's group norms of positions (2t, 2t + 1) and
+// (2t + 8, 2t + 9) as fp16 pairs, multiplied into the A registers.
+template <int D, int B, int ROT>
 __device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_t lane4, int wh, int lane,
                                         uint32_t pb0, uint32_t pb1, const uint32_t (&pl)[2],
-                                        float (&acc)[CDec<D, B>::MT_W][4]) {
-  using C = CDec<D, B>;
+                                        float (&acc)[CDec<D, B, ROT>::MT_W][4], uint32_t nA, uint32_t nB) {
+  using C = CDec<D, B, ROT>;
   uint32_t vw[C::VW];
 #pragma unroll
   for (int c = 0; c < C::NG; ++c)
@@ -198,6 +205,12 @@ __device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_
         av[j] = __byte_perm(lo, hi, 0x5410);
       }
     }
+    if constexpr (ROT) {
+      av[0] = hmul2_u32(av[0], nA);
+      av[1] = hmul2_u32(av[1], nA);
+      av[2] = hmul2_u32(av[2], nB);
+      av[3] = hmul2_u32(av[3], nB);
+    }
     mma16816(acc[i], av[0], av[1], av[2], av[3], pb0, pb1);
     if constexpr (C::PSPLIT) mma16816(acc[i], av[0], av[1], av[2], av[3], pl[0], pl[1]);
   }
@@ -205,9 +218,9 @@ __device__ __forceinline__ void pv_tile(uint32_t rb, const uint8_t* lut, uint32_
 
 // DCA: built with the regime key ranges' lower limits and tile narrowing
 // (the other decodes compile without them).
-template <int D, int B, bool DCA>
-__global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(DecodeArgs a) {
-  using C = CDec<D, B>;
+template <int D, int B, bool DCA, int ROT>
+__global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kernel(DecodeArgs a) {
+  using C = CDec<D, B, ROT>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) uint32_t s_lut[C::LUT * 32];
   __shared__ int s_abort;
@@ -353,11 +366,12 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
         uint8_t* grec = a.cache_w + ((int64_t)(b * a.n_kv_heads + kvh) * (a.capacity / kTile) + pos / kTile) * C::REC;
         pack::PositionCodes<D, B> pc;
         if (pos == sl - 1) {
-          pack::quantise_loaded<D, B>(new_row, static_cast<int>(pos % kTile), lane, pc);
+          pack::quantise_loaded<D, B, ROT>(new_row, static_cast<int>(pos % kTile), lane, pc, a.signs2);
         } else {
-          pack::quantise_position<D, B>(krow, vrow, a.signs, static_cast<int>(pos % kTile), lane, pc);
+          pack::quantise_position<D, B, ROT>(krow, vrow, a.signs, static_cast<int>(pos % kTile), lane, pc,
+                                             a.signs2);
         }
-        pack::store_position_global<D, B>(grec, static_cast<int>(pos % kTile), lane, pc);
+        pack::store_position_global<D, B, ROT>(grec, static_cast<int>(pos % kTile), lane, pc);
       }
       if (n0 < n1) {
         // The rows were written through the generic proxy; the bulk copies that
@@ -465,13 +479,21 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
     if (tile < tile_end) {
       const uint32_t rb = record(it);
       const int64_t tpos = tile * kTile;
-      const float n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D, B) + 2 * g)));
-      const float n1 =
-          __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D, B) + 2 * (g + 8))));
+      float n0 = 1.0f, n1 = 1.0f;
+      uint32_t nA = 0u, nB = 0u;
+      if constexpr (ROT) {
+        // This lane's dims lie in group (D / 8) g / 128; its positions 2t, 2t+1 and 2t+8, 2t+9.
+        const uint32_t nb = rb + v_norm_offset(D, B) + 2 * (16 * ((D / 8) * (lane >> 2) / kRotGroup) + 2 * (lane & 3));
+        nA = lds32(nb);
+        nB = lds32(nb + 16);
+      } else {
+        n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D, B) + 2 * g)));
+        n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D, B) + 2 * (g + 8))));
+      }
       uint32_t pb0, pb1, pl[2] = {0u, 0u};
       softmax_tile<C::MT_W, C::PSPLIT, DCA>(S, tpos, g, lo0, lim0, lo1, lim1, scale_log2, n0, n1, st, acc, pb0,
                                             pb1, pl);
-      pv_tile<D, B>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, pl, acc);
+      pv_tile<D, B, ROT>(rb, lut_bytes, lane4, wh, lane, pb0, pb1, pl, acc, nA, nB);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[it % C::NSTAGE]);
@@ -500,39 +522,42 @@ __global__ void __launch_bounds__(CDec<D, B>::THREADS, 1) attn_decode_kernel(Dec
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
-                                           a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
-                                           centroid_scale(B));
+  decode_epilogue<typename C::Sh, C::MT_W, ROT>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp,
+                                                lane, a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
+                                                centroid_scale(B), a.signs2);
   decode_split_tail<D, C::RING, 256>(a, split, gid, b, kvh, rg, tid, smem);
 }
 
-template <int D, int B, bool DCA>
+template <int D, int B, bool DCA, int ROT>
 static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
-  using C = CDec<D, B>;
+  using C = CDec<D, B, ROT>;
   static bool configured = false;  // per process; the attribute is per function
   static int cap = 0;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, B, DCA>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, B, DCA, ROT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_split_decode(attn_decode_kernel<D, B, DCA>, a, C::THREADS, C::SMEM, &cap, stream);
+  return launch_split_decode(attn_decode_kernel<D, B, DCA, ROT>, a, C::THREADS, C::SMEM, &cap, stream);
 }
 
-template <int D, int B>
+template <int D, int B, int ROT>
 static cudaError_t launch_decode_dim(const DecodeArgs& a, cudaStream_t stream) {
-  return a.dca_chunk > 0 ? launch_decode_d<D, B, true>(a, stream) : launch_decode_d<D, B, false>(a, stream);
+  return a.dca_chunk > 0 ? launch_decode_d<D, B, true, ROT>(a, stream) : launch_decode_d<D, B, false, ROT>(a, stream);
 }
 
-// Every head dim of one bit width.
-template <int B>
+// Every head dim of one bit width and rotation (the block-diagonal rotation
+// needs at least one 128-dim group).
+template <int B, int ROT = 0>
 static cudaError_t launch_decode_bits(const DecodeArgs& a, cudaStream_t stream) {
   switch (a.head_dim) {
-    case 64: return launch_decode_dim<64, B>(a, stream);
-    case 128: return launch_decode_dim<128, B>(a, stream);
-    case 256: return launch_decode_dim<256, B>(a, stream);
-    case 512: return launch_decode_dim<512, B>(a, stream);
+    case 64:
+      if constexpr (ROT) return cudaErrorInvalidValue;
+      else return launch_decode_dim<64, B, 0>(a, stream);
+    case 128: return launch_decode_dim<128, B, ROT>(a, stream);
+    case 256: return launch_decode_dim<256, B, ROT>(a, stream);
+    case 512: return launch_decode_dim<512, B, ROT>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -810,6 +810,9 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
   if (cache->v_bits != 0 && cache->v_bits != 3)
     return static_cast<ckv_status>(ckv::set_last_error(
         CKV_ERR_UNSUPPORTED, "prefill reads 3-bit V codes only (cache v_bits %d)", static_cast<int>(cache->v_bits)));
+  if (cache->v_signs2)
+    return static_cast<ckv_status>(
+        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill runs the full D-point transform only (v_signs2 set)"));
   if (!cache->data || !cache->v_signs || (reinterpret_cast<uintptr_t>(cache->data) & 15))
     return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "cache data / signs"));
   if (n_new == 0) return CKV_OK;

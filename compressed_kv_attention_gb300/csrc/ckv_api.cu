@@ -66,6 +66,8 @@ ckv_status check_cache(const ckv_cache* c) {
     return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive");
   if (c->v_bits != 0 && (c->v_bits < 2 || c->v_bits > 4))
     return fail(CKV_ERR_INVALID_ARG, "v_bits must be 2, 3 or 4 (or 0 for 3), got %d", c->v_bits);
+  if (c->v_signs2 && c->head_dim < ckv::kRotGroup)
+    return fail(CKV_ERR_UNSUPPORTED, "the block-diagonal rotation needs head_dim >= 128 (got %d)", c->head_dim);
   if (c->capacity <= 0 || c->capacity % 16)
     return fail(CKV_ERR_INVALID_ARG, "capacity must be a positive multiple of 16");
   if (!c->data || !aligned(c->data, 16)) return fail(CKV_ERR_INVALID_ARG, "cache data null or not 16-byte aligned");
@@ -137,20 +139,22 @@ int set_last_error(int status, const char* fmt, ...) {
 
 extern "C" {
 
-int32_t ckv_version(void) { return 101; }
+int32_t ckv_version(void) { return 102; }
 
 const char* ckv_last_error(void) { return g_err; }
 
 size_t ckv_cache_bytes_v(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity,
-                         int32_t v_bits) {
+                         int32_t v_bits, int32_t rot_group) {
   if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0 || capacity <= 0 || capacity % 16 ||
-      v_bits < 2 || v_bits > 4)
+      v_bits < 2 || v_bits > 4 || (rot_group != 0 && rot_group != ckv::kRotGroup) ||
+      (rot_group && head_dim < ckv::kRotGroup))
     return 0;
-  return static_cast<size_t>(batch) * n_kv_heads * (capacity / 16) * ckv::record_bytes(head_dim, v_bits);
+  const int ng = rot_group ? head_dim / rot_group : 1;
+  return static_cast<size_t>(batch) * n_kv_heads * (capacity / 16) * ckv::record_bytes(head_dim, v_bits, ng);
 }
 
 size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity) {
-  return ckv_cache_bytes_v(head_dim, n_kv_heads, batch, capacity, 3);
+  return ckv_cache_bytes_v(head_dim, n_kv_heads, batch, capacity, 3, 0);
 }
 
 ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok, const void* k_f16,
@@ -177,6 +181,8 @@ ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok
   a.n_kv_heads = cache->n_kv_heads;
   a.batch = cache->batch;
   a.v_bits = cache_v_bits(cache);
+  a.rot = cache->v_signs2 ? 1 : 0;
+  a.signs2 = cache->v_signs2;
   a.tok_offset = tok_offset;
   a.n_tok = n_tok;
   a.k = static_cast<const __half*>(k_f16);
@@ -250,6 +256,8 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.n_kv_heads = Hkv;
   a.batch = B;
   a.v_bits = compressed ? cache_v_bits(cache) : 0;
+  a.rot = (compressed && cache->v_signs2) ? 1 : 0;
+  a.signs2 = compressed ? cache->v_signs2 : nullptr;
   a.seq_len = seq_len;
   a.max_seq_len = max_seq_len;
   a.q = static_cast<const __half*>(q);

@@ -15,9 +15,14 @@ namespace ckv {
 constexpr int kTile = 16;  // token positions per tile record
 
 // A record holds 16 positions: K codes [0, 16D), K scales [16D, 17D), V codes
-// at B bits per value [17D, 17D + 2BD), V norms (32 bytes). B = 3 is TBQ3;
-// 2 and 4 are the neighbouring tiers of the same quantiser.
-__host__ __device__ constexpr int record_bytes(int D, int B = 3) { return 17 * D + 2 * B * D + 32; }
+// at B bits per value [17D, 17D + 2BD), V norms (32 bytes per norm group).
+// B = 3 is TBQ3; 2 and 4 are the neighbouring tiers of the same quantiser.
+// NG = 1 norm per position for the full D-point transform, D / 128 for the
+// block-diagonal rotation; norm (p, j) at v_norm_offset + 2 (16 j + p).
+__host__ __device__ constexpr int record_bytes(int D, int B = 3, int NG = 1) {
+  return 17 * D + 2 * B * D + 32 * NG;
+}
+constexpr int kRotGroup = 128;  // dims per group of the block-diagonal rotation
 __host__ __device__ constexpr int k_scale_offset(int D) { return 16 * D; }
 __host__ __device__ constexpr int v_code_offset(int D) { return 17 * D; }
 __host__ __device__ constexpr int v_norm_offset(int D, int B = 3) { return 17 * D + 2 * B * D; }
@@ -221,6 +226,13 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // Pack two fp32 into fp16x2 (round to nearest even): lo -> bits 0..15, hi -> 16..31.
+// Lane-wise fp16 product of two packed fp16 pairs (one rounding per half).
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -13,11 +13,13 @@ struct PackArgs {
   int64_t capacity;
   int head_dim, n_kv_heads, batch;
   int v_bits;                          // bits per V code: 2, 3 or 4
+  int rot;                             // 0: full D-point transform; 1: 128-dim groups, two sign diagonals
   int64_t tok_offset, n_tok;
   const __half* k;
   const __half* v;
   int64_t token_stride, batch_stride;  // in elements
   const int8_t* signs;
+  const int8_t* signs2;                // second diagonal (rot = 1)
 };
 cudaError_t launch_kv_pack(const PackArgs& a, cudaStream_t stream);
 
@@ -36,6 +38,8 @@ struct DecodeArgs {
   const __half* k16;         // dense fp16 keys (fp16 decode) or nullptr
   const __half* v16;
   const int8_t* signs;       // sign diagonal (compressed decode) or nullptr
+  const int8_t* signs2;      // second diagonal of the block-diagonal rotation (rot = 1)
+  int rot;                   // 0: full D-point transform; 1: 128-dim groups, two diagonals
   int64_t capacity;
   int head_dim, n_kv_heads, batch;
   int v_bits;                // bits per V code of the compressed cache: 2, 3 or 4
@@ -87,6 +91,9 @@ __host__ __device__ inline MergeTree merge_tree(int n_split) {
 cudaError_t launch_attn_decode(const DecodeArgs& a, cudaStream_t stream);       // dispatches on v_bits
 cudaError_t launch_attn_decode_tbq2(const DecodeArgs& a, cudaStream_t stream);  // v_bits 2
 cudaError_t launch_attn_decode_tbq4(const DecodeArgs& a, cudaStream_t stream);  // v_bits 4
+cudaError_t launch_attn_decode_rot2(const DecodeArgs& a, cudaStream_t stream);  // rot 1, v_bits 2
+cudaError_t launch_attn_decode_rot3(const DecodeArgs& a, cudaStream_t stream);  // rot 1, v_bits 3
+cudaError_t launch_attn_decode_rot4(const DecodeArgs& a, cudaStream_t stream);  // rot 1, v_bits 4
 cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream);
 
 struct LseMergeArgs {

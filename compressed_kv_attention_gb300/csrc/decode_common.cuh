@@ -162,11 +162,25 @@ __device__ __forceinline__ void exchange_S(float (&S)[4], float4* xbuf, int grou
 // 1/sqrt(D) comes from the orthonormal inverse, one from the norm scaling
 // folded into P', and vscale (the centroid table's scale) undoes the
 // table's scaling. Without `signs` (dense values) the row is stored as is.
-template <int D>
+// ROT = 1 (block-diagonal rotation): the second diagonal `signs2` comes first,
+// the butterfly stays inside 128-dim groups (the register stages stop at dim
+// bit 6), and the scale is vscale / 128 (the norms were applied to V itself).
+template <int D, int ROT = 0>
 __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane, const int8_t* signs,
-                                                   float* orow, float vscale = kCentroidScale) {
+                                                   float* orow, float vscale = kCentroidScale,
+                                                   const int8_t* signs2 = nullptr) {
   constexpr int E2 = D / 64;
+  constexpr int EG = ROT ? kRotGroup / 64 : E2;   // register stages inside one transform group
+  constexpr float GSCALE = ROT ? 1.0f / kRotGroup : 1.0f / D;
   if (signs) {
+    if constexpr (ROT) {
+#pragma unroll
+      for (int e = 0; e < E2; ++e) {
+        const char2 sg = *reinterpret_cast<const char2*>(signs2 + 64 * e + 2 * lane);
+        if (sg.x < 0) v[e].x = -v[e].x;
+        if (sg.y < 0) v[e].y = -v[e].y;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < E2; ++e) {
       const float a0 = v[e].x, a1 = v[e].y;
@@ -183,7 +197,7 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
       }
     }
 #pragma unroll
-    for (int hh = 1; hh < E2; hh <<= 1) {
+    for (int hh = 1; hh < EG; hh <<= 1) {
 #pragma unroll
       for (int e = 0; e < E2; ++e) {
         if ((e & hh) == 0) {
@@ -197,8 +211,8 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
     for (int e = 0; e < E2; ++e) {
       const int d = 64 * e + 2 * lane;
       const char2 sg = *reinterpret_cast<const char2*>(signs + d);
-      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (vscale / D);
-      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (vscale / D);
+      v[e].x = (sg.x < 0 ? -v[e].x : v[e].x) * (vscale * GSCALE);
+      v[e].y = (sg.y < 0 ? -v[e].y : v[e].y) * (vscale * GSCALE);
     }
   }
   if (orow) {
@@ -223,11 +237,11 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
 // Each group stores its unscaled accumulators with its own (m, l); warp r < 8
 // owns row r and rescales the groups while summing them (other warps are done
 // after the second barrier).
-template <typename Sh, int MTW>
+template <typename Sh, int MTW, int ROT = 0>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
                                                 float* mlbuf, int group, int wh, int warp, int lane,
                                                 const int8_t* signs, float* slot,
-                                                float vscale = kCentroidScale) {
+                                                float vscale = kCentroidScale, const int8_t* signs2 = nullptr) {
   constexpr int D = Sh::DIM;
   const int g = lane >> 2, t = lane & 3;
   // Reduce the row sums over the 8 lanes that share rows (2t, 2t+1).
@@ -282,7 +296,7 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
     }
     v[e] = x;
   }
-  derotate_store_row<D>(v, lane, signs, slot + r * D, vscale);
+  derotate_store_row<D, ROT>(v, lane, signs, slot + r * D, vscale, signs2);
   if (lane == 0) {
     slot[8 * D + r] = mc;
     slot[8 * D + 8 + r] = lc;

@@ -21,9 +21,9 @@
 
 namespace ckv {
 
-template <int D, int B>
+template <int D, int B, int ROT>
 __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
-  constexpr int REC = record_bytes(D, B);
+  constexpr int REC = record_bytes(D, B, ROT ? D / kRotGroup : 1);
   constexpr int E = D / 32;
   constexpr int LPB = 32 / E;
   using PC = pack::PositionCodes<D, B>;
@@ -54,11 +54,11 @@ __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
       const __half* krow = a.k + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
       const __half* vrow = a.v + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
       PC pc;
-      pack::quantise_position<D, B>(krow, vrow, a.signs, p, lane, pc);
+      pack::quantise_position<D, B, ROT>(krow, vrow, a.signs, p, lane, pc, a.signs2);
       pack::store_k_codes<E>(rec, p, lane, pc.q);
       if (lane % LPB == 0)
         *reinterpret_cast<__half*>(rec + k_scale_offset(D) + 2 * (p * (D / 32) + lane / LPB)) = pc.d16;
-      if (lane == 0) *reinterpret_cast<__half*>(rec + v_norm_offset(D, B) + 2 * p) = pc.n16;
+      pack::store_norm<D, B, ROT>(rec, p, lane, pc.n16);
 #pragma unroll
       for (int w = 0; w < PC::NW; ++w)
         if (pc.mask[w])
@@ -76,21 +76,31 @@ __global__ void __launch_bounds__(512) kv_pack_kernel(PackArgs a) {
   const __half* krow = a.k + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
   const __half* vrow = a.v + b * a.batch_stride + j * a.token_stride + (int64_t)h * D;
   PC pc;
-  pack::quantise_position<D, B>(krow, vrow, a.signs, p, lane, pc);
-  pack::store_position_global<D, B>(grec, p, lane, pc);
+  pack::quantise_position<D, B, ROT>(krow, vrow, a.signs, p, lane, pc, a.signs2);
+  pack::store_position_global<D, B, ROT>(grec, p, lane, pc);
 }
 
-template <int D, int B>
-static cudaError_t launch_pack_db(const PackArgs& a, dim3 grid, cudaStream_t stream) {
+template <int D, int B, int ROT>
+static cudaError_t launch_pack_dbr(const PackArgs& a, dim3 grid, cudaStream_t stream) {
   // Same shared-memory carveout as the decode kernels, so that an SM does not
   // reconfigure its L1 / shared split between a pack and the decode after it.
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(kv_pack_kernel<D, B>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(kv_pack_kernel<D, B, ROT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     configured = true;
   }
-  kv_pack_kernel<D, B><<<grid, 512, 0, stream>>>(a);
+  kv_pack_kernel<D, B, ROT><<<grid, 512, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <int D, int B>
+static cudaError_t launch_pack_db(const PackArgs& a, dim3 grid, cudaStream_t stream) {
+  if constexpr (D >= kRotGroup) {
+    if (a.rot) return launch_pack_dbr<D, B, 1>(a, grid, stream);
+  } else {
+    if (a.rot) return cudaErrorInvalidValue;
+  }
+  return launch_pack_dbr<D, B, 0>(a, grid, stream);
 }
 
 template <int D>

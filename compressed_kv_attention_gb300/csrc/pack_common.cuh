@@ -113,9 +113,13 @@ __device__ __forceinline__ void load_position(const __half* krow, const __half* 
   for (int e = 0; e < E; ++e) in.sg[e] = signs[lane * E + e];
 }
 
-template <int D, int B = 3>
+// ROT = 1: the block-diagonal variant: each 128-dim group is transformed on
+// its own (the butterfly stops at the group's lanes), the second sign diagonal
+// `signs2` follows the transform, and each group has its own norm (every lane
+// of a group holds it in n16).
+template <int D, int B = 3, int ROT = 0>
 __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int p, int lane,
-                                                PositionCodes<D, B>& pc) {
+                                                PositionCodes<D, B>& pc, const int8_t* signs2 = nullptr) {
   constexpr int E = D / 32;            // values per lane
   constexpr int LPB = 32 / E;          // lanes per q8_0 block
   using PC = PositionCodes<D, B>;
@@ -162,16 +166,22 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
     }
   }
   // Remaining stages across lanes: the partner lane differs in one lane bit.
+  constexpr int LANES = ROT ? kRotGroup / E : 32;  // lanes per transform group
 #pragma unroll
-  for (int hl = 1; hl < 32; hl <<= 1) {
+  for (int hl = 1; hl < LANES; hl <<= 1) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const float o = __shfl_xor_sync(0xffffffffu, z[e], hl);
       z[e] = (lane & hl) ? (o - z[e]) : (z[e] + o);
     }
   }
+  if constexpr (ROT) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    for (int e = 0; e < E; ++e)
+      if (signs2[lane * E + e] < 0) z[e] = -z[e];
+  }
+#pragma unroll
+  for (int off = LANES / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   const float r = sqrtf(ss);  // correctly rounded
   pc.n16 = __float2half_rn(r);
 
@@ -210,12 +220,26 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
   }
 }
 
-template <int D, int B = 3>
+template <int D, int B = 3, int ROT = 0>
 __device__ __forceinline__ void quantise_position(const __half* krow, const __half* vrow, const int8_t* signs,
-                                                  int p, int lane, PositionCodes<D, B>& pc) {
+                                                  int p, int lane, PositionCodes<D, B>& pc,
+                                                  const int8_t* signs2 = nullptr) {
   PositionInput<D> in;
   load_position<D>(krow, vrow, signs, lane, in);
-  quantise_loaded<D, B>(in, p, lane, pc);
+  quantise_loaded<D, B, ROT>(in, p, lane, pc, signs2);
+}
+
+// Store a position's V norm(s) into a record: one per position, or (ROT) the
+// first lane of every 128-dim group stores its group's norm at group-major
+// offset 2 (16 j + p).
+template <int D, int B, int ROT>
+__device__ __forceinline__ void store_norm(uint8_t* rec, int p, int lane, __half n16) {
+  if constexpr (ROT) {
+    constexpr int LANES = kRotGroup / (D / 32);
+    if (lane % LANES == 0) *reinterpret_cast<__half*>(rec + v_norm_offset(D, B) + 2 * (16 * (lane / LANES) + p)) = n16;
+  } else {
+    if (lane == 0) *reinterpret_cast<__half*>(rec + v_norm_offset(D, B) + 2 * p) = n16;
+  }
 }
 
 // Byte offset inside a record of the 8-byte K-code chunk that holds dims
@@ -257,7 +281,7 @@ __device__ __forceinline__ void store_k_codes(uint8_t* rec, int p, int lane, con
 // stores for its K codes, scale and norm; word-wide atomic AND then OR for its
 // V fields, whose words it shares with the other positions of the record.
 // Positions own disjoint bits, so concurrent writers of one record commute.
-template <int D, int B = 3>
+template <int D, int B = 3, int ROT = 0>
 __device__ __forceinline__ void store_position_global(uint8_t* grec, int p, int lane,
                                                       const PositionCodes<D, B>& pc) {
   constexpr int E = D / 32;
@@ -266,7 +290,7 @@ __device__ __forceinline__ void store_position_global(uint8_t* grec, int p, int 
   store_k_codes<E>(grec, p, lane, pc.q);
   if (lane % LPB == 0)
     *reinterpret_cast<__half*>(grec + k_scale_offset(D) + 2 * (p * (D / 32) + lane / LPB)) = pc.d16;
-  if (lane == 0) *reinterpret_cast<__half*>(grec + v_norm_offset(D, B) + 2 * p) = pc.n16;
+  store_norm<D, B, ROT>(grec, p, lane, pc.n16);
 #pragma unroll
   for (int w = 0; w < PC::NW; ++w) {
     if (pc.mask[w]) {

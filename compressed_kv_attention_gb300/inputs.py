@@ -46,7 +46,8 @@ def splitmix64_stream(seed: int, n: int) -> list[int]:
 
 
 def tbq_signs(head_dim: int, seed: int = 42) -> np.ndarray:
-    """The +/-1 sign diagonal (int8, length ``head_dim``) shared by every head and token."""
+    """The +/-1 sign diagonal (int8, length ``head_dim``) shared by every head and
+    token; the block-diagonal rotation's second diagonal uses seed 43."""
     words = splitmix64_stream(seed, head_dim)
     return np.array([-1 if (w >> 63) & 1 else 1 for w in words], dtype=np.int8)
 
@@ -116,6 +117,7 @@ class Workload:
     dca_chunk: int = 0    # decode: dual chunk attention with this chunk (three regime queries)
     q_dtype: str = "float16"
     v_bits: int = 3       # bits per V code (3: TBQ3; 2 and 4: the neighbouring tiers)
+    rot_group: int = 0    # 0: full D-point transform; 128: block-diagonal rotation with two sign diagonals
 
     @property
     def group(self) -> int:
@@ -131,7 +133,8 @@ def _one_percent(d: int) -> int:
 # long-context decode and the chunked prefill; and a verify batch of 4 drafted
 # tokens over the Gemma-4 global-layer cache (multi-query decode), dual chunk
 # attention of one token over it with 8192-token chunks, and the long-context
-# decode over caches whose V codes have 2 or 4 bits.
+# decode over caches whose V codes have 2 or 4 bits or use the block-diagonal
+# rotation.
 WORKLOADS = {
     "tiny_decode": Workload("tiny_decode", head_dim=128, n_kv_heads=1, n_q_heads=4, batch=1,
                             seq_len=256, seed=0, n_outliers=2),
@@ -150,13 +153,16 @@ WORKLOADS = {
                                  seq_len=262144, seed=7, n_outliers=_one_percent(512), v_bits=2),
     "long_decode_tbq4": Workload("long_decode_tbq4", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=4,
                                  seq_len=262144, seed=8, n_outliers=_one_percent(512), v_bits=4),
+    "long_decode_rot": Workload("long_decode_rot", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=4,
+                                seq_len=262144, seed=9, n_outliers=_one_percent(512), rot_group=128),
     "chunked_prefill": Workload("chunked_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16,
                                 batch=1, seq_len=32768, seed=4, n_outliers=_one_percent(512),
                                 n_new=2048, q_dtype="bfloat16"),
 }
 
 
-def compressed_bytes_per_token(head_dim: int, v_bits: int = 3) -> int:
+def compressed_bytes_per_token(head_dim: int, v_bits: int = 3, rot_group: int = 0) -> int:
     """Packed bytes per (token, kv-head): q8_0 K (D int8 + D/32 fp16 scales) and TBQ V
-    (v_bits bits per value + one fp16 norm)."""
-    return head_dim + 2 * (head_dim // 32) + v_bits * head_dim // 8 + 2
+    (v_bits bits per value + one fp16 norm per vector, or per rot_group dims)."""
+    n_norms = head_dim // rot_group if rot_group else 1
+    return head_dim + 2 * (head_dim // 32) + v_bits * head_dim // 8 + 2 * n_norms

@@ -100,6 +100,16 @@ typedef enum {
  *
  * v_signs: the +/-1 sign diagonal (int8, D entries, device), one vector shared
  * by every head and token.
+ *
+ * v_signs2: NULL for the transform above (one sign diagonal, the full D-point
+ * FWHT, one norm per vector). Non-NULL selects the block-diagonal rotation of
+ * the fork the PolyKV page builds on (sections "S2 perf-path Level A/B" and
+ * "S2 perf-path D=512 fused turbo-vec": the WHT runs on each 128-dim group,
+ * with a sign diagonal before it and one after it, and each group keeps its
+ * own norm): for every group g of 128 dims, u_g = s2_g * H_128 (s1_g * x_g) /
+ * ||x_g|| with s1 = v_signs, s2 = v_signs2 (device, head_dim entries each), and
+ * the record holds D/128 norms per position, group-major: norm (p, j) at
+ * 17D + 2bD + 2*(16*j + p); R = 17D + 2bD + 32*D/128. Needs head_dim >= 128.
  */
 typedef struct {
   int32_t head_dim;      /* D */
@@ -109,14 +119,17 @@ typedef struct {
   int64_t capacity;      /* token positions per sequence, multiple of 16 */
   void* data;            /* device, ckv_cache_bytes(...) bytes, 16-byte aligned */
   const int8_t* v_signs; /* device, head_dim entries of +1 / -1 */
+  const int8_t* v_signs2; /* NULL, or device, head_dim entries: the block-diagonal rotation */
 } ckv_cache;
 
 /* Bytes of the packed cache at 3 bits per V code: batch * n_kv_heads * capacity/16 * (23*D + 32).
  * 0 if invalid. */
 CKV_API size_t ckv_cache_bytes(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity);
-/* The same at v_bits (2, 3 or 4) bits per V code: ... * (17*D + 2*v_bits*D + 32). 0 if invalid. */
+/* The same at v_bits (2, 3 or 4) bits per V code and rotation: rot_group 0 for
+ * the full transform (... * (17*D + 2*v_bits*D + 32)) or 128 for the
+ * block-diagonal rotation (... * (17*D + 2*v_bits*D + 32*D/128)). 0 if invalid. */
 CKV_API size_t ckv_cache_bytes_v(int32_t head_dim, int32_t n_kv_heads, int32_t batch, int64_t capacity,
-                                 int32_t v_bits);
+                                 int32_t v_bits, int32_t rot_group);
 
 /*
  * kv_pack — quantise n_tok new K and V rows of every sequence into the cache at
@@ -306,7 +319,8 @@ CKV_API ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts,
  * fp16 [batch][n_new][n_kv_heads][D]. out: float32 [batch][n_new][n_q_heads][D];
  * lse: float32 [batch][n_new][n_q_heads]. head_dim 64, 128, 256 or 512; the
  * query-to-kv head ratio must divide 128, and the cache must hold 3-bit V
- * codes (v_bits 0 or 3): else CKV_ERR_UNSUPPORTED.
+ * codes (v_bits 0 or 3) with the full transform (v_signs2 NULL): else
+ * CKV_ERR_UNSUPPORTED.
  */
 CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads);
 CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16,

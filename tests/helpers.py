@@ -30,19 +30,23 @@ def midpoints(bits: int = 3):
 CHUNK = 4096  # tokens per oracle chunk
 
 
-def oracle_quantize(k, v, signs, bits: int = 3):
+def oracle_quantize(k, v, signs, bits: int = 3, signs2=None):
     """Oracle q8_0 / TBQ (``bits`` per V code) of fp16 K, V [..., T, D] (leading
-    dims kept), chunked over T."""
+    dims kept), chunked over T; ``signs2`` given: the block-diagonal rotation
+    (norms then [..., T, D/128])."""
     k = np.asarray(k, np.float16)
     v = np.asarray(v, np.float16)
     T = k.shape[-2]
     qs, d16, codes, n16, u = [], [], [], [], []
     for a in range(0, T, CHUNK):
         q_, d_ = O.q8_0_quantize(k[..., a:a + CHUNK, :])
-        c_, n_, u_ = O.tbq_quantize(v[..., a:a + CHUNK, :], signs, bits)
+        if signs2 is None:
+            c_, n_, u_ = O.tbq_quantize(v[..., a:a + CHUNK, :], signs, bits)
+        else:
+            c_, n_, u_ = O.tbq_quantize_blocked(v[..., a:a + CHUNK, :], signs, signs2, bits)
         qs.append(q_); d16.append(d_); codes.append(c_); n16.append(n_); u.append(u_.astype(np.float32))
     return (np.concatenate(qs, -2), np.concatenate(d16, -2), np.concatenate(codes, -2),
-            np.concatenate(n16, -1), np.concatenate(u, -2))
+            np.concatenate(n16, -1 if signs2 is None else -2), np.concatenate(u, -2))
 
 
 def oracle_attention_chunked(q, k_of, v_of, T, scale, visible_of=None):
@@ -93,29 +97,32 @@ def check_attention(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
 
 # ------------------------------------------------------------- packed bytes --
 
-def oracle_records(qs, d16, codes, n16, capacity, bits: int = 3):
+def oracle_records(qs, d16, codes, n16, capacity, bits: int = 3, groups: int = 1):
     """Oracle byte layout of a whole cache: qs etc. shaped [B, Hkv, T, ...] -> uint8
     [B, Hkv, capacity/16, record]."""
     B, H = qs.shape[:2]
     D = qs.shape[-1]
-    out = np.zeros((B, H, capacity // 16, LY.record_bytes(D, bits)), np.uint8)
+    out = np.zeros((B, H, capacity // 16, LY.record_bytes(D, bits, groups)), np.uint8)
     for b in range(B):
         for h in range(H):
-            out[b, h] = LY.pack_records(qs[b, h], d16[b, h], codes[b, h], n16[b, h], capacity, bits)
+            out[b, h] = LY.pack_records(qs[b, h], d16[b, h], codes[b, h], n16[b, h], capacity, bits, groups)
     return out
 
 
-def read_fields(records, D, T, bits: int = 3):
+def read_fields(records, D, T, bits: int = 3, groups: int = 1):
     """Read the fields of the first T positions out of one stream's records
     (uint8 [n_tiles, record]) using the layout's index maps. Returns
     (qs int8 [T, D], d16 uint16 [T, D/32], codes uint8 [T, D], n16 uint16 [T])."""
-    kofs, sofs, nofs = LY.k_code_offsets(D), LY.k_scale_offsets(D), LY.v_norm_offsets(D, bits)
+    kofs, sofs = LY.k_code_offsets(D), LY.k_scale_offsets(D)
+    nofs = LY.v_norm_offsets(D, bits, groups).reshape(16, groups)
     vbits = LY.v_code_bits(D, bits)
     n_tiles = (T + 15) // 16
     rec = records[:n_tiles]
     qs = rec[:, kofs].view(np.int8).reshape(n_tiles * 16, D)[:T]
     sc = (rec[:, sofs].astype(np.uint16) | (rec[:, sofs + 1].astype(np.uint16) << 8)).reshape(-1, D // 32)[:T]
-    nm = (rec[:, nofs].astype(np.uint16) | (rec[:, nofs + 1].astype(np.uint16) << 8)).reshape(-1)[:T]
+    nm = (rec[:, nofs].astype(np.uint16) | (rec[:, nofs + 1].astype(np.uint16) << 8)).reshape(-1, groups)[:T]
+    if groups == 1:
+        nm = nm[:, 0]
     codes = np.zeros((n_tiles, 16, D), np.uint8)
     for k in range(bits):
         bit = vbits[..., k]
@@ -123,12 +130,12 @@ def read_fields(records, D, T, bits: int = 3):
     return qs, sc, codes.reshape(-1, D)[:T], nm
 
 
-def compare_pack(gpu_records, qs, d16, codes, n16, u, T, bits: int = 3):
+def compare_pack(gpu_records, qs, d16, codes, n16, u, T, bits: int = 3, groups: int = 1):
     """Compare one stream's GPU records with the oracle's fields. q8_0 bytes and
     scales must match bit for bit; V codes may differ only at centroid-midpoint
     ties (|u - t| < TIE_WINDOW), fp16 norms by at most one ulp. Returns counts."""
     D = qs.shape[-1]
-    gq, gs, gc, gn = read_fields(gpu_records, D, T, bits)
+    gq, gs, gc, gn = read_fields(gpu_records, D, T, bits, groups)
     assert np.array_equal(gq, qs[:T]), "q8_0 codes differ"
     assert np.array_equal(gs, d16[:T].view(np.uint16)), "q8_0 scales differ"
     mism = gc != codes[:T]
@@ -138,7 +145,7 @@ def compare_pack(gpu_records, qs, d16, codes, n16, u, T, bits: int = 3):
         dist = np.abs(uu[:, None] - midpoints(bits)[None, :]).min(axis=1)
         assert np.all(dist < TIE_WINDOW), f"{n_mism} code mismatches, worst distance to a midpoint {dist.max():.3e}"
         assert np.all(np.abs(gc[mism].astype(int) - codes[:T][mism].astype(int)) == 1)
-    on = n16[:T].view(np.uint16).astype(np.int64)
+    on = np.asarray(n16)[:T].view(np.uint16).astype(np.int64).reshape(gn.shape)
     dn = np.abs(gn.astype(np.int64) - on)
     assert np.all(dn <= 1), f"norms differ by up to {dn.max()} ulp"
     return {"code_ties": n_mism, "norm_ulp": int((dn == 1).sum())}

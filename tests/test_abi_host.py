@@ -39,23 +39,28 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_cache_bytes(lib):
-    assert lib.ckv_version() == 101
+    assert lib.ckv_version() == 102
     assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * (32768 // 16) * (23 * 512 + 32)
     assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * 32768 * 738
     assert lib.ckv_cache_bytes(128, 1, 1, 256) == 256 * 186
     for bad in [(96, 1, 1, 16), (128, 0, 1, 16), (128, 1, 0, 16), (128, 1, 1, 20), (128, 1, 1, 0)]:
         assert lib.ckv_cache_bytes(*bad) == 0
     # other V bit widths: 17 D + 2 b D + 32 bytes per 16 positions
-    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 3) == lib.ckv_cache_bytes(512, 2, 1, 32768)
-    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 2) == 2 * 32768 * 674
-    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 4) == 2 * 32768 * 802
-    assert lib.ckv_cache_bytes_v(64, 1, 1, 16, 2) == 17 * 64 + 4 * 64 + 32
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 3, 0) == lib.ckv_cache_bytes(512, 2, 1, 32768)
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 2, 0) == 2 * 32768 * 674
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 4, 0) == 2 * 32768 * 802
+    assert lib.ckv_cache_bytes_v(64, 1, 1, 16, 2, 0) == 17 * 64 + 4 * 64 + 32
     for bits in (0, 1, 5, 8):
-        assert lib.ckv_cache_bytes_v(128, 1, 1, 256, bits) == 0
+        assert lib.ckv_cache_bytes_v(128, 1, 1, 256, bits, 0) == 0
+    # block-diagonal rotation: one norm per 128 dims (744 B/token at D = 512, 3 bits)
+    assert lib.ckv_cache_bytes_v(512, 2, 1, 32768, 3, 128) == 2 * 32768 * 744
+    assert lib.ckv_cache_bytes_v(128, 1, 1, 16, 3, 128) == lib.ckv_cache_bytes(128, 1, 1, 16)
+    assert lib.ckv_cache_bytes_v(64, 1, 1, 16, 3, 128) == 0
+    assert lib.ckv_cache_bytes_v(256, 1, 1, 16, 3, 64) == 0
 
 
-def _fake_cache(D=128, Hkv=1, batch=1, cap=256, data=0x10000, signs=0x20000, v_bits=0):
-    return B.CkvCacheStruct(D, Hkv, batch, v_bits, cap, data, signs)
+def _fake_cache(D=128, Hkv=1, batch=1, cap=256, data=0x10000, signs=0x20000, v_bits=0, signs2=0):
+    return B.CkvCacheStruct(D, Hkv, batch, v_bits, cap, data, signs, signs2)
 
 
 def test_pack_argument_checks(lib):
@@ -67,6 +72,8 @@ def test_pack_argument_checks(lib):
     for bits in (1, 5, -1):
         assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(v_bits=bits)), 0, 1, fake, fake, 128, 0, None) == -1
     assert b"v_bits" in lib.ckv_last_error()
+    # the block-diagonal rotation needs a 128-dim group
+    assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(D=64, signs2=0x30000)), 0, 1, fake, fake, 128, 0, None) == -2
     assert lib.ckv_kv_pack(ctypes.byref(_fake_cache(data=0x10008)), 0, 1, fake, fake, 128, 0, None) == -1
     assert lib.ckv_kv_pack(ctypes.byref(c), 250, 10, fake, fake, 128, 0, None) == -1   # past capacity
     assert lib.ckv_kv_pack(ctypes.byref(c), -1, 1, fake, fake, 128, 0, None) == -1
@@ -156,6 +163,7 @@ def test_prefill_argument_checks(lib):
     assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=2)) == -2   # prefill reads 3-bit V only
     assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=4)) == -2
     assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=3)) == -3   # 3 passes (then the workspace)
+    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, signs2=0x30000)) == -2  # full transform only
     assert call(q=fake + 8) == -1
     assert call(out=None) == -1
     assert call(w=None) == -3

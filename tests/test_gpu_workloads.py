@@ -97,19 +97,21 @@ def test_fanout_decode_full():
 
 
 @pytest.mark.parametrize("name,heads", [("long_decode", (0, 1)), ("long_decode_tbq2", (1,)),
-                                        ("long_decode_tbq4", (0,))])
+                                        ("long_decode_tbq4", (0,)), ("long_decode_rot", (1,))])
 def test_long_decode_sampled(name, heads):
     """The long-context decode at full size (4 x 262144 tokens), one sampled
     sequence checked against the oracle: packed bytes and attention."""
     _need_gpu()
     w = inputs.WORKLOADS[name]
     D, Hkv, Hq, T, B, bits = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.batch, w.v_bits
+    groups = D // w.rot_group if w.rot_group else 1
+    signs2 = inputs.tbq_signs(D, seed=43) if w.rot_group else None
     outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
     k = inputs.normal_tensor((B, T, Hkv, D), w.seed, "k", outl, device=DEV)
     v = inputs.normal_tensor((B, T, Hkv, D), w.seed, "v", outl, device=DEV)
     q = inputs.normal_tensor((B, 1, Hq, D), w.seed, "q", outl, device=DEV)
     signs = inputs.tbq_signs(D)
-    cache = ckv.PackedCache(D, Hkv, B, T, signs, v_bits=bits)
+    cache = ckv.PackedCache(D, Hkv, B, T, signs, v_bits=bits, signs2=signs2)
     ckv.kv_pack(cache, 0, k, v)
     out = torch.empty((B, 1, Hq, D), dtype=torch.float32, device=DEV)
     lse = torch.empty((B, 1, Hq), dtype=torch.float32, device=DEV)
@@ -123,14 +125,17 @@ def test_long_decode_sampled(name, heads):
     ks = k[bs].transpose(0, 1).contiguous().cpu().numpy()   # [Hkv, T, D]
     vs = v[bs].transpose(0, 1).contiguous().cpu().numpy()
     del k, v
-    recs = cache.data.view(B, Hkv, T // 16, 17 * D + 2 * bits * D + 32)[bs].cpu().numpy()
+    recs = cache.data.view(B, Hkv, T // 16, 17 * D + 2 * bits * D + 32 * groups)[bs].cpu().numpy()
     qn = q[bs, 0].cpu().numpy().astype(np.float64)
     scale = 1.0 / math.sqrt(D)
     for h in heads:
-        qs, d16, codes, n16, u = H.oracle_quantize(ks[h], vs[h], signs, bits)
-        H.compare_pack(recs[h], qs, d16, codes, n16, u, T, bits)
+        qs, d16, codes, n16, u = H.oracle_quantize(ks[h], vs[h], signs, bits, signs2=signs2)
+        H.compare_pack(recs[h], qs, d16, codes, n16, u, T, bits, groups)
+        if signs2 is None:
+            v_of = lambda a, b: O.tbq_dequantize(codes[a:b], n16[a:b], signs, bits)  # noqa: E731
+        else:
+            v_of = lambda a, b: O.tbq_dequantize_blocked(codes[a:b], n16[a:b], signs, signs2, bits)  # noqa: E731
         rows = [hq for hq in range(Hq) if O.kv_head_of(hq, Hq, Hkv) == h]
         o_ref, l_ref = H.oracle_attention_chunked(
-            qn[rows], lambda a, b: O.q8_0_dequantize(qs[a:b], d16[a:b]),
-            lambda a, b: O.tbq_dequantize(codes[a:b], n16[a:b], signs, bits), T, scale)
+            qn[rows], lambda a, b: O.q8_0_dequantize(qs[a:b], d16[a:b]), v_of, T, scale)
         H.check_attention(o_gpu[bs, 0, rows], l_gpu[bs, 0, rows], o_ref, l_ref, f"{name} b={bs} h={h}")
