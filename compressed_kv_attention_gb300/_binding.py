@@ -63,6 +63,14 @@ SIGNATURES = {
     "ckv_attn_prefill_workspace": (_c_size, [_cache_p, _c_int, _c_int]),
     "ckv_attn_prefill": (_c_int, [_cache_p, _c_i64, _vp, _c_int, _c_int, _vp, _vp, _c_f, _vp, _vp, _vp,
                                   _c_size, _vp]),
+    "ckv_attn_prefill_prefix": (_c_int, [_cache_p, _c_i64, _vp, _c_int, _c_int, _c_f, _vp, _vp, _vp, _c_size, _vp]),
+    "ckv_f16_append": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _vp, _vp, _c_int, _c_i64, _c_i64,
+                                _vp]),
+    "ckv_attn_prefill_f16": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int, _c_int,
+                                      _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "ckv_attn_prefill_shared_workspace": (_c_size, [_cache_p, _c_int, _c_i64, _c_int, _c_int]),
+    "ckv_attn_prefill_shared": (_c_int, [_cache_p, _c_i64, _vp, _vp, _c_i64, _vp, _c_int, _vp, _vp, _vp, _c_int,
+                                         _c_int, _c_f, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_read_device_flag": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
 }
 
@@ -249,3 +257,43 @@ def read_device_flag(workspace, stream=None) -> int:
     if status not in (CKV_OK, -5):
         _check(status)
     return int(flag.value)
+
+
+def attn_prefill_prefix(cache: PackedCache, n_prefix: int, q, scale: float, out, lse, workspace, stream=None):
+    """q: bf16 [batch, n_q_tokens, n_q_heads, D]; every query sees the packed prefix [0, n_prefix)."""
+    _, n_tok, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_prefill_prefix(cache.ref(), n_prefix, _ptr(q), n_tok, n_q_heads, scale, _ptr(out),
+                                          _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def f16_append(k, v, capacity: int, seq_len, k_new, v_new, stream=None):
+    """k, v: fp16 [batch, n_kv_heads, capacity, D]; k_new/v_new: fp16 [batch, n_new, n_kv_heads, D]."""
+    batch, n_kv_heads, _, head_dim = k.shape
+    _check(load().ckv_f16_append(_ptr(k), _ptr(v), head_dim, n_kv_heads, batch, capacity, _ptr(seq_len),
+                                 _ptr(k_new), _ptr(v_new), k_new.shape[1], k_new.stride(1), k_new.stride(0),
+                                 _stream(stream)))
+
+
+def attn_prefill_f16(k, v, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace, n_split: int = 0,
+                     stream=None):
+    """Causal prefill over fp16 caches [batch, n_kv_heads, capacity, D]; q: bf16 [batch, n_new, n_q_heads, D]."""
+    batch, n_kv_heads, capacity, head_dim = k.shape
+    _, n_new, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_prefill_f16(_ptr(k), _ptr(v), head_dim, n_kv_heads, batch, capacity, _ptr(seq_len),
+                                       max_seq_len, _ptr(q), n_new, n_q_heads, scale, n_split, _ptr(out), _ptr(lse),
+                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def attn_prefill_shared_workspace(prefix: PackedCache, n_agents: int, tail_capacity: int, n_new: int,
+                                  n_q_heads: int) -> int:
+    return int(load().ckv_attn_prefill_shared_workspace(prefix.ref(), n_agents, tail_capacity, n_new, n_q_heads))
+
+
+def attn_prefill_shared(prefix: PackedCache, n_prefix: int, k_tail, v_tail, tail_len, q, k_new, v_new,
+                        scale: float, out, lse, workspace, stream=None):
+    """Multi-tenant prefill: q bf16 [n_agents, n_new, n_q_heads, D]; tails fp16 [n_agents, Hkv, cap, D]."""
+    n_agents, n_new, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_prefill_shared(prefix.ref(), n_prefix, _ptr(k_tail), _ptr(v_tail), k_tail.shape[2],
+                                          _ptr(tail_len), n_agents, _ptr(q), _ptr(k_new), _ptr(v_new), n_new,
+                                          n_q_heads, scale, _ptr(out), _ptr(lse), _ptr(workspace),
+                                          workspace.numel(), _stream(stream)))

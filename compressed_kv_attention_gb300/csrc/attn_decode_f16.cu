@@ -65,6 +65,17 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     if (ok) row_to_query(rr, group_q, kvh, qi, h);
     const __half* qrow = a.q + ((int64_t)(b * a.n_q + qi) * a.n_q_heads + h) * D;
     load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
+    if (a.q_bf16) {
+      // bf16 queries: every bf16 value in the fp16 range converts exactly.
+#pragma unroll
+      for (int i = 0; i < C::NB_W; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qf[i][j]));
+          const __half2 hq = __floats2half2_rn(f.x, f.y);
+          qf[i][j] = *reinterpret_cast<const uint32_t*>(&hq);
+        }
+    }
   }
   float acc[C::MT_W][4];
 #pragma unroll
@@ -133,6 +144,31 @@ static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
     configured = true;
   }
   return launch_split_decode(attn_decode_f16_kernel<D>, a, C::THREADS, C::SMEM, &cap, stream);
+}
+
+// Copy n_new rows per sequence into dense fp16 caches [batch][n_kv_heads]
+// [capacity][D] at positions [seq_len[b] - n_new, seq_len[b]) (positions
+// outside [0, capacity) are skipped). One CTA per (row, sequence), one 16-byte
+// word per thread.
+__global__ void f16_append_kernel(F16AppendArgs a) {
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int64_t pos = (int64_t)a.seq_len[b] - a.n_new + j;
+  if (pos < 0 || pos >= a.capacity) return;
+  const int words = a.head_dim / 8;  // uint4 per (head) row
+  for (int w = threadIdx.x; w < a.n_kv_heads * words; w += blockDim.x) {
+    const int h = w / words, c = w % words;
+    const int64_t src = b * a.batch_stride + (int64_t)j * a.token_stride + (int64_t)h * a.head_dim + 8 * c;
+    const int64_t dst = (((int64_t)b * a.n_kv_heads + h) * a.capacity + pos) * a.head_dim + 8 * c;
+    *reinterpret_cast<uint4*>(a.k + dst) = *reinterpret_cast<const uint4*>(a.k_new + src);
+    *reinterpret_cast<uint4*>(a.v + dst) = *reinterpret_cast<const uint4*>(a.v_new + src);
+  }
+}
+
+cudaError_t launch_f16_append(const F16AppendArgs& a, cudaStream_t stream) {
+  if (a.n_new == 0 || a.batch == 0) return cudaSuccess;
+  const int threads = a.n_kv_heads * a.head_dim / 8 < 256 ? a.n_kv_heads * a.head_dim / 8 : 256;
+  f16_append_kernel<<<dim3(a.n_new, a.batch), (threads + 31) / 32 * 32, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream) {

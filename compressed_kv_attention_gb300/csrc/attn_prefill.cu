@@ -42,6 +42,9 @@ struct PrefillArgs {
   int n_kv_heads, batch;
   int64_t n_cached;
   int n_new, n_q_heads;
+  // 0: causal chunked prefill (query i sees [0, n_cached + i]); 1: every query
+  // sees exactly [0, n_cached) (queries of other sequences over a shared prefix).
+  int prefix_only;
   const __nv_bfloat16* q;  // [batch][n_new][n_q_heads][D]
   float scale_log2;
   float* out;              // [batch][n_new][n_q_heads][D]
@@ -118,9 +121,10 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   const int QT = C::M / group_q;  // query tokens per tile
   const int n_qt = (a.n_new + QT - 1) / QT;
   const int64_t n_rec = a.capacity / kTile;
-  // 64-key steps of query tile qt: its rows see keys [0, n_cached + last row].
+  // 64-key steps of query tile qt: its rows see keys [0, n_cached + last row]
+  // (prefix_only: [0, n_cached)).
   auto steps_of = [&](int qt) {
-    const int64_t kv_end = a.n_cached + min((qt + 1) * QT, a.n_new);
+    const int64_t kv_end = a.prefix_only ? a.n_cached : a.n_cached + min((qt + 1) * QT, a.n_new);
     return static_cast<int>((kv_end + C::NKV - 1) / C::NKV);
   };
 
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         tmem_ld_wait();
         // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
         const int row_qi = s_q0 + row / group_q;
-        const int64_t rel = row_qi < a.n_new ? a.n_cached + row_qi - j0 + 1 : 0;
+        const int64_t rel = row_qi >= a.n_new ? 0 : a.prefix_only ? a.n_cached - j0 : a.n_cached + row_qi - j0 + 1;
         const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
         const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
         float x[C::NKV];
@@ -732,7 +736,8 @@ struct PrefillPlan {
   int grid;
   int stream_k;
 };
-static PrefillPlan plan_prefill(int batch, int n_kv_heads, int n_q_heads, int64_t n_cached, int n_new) {
+static PrefillPlan plan_prefill(int batch, int n_kv_heads, int n_q_heads, int64_t n_cached, int n_new,
+                                int prefix_only) {
   PrefillPlan p{};
   p.qt = 128 / (n_q_heads / n_kv_heads);
   p.n_qt = (n_new + p.qt - 1) / p.qt;
@@ -740,7 +745,7 @@ static PrefillPlan plan_prefill(int batch, int n_kv_heads, int n_q_heads, int64_
   p.grid = device_sms();
   int64_t s_bh = 0, max_steps = 0;
   for (int t = 0; t < p.n_qt; ++t) {
-    const int64_t kv_end = n_cached + std::min((t + 1) * p.qt, n_new);
+    const int64_t kv_end = prefix_only ? n_cached : n_cached + std::min((t + 1) * p.qt, n_new);
     const int64_t st = (kv_end + 63) / 64;
     s_bh += st;
     max_steps = std::max(max_steps, st);
@@ -770,7 +775,7 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const PrefillPlan pl = plan_prefill(a.batch, a.n_kv_heads, a.n_q_heads, a.n_cached, a.n_new);
+  const PrefillPlan pl = plan_prefill(a.batch, a.n_kv_heads, a.n_q_heads, a.n_cached, a.n_new, a.prefix_only);
   PrefillArgs k = a;
   k.stream_k = pl.stream_k;
   const unsigned grid = static_cast<unsigned>(pl.stream_k ? pl.grid : pl.n_tiles);
@@ -793,43 +798,50 @@ CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new,
   return ckv::prefill_ws_bytes(cache->head_dim, cache->batch, cache->n_kv_heads, n_q_heads, n_new);
 }
 
-CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16, int32_t n_new,
-                                    int32_t n_q_heads, const void* k_new_f16, const void* v_new_f16, float scale,
-                                    float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
-  if (!cache) return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "cache is null"));
-  if (n_new < 0 || n_cached < 0 || n_cached + n_new > cache->capacity || cache->capacity % 16)
-    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "token range outside the cache"));
+}  // extern "C"
+
+namespace {
+
+ckv_status prefill_fail(ckv_status st, const char* msg) {
+  return static_cast<ckv_status>(ckv::set_last_error(st, "%s", msg));
+}
+
+// Checks shared by both prefill entry points (n_new > 0 queries over a cache
+// whose keys end at n_cached, or n_cached + n_new for the causal prefill).
+ckv_status prefill_checks(const ckv_cache* cache, int64_t kv_end, const void* q_bf16, int32_t n_new,
+                          int32_t n_q_heads, float* out, float* lse) {
+  if (!cache) return prefill_fail(CKV_ERR_INVALID_ARG, "cache is null");
+  if (n_new < 0 || kv_end < 0 || kv_end > cache->capacity || cache->capacity % 16)
+    return prefill_fail(CKV_ERR_INVALID_ARG, "token range outside the cache");
   if (cache->head_dim != 64 && cache->head_dim != 128 && cache->head_dim != 256 && cache->head_dim != 512)
     return static_cast<ckv_status>(
         ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill supports head_dim 64, 128, 256, 512 (got %d)",
                             static_cast<int>(cache->head_dim)));
-  if (n_q_heads <= 0 || cache->n_kv_heads <= 0 || n_q_heads % cache->n_kv_heads ||
+  if (n_q_heads <= 0 || cache->n_kv_heads <= 0 || cache->batch <= 0 || n_q_heads % cache->n_kv_heads ||
       128 % (n_q_heads / cache->n_kv_heads))
-    return static_cast<ckv_status>(
-        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill needs n_q_heads / n_kv_heads dividing 128"));
+    return prefill_fail(CKV_ERR_UNSUPPORTED, "prefill needs n_q_heads / n_kv_heads dividing 128");
   if (cache->v_bits != 0 && cache->v_bits != 3)
     return static_cast<ckv_status>(ckv::set_last_error(
         CKV_ERR_UNSUPPORTED, "prefill reads 3-bit V codes only (cache v_bits %d)", static_cast<int>(cache->v_bits)));
-  if (cache->v_signs2)
-    return static_cast<ckv_status>(
-        ckv::set_last_error(CKV_ERR_UNSUPPORTED, "prefill runs the full D-point transform only (v_signs2 set)"));
+  if (cache->v_signs2) return prefill_fail(CKV_ERR_UNSUPPORTED, "prefill runs the full D-point transform only (v_signs2 set)");
   if (!cache->data || !cache->v_signs || (reinterpret_cast<uintptr_t>(cache->data) & 15))
-    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "cache data / signs"));
+    return prefill_fail(CKV_ERR_INVALID_ARG, "cache data / signs");
   if (n_new == 0) return CKV_OK;
-  if (!q_bf16 || !k_new_f16 || !v_new_f16 || !out || !lse || (reinterpret_cast<uintptr_t>(q_bf16) & 15) ||
-      (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(k_new_f16) & 15) ||
-      (reinterpret_cast<uintptr_t>(v_new_f16) & 15))
-    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "null or misaligned tensor"));
+  if (!q_bf16 || !out || !lse || (reinterpret_cast<uintptr_t>(q_bf16) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15))
+    return prefill_fail(CKV_ERR_INVALID_ARG, "null or misaligned tensor");
+  return CKV_OK;
+}
+
+ckv_status run_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16, int32_t n_new,
+                       int32_t n_q_heads, float scale, float* out, float* lse, void* workspace, size_t ws_bytes,
+                       void* stream, int prefix_only) {
   const size_t need = ckv::prefill_ws_bytes(cache->head_dim, cache->batch, cache->n_kv_heads, n_q_heads, n_new);
   if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return static_cast<ckv_status>(ckv::set_last_error(
         CKV_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  // Pack the new rows (same quantisers as kv_pack) at [n_cached, n_cached + n_new).
-  const int64_t row = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
-  const ckv_status ps = ckv_kv_pack(cache, n_cached, n_new, k_new_f16, v_new_f16, row, row * n_new, stream);
-  if (ps != CKV_OK) return ps;
   ckv::PrefillArgs a{};
   a.cache = static_cast<const uint8_t*>(cache->data);
   a.capacity = cache->capacity;
@@ -838,6 +850,7 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
   a.n_cached = n_cached;
   a.n_new = n_new;
   a.n_q_heads = n_q_heads;
+  a.prefix_only = prefix_only;
   a.q = static_cast<const __nv_bfloat16*>(q_bf16);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out;
@@ -862,6 +875,40 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
   if (e != cudaSuccess)
     return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e)));
   return CKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16, int32_t n_new,
+                                    int32_t n_q_heads, const void* k_new_f16, const void* v_new_f16, float scale,
+                                    float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  if (n_cached < 0) return prefill_fail(CKV_ERR_INVALID_ARG, "token range outside the cache");
+  ckv_status s = prefill_checks(cache, n_cached + (n_new > 0 ? n_new : 0), q_bf16, n_new, n_q_heads, out, lse);
+  if (s != CKV_OK || n_new == 0) return s;
+  if (!k_new_f16 || !v_new_f16 || (reinterpret_cast<uintptr_t>(k_new_f16) & 15) ||
+      (reinterpret_cast<uintptr_t>(v_new_f16) & 15))
+    return prefill_fail(CKV_ERR_INVALID_ARG, "null or misaligned tensor");
+  const size_t need = ckv::prefill_ws_bytes(cache->head_dim, cache->batch, cache->n_kv_heads, n_q_heads, n_new);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need));
+  // Pack the new rows (same quantisers as kv_pack) at [n_cached, n_cached + n_new).
+  const int64_t row = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
+  s = ckv_kv_pack(cache, n_cached, n_new, k_new_f16, v_new_f16, row, row * n_new, stream);
+  if (s != CKV_OK) return s;
+  return run_prefill(cache, n_cached, q_bf16, n_new, n_q_heads, scale, out, lse, workspace, ws_bytes, stream, 0);
+}
+
+CKV_API ckv_status ckv_attn_prefill_prefix(const ckv_cache* cache, int64_t n_prefix, const void* q_bf16,
+                                           int32_t n_q_tokens, int32_t n_q_heads, float scale, float* out,
+                                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  if (n_prefix < 1) return prefill_fail(CKV_ERR_INVALID_ARG, "n_prefix must be at least 1");
+  ckv_status s = prefill_checks(cache, n_prefix, q_bf16, n_q_tokens, n_q_heads, out, lse);
+  if (s != CKV_OK || n_q_tokens == 0) return s;
+  return run_prefill(cache, n_prefix, q_bf16, n_q_tokens, n_q_heads, scale, out, lse, workspace, ws_bytes, stream,
+                     1);
 }
 
 }  // extern "C"

@@ -218,7 +218,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
                              void* stream, const AppendRows* app = nullptr, int causal_q = 0,
-                             int dca_chunk = 0) {
+                             int dca_chunk = 0, int q_bf16 = 0) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
   if (s != CKV_OK) return s;
@@ -261,6 +261,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.seq_len = seq_len;
   a.max_seq_len = max_seq_len;
   a.q = static_cast<const __half*>(q);
+  a.q_bf16 = q_bf16;
   a.n_q = n_q;
   a.n_q_heads = n_q_heads;
   a.causal_q = causal_q;
@@ -407,6 +408,125 @@ ckv_status ckv_attn_decode_f16(const void* k_f16, const void* v_f16, int32_t hea
     return fail(CKV_ERR_INVALID_ARG, "k/v null or not 16-byte aligned");
   return run_decode(false, nullptr, k_f16, v_f16, head_dim, n_kv_heads, batch, capacity, seq_len, max_seq_len,
                     q_f16, n_q, n_q_heads, scale, n_split, out, lse, workspace, ws_bytes, stream);
+}
+
+ckv_status ckv_f16_append(void* k_f16, void* v_f16, int32_t head_dim, int32_t n_kv_heads, int32_t batch,
+                          int64_t capacity, const int32_t* seq_len, const void* k_new_f16, const void* v_new_f16,
+                          int32_t n_new, int64_t token_stride, int64_t batch_stride, void* stream) {
+  if (!supported_dim(head_dim)) return fail(CKV_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256,512}", head_dim);
+  if (n_kv_heads <= 0 || batch <= 0 || capacity <= 0 || n_new < 0)
+    return fail(CKV_ERR_INVALID_ARG, "bad geometry");
+  if (n_new == 0) return CKV_OK;
+  if (!k_f16 || !v_f16 || !seq_len || !k_new_f16 || !v_new_f16 || !aligned(k_f16, 16) || !aligned(v_f16, 16) ||
+      !aligned(k_new_f16, 16) || !aligned(v_new_f16, 16) || !aligned(seq_len, 4))
+    return fail(CKV_ERR_INVALID_ARG, "null or misaligned pointer");
+  const int64_t row = static_cast<int64_t>(n_kv_heads) * head_dim;
+  if (token_stride < row || token_stride % 8 || batch_stride < 0 || batch_stride % 8 ||
+      (batch > 1 && batch_stride < token_stride * n_new))
+    return fail(CKV_ERR_INVALID_ARG, "bad strides (token %lld, batch %lld)", (long long)token_stride,
+                (long long)batch_stride);
+  if (n_new > 65535 || batch > 65535) return fail(CKV_ERR_UNSUPPORTED, "n_new and batch must be at most 65535");
+  ckv::F16AppendArgs a{};
+  a.k = static_cast<__half*>(k_f16);
+  a.v = static_cast<__half*>(v_f16);
+  a.head_dim = head_dim;
+  a.n_kv_heads = n_kv_heads;
+  a.batch = batch;
+  a.capacity = capacity;
+  a.seq_len = seq_len;
+  a.k_new = static_cast<const __half*>(k_new_f16);
+  a.v_new = static_cast<const __half*>(v_new_f16);
+  a.n_new = n_new;
+  a.token_stride = token_stride;
+  a.batch_stride = batch_stride;
+  const cudaError_t e = ckv::launch_f16_append(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "f16_append launch");
+  return CKV_OK;
+}
+
+ckv_status ckv_attn_prefill_f16(const void* k_f16, const void* v_f16, int32_t head_dim, int32_t n_kv_heads,
+                                int32_t batch, int64_t capacity, const int32_t* seq_len, int64_t max_seq_len,
+                                const void* q_bf16, int32_t n_new, int32_t n_q_heads, float scale, int32_t n_split,
+                                float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  if (!supported_dim(head_dim))
+    return fail(CKV_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256,512}", head_dim);
+  if (n_kv_heads <= 0 || batch <= 0) return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive");
+  if (capacity <= 0 || capacity % 16) return fail(CKV_ERR_INVALID_ARG, "capacity must be a positive multiple of 16");
+  if (!k_f16 || !v_f16 || !aligned(k_f16, 16) || !aligned(v_f16, 16))
+    return fail(CKV_ERR_INVALID_ARG, "k/v null or not 16-byte aligned");
+  return run_decode(false, nullptr, k_f16, v_f16, head_dim, n_kv_heads, batch, capacity, seq_len, max_seq_len,
+                    q_bf16, n_new, n_q_heads, scale, n_split, out, lse, workspace, ws_bytes, stream, nullptr, 1, 0,
+                    1);
+}
+
+// Shared-prefix prefill workspace: [prefix prefill][tail prefill][prefix O, lse][tail O, lse].
+struct SharedWs {
+  size_t pre, tail, o_pre, l_pre, o_tail, l_tail, total;
+};
+static bool shared_ws(const ckv_cache* prefix, int32_t n_agents, int64_t tail_capacity, int32_t n_new,
+                      int32_t n_q_heads, SharedWs* w) {
+  if (!prefix || n_agents <= 0 || n_new <= 0 || tail_capacity <= 0) return false;
+  const size_t pre = ckv_attn_prefill_workspace(prefix, n_agents * n_new, n_q_heads);
+  const size_t tail = ckv_attn_decode_f16_workspace(prefix->head_dim, prefix->n_kv_heads, n_agents, tail_capacity,
+                                                    n_new, n_q_heads, 0);
+  if (tail == 0) return false;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(n_agents) * n_new * n_q_heads;
+  w->pre = 0;
+  w->tail = up(pre);
+  w->o_pre = w->tail + up(tail);
+  w->l_pre = w->o_pre + up(rows * prefix->head_dim * sizeof(float));
+  w->o_tail = w->l_pre + up(rows * sizeof(float));
+  w->l_tail = w->o_tail + up(rows * prefix->head_dim * sizeof(float));
+  w->total = w->l_tail + up(rows * sizeof(float));
+  return true;
+}
+
+size_t ckv_attn_prefill_shared_workspace(const ckv_cache* prefix, int32_t n_agents, int64_t tail_capacity,
+                                         int32_t n_new, int32_t n_q_heads) {
+  SharedWs w;
+  return shared_ws(prefix, n_agents, tail_capacity, n_new, n_q_heads, &w) ? w.total : 0;
+}
+
+ckv_status ckv_attn_prefill_shared(const ckv_cache* prefix, int64_t n_prefix, void* k_tail, void* v_tail,
+                                   int64_t tail_capacity, const int32_t* tail_len, int32_t n_agents,
+                                   const void* q_bf16, const void* k_new_f16, const void* v_new_f16, int32_t n_new,
+                                   int32_t n_q_heads, float scale, float* out, float* lse, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  if (!prefix) return fail(CKV_ERR_INVALID_ARG, "prefix cache is null");
+  if (prefix->batch != 1) return fail(CKV_ERR_INVALID_ARG, "the shared prefix cache holds one sequence (batch 1)");
+  if (n_prefix < 0 || n_prefix > prefix->capacity) return fail(CKV_ERR_INVALID_ARG, "n_prefix outside the cache");
+  if (n_agents <= 0 || n_new < 0) return fail(CKV_ERR_INVALID_ARG, "n_agents must be positive, n_new >= 0");
+  if (n_new == 0) return CKV_OK;
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return fail(CKV_ERR_INVALID_ARG, "null or misaligned out/lse");
+  SharedWs w;
+  if (!shared_ws(prefix, n_agents, tail_capacity, n_new, n_q_heads, &w))
+    return fail(CKV_ERR_INVALID_ARG, "invalid shared-prefix prefill geometry");
+  ckv_status s = check_ws(workspace, ws_bytes, w.total);
+  if (s != CKV_OK) return s;
+  const int D = prefix->head_dim, Hkv = prefix->n_kv_heads;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  // 1. The new rows join each agent's fp16 tail at [tail_len - n_new, tail_len).
+  const int64_t row = static_cast<int64_t>(Hkv) * D;
+  s = ckv_f16_append(k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, k_new_f16, v_new_f16, n_new, row,
+                     row * n_new, stream);
+  if (s != CKV_OK) return s;
+  // 2. Every agent's queries over its own tail, causal (token i sees [0, tail_len - n_new + i]).
+  float* o_tail = n_prefix > 0 ? reinterpret_cast<float*>(base + w.o_tail) : out;
+  float* l_tail = n_prefix > 0 ? reinterpret_cast<float*>(base + w.l_tail) : lse;
+  s = ckv_attn_prefill_f16(k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, tail_capacity, q_bf16, n_new,
+                           n_q_heads, scale, 0, o_tail, l_tail, base + w.tail, w.o_pre - w.tail, stream);
+  if (s != CKV_OK || n_prefix == 0) return s;
+  // 3. All agents' queries over the shared compressed prefix, one sequence of n_agents * n_new tokens.
+  float* o_pre = reinterpret_cast<float*>(base + w.o_pre);
+  float* l_pre = reinterpret_cast<float*>(base + w.l_pre);
+  s = ckv_attn_prefill_prefix(prefix, n_prefix, q_bf16, n_agents * n_new, n_q_heads, scale, o_pre, l_pre,
+                              base + w.pre, w.tail - w.pre, stream);
+  if (s != CKV_OK) return s;
+  // 4. Exact log-sum-exp merge of the two partials of every row.
+  const float* op[2] = {o_pre, o_tail};
+  const float* lp[2] = {l_pre, l_tail};
+  return ckv_lse_merge(2, op, lp, static_cast<int64_t>(n_agents) * n_new * n_q_heads, D, out, lse, stream);
 }
 
 ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts, const float* const* lse_parts,

@@ -46,6 +46,7 @@ struct DecodeArgs {
   const int32_t* seq_len;
   int64_t max_seq_len;
   const __half* q;
+  int q_bf16;                // fp16 decode only: q holds bf16 values (converted exactly on load)
   int n_q, n_q_heads;
   int causal_q;              // 1: query token qi sees [0, seq_len - n_q + qi + 1) (verify batch)
   int dca_chunk;             // > 0: the n_q = 3 query tokens are the DCA regimes (decode_common.cuh)
@@ -95,6 +96,20 @@ cudaError_t launch_attn_decode_rot2(const DecodeArgs& a, cudaStream_t stream);  
 cudaError_t launch_attn_decode_rot3(const DecodeArgs& a, cudaStream_t stream);  // rot 1, v_bits 3
 cudaError_t launch_attn_decode_rot4(const DecodeArgs& a, cudaStream_t stream);  // rot 1, v_bits 4
 cudaError_t launch_attn_decode_f16(const DecodeArgs& a, cudaStream_t stream);
+
+// New rows into dense fp16 K/V caches [batch][n_kv_heads][capacity][D].
+struct F16AppendArgs {
+  __half* k;
+  __half* v;
+  int head_dim, n_kv_heads, batch;
+  int64_t capacity;
+  const int32_t* seq_len;       // per sequence, counting the new rows
+  const __half* k_new;          // [batch][n_new][n_kv_heads][D] with the strides below
+  const __half* v_new;
+  int n_new;
+  int64_t token_stride, batch_stride;  // in elements
+};
+cudaError_t launch_f16_append(const F16AppendArgs& a, cudaStream_t stream);
 
 struct LseMergeArgs {
   const float* o[16];

@@ -328,6 +328,75 @@ CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, co
                             const void* v_new_f16, float scale, float* out, float* lse,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * attn_prefill_prefix — every one of n_q_tokens query tokens attends to the
+ * whole packed prefix [0, n_prefix) of each sequence (no causal limit, nothing
+ * packed): the shared-pool part of a multi-tenant prefill, where the queries of
+ * several agents that share one compressed prefix run as one sequence (PolyKV
+ * page, section "S1 — SharedKVPool": shared prefix cells are attended by every
+ * agent). Same kernels, arguments, layouts, limits and workspace
+ * (ckv_attn_prefill_workspace(cache, n_q_tokens, n_q_heads)) as
+ * ckv_attn_prefill; n_prefix in [1, capacity].
+ */
+CKV_API ckv_status ckv_attn_prefill_prefix(const ckv_cache* cache, int64_t n_prefix, const void* q_bf16,
+                                   int32_t n_q_tokens, int32_t n_q_heads, float scale, float* out,
+                                   float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * f16_append — copy n_new rows per sequence into dense fp16 K/V caches laid out
+ * [batch][n_kv_heads][capacity][D] (the layout of ckv_attn_decode_f16) at
+ * positions [seq_len[b] - n_new, seq_len[b]); seq_len (device, int32 [batch])
+ * counts the new rows. Rows whose position falls outside [0, capacity) are
+ * skipped. k_new/v_new: fp16 with the strides of ckv_kv_pack.
+ */
+CKV_API ckv_status ckv_f16_append(void* k_f16, void* v_f16, int32_t head_dim, int32_t n_kv_heads,
+                          int32_t batch, int64_t capacity, const int32_t* seq_len,
+                          const void* k_new_f16, const void* v_new_f16, int32_t n_new,
+                          int64_t token_stride, int64_t batch_stride, void* stream);
+
+/*
+ * attn_prefill_f16 — causal prefill over dense fp16 caches (a private,
+ * uncompressed per-agent tail: PolyKV page, section "S1 — SharedKVPool", the
+ * private suffix): query token i of n_new sees positions [0, seq_len[b] - n_new
+ * + i] (the new rows are the sequence's last n_new positions, already in the
+ * cache). q_bf16: bf16 [batch][n_new][n_q_heads][D], converted exactly to fp16
+ * for the tensor cores (|q| < 65504). Runs the fp16 decode kernel with n_new
+ * query tokens; workspace as ckv_attn_decode_f16_workspace(..., n_q = n_new, ...).
+ */
+CKV_API ckv_status ckv_attn_prefill_f16(const void* k_f16, const void* v_f16, int32_t head_dim,
+                                int32_t n_kv_heads, int32_t batch, int64_t capacity,
+                                const int32_t* seq_len, int64_t max_seq_len, const void* q_bf16,
+                                int32_t n_new, int32_t n_q_heads, float scale, int32_t n_split,
+                                float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * attn_prefill_shared — multi-tenant prefill over a shared compressed prefix
+ * plus private fp16 tails (PolyKV page, section "S1 — SharedKVPool": one
+ * shared prefix counted once, a private suffix per agent). n_agents agents each
+ * prefill n_new tokens; query token i of agent a sees the whole prefix
+ * [0, n_prefix) of `prefix` (a packed cache holding one sequence, batch 1) and
+ * its own tail positions [0, tail_len[a] - n_new + i]. Steps, all on the device:
+ * the new K/V rows are copied into the tails (ckv_f16_append), the tail part
+ * runs causally (ckv_attn_prefill_f16), the prefix part runs as one sequence of
+ * n_agents * n_new query tokens (ckv_attn_prefill_prefix), and the two partials
+ * of every row merge exactly (ckv_lse_merge); n_prefix = 0 leaves only the
+ * tail part.
+ * k_tail, v_tail: fp16 [n_agents][Hkv][tail_capacity][D] (written: new rows).
+ * tail_len: device int32 [n_agents], each tail's length counting the new rows.
+ * q_bf16: [n_agents][n_new][n_q_heads][D]; k_new_f16, v_new_f16: fp16
+ * [n_agents][n_new][Hkv][D]; out: float32 [n_agents][n_new][n_q_heads][D];
+ * lse: float32 [n_agents][n_new][n_q_heads]. Head dim, head ratio and the V
+ * format follow ckv_attn_prefill.
+ */
+CKV_API size_t ckv_attn_prefill_shared_workspace(const ckv_cache* prefix, int32_t n_agents,
+                                         int64_t tail_capacity, int32_t n_new, int32_t n_q_heads);
+CKV_API ckv_status ckv_attn_prefill_shared(const ckv_cache* prefix, int64_t n_prefix, void* k_tail,
+                                   void* v_tail, int64_t tail_capacity, const int32_t* tail_len,
+                                   int32_t n_agents, const void* q_bf16, const void* k_new_f16,
+                                   const void* v_new_f16, int32_t n_new, int32_t n_q_heads,
+                                   float scale, float* out, float* lse, void* workspace,
+                                   size_t ws_bytes, void* stream);
+
 /* Synchronously read the device flag (first 4 bytes of a workspace) after draining
  * `stream`. *flag receives it; when it is nonzero the flag is cleared and
  * CKV_ERR_DEVICE_FLAG returned. */

@@ -479,6 +479,37 @@ def dca_decode_reference(q, k_hat, v_hat, seq_len: int, chunk: int, scale: float
     return o, lse
 
 
+def shared_prefill_reference(q, k_prefix, v_prefix, k_tail, v_tail, tail_len: int, scale: float):
+    """Multi-tenant prefill of one agent: [PolyKV] section "S1 — SharedKVPool"
+    (shared prefix cells are attended by every agent, private suffix cells only
+    by their own; the per-agent cost is just the suffix).
+
+    ``q [n_new, Hq, D]`` are the agent's new query tokens, the last n_new
+    positions of its private tail; ``k_prefix, v_prefix [Hkv, P, D]`` the shared
+    prefix (dequantised); ``k_tail, v_tail [Hkv, >= tail_len, D]`` the agent's
+    tail, whose first tail_len rows include the n_new new ones. Query i attends,
+    in one softmax, to the P prefix keys followed by tail keys [0, tail_len -
+    n_new + i].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n_new, Hq, D = q.shape
+    Hkv = k_prefix.shape[0]
+    P = k_prefix.shape[1]
+    L = tail_len
+    vis = np.ones((n_new, P + L), dtype=bool)
+    vis[:, P:] = np.arange(L)[None, :] <= (L - n_new + np.arange(n_new))[:, None]
+    o = np.zeros((n_new, Hq, v_prefix.shape[-1]))
+    lse = np.zeros((n_new, Hq))
+    for h in range(Hq):
+        kh = kv_head_of(h, Hq, Hkv)
+        keys = np.concatenate([k_prefix[kh], k_tail[kh, :L]], axis=0)
+        vals = np.concatenate([v_prefix[kh], v_tail[kh, :L]], axis=0)
+        oh, lh = attention(q[:, h, :], keys, vals, scale, visible=vis)
+        o[:, h, :] = oh
+        lse[:, h] = lh
+    return o, lse
+
+
 def prefill_reference(q, k_hat, v_hat, n_cached: int, scale: float):
     """Causal chunked prefill for one sequence.
 

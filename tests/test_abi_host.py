@@ -188,3 +188,29 @@ def test_decode_append_argument_checks(lib):
     assert call(ts=1028) == -1       # not a multiple of 8 elements
     assert call(bs=-8) == -1
     assert call(wsb=need - 1) == -3
+
+
+def test_multitenant_prefill_argument_checks(lib):
+    fake = 0x7f0000000000
+    pre = _fake_cache(D=512, Hkv=2, cap=4096)
+    two = _fake_cache(D=512, Hkv=2, batch=2, cap=4096)
+    ws = lib.ckv_attn_prefill_shared_workspace(ctypes.byref(pre), 15, 1024, 64, 16)
+    assert ws > 0
+    assert lib.ckv_attn_prefill_shared_workspace(ctypes.byref(pre), 0, 1024, 64, 16) == 0
+
+    def shared(cache=pre, n_prefix=4096, n_agents=15, n_new=64, hq=16, w=fake, wb=ws):
+        return lib.ckv_attn_prefill_shared(ctypes.byref(cache), n_prefix, fake, fake, 1024, fake, n_agents, fake,
+                                           fake, fake, n_new, hq, 0.04, fake, fake, w, wb, None)
+    assert shared(cache=two) == -1          # the shared prefix is one sequence
+    assert shared(n_prefix=4097) == -1      # past the prefix cache
+    assert shared(n_agents=0) == -1
+    assert shared(n_new=0) == 0             # nothing to do
+    assert shared(wb=ws - 1) == -3
+    assert shared(w=fake + 8) == -3         # workspace alignment
+    # prefix-only prefill: at least one prefix token, inside the cache
+    pf = lambda n_prefix, n_tok=16: lib.ckv_attn_prefill_prefix(ctypes.byref(pre), n_prefix, fake, n_tok, 16, 0.04,
+                                                                 fake, fake, fake, 1 << 20, None)
+    assert pf(0) == -1 and pf(4097) == -1 and pf(100, 0) == 0
+    # tail append: strides and geometry
+    ap = lambda ts, hd=512: lib.ckv_f16_append(fake, fake, hd, 2, 3, 1024, fake, fake, fake, 8, ts, ts * 8, None)
+    assert ap(1000) == -1 and ap(1024, hd=96) == -2

@@ -696,3 +696,31 @@ def test_blocked_layout_roundtrips_and_matches_page_bytes_per_value(D, bits):
     page = {int(r[1]): float(r[2]) for r in _golden_lines("tier_bpv.txt")}
     if bits in page:
         assert round(v_bytes / (16 * D), 3) == page[bits]
+
+
+# ------------------------------------------ multi-tenant shared prefill ----
+
+def test_shared_prefill_reference_brute_force_and_reductions():
+    rng = np.random.default_rng(77)
+    Hq, Hkv, D, P, L, n = 4, 2, 8, 5, 6, 3
+    q = rng.standard_normal((n, Hq, D))
+    kp, vp = rng.standard_normal((Hkv, P, D)), rng.standard_normal((Hkv, P, D))
+    kt, vt = rng.standard_normal((Hkv, L + 2, D)), rng.standard_normal((Hkv, L + 2, D))
+    sc = 0.3
+    o, lse = O.shared_prefill_reference(q, kp, vp, kt, vt, L, sc)
+    for i in range(n):                      # brute force, one row at a time
+        for h in range(Hq):
+            kh = h // (Hq // Hkv)
+            keys = [kp[kh, j] for j in range(P)] + [kt[kh, j] for j in range(L - n + i + 1)]
+            vals = [vp[kh, j] for j in range(P)] + [vt[kh, j] for j in range(L - n + i + 1)]
+            w = np.array([math.exp(sc * float(q[i, h] @ kk)) for kk in keys])
+            assert np.allclose(o[i, h], (w[:, None] * np.array(vals)).sum(0) / w.sum(), atol=1e-12)
+            assert abs(lse[i, h] - math.log(w.sum())) < 1e-12
+    # Without a prefix it is the causal verify-batch attention over the tail.
+    o0, l0 = O.shared_prefill_reference(q, kp[:, :0], vp[:, :0], kt, vt, L, sc)
+    ov, lv = O.verify_decode_reference(q, kt, vt, L, sc)
+    assert np.allclose(o0, ov, atol=1e-13) and np.allclose(l0, lv, atol=1e-13)
+    # The prefix part and the tail part merge exactly into the whole.
+    op, lp = O.decode_reference(q, kp, vp, P, sc)
+    om, lm = O.lse_merge([op.reshape(-1, D), ov.reshape(-1, D)], [lp.ravel(), lv.ravel()])
+    assert np.allclose(om.reshape(o.shape), o, atol=1e-12) and np.allclose(lm.reshape(lse.shape), lse, atol=1e-12)
