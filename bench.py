@@ -58,7 +58,7 @@ def _args():
     p.add_argument("--workload", default="gemma4_decode",
                    choices=["gemma4_decode", "long_decode", "fanout_decode", "tiny_decode", "chunked_prefill",
                             "kv_pack", "verify_decode", "dca_decode", "long_decode_tbq2", "long_decode_tbq4",
-                            "long_decode_rot"])
+                            "long_decode_rot", "shared_prefill"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -448,6 +448,96 @@ class PrefillWork:
                 "algorithmic_flops": self.flops, "launch_ms": round(kernel_ms, 6)}
 
 
+class SharedPrefillWork:
+    """Multi-tenant prefill: 15 agents prefill 128 tokens each over one shared compressed prefix
+    (tcgen05, prefix-only) and their private fp16 tails (causal), merged exactly."""
+
+    graph = False  # ~1 ms steps: launched eagerly, L2 flushed before each timed step
+
+    def __init__(self, dev, stream):
+        import torch
+        import compressed_kv_attention_gb300 as ckv
+        from compressed_kv_attention_gb300 import inputs
+        self.ckv, self.torch, self.stream = ckv, torch, stream
+        w = inputs.WORKLOADS["shared_prefill"]
+        self.w = w
+        D, Hkv, Hq, P, A, TL, n = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.n_agents, w.tail_len, w.n_new
+        self.D, self.Hkv, self.Hq, self.P, self.A, self.TL, self.n = D, Hkv, Hq, P, A, TL, n
+        outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
+        self.scale = 1.0 / math.sqrt(D)
+        cap = TL + n
+        with torch.cuda.stream(stream):
+            k = inputs.normal_tensor((1, P, Hkv, D), w.seed, "prefix/k", outl, device=str(dev))
+            v = inputs.normal_tensor((1, P, Hkv, D), w.seed, "prefix/v", outl, device=str(dev))
+            self.cache = ckv.PackedCache(D, Hkv, 1, P, inputs.tbq_signs(D), device=dev)
+            ckv.kv_pack(self.cache, 0, k, v, stream=stream)
+            del k, v
+            self.kt = inputs.normal_tensor((A, Hkv, cap, D), w.seed, "tail/k", outl, device=str(dev))
+            self.vt = inputs.normal_tensor((A, Hkv, cap, D), w.seed, "tail/v", outl, device=str(dev))
+            self.kn = inputs.normal_tensor((A, n, Hkv, D), w.seed, "new/k", outl, device=str(dev))
+            self.vn = inputs.normal_tensor((A, n, Hkv, D), w.seed, "new/v", outl, device=str(dev))
+            self.q = inputs.normal_tensor((A, n, Hq, D), w.seed, "new/q", outl, device=str(dev), dtype="bfloat16")
+            self.tail_len = torch.full((A,), cap, dtype=torch.int32, device=dev)
+            self.out = torch.empty((A, n, Hq, D), dtype=torch.float32, device=dev)
+            self.lse = torch.empty((A, n, Hq), dtype=torch.float32, device=dev)
+            self.ws = torch.zeros(ckv.attn_prefill_shared_workspace(self.cache, A, cap, n, Hq), dtype=torch.uint8,
+                                  device=dev)
+            self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            self.flush = torch.empty(2 * self.l2, dtype=torch.uint8, device=dev)
+        stream.synchronize()
+        self.tokens_per_step = A * n
+        self.launches_per_step = 5  # tail append, tail prefill, prefix prefill, de-rotation, merge
+        # QK^T and PV: every query row sees the P prefix keys and TL + i + 1 tail keys.
+        self.flops = 2 * 2 * Hq * D * A * (n * P + n * TL + n * (n + 1) // 2)
+
+    def step(self, i):
+        self.ckv.attn_prefill_shared(self.cache, self.P, self.kt, self.vt, self.tail_len, self.q, self.kn, self.vn,
+                                     self.scale, self.out, self.lse, self.ws, stream=self.stream)
+
+    kernel_call = step
+
+    def between(self):
+        with self.torch.cuda.stream(self.stream):
+            self.flush.fill_(1)
+
+    def check(self):
+        assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
+
+    def e2e_setup(self):
+        t = self.torch
+        self.h_in = [x.cpu().pin_memory() for x in (self.q, self.kn, self.vn)]
+        self.d_in = [t.empty_like(x) for x in (self.q, self.kn, self.vn)]
+        self.h_out = [t.empty(x.shape, dtype=x.dtype).pin_memory() for x in (self.out, self.lse)]
+        return (sum(x.numel() * x.element_size() for x in self.h_in),
+                sum(x.numel() * x.element_size() for x in self.h_out))
+
+    def e2e_step(self, i):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        self.ckv.attn_prefill_shared(self.cache, self.P, self.kt, self.vt, self.tail_len, self.d_in[0],
+                                     self.d_in[1], self.d_in[2], self.scale, self.out, self.lse, self.ws,
+                                     stream=self.stream)
+        self.h_out[0].copy_(self.out, non_blocking=True)
+        self.h_out[1].copy_(self.lse, non_blocking=True)
+
+    def describe(self):
+        return {"workload": "shared_prefill", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
+                "agents": self.A, "prefix_tokens": self.P, "tail_tokens": self.TL, "new_tokens_per_agent": self.n,
+                "q_dtype": "bf16",
+                "step": "attn_prefill_shared (tail append + causal fp16 tail prefill + prefix-only tcgen05 "
+                        "prefill + lse merge)",
+                "l2": f"flushed before each step ({2 * self.l2 / 1e6:.0f} MB write)"}
+
+    def roofline(self, kernel_ms, peaks):
+        _, tf, kind = peaks
+        achieved = self.flops / (kernel_ms / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": "attn_prefill_shared (whole step; tcgen05 prefix prefill + mma.sync "
+                "fp16 tail prefill)", "achieved": round(achieved, 1), "peak": tf, "unit": "TFLOP/s",
+                "frac": round(achieved / tf, 4),
+                "peak_kind": kind + " bf16 dense (fp16 operands run at the same rate)", "traffic": None,
+                "algorithmic_flops": self.flops, "launch_ms": round(kernel_ms, 6)}
+
+
 class PackWork:
     """kv_pack of 2048 tokens x 2 kv heads (the size of one prefill chunk)."""
 
@@ -516,6 +606,8 @@ def _make_work(name, dev, stream):
         return FanoutWork(dev, stream)
     if name == "chunked_prefill":
         return PrefillWork(dev, stream)
+    if name == "shared_prefill":
+        return SharedPrefillWork(dev, stream)
     return PackWork(dev, stream)
 
 

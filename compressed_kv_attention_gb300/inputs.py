@@ -134,7 +134,8 @@ def _one_percent(d: int) -> int:
 # tokens over the Gemma-4 global-layer cache (multi-query decode), dual chunk
 # attention of one token over it with 8192-token chunks, and the long-context
 # decode over caches whose V codes have 2 or 4 bits or use the block-diagonal
-# rotation.
+# rotation; and the multi-tenant prefill of 15 agents, 128 new tokens each,
+# over the shared 4096-token compressed prefix and their 512-token fp16 tails.
 WORKLOADS = {
     "tiny_decode": Workload("tiny_decode", head_dim=128, n_kv_heads=1, n_q_heads=4, batch=1,
                             seq_len=256, seed=0, n_outliers=2),
@@ -155,6 +156,9 @@ WORKLOADS = {
                                  seq_len=262144, seed=8, n_outliers=_one_percent(512), v_bits=4),
     "long_decode_rot": Workload("long_decode_rot", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=4,
                                 seq_len=262144, seed=9, n_outliers=_one_percent(512), rot_group=128),
+    "shared_prefill": Workload("shared_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16, batch=1,
+                               seq_len=4096, seed=10, n_outliers=_one_percent(512), n_agents=15, tail_len=512,
+                               n_new=128, q_dtype="bfloat16"),
     "chunked_prefill": Workload("chunked_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16,
                                 batch=1, seq_len=32768, seed=4, n_outliers=_one_percent(512),
                                 n_new=2048, q_dtype="bfloat16"),

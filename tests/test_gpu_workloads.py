@@ -139,3 +139,44 @@ def test_long_decode_sampled(name, heads):
         o_ref, l_ref = H.oracle_attention_chunked(
             qn[rows], lambda a, b: O.q8_0_dequantize(qs[a:b], d16[a:b]), v_of, T, scale)
         H.check_attention(o_gpu[bs, 0, rows], l_gpu[bs, 0, rows], o_ref, l_ref, f"{name} b={bs} h={h}")
+
+
+def test_shared_prefill_full_sampled():
+    """The multi-tenant prefill workload at full size (15 agents x 128 new tokens,
+    4096-token compressed prefix, 512-token fp16 tails), as the benchmark runs it;
+    sampled agents and tokens checked against the oracle."""
+    _need_gpu()
+    w = inputs.WORKLOADS["shared_prefill"]
+    D, Hkv, Hq, P, A, TL, n = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.n_agents, w.tail_len, w.n_new
+    cap = TL + n
+    outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
+    signs = inputs.tbq_signs(D)
+    kp = inputs.normal_tensor((1, P, Hkv, D), w.seed, "fp/k", outl)
+    vp = inputs.normal_tensor((1, P, Hkv, D), w.seed, "fp/v", outl)
+    kt = inputs.normal_tensor((A, Hkv, cap, D), w.seed, "ft/k", outl)
+    vt = inputs.normal_tensor((A, Hkv, cap, D), w.seed, "ft/v", outl)
+    kn = inputs.normal_tensor((A, n, Hkv, D), w.seed, "fn/k", outl)
+    vn = inputs.normal_tensor((A, n, Hkv, D), w.seed, "fn/v", outl)
+    q = inputs.normal_tensor((A, n, Hq, D), w.seed, "fn/q", outl, dtype="bfloat16", torch_out=True)
+    cache = ckv.PackedCache(D, Hkv, 1, P, signs)
+    ckv.kv_pack(cache, 0, torch.from_numpy(kp).to(DEV), torch.from_numpy(vp).to(DEV))
+    kt_d, vt_d = torch.from_numpy(kt).to(DEV), torch.from_numpy(vt).to(DEV)
+    out = torch.empty((A, n, Hq, D), dtype=torch.float32, device=DEV)
+    lse = torch.empty((A, n, Hq), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(ckv.attn_prefill_shared_workspace(cache, A, cap, n, Hq), dtype=torch.uint8, device=DEV)
+    sl = torch.full((A,), cap, dtype=torch.int32, device=DEV)
+    ckv.attn_prefill_shared(cache, P, kt_d, vt_d, sl, q.to(DEV), torch.from_numpy(kn).to(DEV),
+                            torch.from_numpy(vn).to(DEV), 1.0 / math.sqrt(D), out, lse, ws)
+    torch.cuda.synchronize()
+    assert ckv.read_device_flag(ws) == 0
+    qs, d16, codes, n16, _ = H.oracle_quantize(np.swapaxes(kp[0], 0, 1), np.swapaxes(vp[0], 0, 1), signs)
+    kh, vh = O.q8_0_dequantize(qs, d16), O.tbq3_dequantize(codes, n16, signs)
+    qf = q.float().numpy().astype(np.float64)
+    o_gpu, l_gpu = out.cpu().numpy(), lse.cpu().numpy()
+    for a in (0, 7, A - 1):
+        ka, va = kt[a].astype(np.float64), vt[a].astype(np.float64)
+        ka[:, TL:] = np.swapaxes(kn[a], 0, 1)
+        va[:, TL:] = np.swapaxes(vn[a], 0, 1)
+        rows = [0, 1, 63, n - 1]
+        o_ref, l_ref = O.shared_prefill_reference(qf[a], kh, vh, ka, va, cap, 1.0 / math.sqrt(D))
+        H.check_attention(o_gpu[a, rows], l_gpu[a, rows], o_ref[rows], l_ref[rows], f"shared full a={a}")
