@@ -24,13 +24,70 @@ struct FDec : DecodeShape<D> {
   static constexpr int SMEM = OFF_ML + Sh::NP * 16 * 4;
 };
 
-template <int D>
+// Epilogue of the row-parallel form: group q holds the 8 rows of row group
+// rg0 + q. Each group stores its accumulators and (m, l) as in the split
+// epilogue; warp r < 8 then writes row r of every group, divided by its sum.
+template <typename C>
+__device__ __forceinline__ void rows_epilogue(const DecodeArgs& a, SoftmaxState st, float (&acc)[C::MT_W][4],
+                                              float* red, float* mlbuf, int group, int wh, int warp, int lane, int b,
+                                              int kvh, int rg0) {
+  using Sh = typename C::Sh;
+  constexpr int D = Sh::DIM;
+  const int g = lane >> 2, t = lane & 3;
+  st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 4);
+  st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 8);
+  st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 16);
+  st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 4);
+  st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 8);
+  st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 16);
+  if (wh == 0 && lane < 4) {
+    mlbuf[group * 16 + (2 * t) * 2 + 0] = st.m0;
+    mlbuf[group * 16 + (2 * t) * 2 + 1] = st.l0;
+    mlbuf[group * 16 + (2 * t + 1) * 2 + 0] = st.m1;
+    mlbuf[group * 16 + (2 * t + 1) * 2 + 1] = st.l1;
+  }
+  float* myred = red + group * Sh::RED_FLOATS;
+#pragma unroll
+  for (int i = 0; i < C::MT_W; ++i) {
+    const int pd = Sh::GD * g + 2 * (wh * C::MT_W + i) + 2 * Sh::PS * g;
+    *reinterpret_cast<float2*>(myred + (2 * t) * Sh::RP + pd) = make_float2(acc[i][0], acc[i][2]);
+    *reinterpret_cast<float2*>(myred + (2 * t + 1) * Sh::RP + pd) = make_float2(acc[i][1], acc[i][3]);
+  }
+  named_bar(1, Sh::NCW * 32);
+  if (warp >= 8) return;
+  const int r = warp;
+  for (int q = 0; q < Sh::NP; ++q) {
+    float* orow;
+    float* lrow;
+    row_outputs(a, b, kvh, rg0 + q, r, &orow, &lrow);
+    if (rg0 + q >= a.n_row_groups || !orow) continue;
+    const float m = mlbuf[q * 16 + r * 2], l = mlbuf[q * 16 + r * 2 + 1];
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    float2* o2 = reinterpret_cast<float2*>(orow) + lane;
+#pragma unroll
+    for (int e = 0; e < D / 64; ++e) {
+      const int d = 64 * e + 2 * lane;
+      const float2 y = *reinterpret_cast<const float2*>(red + q * Sh::RED_FLOATS + r * Sh::RP + d +
+                                                        2 * Sh::PS * (d / Sh::GD));
+      o2[32 * e] = make_float2(y.x * inv, y.y * inv);
+    }
+    if (lane == 0) *lrow = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+// ROWS: the NP tile groups of a CTA take NP different row groups over the
+// same tiles instead of splitting one row group's tiles (one split): each
+// tile is then fetched from L2 once per CTA and served to the other groups
+// from L1, which matters when many query rows share a short sequence (a
+// prefill over a private fp16 tail). Each group writes its rows directly.
+template <int D, bool ROWS>
 __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(DecodeArgs a) {
   using C = FDec<D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
-  const int split = blockIdx.x, rg = blockIdx.y, bh = blockIdx.z;
+  const int split = blockIdx.x, bh = blockIdx.z;
+  const int rg = ROWS ? blockIdx.y * C::NP + warp / C::WT : blockIdx.y;
   const int b = bh / a.n_kv_heads, kvh = bh % a.n_kv_heads;
   const int group_q = a.n_q_heads / a.n_kv_heads;
   const int R = group_q * a.n_q;
@@ -51,9 +108,19 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   row_key_range(a, rg * 8 + 2 * t, seqlen, lo0, lim0);
   row_key_range(a, rg * 8 + 2 * t + 1, seqlen, lo1, lim1);
   const int64_t n_tiles = (seqlen + kTile - 1) / kTile;
-  const int64_t tile_begin = split * n_tiles / a.n_split;
-  const int64_t tile_end = (split + 1) * n_tiles / a.n_split;
-  const int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+  int64_t tile_begin = split * n_tiles / a.n_split;
+  int64_t tile_end = (split + 1) * n_tiles / a.n_split;
+  int n_iters = static_cast<int>((tile_end - tile_begin + C::NP - 1) / C::NP);
+  if constexpr (ROWS) {
+    // Every tile up to the last one any row of this group sees, one per iteration.
+    int hi = lim0 > lim1 ? lim0 : lim1;
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
+    tile_begin = 0;
+    tile_end = (hi + kTile - 1) / kTile;
+    if (tile_end > n_tiles) tile_end = n_tiles;
+    n_iters = static_cast<int>(tile_end);
+  }
   const __half* kb = a.k16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
   const __half* vb = a.v16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
 
@@ -84,7 +151,7 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   const int dbase = C::GD * g + 2 * wh * C::MT_W;  // first output dim of this lane's m-tiles
 
   for (int it = 0; it < n_iters; ++it) {
-    const int64_t tile = tile_begin + (int64_t)it * C::NP + group;
+    const int64_t tile = ROWS ? (int64_t)it : tile_begin + (int64_t)it * C::NP + group;
     if (tile >= tile_end) break;  // uniform across the warps of a group
     const int64_t tpos = tile * kTile;
     // ---- S^T = K Q^T ----
@@ -126,10 +193,15 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     }
   }
 
-  const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
-  decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
-                                           nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
-  decode_split_tail<D, C::RED_BYTES, C::THREADS>(a, split, gid, b, kvh, rg, tid, smem);
+  if constexpr (ROWS) {
+    rows_epilogue<C>(a, st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane, b, kvh,
+                     blockIdx.y * C::NP);
+  } else {
+    const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
+    decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
+                                             nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
+    decode_split_tail<D, C::RED_BYTES, C::THREADS>(a, split, gid, b, kvh, rg, tid, smem);
+  }
 }
 
 template <int D>
@@ -138,12 +210,29 @@ static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
   static bool configured = false;
   static int cap = 0;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_f16_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_f16_kernel<D, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_decode_f16_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_split_decode(attn_decode_f16_kernel<D>, a, C::THREADS, C::SMEM, &cap, stream);
+  if (a.n_split == 1 && a.n_row_groups >= C::NP) {
+    // Row-parallel CTAs: NP row groups each, no split merge.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, (a.n_row_groups + C::NP - 1) / C::NP, a.batch * a.n_kv_heads);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_decode_f16_kernel<D, true>, a);
+  }
+  return launch_split_decode(attn_decode_f16_kernel<D, false>, a, C::THREADS, C::SMEM, &cap, stream);
 }
 
 // Copy n_new rows per sequence into dense fp16 caches [batch][n_kv_heads]

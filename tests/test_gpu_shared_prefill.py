@@ -66,8 +66,11 @@ def _tails(D, Hkv, A, cap, lens, seed):
     return k, v, outl
 
 
-@pytest.mark.parametrize("D,Hkv,Hq,n_new", [(128, 2, 16, 20), (512, 2, 16, 7), (64, 1, 2, 33)])
-def test_prefill_f16_is_causal_over_the_tail(D, Hkv, Hq, n_new):
+@pytest.mark.parametrize("D,Hkv,Hq,n_new", [(128, 2, 16, 20), (512, 2, 16, 7), (64, 1, 2, 33), (256, 1, 8, 3)])
+# n_split 0 runs row-parallel CTAs (several row groups per CTA, no split);
+# 3 forces the split-K form with its merge.
+@pytest.mark.parametrize("n_split", [0, 3])
+def test_prefill_f16_is_causal_over_the_tail(D, Hkv, Hq, n_new, n_split):
     _need_gpu()
     A, cap = 3, 96
     lens = [90, n_new, 5]                       # the last tail is shorter than the new batch
@@ -75,10 +78,11 @@ def test_prefill_f16_is_causal_over_the_tail(D, Hkv, Hq, n_new):
     q = inputs.normal_tensor((A, n_new, Hq, D), 96 + D, "tl/q", outl, dtype="bfloat16", torch_out=True)
     out = torch.empty((A, n_new, Hq, D), dtype=torch.float32, device=DEV)
     lse = torch.empty((A, n_new, Hq), dtype=torch.float32, device=DEV)
-    ws = torch.zeros(ckv.attn_decode_f16_workspace(D, Hkv, A, cap, n_new, Hq), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ckv.attn_decode_f16_workspace(D, Hkv, A, cap, n_new, Hq, n_split), dtype=torch.uint8,
+                     device=DEV)
     sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
     ckv.attn_prefill_f16(torch.from_numpy(k).to(DEV), torch.from_numpy(v).to(DEV), sl, cap, q.to(DEV),
-                         1.0 / math.sqrt(D), out, lse, ws)
+                         1.0 / math.sqrt(D), out, lse, ws, n_split=n_split)
     assert ckv.read_device_flag(ws) == 0
     qf = q.float().numpy().astype(np.float64)
     for a in range(A):
