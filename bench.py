@@ -192,8 +192,11 @@ class DecodeWork:
                 ckv.kv_pack(c, 0, k, v, stream=stream)
             self.k_new, self.v_new = k[:, T - 1:T].clone(), v[:, T - 1:T].clone()
             del k, v
-            self.out = torch.empty((B, self.n_q, Hq, D), dtype=torch.float32, device=dev)
-            self.lse = torch.empty((B, self.n_q, Hq), dtype=torch.float32, device=dev)
+            # out and lse live in one allocation, so that a step's result comes back in one copy
+            n_out = B * self.n_q * Hq * D
+            self.out_lse = torch.empty(n_out + B * self.n_q * Hq, dtype=torch.float32, device=dev)
+            self.out = self.out_lse[:n_out].view(B, self.n_q, Hq, D)
+            self.lse = self.out_lse[n_out:].view(B, self.n_q, Hq)
             ws_bytes = (ckv.attn_decode_dca_workspace(self.caches[0], T, Hq) if self.dca else
                         ckv.attn_decode_workspace(self.caches[0], T, self.n_q, Hq))
             self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
@@ -223,17 +226,23 @@ class DecodeWork:
 
     def e2e_setup(self):
         t = self.torch
-        # a verify batch or a DCA step sends only Q
+        # A verify batch or a DCA step sends only Q; an append sends Q and the new K/V row. The step's
+        # inputs sit in one pinned buffer and one device buffer (views), so they go over in one copy,
+        # and the result (out, lse) comes back in one.
         ins = (self.q,) if (self.n_q > 1 or self.dca) else (self.q, self.k_new, self.v_new)
-        self.h_in = [x.cpu().pin_memory() for x in ins]
-        self.d_in = [t.empty_like(x) for x in ins]
-        self.h_out = [t.empty(x.shape, dtype=x.dtype).pin_memory() for x in (self.out, self.lse)]
-        return (sum(x.numel() * x.element_size() for x in self.h_in),
-                sum(x.numel() * x.element_size() for x in self.h_out))
+        n_in = sum(x.numel() for x in ins)
+        self.h_in = t.empty(n_in, dtype=t.float16).pin_memory()
+        self.d_in_flat = t.empty(n_in, dtype=t.float16, device=self.q.device)
+        self.d_in, o = [], 0
+        for x in ins:
+            self.h_in[o:o + x.numel()].copy_(x.reshape(-1).cpu())
+            self.d_in.append(self.d_in_flat[o:o + x.numel()].view(x.shape))
+            o += x.numel()
+        self.h_out = t.empty(self.out_lse.shape, dtype=t.float32).pin_memory()
+        return n_in * 2, self.out_lse.numel() * 4
 
     def e2e_step(self, i):
-        for h, d in zip(self.h_in, self.d_in):
-            d.copy_(h, non_blocking=True)
+        self.d_in_flat.copy_(self.h_in, non_blocking=True)
         c = self.caches[i % self.n_rot]
         if self.dca:
             self.ckv.attn_decode_dca(c, self.seq, self.T, self.dca, self.d_in[0], self.scale, self.out, self.lse,
@@ -244,8 +253,7 @@ class DecodeWork:
         else:
             self.ckv.attn_decode_append(c, self.seq, self.T, self.d_in[1], self.d_in[2], self.d_in[0], self.scale,
                                         self.out, self.lse, self.ws, stream=self.stream)
-        self.h_out[0].copy_(self.out, non_blocking=True)
-        self.h_out[1].copy_(self.lse, non_blocking=True)
+        self.h_out.copy_(self.out_lse, non_blocking=True)
 
     def describe(self):
         return {"workload": self.w.name, "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
