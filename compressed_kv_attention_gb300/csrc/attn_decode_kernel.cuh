@@ -15,8 +15,9 @@
 //    A producer warp streams the split's tile records (16 tokens each, one
 //    contiguous bulk copy per stage of NP records) into a 4-stage shared-memory
 //    ring guarded by mbarriers; 8 consumer warps take one record each.
-//  * S^T = K_hat Q^T on tensor cores (mma.sync m16n8k16): the int8 codes turn
-//    into exact fp16 integers with two byte permutes and a subtraction, each
+//  * S^T = K_hat Q^T on tensor cores (mma.sync m16n8k16): the codes (bytes
+//    q + 128) turn into fp16 subnormals (q + 128) 2^-24 with two byte permutes
+//    per four codes (the 128 offset is removed through the accumulator), each
 //    32-dim block is multiplied into its own accumulator and scaled by its fp16
 //    scale (so K_hat = q * d16 is exact, never rounded to fp16).
 //  * P'^T = exp2(S - m) * norm / (fp16) and O^T += C^T P'^T where C holds the

@@ -239,10 +239,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return r;
 }
 
-// Four int8 codes (one 32-bit word) -> two fp16x2 holding the same integers
-// exactly: byte b becomes fp16 (1024 + (b ^ 0x80)) - 1152 = b.
-__device__ __forceinline__ void i8x4_to_half2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+// Four K codes (one 32-bit word, each the byte q + 128) -> two fp16x2 holding
+// the integers q exactly: byte u becomes fp16 (1024 + u) - 1152 = q.
+__device__ __forceinline__ void i8x4_to_half2x2(uint32_t u, uint32_t& lo, uint32_t& hi) {
   const uint32_t e = 0x64646464u;
   uint32_t x0, x1;
   asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(x0) : "r"(u), "r"(e));
@@ -254,13 +253,11 @@ __device__ __forceinline__ void i8x4_to_half2x2(uint32_t w, uint32_t& lo, uint32
   hi = *reinterpret_cast<uint32_t*>(&h1);
 }
 
-// Four int8 codes (one 32-bit word) -> two fp16x2 holding (q + 128) * 2^-24:
-// after flipping the sign bit each byte is q + 128 in [1, 255], and a byte in
-// the low half of an fp16 with a zero high half is exactly that many units of
-// the smallest subnormal. The constant 128 * 2^-24 per code is removed by
+// Four K codes (one 32-bit word, each the byte q + 128 in [1, 255]) -> two
+// fp16x2 holding (q + 128) * 2^-24: a byte in the low half of an fp16 with a
+// zero high half is exactly that many units of the smallest subnormal. The constant 128 * 2^-24 per code is removed by
 // starting the accumulator at -2^-17 times the sum of the other operand.
-__device__ __forceinline__ void i8x4_to_sub_half2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+__device__ __forceinline__ void i8x4_to_sub_half2x2(uint32_t u, uint32_t& lo, uint32_t& hi) {
   asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0u));
   asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0u));
 }

@@ -86,7 +86,7 @@ struct PositionCodes {
   static constexpr int E = D / 32;
   // Window words: the compact bits span [0, 4BE - 5B), shifted by up to 31.
   static constexpr int NW = (4 * B * E - 5 * B + 31 + 31) / 32;
-  uint8_t q[E];        // q8_0 codes
+  uint8_t q[E];        // q8_0 codes, offset by 128
   __half d16;          // scale of this lane's block
   __half n16;          // fp16 norm (same in every lane)
   uint32_t val[NW];    // V code bits of the window, aligned to stream word w0
@@ -142,7 +142,9 @@ __device__ __forceinline__ void quantise_loaded(const PositionInput<D>& in, int 
       q = copysignf(floorf(fabsf(r) + 0.5f), r);
       q = fminf(fmaxf(q, -127.0f), 127.0f);
     }
-    pc.q[e] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    // Stored offset by 128 (the byte q + 128): the readers then widen a code
+    // to fp16 with byte permutes alone.
+    pc.q[e] = static_cast<uint8_t>(static_cast<int8_t>(q)) ^ 0x80u;
   }
 
   // ---- V: B-bit TBQ ----

@@ -78,7 +78,7 @@ typedef enum {
  * ((b * n_kv_heads + h) * (capacity / 16) + t) * R. Inside a record
  * (p = position in the tile, i = dim, D = head_dim):
  *
- *   [0, 16D)       K q8_0 codes (int8). (p, i) is at
+ *   [0, 16D)       K q8_0 codes, each stored as the byte q + 128. (p, i) is at
  *                  ((i/32)*32 + L)*16 + (p/8)*8 + (i%8), L = 4*(p%8) + (i%32)/8.
  *   [16D, 17D)     K q8_0 scales (fp16), row-major [16][D/32].
  *   [17D, 17D+2bD) V codes, b bits each. With G = D/8, L = 4*(i/G) + (p%8)/2

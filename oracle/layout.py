@@ -11,7 +11,8 @@ token positions [16 t, 16 t + 16). With b bits per V code (b = 2, 3 or 4; 3 is
 the method's TBQ3) a record is 17 D + 2 b D + 32 bytes (D = head_dim; 23 D + 32
 at b = 3):
 
-  [0, 16D)      K codes. Element (p, i) (p = position in tile, i = dim) sits at
+  [0, 16D)      K codes, each stored as the byte q + 128 (offset binary; q in
+                [-127, 127]). Element (p, i) (p = position in tile, i = dim) sits at
                 ((i // 32) * 32 + L) * 16 + (p // 8) * 8 + (i % 8),
                 with lane L = 4 * (p % 8) + (i % 32) // 8.
   [16D, 17D)    K scales, fp16, [16][D/32] row-major: (p, block) at 16D + 2 (p D/32 + block).
@@ -104,7 +105,7 @@ def pack_records(qs, d16, codes, n16, capacity: int, bits: int = 3, groups: int 
     out = np.zeros((n_tiles, record_bytes(D, bits, groups)), dtype=np.uint8)
     kofs, sofs = k_code_offsets(D), k_scale_offsets(D)
     vbits, nofs = v_code_bits(D, bits), v_norm_offsets(D, bits, groups).reshape(TILE, groups)
-    qs_u8 = qs.view(np.uint8)
+    qs_u8 = qs.view(np.uint8) ^ np.uint8(0x80)
     d16_u8 = np.asarray(d16, dtype=np.float16).view(np.uint8).reshape(T, D // 32, 2)
     n16_u8 = np.asarray(n16, dtype=np.float16).view(np.uint8).reshape(T, groups, 2)
     codes = np.asarray(codes, dtype=np.uint8)
@@ -135,7 +136,7 @@ def unpack_records(records, T: int, D: int, bits: int = 3, groups: int = 1):
     for t in range(T):
         tile, p = divmod(t, TILE)
         rec = records[tile]
-        qs[t] = rec[kofs[p]].view(np.int8)
+        qs[t] = (rec[kofs[p]] ^ np.uint8(0x80)).view(np.int8)
         d16[t] = (rec[sofs[p]].astype(np.uint16) | (rec[sofs[p] + 1].astype(np.uint16) << 8)).view(np.float16)
         n16[t] = (rec[nofs[p]].astype(np.uint16) | (rec[nofs[p] + 1].astype(np.uint16) << 8)).view(np.float16)
         c = np.zeros(D, dtype=np.uint8)

@@ -118,7 +118,7 @@ def read_fields(records, D, T, bits: int = 3, groups: int = 1):
     vbits = LY.v_code_bits(D, bits)
     n_tiles = (T + 15) // 16
     rec = records[:n_tiles]
-    qs = rec[:, kofs].view(np.int8).reshape(n_tiles * 16, D)[:T]
+    qs = (rec[:, kofs] ^ np.uint8(0x80)).view(np.int8).reshape(n_tiles * 16, D)[:T]
     sc = (rec[:, sofs].astype(np.uint16) | (rec[:, sofs + 1].astype(np.uint16) << 8)).reshape(-1, D // 32)[:T]
     nm = (rec[:, nofs].astype(np.uint16) | (rec[:, nofs + 1].astype(np.uint16) << 8)).reshape(-1, groups)[:T]
     if groups == 1:
