@@ -300,7 +300,10 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
     int qi = 0, h = 0;
     const bool ok = rr < R;
     if (ok) row_to_query(rr, group_q, kvh, qi, h);
-    const __half* qrow = a.q + ((int64_t)(b * a.n_q + qi) * a.n_q_heads + h) * D;
+    // DCA: rows qi >= 2 are pieces of the inter regime and share its query (q holds 3 tokens).
+    const int q_tokens = DCA ? 3 : a.n_q;
+    const int q_src = (DCA && qi > 2) ? 2 : qi;
+    const __half* qrow = a.q + ((int64_t)(b * q_tokens + q_src) * a.n_q_heads + h) * D;
     load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
   }
 

@@ -218,7 +218,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
                              void* stream, const AppendRows* app = nullptr, int causal_q = 0,
-                             int dca_chunk = 0, int q_bf16 = 0) {
+                             int dca_chunk = 0, int q_bf16 = 0, int dca_parts = 0) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
   if (s != CKV_OK) return s;
@@ -266,6 +266,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.n_q_heads = n_q_heads;
   a.causal_q = causal_q;
   a.dca_chunk = dca_chunk;
+  a.dca_parts = dca_parts;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_split = p.n_split;
   a.n_row_groups = p.n_row_groups;
@@ -301,21 +302,47 @@ ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64
                     workspace, ws_bytes, stream);
 }
 
-// DCA decode workspace: the decode's (3 query rows per query head), then the
-// three regimes' partial outputs [batch][3][n_q_heads][D] and lse values.
-static size_t dca_ws_parts(const ckv_cache* cache, int n_q_heads, size_t* o_off, size_t* l_off) {
-  const size_t rows = static_cast<size_t>(cache->batch) * 3 * n_q_heads;
+// DCA: the inter regime's range, up to max_seq_len - 2 chunk keys, is cut into
+// pieces of about one chunk (1 to 14: the merge takes 16 parts), so that its
+// rows' CTAs carry about as many keys as the intra and successive regimes'.
+static int dca_parts_for(int64_t max_seq_len, int chunk) {
+  const int64_t inter = max_seq_len > 2LL * chunk ? max_seq_len - 2LL * chunk : 0;
+  int64_t m = (inter + chunk / 2) / chunk;
+  if (m < 1) m = 1;
+  if (m > 14) m = 14;
+  return static_cast<int>(m);
+}
+
+// DCA workspace: the decode's (2 + parts query rows per query head, one row
+// group each), then the rows' partial outputs [batch][2 + parts][n_q_heads][D]
+// and lse values.
+static size_t dca_ws_parts(const ckv_cache* cache, int n_rows_per_head, int n_q_heads, size_t* o_off,
+                           size_t* l_off) {
+  const size_t rows = static_cast<size_t>(cache->batch) * n_rows_per_head * n_q_heads;
   *o_off = 0;
   *l_off = (rows * cache->head_dim * sizeof(float) + 255) / 256 * 256;
   return *l_off + (rows * sizeof(float) + 255) / 256 * 256;
 }
 
-size_t ckv_attn_decode_dca_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q_heads,
-                                     int32_t n_split) {
-  const size_t dec = ckv_attn_decode_workspace(cache, max_seq_len, 3, n_q_heads, n_split);
+static size_t dca_ws_for(const ckv_cache* cache, int64_t max_seq_len, int n_q_heads, int n_split, int parts,
+                         size_t* dec_out) {
+  const size_t dec = ckv_attn_decode_workspace(cache, max_seq_len, 2 + parts, n_q_heads, n_split);
+  if (dec_out) *dec_out = dec;
   if (dec == 0) return 0;
   size_t o_off, l_off;
-  return (dec + 255) / 256 * 256 + dca_ws_parts(cache, n_q_heads, &o_off, &l_off);
+  return (dec + 255) / 256 * 256 + dca_ws_parts(cache, 2 + parts, n_q_heads, &o_off, &l_off);
+}
+
+size_t ckv_attn_decode_dca_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q_heads,
+                                     int32_t n_split) {
+  // Enough for any chunk: the largest need over the piece counts a call can choose.
+  size_t need = 0;
+  for (int parts = 1; parts <= 14; ++parts) {
+    const size_t w = dca_ws_for(cache, max_seq_len, n_q_heads, n_split, parts, nullptr);
+    if (w == 0) return 0;
+    need = w > need ? w : need;
+  }
+  return need;
 }
 
 ckv_status ckv_attn_decode_dca(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
@@ -325,38 +352,40 @@ ckv_status ckv_attn_decode_dca(const ckv_cache* cache, const int32_t* seq_len, i
   if (s != CKV_OK) return s;
   if (chunk < 1) return fail(CKV_ERR_INVALID_ARG, "chunk must be positive (got %d)", chunk);
   if (!out || !lse) return fail(CKV_ERR_INVALID_ARG, "null out/lse");
-  const size_t dec = ckv_attn_decode_workspace(cache, max_seq_len, 3, n_q_heads, n_split);
+  const int parts = dca_parts_for(max_seq_len, chunk);
+  const int n_rows = 2 + parts;
+  size_t dec = 0;
+  const size_t need = dca_ws_for(cache, max_seq_len, n_q_heads, n_split, parts, &dec);
   if (dec == 0) {
     // Invalid geometry: the decode's own checks give the status and message.
     return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
-                      cache->capacity, seq_len, max_seq_len, q_f16, 3, n_q_heads, scale, n_split, out, lse,
-                      workspace, ws_bytes, stream, nullptr, 0, chunk);
+                      cache->capacity, seq_len, max_seq_len, q_f16, n_rows, n_q_heads, scale, n_split, out, lse,
+                      workspace, ws_bytes, stream, nullptr, 0, chunk, 0, parts);
   }
-  const size_t need = ckv_attn_decode_dca_workspace(cache, max_seq_len, n_q_heads, n_split);
   s = check_ws(workspace, ws_bytes, need);
   if (s != CKV_OK) return s;
   size_t o_off, l_off;
-  dca_ws_parts(cache, n_q_heads, &o_off, &l_off);
-  uint8_t* parts = static_cast<uint8_t*>(workspace) + (dec + 255) / 256 * 256;
-  float* po = reinterpret_cast<float*>(parts + o_off);
-  float* pl = reinterpret_cast<float*>(parts + l_off);
-  // The three regimes as the three query tokens of one decode.
+  dca_ws_parts(cache, n_rows, n_q_heads, &o_off, &l_off);
+  uint8_t* pbase = static_cast<uint8_t*>(workspace) + (dec + 255) / 256 * 256;
+  float* po = reinterpret_cast<float*>(pbase + o_off);
+  float* pl = reinterpret_cast<float*>(pbase + l_off);
+  // The regimes (the inter one in pieces) as the query tokens of one decode.
   s = run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
-                 cache->capacity, seq_len, max_seq_len, q_f16, 3, n_q_heads, scale, n_split, po, pl, workspace,
-                 dec, stream, nullptr, 0, chunk);
+                 cache->capacity, seq_len, max_seq_len, q_f16, n_rows, n_q_heads, scale, n_split, po, pl, workspace,
+                 dec, stream, nullptr, 0, chunk, 0, parts);
   if (s != CKV_OK) return s;
   const int D = cache->head_dim;
   ckv::LseMergeArgs m{};
-  for (int r = 0; r < 3; ++r) {
+  for (int r = 0; r < n_rows; ++r) {
     m.o[r] = po + static_cast<size_t>(r) * n_q_heads * D;
     m.l[r] = pl + static_cast<size_t>(r) * n_q_heads;
   }
-  m.n_parts = 3;
+  m.n_parts = n_rows;
   m.n_rows = static_cast<int64_t>(cache->batch) * n_q_heads;
   m.d = D;
   m.rows_per_group = n_q_heads;
-  m.o_group_stride = 3LL * n_q_heads * D;
-  m.l_group_stride = 3LL * n_q_heads;
+  m.o_group_stride = static_cast<int64_t>(n_rows) * n_q_heads * D;
+  m.l_group_stride = static_cast<int64_t>(n_rows) * n_q_heads;
   m.out = out;
   m.lse = lse;
   const cudaError_t e = ckv::launch_lse_merge(m, static_cast<cudaStream_t>(stream));

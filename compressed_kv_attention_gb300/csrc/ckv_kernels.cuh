@@ -49,7 +49,8 @@ struct DecodeArgs {
   int q_bf16;                // fp16 decode only: q holds bf16 values (converted exactly on load)
   int n_q, n_q_heads;
   int causal_q;              // 1: query token qi sees [0, seq_len - n_q + qi + 1) (verify batch)
-  int dca_chunk;             // > 0: the n_q = 3 query tokens are the DCA regimes (decode_common.cuh)
+  int dca_chunk;             // > 0: dual chunk attention regimes as query rows (decode_common.cuh)
+  int dca_parts;             // DCA: the inter regime's range is split into this many rows (n_q = 2 + parts)
   float scale_log2;          // logit scale * log2(e)
   int n_split, n_row_groups;
   float* part;

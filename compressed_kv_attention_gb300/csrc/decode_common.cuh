@@ -310,9 +310,12 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
 //  * causal_q (a verify batch: the n_q tokens are the last n_q positions):
 //    [0, seqlen - n_q + qi + 1);
 //  * dca_chunk = c (dual chunk attention of the query at position
-//    i = seqlen - 1, chunk k = i / c; token qi is the regime): intra
-//    [k c, seqlen), successive [(k - 1) c, k c), inter [0, (k - 1) c) — the
-//    three partition [0, seqlen) (DCA page, "Section C design").
+//    i = seqlen - 1, chunk k = i / c): intra [k c, seqlen) (qi = 0),
+//    successive [(k - 1) c, k c) (qi = 1), inter [0, (k - 1) c) — the three
+//    partition [0, seqlen) (DCA page, "Section C design"). The inter range is
+//    cut into dca_parts equal pieces, rows qi = 2 .. 1 + dca_parts (all with
+//    the inter query), so that its CTAs carry no more keys than the others;
+//    the exact merge of the pieces is the inter regime's attention.
 __device__ __forceinline__ void row_key_range(const DecodeArgs& a, int rr, int seqlen, int& lo, int& hi) {
   const int qi = rr / (a.n_q_heads / a.n_kv_heads);
   lo = 0;
@@ -329,7 +332,10 @@ __device__ __forceinline__ void row_key_range(const DecodeArgs& a, int rr, int s
       lo = k >= 1 ? (k - 1) * c : 0;
       hi = k >= 1 ? k * c : 0;
     } else {
-      hi = k >= 2 ? (k - 1) * c : 0;
+      const int64_t L = k >= 2 ? (int64_t)(k - 1) * c : 0;
+      const int m = a.dca_parts > 0 ? a.dca_parts : 1, p = qi - 2;
+      lo = static_cast<int>(p * L / m);
+      hi = static_cast<int>((p + 1) * L / m);
     }
   }
 }

@@ -219,9 +219,13 @@ CKV_API ckv_status ckv_attn_decode_verify(const ckv_cache* cache, const int32_t*
  * roped once), and their softmaxes are merged exactly by log-sum-exp.
  * q_f16: fp16 [batch][3][n_q_heads][D]; out: float32 [batch][n_q_heads][D];
  * lse: float32 [batch][n_q_heads]. chunk >= 1. Two launches: the decode
- * kernel with the regimes as its three query rows (each row group reads only
- * its regime's tiles) and the merge. workspace:
- * ckv_attn_decode_dca_workspace() bytes, zero-filled before first use.
+ * kernel with the regimes as its query rows (each row group reads only its
+ * regime's tiles; the inter range is cut into m equal pieces of about one
+ * chunk, m = clamp(round((max_seq_len - 2 chunk) / chunk), 1, 14), rows that
+ * all use the inter query, so that no regime's CTAs carry more keys than the
+ * others) and the exact merge of the 2 + m rows. workspace:
+ * ckv_attn_decode_dca_workspace() bytes (enough for any chunk), zero-filled
+ * before first use.
  */
 CKV_API size_t ckv_attn_decode_dca_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q_heads,
                                              int32_t n_split);

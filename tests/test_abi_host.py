@@ -115,8 +115,10 @@ def test_dca_and_verify_argument_checks(lib):
     fake = 0x7f0000000000
     c = _fake_cache(D=512, Hkv=2, cap=4096)
     need = lib.ckv_attn_decode_dca_workspace(ctypes.byref(c), 4096, 16, 8)
-    dec = lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 3, 16, 8)
-    assert need > dec > 0                           # the decode's workspace plus the three regimes' partials
+    # the decode's workspace for 2 + m regime rows plus their partials, for any piece count m in [1, 14]
+    for m in (1, 14):
+        dec = lib.ckv_attn_decode_workspace(ctypes.byref(c), 4096, 2 + m, 16, 8)
+        assert need > dec > 0
     call = lambda chunk=64, hq=16, ws=fake, wsb=need: lib.ckv_attn_decode_dca(
         ctypes.byref(c), fake, 4096, chunk, fake, hq, 0.04, 8, fake, fake, ws, wsb, None)
     assert call(chunk=0) == -1
