@@ -15,8 +15,16 @@ Other workloads (`--workload`), one line each:
                    120-row pass per kv head), a private 512-token fp16 tail per
                    agent, the two partials merged by log-sum-exp
   tiny_decode      1 kv head, 4 query heads, head_dim 128, 256 tokens
+  verify_decode    a verify batch of 4 drafted tokens over 32768 tokens
+  dca_decode       dual chunk attention decode, 32768 tokens, chunk 8192
+  long_decode_tbq2, long_decode_tbq4, long_decode_rot
+                   long_decode with 2- or 4-bit V codes, or with the
+                   block-diagonal rotation (128-dim groups, two sign diagonals)
   chunked_prefill  2048 new query tokens over 32768 cached ones (pack the new
                    rows, causal attention on tcgen05); tensor roofline
+  chunked_prefill_rot  the same over a cache with the block-diagonal rotation
+  shared_prefill   15 agents prefill 128 tokens each over one 4096-token
+                   compressed prefix plus their private 512-token fp16 tails
   kv_pack          packing 2048 tokens x 2 kv heads of fp16 K/V
 
 --impl reference times the float64 oracle (dequantise to dense, then softmax
@@ -46,7 +54,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (read + write) of one decode-kernel launch on gemma4_decode from
 # one ncu capture, valid for the kernel sources whose hash is recorded beside it
 # (null once they change).
-NCU_TRAFFIC = {"bytes": 48513280, "source_sha": "36c208789993a3e4"}
+NCU_TRAFFIC = {"bytes": 48513536, "source_sha": "08e02f7ea6b9039d"}
 
 
 def _args():
@@ -58,7 +66,7 @@ def _args():
     p.add_argument("--workload", default="gemma4_decode",
                    choices=["gemma4_decode", "long_decode", "fanout_decode", "tiny_decode", "chunked_prefill",
                             "kv_pack", "verify_decode", "dca_decode", "long_decode_tbq2", "long_decode_tbq4",
-                            "long_decode_rot", "shared_prefill"])
+                            "long_decode_rot", "shared_prefill", "chunked_prefill_rot"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -382,13 +390,13 @@ class PrefillWork:
 
     graph = False  # long steps: launched eagerly, L2 flushed before each timed step
 
-    def __init__(self, dev, stream):
+    def __init__(self, name, dev, stream):
         import torch
         import compressed_kv_attention_gb300 as ckv
         from compressed_kv_attention_gb300 import inputs
         self.ckv, self.torch, self.stream = ckv, torch, stream
-        w = inputs.WORKLOADS["chunked_prefill"]
-        self.w = w
+        w = inputs.WORKLOADS[name]
+        self.w, self.name = w, name
         D, Hkv, Hq, nc, nn = w.head_dim, w.n_kv_heads, w.n_q_heads, w.seq_len, w.n_new
         self.D, self.Hkv, self.Hq, self.nc, self.nn = D, Hkv, Hq, nc, nn
         outl = inputs.outlier_channels(D, w.n_outliers, w.seed)
@@ -397,7 +405,9 @@ class PrefillWork:
             k = inputs.normal_tensor((1, nc + nn, Hkv, D), w.seed, "k", outl, device=str(dev))
             v = inputs.normal_tensor((1, nc + nn, Hkv, D), w.seed, "v", outl, device=str(dev))
             self.q = inputs.normal_tensor((1, nn, Hq, D), w.seed, "q", outl, device=str(dev), dtype="bfloat16")
-            self.cache = ckv.PackedCache(D, Hkv, 1, nc + nn, inputs.tbq_signs(D), device=dev)
+            signs2 = inputs.tbq_signs(D, seed=43) if w.rot_group else None
+            self.cache = ckv.PackedCache(D, Hkv, 1, nc + nn, inputs.tbq_signs(D), device=dev, v_bits=w.v_bits,
+                                         signs2=signs2)
             ckv.kv_pack(self.cache, 0, k[:, :nc].contiguous(), v[:, :nc].contiguous(), stream=stream)
             self.kn, self.vn = k[:, nc:].contiguous(), v[:, nc:].contiguous()
             del k, v
@@ -442,15 +452,17 @@ class PrefillWork:
         self.h_out[1].copy_(self.lse, non_blocking=True)
 
     def describe(self):
-        return {"workload": "chunked_prefill", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
-                "cached_tokens": self.nc, "new_tokens": self.nn, "q_dtype": "bf16",
+        return {"workload": self.name, "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
+                "cached_tokens": self.nc, "new_tokens": self.nn, "q_dtype": "bf16", "v_bits": self.w.v_bits,
+                "rotation": "128-dim groups, two sign diagonals" if self.w.rot_group else "full D-point",
                 "step": "attn_prefill (pack 2048 rows + causal attention + de-rotation)",
                 "l2": f"flushed before each step ({2 * self.l2 / 1e6:.0f} MB write)"}
 
     def roofline(self, kernel_ms, peaks):
         _, tf, kind = peaks
         achieved = self.flops / (kernel_ms / 1e3) / 1e12
-        return {"bound": "tensor", "kernel": "attn_prefill_kernel<512> (+ pack, de-rotation) on tcgen05",
+        kern = f"attn_prefill_kernel<{self.D}, {self.w.v_bits}, {bool(self.w.rot_group)}>"
+        return {"bound": "tensor", "kernel": kern + " (+ pack, de-rotation) on tcgen05",
                 "achieved": round(achieved, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(achieved / tf, 4),
                 "peak_kind": kind + " bf16 dense (fp16 operands run at the same rate)", "traffic": None,
                 "algorithmic_flops": self.flops, "launch_ms": round(kernel_ms, 6)}
@@ -612,8 +624,8 @@ def _make_work(name, dev, stream):
         return DecodeWork(name, dev, stream)
     if name == "fanout_decode":
         return FanoutWork(dev, stream)
-    if name == "chunked_prefill":
-        return PrefillWork(dev, stream)
+    if name in ("chunked_prefill", "chunked_prefill_rot"):
+        return PrefillWork(name, dev, stream)
     if name == "shared_prefill":
         return SharedPrefillWork(dev, stream)
     return PackWork(dev, stream)

@@ -172,12 +172,17 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
                                      pb1, pl);
     // ---- O^T += V^T P^T: lane reads positions 2t, 2t+1, 2t+8, 2t+9 ----
     const __half* vp = vb + tpos * D + dbase;
+    // Rows at or past seq_len may hold any bytes (a NaN there would reach O
+    // through P = 0): they enter as zero.
+    const int64_t vrem = seqlen - tpos;
+    const bool ve0 = 2 * t < vrem, vo0 = 2 * t + 1 < vrem, ve1 = 2 * t + 8 < vrem, vo1 = 2 * t + 9 < vrem;
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int c4 = 0; c4 < C::MT_W / 4; ++c4) {
-      const uint4 e0 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t) * D + c4 * 8));
-      const uint4 o0 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 1) * D + c4 * 8));
-      const uint4 e1 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 8) * D + c4 * 8));
-      const uint4 o1 = __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 9) * D + c4 * 8));
+      const uint4 e0 = ve0 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t) * D + c4 * 8)) : z4;
+      const uint4 o0 = vo0 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 1) * D + c4 * 8)) : z4;
+      const uint4 e1 = ve1 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 8) * D + c4 * 8)) : z4;
+      const uint4 o1 = vo1 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 9) * D + c4 * 8)) : z4;
       const uint32_t we[4] = {e0.x, e0.y, e0.z, e0.w}, wo[4] = {o0.x, o0.y, o0.z, o0.w};
       const uint32_t xe[4] = {e1.x, e1.y, e1.z, e1.w}, xo[4] = {o1.x, o1.y, o1.z, o1.w};
 #pragma unroll

@@ -490,6 +490,12 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
         const uint32_t nb = rb + v_norm_offset(D, B) + 2 * (16 * ((D / 8) * (lane >> 2) / kRotGroup) + 2 * (lane & 3));
         nA = lds32(nb);
         nB = lds32(nb + 16);
+        // Positions at or past seq_len may hold any bytes (a NaN norm would
+        // reach O through P' = 0): their norms enter as zero. r >= 10 on every
+        // tile but a sequence's last.
+        const int r = seqlen - static_cast<int>(tpos) - 2 * (lane & 3);
+        nA &= r >= 2 ? 0xffffffffu : r == 1 ? 0xffffu : 0u;
+        nB &= r >= 10 ? 0xffffffffu : r == 9 ? 0xffffu : 0u;
       } else {
         n0 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D, B) + 2 * g)));
         n1 = __half2float(__ushort_as_half((unsigned short)lds16(rb + v_norm_offset(D, B) + 2 * (g + 8))));

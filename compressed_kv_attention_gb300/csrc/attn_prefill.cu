@@ -62,23 +62,28 @@ struct PrefillArgs {
   int32_t* tile_split;
 };
 
-__constant__ float kPrefillCentroids[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
-                                           0.2451f,  0.7560f,  1.3439f,  2.1520f};
-
-template <int D>
+// B: bits per V code (2, 3 or 4). ROT: the block-diagonal rotation (one V
+// norm per 128-dim group and position; the norms then scale the centroids in
+// C^T instead of entering P').
+template <int D, int B, bool ROT>
 struct PCfg {
   static constexpr int M = 128;                  // query rows per CTA
   static constexpr int NKV = 64;                 // cached tokens per step
   static constexpr int NB = D / 32;              // q8_0 blocks per vector
   static constexpr int OT = D < 448 ? D : 448;   // output dims accumulated in TMEM
   static constexpr int OR = D - OT;              // output dims summed in registers (0 or 64)
-  static constexpr int REC = record_bytes(D);
+  static constexpr int NG = ROT ? D / kRotGroup : 1;
+  static constexpr int REC = record_bytes(D, B, NG);
+  // Value table: 3 bits, 64 entries, one per 6-bit field (a pair of codes);
+  // 2 bits, 16 entries per 4-bit field; 4 bits, 16 entries, one per code
+  // (two loads per field).
+  static constexpr int LUT_N = B == 3 ? 64 : 16;
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = M * D * 2;                 // K_hat hi, then lo, then C^T
   static constexpr int P_OFF = KV_OFF + NKV * D * 2;
   static constexpr int NORM_OFF = P_OFF + M * NKV * 2;
-  static constexpr int LUT_OFF = NORM_OFF + NKV * 4;        // 64 centroid pairs x 32 lanes
-  static constexpr int SCALE_OFF = LUT_OFF + 64 * 32 * 4; // two steps' q8_0 scales
+  static constexpr int LUT_OFF = NORM_OFF + NKV * 4;        // LUT_N table words x 32 lanes
+  static constexpr int SCALE_OFF = LUT_OFF + LUT_N * 32 * 4; // two steps' q8_0 scales
   // Up to head dim 128, P' enters the P.V product as the fp16 pair hi (P_OFF)
   // + lo (P_LO_OFF): fp16 rounding of P' alone costs up to 2.7e-3 of |o|_inf
   // at head dim 64 over long rows (2.1e-3 at 128; 1.4e-3 at 256, 8e-4 at 512).
@@ -99,9 +104,9 @@ struct OChunk {
 
 }  // namespace
 
-template <int D>
+template <int D, int B, bool ROT>
 __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
-  using C = PCfg<D>;
+  using C = PCfg<D, B, ROT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_bar;
@@ -121,6 +126,10 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   const int QT = C::M / group_q;  // query tokens per tile
   const int n_qt = (a.n_new + QT - 1) / QT;
   const int64_t n_rec = a.capacity / kTile;
+  // Positions [0, kv_lim) hold packed rows; the ones after it in the last
+  // step may hold any bytes, so their V norms enter as zero (a NaN there
+  // would reach O through P' = 0).
+  const int64_t kv_lim = a.prefix_only ? a.n_cached : a.n_cached + a.n_new;
   // 64-key steps of query tile qt: its rows see keys [0, n_cached + last row]
   // (prefix_only: [0, n_cached)).
   auto steps_of = [&](int qt) {
@@ -140,12 +149,19 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     s_abort = 0;
     fence_barrier_init();
   }
-  // Centroid pairs: entry f (6 bits) = fp16x2(c[f & 7], c[f >> 3]) / kCentroidScale,
-  // one copy per lane (the de-rotation multiplies the scale back).
-  for (int e = tid; e < 64 * 32; e += C::THREADS) {
+  // Value table, one copy per lane, in units of the tier's centroid scale
+  // (the de-rotation multiplies it back). 3 bits: entry f (6 bits) =
+  // fp16x2(c[f & 7], c[f >> 3]); 2 bits: entry f (4 bits) = fp16x2(c[f & 3],
+  // c[f >> 2]); 4 bits: entry k = fp16x2(c[k], c[k]).
+  for (int e = tid; e < C::LUT_N * 32; e += C::THREADS) {
     const int f = e >> 5;
-    sLut[e] = pack_half2(kPrefillCentroids[f & 7] * (1.0f / kCentroidScale),
-                         kPrefillCentroids[f >> 3] * (1.0f / kCentroidScale));
+    constexpr float inv = 1.0f / centroid_scale(B);
+    if constexpr (B == 3)
+      sLut[e] = pack_half2(tbq_centroid<3>(f & 7) * inv, tbq_centroid<3>(f >> 3) * inv);
+    else if constexpr (B == 2)
+      sLut[e] = pack_half2(tbq_centroid<2>(f & 3) * inv, tbq_centroid<2>(f >> 2) * inv);
+    else
+      sLut[e] = pack_half2(tbq_centroid<4>(f) * inv, tbq_centroid<4>(f) * inv);
   }
   tc_fence_before();
   __syncthreads();
@@ -219,7 +235,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   //  V: threads 128..255; warp w takes lane streams [8w, 8w + 8) of the
   //     step's 4 records (lane = 8 * record + stream), which spreads one
   //     store instruction over 16 banks.
-  constexpr int G = D / 8, LB = 3 * D / 16, GR = v_granule(D), NW = LB / 4;
+  constexpr int G = D / 8, LB = v_lane_bytes(D, B), GR = v_granule(D, B), NW = LB / 4;
   constexpr int KR = 4 * D / C::THREADS;    // code chunks per thread per step
   constexpr int NSW = C::NKV * C::NB / 4;   // 8-byte scale words per step
   constexpr int VPRE = G;                   // value fields whose table loads overlap the second S pass
@@ -247,18 +263,31 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
                                                           2 * (h0 % (kTile * C::NB)))
                         : make_uint2(0, 0);
     }
-    if (tid < C::NKV) {
+    if (!ROT && tid < C::NKV) {
       const int64_t rec = rec0 + tid / kTile;
-      nrm = (rec < n_rec) ? __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D) +
-                                                                          2 * (tid % kTile)))
-                          : 0.0f;
+      nrm = (rec < n_rec && rec0 * kTile + tid < kv_lim)
+                ? __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D, B) +
+                                                                2 * (tid % kTile)))
+                : 0.0f;
     }
   };
   // V codes of a step (value warps), loaded once the previous step's build
-  // has consumed them.
-  auto fetch_v = [&](uint32_t (&vw)[NW], int step) {
+  // has consumed them. ROT: also the thread's group norms of positions
+  // (p0, p0 + 1) and (p0 + 8, p0 + 9), p0 = 2 (vL & 3), as fp16 pairs (its
+  // dims [G (vL >> 2), + G) lie in one 128-dim group).
+  auto fetch_v = [&](uint32_t (&vw)[NW], uint32_t (&vn)[2], int step) {
     const uint8_t* stream = s_stream;
     const int64_t rec0 = (int64_t)step * (C::NKV / kTile);
+    if constexpr (ROT) {
+      const int64_t rec = rec0 + vr4;
+      const int p0 = 2 * (vL & 3), grp = G * (vL >> 2) / kRotGroup;
+      const uint8_t* nb = stream + rec * C::REC + v_norm_offset(D, B) + 2 * (kTile * grp + p0);
+      const int64_t r = kv_lim - rec * kTile - p0;  // positions p0 + i with i < r hold rows
+      vn[0] = (rec < n_rec && r > 0) ? *reinterpret_cast<const uint32_t*>(nb) & (r >= 2 ? 0xffffffffu : 0xffffu)
+                                     : 0u;
+      vn[1] = (rec < n_rec && r > 8) ? *reinterpret_cast<const uint32_t*>(nb + 16) & (r >= 10 ? 0xffffffffu : 0xffffu)
+                                     : 0u;
+    }
     {
       const int64_t rec = rec0 + vr4;
       const uint8_t* vb = stream + rec * C::REC + v_code_offset(D);
@@ -288,22 +317,34 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     if (tid < NSW) *reinterpret_cast<uint2*>(sScale + buf * C::NKV * C::NB + tid * 4) = ksc;
   };
 
-  // C^T (centroids, rotated basis): rows = dims, K = tokens. A 6-bit field
-  // pairs the codes of two adjacent positions of one dim, which is one fp16x2
-  // word of C^T: one shared table load per field (v_field), one store (v_store).
+  // C^T (centroids, rotated basis): rows = dims, K = tokens. A field of 2B
+  // bits pairs the codes of two adjacent positions of one dim (the even
+  // position in the low bits), which is one fp16x2 word of C^T: one table
+  // load per field at 2 and 3 bits, two at 4 bits (v_field), one store
+  // (v_store). ROT: the word is scaled by the positions' group norms.
   const uint32_t v_lut = smem_u32(sLut) + (uint32_t)(lane << 2);
   const int v_g = vL >> 2, v_tok0 = vr4 * 16 + 2 * (vL & 3);
   auto v_field = [&](const uint32_t (&vc)[NW], int pi) -> uint32_t {
-    const int bit = 6 * pi;
-    const int wi = bit >> 5, sh = bit & 31;
-    uint32_t f = vc[wi] >> sh;
-    if (sh > 26 && wi + 1 < NW) f |= vc[wi + 1] << (32 - sh);
-    return lds32(v_lut + ((f & 63u) << 7));
+    if constexpr (B == 3) {
+      const int bit = 6 * pi;
+      const int wi = bit >> 5, sh = bit & 31;
+      uint32_t f = vc[wi] >> sh;
+      if (sh > 26 && wi + 1 < NW) f |= vc[wi + 1] << (32 - sh);
+      return lds32(v_lut + ((f & 63u) << 7));
+    } else if constexpr (B == 2) {
+      const uint32_t f = (vc[pi >> 3] >> (4 * (pi & 7))) & 15u;
+      return lds32(v_lut + (f << 7));
+    } else {
+      const uint32_t f = (vc[pi >> 2] >> (8 * (pi & 3))) & 255u;
+      const uint32_t lo = lds32(v_lut + ((f & 15u) << 7)), hi = lds32(v_lut + ((f >> 4) << 7));
+      return __byte_perm(lo, hi, 0x7610);  // (c[even], c[odd])
+    }
   };
-  auto v_store = [&](int pi, uint32_t val) {
+  auto v_store = [&](int pi, uint32_t val, const uint32_t (&vn)[2]) {
     const int mt = pi >> 2, rh = pi & 1, h2 = (pi >> 1) & 1;
     const int dim = G * v_g + 2 * mt + rh;
     const int tok = v_tok0 + 8 * h2;  // even position; the odd one follows it in K
+    if constexpr (ROT) val = hmul2_u32(val, vn[h2]);
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(sKV) + sw128_offset(dim, tok, D)), "r"(val));
   };
 
@@ -319,8 +360,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
 #pragma unroll
     for (int i = 0; i < (SM && C::OR > 0 ? C::OR : 1); ++i) otail[i] = 0.0f;
     uint32_t vw[SM ? 1 : NW];
+    uint32_t vn[2] = {0u, 0u};
     if constexpr (!SM) {
-      if (s_s0 < s1) fetch_v(vw, s_s0);
+      if (s_s0 < s1) fetch_v(vw, vn, s_s0);
     }
     for (int step = s_s0; step < s1; ++step) {
       const int64_t j0 = (int64_t)step * C::NKV;
@@ -354,7 +396,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
               make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
       }
-      if (tid < C::NKV) sNorm[tid] = nrm;
+      if (!ROT && tid < C::NKV) sNorm[tid] = nrm;
       sync_for_mma();
       if (SM && tid == 0) {
         // First pass of S overwrites the accumulator (columns [0, 64)).
@@ -442,7 +484,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
         float ps = 0.0f;
         uint32_t pw[C::NKV / 2];
-        uint32_t pwl[C::PSPLIT ? C::NKV / 2 : 1];
+        [[maybe_unused]] uint32_t pwl[C::PSPLIT ? C::NKV / 2 : 1];
         const float4* n4 = reinterpret_cast<const float4*>(sNorm);
         auto pack_p = [&](int i, float y0, float y1) {  // P' pair i: fp16 hi, and lo when split
           pw[i] = pack_half2(y0, y1);
@@ -453,7 +495,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         };
 #pragma unroll
         for (int j = 0; j < C::NKV; j += 4) {
-          const float4 nn = n4[j / 4];
+          const float4 nn = ROT ? make_float4(1.0f, 1.0f, 1.0f, 1.0f) : n4[j / 4];
           const float p0 = fast_exp2(x[j] - mref), p1 = fast_exp2(x[j + 1] - mref);
           const float p2 = fast_exp2(x[j + 2] - mref), p3 = fast_exp2(x[j + 3] - mref);
           ps += (p0 + p1) + (p2 + p3);
@@ -472,7 +514,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       } else {
         // ---- C^T for the step: the prefetched fields, then the rest ----
 #pragma unroll
-        for (int u = 0; u < VPRE; ++u) v_store(u, vpre[u]);
+        for (int u = 0; u < VPRE; ++u) v_store(u, vpre[u], vn);
         // Table loads are issued in batches ahead of their stores, so one
         // shared-memory latency is exposed per batch rather than per field.
         constexpr int VB = G < 16 ? G : 16;  // divides the G fields left
@@ -482,9 +524,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
 #pragma unroll
           for (int u = 0; u < VB; ++u) val[u] = v_field(vw, pb + u);
 #pragma unroll
-          for (int u = 0; u < VB; ++u) v_store(pb + u, val[u]);
+          for (int u = 0; u < VB; ++u) v_store(pb + u, val[u], vn);
         }
-        if (step + 1 < s1) fetch_v(vw, step + 1);
+        if (step + 1 < s1) fetch_v(vw, vn, step + 1);
       }
       sync_for_mma();
       if (SM && tid == 0) {
@@ -645,11 +687,14 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
 }
 
 // Inverse transform of the prefill output rows in place:
-// row = s * H_D(row) * kCentroidScale / D.
+// row = s * H_D(row) * scale_B / D (scale_B: the tier's centroid scale); with
+// the block-diagonal rotation, per 128-dim group, row = s1 * H_128(s2 * row) *
+// scale_B / 128.
 // Rows of a tile cut by the stream-K schedule are first merged from the two
 // partial slots (exact log-sum-exp combine), and their lse written.
-template <int D>
-__global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const int8_t* signs, int QT) {
+template <int D, int B, bool ROT>
+__global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const int8_t* signs, const int8_t* signs2,
+                                                            int QT) {
   constexpr int E = D / 32;
   const int64_t n_rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -687,6 +732,11 @@ __global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const
       v[e] = (w0 * s0[(int64_t)rin * D + 32 * e + lane] + w1 * s1[(int64_t)rin * D + 32 * e + lane]) * inv;
     if (lane == 0) a.lse[r] = L > 0.0f ? M + logf(L) : -INFINITY;
   }
+  if constexpr (ROT) {
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (signs2[32 * e + lane] < 0) v[e] = -v[e];
+  }
 #pragma unroll
   for (int hl = 1; hl < 32; hl <<= 1) {
 #pragma unroll
@@ -695,8 +745,11 @@ __global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const
       v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
     }
   }
+  // Butterflies across registers: dims 32 e + lane, e < E; the rotation's
+  // groups are 4 registers wide.
+  constexpr int EW = ROT ? kRotGroup / 32 : E;
 #pragma unroll
-  for (int hh = 1; hh < E; hh <<= 1) {
+  for (int hh = 1; hh < EW; hh <<= 1) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       if ((e & hh) == 0) {
@@ -709,7 +762,7 @@ __global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int d = 32 * e + lane;
-    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (kCentroidScale / D);
+    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (centroid_scale(B) / (ROT ? kRotGroup : D));
   }
 }
 
@@ -766,12 +819,14 @@ static size_t prefill_ws_bytes(int D, int batch, int n_kv_heads, int n_q_heads, 
   return bytes;
 }
 
-template <int D>
-static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, cudaStream_t stream) {
-  using Cf = PCfg<D>;
+template <int D, int B, bool ROT>
+static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, const int8_t* signs2,
+                                    cudaStream_t stream) {
+  using Cf = PCfg<D, B, ROT>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_prefill_kernel<D, B, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -779,12 +834,29 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
   PrefillArgs k = a;
   k.stream_k = pl.stream_k;
   const unsigned grid = static_cast<unsigned>(pl.stream_k ? pl.grid : pl.n_tiles);
-  attn_prefill_kernel<D><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
+  attn_prefill_kernel<D, B, ROT><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
-  derotate_rows_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(k, signs, pl.qt);
+  derotate_rows_kernel<D, B, ROT><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(k, signs, signs2, pl.qt);
   return cudaGetLastError();
+}
+
+// Instantiation for the cache's V code width and rotation (checked before).
+template <int D>
+static cudaError_t launch_prefill_v(const PrefillArgs& a, const ckv_cache* cache, cudaStream_t stream) {
+  const int bits = cache->v_bits == 0 ? 3 : cache->v_bits;
+  if (cache->v_signs2) {
+    if constexpr (D >= kRotGroup) {
+      if (bits == 2) return launch_prefill_d<D, 2, true>(a, cache->v_signs, cache->v_signs2, stream);
+      if (bits == 4) return launch_prefill_d<D, 4, true>(a, cache->v_signs, cache->v_signs2, stream);
+      return launch_prefill_d<D, 3, true>(a, cache->v_signs, cache->v_signs2, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (bits == 2) return launch_prefill_d<D, 2, false>(a, cache->v_signs, nullptr, stream);
+  if (bits == 4) return launch_prefill_d<D, 4, false>(a, cache->v_signs, nullptr, stream);
+  return launch_prefill_d<D, 3, false>(a, cache->v_signs, nullptr, stream);
 }
 
 }  // namespace ckv
@@ -820,10 +892,11 @@ ckv_status prefill_checks(const ckv_cache* cache, int64_t kv_end, const void* q_
   if (n_q_heads <= 0 || cache->n_kv_heads <= 0 || cache->batch <= 0 || n_q_heads % cache->n_kv_heads ||
       128 % (n_q_heads / cache->n_kv_heads))
     return prefill_fail(CKV_ERR_UNSUPPORTED, "prefill needs n_q_heads / n_kv_heads dividing 128");
-  if (cache->v_bits != 0 && cache->v_bits != 3)
-    return static_cast<ckv_status>(ckv::set_last_error(
-        CKV_ERR_UNSUPPORTED, "prefill reads 3-bit V codes only (cache v_bits %d)", static_cast<int>(cache->v_bits)));
-  if (cache->v_signs2) return prefill_fail(CKV_ERR_UNSUPPORTED, "prefill runs the full D-point transform only (v_signs2 set)");
+  if (cache->v_bits != 0 && cache->v_bits != 2 && cache->v_bits != 3 && cache->v_bits != 4)
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "v_bits must be 2, 3 or 4 (got %d)",
+                                                       static_cast<int>(cache->v_bits)));
+  if (cache->v_signs2 && cache->head_dim < ckv::kRotGroup)
+    return prefill_fail(CKV_ERR_UNSUPPORTED, "the block-diagonal rotation needs head_dim >= 128");
   if (!cache->data || !cache->v_signs || (reinterpret_cast<uintptr_t>(cache->data) & 15))
     return prefill_fail(CKV_ERR_INVALID_ARG, "cache data / signs");
   if (n_new == 0) return CKV_OK;
@@ -864,10 +937,10 @@ ckv_status run_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_b
     a.part = reinterpret_cast<float*>(ws + 256 + (4 * n_tiles + 255) / 256 * 256);
   }
   switch (cache->head_dim) {
-    case 64: e = ckv::launch_prefill_d<64>(a, cache->v_signs, st); break;
-    case 128: e = ckv::launch_prefill_d<128>(a, cache->v_signs, st); break;
-    case 256: e = ckv::launch_prefill_d<256>(a, cache->v_signs, st); break;
-    case 512: e = ckv::launch_prefill_d<512>(a, cache->v_signs, st); break;
+    case 64: e = ckv::launch_prefill_v<64>(a, cache, st); break;
+    case 128: e = ckv::launch_prefill_v<128>(a, cache, st); break;
+    case 256: e = ckv::launch_prefill_v<256>(a, cache, st); break;
+    case 512: e = ckv::launch_prefill_v<512>(a, cache, st); break;
     default:
       return static_cast<ckv_status>(
           ckv::set_last_error(CKV_ERR_UNSUPPORTED, "head_dim %d", static_cast<int>(cache->head_dim)));

@@ -162,6 +162,9 @@ WORKLOADS = {
     "chunked_prefill": Workload("chunked_prefill", head_dim=512, n_kv_heads=2, n_q_heads=16,
                                 batch=1, seq_len=32768, seed=4, n_outliers=_one_percent(512),
                                 n_new=2048, q_dtype="bfloat16"),
+    "chunked_prefill_rot": Workload("chunked_prefill_rot", head_dim=512, n_kv_heads=2, n_q_heads=16,
+                                    batch=1, seq_len=32768, seed=11, n_outliers=_one_percent(512),
+                                    n_new=2048, q_dtype="bfloat16", rot_group=128),
 }
 
 

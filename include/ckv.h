@@ -321,10 +321,11 @@ CKV_API ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts,
  * reads it back). S = Q K_hat^T and P V_hat run on tcgen05 tensor cores.
  * q_bf16: device bf16 [batch][n_new][n_q_heads][D]. k_new_f16, v_new_f16: device
  * fp16 [batch][n_new][n_kv_heads][D]. out: float32 [batch][n_new][n_q_heads][D];
- * lse: float32 [batch][n_new][n_q_heads]. head_dim 64, 128, 256 or 512; the
- * query-to-kv head ratio must divide 128, and the cache must hold 3-bit V
- * codes (v_bits 0 or 3) with the full transform (v_signs2 NULL): else
- * CKV_ERR_UNSUPPORTED.
+ * lse: float32 [batch][n_new][n_q_heads]. head_dim 64, 128, 256 or 512 and
+ * the query-to-kv head ratio dividing 128, else CKV_ERR_UNSUPPORTED. Every V
+ * tier (v_bits 2, 3, 4) and both rotations (v_signs2 NULL, or the
+ * block-diagonal one at head_dim >= 128) are read; positions past
+ * n_cached + n_new may hold any bytes.
  */
 CKV_API size_t ckv_attn_prefill_workspace(const ckv_cache* cache, int32_t n_new, int32_t n_q_heads);
 CKV_API ckv_status ckv_attn_prefill(const ckv_cache* cache, int64_t n_cached, const void* q_bf16,

@@ -162,10 +162,11 @@ def test_prefill_argument_checks(lib):
     assert call(cache=_fake_cache(D=32)) == -2       # prefill head dims: 64, 128, 256, 512
     assert call(n_cached=4090) == -1                 # past capacity
     assert call(hq=12) == -2                         # 6 heads per kv head does not divide 128
-    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=2)) == -2   # prefill reads 3-bit V only
-    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=4)) == -2
-    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=3)) == -3   # 3 passes (then the workspace)
-    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, signs2=0x30000)) == -2  # full transform only
+    for bits in (2, 3, 4):   # every tier passes the checks (then the workspace)
+        assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=bits)) == -3
+        assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=bits, signs2=0x30000)) == -3
+    assert call(cache=_fake_cache(D=512, Hkv=2, cap=4096, v_bits=5)) == -1
+    assert call(cache=_fake_cache(D=64, Hkv=2, cap=4096, signs2=0x30000)) == -2   # rotation needs D >= 128
     assert call(q=fake + 8) == -1
     assert call(out=None) == -1
     assert call(w=None) == -3
