@@ -64,7 +64,14 @@ extern "C" CKV_API ckv_status ckv_attn_decode_noalloc(const ckv_cache* cache, co
                                                       int32_t n_q_heads, float scale, int32_t n_split,
                                                       float* out, float* lse, void* stream) {
   // Size the scratch exactly as ckv_attn_decode would, and refuse what does not fit.
-  const size_t need = ckv_attn_decode_workspace(cache, max_seq_len, n_q, n_q_heads, n_split);
+  size_t need = ckv_attn_decode_workspace(cache, max_seq_len, n_q, n_q_heads, n_split);
+  if (need > kNoAllocScratchBytes && n_split == 0 && cache &&
+      ckv::rows_decode_applies(cache->batch, cache->n_kv_heads, n_q_heads, n_q, n_split, max_seq_len)) {
+    // The many-row tile path keeps one partial per tile and split; the
+    // mma.sync path at its own automatic split count needs far less scratch.
+    n_split = ckv::decode_auto_split(cache, max_seq_len, n_q, n_q_heads);
+    need = ckv_attn_decode_workspace(cache, max_seq_len, n_q, n_q_heads, n_split);
+  }
   if (need == 0) {
     // Invalid geometry: let the regular entry point produce the precise status and message.
     return ckv_attn_decode(cache, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,

@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <type_traits>
 
 #include "../../include/ckv.h"
@@ -60,6 +61,14 @@ struct PrefillArgs {
   int stream_k;
   float* part;
   int32_t* tile_split;
+  // Decode over many query rows (n_split > 0, with prefix_only = 1): the
+  // queries of sequence b see [0, seq_len[b]) (device array, each entry in
+  // [0, n_cached]); CTA c runs tile c / n_split over its share c % n_split of
+  // the ceil(n_cached / 64) steps and writes its rows to slot c; the
+  // de-rotation kernel merges a row's n_split slots.
+  const int32_t* seq_len;
+  int n_split;
+  int q_f16;  // queries are fp16 (else bf16)
 };
 
 // B: bits per V code (2, 3 or 4). ROT: the block-diagonal rotation (one V
@@ -126,10 +135,6 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   const int QT = C::M / group_q;  // query tokens per tile
   const int n_qt = (a.n_new + QT - 1) / QT;
   const int64_t n_rec = a.capacity / kTile;
-  // Positions [0, kv_lim) hold packed rows; the ones after it in the last
-  // step may hold any bytes, so their V norms enter as zero (a NaN there
-  // would reach O through P' = 0).
-  const int64_t kv_lim = a.prefix_only ? a.n_cached : a.n_cached + a.n_new;
   // 64-key steps of query tile qt: its rows see keys [0, n_cached + last row]
   // (prefix_only: [0, n_cached)).
   auto steps_of = [&](int qt) {
@@ -138,8 +143,12 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   };
 
   // The tile being run, set per segment (CTA-uniform, kept in shared memory
-  // so that the step loop does not hold it in registers).
+  // so that the step loop does not hold it in registers). s_kv_end: the end
+  // of the keys every query sees (prefix_only) and of the packed rows; the
+  // positions after it in the last step may hold any bytes, so their V norms
+  // enter as zero (a NaN there would reach O through P' = 0).
   __shared__ int s_q0, s_kvh, s_b, s_s0;
+  __shared__ long long s_kv_end;
   __shared__ const uint8_t* s_stream;
   __shared__ float* s_slot;  // nullptr: rows to `out`
 
@@ -171,6 +180,24 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
 
   // ---- Q tile: bf16 -> fp16 (exact in range), 128-byte swizzled K-major ----
   auto load_q = [&]() {
+  if (a.q_f16) {
+    // fp16 queries go to shared memory as they are: 16-byte asynchronous
+    // copies, all in flight at once (a split decode runs few steps per CTA,
+    // so this load is not amortised).
+    for (int piece = tid; piece < C::M * (D / 8); piece += C::THREADS) {
+      const int r = piece / (D / 8), k0 = (piece % (D / 8)) * 8;
+      const int qi = s_q0 + r / group_q, h = s_kvh * group_q + r % group_q;
+      const uint32_t dst = smem_u32(sQ + sw128_offset(r, k0, C::M));
+      if (qi < a.n_new) {
+        const void* src = a.q + (((int64_t)s_b * a.n_new + qi) * a.n_q_heads + h) * D + k0;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    return;
+  }
   for (int piece = tid; piece < C::M * (D / 8); piece += C::THREADS) {
     const int r = piece / (D / 8), k0 = (piece % (D / 8)) * 8;
     const int qi = s_q0 + r / group_q, h = s_kvh * group_q + r % group_q;
@@ -178,14 +205,18 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     if (qi < a.n_new) {
       const uint4 v =
           *reinterpret_cast<const uint4*>(a.q + (((int64_t)s_b * a.n_new + qi) * a.n_q_heads + h) * D + k0);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+      if (a.q_f16) {
+        outv = v;
+      } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-        o[i] = pack_half2(__low2float(x), __high2float(x));
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+          o[i] = pack_half2(__low2float(x), __high2float(x));
+        }
+        outv = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      outv = make_uint4(o[0], o[1], o[2], o[3]);
     }
     *reinterpret_cast<uint4*>(sQ + sw128_offset(r, k0, C::M)) = outv;
   }
@@ -265,7 +296,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     }
     if (!ROT && tid < C::NKV) {
       const int64_t rec = rec0 + tid / kTile;
-      nrm = (rec < n_rec && rec0 * kTile + tid < kv_lim)
+      nrm = (rec < n_rec && rec0 * kTile + tid < s_kv_end)
                 ? __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D, B) +
                                                                 2 * (tid % kTile)))
                 : 0.0f;
@@ -282,7 +313,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       const int64_t rec = rec0 + vr4;
       const int p0 = 2 * (vL & 3), grp = G * (vL >> 2) / kRotGroup;
       const uint8_t* nb = stream + rec * C::REC + v_norm_offset(D, B) + 2 * (kTile * grp + p0);
-      const int64_t r = kv_lim - rec * kTile - p0;  // positions p0 + i with i < r hold rows
+      const int64_t r = s_kv_end - rec * kTile - p0;  // positions p0 + i with i < r hold rows
       vn[0] = (rec < n_rec && r > 0) ? *reinterpret_cast<const uint32_t*>(nb) & (r >= 2 ? 0xffffffffu : 0xffffu)
                                      : 0u;
       vn[1] = (rec < n_rec && r > 8) ? *reinterpret_cast<const uint32_t*>(nb + 16) & (r >= 10 ? 0xffffffffu : 0xffffu)
@@ -447,7 +478,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         tmem_ld_wait();
         // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
         const int row_qi = s_q0 + row / group_q;
-        const int64_t rel = row_qi >= a.n_new ? 0 : a.prefix_only ? a.n_cached - j0 : a.n_cached + row_qi - j0 + 1;
+        const int64_t rel = row_qi >= a.n_new ? 0 : a.prefix_only ? s_kv_end - j0 : a.n_cached + row_qi - j0 + 1;
         const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
         const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
         float x[C::NKV];
@@ -627,6 +658,53 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   }
   __syncthreads();
   const int64_t n_bh = (int64_t)a.batch * a.n_kv_heads;
+  if (a.n_split > 0) {
+    // One segment: tile blockIdx / n_split, share blockIdx % n_split of the steps.
+    __shared__ int s_s1;
+    if (tid == 0) {
+      const int64_t t = blockIdx.x / a.n_split;
+      const int sp = static_cast<int>(blockIdx.x % a.n_split);
+      const int64_t bh = t / n_qt;
+      const int qt = static_cast<int>(t % n_qt);
+      const int b = static_cast<int>(bh / a.n_kv_heads);
+      const int64_t S = (a.n_cached + C::NKV - 1) / C::NKV;
+      int64_t len = a.seq_len[b];
+      if (len < 0 || len > a.n_cached) {
+        raise_flag(a.flag, kFlagSeqLenRange);
+        len = 0;
+      }
+      const int64_t sb = (len + C::NKV - 1) / C::NKV;  // steps this sequence has
+      const int64_t s0 = sp * S / a.n_split;
+      int64_t s1 = (sp + 1) * S / a.n_split;
+      if (s1 > sb) s1 = sb;
+      if (s1 < s0) s1 = s0;
+      s_b = b;
+      s_kvh = static_cast<int>(bh % a.n_kv_heads);
+      s_q0 = qt * QT;
+      s_s0 = static_cast<int>(s0);
+      s_s1 = static_cast<int>(s1);
+      s_kv_end = len;
+      s_stream = a.cache + bh * n_rec * C::REC;
+      s_slot = a.part + (int64_t)blockIdx.x * (C::M * (D + 1));
+    }
+    __syncthreads();
+    const int s0 = s_s0, s1 = s_s1;
+    load_q();
+    if (s0 < s1) {
+      fetch(s0);
+      put_scales(s0 & 1);
+    }
+    __syncthreads();
+    if (softmax_warp)
+      role_loop(std::true_type{}, s1);
+    else
+      role_loop(std::false_type{}, s1);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+    return;
+  }
   while (true) {
     const int64_t left = s_walk[0], bh = s_walk[1];
     const int qt = static_cast<int>(s_walk[2]), s0 = static_cast<int>(s_walk[3]);
@@ -653,6 +731,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       s_kvh = static_cast<int>(bh % a.n_kv_heads);
       s_q0 = qt * QT;
       s_s0 = s0;
+      s_kv_end = a.prefix_only ? a.n_cached : a.n_cached + a.n_new;
       s_stream = a.cache + bh * n_rec * C::REC;
       s_slot = slot;
     }
@@ -684,6 +763,47 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Inverse transform of one row held by a warp (v[e] = dim 32 e + lane) into p:
+// p = s * H_D(v) * scale_B / D, or per 128-dim group s1 * H_128(s2 * v) *
+// scale_B / 128.
+template <int D, int B, bool ROT>
+__device__ __forceinline__ void derotate_row(float (&v)[D / 32], int lane, const int8_t* signs,
+                                             const int8_t* signs2, float* p) {
+  constexpr int E = D / 32;
+  if constexpr (ROT) {
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (signs2[32 * e + lane] < 0) v[e] = -v[e];
+  }
+#pragma unroll
+  for (int hl = 1; hl < 32; hl <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
+      v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+    }
+  }
+  // Butterflies across registers: dims 32 e + lane, e < E; the rotation's
+  // groups are 4 registers wide.
+  constexpr int EW = ROT ? kRotGroup / 32 : E;
+#pragma unroll
+  for (int hh = 1; hh < EW; hh <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & hh) == 0) {
+        const float x0 = v[e], x1 = v[e + hh];
+        v[e] = x0 + x1;
+        v[e + hh] = x0 - x1;
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int d = 32 * e + lane;
+    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (centroid_scale(B) / (ROT ? kRotGroup : D));
+  }
 }
 
 // Inverse transform of the prefill output rows in place:
@@ -732,37 +852,74 @@ __global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const
       v[e] = (w0 * s0[(int64_t)rin * D + 32 * e + lane] + w1 * s1[(int64_t)rin * D + 32 * e + lane]) * inv;
     if (lane == 0) a.lse[r] = L > 0.0f ? M + logf(L) : -INFINITY;
   }
-  if constexpr (ROT) {
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      if (signs2[32 * e + lane] < 0) v[e] = -v[e];
+  derotate_row<D, B, ROT>(v, lane, signs, signs2, p);
+}
+
+// Split many-row decode: one CTA per output row merges the row's n_split
+// slots exactly (log-sum-exp; slots of an empty key range carry lse = -inf,
+// zero rows, and weigh 0), then one warp applies the inverse transform. The
+// weights go to shared memory first, so the slot loads of the accumulation
+// depend on nothing and several are in flight per thread.
+constexpr int kMaxRowSplits = 1024;
+template <int D, int B, bool ROT>
+__global__ void __launch_bounds__(128) merge_split_rows_kernel(PrefillArgs a, const int8_t* signs,
+                                                               const int8_t* signs2, int QT) {
+  constexpr int64_t SLOT = 128 * (int64_t)(D + 1);
+  __shared__ float s_w[kMaxRowSplits];
+  __shared__ __align__(16) float s_o[D];
+  __shared__ float s_red[4];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_split = a.n_split;
+  const int group_q = a.n_q_heads / a.n_kv_heads;
+  const int h = static_cast<int>(r % a.n_q_heads);
+  const int64_t bq = r / a.n_q_heads;
+  const int qi = static_cast<int>(bq % a.n_new);
+  const int64_t b = bq / a.n_new;
+  const int n_qt = (a.n_new + QT - 1) / QT;
+  const int64_t t = (b * a.n_kv_heads + h / group_q) * n_qt + qi / QT;
+  const int rin = (qi % QT) * group_q + h % group_q;
+  const float* base = a.part + t * n_split * SLOT;
+  float M = -INFINITY;
+  for (int sp = tid; sp < n_split; sp += 128) {
+    const float l = base[sp * SLOT + 128 * D + rin];
+    s_w[sp] = l;
+    M = fmaxf(M, l);
   }
 #pragma unroll
-  for (int hl = 1; hl < 32; hl <<= 1) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
-      v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+  for (int sp = tid; sp < n_split; sp += 128) {
+    const float l = s_w[sp];
+    s_w[sp] = (l == -INFINITY) ? 0.0f : __expf(l - M);
+  }
+  __syncthreads();
+  float L = 0.0f;
+  for (int sp = 0; sp < n_split; ++sp) L += s_w[sp];
+  if (tid < D / 4) {
+    const float* row = base + (int64_t)rin * D + 4 * tid;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 8
+    for (int sp = 0; sp < n_split; ++sp) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(row + sp * SLOT));
+      const float w = s_w[sp];
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
     }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    *reinterpret_cast<float4*>(s_o + 4 * tid) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
-  // Butterflies across registers: dims 32 e + lane, e < E; the rotation's
-  // groups are 4 registers wide.
-  constexpr int EW = ROT ? kRotGroup / 32 : E;
+  __syncthreads();
+  if (warp == 0) {
+    float v[D / 32];
 #pragma unroll
-  for (int hh = 1; hh < EW; hh <<= 1) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      if ((e & hh) == 0) {
-        const float x0 = v[e], x1 = v[e + hh];
-        v[e] = x0 + x1;
-        v[e + hh] = x0 - x1;
-      }
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int d = 32 * e + lane;
-    p[d] = (signs[d] < 0 ? -v[e] : v[e]) * (centroid_scale(B) / (ROT ? kRotGroup : D));
+    for (int e = 0; e < D / 32; ++e) v[e] = s_o[32 * e + lane];
+    derotate_row<D, B, ROT>(v, lane, signs, signs2, a.out + r * D);
+    if (lane == 0) a.lse[r] = L > 0.0f ? M + logf(L) : -INFINITY;
   }
 }
 
@@ -832,13 +989,18 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
   }
   const PrefillPlan pl = plan_prefill(a.batch, a.n_kv_heads, a.n_q_heads, a.n_cached, a.n_new, a.prefix_only);
   PrefillArgs k = a;
-  k.stream_k = pl.stream_k;
-  const unsigned grid = static_cast<unsigned>(pl.stream_k ? pl.grid : pl.n_tiles);
+  k.stream_k = a.n_split > 0 ? 0 : pl.stream_k;
+  const unsigned grid = static_cast<unsigned>(a.n_split > 0 ? pl.n_tiles * a.n_split
+                                                            : (pl.stream_k ? pl.grid : pl.n_tiles));
   attn_prefill_kernel<D, B, ROT><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
-  derotate_rows_kernel<D, B, ROT><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(k, signs, signs2, pl.qt);
+  if (a.n_split > 0)
+    merge_split_rows_kernel<D, B, ROT><<<static_cast<unsigned>(rows), 128, 0, stream>>>(k, signs, signs2, pl.qt);
+  else
+    derotate_rows_kernel<D, B, ROT><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(k, signs, signs2,
+                                                                                              pl.qt);
   return cudaGetLastError();
 }
 
@@ -857,6 +1019,85 @@ static cudaError_t launch_prefill_v(const PrefillArgs& a, const ckv_cache* cache
   if (bits == 2) return launch_prefill_d<D, 2, false>(a, cache->v_signs, nullptr, stream);
   if (bits == 4) return launch_prefill_d<D, 4, false>(a, cache->v_signs, nullptr, stream);
   return launch_prefill_d<D, 3, false>(a, cache->v_signs, nullptr, stream);
+}
+
+// ---- decode with many query rows per kv head ----
+// With many rows per kv head (for example 15 agents x 8 heads over one shared
+// prefix) the mma.sync decode, 8 rows per CTA, dequantises every tile once per
+// 8 rows; a 128-row tile dequantises it once but pays about 40 us of fixed
+// cost (Q load, a partial slot per CTA, the merge). Measured at head_dim 512
+// (B * Hkv = 2, 120 rows): 49 against 24 us at 4096 tokens, 72 against 70 at
+// 16384, 100 against 129 at 32768, 158 against 248 at 65536; with 64 rows the
+// mma.sync decode stays ahead through 65536. Fitted costs in us, X = batch *
+// n_kv_heads * max_seq_len / 1024: mma.sync 10 + 0.125 X per row group of 8,
+// tiles 40 + 0.9 X per 128-row tile. n_split 0 takes the cheaper; -1 forces
+// the tiles.
+bool rows_decode_applies(int batch, int n_kv_heads, int n_q_heads, int n_q, int n_split, int64_t max_seq_len) {
+  if ((n_split != 0 && n_split != -1) || max_seq_len <= 0 || n_kv_heads <= 0 || batch <= 0 || n_q <= 0 ||
+      n_q_heads % n_kv_heads)
+    return false;
+  const int g = n_q_heads / n_kv_heads;
+  if (128 % g) return false;
+  if (n_split == -1) return true;
+  const double rows = static_cast<double>(g) * n_q;
+  const double groups = std::ceil(rows / 8.0), tiles = std::ceil(n_q / (128.0 / g));
+  const double x = static_cast<double>(batch) * n_kv_heads * static_cast<double>(max_seq_len) / 1024.0;
+  return rows >= 64 && (0.125 * groups - 0.9 * tiles) * x > 30.0;
+}
+
+struct RowsPlan {
+  int qt, n_split;
+  int64_t n_tiles;
+  size_t ws;
+};
+static RowsPlan plan_rows(int D, int n_kv_heads, int batch, int n_q_heads, int n_q, int64_t key_end) {
+  RowsPlan p{};
+  p.qt = 128 / (n_q_heads / n_kv_heads);
+  p.n_tiles = static_cast<int64_t>(batch) * n_kv_heads * ((n_q + p.qt - 1) / p.qt);
+  const int64_t steps = (key_end + 63) / 64;
+  int64_t s = device_sms() / (p.n_tiles > 0 ? p.n_tiles : 1);  // one wave
+  if (s > steps) s = steps;
+  if (s > kMaxRowSplits) s = kMaxRowSplits;
+  if (s < 1) s = 1;
+  p.n_split = static_cast<int>(s);
+  p.ws = 256 + static_cast<size_t>(p.n_tiles) * p.n_split * 128 * (D + 1) * sizeof(float);
+  return p;
+}
+
+size_t rows_decode_ws_bytes(int head_dim, int n_kv_heads, int batch, int n_q_heads, int n_q, int64_t max_seq_len) {
+  return plan_rows(head_dim, n_kv_heads, batch, n_q_heads, n_q, max_seq_len).ws;
+}
+
+cudaError_t launch_rows_decode(const void* cache_v, int64_t key_end, const int32_t* seq_len, const void* q_f16,
+                               int n_q, int n_q_heads, float scale, float* out, float* lse, void* ws,
+                               cudaStream_t stream) {
+  const ckv_cache* cache = static_cast<const ckv_cache*>(cache_v);
+  const RowsPlan pl = plan_rows(cache->head_dim, cache->n_kv_heads, cache->batch, n_q_heads, n_q, key_end);
+  PrefillArgs a{};
+  a.cache = static_cast<const uint8_t*>(cache->data);
+  a.capacity = cache->capacity;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.batch = cache->batch;
+  a.n_cached = key_end;
+  a.n_new = n_q;
+  a.n_q_heads = n_q_heads;
+  a.prefix_only = 1;
+  a.q = static_cast<const __nv_bfloat16*>(q_f16);
+  a.q_f16 = 1;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  a.lse = lse;
+  a.flag = static_cast<int32_t*>(ws);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+  a.seq_len = seq_len;
+  a.n_split = pl.n_split;
+  switch (cache->head_dim) {
+    case 64: return launch_prefill_v<64>(a, cache, stream);
+    case 128: return launch_prefill_v<128>(a, cache, stream);
+    case 256: return launch_prefill_v<256>(a, cache, stream);
+    case 512: return launch_prefill_v<512>(a, cache, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ckv

@@ -195,14 +195,51 @@ ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64_t n_tok
   return CKV_OK;
 }
 
-size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q,
-                                 int32_t n_q_heads, int32_t n_split) {
+// Workspace of the mma.sync decode family (decode, verify, DCA, append).
+static size_t mma_decode_ws(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q, int32_t n_q_heads,
+                            int32_t n_split) {
   if (check_cache(cache) != CKV_OK) return 0;
   DecodePlan p;
   if (plan_decode(cache->head_dim, cache->n_kv_heads, cache->batch, max_seq_len, n_q, n_q_heads, n_split,
                   &p) != CKV_OK)
     return 0;
   return p.ws;
+}
+
+}  // extern "C"
+
+namespace ckv {
+int decode_auto_split(const void* cache_v, int64_t max_seq_len, int n_q, int n_q_heads) {
+  const ckv_cache* cache = static_cast<const ckv_cache*>(cache_v);
+  DecodePlan p;
+  if (check_cache(cache) != CKV_OK ||
+      plan_decode(cache->head_dim, cache->n_kv_heads, cache->batch, max_seq_len, n_q, n_q_heads, 0, &p) != CKV_OK)
+    return 1;
+  return p.n_split;
+}
+}  // namespace ckv
+
+extern "C" {
+
+// Key range the many-row decode splits: seq_len never exceeds this.
+static int64_t rows_key_end(const ckv_cache* cache, int64_t max_seq_len) {
+  return max_seq_len < cache->capacity ? max_seq_len : cache->capacity;
+}
+
+size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q,
+                                 int32_t n_q_heads, int32_t n_split) {
+  if (check_cache(cache) != CKV_OK) return 0;
+  const bool rows = ckv::rows_decode_applies(cache->batch, cache->n_kv_heads, n_q_heads, n_q, n_split, max_seq_len);
+  if (n_split == -1) {
+    if (!rows || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return 0;
+    return ckv::rows_decode_ws_bytes(cache->head_dim, cache->n_kv_heads, cache->batch, n_q_heads, n_q,
+                                     rows_key_end(cache, max_seq_len));
+  }
+  const size_t ws = mma_decode_ws(cache, max_seq_len, n_q, n_q_heads, n_split);
+  if (ws == 0 || !rows) return ws;
+  const size_t rw = ckv::rows_decode_ws_bytes(cache->head_dim, cache->n_kv_heads, cache->batch, n_q_heads, n_q,
+                                              rows_key_end(cache, max_seq_len));
+  return rw > ws ? rw : ws;
 }
 
 // New rows appended by the decode kernel itself (ckv_attn_decode_append).
@@ -297,6 +334,27 @@ ckv_status ckv_attn_decode(const ckv_cache* cache, const int32_t* seq_len, int64
                            float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
   ckv_status s = check_cache(cache);
   if (s != CKV_OK) return s;
+  if (n_split == -1 &&
+      !ckv::rows_decode_applies(cache->batch, cache->n_kv_heads, n_q_heads, n_q, n_split, max_seq_len))
+    return fail(CKV_ERR_UNSUPPORTED, "n_split -1 (tile path) needs n_q_heads / n_kv_heads dividing 128 and "
+                                     "max_seq_len > 0");
+  if (ckv::rows_decode_applies(cache->batch, cache->n_kv_heads, n_q_heads, n_q, n_split, max_seq_len)) {
+    // Many query rows per kv head: the tcgen05 tile path (same checks as below).
+    DecodePlan p;
+    s = plan_decode(cache->head_dim, cache->n_kv_heads, cache->batch, max_seq_len, n_q, n_q_heads, 0, &p);
+    if (s != CKV_OK) return s;
+    if (!seq_len || !q_f16 || !out || !lse) return fail(CKV_ERR_INVALID_ARG, "null seq_len/q/out/lse");
+    if (!aligned(q_f16, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_len, 4))
+      return fail(CKV_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(CKV_ERR_INVALID_ARG, "scale not finite");
+    s = check_ws(workspace, ws_bytes, ckv_attn_decode_workspace(cache, max_seq_len, n_q, n_q_heads, n_split));
+    if (s != CKV_OK) return s;
+    const cudaError_t e = ckv::launch_rows_decode(cache, rows_key_end(cache, max_seq_len), seq_len, q_f16, n_q,
+                                                  n_q_heads, scale, out, lse, workspace,
+                                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return CKV_OK;
+  }
   return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
                     cache->capacity, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
                     workspace, ws_bytes, stream);
@@ -326,7 +384,7 @@ static size_t dca_ws_parts(const ckv_cache* cache, int n_rows_per_head, int n_q_
 
 static size_t dca_ws_for(const ckv_cache* cache, int64_t max_seq_len, int n_q_heads, int n_split, int parts,
                          size_t* dec_out) {
-  const size_t dec = ckv_attn_decode_workspace(cache, max_seq_len, 2 + parts, n_q_heads, n_split);
+  const size_t dec = mma_decode_ws(cache, max_seq_len, 2 + parts, n_q_heads, n_split);
   if (dec_out) *dec_out = dec;
   if (dec == 0) return 0;
   size_t o_off, l_off;

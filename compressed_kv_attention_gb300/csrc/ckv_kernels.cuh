@@ -127,6 +127,20 @@ struct LseMergeArgs {
 };
 cudaError_t launch_lse_merge(const LseMergeArgs& a, cudaStream_t stream);
 
+// Decode with many query rows per kv head (a shared prefix read by many
+// agents): the tcgen05 prefill kernel runs every 128-row tile split over the
+// key range (each CTA a share of the 64-key steps, writing one partial slot),
+// then a merge kernel combines each row's slots. Used by attn_decode when
+// rows_decode_applies() (n_split 0: where a fitted cost model prefers it; -1:
+// forced); the workspace holds the flag (bytes 0..255) and the slots.
+bool rows_decode_applies(int batch, int n_kv_heads, int n_q_heads, int n_q, int n_split, int64_t max_seq_len);
+size_t rows_decode_ws_bytes(int head_dim, int n_kv_heads, int batch, int n_q_heads, int n_q, int64_t max_seq_len);
+// The mma.sync decode's automatic split count for this call (>= 1; 1 on invalid input).
+int decode_auto_split(const void* cache, int64_t max_seq_len, int n_q, int n_q_heads);
+cudaError_t launch_rows_decode(const void* cache, int64_t key_end, const int32_t* seq_len, const void* q_f16,
+                               int n_q, int n_q_heads, float scale, float* out, float* lse, void* ws,
+                               cudaStream_t stream);
+
 // Record a failure message for ckv_last_error() on this thread; returns `status`.
 int set_last_error(int status, const char* fmt, ...);
 

@@ -183,6 +183,19 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
  *   float32 [batch][n_q][n_q_heads].
  * workspace: ckv_attn_decode_workspace() bytes, 256-byte aligned, zero-filled
  *   before first use; its merge counters are back at zero after every call.
+ *
+ * Many query rows per kv head (n_q * n_q_heads / n_kv_heads >= 64, as when
+ * many agents read one shared prefix: PolyKV page, section "S2 perf-path
+ * Level B" — large-n_q attention over turbo KV belongs on the tensor cores):
+ * the row groups above dequantise every tile once per 8 rows, so with n_split
+ * 0 the call instead runs the tcgen05 prefill kernel on 128-row tiles (query
+ * heads / kv heads must divide 128), each CTA taking a share of the 64-key
+ * steps and writing one partial, then a merge kernel (two launches) — where a
+ * cost model fitted on GB300 at head_dim 512 says it is faster (long prefixes:
+ * 1.3x at 32768 tokens and 1.6x at 65536 with 120 rows per kv head). n_split
+ * -1 forces that path (CKV_ERR_UNSUPPORTED if the head ratio does not divide
+ * 128 or max_seq_len is 0); its workspace is one 128 x (D + 1) float slot per
+ * tile and split.
  */
 CKV_API size_t ckv_attn_decode_workspace(const ckv_cache* cache, int64_t max_seq_len, int32_t n_q,
                                  int32_t n_q_heads, int32_t n_split);

@@ -106,7 +106,8 @@ def test_decode_argument_checks(lib):
     assert call(wsb=need - 1) == -3
     assert call(ws=fake + 16) == -3               # workspace must be 256-byte aligned
     assert call(scale=float("nan")) == -1
-    assert call(ns=-1) == -1
+    assert call(ns=-1) == -3                      # -1: the tile path, whose workspace is larger
+    assert call(ns=-2) == -1
     assert call(ns=1025) == -1                    # at most 1024 splits
     assert call(cache=_fake_cache(D=100)) == -2
 
@@ -217,3 +218,25 @@ def test_multitenant_prefill_argument_checks(lib):
     # tail append: strides and geometry
     ap = lambda ts, hd=512: lib.ckv_f16_append(fake, fake, hd, 2, 3, 1024, fake, fake, fake, 8, ts, ts * 8, None)
     assert ap(1000) == -1 and ap(1024, hd=96) == -2
+
+
+def test_many_row_decode_path_selection(lib):
+    """n_split 0 takes the 128-row tile path only where the cost model prefers
+    it (long prefixes with many rows per kv head); -1 forces it; a head ratio
+    that does not divide 128 cannot take it. The choice shows in the workspace
+    size (the tile path keeps one 128 x (D + 1) float slot per tile and split)."""
+    c_short = _fake_cache(D=512, Hkv=2, cap=4096)
+    c_long = _fake_cache(D=512, Hkv=2, cap=65536)
+    ws = lambda c, P, n_q, hq, ns: lib.ckv_attn_decode_workspace(ctypes.byref(c), P, n_q, hq, ns)  # noqa: E731
+    tiles_short, auto_short = ws(c_short, 4096, 15, 16, -1), ws(c_short, 4096, 15, 16, 0)
+    assert tiles_short > 256 + 2 * 128 * 513 * 4 and auto_short < tiles_short     # 4096 tokens: mma.sync
+    tiles_long, auto_long = ws(c_long, 65536, 15, 16, -1), ws(c_long, 65536, 15, 16, 0)
+    assert auto_long == tiles_long                                                # 65536 tokens: tiles
+    assert ws(c_long, 65536, 8, 16, 0) < ws(c_long, 65536, 8, 16, -1)            # 64 rows: mma.sync
+    assert ws(_fake_cache(D=128, Hkv=1, cap=64), 64, 8, 12, -1) == 0             # 12 heads per kv head
+    fake = 0x7f0000000000
+    c = _fake_cache(D=128, Hkv=1, cap=64)
+    assert lib.ckv_attn_decode(ctypes.byref(c), fake, 64, fake, 8, 12, 0.1, -1, fake, fake, fake, 1 << 20,
+                               None) == -2
+    assert lib.ckv_attn_decode(ctypes.byref(c), fake, 64, fake, 8, 16, 0.1, -2, fake, fake, fake, 1 << 20,
+                               None) == -1
