@@ -113,7 +113,10 @@ struct OChunk {
 
 }  // namespace
 
-template <int D, int B, bool ROT>
+// SPLIT: the split many-row decode (one segment per CTA, keys per sequence
+// from seq_len); otherwise the causal or prefix-only prefill, whose key end is
+// a launch constant (kept out of shared memory: the step loop reads it).
+template <int D, int B, bool ROT, bool SPLIT>
 __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   using C = PCfg<D, B, ROT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -148,7 +151,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   // positions after it in the last step may hold any bytes, so their V norms
   // enter as zero (a NaN there would reach O through P' = 0).
   __shared__ int s_q0, s_kvh, s_b, s_s0;
-  __shared__ long long s_kv_end;
+  __shared__ long long s_kv_end;  // SPLIT only
+  // The key end of the other modes, read from the launch arguments at each use.
+  auto kv_end_const = [&]() -> int64_t { return a.prefix_only ? a.n_cached : a.n_cached + a.n_new; };
   __shared__ const uint8_t* s_stream;
   __shared__ float* s_slot;  // nullptr: rows to `out`
 
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     }
     if (!ROT && tid < C::NKV) {
       const int64_t rec = rec0 + tid / kTile;
-      nrm = (rec < n_rec && rec0 * kTile + tid < s_kv_end)
+      nrm = (rec < n_rec && rec0 * kTile + tid < (SPLIT ? s_kv_end : kv_end_const()))
                 ? __half2float(*reinterpret_cast<const __half*>(stream + rec * C::REC + v_norm_offset(D, B) +
                                                                 2 * (tid % kTile)))
                 : 0.0f;
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       const int64_t rec = rec0 + vr4;
       const int p0 = 2 * (vL & 3), grp = G * (vL >> 2) / kRotGroup;
       const uint8_t* nb = stream + rec * C::REC + v_norm_offset(D, B) + 2 * (kTile * grp + p0);
-      const int64_t r = s_kv_end - rec * kTile - p0;  // positions p0 + i with i < r hold rows
+      const int64_t r = (SPLIT ? s_kv_end : kv_end_const()) - rec * kTile - p0;  // positions p0 + i, i < r, hold rows
       vn[0] = (rec < n_rec && r > 0) ? *reinterpret_cast<const uint32_t*>(nb) & (r >= 2 ? 0xffffffffu : 0xffffu)
                                      : 0u;
       vn[1] = (rec < n_rec && r > 8) ? *reinterpret_cast<const uint32_t*>(nb + 16) & (r >= 10 ? 0xffffffffu : 0xffffu)
@@ -478,7 +483,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         tmem_ld_wait();
         // Columns [0, nvis) are visible to the row: all of them except near the diagonal.
         const int row_qi = s_q0 + row / group_q;
-        const int64_t rel = row_qi >= a.n_new ? 0 : a.prefix_only ? s_kv_end - j0 : a.n_cached + row_qi - j0 + 1;
+        const int64_t rel = row_qi >= a.n_new     ? 0
+                            : a.prefix_only ? (SPLIT ? s_kv_end : a.n_cached) - j0
+                                            : a.n_cached + row_qi - j0 + 1;
         const int nvis = rel <= 0 ? 0 : (rel >= C::NKV ? C::NKV : static_cast<int>(rel));
         const bool all_vis = __all_sync(0xffffffffu, nvis == C::NKV);
         float x[C::NKV];
@@ -658,7 +665,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   }
   __syncthreads();
   const int64_t n_bh = (int64_t)a.batch * a.n_kv_heads;
-  if (a.n_split > 0) {
+  if constexpr (SPLIT) {
     // One segment: tile blockIdx / n_split, share blockIdx % n_split of the steps.
     __shared__ int s_s1;
     if (tid == 0) {
@@ -699,13 +706,8 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       role_loop(std::true_type{}, s1);
     else
       role_loop(std::false_type{}, s1);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
-    return;
   }
-  while (true) {
+  if constexpr (!SPLIT) while (true) {
     const int64_t left = s_walk[0], bh = s_walk[1];
     const int qt = static_cast<int>(s_walk[2]), s0 = static_cast<int>(s_walk[3]);
     if (left <= 0 || bh >= n_bh) break;
@@ -731,7 +733,6 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       s_kvh = static_cast<int>(bh % a.n_kv_heads);
       s_q0 = qt * QT;
       s_s0 = s0;
-      s_kv_end = a.prefix_only ? a.n_cached : a.n_cached + a.n_new;
       s_stream = a.cache + bh * n_rec * C::REC;
       s_slot = slot;
     }
@@ -982,8 +983,11 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
   using Cf = PCfg<D, B, ROT>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_prefill_kernel<D, B, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D, B, ROT, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_prefill_kernel<D, B, ROT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cf::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -992,7 +996,10 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
   k.stream_k = a.n_split > 0 ? 0 : pl.stream_k;
   const unsigned grid = static_cast<unsigned>(a.n_split > 0 ? pl.n_tiles * a.n_split
                                                             : (pl.stream_k ? pl.grid : pl.n_tiles));
-  attn_prefill_kernel<D, B, ROT><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
+  if (a.n_split > 0)
+    attn_prefill_kernel<D, B, ROT, true><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
+  else
+    attn_prefill_kernel<D, B, ROT, false><<<grid, Cf::THREADS, Cf::SMEM, stream>>>(k);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
