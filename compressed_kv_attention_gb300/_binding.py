@@ -156,7 +156,9 @@ def attn_decode_workspace(cache: PackedCache, max_seq_len: int, n_q: int, n_q_he
 
 def attn_decode(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,
                 n_split: int = 0, stream=None):
-    """q: fp16 [batch, n_q, n_q_heads, D]; out float32 like q; lse float32 [batch, n_q, n_q_heads]."""
+    """q: fp16 [batch, n_q, n_q_heads, D]; out float32 like q; lse float32 [batch, n_q, n_q_heads].
+    n_split: 0 automatic, > 0 that many key splits on the mma.sync decode, -1 the 128-row tcgen05
+    tile path for many query rows per kv head (size the workspace with the same n_split)."""
     _, n_q, n_q_heads, _ = q.shape
     _check(load().ckv_attn_decode(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(q), n_q, n_q_heads, scale,
                                   n_split, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
