@@ -633,6 +633,17 @@ def _make_work(name, dev, stream):
 
 # --------------------------------------------------------------------- ours --
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each timing's largest value over all ranks: the replica that finishes
+    last sets the whole job's time. Without a process group, the values."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def run_ours(args):
     import torch
 
@@ -702,9 +713,7 @@ def run_ours(args):
             ms += _timed(stream, lambda: work.step(i), 1)
     torch.cuda.synchronize(dev)
     if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        (ms,) = max_over_ranks([ms], dist, dev)
         dist.barrier()
 
     # The dominant kernel call alone, back to back.
@@ -728,6 +737,8 @@ def run_ours(args):
             work.e2e_step(i)
         stream.synchronize()
         e2e_s = time.perf_counter() - t0
+    if dist:
+        (e2e_s,) = max_over_ranks([e2e_s], dist, dev)
 
     peaks = _peaks()
     value = world * work.tokens_per_step * args.steps / (ms / 1e3)
