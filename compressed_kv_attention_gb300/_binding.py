@@ -61,6 +61,7 @@ SIGNATURES = {
     "ckv_lse_merge": (_c_int, [_c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _c_i64, _c_int, _vp, _vp,
                                _vp]),
     "ckv_attn_prefill_workspace": (_c_size, [_cache_p, _c_int, _c_int]),
+    "ckv_selftest_bounded_waits": (_c_int, [_vp, _c_size, _vp]),
     "ckv_attn_prefill": (_c_int, [_cache_p, _c_i64, _vp, _c_int, _c_int, _vp, _vp, _c_f, _vp, _vp, _vp,
                                   _c_size, _vp]),
     "ckv_attn_prefill_prefix": (_c_int, [_cache_p, _c_i64, _vp, _c_int, _c_int, _c_f, _vp, _vp, _vp, _c_size, _vp]),
@@ -299,3 +300,9 @@ def attn_prefill_shared(prefix: PackedCache, n_prefix: int, k_tail, v_tail, tail
                                           _ptr(tail_len), n_agents, _ptr(q), _ptr(k_new), _ptr(v_new), n_new,
                                           n_q_heads, scale, _ptr(out), _ptr(lse), _ptr(workspace),
                                           workspace.numel(), _stream(stream)))
+
+
+def selftest_bounded_waits(workspace, stream=None):
+    """Run the kernels' two bounded-wait forms on events that never come; afterwards the int32
+    words at workspace bytes 0 and 4 read 1 (workspace: >= 256 zero-filled device bytes)."""
+    _check(load().ckv_selftest_bounded_waits(_ptr(workspace), workspace.numel(), _stream(stream)))

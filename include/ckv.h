@@ -157,6 +157,19 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
                        int64_t token_stride, int64_t batch_stride, void* stream);
 
 /*
+ * selftest_bounded_waits — the failure path of the library's asynchronous
+ * waits. Every wait in its kernels (an mbarrier phase, a global counter
+ * written by other CTAs) gives up after 2 s of wall time, raises the device
+ * flag (1 = a bounded wait ran out) and lets the kernel finish, so a lost
+ * event becomes an error status instead of a hung context. This call runs
+ * both forms on events that never come: after it, the int32 at workspace
+ * byte 0 (the mbarrier form) and at byte 4 (the counter form) read 1.
+ * workspace: device, at least 256 bytes, 256-byte aligned, zero-filled (the
+ * counter at byte 64 must stay 0). Takes about 4 s of GPU time.
+ */
+CKV_API ckv_status ckv_selftest_bounded_waits(void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * attn_decode — attention of n_q query tokens per sequence over the packed
  * cache, every query seeing cached positions [0, seq_len[b]).
  *

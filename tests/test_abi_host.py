@@ -240,3 +240,9 @@ def test_many_row_decode_path_selection(lib):
                                None) == -2
     assert lib.ckv_attn_decode(ctypes.byref(c), fake, 64, fake, 8, 16, 0.1, -2, fake, fake, fake, 1 << 20,
                                None) == -1
+
+
+def test_selftest_argument_checks(lib):
+    assert lib.ckv_selftest_bounded_waits(None, 256, None) == -3
+    assert lib.ckv_selftest_bounded_waits(0x7f0000000000, 128, None) == -3    # fewer than 256 bytes
+    assert lib.ckv_selftest_bounded_waits(0x7f0000000010, 256, None) == -3    # not 256-byte aligned
