@@ -246,3 +246,17 @@ def test_selftest_argument_checks(lib):
     assert lib.ckv_selftest_bounded_waits(None, 256, None) == -3
     assert lib.ckv_selftest_bounded_waits(0x7f0000000000, 128, None) == -3    # fewer than 256 bytes
     assert lib.ckv_selftest_bounded_waits(0x7f0000000010, 256, None) == -3    # not 256-byte aligned
+
+
+def test_prefill_workspace_sizes(lib):
+    """Flag (256 bytes) + one int32 per 128-row tile (rounded to 256 bytes) and,
+    once there are more tiles than SMs, two partial slots of 128 x (D + 1)
+    floats per SM for the tiles the stream-K schedule cuts."""
+    c = _fake_cache(D=64, Hkv=2, cap=4096)
+    small = lib.ckv_attn_prefill_workspace(ctypes.byref(c), 48, 16)          # 2 kv heads x 3 tiles of 16 tokens
+    assert small == 256 + 256
+    big = lib.ckv_attn_prefill_workspace(ctypes.byref(c), 2560, 16)         # 2 x 160 tiles
+    slots = big - 256 - (4 * 320 + 255) // 256 * 256
+    per_sm = 2 * 128 * 65 * 4
+    assert slots > 0 and slots % per_sm == 0                               # whole SMs' worth of slot pairs
+    assert lib.ckv_attn_prefill_workspace(None, 16, 16) == 256
