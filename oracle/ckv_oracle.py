@@ -32,7 +32,9 @@ stores code 4 everywhere and norm 0; a query row with no visible key returns
 output 0 and lse -inf.
 
 Parity status: every function here is pinned by the CPU tests against values
-the pages print, closed forms or library routines (see tests/test_oracle_pins.py),
+the pages print, closed forms or library routines (see tests/test_oracle_pins.py;
+the dequantisers by hand-derived worked records, per-block scale indexing and
+the relative reconstruction error against the quantiser's distortion),
 except end-to-end quality against the pages' models (perplexity, RULER), which
 needs trained weights and datasets: parity unpinned for that, and it is not
 computed here.

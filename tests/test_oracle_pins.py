@@ -724,3 +724,124 @@ def test_shared_prefill_reference_brute_force_and_reductions():
     op, lp = O.decode_reference(q, kp, vp, P, sc)
     om, lm = O.lse_merge([op.reshape(-1, D), ov.reshape(-1, D)], [lp.ravel(), lv.ravel()])
     assert np.allclose(om.reshape(o.shape), o, atol=1e-12) and np.allclose(lm.reshape(lse.shape), lse, atol=1e-12)
+
+
+# ------------------------------------------------ dequantiser magnitude ---
+# The checks above on the TBQ dequantisers are scale-invariant (cosines,
+# re-encoding). These fix the magnitude and the block indexing: a dropped
+# n16 / sqrt(d) factor, sqrt(G) for sqrt(d), or a transposed scale index fails.
+
+def test_q8_0_dequantize_worked_blocks():
+    g = _golden_kv("q8_0_worked.txt")
+    qa = np.array([int(v) for v in g["A_q"]], dtype=np.int8)
+    assert np.array_equal(O.q8_0_dequantize(qa, np.array([float(g["A_d16"][0])], np.float16)),
+                          qa.astype(np.float64))
+    qb = np.zeros(32, np.int8)
+    qb[0] = 127
+    kb = O.q8_0_dequantize(qb, np.array([float(g["B_d16"][0])], np.float16))
+    assert kb[0] == float(g["B_khat0"][0]) and (kb[1:] == 0).all()
+
+
+def test_q8_0_dequantize_uses_each_blocks_own_scale():
+    # Two rows of two blocks, four distinct power-of-two scales, codes 1..32 in
+    # every block: element i of block b of row r must be (i + 1) * scale[r][b].
+    scales = np.array([[0.5, 2.0], [4.0, 0.125]], np.float16)
+    q = np.tile(np.arange(1, 33, dtype=np.int8), (2, 2))
+    k = O.q8_0_dequantize(q, scales)
+    ramp = np.arange(1, 33, dtype=np.float64)
+    expect = np.array([np.concatenate([ramp * 0.5, ramp * 2.0]),
+                       np.concatenate([ramp * 4.0, ramp * 0.125])])
+    assert np.array_equal(k, expect)
+
+
+def test_tbq3_dequantize_worked_example_d4():
+    g = _golden_kv("tbq3_worked_d4.txt")
+    codes = np.array([int(v) for v in g["codes"]], dtype=np.uint8)
+    s = np.array([int(v) for v in g["signs"]], dtype=np.int8)
+    v = O.tbq3_dequantize(codes, np.float16(float(g["norm16"][0])), s)
+    assert np.abs(v - np.array([float(t) for t in g["dequant"]])).max() < 1e-12
+    # the general-width entry point at 3 bits is the same map
+    v3 = O.tbq_dequantize(codes, np.float16(float(g["norm16"][0])), s, 3)
+    assert np.abs(v3 - v).max() == 0.0
+
+
+def _sphere_marginal_distortion(table, dim):
+    """E[(u - Q(u))^2] for u = sqrt(dim) * t, t one coordinate of a uniform point
+    on the unit sphere in R^dim: density of u proportional to
+    (1 - u^2 / dim)^((dim - 3) / 2) on |u| < sqrt(dim). This is exactly the law
+    of a normalised rotated coordinate of a Gaussian vector; it tends to N(0,1)
+    as dim grows."""
+    import scipy.integrate
+    table = np.asarray(table, dtype=np.float64)
+    lim = math.sqrt(dim)
+    t = np.concatenate([[-lim], 0.5 * (table[:-1] + table[1:]), [lim]])
+    dens = lambda u: (1.0 - u * u / dim) ** ((dim - 3) / 2.0)
+    z = scipy.integrate.quad(dens, -lim, lim, limit=200)[0]
+    total = 0.0
+    for k in range(len(table)):
+        total += scipy.integrate.quad(lambda u: (u - table[k]) ** 2 * dens(u), t[k], t[k + 1],
+                                      limit=200)[0]
+    return total / z
+
+
+def _relative_mse(x, xh):
+    xf = x.astype(np.float64)
+    return np.sum((xf - xh) ** 2, 1) / np.sum(xf * xf, 1)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_tbq_dequantize_relative_mse_equals_distortion(bits):
+    # For a Gaussian vector, ||x - x_hat||^2 / ||x||^2 = (1/d) sum (u_i - c_i)^2
+    # (the transform is orthonormal; the fp16 norm's rounding enters only at
+    # second order because E[(u - c) c] = 0 for a Lloyd-Max quantiser), so its
+    # mean is the per-coordinate distortion under the sphere marginal: within
+    # 0.5 % of the classic Gaussian D_b = 0.1175 / 0.03455 / 0.009497 at d = 512.
+    d = 512
+    rng = np.random.default_rng(60 + bits)
+    x = rng.standard_normal((1500, d)).astype(np.float16)
+    s = inputs.tbq_signs(d)
+    codes, n16, _ = O.tbq_quantize(x, s, bits)
+    rel = _relative_mse(x, O.tbq_dequantize(codes, n16, s, bits))
+    target = _sphere_marginal_distortion(O.tbq_centroids(bits), d)
+    classic = {2: 0.1175, 3: 0.03455, 4: 0.009497}[bits]
+    assert abs(target - classic) < 0.005 * classic
+    sem = rel.std() / math.sqrt(len(rel))
+    assert abs(rel.mean() - target) < 4 * sem + 1e-3 * target
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_tbq_dequantize_blocked_relative_mse_equals_distortion(bits):
+    # Same identity per 128-dim group: the normalised coordinates follow the
+    # sphere marginal of dimension 128, so the mean relative error is that
+    # distortion (1-2 % below the Gaussian D_b, whose tails are heavier).
+    d, G = 512, 128
+    rng = np.random.default_rng(70 + bits)
+    x = rng.standard_normal((1500, d)).astype(np.float16)
+    s1, s2 = inputs.tbq_signs(d), inputs.tbq_signs(d, seed=43)
+    codes, n16, _ = O.tbq_quantize_blocked(x, s1, s2, bits)
+    xh = O.tbq_dequantize_blocked(codes, n16, s1, s2, bits)
+    # per group: each group is its own quantiser with its own norm
+    xg = x.astype(np.float64).reshape(-1, d // G, G)
+    rel = (np.sum((xg - xh.reshape(xg.shape)) ** 2, -1) / np.sum(xg * xg, -1)).ravel()
+    target = _sphere_marginal_distortion(O.tbq_centroids(bits), G)
+    sem = rel.std() / math.sqrt(len(rel))
+    assert abs(rel.mean() - target) < 4 * sem + 1e-3 * target
+
+
+def test_tbq_dequantize_scales_linearly_with_the_stored_norm():
+    # The dequantised vector is proportional to the stored norm (doubling an
+    # fp16 norm doubles the vector exactly), and a unit-norm record whose codes
+    # are all the same centroid c has ||V_hat|| = |c| (orthonormal transform,
+    # d coordinates of size |c| / sqrt(d)).
+    d = 256
+    s = inputs.tbq_signs(d)
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 8, (4, d)).astype(np.uint8)
+    n = np.array([0.5, 1.0, 3.0, 1000.0], np.float16)
+    v1 = O.tbq3_dequantize(codes, n, s)
+    v2 = O.tbq3_dequantize(codes, (n.astype(np.float64) * 2).astype(np.float16), s)
+    assert np.array_equal(v2, 2 * v1)
+    for k, c in enumerate(O.LLOYD_MAX_3BIT):
+        same = np.full((1, d), k, np.uint8)
+        vk = O.tbq3_dequantize(same, np.array([1.0], np.float16), s)
+        assert abs(np.linalg.norm(vk) - abs(c)) < 1e-12
