@@ -73,6 +73,7 @@ SIGNATURES = {
     "ckv_attn_prefill_shared": (_c_int, [_cache_p, _c_i64, _vp, _vp, _c_i64, _vp, _c_int, _vp, _vp, _vp, _c_int,
                                          _c_int, _c_f, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_read_device_flag": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
+    "ckv_read_noalloc_flag": (_c_int, [ctypes.POINTER(_c_int), _vp]),
 }
 
 
@@ -257,6 +258,15 @@ def attn_prefill(cache: PackedCache, n_cached: int, q, k_new, v_new, scale: floa
 def read_device_flag(workspace, stream=None) -> int:
     flag = ctypes.c_int32(0)
     status = load().ckv_read_device_flag(_ptr(workspace), ctypes.byref(flag), _stream(stream))
+    if status not in (CKV_OK, -5):
+        _check(status)
+    return int(flag.value)
+
+
+def read_noalloc_flag(stream=None) -> int:
+    """Read and clear the device flag of attn_decode_noalloc's built-in array."""
+    flag = ctypes.c_int32(0)
+    status = load().ckv_read_noalloc_flag(ctypes.byref(flag), _stream(stream))
     if status not in (CKV_OK, -5):
         _check(status)
     return int(flag.value)

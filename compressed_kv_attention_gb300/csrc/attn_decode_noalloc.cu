@@ -15,14 +15,19 @@
 //    library, for the life of the process. A call whose scratch would not fit
 //    (see ckv_attn_decode_workspace) is rejected with CKV_ERR_WORKSPACE.
 //  * All calls share the one array and it keeps the previous call's contents.
-//    It is zero when the library loads; every call puts the split-merge
-//    counters back to zero and rewrites every partial it reads (the device
-//    flag word keeps any error). Calls that overlap on the GPU (different
-//    streams, no ordering between them) race on the array and give wrong
-//    results: order them on one stream or with events.
-//  * The first call on a device looks up the array's device address on that
-//    device (cudaGetSymbolAddress, with the device current). Make that first
-//    call before any stream capture on the device.
+//    Each call first clears, on its stream, the part of the array that holds
+//    its split-merge counters (their size depends on the call's shape, and an
+//    earlier call of another shape may have left partials or, after a timed-out
+//    wait, counters there), then runs the decode, which rewrites every partial
+//    it reads. Calls that overlap on the GPU (different streams, no ordering
+//    between them) race on the array and give wrong results: order them on one
+//    stream or with events.
+//  * The device flag word (bounded-wait timeouts, out-of-range seq_len) sits at
+//    the start of the array and is not cleared by a call: it keeps the first
+//    error since it was last read. ckv_read_noalloc_flag() reads and clears it.
+//  * The first call on a device (either entry point) looks up the array's
+//    device address on that device (cudaGetSymbolAddress, with the device
+//    current). Make that first call before any stream capture on the device.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -82,11 +87,30 @@ extern "C" CKV_API ckv_status ckv_attn_decode_noalloc(const ckv_cache* cache, co
         CKV_ERR_WORKSPACE, "attn_decode_noalloc: needs %zu bytes of scratch, the built-in array holds %zu",
         need, kNoAllocScratchBytes));
   void* scratch = nullptr;
-  const cudaError_t e = scratch_address(&scratch);
+  cudaError_t e = scratch_address(&scratch);
   if (e != cudaSuccess)
     return static_cast<ckv_status>(ckv::set_last_error(
         CKV_ERR_CUDA, "attn_decode_noalloc: scratch address lookup: %s", cudaGetErrorString(e)));
-  // ckv_attn_decode leaves the counters at zero and rewrites every partial it reads.
+  // Clear this call's counter words (bytes [4, header)); the flag word at 0 stays.
+  const size_t header = ckv::decode_header_bytes(cache, max_seq_len, n_q, n_q_heads, n_split);
+  if (header > kNoAllocScratchBytes)
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_WORKSPACE, "attn_decode_noalloc: header of %zu bytes exceeds the built-in array", header));
+  e = cudaMemsetAsync(static_cast<unsigned char*>(scratch) + 4, 0, header - 4, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_CUDA, "attn_decode_noalloc: counter clear: %s", cudaGetErrorString(e)));
   return ckv_attn_decode(cache, seq_len, max_seq_len, q_f16, n_q, n_q_heads, scale, n_split, out, lse,
                          scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" CKV_API ckv_status ckv_read_noalloc_flag(int32_t* flag, void* stream) {
+  if (!flag)
+    return static_cast<ckv_status>(ckv::set_last_error(CKV_ERR_INVALID_ARG, "read_noalloc_flag: flag is null"));
+  void* scratch = nullptr;
+  const cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess)
+    return static_cast<ckv_status>(ckv::set_last_error(
+        CKV_ERR_CUDA, "read_noalloc_flag: scratch address lookup: %s", cudaGetErrorString(e)));
+  return ckv_read_device_flag(scratch, flag, stream);
 }

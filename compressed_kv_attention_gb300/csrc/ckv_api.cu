@@ -217,6 +217,17 @@ int decode_auto_split(const void* cache_v, int64_t max_seq_len, int n_q, int n_q
     return 1;
   return p.n_split;
 }
+
+size_t decode_header_bytes(const void* cache_v, int64_t max_seq_len, int n_q, int n_q_heads, int n_split) {
+  const ckv_cache* cache = static_cast<const ckv_cache*>(cache_v);
+  if (check_cache(cache) != CKV_OK) return 256;
+  if (rows_decode_applies(cache->batch, cache->n_kv_heads, n_q_heads, n_q, n_split, max_seq_len)) return 256;
+  DecodePlan p;
+  if (plan_decode(cache->head_dim, cache->n_kv_heads, cache->batch, max_seq_len, n_q, n_q_heads, n_split, &p) !=
+      CKV_OK)
+    return 256;
+  return ws_header_bytes(p.groups, p.n_split);
+}
 }  // namespace ckv
 
 extern "C" {

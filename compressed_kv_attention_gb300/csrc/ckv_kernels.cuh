@@ -137,6 +137,10 @@ bool rows_decode_applies(int batch, int n_kv_heads, int n_q_heads, int n_q, int 
 size_t rows_decode_ws_bytes(int head_dim, int n_kv_heads, int batch, int n_q_heads, int n_q, int64_t max_seq_len);
 // The mma.sync decode's automatic split count for this call (>= 1; 1 on invalid input).
 int decode_auto_split(const void* cache, int64_t max_seq_len, int n_q, int n_q_heads);
+// Bytes at the start of the workspace that ckv_attn_decode uses for the device
+// flag (bytes 0..3) and its split-merge counters (from byte 64) for this call:
+// 256 on the tile path, which keeps no counters.
+size_t decode_header_bytes(const void* cache, int64_t max_seq_len, int n_q, int n_q_heads, int n_split);
 cudaError_t launch_rows_decode(const void* cache, int64_t key_end, const int32_t* seq_len, const void* q_f16,
                                int n_q, int n_q_heads, float scale, float* out, float* lse, void* ws,
                                cudaStream_t stream);

@@ -296,10 +296,13 @@ CKV_API ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t*
  * scratch is a 4 MiB array compiled into the library (held on every device that
  * loads it until the process exits); a call whose scratch would exceed it (see
  * ckv_attn_decode_workspace) returns CKV_ERR_WORKSPACE. Nothing is allocated.
- * Every call shares that one array (zero when the library loads; every call
- * leaves its header at zero, except the device flag after an error); calls
- * that overlap on the GPU race and give wrong results (order them on one
- * stream or with events). The first
+ * Every call shares that one array, which keeps the last call's contents: each
+ * call first clears, on its stream, the counter words its own shape uses
+ * (cudaMemsetAsync of at most a few KB), so a call of any shape may follow a
+ * call of any other, or a call whose bounded wait timed out. Calls that overlap
+ * on the GPU race on the array and give wrong results (order them on one
+ * stream or with events). The device flag (first 4 bytes of the array) is not
+ * cleared by a call; read and clear it with ckv_read_noalloc_flag. The first
  * call on a device looks up the array's address on that device; make that
  * first call before any stream capture on the device.
  */
@@ -307,6 +310,15 @@ CKV_API ckv_status ckv_attn_decode_noalloc(const ckv_cache* cache, const int32_t
                                            int64_t max_seq_len, const void* q_f16, int32_t n_q,
                                            int32_t n_q_heads, float scale, int32_t n_split, float* out,
                                            float* lse, void* stream);
+
+/*
+ * read_noalloc_flag — ckv_read_device_flag for the built-in array of
+ * attn_decode_noalloc, whose address callers never see. Drains `stream`, stores
+ * the flag word in *flag (host memory), and when it is nonzero (1 = a bounded
+ * wait ran out, 2 = a seq_len outside [0, min(capacity, max_seq_len)], counted
+ * as 0) clears it and returns CKV_ERR_DEVICE_FLAG. No counterpart in the pages.
+ */
+CKV_API ckv_status ckv_read_noalloc_flag(int32_t* flag, void* stream);
 
 /*
  * attn_decode_f16 — the same decode over a dense fp16 KV cache (the private,

@@ -150,6 +150,7 @@ def test_decode_f16_and_merge_argument_checks(lib):
 def test_read_device_flag_checks(lib):
     flag = ctypes.c_int32(7)
     assert lib.ckv_read_device_flag(None, ctypes.byref(flag), None) == -1
+    assert lib.ckv_read_noalloc_flag(None, None) == -1
 
 
 def test_prefill_argument_checks(lib):
