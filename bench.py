@@ -51,15 +51,50 @@ METRIC = "compressed-KV decode attn: tokens/s and effective HBM GB/s (% of GB300
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM traffic (read + write) of one decode-kernel launch on gemma4_decode from
-# one ncu capture, valid for the kernel sources whose hash is recorded beside it
-# (null once they change).
-NCU_TRAFFIC = {"bytes": 48513536, "source_sha": "08e02f7ea6b9039d"}
+# DRAM traffic (read + write, bytes) of one step's kernels per workload, from
+# one ncu capture of the bench's own workload; each figure holds only for the
+# kernel sources whose hash is recorded beside it (null once they change).
+# Fan-out and prefill: the sum over the step's kernels (their rooflines time the whole step).
+NCU_TRAFFIC = {
+    "gemma4_decode": {"bytes": 48513792, "source_sha": "91b12a86972dbb35"},
+    "tiny_decode": {"bytes": 122112, "source_sha": "91b12a86972dbb35"},
+    "long_decode": {"bytes": 1547958528 + 3407872, "source_sha": "91b12a86972dbb35"},
+    "fanout_decode": {"bytes": 6431744 + 31771392 + 1004288, "source_sha": "15c606b8570e9538"},
+    "chunked_prefill": {"bytes": 8451328 + (113881856 + 57169920) + (106606592 + 23946496),
+                        "source_sha": "4a5d1ed4e56b9f4b"},
+}
+
+_DECODE_SOURCES = ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh",
+                   "ckv_kernels.cuh", "pack_common.cuh")
+_SOURCES = {
+    "decode": _DECODE_SOURCES,
+    "fanout": _DECODE_SOURCES + ("attn_decode_f16.cu", "lse_merge.cu", "attn_prefill.cu", "ckv_api.cu"),
+    "prefill": ("attn_prefill.cu", "kv_pack.cu", "pack_common.cuh", "ckv_device.cuh", "ckv_kernels.cuh",
+                "ckv_api.cu"),
+}
+
+
+def _source_sha(kind):
+    h = hashlib.sha256()
+    for name in _SOURCES[kind]:
+        with open(os.path.join(ROOT, "compressed_kv_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kind):
+    """The recorded ncu DRAM traffic of one step of `workload`, or None when
+    none is recorded for the current sources."""
+    rec = NCU_TRAFFIC.get(workload)
+    if rec and rec["source_sha"] == _source_sha(kind):
+        return rec["bytes"]
+    return None
 
 
 def _args():
     p = argparse.ArgumentParser()
-    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--gpus", type=int, default=None,
+                   help="ranks (one GPU each); without WORLD_SIZE in the environment, N > 1 starts N ranks")
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -68,6 +103,7 @@ def _args():
                             "kv_pack", "verify_decode", "dca_decode", "long_decode_tbq2", "long_decode_tbq4",
                             "long_decode_rot", "shared_prefill", "chunked_prefill_rot"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", action="store_true", help="skip the other workloads' figures")
     return p.parse_args()
 
 
@@ -79,15 +115,6 @@ def _peaks():
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
-
-
-def _decode_source_sha():
-    h = hashlib.sha256()
-    for name in ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh", "ckv_kernels.cuh",
-                 "pack_common.cuh"):
-        with open(os.path.join(ROOT, "compressed_kv_attention_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
 
 
 class ClockSampler:
@@ -227,7 +254,6 @@ class DecodeWork:
             self.ckv.attn_decode_append(c, self.seq, self.T, self.k_new, self.v_new, self.q, self.scale, self.out,
                                         self.lse, self.ws, stream=self.stream)
 
-    kernel_call = step
 
     def check(self):
         assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
@@ -277,8 +303,7 @@ class DecodeWork:
     def roofline(self, kernel_ms, peaks):
         hbm, _, kind = peaks
         achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
-        traffic = NCU_TRAFFIC["bytes"] if (self.w.name == "gemma4_decode" and
-                                           NCU_TRAFFIC["source_sha"] == _decode_source_sha()) else None
+        traffic = ncu_traffic(self.w.name, "decode")
         what = ("DCA regimes as three query rows" if self.dca else
                 "verify batch, per-row causal limits" if self.n_q > 1 else "append")
         return {"bound": "hbm",
@@ -351,7 +376,6 @@ class FanoutWork:
     def step(self, i):
         self._run(i, self.qa)
 
-    kernel_call = step
 
     def check(self):
         assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
@@ -381,7 +405,7 @@ class FanoutWork:
         achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
         return {"bound": "hbm", "kernel": "prefix decode + fp16 tail decode + lse merge (whole step)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "peak_kind": kind, "traffic": None, "algorithmic_bytes": self.algo_bytes,
+                "peak_kind": kind, "traffic": ncu_traffic("fanout_decode", "fanout"), "algorithmic_bytes": self.algo_bytes,
                 "launch_ms": round(kernel_ms, 6)}
 
 
@@ -426,7 +450,6 @@ class PrefillWork:
         self.ckv.attn_prefill(self.cache, self.nc, self.q, self.kn, self.vn, self.scale, self.out, self.lse,
                               self.ws, stream=self.stream)
 
-    kernel_call = step
 
     def between(self):
         with self.torch.cuda.stream(self.stream):
@@ -464,7 +487,7 @@ class PrefillWork:
         kern = f"attn_prefill_kernel<{self.D}, {self.w.v_bits}, {bool(self.w.rot_group)}>"
         return {"bound": "tensor", "kernel": kern + " (+ pack, de-rotation) on tcgen05",
                 "achieved": round(achieved, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(achieved / tf, 4),
-                "peak_kind": kind + " bf16 dense (fp16 operands run at the same rate)", "traffic": None,
+                "peak_kind": kind + " bf16 dense (fp16 operands run at the same rate)", "traffic": ncu_traffic(self.name, "prefill"),
                 "algorithmic_flops": self.flops, "launch_ms": round(kernel_ms, 6)}
 
 
@@ -514,7 +537,6 @@ class SharedPrefillWork:
         self.ckv.attn_prefill_shared(self.cache, self.P, self.kt, self.vt, self.tail_len, self.q, self.kn, self.vn,
                                      self.scale, self.out, self.lse, self.ws, stream=self.stream)
 
-    kernel_call = step
 
     def between(self):
         with self.torch.cuda.stream(self.stream):
@@ -589,7 +611,6 @@ class PackWork:
         k, v = self.ins[i % self.n_rot]
         self.ckv.kv_pack(self.caches[i % self.n_rot], 0, k, v, stream=self.stream)
 
-    kernel_call = step
 
     def check(self):
         pass
@@ -644,12 +665,108 @@ def max_over_ranks(values, dist=None, device="cpu"):
     return [float(v) for v in t.tolist()]
 
 
+def _graph_runner(work, stream, steps):
+    """CUDA graphs for `steps` back-to-back steps: one graph of per_big steps
+    replayed steps // per_big times, and one graph of the remaining steps, so
+    that a timed run of `steps` steps has at most a few graph-launch gaps."""
+    import torch
+    n_rot = getattr(work, "n_rot", 1)
+    reps = max(1, 128 // n_rot)
+    per_big = reps * n_rot
+    big = None
+    if steps >= per_big:
+        big = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(big, stream=stream):
+            for i in range(per_big):
+                work.step(i)
+    rem, tail = steps % per_big, None
+    if rem:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for i in range(rem):
+                work.step(i)
+
+    def run():
+        with torch.cuda.stream(stream):
+            for _ in range(steps // per_big):
+                big.replay()
+            if tail is not None:
+                tail.replay()
+    return run
+
+
+def measure(work, stream, dev, steps, warmup, dist=None):
+    """Time `steps` steps of `work` (after `warmup`), on the device with CUDA
+    events on the launching stream, bracketed by a barrier and a synchronize on
+    both sides; returns the whole timed region in ms (max over ranks)."""
+    import torch
+    n_rot = getattr(work, "n_rot", 1)
+    # Eager warm-up (configures kernel attributes before any capture).
+    with torch.cuda.stream(stream):
+        for i in range(max(n_rot, 2)):
+            work.step(i)
+    stream.synchronize()
+    work.check()
+    if work.graph:
+        run = _graph_runner(work, stream, steps)
+        warm = _graph_runner(work, stream, max(warmup, 3))
+        warm()
+        stream.synchronize()
+    else:
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, 3)):
+                work.between()
+                work.step(i)
+        stream.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if work.graph:
+        ms = _timed(stream, run, 1)
+    else:
+        ms = 0.0
+        for i in range(steps):
+            work.between()
+            ms += _timed(stream, lambda: work.step(i), 1)
+    torch.cuda.synchronize(dev)
+    if dist:
+        (ms,) = max_over_ranks([ms], dist, dev)
+        dist.barrier()
+    work.check()
+    return ms
+
+
+# Other single-GPU workloads measured in the same run as the headline (steps, warm-up).
+PER_CONFIG = (("tiny_decode", 2000, 100), ("fanout_decode", 1000, 50), ("long_decode", 200, 10),
+              ("chunked_prefill", 5, 3))
+
+
+def per_config_lines(dev, stream, peaks):
+    """ms per step, roofline fraction and ncu traffic of each other workload."""
+    import torch
+    res = {}
+    for name, steps, warm in PER_CONFIG:
+        work = _make_work(name, dev, stream)
+        ms = measure(work, stream, dev, steps, warm)
+        rl = work.roofline(ms / steps, peaks)
+        res[name] = {"ms_per_step": round(ms / steps, 6), "steps": steps,
+                     "tokens_per_s": round(work.tokens_per_step * steps / (ms / 1e3), 1),
+                     "bound": rl["bound"], "achieved": rl["achieved"], "unit": rl["unit"], "frac": rl["frac"],
+                     "traffic": rl["traffic"], "kernel": rl["kernel"]}
+        del work
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        sys.stderr.write(f"bench.py: rank {rank} of {world}: no CUDA device\n")
+        sys.exit(3)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -658,72 +775,12 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(dev)
     work = _make_work(args.workload, dev, stream)
-    n_rot = getattr(work, "n_rot", 1)
-
-    # Eager warm-up (configures kernel attributes before any capture).
-    with torch.cuda.stream(stream):
-        for i in range(max(n_rot, 2)):
-            work.step(i)
-    stream.synchronize()
-    work.check()
-
-    if work.graph:
-        reps = max(1, 128 // n_rot)
-        per_big = reps * n_rot
-        big, single, kgraph = torch.cuda.CUDAGraph(), [], torch.cuda.CUDAGraph()
-        with torch.cuda.graph(big, stream=stream):
-            for i in range(per_big):
-                work.step(i)
-        for i in range(n_rot):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                work.step(i)
-            single.append(g)
-        with torch.cuda.graph(kgraph, stream=stream):
-            for i in range(per_big):
-                work.kernel_call(i)
-
-        def run_steps(n):
-            with torch.cuda.stream(stream):
-                for _ in range(n // per_big):
-                    big.replay()
-                for i in range(n % per_big):
-                    single[i % n_rot].replay()
-    else:
-        def run_steps(n):
-            with torch.cuda.stream(stream):
-                for i in range(n):
-                    work.step(i)
-
-    run_steps(max(args.warmup, 3))
-    stream.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    if work.graph:
-        ms = _timed(stream, lambda: run_steps(args.steps), 1)
-    else:
-        ms = 0.0
-        for i in range(args.steps):
-            work.between()
-            ms += _timed(stream, lambda: work.step(i), 1)
-    torch.cuda.synchronize(dev)
-    if dist:
-        (ms,) = max_over_ranks([ms], dist, dev)
-        dist.barrier()
-
-    # The dominant kernel call alone, back to back.
-    if work.graph:
-        n_k = max(1, 2000 // per_big) * per_big
-        k_ms = _timed(stream, kgraph.replay, n_k // per_big) / n_k
-    else:
-        k_ms = ms / args.steps
+    ms = measure(work, stream, dev, args.steps, args.warmup, dist)
     clocks = sampler.stop()
-    work.check()
 
     # End to end through the public API with pinned host buffers, eager calls.
     h2d, d2h = work.e2e_setup()
@@ -748,9 +805,11 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": getattr(work, "dtype", "f16 mma, f32 accumulate (int8 / 3-bit storage)"),
         "data": "synthetic",
         "config": dict(work.describe(), parallelism=f"replicas x{world}",
-                       timing="CUDA graphs, events on the launching stream" if work.graph else
-                       "events around each step on the launching stream"),
-        "roofline": work.roofline(k_ms, peaks),
+                       timing=("CUDA graphs of exactly `steps` back-to-back steps, events on the launching stream"
+                               if work.graph else "events around each step on the launching stream")),
+        # the step is one launch of the dominant kernel (decode) or its whole
+        # call (prefill, fan-out): the roofline uses the timed region itself
+        "roofline": work.roofline(ms / args.steps, peaks),
         "e2e": {"value": round(world * work.tokens_per_step * n_e2e / e2e_s, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "api": "public Python API, eager"},
@@ -761,9 +820,13 @@ def run_ours(args):
         line["effective_gbs"] = round(work.algo_bytes * world * args.steps / (ms / 1e3) / 1e9, 1)
     if hasattr(work, "flops"):
         line["effective_tflops"] = round(work.flops * world * args.steps / (ms / 1e3) / 1e12, 1)
+    del work
+    torch.cuda.empty_cache()
+    if args.workload == "gemma4_decode" and not args.no_per_config:
+        line["per_config"] = per_config_lines(dev, stream, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ("gemma4_decode",
                                                                                    "chunked_prefill"):
-        line["cpu_baseline"] = cpu_baseline(args.workload, min_seconds=10.0)
+        line["cpu_baseline"] = cpu_baseline(args.workload)
     if dist:
         dist.destroy_process_group()
     if rank == 0:
@@ -772,7 +835,11 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ oracle --
 
+ORACLE_CHUNK = 2048  # tokens per oracle work unit
+
+
 def _oracle_setup(sample_tokens=None, workload="gemma4_decode"):
+    """Seeded inputs of one step and the oracle's quantised cache fields."""
     import numpy as np
     from compressed_kv_attention_gb300 import inputs
     from tests import helpers as H
@@ -790,16 +857,81 @@ def _oracle_setup(sample_tokens=None, workload="gemma4_decode"):
                 qs=qs, d16=d16, codes=codes, n16=n16)
 
 
-def _oracle_step(s):
-    """Oracle work for one query token: quantise the new token, dequantise the
-    cache to dense float64, softmax attention for every query head
-    (decompress-then-attend)."""
+# Worker side of the oracle pool: the step's arrays, memory-mapped from files
+# the parent wrote (spawned processes, one BLAS thread each).
+_OW = {}
+
+
+def _oracle_worker_init(paths):
+    import numpy as np
+    for k, pth in paths.items():
+        _OW[k] = np.load(pth, mmap_mode="r")
+
+
+def _oracle_unit(unit):
+    """Oracle work of one (kv head, token chunk): dequantise the chunk to dense
+    float64 and attend with the kv head's query heads. Returns the partial
+    (output, lse) of those heads over the chunk."""
+    import numpy as np
     from oracle import ckv_oracle as O
-    O.q8_0_quantize(s["k_new"])
-    O.tbq3_quantize(s["v_new"], s["signs"])
-    kh = O.q8_0_dequantize(s["qs"], s["d16"])
-    vh = O.tbq3_dequantize(s["codes"], s["n16"], s["signs"])
-    return O.decode_reference(s["q"], kh, vh, s["Ts"], 1.0 / math.sqrt(s["D"]))
+    h, a, b, G, scale = unit
+    kh = O.q8_0_dequantize(np.asarray(_OW["qs"][h, a:b]), np.asarray(_OW["d16"][h, a:b]))
+    vh = O.tbq3_dequantize(np.asarray(_OW["codes"][h, a:b]), np.asarray(_OW["n16"][h, a:b]),
+                           np.asarray(_OW["signs"]))
+    q = np.asarray(_OW["q"][0, h * G:(h + 1) * G], dtype=np.float64)
+    o, lse = O.attention(q, kh, vh, scale)
+    return h, o, lse
+
+
+class OraclePool:
+    """The oracle's decode step over a pool of spawned processes: independent
+    (kv head, 2048-token chunk) units, each dequantise-then-attend, combined
+    per query head with the oracle's exact log-sum-exp merge."""
+
+    def __init__(self, s, procs):
+        import multiprocessing as mp
+        import numpy as np
+        self.s = s
+        self.dir = tempfile.mkdtemp(prefix="ckv_oracle_")
+        paths = {}
+        for k in ("qs", "d16", "codes", "n16", "signs", "q"):
+            paths[k] = os.path.join(self.dir, k + ".npy")
+            np.save(paths[k], s[k])
+        G = s["Hq"] // s["Hkv"]
+        scale = 1.0 / math.sqrt(s["D"])
+        self.units = [(h, a, min(a + ORACLE_CHUNK, s["Ts"]), G, scale)
+                      for h in range(s["Hkv"]) for a in range(0, s["Ts"], ORACLE_CHUNK)]
+        # One BLAS thread per process: children take the environment at spawn time.
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(procs, initializer=_oracle_worker_init, initargs=(paths,))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.procs = procs
+
+    def step(self):
+        from oracle import ckv_oracle as O
+        s = self.s
+        O.q8_0_quantize(s["k_new"])
+        O.tbq3_quantize(s["v_new"], s["signs"])
+        parts = {}
+        for h, o, lse in self.pool.map(self._unit, self.units, chunksize=1):
+            parts.setdefault(h, []).append((o, lse))
+        return {h: O.lse_merge([p[0] for p in ps], [p[1] for p in ps]) for h, ps in parts.items()}
+
+    _unit = staticmethod(_oracle_unit)
+
+    def close(self):
+        import shutil
+        self.pool.close()
+        self.pool.join()
+        shutil.rmtree(self.dir, ignore_errors=True)
 
 
 def _cores():
@@ -809,26 +941,53 @@ def _cores():
         return os.cpu_count()
 
 
-def cpu_baseline(workload="gemma4_decode", min_seconds=10.0, max_seconds=30.0):
-    """The oracle timed on the host cores. Decode: whole decode steps. Prefill:
-    one query token's work over the full key range (the last query's), in
-    query tokens per second."""
-    s = _oracle_setup(workload=workload)
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _time_pool(pool, min_seconds, max_seconds):
+    pool.step()  # warm: workers loaded, pages mapped
     n, t0 = 0, time.perf_counter()
     while True:
-        _oracle_step(s)
+        pool.step()
         n += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or el * (n + 1) / n > max_seconds:
-            break
-    rate = n / el
-    if workload == "chunked_prefill":
-        sample = (f"{n} query tokens of chunked_prefill, each attending over {s['Ts']} dequantised tokens "
-                  "(the last query's key range), numpy float64")
-    else:
-        sample = (f"{n} full decode steps of {workload} (dequantise {s['T']} tokens x {s['Hkv']} kv heads to "
-                  "float64, attend 16 heads), numpy float64")
-    return {"value": round(rate, 4), "unit": "tokens/s", "cores": _cores(), "kind": "oracle", "sample": sample}
+            return n, el
+
+
+def cpu_baseline(workload="gemma4_decode", min_seconds=8.0, max_seconds=20.0):
+    """The oracle timed on the host cores, single-threaded and over every core.
+    Decode: whole decode steps. Prefill: one query token's work over the full key
+    range (the last query's), in query tokens per second."""
+    s = _oracle_setup(workload=workload)
+    cores = _cores()
+    res = {}
+    for label, procs in (("single_thread", 1), ("all_cores", cores)):
+        pool = OraclePool(s, procs)
+        try:
+            n, el = _time_pool(pool, min_seconds, max_seconds)
+        finally:
+            pool.close()
+        res[label] = {"value": round(n / el, 4), "processes": procs, "steps": n, "seconds": round(el, 2)}
+    what = ("query tokens of chunked_prefill, each attending over the last query's "
+            f"{s['Ts']} dequantised tokens" if workload == "chunked_prefill" else
+            f"full decode steps of {workload} (dequantise {s['T']} tokens x {s['Hkv']} kv heads to float64, "
+            f"attend {s['Hq']} heads)")
+    sample = (f"{res['all_cores']['steps']} {what}, numpy float64, as (kv head, {ORACLE_CHUNK}-token chunk) units "
+              f"over {cores} spawned processes of one BLAS thread, merged by the oracle's lse_merge; single-thread: "
+              f"{res['single_thread']['steps']} steps in one such process")
+    return {"value": res["all_cores"]["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "single_thread": res["single_thread"], "all_cores": res["all_cores"],
+            "cpu_model": _cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_reference(args):
@@ -836,39 +995,70 @@ def run_reference(args):
     if rank != 0:
         return
     workload = args.workload if args.workload in ("gemma4_decode", "chunked_prefill") else "gemma4_decode"
-    # Size each step's sample so that warm-up + timed steps take about 2 minutes:
-    # a step attends over the first Ts tokens of the cache and its time is
-    # scaled by T / Ts to a full step.
-    cal = _oracle_setup(sample_tokens=1024, workload=workload)
-    t0 = time.perf_counter()
-    _oracle_step(cal)
-    full_est = (time.perf_counter() - t0) * cal["T"] / cal["Ts"]
+    cores = _cores()
+    # Size each step's sample so that warm-up + timed steps take about 2
+    # minutes: a step attends over the first Ts tokens of the cache and its
+    # time is scaled by T / Ts to a full step.
+    cal = OraclePool(_oracle_setup(sample_tokens=cores * ORACLE_CHUNK // 2, workload=workload), cores)
+    try:
+        cal.step()
+        t0 = time.perf_counter()
+        cal.step()
+        full_est = (time.perf_counter() - t0) * cal.s["T"] / cal.s["Ts"]
+    finally:
+        cal.close()
     per_step = 120.0 / max(1, args.steps + args.warmup)
-    Ts = int(min(cal["T"], max(16, (cal["T"] * per_step / full_est) // 16 * 16)))
-    s = _oracle_setup(sample_tokens=Ts, workload=workload)
-    frac = s["Ts"] / s["T"]
-    for _ in range(max(args.warmup, 0)):
-        _oracle_step(s)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        _oracle_step(s)
-    el = (time.perf_counter() - t0) / frac
+    Ts = int(min(cal.s["T"], max(16, (cal.s["T"] * per_step / full_est) // 16 * 16)))
+    pool = OraclePool(_oracle_setup(sample_tokens=Ts, workload=workload), cores)
+    try:
+        s = pool.s
+        frac = s["Ts"] / s["T"]
+        for _ in range(max(args.warmup, 1)):
+            pool.step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pool.step()
+        el = (time.perf_counter() - t0) / frac
+    finally:
+        pool.close()
     value = args.steps / el
-    sample = (f"each step: oracle work for one query token (dequantise to float64 + attend 16 heads) over "
-              f"{s['Ts']} of {s['T']} tokens of {workload}, time scaled by {1 / frac:.2f}")
+    sample = (f"each step: oracle work for one query token (dequantise to float64 + attend {s['Hq']} heads) over "
+              f"{s['Ts']} of {s['T']} tokens of {workload}, as (kv head, {ORACLE_CHUNK}-token chunk) units over "
+              f"{cores} spawned processes, time scaled by {1 / frac:.2f}")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / max(args.steps, 1) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": workload, "sample": sample},
-        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample, "cpu_model": _cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n, argv):
+    """Start `n` ranks of this script (one per GPU of this node) with
+    torch.distributed.run on 127.0.0.1; returns the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main():
     args = _args()
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus is not None and args.gpus > 1:
+        sys.exit(launch_ranks(args.gpus, sys.argv[1:]))
+    if env_world is not None and args.gpus is not None and int(env_world) != args.gpus:
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={env_world}\n")
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -76,9 +76,12 @@ def test_prefill_small(D, Hkv, Hq, n_cached, n_new):
         H.check_attention(out[b], lse[b], o_ref, l_ref, f"prefill D={D} b={b}")
 
 
-def test_chunked_prefill_workload_sampled():
-    """2048 new queries over 32768 cached tokens (Gemma-4 global-layer shapes):
-    query tokens sampled across every 128-row tile position and the last one."""
+def test_chunked_prefill_workload():
+    """2048 new queries over 32768 cached tokens (Gemma-4 global-layer shapes),
+    in the benchmark's launch configuration: every query row of kv head 0 (all
+    2048 tokens x its 8 query heads, each over its causal key range) checked in
+    full, and query tokens sampled across every 128-row tile position for both
+    kv heads."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     w = inputs.WORKLOADS["chunked_prefill"]
@@ -87,7 +90,18 @@ def test_chunked_prefill_workload_sampled():
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     rows = [0, 1, 15, 16, 17, 500, 1023, 1024, 1777, 2046, 2047]
     o_ref, l_ref = _oracle(k, v, qf, signs, nc, 0, rows=rows)
-    H.check_attention(out[0][rows], lse[0][rows], o_ref, l_ref, "chunked prefill")
+    H.check_attention(out[0][rows], lse[0][rows], o_ref, l_ref, "chunked prefill (sampled)")
+    # Kv head 0 in full, chunked over the keys: query i sees [0, nc + i].
+    kt = np.ascontiguousarray(k[0, :, 0])
+    vt = np.ascontiguousarray(v[0, :, 0])
+    qs, d16, codes, n16, _ = H.oracle_quantize(kt, vt, signs)
+    kh, vh = O.q8_0_dequantize(qs, d16), O.tbq3_dequantize(codes, n16, signs)
+    qpos = np.arange(nn)
+    for h in [hq for hq in range(Hq) if O.kv_head_of(hq, Hq, Hkv) == 0]:
+        o_ref, l_ref = H.oracle_attention_chunked(
+            qf[0, :, h], lambda a, b: kh[a:b], lambda a, b: vh[a:b], nc + nn, 1.0 / math.sqrt(D),
+            visible_of=lambda a, b: np.arange(a, b)[None, :] <= nc + qpos[:, None])
+        H.check_attention(out[0, :, h], lse[0, :, h], o_ref, l_ref, f"chunked prefill kv head 0, q head {h}")
 
 
 def test_prefill_stream_k_schedule():
@@ -103,3 +117,30 @@ def test_prefill_stream_k_schedule():
     for b in range(B):
         o_ref, l_ref = _oracle(k, v, qf, signs, nc, b)
         H.check_attention(out[b], lse[b], o_ref, l_ref, f"stream-K prefill b={b}")
+
+
+def _stream_k_applies(B, Hkv, Hq, nc, nn, sms):
+    """The prefill's schedule rule, restated: more 128-row tiles than SMs, and
+    every CTA's share of the 64-key steps at least as long as any tile."""
+    qt = 128 // (Hq // Hkv)
+    n_qt = -(-nn // qt)
+    steps = [-(-(nc + min((t + 1) * qt, nn)) // 64) for t in range(n_qt)]
+    return B * Hkv * n_qt > sms and B * Hkv * sum(steps) // sms >= max(steps)
+
+
+def test_prefill_stream_k_schedule_d512():
+    """The stream-K schedule at head_dim 512 (Gemma-4 shapes, 2 sequences of
+    2048 cached + 1024 new tokens: 256 tiles of 16 tokens x 8 heads): every
+    row of both sequences checked, including the rows of tiles cut between two
+    CTAs at the full head dim."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    D, Hkv, Hq, B, nc, nn = 512, 2, 16, 2, 2048, 1024
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _stream_k_applies(B, Hkv, Hq, nc, nn, sms)
+    cap = nc + nn + 16
+    k, v, qf, signs, out, lse = _case(D, Hkv, Hq, B, nc, nn, cap, seed=78)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    for b in range(B):
+        o_ref, l_ref = _oracle(k, v, qf, signs, nc, b)
+        H.check_attention(out[b], lse[b], o_ref, l_ref, f"stream-K prefill D=512 b={b}")

@@ -52,7 +52,26 @@ def test_max_over_ranks_single_process():
 
 def test_reference_arm_runs_on_rank_zero_only():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
-    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                          "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
     assert res.returncode == 0
     assert res.stdout.strip() == ""
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    # Without WORLD_SIZE, `bench.py --gpus 2` starts two ranks itself
+    # (torch.distributed.run on 127.0.0.1). On this host neither rank finds a
+    # GPU, so each reports its rank and the world size and the run fails.
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1",
+                          "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode != 0
+    assert "rank 0 of 2: no CUDA device" in res.stderr and "rank 1 of 2: no CUDA device" in res.stderr
+
+
+def test_gpus_flag_must_match_world_size():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="2", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "4", "--steps", "1"],
+                         env=env, capture_output=True, text=True, timeout=120)
+    assert res.returncode == 2 and "WORLD_SIZE=2" in res.stderr
