@@ -736,6 +736,42 @@ def measure(work, stream, dev, steps, warmup, dist=None):
     return ms
 
 
+def _graph_time_ms(fn, stream, n):
+    """ms per call of fn(i), n calls back to back in one CUDA graph (after 3 eager calls)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fn(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+        g.replay()
+        stream.synchronize()
+    return _timed(stream, g.replay, 1) / n
+
+
+def stream_floor(work, stream, dev, n=2000):
+    """The decode's data movement alone on the same cache copies (ckv_calibrate_stream):
+    the same split grid and staging, no compute; then with the split rendezvous."""
+    import torch
+    ckv = work.ckv
+    n_tiles = work.T // 16
+    streams = work.B * work.Hkv
+    rec = work.cache_bytes // (streams * n_tiles)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_split = max(1, min(sms // streams, n_tiles // 4))
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    res = {"n_split": n_split, "record_bytes": rec}
+    for key, rv in (("stream_us", 0), ("stream_rendezvous_us", 1)):
+        ms = _graph_time_ms(lambda i: ckv.calibrate_stream(work.caches[i % work.n_rot].data, n_tiles, rec, streams,
+                                                           n_split, rv, ws, stream=stream), stream, n)
+        res[key] = round(ms * 1e3, 3)
+    assert ckv.read_device_flag(ws, stream=stream) == 0
+    return res
+
+
 # Other single-GPU workloads measured in the same run as the headline (steps, warm-up).
 PER_CONFIG = (("tiny_decode", 2000, 100), ("fanout_decode", 1000, 50), ("long_decode", 200, 10),
               ("chunked_prefill", 5, 3))
@@ -820,6 +856,13 @@ def run_ours(args):
         line["effective_gbs"] = round(work.algo_bytes * world * args.steps / (ms / 1e3) / 1e9, 1)
     if hasattr(work, "flops"):
         line["effective_tflops"] = round(work.flops * world * args.steps / (ms / 1e3) / 1e12, 1)
+    if args.workload == "gemma4_decode" and not args.no_per_config:
+        fl = stream_floor(work, stream, dev)
+        fl["decode_us"] = round(ms / args.steps * 1e3, 3)
+        fl["floor_frac"] = round(work.algo_bytes / (fl["stream_us"] / 1e6) / 1e9 / peaks[0], 4)
+        fl["what"] = ("ckv_calibrate_stream on the same cache copies: the decode's grid, staging and programmatic "
+                      "launch with no compute (then with the split rendezvous), back to back in a graph")
+        line["floor"] = fl
     del work
     torch.cuda.empty_cache()
     if args.workload == "gemma4_decode" and not args.no_per_config:

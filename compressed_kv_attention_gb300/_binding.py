@@ -74,6 +74,7 @@ SIGNATURES = {
                                          _c_int, _c_f, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_read_device_flag": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
     "ckv_read_noalloc_flag": (_c_int, [ctypes.POINTER(_c_int), _vp]),
+    "ckv_calibrate_stream": (_c_int, [_vp, _c_i64, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
 }
 
 
@@ -316,3 +317,10 @@ def selftest_bounded_waits(workspace, stream=None):
     """Run the kernels' two bounded-wait forms on events that never come; afterwards the int32
     words at workspace bytes 0 and 4 read 1 (workspace: >= 256 zero-filled device bytes)."""
     _check(load().ckv_selftest_bounded_waits(_ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def calibrate_stream(src, n_tiles: int, record_bytes: int, n_streams: int, n_split: int, rendezvous: bool,
+                     workspace, stream=None):
+    """Stream the records at `src` (a device tensor) through the decode's staging without computing."""
+    _check(load().ckv_calibrate_stream(_ptr(src), n_tiles, record_bytes, n_streams, n_split, int(rendezvous),
+                                       _ptr(workspace), workspace.numel(), _stream(stream)))

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libckv.so")
 SOURCES = ["kv_pack.cu", "attn_decode.cu", "attn_decode_tbq2.cu", "attn_decode_tbq4.cu", "attn_decode_rot2.cu",
            "attn_decode_rot3.cu", "attn_decode_rot4.cu", "attn_decode_f16.cu", "lse_merge.cu", "attn_prefill.cu",
-           "ckv_api.cu", "attn_decode_noalloc.cu", "selftest.cu"]
+           "ckv_api.cu", "attn_decode_noalloc.cu", "selftest.cu", "stream_floor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -170,6 +170,24 @@ CKV_API ckv_status ckv_kv_pack(const ckv_cache* cache, int64_t tok_offset, int64
 CKV_API ckv_status ckv_selftest_bounded_waits(void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * calibrate_stream — a measuring aid with no counterpart in the pages: the
+ * decode's data movement alone. Streams n_streams runs of n_tiles records of
+ * record_bytes each (device memory at src, 16-byte aligned, record_bytes a
+ * multiple of 16, 4 x 4 records <= 200 KB), split over n_split CTAs per run,
+ * through the decode's staging (bulk copies of 4 records into a 4-stage
+ * shared-memory ring, programmatic launch) and computes nothing; with
+ * rendezvous != 0 the CTAs of a run then meet on a counter as the decode's
+ * split merge does (refused with CKV_ERR_UNSUPPORTED unless the grid fits on
+ * the device at once). Its time per launch, back to back, is the floor of any
+ * kernel with that launch shape on those bytes. workspace: 64 + 8 n_streams
+ * zero-filled device bytes, 256-byte aligned (flag at 0, counters from 64,
+ * left at zero). Asynchronous on `stream`.
+ */
+CKV_API ckv_status ckv_calibrate_stream(const void* src, int64_t n_tiles, int32_t record_bytes, int32_t n_streams,
+                                        int32_t n_split, int32_t rendezvous, void* workspace, size_t ws_bytes,
+                                        void* stream);
+
+/*
  * attn_decode — attention of n_q query tokens per sequence over the packed
  * cache, every query seeing cached positions [0, seq_len[b]).
  *

@@ -151,6 +151,7 @@ def test_read_device_flag_checks(lib):
     flag = ctypes.c_int32(7)
     assert lib.ckv_read_device_flag(None, ctypes.byref(flag), None) == -1
     assert lib.ckv_read_noalloc_flag(None, None) == -1
+    assert lib.ckv_calibrate_stream(None, 16, 11808, 1, 1, 0, None, 0, None) == -1
 
 
 def test_prefill_argument_checks(lib):
