@@ -314,7 +314,8 @@ class DecodeWork:
 
 
 class FanoutWork:
-    """Shared-prefix fan-out: prefix decode (15 agents as 15 query tokens) + fp16 tails + LSE merge."""
+    """Shared-prefix fan-out: prefix decode (15 agents as 15 query tokens), then the fp16 tails' decode whose
+    split merge takes in the prefix partial (attn_decode_f16_merge)."""
 
     graph = True
 
@@ -347,19 +348,17 @@ class FanoutWork:
                 self.tails.append((kt, vt))
             self.o_pre = torch.empty((1, A, Hq, D), dtype=torch.float32, device=dev)
             self.l_pre = torch.empty((1, A, Hq), dtype=torch.float32, device=dev)
-            self.o_t = torch.empty((A, 1, Hq, D), dtype=torch.float32, device=dev)
-            self.l_t = torch.empty((A, 1, Hq), dtype=torch.float32, device=dev)
             self.out = torch.empty((A * Hq, D), dtype=torch.float32, device=dev)
             self.lse = torch.empty(A * Hq, dtype=torch.float32, device=dev)
             self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], P, A, Hq), dtype=torch.uint8,
                                   device=dev)
-            self.ws_t = torch.zeros(ckv.attn_decode_f16_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8,
+            self.ws_t = torch.zeros(ckv.attn_decode_f16_merge_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8,
                                     device=dev)
             self.seq_p = torch.full((1,), P, dtype=torch.int32, device=dev)
             self.seq_t = torch.full((A,), TL, dtype=torch.int32, device=dev)
         stream.synchronize()
         self.tokens_per_step = A
-        self.launches_per_step = 3  # prefix decode, tail decode, merge
+        self.launches_per_step = 2  # prefix decode, tail decode with the merge
         self.algo_bytes = Hkv * P * inputs.compressed_bytes_per_token(D) + 2 * A * Hkv * TL * D * 2
 
     def _run(self, i, qa):
@@ -368,10 +367,10 @@ class FanoutWork:
         # The agents' queries as 15 query tokens of one sequence over the prefix,
         # and as 15 sequences of one query token over their own tails.
         ckv.attn_decode(c, self.seq_p, self.P, qa[None], self.scale, self.o_pre, self.l_pre, self.ws, stream=s)
-        ckv.attn_decode_f16(kt, vt, self.seq_t, self.TL, qa[:, None], self.scale, self.o_t, self.l_t, self.ws_t,
-                            stream=s)
-        ckv.lse_merge([self.o_pre.view(-1, self.D), self.o_t.view(-1, self.D)],
-                      [self.l_pre.view(-1), self.l_t.view(-1)], self.out, self.lse, stream=s)
+        A, Hq, D = self.A, self.Hq, self.D
+        ckv.attn_decode_f16_merge(kt, vt, self.seq_t, self.TL, qa[:, None], self.scale, self.o_pre.view(A, 1, Hq, D),
+                                  self.l_pre.view(A, 1, Hq), self.out.view(A, 1, Hq, D), self.lse.view(A, 1, Hq),
+                                  self.ws_t, stream=s)
 
     def step(self, i):
         self._run(i, self.qa)
@@ -397,13 +396,13 @@ class FanoutWork:
     def describe(self):
         return {"workload": "fanout_decode", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
                 "agents": self.A, "prefix_tokens": self.P, "tail_tokens": self.TL,
-                "step": "attn_decode(prefix, 15 agents) + attn_decode_f16(tails) + lse_merge",
+                "step": "attn_decode(prefix, 15 agents) + attn_decode_f16_merge(tails, merged with the prefix)",
                 "l2": f"rotating {self.n_rot} copies ({self.n_rot * self.per_copy / 1e6:.0f} MB > 4x L2)"}
 
     def roofline(self, kernel_ms, peaks):
         hbm, _, kind = peaks
         achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "prefix decode + fp16 tail decode + lse merge (whole step)",
+        return {"bound": "hbm", "kernel": "prefix decode + fp16 tail decode with the merge (whole step)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_kind": kind, "traffic": ncu_traffic("fanout_decode", "fanout"), "algorithmic_bytes": self.algo_bytes,
                 "launch_ms": round(kernel_ms, 6)}

@@ -56,6 +56,9 @@ SIGNATURES = {
     "ckv_attn_decode_noalloc": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp,
                                          _vp, _vp]),
     "ckv_attn_decode_f16_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
+    "ckv_attn_decode_f16_merge_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
+    "ckv_attn_decode_f16_merge": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
+                                           _c_int, _c_f, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_attn_decode_f16": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
                                      _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_lse_merge": (_c_int, [_c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _c_i64, _c_int, _vp, _vp,
@@ -221,6 +224,23 @@ def attn_decode_f16_workspace(head_dim: int, n_kv_heads: int, batch: int, max_se
                               n_q_heads: int, n_split: int = 0) -> int:
     return int(load().ckv_attn_decode_f16_workspace(head_dim, n_kv_heads, batch, max_seq_len, n_q,
                                                     n_q_heads, n_split))
+
+
+def attn_decode_f16_merge_workspace(head_dim: int, n_kv_heads: int, batch: int, max_seq_len: int, n_q: int,
+                                    n_q_heads: int, n_split: int = 0) -> int:
+    return int(load().ckv_attn_decode_f16_merge_workspace(head_dim, n_kv_heads, batch, max_seq_len, n_q,
+                                                          n_q_heads, n_split))
+
+
+def attn_decode_f16_merge(k, v, seq_len, max_seq_len: int, q, scale: float, prior_o, prior_lse, out, lse,
+                          workspace, n_split: int = 0, stream=None):
+    """attn_decode_f16 merged exactly with a prior partial (rows and lse laid out as out / lse)."""
+    batch, n_kv_heads, capacity, D = k.shape
+    _, n_q, n_q_heads, _ = q.shape
+    _check(load().ckv_attn_decode_f16_merge(_ptr(k), _ptr(v), D, n_kv_heads, batch, capacity, _ptr(seq_len),
+                                            max_seq_len, _ptr(q), n_q, n_q_heads, scale, n_split, _ptr(prior_o),
+                                            _ptr(prior_lse), _ptr(out), _ptr(lse), _ptr(workspace),
+                                            workspace.numel(), _stream(stream)))
 
 
 def attn_decode_f16(k, v, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,

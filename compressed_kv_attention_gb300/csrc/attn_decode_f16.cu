@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   }
   const __half* kb = a.k16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
   const __half* vb = a.v16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
+  }
 
   uint32_t qf[C::NB_W][4];
   {
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
     decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
                                              nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
+    if (a.prior_o && split == 0) write_prior_slot<D>(a, gid, b, kvh, rg, tid, C::THREADS);
     decode_split_tail<D, C::RED_BYTES, C::THREADS>(a, split, gid, b, kvh, rg, tid, smem);
   }
 }
@@ -223,7 +225,7 @@ static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (a.n_split == 1 && a.n_row_groups >= C::NP) {
+  if (a.n_split == 1 && a.n_row_groups >= C::NP && !a.prior_o) {
     // Row-parallel CTAs: NP row groups each, no split merge.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, (a.n_row_groups + C::NP - 1) / C::NP, a.batch * a.n_kv_heads);

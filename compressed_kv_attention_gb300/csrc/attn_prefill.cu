@@ -157,6 +157,15 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   __shared__ const uint8_t* s_stream;
   __shared__ float* s_slot;  // nullptr: rows to `out`
 
+  // Split decode: the sequence length of this CTA's tile, loaded now so that
+  // its latency overlaps the setup below.
+  int split_len = 0;
+  if constexpr (SPLIT) {
+    if (tid == 0) {
+      const int64_t bh = (blockIdx.x / a.n_split) / n_qt;
+      split_len = a.seq_len[bh / a.n_kv_heads];
+    }
+  }
   if (warp == 0) tmem_alloc(&s_tmem, 512);
   if (tid == 0) {
     mbar_init(&s_bar, 1);
@@ -184,12 +193,20 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
   const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
 
   // ---- Q tile: bf16 -> fp16 (exact in range), 128-byte swizzled K-major ----
+  // fp16 queries arrive by asynchronous copies that the caller waits for
+  // (q_wait) after issuing the first step's code loads, so the two overlap.
+  // Many CTAs load the same tile at once (the splits of a many-row decode):
+  // each starts its walk over the tile's 16-byte pieces at its own offset, so
+  // that they do not all request the same L2 lines together.
+  constexpr int QPIECES = C::M * (D / 8);
+  const int q_rot = static_cast<int>((blockIdx.x * 37u) % (QPIECES / C::THREADS)) * C::THREADS;
   auto load_q = [&]() {
   if (a.q_f16) {
     // fp16 queries go to shared memory as they are: 16-byte asynchronous
     // copies, all in flight at once (a split decode runs few steps per CTA,
     // so this load is not amortised).
-    for (int piece = tid; piece < C::M * (D / 8); piece += C::THREADS) {
+    for (int pc = tid; pc < QPIECES; pc += C::THREADS) {
+      const int piece = pc + q_rot < QPIECES ? pc + q_rot : pc + q_rot - QPIECES;
       const int r = piece / (D / 8), k0 = (piece % (D / 8)) * 8;
       const int qi = s_q0 + r / group_q, h = s_kvh * group_q + r % group_q;
       const uint32_t dst = smem_u32(sQ + sw128_offset(r, k0, C::M));
@@ -200,7 +217,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
       }
     }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
     return;
   }
   for (int piece = tid; piece < C::M * (D / 8); piece += C::THREADS) {
@@ -599,38 +616,69 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     }
 
     // ---- normalise and write the rotated-basis rows; lse ----
+    // A thread holds one row, so row-wise global stores would scatter each
+    // warp instruction over 32 rows. The rows pass through shared memory
+    // instead (the Q tile, free after the last step until the next segment
+    // loads its own), CW columns at a time, 16-byte units XOR-swizzled by the
+    // row, and each warp then writes whole contiguous row pieces.
     if constexpr (SM) {
+      constexpr int CW = D / 2 < 128 ? D / 2 : 128;  // columns per pass: 128 rows x CW floats fit in the Q tile
+      constexpr int U = CW / 4;                     // 16-byte units per row piece
+      constexpr int RPI = 32 / U;                   // rows one warp instruction covers
       const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
       float* const slot = s_slot;
-      const int h = s_kvh * group_q + row % group_q;
-      const int row_qi = s_q0 + row / group_q;
-      const bool wr = slot ? true : row_qi < a.n_new;
-      const int64_t orow_i = ((int64_t)s_b * a.n_new + row_qi) * a.n_q_heads + h;
-      float* orow = slot ? slot + (int64_t)row * D : a.out + orow_i * D;
-      float* olse = slot ? slot + (int64_t)C::M * D + row : a.lse + orow_i;
-#pragma unroll 1
-      for (int c0 = 0; c0 < C::OT; c0 += 32) {
-        uint32_t ov[32];
-        if (s_s0 < s1) {
-          tmem_ld32(row_tmem + 64 + c0, ov);
-          tmem_ld_wait();
-        } else {
+      float* const sT = reinterpret_cast<float*>(sQ);
+      static_assert(C::M * CW * 4 <= C::M * D * 2 && CW % 32 == 0, "transpose buffer");
+      // Output row of tile row rr (nullptr: a row past the last query token).
+      auto out_row = [&](int rr) -> float* {
+        if (slot) return slot + (int64_t)rr * D;
+        const int qi = s_q0 + rr / group_q;
+        if (qi >= a.n_new) return nullptr;
+        return a.out + (((int64_t)s_b * a.n_new + qi) * a.n_q_heads + s_kvh * group_q + rr % group_q) * D;
+      };
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = 0u;
-        }
-        if (wr) {
+      for (int c0 = 0; c0 < D; c0 += CW) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(orow + c0 + i) =
-                make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                            __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+        for (int j = 0; j < CW; j += 32) {
+          uint32_t ov[32];
+          const int c = c0 + j;
+          if (c < C::OT) {
+            if (s_s0 < s1) {
+              tmem_ld32(row_tmem + 64 + c, ov);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = 0u;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(otail[(c - C::OT + i) % (C::OR > 0 ? C::OR : 1)]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int u = j / 4 + q;
+            *reinterpret_cast<float4*>(sT + row * CW + 4 * (u ^ (row % U))) =
+                make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
+                            __uint_as_float(ov[4 * q + 2]) * inv, __uint_as_float(ov[4 * q + 3]) * inv);
+          }
         }
+        named_bar(1, 128);
+        {
+          const int sub = lane / U, ul = lane % U;
+          for (int r0 = warp * 32; r0 < warp * 32 + 32; r0 += RPI) {
+            const int rr = r0 + sub;
+            float* orow = out_row(rr);
+            const float4 v = *reinterpret_cast<const float4*>(sT + rr * CW + 4 * (ul ^ (rr % U)));
+            if (orow) *reinterpret_cast<float4*>(orow + c0 + 4 * ul) = v;
+          }
+        }
+        named_bar(1, 128);
       }
-      if (wr) {
-#pragma unroll
-        for (int i = 0; i < C::OR; i += 4)
-          *reinterpret_cast<float4*>(orow + C::OT + i) =
-              make_float4(otail[i] * inv, otail[i + 1] * inv, otail[i + 2] * inv, otail[i + 3] * inv);
+      float* orow = out_row(row);
+      if (orow) {
+        float* olse = slot ? slot + (int64_t)C::M * D + row
+                           : a.lse + (((int64_t)s_b * a.n_new + s_q0 + row / group_q) * a.n_q_heads +
+                                      s_kvh * group_q + row % group_q);
         *olse = l_sum > 0.0f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
       }
     }
@@ -675,7 +723,7 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
       const int qt = static_cast<int>(t % n_qt);
       const int b = static_cast<int>(bh / a.n_kv_heads);
       const int64_t S = (a.n_cached + C::NKV - 1) / C::NKV;
-      int64_t len = a.seq_len[b];
+      int64_t len = split_len;
       if (len < 0 || len > a.n_cached) {
         raise_flag(a.flag, kFlagSeqLenRange);
         len = 0;
@@ -697,10 +745,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     __syncthreads();
     const int s0 = s_s0, s1 = s_s1;
     load_q();
-    if (s0 < s1) {
-      fetch(s0);
-      put_scales(s0 & 1);
-    }
+    if (s0 < s1) fetch(s0);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (s0 < s1) put_scales(s0 & 1);
     __syncthreads();
     if (softmax_warp)
       role_loop(std::true_type{}, s1);
@@ -738,10 +785,9 @@ __global__ void __launch_bounds__(256, 1) attn_prefill_kernel(PrefillArgs a) {
     }
     __syncthreads();
     load_q();
-    if (s0 < s1) {
-      fetch(s0);
-      put_scales(s0 & 1);
-    }
+    if (s0 < s1) fetch(s0);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (s0 < s1) put_scales(s0 & 1);
     __syncthreads();  // also: every thread has read the walk state
     if (tid == 0) {
       s_walk[0] = left - (s1 - s0);
@@ -863,12 +909,18 @@ __global__ void __launch_bounds__(256) derotate_rows_kernel(PrefillArgs a, const
 // depend on nothing and several are in flight per thread.
 constexpr int kMaxRowSplits = 1024;
 template <int D, int B, bool ROT>
-__global__ void __launch_bounds__(128) merge_split_rows_kernel(PrefillArgs a, const int8_t* signs,
+__global__ void __launch_bounds__(512) merge_split_rows_kernel(PrefillArgs a, const int8_t* signs,
                                                                const int8_t* signs2, int QT) {
+  // One CTA per output row. The row's n_split partial slots sit in L2; every
+  // thread takes one 16-byte unit of the row over a strided subset of the
+  // slots with all its loads in flight, so the merge costs about one L2 round
+  // trip; the subsets are then summed in shared memory.
   constexpr int64_t SLOT = 128 * (int64_t)(D + 1);
+  constexpr int NT = 512, UNITS = D / 4, SG = NT / UNITS, PER = 20;  // loads in flight per thread and batch
   __shared__ float s_w[kMaxRowSplits];
+  __shared__ __align__(16) float4 s_acc[SG][UNITS];
   __shared__ __align__(16) float s_o[D];
-  __shared__ float s_red[4];
+  __shared__ float s_red[NT / 32];
   const int64_t r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_split = a.n_split;
@@ -881,9 +933,18 @@ __global__ void __launch_bounds__(128) merge_split_rows_kernel(PrefillArgs a, co
   const int64_t t = (b * a.n_kv_heads + h / group_q) * n_qt + qi / QT;
   const int rin = (qi % QT) * group_q + h % group_q;
   const float* base = a.part + t * n_split * SLOT;
+  // The row's partial units, issued before the weights are known.
+  const int u = tid % UNITS, g = tid / UNITS;
+  float4 x[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int sp = g + j * SG;
+    x[j] = sp < n_split ? __ldcg(reinterpret_cast<const float4*>(base + sp * SLOT + (int64_t)rin * D + 4 * u))
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
   float M = -INFINITY;
-  for (int sp = tid; sp < n_split; sp += 128) {
-    const float l = base[sp * SLOT + 128 * D + rin];
+  for (int sp = tid; sp < n_split; sp += NT) {
+    const float l = __ldcg(base + sp * SLOT + 128 * D + rin);
     s_w[sp] = l;
     M = fmaxf(M, l);
   }
@@ -891,28 +952,53 @@ __global__ void __launch_bounds__(128) merge_split_rows_kernel(PrefillArgs a, co
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (lane == 0) s_red[warp] = M;
   __syncthreads();
-  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-  for (int sp = tid; sp < n_split; sp += 128) {
+  M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < NT / 32; ++w) M = fmaxf(M, s_red[w]);
+  __syncthreads();
+  for (int sp = tid; sp < n_split; sp += NT) {
     const float l = s_w[sp];
     s_w[sp] = (l == -INFINITY) ? 0.0f : __expf(l - M);
   }
   __syncthreads();
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int sp0 = 0; sp0 < n_split; sp0 += PER * SG) {
+    if (sp0 > 0) {  // further batches (more than PER * SG splits)
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int sp = sp0 + g + j * SG;
+        x[j] = sp < n_split ? __ldcg(reinterpret_cast<const float4*>(base + sp * SLOT + (int64_t)rin * D + 4 * u))
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int sp = sp0 + g + j * SG;
+      if (sp < n_split) {
+        const float w = s_w[sp];
+        acc.x += w * x[j].x;
+        acc.y += w * x[j].y;
+        acc.z += w * x[j].z;
+        acc.w += w * x[j].w;
+      }
+    }
+  }
+  s_acc[g][u] = acc;
+  __syncthreads();
   float L = 0.0f;
   for (int sp = 0; sp < n_split; ++sp) L += s_w[sp];
-  if (tid < D / 4) {
-    const float* row = base + (int64_t)rin * D + 4 * tid;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 8
-    for (int sp = 0; sp < n_split; ++sp) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(row + sp * SLOT));
-      const float w = s_w[sp];
-      acc.x += w * x.x;
-      acc.y += w * x.y;
-      acc.z += w * x.z;
-      acc.w += w * x.w;
+  if (tid < UNITS) {
+    float4 y = s_acc[0][tid];
+#pragma unroll
+    for (int gg = 1; gg < SG; ++gg) {
+      const float4 z = s_acc[gg][tid];
+      y.x += z.x;
+      y.y += z.y;
+      y.z += z.z;
+      y.w += z.w;
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    *reinterpret_cast<float4*>(s_o + 4 * tid) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    *reinterpret_cast<float4*>(s_o + 4 * tid) = make_float4(y.x * inv, y.y * inv, y.z * inv, y.w * inv);
   }
   __syncthreads();
   if (warp == 0) {
@@ -1004,7 +1090,7 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, const int8_t* signs, c
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.batch * a.n_new * a.n_q_heads;
   if (a.n_split > 0)
-    merge_split_rows_kernel<D, B, ROT><<<static_cast<unsigned>(rows), 128, 0, stream>>>(k, signs, signs2, pl.qt);
+    merge_split_rows_kernel<D, B, ROT><<<static_cast<unsigned>(rows), 512, 0, stream>>>(k, signs, signs2, pl.qt);
   else
     derotate_rows_kernel<D, B, ROT><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(k, signs, signs2,
                                                                                               pl.qt);
@@ -1031,14 +1117,15 @@ static cudaError_t launch_prefill_v(const PrefillArgs& a, const ckv_cache* cache
 // ---- decode with many query rows per kv head ----
 // With many rows per kv head (for example 15 agents x 8 heads over one shared
 // prefix) the mma.sync decode, 8 rows per CTA, dequantises every tile once per
-// 8 rows; a 128-row tile dequantises it once but pays about 40 us of fixed
-// cost (Q load, a partial slot per CTA, the merge). Measured at head_dim 512
-// (B * Hkv = 2, 120 rows): 49 against 24 us at 4096 tokens, 72 against 70 at
-// 16384, 100 against 129 at 32768, 158 against 248 at 65536; with 64 rows the
-// mma.sync decode stays ahead through 65536. Fitted costs in us, X = batch *
-// n_kv_heads * max_seq_len / 1024: mma.sync 10 + 0.125 X per row group of 8,
-// tiles 40 + 0.9 X per 128-row tile. n_split 0 takes the cheaper; -1 forces
-// the tiles.
+// 8 rows; a 128-row tile dequantises it once but pays about 28 us of fixed
+// cost (Q load, a 256 KB partial slot per CTA, the merge; the slots cross
+// between the two dies' L2 halves). Measured at head_dim 512 (B * Hkv = 2,
+// 120 rows), tiles against mma.sync: 34 against 24 us at 4096 tokens, 57
+// against 70 at 16384, 81 against 129 at 32768, 133 against 248 at 65536.
+// Fitted costs in us, X = batch * n_kv_heads * max_seq_len / 1024: mma.sync
+// 10 + 0.125 X per row group of 8, tiles 28 + 0.82 X per 128-row tile. n_split
+// 0 takes the tiles only where they save at least 30 us (near a tie the
+// mma.sync decode, measured more widely, is kept); -1 forces the tiles.
 bool rows_decode_applies(int batch, int n_kv_heads, int n_q_heads, int n_q, int n_split, int64_t max_seq_len) {
   if ((n_split != 0 && n_split != -1) || max_seq_len <= 0 || n_kv_heads <= 0 || batch <= 0 || n_q <= 0 ||
       n_q_heads % n_kv_heads)
@@ -1049,7 +1136,7 @@ bool rows_decode_applies(int batch, int n_kv_heads, int n_q_heads, int n_q, int 
   const double rows = static_cast<double>(g) * n_q;
   const double groups = std::ceil(rows / 8.0), tiles = std::ceil(n_q / (128.0 / g));
   const double x = static_cast<double>(batch) * n_kv_heads * static_cast<double>(max_seq_len) / 1024.0;
-  return rows >= 64 && (0.125 * groups - 0.9 * tiles) * x > 30.0;
+  return rows >= 64 && (0.125 * groups - 0.82 * tiles) * x > 30.0;
 }
 
 struct RowsPlan {

@@ -89,10 +89,11 @@ int auto_split(int64_t units, int64_t max_seq_len, int tiles_per_cta_iter) {
   return static_cast<int>(s);
 }
 
-size_t decode_ws_bytes(int D, int64_t groups, int n_split) {
+// prior: one more slot per group for a prior partial (after the leaf slots).
+size_t decode_ws_bytes(int D, int64_t groups, int n_split, int prior = 0) {
   const ckv::MergeTree tr = ckv::merge_tree(n_split);
   return ws_header_bytes(groups, n_split) +
-         static_cast<size_t>(groups) * (n_split + tr.nl) * ckv::merge_slot_floats(D) * sizeof(float);
+         static_cast<size_t>(groups) * (n_split + tr.nl + prior) * ckv::merge_slot_floats(D) * sizeof(float);
 }
 
 struct DecodePlan {
@@ -102,7 +103,7 @@ struct DecodePlan {
 };
 
 ckv_status plan_decode(int D, int n_kv_heads, int batch, int64_t max_seq_len, int n_q, int n_q_heads,
-                       int n_split, DecodePlan* p) {
+                       int n_split, DecodePlan* p, int prior = 0) {
   if (n_q <= 0 || n_q_heads <= 0) return fail(CKV_ERR_INVALID_ARG, "n_q and n_q_heads must be positive");
   if (n_q_heads % n_kv_heads)
     return fail(CKV_ERR_UNSUPPORTED, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, n_kv_heads);
@@ -115,7 +116,7 @@ ckv_status plan_decode(int D, int n_kv_heads, int batch, int64_t max_seq_len, in
   p->groups = static_cast<int64_t>(batch) * n_kv_heads * nrg;
   const int per_iter = (D == 512) ? 4 : 8;
   p->n_split = n_split ? n_split : auto_split(p->groups, max_seq_len, per_iter);
-  p->ws = decode_ws_bytes(D, p->groups, p->n_split);
+  p->ws = decode_ws_bytes(D, p->groups, p->n_split, prior);
   return CKV_OK;
 }
 
@@ -266,9 +267,10 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
                              void* stream, const AppendRows* app = nullptr, int causal_q = 0,
-                             int dca_chunk = 0, int q_bf16 = 0, int dca_parts = 0) {
+                             int dca_chunk = 0, int q_bf16 = 0, int dca_parts = 0,
+                             const float* prior_o = nullptr, const float* prior_lse = nullptr) {
   DecodePlan p;
-  ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p);
+  ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p, prior_o ? 1 : 0);
   if (s != CKV_OK) return s;
   if (app) {
     if (p.n_row_groups != 1)
@@ -322,6 +324,9 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.sub = a.part + static_cast<size_t>(p.groups) * p.n_split * ckv::merge_slot_floats(D);
   a.merge_ls = tr.ls;
   a.merge_nl = tr.nl;
+  a.sub_stride = tr.nl + (prior_o ? 1 : 0);
+  a.prior_o = prior_o;
+  a.prior_lse = prior_lse;
   a.ctr_stride = ctr_stride(p.n_split);
   a.flag = reinterpret_cast<int32_t*>(base);
   a.counters = reinterpret_cast<uint32_t*>(base + 64);
@@ -506,6 +511,33 @@ ckv_status ckv_attn_decode_f16(const void* k_f16, const void* v_f16, int32_t hea
     return fail(CKV_ERR_INVALID_ARG, "k/v null or not 16-byte aligned");
   return run_decode(false, nullptr, k_f16, v_f16, head_dim, n_kv_heads, batch, capacity, seq_len, max_seq_len,
                     q_f16, n_q, n_q_heads, scale, n_split, out, lse, workspace, ws_bytes, stream);
+}
+
+size_t ckv_attn_decode_f16_merge_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
+                                           int64_t max_seq_len, int32_t n_q, int32_t n_q_heads, int32_t n_split) {
+  if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0) return 0;
+  DecodePlan p;
+  if (plan_decode(head_dim, n_kv_heads, batch, max_seq_len, n_q, n_q_heads, n_split, &p, 1) != CKV_OK) return 0;
+  return p.ws;
+}
+
+ckv_status ckv_attn_decode_f16_merge(const void* k_f16, const void* v_f16, int32_t head_dim, int32_t n_kv_heads,
+                                     int32_t batch, int64_t capacity, const int32_t* seq_len, int64_t max_seq_len,
+                                     const void* q_f16, int32_t n_q, int32_t n_q_heads, float scale, int32_t n_split,
+                                     const float* prior_o, const float* prior_lse, float* out, float* lse,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  if (!supported_dim(head_dim))
+    return fail(CKV_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256,512}", head_dim);
+  if (n_kv_heads <= 0 || batch <= 0) return fail(CKV_ERR_INVALID_ARG, "n_kv_heads and batch must be positive");
+  if (capacity <= 0 || capacity % 16) return fail(CKV_ERR_INVALID_ARG, "capacity must be a positive multiple of 16");
+  if (!k_f16 || !v_f16 || !aligned(k_f16, 16) || !aligned(v_f16, 16))
+    return fail(CKV_ERR_INVALID_ARG, "k/v null or not 16-byte aligned");
+  if (!prior_o || !prior_lse || !aligned(prior_o, 16) || !aligned(prior_lse, 4))
+    return fail(CKV_ERR_INVALID_ARG, "prior_o (16-byte aligned) and prior_lse are required");
+  if (prior_o == out || prior_lse == lse) return fail(CKV_ERR_INVALID_ARG, "prior and output must not alias");
+  return run_decode(false, nullptr, k_f16, v_f16, head_dim, n_kv_heads, batch, capacity, seq_len, max_seq_len,
+                    q_f16, n_q, n_q_heads, scale, n_split, out, lse, workspace, ws_bytes, stream, nullptr, 0, 0, 0,
+                    0, prior_o, prior_lse);
 }
 
 ckv_status ckv_f16_append(void* k_f16, void* v_f16, int32_t head_dim, int32_t n_kv_heads, int32_t batch,

@@ -54,8 +54,15 @@ struct DecodeArgs {
   float scale_log2;          // logit scale * log2(e)
   int n_split, n_row_groups;
   float* part;
-  float* sub;
+  float* sub;                // merge-tree leaf slots, sub_stride per group
+  int sub_stride;            // merge_nl, plus one slot for the prior partial when there is one
   int merge_ls, merge_nl;    // leaf size and leaf count of the merge tree
+  // Optional prior partial per output row (fp16 decode only), computed over
+  // other keys: normalised rows and lse laid out as out and lse. The split
+  // merge combines it with the splits exactly; it enters as one more slot
+  // (sub + (group * sub_stride + merge_nl) * slot), written by split 0.
+  const float* prior_o;
+  const float* prior_lse;
   int rendezvous;            // 1: every CTA resident at once, merge by rendezvous
   int32_t* flag;
   uint32_t* counters;        // ctr_stride words per group, zero between calls

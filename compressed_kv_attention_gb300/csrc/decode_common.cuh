@@ -409,6 +409,33 @@ __device__ __forceinline__ void row_outputs(const DecodeArgs& a, int b, int kvh,
   *l = a.lse + orow;
 }
 
+// The prior partial of row group (b, kvh, rg) as one more merge slot: rows
+// o (normalised) with m = lse log2(e) and l = 1 (an empty row: 0, -inf, 0).
+// Written by split 0 of the group before it counts its own slot in, so the
+// merge's release/acquire covers it. nthr threads.
+template <int D>
+__device__ __forceinline__ void write_prior_slot(const DecodeArgs& a, int64_t gid, int b, int kvh, int rg, int tid,
+                                                 int nthr) {
+  float* slot = a.sub + (gid * a.sub_stride + a.merge_nl) * merge_slot_floats(D);
+  for (int i = tid; i < 8 * (D / 4); i += nthr) {
+    const int r = i / (D / 4), c = i % (D / 4);
+    float* orow;
+    float* lrow;
+    row_outputs(a, b, kvh, rg, r, &orow, &lrow);
+    const float4 v = orow ? __ldg(reinterpret_cast<const float4*>(a.prior_o + (orow - a.out)) + c)
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    reinterpret_cast<float4*>(slot)[i] = v;
+  }
+  if (tid < 8) {
+    float* orow;
+    float* lrow;
+    row_outputs(a, b, kvh, rg, tid, &orow, &lrow);
+    const float l = lrow ? __ldg(a.prior_lse + (lrow - a.lse)) : -INFINITY;
+    slot[8 * D + tid] = (l == -INFINITY) ? -INFINITY : l * 1.4426950408889634f;
+    slot[8 * D + 8 + tid] = (l == -INFINITY) ? 0.0f : 1.0f;
+  }
+}
+
 // ------------------------------------------------------------ split merge --
 //
 // Merging is exact: with M = max_s m_s and w_s = 2^(m_s - M), the merge of
@@ -433,6 +460,9 @@ __device__ __forceinline__ void row_outputs(const DecodeArgs& a, int b, int kvh,
 // of the weighted sum is in acc[k]; s_M / s_L hold the row maxima and sums.
 // 256 threads, named barrier 1. False when a copy wait ran out (the device
 // flag is raised; the sums are then incomplete).
+// Most slots one merge_slots call combines: the tree's 32 leaves and a prior.
+constexpr int kMergeSlots = 33;
+
 template <int D, int SCR>
 __device__ __forceinline__ bool merge_slots(const float* src, int cnt, uint8_t* scratch, uint64_t* mbar,
                                             uint32_t& mphase, int tid, float* s_w, float* s_M, float* s_L,
@@ -441,11 +471,12 @@ __device__ __forceinline__ bool merge_slots(const float* src, int cnt, uint8_t* 
   constexpr int NK = (2 * D + 255) / 256;
   constexpr int KC = SCR / (32 * D);
   static_assert(KC >= 1, "merge scratch holds at least one slot");
-  // Maxima and sums of every slot and row, then the weights.
-  if (tid < cnt * 8) {
-    const float* ml = src + (tid >> 3) * SLOT + 8 * D;
-    s_w[tid] = __ldcg(ml + (tid & 7));
-    s_w[256 + tid] = __ldcg(ml + 8 + (tid & 7));
+  // Maxima and sums of every slot and row (s_w: kMergeSlots * 8 maxima, then
+  // as many sums), then the weights.
+  for (int i = tid; i < cnt * 8; i += 256) {
+    const float* ml = src + (i >> 3) * SLOT + 8 * D;
+    s_w[i] = __ldcg(ml + (i & 7));
+    s_w[kMergeSlots * 8 + i] = __ldcg(ml + 8 + (i & 7));
   }
   named_bar(1, 256);
   if (tid < 8) {
@@ -456,7 +487,7 @@ __device__ __forceinline__ bool merge_slots(const float* src, int cnt, uint8_t* 
       const float m = s_w[q * 8 + tid];
       const float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
       s_w[q * 8 + tid] = w;
-      L = fmaf(w, s_w[256 + q * 8 + tid], L);
+      L = fmaf(w, s_w[kMergeSlots * 8 + q * 8 + tid], L);
     }
     s_M[tid] = M;
     s_L[tid] = L;
@@ -509,7 +540,7 @@ __device__ __forceinline__ void tree_merge_tail(const DecodeArgs& a, int split, 
   constexpr int64_t SLOT = merge_slot_floats(D);
   constexpr int NK = (2 * D + 255) / 256;
   __shared__ __align__(8) uint64_t s_mbar;
-  __shared__ float s_w[512], s_M[8], s_L[8];
+  __shared__ float s_w[2 * kMergeSlots * 8], s_M[8], s_L[8];
   __shared__ int s_last;
   __shared__ float* s_out[8];
   __shared__ float* s_lse[8];
@@ -542,7 +573,7 @@ __device__ __forceinline__ void tree_merge_tail(const DecodeArgs& a, int split, 
   merge_slots<D, SCR>(leaf_src, leaf_cnt, scratch, &s_mbar, mphase, tid, s_w, s_M, s_L, a.flag, acc);
 
   // 2. Write the leaf slot and count it into the root.
-  float* lslot = a.sub + (gid * tr.nl + leaf) * SLOT;
+  float* lslot = a.sub + (gid * a.sub_stride + leaf) * SLOT;
 #pragma unroll
   for (int k = 0; k < NK; ++k) {
     const int u = tid + 256 * k;
@@ -569,7 +600,7 @@ __device__ __forceinline__ void tree_merge_tail(const DecodeArgs& a, int split, 
 
   // 3. Merge the leaves; normalise; rows through shared memory to the warp
   //    that stores each.
-  merge_slots<D, SCR>(a.sub + gid * tr.nl * SLOT, tr.nl, scratch, &s_mbar, mphase, tid, s_w, s_M, s_L, a.flag,
+  merge_slots<D, SCR>(a.sub + gid * a.sub_stride * SLOT, a.sub_stride, scratch, &s_mbar, mphase, tid, s_w, s_M, s_L, a.flag,
                       acc);
   float* rows = reinterpret_cast<float*>(scratch);
 #pragma unroll
@@ -617,17 +648,19 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 template <int D>
 __device__ __forceinline__ void merge_slice(const float* slots, int n_split, int u0, int u1, int tid, int nthr,
                                             float* sm, float* const* out_rows, float* const* lse_rows,
-                                            bool write_lse, int bar_id) {
+                                            bool write_lse, int bar_id, const float* extra = nullptr) {
   constexpr int U = D / 4;                               // float4 units per row
   constexpr int64_t SLOT = merge_slot_floats(D);
-  constexpr int64_t SLOT4 = SLOT / 4;
   constexpr int MLR = 4;                                 // (m, l) pairs per thread in registers
   constexpr int PB = 8;                                  // partial loads per thread per batch
   const int nw = nthr >> 5;
   float* w = sm;                   // [n_split][8] weights
   float* wmax = w + n_split * 8;   // [nw][8] per-warp row maxima
   float* wsum = wmax + nw * 8;     // [nw][8] per-warp row sums
-  const float4* part4 = reinterpret_cast<const float4*>(slots);
+  // Slot s < n_split at slots + s SLOT; with `extra`, slot n_split is there.
+  if (extra) ++n_split;
+  const int n_real = extra ? n_split - 1 : n_split;
+  auto slot_at = [&](int sidx) { return sidx < n_real ? slots + (int64_t)sidx * SLOT : extra; };
   const int n_ml = n_split * 8;
   const int nu = u1 - u0;
   const int lane = tid & 31, warp = tid >> 5;
@@ -636,7 +669,7 @@ __device__ __forceinline__ void merge_slice(const float* slots, int n_split, int
   const int cs = nthr / k;
   const int ui = tid / k, sub = tid % k;
   auto ml_at = [&](int i) {  // (max, sum) of entry i = slot * 8 + row
-    const float* p = slots + (int64_t)(i >> 3) * SLOT + 8 * D + (i & 7);
+    const float* p = slot_at(i >> 3) + 8 * D + (i & 7);
     return make_float2(__ldcg(p), __ldcg(p + 8));
   };
 
@@ -651,7 +684,8 @@ __device__ __forceinline__ void merge_slice(const float* slots, int n_split, int
 #pragma unroll
   for (int j = 0; j < PB; ++j) {
     const int s = sub + j * k;
-    x[j] = (ui < nu && s < n_split) ? __ldcg(part4 + s * SLOT4 + u0 + ui) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    x[j] = (ui < nu && s < n_split) ? __ldcg(reinterpret_cast<const float4*>(slot_at(s)) + u0 + ui)
+                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
   // 2. Row maxima.
   float m = -INFINITY;
@@ -717,7 +751,8 @@ __device__ __forceinline__ void merge_slice(const float* slots, int n_split, int
 #pragma unroll
         for (int j = 0; j < PB; ++j) {
           const int s = s0 + j * k;
-          x[j] = (s < n_split) ? __ldcg(part4 + s * SLOT4 + u) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          x[j] = (s < n_split) ? __ldcg(reinterpret_cast<const float4*>(slot_at(s)) + u)
+                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
         for (int j = 0; j < PB; ++j) {
@@ -793,7 +828,8 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
   const int u0 = (int)((int64_t)split * 2 * D / a.n_split);
   const int u1 = (int)((int64_t)(split + 1) * 2 * D / a.n_split);
   merge_slice<D>(a.part + gid * a.n_split * merge_slot_floats(D), a.n_split, u0, u1, tid, NT, scratch, s_out,
-                 s_lse, split == 0, 1);
+                 s_lse, split == 0, 1,
+                 a.prior_o ? a.sub + (gid * a.sub_stride + a.merge_nl) * merge_slot_floats(D) : nullptr);
   if (tid == 0 && dep + 1 == n) {  // the last CTA to leave: nobody reads the counters any more
     *arrive = 0u;
     *depart = 0u;

@@ -356,6 +356,32 @@ CKV_API ckv_status ckv_attn_decode_f16(const void* k_f16, const void* v_f16, int
                                void* stream);
 
 /*
+ * attn_decode_f16_merge — attn_decode_f16 whose split merge also takes in one
+ * prior partial per output row, computed over other keys: the result is the
+ * attention over the union of the two key sets (the exact log-sum-exp combine
+ * of lse_merge, done inside the decode's own merge, so no separate merge
+ * launch). For the shared-pool fan-out, the prior is each agent's attention
+ * over the shared compressed prefix and the fp16 keys are its private tail
+ * (PolyKV page, section "S1 — SharedKVPool": shared prefix plus private
+ * suffix; DCA page, "Implementation progress + Section-D simplification":
+ * partials packed with their per-row lse and combined by the LSE merge).
+ * prior_o: device fp32 rows laid out as out ([batch][n_q][n_q_heads][D],
+ * 16-byte aligned), prior_lse as lse; an empty prior row has lse -inf. Neither
+ * may alias out or lse. Workspace: ckv_attn_decode_f16_merge_workspace (one
+ * more merge slot per row group than attn_decode_f16). Other arguments and
+ * errors as attn_decode_f16.
+ */
+CKV_API size_t ckv_attn_decode_f16_merge_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
+                                                   int64_t max_seq_len, int32_t n_q, int32_t n_q_heads,
+                                                   int32_t n_split);
+CKV_API ckv_status ckv_attn_decode_f16_merge(const void* k_f16, const void* v_f16, int32_t head_dim,
+                                             int32_t n_kv_heads, int32_t batch, int64_t capacity,
+                                             const int32_t* seq_len, int64_t max_seq_len, const void* q_f16,
+                                             int32_t n_q, int32_t n_q_heads, float scale, int32_t n_split,
+                                             const float* prior_o, const float* prior_lse, float* out, float* lse,
+                                             void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * lse_merge — exact merge of n_parts normalised partials computed over
  * disjoint key sets (DCA page, "Implementation progress + Section-D
  * simplification": M = max lse_r, w_r = exp(lse_r - M), O = sum w_r O_r / sum w_r,
