@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   }
   const __half* kb = a.k16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
   const __half* vb = a.v16 + (int64_t)(b * a.n_kv_heads + kvh) * a.capacity * D;
-  }
 
   uint32_t qf[C::NB_W][4];
   {
