@@ -260,6 +260,18 @@ class DecodeWork:
 
     def e2e_setup(self):
         t = self.torch
+        if not (self.n_q > 1 or self.dca):
+            # An append step through the C ABI entry that takes host buffers: Q and the new K/V rows
+            # (pinned) in, out and lse back, the copies on the stream inside the call.
+            self.h_q = self.q.cpu().pin_memory()
+            self.h_k, self.h_v = self.k_new.cpu().pin_memory(), self.v_new.cpu().pin_memory()
+            self.h_o = t.empty(self.out.shape, dtype=t.float32).pin_memory()
+            self.h_l = t.empty(self.lse.shape, dtype=t.float32).pin_memory()
+            self.e2e_api = ("C ABI ckv_attn_decode_append_host: pinned host buffers read and written by the "
+                            "kernel across NVLink-C2C, no staging copies")
+            return (sum(x.numel() * 2 for x in (self.h_q, self.h_k, self.h_v)),
+                    self.h_o.numel() * 4 + self.h_l.numel() * 4)
+        self.e2e_api = "public Python API, eager (torch copies)"
         # A verify batch or a DCA step sends only Q; an append sends Q and the new K/V row. The step's
         # inputs sit in one pinned buffer and one device buffer (views), so they go over in one copy,
         # and the result (out, lse) comes back in one.
@@ -276,8 +288,12 @@ class DecodeWork:
         return n_in * 2, self.out_lse.numel() * 4
 
     def e2e_step(self, i):
-        self.d_in_flat.copy_(self.h_in, non_blocking=True)
         c = self.caches[i % self.n_rot]
+        if not (self.n_q > 1 or self.dca):
+            self.ckv.attn_decode_append_host(c, self.seq, self.T, self.h_k, self.h_v, self.h_q, self.scale, self.h_o,
+                                             self.h_l, self.ws, stream=self.stream)
+            return
+        self.d_in_flat.copy_(self.h_in, non_blocking=True)
         if self.dca:
             self.ckv.attn_decode_dca(c, self.seq, self.T, self.dca, self.d_in[0], self.scale, self.out, self.lse,
                                      self.ws, stream=self.stream)
@@ -847,7 +863,7 @@ def run_ours(args):
         "roofline": work.roofline(ms / args.steps, peaks),
         "e2e": {"value": round(world * work.tokens_per_step * n_e2e / e2e_s, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-                "api": "public Python API, eager"},
+                "api": getattr(work, "e2e_api", "public Python API, eager")},
         "gpu_launches": work.launches_per_step * args.steps,
         "clocks": clocks,
     }

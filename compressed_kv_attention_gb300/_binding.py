@@ -53,6 +53,8 @@ SIGNATURES = {
                                         _vp, _c_size, _vp]),
     "ckv_attn_decode_append": (_c_int, [_cache_p, _vp, _c_i64, _vp, _vp, _c_int, _c_i64, _c_i64, _vp, _c_int,
                                         _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "ckv_attn_decode_append_host": (_c_int, [_cache_p, _vp, _c_i64, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_f,
+                                             _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_attn_decode_noalloc": (_c_int, [_cache_p, _vp, _c_i64, _vp, _c_int, _c_int, _c_f, _c_int, _vp,
                                          _vp, _vp]),
     "ckv_attn_decode_f16_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
@@ -208,6 +210,18 @@ def attn_decode_append(cache: PackedCache, seq_len, max_seq_len: int, k_new, v_n
                                          k_new.stride(1), k_new.stride(0), _ptr(q), n_q, n_q_heads, scale, n_split,
                                          _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                          _stream(stream)))
+
+
+def attn_decode_append_host(cache: PackedCache, seq_len, max_seq_len: int, k_new_host, v_new_host, q_host,
+                            scale: float, out_host, lse_host, workspace, n_split: int = 0, stream=None):
+    """One decode step on pinned host tensors (contiguous): q [B, n_q, Hq, D], k_new / v_new
+    [B, n_new, Hkv, D] fp16 read, out [B, n_q, Hq, D] / lse [B, n_q, Hq] fp32 written by the kernel
+    across the CPU-GPU interconnect; asynchronous on `stream`."""
+    _, n_q, n_q_heads, _ = q_host.shape
+    _check(load().ckv_attn_decode_append_host(cache.ref(), _ptr(seq_len), max_seq_len, _ptr(k_new_host),
+                                              _ptr(v_new_host), k_new_host.shape[1], _ptr(q_host), n_q, n_q_heads,
+                                              scale, n_split, _ptr(out_host), _ptr(lse_host), _ptr(workspace),
+                                              workspace.numel(), _stream(stream)))
 
 
 def attn_decode_noalloc(cache: PackedCache, seq_len, max_seq_len: int, q, scale: float, out, lse,

@@ -490,6 +490,38 @@ ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t* seq_len
                     workspace, ws_bytes, stream, &app);
 }
 
+// The device address of a page-locked host buffer (mapped into the device's
+// address space), or nullptr for memory the device cannot reach this way.
+static void* mapped_host(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error of an unregistered pointer
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+ckv_status ckv_attn_decode_append_host(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                                       const void* k_new_host, const void* v_new_host, int32_t n_new,
+                                       const void* q_host, int32_t n_q, int32_t n_q_heads, float scale,
+                                       int32_t n_split, float* out_host, float* lse_host, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  ckv_status s = check_cache(cache);
+  if (s != CKV_OK) return s;
+  void* k = mapped_host(k_new_host);
+  void* v = mapped_host(v_new_host);
+  void* q = mapped_host(q_host);
+  void* o = mapped_host(out_host);
+  void* l = mapped_host(lse_host);
+  if (!k || !v || !q || !o || !l)
+    return fail(CKV_ERR_INVALID_ARG, "host buffers must be page-locked and mapped (cudaHostAlloc / pinned)");
+  const int64_t tok = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
+  return ckv_attn_decode_append(cache, seq_len, max_seq_len, k, v, n_new, tok, tok * n_new, q, n_q, n_q_heads,
+                                scale, n_split, static_cast<float*>(o), static_cast<float*>(l), workspace, ws_bytes,
+                                stream);
+}
+
 size_t ckv_attn_decode_f16_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
                                      int64_t max_seq_len, int32_t n_q, int32_t n_q_heads, int32_t n_split) {
   if (!supported_dim(head_dim) || n_kv_heads <= 0 || batch <= 0) return 0;

@@ -303,6 +303,27 @@ CKV_API ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t*
                                           size_t ws_bytes, void* stream);
 
 /*
+ * attn_decode_append_host — one decode step (attn_decode_append) on HOST
+ * buffers, with no staging copies: the kernel reads q
+ * [batch][n_q][n_q_heads][D] and k_new, v_new [batch][n_new][n_kv_heads][D]
+ * (fp16, packed, 16-byte aligned) from page-locked host memory and writes out
+ * [batch][n_q][n_q_heads][D] and lse [batch][n_q][n_q_heads] (fp32) back to
+ * it, across the CPU-GPU interconnect (on GB300, NVLink-C2C with the Grace
+ * host's memory). Host buffers must be page-locked and mapped into the device
+ * address space (cudaHostAlloc or cudaHostRegister; with unified addressing
+ * their device address is the host address): anything else is refused with
+ * CKV_ERR_INVALID_ARG before any launch. The results are in host memory once
+ * `stream` has completed. seq_len stays a device array. Other arguments and
+ * errors as attn_decode_append. No counterpart in the pages: it is the host
+ * side of a serving loop.
+ */
+CKV_API ckv_status ckv_attn_decode_append_host(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
+                                               const void* k_new_host, const void* v_new_host, int32_t n_new,
+                                               const void* q_host, int32_t n_q, int32_t n_q_heads, float scale,
+                                               int32_t n_split, float* out_host, float* lse_host, void* workspace,
+                                               size_t ws_bytes, void* stream);
+
+/*
  * attn_decode_noalloc — attn_decode for callers that cannot allocate device
  * memory. The pages have no counterpart to this entry point; it exists for
  * callers with no way to hand in a workspace: a host framework that owns all

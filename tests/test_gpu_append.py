@@ -99,3 +99,49 @@ def test_append_against_oracle():
         vh = O.tbq3_dequantize(codes, n16, signs)
         o_ref, l_ref = O.decode_reference(qn[b], kh, vh, L, 1.0 / math.sqrt(D))
         H.check_attention(out[b].numpy(), lse[b].numpy(), o_ref, l_ref, f"append b={b}")
+
+
+@pytest.mark.parametrize("D,Hkv,Hq,lens,n_new", [(512, 2, 16, [4096], 1), (128, 1, 4, [200, 64, 131], 2)])
+def test_append_host_matches_device_append(D, Hkv, Hq, lens, n_new):
+    """ckv_attn_decode_append_host (pinned host buffers read and written by the
+    kernel, no staging copies) leaves the same cache bytes and returns the
+    same outputs, bit for bit, as attn_decode_append on device buffers; host
+    memory that is not page-locked is refused before any launch."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B, cap, seed = len(lens), (max(lens) + 15) // 16 * 16 + 16, 90 + D
+    outl = inputs.outlier_channels(D, max(1, round(0.01 * D)), seed)
+    signs = inputs.tbq_signs(D)
+    k = torch.from_numpy(inputs.normal_tensor((B, cap, Hkv, D), seed, "ah/k", outl)).to(DEV)
+    v = torch.from_numpy(inputs.normal_tensor((B, cap, Hkv, D), seed, "ah/v", outl)).to(DEV)
+    q = inputs.normal_tensor((B, 1, Hq, D), seed, "ah/q", outl)
+    kn = np.stack([inputs.normal_tensor((n_new, Hkv, D), seed + b, "ah/kn", outl) for b in range(B)])
+    vn = np.stack([inputs.normal_tensor((n_new, Hkv, D), seed + b, "ah/vn", outl) for b in range(B)])
+    base = ckv.PackedCache(D, Hkv, B, cap, signs)
+    ckv.kv_pack(base, 0, k, v)
+    dev_c = ckv.PackedCache(D, Hkv, B, cap, signs, data=base.data.clone())
+    host_c = ckv.PackedCache(D, Hkv, B, cap, signs, data=base.data.clone())
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    ws = torch.zeros(ckv.attn_decode_workspace(dev_c, max(lens), 1, Hq), dtype=torch.uint8, device=DEV)
+    out_d = torch.empty((B, 1, Hq, D), dtype=torch.float32, device=DEV)
+    lse_d = torch.empty((B, 1, Hq), dtype=torch.float32, device=DEV)
+    ckv.attn_decode_append(dev_c, seq, max(lens), torch.from_numpy(kn).to(DEV), torch.from_numpy(vn).to(DEV),
+                           torch.from_numpy(q).to(DEV), scale, out_d, lse_d, ws)
+    torch.cuda.synchronize()
+    assert ckv.read_device_flag(ws) == 0
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()  # noqa: E731
+    q_h, k_h, v_h = pin(q), pin(kn), pin(vn)
+    out_h = torch.full((B, 1, Hq, D), float("nan"), dtype=torch.float32).pin_memory()
+    lse_h = torch.full((B, 1, Hq), float("nan"), dtype=torch.float32).pin_memory()
+    ws2 = torch.zeros_like(ws)
+    ckv.attn_decode_append_host(host_c, seq, max(lens), k_h, v_h, q_h, scale, out_h, lse_h, ws2)
+    torch.cuda.synchronize()
+    assert ckv.read_device_flag(ws2) == 0
+    assert torch.equal(host_c.data, dev_c.data)
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    unpinned = torch.zeros_like(out_h, device="cpu").clone()
+    assert not unpinned.is_pinned()
+    with pytest.raises(ckv.CkvError) as err:
+        ckv.attn_decode_append_host(host_c, seq, max(lens), k_h, v_h, q_h, scale, unpinned, lse_h, ws2)
+    assert err.value.status == -1 and "page-locked" in str(err.value)
