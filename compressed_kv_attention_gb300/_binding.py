@@ -78,6 +78,7 @@ SIGNATURES = {
     "ckv_attn_prefill_shared": (_c_int, [_cache_p, _c_i64, _vp, _vp, _c_i64, _vp, _c_int, _vp, _vp, _vp, _c_int,
                                          _c_int, _c_f, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_read_device_flag": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
+    "ckv_set_concurrent_kernels": (None, [_c_int]),
     "ckv_read_noalloc_flag": (_c_int, [ctypes.POINTER(_c_int), _vp]),
     "ckv_calibrate_stream": (_c_int, [_vp, _c_i64, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
 }
@@ -358,3 +359,8 @@ def calibrate_stream(src, n_tiles: int, record_bytes: int, n_streams: int, n_spl
     """Stream the records at `src` (a device tensor) through the decode's staging without computing."""
     _check(load().ckv_calibrate_stream(_ptr(src), n_tiles, record_bytes, n_streams, n_split, int(rendezvous),
                                        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def set_concurrent_kernels(on: bool) -> None:
+    """Declare that other kernels may run on the device concurrently (split merges then never wait)."""
+    load().ckv_set_concurrent_kernels(int(bool(on)))

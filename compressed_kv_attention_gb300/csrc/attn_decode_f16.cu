@@ -214,7 +214,7 @@ template <int D>
 static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = FDec<D>;
   static bool configured = false;
-  static int cap = 0;
+  static ResidencyCache cap{};  // per device
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_f16_kernel<D, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

@@ -542,7 +542,7 @@ template <int D, int B, bool DCA, int ROT>
 static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = CDec<D, B, ROT>;
   static bool configured = false;  // per process; the attribute is per function
-  static int cap = 0;
+  static ResidencyCache cap{};  // per device
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, B, DCA, ROT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

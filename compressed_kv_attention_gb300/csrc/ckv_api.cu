@@ -2,6 +2,8 @@
 // checks, workspace sizing and kernel launches on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -129,6 +131,9 @@ ckv_status check_ws(void* ws, size_t have, size_t need) {
 }  // namespace
 
 namespace ckv {
+static std::atomic<int> g_concurrent{0};
+bool concurrent_kernels() { return g_concurrent.load(std::memory_order_relaxed) != 0; }
+
 int set_last_error(int status, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -140,7 +145,9 @@ int set_last_error(int status, const char* fmt, ...) {
 
 extern "C" {
 
-int32_t ckv_version(void) { return 102; }
+int32_t ckv_version(void) { return 103; }
+
+void ckv_set_concurrent_kernels(int32_t on) { ckv::g_concurrent.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 const char* ckv_last_error(void) { return g_err; }
 

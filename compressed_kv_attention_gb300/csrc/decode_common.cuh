@@ -849,6 +849,10 @@ __device__ __forceinline__ void decode_split_tail(const DecodeArgs& a, int split
   }
 }
 
+// Whether the caller declared that other kernels may run concurrently with
+// this library's on the device (ckv_set_concurrent_kernels; process-wide).
+bool concurrent_kernels();
+
 // Blocks of `kernel` that can be resident at once on the current device.
 template <typename K>
 static inline int coresident_blocks(K kernel, int threads, size_t smem) {
@@ -859,18 +863,30 @@ static inline int coresident_blocks(K kernel, int threads, size_t smem) {
   return sms * per_sm;
 }
 
+// Per-device residency figures of one kernel (blocks resident at once).
+constexpr int kMaxDevices = 64;
+struct ResidencyCache {
+  int blocks[kMaxDevices];
+};
+
 // Launch a split decode kernel. The splits merge by rendezvous when the whole
 // grid fits on the device at once, else by the tree. With programmatic stream
 // serialisation the grid may begin while the previous grid on the stream
 // finishes; the kernel waits for it (griddep_wait) before touching global
 // memory, and every one of this grid's CTAs has started before the next grid
-// can begin, so the rendezvous never waits on a CTA that cannot run.
+// can begin, so the rendezvous never waits on a CTA that cannot run. When the
+// caller has declared that other kernels may run at the same time on the
+// device (ckv_set_concurrent_kernels), a grid that fits may still not be
+// resident all at once, so the tree merge, which never waits for another
+// CTA, is used instead.
 template <typename K>
-static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, int threads, size_t smem, int* cap_cache,
+static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, int threads, size_t smem, ResidencyCache* cache,
                                               cudaStream_t stream) {
   const int64_t grid_total = (int64_t)a.n_split * a.n_row_groups * a.batch * a.n_kv_heads;
-  if (*cap_cache == 0) *cap_cache = coresident_blocks(kernel, threads, smem);
-  a.rendezvous = (grid_total <= *cap_cache) ? 1 : 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  if (cache->blocks[dev] == 0) cache->blocks[dev] = coresident_blocks(kernel, threads, smem);
+  a.rendezvous = (!concurrent_kernels() && grid_total <= cache->blocks[dev]) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
   cfg.blockDim = dim3(threads);

@@ -505,6 +505,19 @@ CKV_API ckv_status ckv_attn_prefill_shared(const ckv_cache* prefix, int64_t n_pr
                                    float scale, float* out, float* lse, void* workspace,
                                    size_t ws_bytes, void* stream);
 
+/*
+ * set_concurrent_kernels — declare (on != 0) that other kernels may run on the
+ * device at the same time as this library's, e.g. on another stream or in
+ * another process under MPS; process-wide, default off. A split decode whose
+ * grid fits on the device merges its splits by a rendezvous in which every
+ * CTA waits for the others; with other kernels holding SMs, part of the grid
+ * may not be resident and the wait would run out (2 s, device flag 1, rows
+ * left unmerged). With this set, the split decodes use the tree merge, in
+ * which no CTA waits for another (slower: about 30 against 21 us for the
+ * Gemma-4 step). Takes effect for launches after the call.
+ */
+CKV_API void ckv_set_concurrent_kernels(int32_t on);
+
 /* Synchronously read the device flag (first 4 bytes of a workspace) after draining
  * `stream`. *flag receives it; when it is nonzero the flag is cleared and
  * CKV_ERR_DEVICE_FLAG returned. */

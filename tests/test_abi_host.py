@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_cache_bytes(lib):
-    assert lib.ckv_version() == 102
+    assert lib.ckv_version() == 103
     assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * (32768 // 16) * (23 * 512 + 32)
     assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * 32768 * 738
     assert lib.ckv_cache_bytes(128, 1, 1, 256) == 256 * 186
