@@ -56,12 +56,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel sources whose hash is recorded beside it (null once they change).
 # Fan-out and prefill: the sum over the step's kernels (their rooflines time the whole step).
 NCU_TRAFFIC = {
-    "gemma4_decode": {"bytes": 48513792, "source_sha": "91b12a86972dbb35"},
-    "tiny_decode": {"bytes": 122112, "source_sha": "91b12a86972dbb35"},
-    "long_decode": {"bytes": 1547958528 + 3407872, "source_sha": "91b12a86972dbb35"},
-    "fanout_decode": {"bytes": 6431744 + 31771392 + 1004288, "source_sha": "15c606b8570e9538"},
-    "chunked_prefill": {"bytes": 8451328 + (113881856 + 57169920) + (106606592 + 23946496),
-                        "source_sha": "4a5d1ed4e56b9f4b"},
+    "gemma4_decode": {"bytes": 48515840, "source_sha": "591b892e332a0fc1"},
+    "tiny_decode": {"bytes": 128768, "source_sha": "591b892e332a0fc1"},
+    "long_decode": {"bytes": 1548006400 + 3398656, "source_sha": "591b892e332a0fc1"},
+    "fanout_decode": {"bytes": 6421248 + 32262912, "source_sha": "de5ef6370e4e0462"},
+    "chunked_prefill": {"bytes": 8453120 + (121486336 + 61794304) + (106606080 + 24052992),
+                        "source_sha": "fb178fce3956d804"},
 }
 
 _DECODE_SOURCES = ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh",
@@ -175,10 +175,15 @@ class ClockSampler:
 
 
 def _timed(stream, fn, n):
-    """Run fn() n times on `stream`; elapsed ms from CUDA events recorded on that stream."""
+    """Run fn() n times on `stream`; elapsed ms from CUDA events recorded on that stream.
+    A short device-side sleep (a torch kernel, before the start event) holds the stream
+    while the host submits the work, so the events bracket the device work itself and
+    not the host's launch latency."""
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(200000)  # ~0.1 ms at GB300 clocks
         e0.record(stream)
         for _ in range(n):
             fn()
@@ -723,9 +728,11 @@ def measure(work, stream, dev, steps, warmup, dist=None):
     stream.synchronize()
     work.check()
     if work.graph:
+        # Warm-up replays the timed graph itself (at least max(warmup, 3) steps), so that
+        # the timed replay is not the graph's first (its upload would land in the timing).
         run = _graph_runner(work, stream, steps)
-        warm = _graph_runner(work, stream, max(warmup, 3))
-        warm()
+        for _ in range(-(-max(warmup, 3) // steps)):
+            run()
         stream.synchronize()
     else:
         with torch.cuda.stream(stream):
@@ -856,7 +863,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": getattr(work, "dtype", "f16 mma, f32 accumulate (int8 / 3-bit storage)"),
         "data": "synthetic",
         "config": dict(work.describe(), parallelism=f"replicas x{world}",
-                       timing=("CUDA graphs of exactly `steps` back-to-back steps, events on the launching stream"
+                       timing=("CUDA graphs of exactly `steps` back-to-back steps, events on the launching stream; "
+                               "warm-up replays the same graphs (max(warmup, 3) steps rounded up to whole replays)"
                                if work.graph else "events around each step on the launching stream")),
         # the step is one launch of the dominant kernel (decode) or its whole
         # call (prefill, fan-out): the roofline uses the timed region itself
