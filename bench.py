@@ -175,15 +175,10 @@ class ClockSampler:
 
 
 def _timed(stream, fn, n):
-    """Run fn() n times on `stream`; elapsed ms from CUDA events recorded on that stream.
-    A short device-side sleep (a torch kernel, before the start event) holds the stream
-    while the host submits the work, so the events bracket the device work itself and
-    not the host's launch latency."""
+    """Run fn() n times on `stream`; elapsed ms from CUDA events recorded on that stream."""
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        if hasattr(torch.cuda, "_sleep"):
-            torch.cuda._sleep(200000)  # ~0.1 ms at GB300 clocks
         e0.record(stream)
         for _ in range(n):
             fn()
