@@ -238,8 +238,9 @@ class DecodeWork:
             self.seq = torch.full((B,), T, dtype=torch.int32, device=dev)
         stream.synchronize()
         self.tokens_per_step = B * self.n_q
-        # the decode kernel (packs the new token or runs the batch, merges splits); DCA adds the regime merge
-        self.launches_per_step = 2 if self.dca else 1
+        # the decode kernel (packs the new token or runs the batch, merges splits); DCA with 8 query heads
+        # per kv head merges its regimes inside the same launch (co-resident grid), otherwise in a second
+        self.launches_per_step = 2 if (self.dca and Hq != 8 * Hkv) else 1
         self.algo_bytes = B * Hkv * T * inputs.compressed_bytes_per_token(D, w.v_bits, w.rot_group)
 
     def step(self, i):

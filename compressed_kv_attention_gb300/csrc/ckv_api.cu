@@ -275,7 +275,8 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int n_split, float* out, float* lse, void* ws, size_t ws_bytes,
                              void* stream, const AppendRows* app = nullptr, int causal_q = 0,
                              int dca_chunk = 0, int q_bf16 = 0, int dca_parts = 0,
-                             const float* prior_o = nullptr, const float* prior_lse = nullptr) {
+                             const float* prior_o = nullptr, const float* prior_lse = nullptr,
+                             float* fold_out = nullptr, float* fold_lse = nullptr, int* host_folded = nullptr) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p, prior_o ? 1 : 0);
   if (s != CKV_OK) return s;
@@ -334,6 +335,10 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.sub_stride = tr.nl + (prior_o ? 1 : 0);
   a.prior_o = prior_o;
   a.prior_lse = prior_lse;
+  a.dca_fold = fold_out ? 1 : 0;
+  a.fold_out = fold_out;
+  a.fold_lse = fold_lse;
+  a.host_folded = host_folded;
   a.ctr_stride = ctr_stride(p.n_split);
   a.flag = reinterpret_cast<int32_t*>(base);
   a.counters = reinterpret_cast<uint32_t*>(base + 64);
@@ -451,10 +456,18 @@ ckv_status ckv_attn_decode_dca(const ckv_cache* cache, const int32_t* seq_len, i
   float* po = reinterpret_cast<float*>(pbase + o_off);
   float* pl = reinterpret_cast<float*>(pbase + l_off);
   // The regimes (the inter one in pieces) as the query tokens of one decode.
+  // With 8 query heads per kv head every row group is one piece of the same
+  // 8 heads, and a rendezvous launch merges the pieces inside the decode
+  // (folded: the output lands in out / lse directly); otherwise the pieces'
+  // rows go to the workspace and lse_merge combines them.
+  const bool fold = n_q_heads == 8 * cache->n_kv_heads;
+  int folded = 0;
   s = run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
                  cache->capacity, seq_len, max_seq_len, q_f16, n_rows, n_q_heads, scale, n_split, po, pl, workspace,
-                 dec, stream, nullptr, 0, chunk, 0, parts);
+                 dec, stream, nullptr, 0, chunk, 0, parts, nullptr, nullptr, fold ? out : nullptr,
+                 fold ? lse : nullptr, &folded);
   if (s != CKV_OK) return s;
+  if (folded) return CKV_OK;
   const int D = cache->head_dim;
   ckv::LseMergeArgs m{};
   for (int r = 0; r < n_rows; ++r) {

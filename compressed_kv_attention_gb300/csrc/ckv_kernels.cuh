@@ -63,6 +63,17 @@ struct DecodeArgs {
   // (sub + (group * sub_stride + merge_nl) * slot), written by split 0.
   const float* prior_o;
   const float* prior_lse;
+  // DCA with 8 query heads per kv head: the regime pieces are row groups with
+  // the same 8 heads, so with dca_fold the split rendezvous spans all row
+  // groups of a (sequence, kv head) and merges every (piece, split) slot:
+  // the result is the DCA output itself, written to fold_out / fold_lse
+  // ([batch][n_q_heads][D], [batch][n_q_heads]) instead of per-piece rows.
+  // The launcher keeps it only for a rendezvous launch and reports the
+  // choice in *host_folded (host memory).
+  int dca_fold;
+  float* fold_out;
+  float* fold_lse;
+  int* host_folded;
   int rendezvous;            // 1: every CTA resident at once, merge by rendezvous
   int32_t* flag;
   uint32_t* counters;        // ctr_stride words per group, zero between calls

@@ -797,9 +797,14 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
   __shared__ int s_ok;
   __shared__ float* s_out[8];
   __shared__ float* s_lse[8];
-  uint32_t* arrive = a.counters + gid * a.ctr_stride;
+  // Fold (DCA): the merge group is the (sequence, kv head), its members every
+  // (row group, split) CTA, whose slots are contiguous.
+  const int64_t mg = a.dca_fold ? gid / a.n_row_groups : gid;
+  const int nm = a.dca_fold ? a.n_split * a.n_row_groups : a.n_split;
+  const int cm = a.dca_fold ? rg * a.n_split + split : split;
+  uint32_t* arrive = a.counters + mg * a.ctr_stride;
   uint32_t* depart = arrive + 1;
-  const uint32_t n = (uint32_t)a.n_split;
+  const uint32_t n = (uint32_t)nm;
   __threadfence();  // this CTA's slot, released to the group
   named_bar(1, NT);
   uint32_t dep = 0;
@@ -822,13 +827,20 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
     if (ok) dep = atomicAdd(depart, 1u);
     s_ok = ok;
   }
-  if (tid < 8) row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
+  if (tid < 8) {
+    if (a.dca_fold) {  // row tid of the group: head kvh * 8 + tid of the single output token
+      const int64_t orow = (int64_t)b * a.n_q_heads + kvh * 8 + tid;
+      s_out[tid] = a.fold_out + orow * a.head_dim;
+      s_lse[tid] = a.fold_lse + orow;
+    } else {
+      row_outputs(a, b, kvh, rg, tid, &s_out[tid], &s_lse[tid]);
+    }
+  }
   named_bar(1, NT);
   if (!s_ok) return;
-  const int u0 = (int)((int64_t)split * 2 * D / a.n_split);
-  const int u1 = (int)((int64_t)(split + 1) * 2 * D / a.n_split);
-  merge_slice<D>(a.part + gid * a.n_split * merge_slot_floats(D), a.n_split, u0, u1, tid, NT, scratch, s_out,
-                 s_lse, split == 0, 1,
+  const int u0 = (int)((int64_t)cm * 2 * D / nm);
+  const int u1 = (int)((int64_t)(cm + 1) * 2 * D / nm);
+  merge_slice<D>(a.part + mg * nm * merge_slot_floats(D), nm, u0, u1, tid, NT, scratch, s_out, s_lse, cm == 0, 1,
                  a.prior_o ? a.sub + (gid * a.sub_stride + a.merge_nl) * merge_slot_floats(D) : nullptr);
   if (tid == 0 && dep + 1 == n) {  // the last CTA to leave: nobody reads the counters any more
     *arrive = 0u;
@@ -887,6 +899,8 @@ static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, int thread
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
   if (cache->blocks[dev] == 0) cache->blocks[dev] = coresident_blocks(kernel, threads, smem);
   a.rendezvous = (!concurrent_kernels() && grid_total <= cache->blocks[dev]) ? 1 : 0;
+  if (!a.rendezvous) a.dca_fold = 0;
+  if (a.host_folded) *a.host_folded = a.dca_fold;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_split, a.n_row_groups, a.batch * a.n_kv_heads);
   cfg.blockDim = dim3(threads);
