@@ -56,12 +56,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel sources whose hash is recorded beside it (null once they change).
 # Fan-out and prefill: the sum over the step's kernels (their rooflines time the whole step).
 NCU_TRAFFIC = {
-    "gemma4_decode": {"bytes": 48515840, "source_sha": "591b892e332a0fc1"},
-    "tiny_decode": {"bytes": 128768, "source_sha": "591b892e332a0fc1"},
-    "long_decode": {"bytes": 1548006400 + 3398656, "source_sha": "591b892e332a0fc1"},
-    "fanout_decode": {"bytes": 6421248 + 32262912, "source_sha": "de5ef6370e4e0462"},
+    "gemma4_decode": {"bytes": 48523264, "source_sha": "513ce3b52e3ae85c"},
+    "tiny_decode": {"bytes": 126208, "source_sha": "513ce3b52e3ae85c"},
+    "long_decode": {"bytes": 1547992320 + 3383552, "source_sha": "513ce3b52e3ae85c"},
+    "fanout_decode": {"bytes": 6422528 + 32275456, "source_sha": "fc5e6005f7459510"},
     "chunked_prefill": {"bytes": 8453120 + (121486336 + 61794304) + (106606080 + 24052992),
-                        "source_sha": "fb178fce3956d804"},
+                        "source_sha": "af4591aa2d03b232"},
 }
 
 _DECODE_SOURCES = ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh",
