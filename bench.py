@@ -545,7 +545,7 @@ class SharedPrefillWork:
             self.flush = torch.empty(2 * self.l2, dtype=torch.uint8, device=dev)
         stream.synchronize()
         self.tokens_per_step = A * n
-        self.launches_per_step = 5  # tail append, tail prefill, prefix prefill, de-rotation, merge
+        self.launches_per_step = 4  # tail append, prefix prefill, de-rotation, tail prefill with the merge
         # QK^T and PV: every query row sees the P prefix keys and TL + i + 1 tail keys.
         self.flops = 2 * 2 * Hq * D * A * (n * P + n * TL + n * (n + 1) // 2)
 
@@ -582,8 +582,8 @@ class SharedPrefillWork:
         return {"workload": "shared_prefill", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
                 "agents": self.A, "prefix_tokens": self.P, "tail_tokens": self.TL, "new_tokens_per_agent": self.n,
                 "q_dtype": "bf16",
-                "step": "attn_prefill_shared (tail append + causal fp16 tail prefill + prefix-only tcgen05 "
-                        "prefill + lse merge)",
+                "step": "attn_prefill_shared (tail append + prefix-only tcgen05 prefill + causal fp16 tail "
+                        "prefill with the prefix partial merged in)",
                 "l2": f"flushed before each step ({2 * self.l2 / 1e6:.0f} MB write)"}
 
     def roofline(self, kernel_ms, peaks):

@@ -61,14 +61,33 @@ __device__ __forceinline__ void rows_epilogue(const DecodeArgs& a, SoftmaxState 
     float* lrow;
     row_outputs(a, b, kvh, rg0 + q, r, &orow, &lrow);
     if (rg0 + q >= a.n_row_groups || !orow) continue;
-    const float m = mlbuf[q * 16 + r * 2], l = mlbuf[q * 16 + r * 2 + 1];
+    float m = mlbuf[q * 16 + r * 2], l = mlbuf[q * 16 + r * 2 + 1];
+    // With a prior partial (normalised row, lse) over other keys, the two merge
+    // exactly: weights 2^(m - M) for this row's sums and 2^(m_p - M) for the
+    // prior, whose sum is 1.
+    float w0 = 1.0f, w1 = 0.0f;
+    const float2* p2 = nullptr;
+    if (a.prior_o) {
+      const float lp = __ldg(a.prior_lse + (lrow - a.lse));
+      const float mp = lp == -INFINITY ? -INFINITY : lp * 1.4426950408889634f;
+      const float M = fmaxf(m, mp);
+      w0 = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+      w1 = (mp == -INFINITY) ? 0.0f : exp2f(mp - M);
+      l = w0 * l + w1;
+      m = M;
+      p2 = reinterpret_cast<const float2*>(a.prior_o + (orow - a.out)) + lane;
+    }
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
     float2* o2 = reinterpret_cast<float2*>(orow) + lane;
 #pragma unroll
     for (int e = 0; e < D / 64; ++e) {
       const int d = 64 * e + 2 * lane;
-      const float2 y = *reinterpret_cast<const float2*>(red + q * Sh::RED_FLOATS + r * Sh::RP + d +
-                                                        2 * Sh::PS * (d / Sh::GD));
+      float2 y = *reinterpret_cast<const float2*>(red + q * Sh::RED_FLOATS + r * Sh::RP + d +
+                                                  2 * Sh::PS * (d / Sh::GD));
+      if (p2) {
+        const float2 pv = __ldg(p2 + 32 * e);
+        y = make_float2(w0 * y.x + w1 * pv.x, w0 * y.y + w1 * pv.y);
+      }
       o2[32 * e] = make_float2(y.x * inv, y.y * inv);
     }
     if (lane == 0) *lrow = l > 0.0f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -224,7 +243,7 @@ static cudaError_t launch_f16_d(const DecodeArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (a.n_split == 1 && a.n_row_groups >= C::NP && !a.prior_o) {
+  if (a.n_split == 1 && a.n_row_groups >= C::NP) {
     // Row-parallel CTAs: NP row groups each, no split merge.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, (a.n_row_groups + C::NP - 1) / C::NP, a.batch * a.n_kv_heads);

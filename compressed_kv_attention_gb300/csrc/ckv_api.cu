@@ -641,16 +641,16 @@ ckv_status ckv_attn_prefill_f16(const void* k_f16, const void* v_f16, int32_t he
                     1);
 }
 
-// Shared-prefix prefill workspace: [prefix prefill][tail prefill][prefix O, lse][tail O, lse].
+// Shared-prefix prefill workspace: [prefix prefill][tail pass][prefix O, lse].
 struct SharedWs {
-  size_t pre, tail, o_pre, l_pre, o_tail, l_tail, total;
+  size_t pre, tail, o_pre, l_pre, total;
 };
 static bool shared_ws(const ckv_cache* prefix, int32_t n_agents, int64_t tail_capacity, int32_t n_new,
                       int32_t n_q_heads, SharedWs* w) {
   if (!prefix || n_agents <= 0 || n_new <= 0 || tail_capacity <= 0) return false;
   const size_t pre = ckv_attn_prefill_workspace(prefix, n_agents * n_new, n_q_heads);
-  const size_t tail = ckv_attn_decode_f16_workspace(prefix->head_dim, prefix->n_kv_heads, n_agents, tail_capacity,
-                                                    n_new, n_q_heads, 0);
+  const size_t tail = ckv_attn_decode_f16_merge_workspace(prefix->head_dim, prefix->n_kv_heads, n_agents,
+                                                          tail_capacity, n_new, n_q_heads, 0);
   if (tail == 0) return false;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = static_cast<size_t>(n_agents) * n_new * n_q_heads;
@@ -658,9 +658,7 @@ static bool shared_ws(const ckv_cache* prefix, int32_t n_agents, int64_t tail_ca
   w->tail = up(pre);
   w->o_pre = w->tail + up(tail);
   w->l_pre = w->o_pre + up(rows * prefix->head_dim * sizeof(float));
-  w->o_tail = w->l_pre + up(rows * sizeof(float));
-  w->l_tail = w->o_tail + up(rows * prefix->head_dim * sizeof(float));
-  w->total = w->l_tail + up(rows * sizeof(float));
+  w->total = w->l_pre + up(rows * sizeof(float));
   return true;
 }
 
@@ -687,28 +685,29 @@ ckv_status ckv_attn_prefill_shared(const ckv_cache* prefix, int64_t n_prefix, vo
   ckv_status s = check_ws(workspace, ws_bytes, w.total);
   if (s != CKV_OK) return s;
   const int D = prefix->head_dim, Hkv = prefix->n_kv_heads;
+  if (tail_capacity % 16) return fail(CKV_ERR_INVALID_ARG, "tail capacity must be a multiple of 16");
+  if (!k_tail || !v_tail || !aligned(k_tail, 16) || !aligned(v_tail, 16))
+    return fail(CKV_ERR_INVALID_ARG, "tail k/v null or not 16-byte aligned");
   uint8_t* base = static_cast<uint8_t*>(workspace);
   // 1. The new rows join each agent's fp16 tail at [tail_len - n_new, tail_len).
   const int64_t row = static_cast<int64_t>(Hkv) * D;
   s = ckv_f16_append(k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, k_new_f16, v_new_f16, n_new, row,
                      row * n_new, stream);
   if (s != CKV_OK) return s;
-  // 2. Every agent's queries over its own tail, causal (token i sees [0, tail_len - n_new + i]).
-  float* o_tail = n_prefix > 0 ? reinterpret_cast<float*>(base + w.o_tail) : out;
-  float* l_tail = n_prefix > 0 ? reinterpret_cast<float*>(base + w.l_tail) : lse;
-  s = ckv_attn_prefill_f16(k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, tail_capacity, q_bf16, n_new,
-                           n_q_heads, scale, 0, o_tail, l_tail, base + w.tail, w.o_pre - w.tail, stream);
-  if (s != CKV_OK || n_prefix == 0) return s;
-  // 3. All agents' queries over the shared compressed prefix, one sequence of n_agents * n_new tokens.
+  // 2. All agents' queries over the shared compressed prefix, one sequence of n_agents * n_new tokens
+  //    (its rows are laid out as the output's).
   float* o_pre = reinterpret_cast<float*>(base + w.o_pre);
   float* l_pre = reinterpret_cast<float*>(base + w.l_pre);
-  s = ckv_attn_prefill_prefix(prefix, n_prefix, q_bf16, n_agents * n_new, n_q_heads, scale, o_pre, l_pre,
-                              base + w.pre, w.tail - w.pre, stream);
-  if (s != CKV_OK) return s;
-  // 4. Exact log-sum-exp merge of the two partials of every row.
-  const float* op[2] = {o_pre, o_tail};
-  const float* lp[2] = {l_pre, l_tail};
-  return ckv_lse_merge(2, op, lp, static_cast<int64_t>(n_agents) * n_new * n_q_heads, D, out, lse, stream);
+  if (n_prefix > 0) {
+    s = ckv_attn_prefill_prefix(prefix, n_prefix, q_bf16, n_agents * n_new, n_q_heads, scale, o_pre, l_pre,
+                                base + w.pre, w.tail - w.pre, stream);
+    if (s != CKV_OK) return s;
+  }
+  // 3. Every agent's queries over its own tail, causal (token i sees [0, tail_len - n_new + i]), merged
+  //    exactly with the prefix partial inside the same launch.
+  return run_decode(false, nullptr, k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, tail_capacity, q_bf16,
+                    n_new, n_q_heads, scale, 0, out, lse, base + w.tail, w.o_pre - w.tail, stream, nullptr, 1, 0, 1, 0,
+                    n_prefix > 0 ? o_pre : nullptr, n_prefix > 0 ? l_pre : nullptr);
 }
 
 ckv_status ckv_lse_merge(int32_t n_parts, const float* const* o_parts, const float* const* lse_parts,

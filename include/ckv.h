@@ -484,11 +484,12 @@ CKV_API ckv_status ckv_attn_prefill_f16(const void* k_f16, const void* v_f16, in
  * prefill n_new tokens; query token i of agent a sees the whole prefix
  * [0, n_prefix) of `prefix` (a packed cache holding one sequence, batch 1) and
  * its own tail positions [0, tail_len[a] - n_new + i]. Steps, all on the device:
- * the new K/V rows are copied into the tails (ckv_f16_append), the tail part
- * runs causally (ckv_attn_prefill_f16), the prefix part runs as one sequence of
- * n_agents * n_new query tokens (ckv_attn_prefill_prefix), and the two partials
- * of every row merge exactly (ckv_lse_merge); n_prefix = 0 leaves only the
- * tail part.
+ * the new K/V rows are copied into the tails (ckv_f16_append), the prefix part
+ * runs as one sequence of n_agents * n_new query tokens
+ * (ckv_attn_prefill_prefix), and the tail part runs causally with the prefix
+ * partial of every row merged exactly into its epilogue (the kernel of
+ * ckv_attn_decode_f16_merge, bf16 queries); n_prefix = 0 leaves only the tail
+ * part. Three launches.
  * k_tail, v_tail: fp16 [n_agents][Hkv][tail_capacity][D] (written: new rows).
  * tail_len: device int32 [n_agents], each tail's length counting the new rows.
  * q_bf16: [n_agents][n_new][n_q_heads][D]; k_new_f16, v_new_f16: fp16
