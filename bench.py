@@ -56,12 +56,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel sources whose hash is recorded beside it (null once they change).
 # Fan-out and prefill: the sum over the step's kernels (their rooflines time the whole step).
 NCU_TRAFFIC = {
-    "gemma4_decode": {"bytes": 48523264, "source_sha": "513ce3b52e3ae85c"},
-    "tiny_decode": {"bytes": 126208, "source_sha": "513ce3b52e3ae85c"},
-    "long_decode": {"bytes": 1547992320 + 3383552, "source_sha": "513ce3b52e3ae85c"},
-    "fanout_decode": {"bytes": 6422528 + 32275456, "source_sha": "fc5e6005f7459510"},
-    "chunked_prefill": {"bytes": 8453120 + (121486336 + 61794304) + (106606080 + 24052992),
-                        "source_sha": "af4591aa2d03b232"},
+    "gemma4_decode": {"bytes": 48517376 + 256, "source_sha": "2b55baa1e3b608b8"},
+    "tiny_decode": {"bytes": 126208, "source_sha": "2b55baa1e3b608b8"},
+    "long_decode": {"bytes": 1547959808 + 3394816, "source_sha": "2b55baa1e3b608b8"},
+    "fanout_decode": {"bytes": 6422272 + 32283392, "source_sha": "d1b44b3f15f3dd7a"},
+    "chunked_prefill": {"bytes": 8451072 + (121420032 + 61526272) + (106605568 + 23967232),
+                        "source_sha": "095252ce3cb0fb23"},
 }
 
 _DECODE_SOURCES = ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh",
@@ -367,10 +367,12 @@ class FanoutWork:
             self.l_pre = torch.empty((1, A, Hq), dtype=torch.float32, device=dev)
             self.out = torch.empty((A * Hq, D), dtype=torch.float32, device=dev)
             self.lse = torch.empty(A * Hq, dtype=torch.float32, device=dev)
-            self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], P, A, Hq), dtype=torch.uint8,
+            # Split counts that let the tail pass run beside the prefix pass (it waits for it only to merge).
+            self.ps, self.ts = ckv.fanout_plan(A, Hkv, Hq)
+            self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], P, A, Hq, self.ps), dtype=torch.uint8,
                                   device=dev)
-            self.ws_t = torch.zeros(ckv.attn_decode_f16_merge_workspace(D, Hkv, A, TL, 1, Hq), dtype=torch.uint8,
-                                    device=dev)
+            self.ws_t = torch.zeros(ckv.attn_decode_f16_merge_workspace(D, Hkv, A, TL, 1, Hq, self.ts),
+                                    dtype=torch.uint8, device=dev)
             self.seq_p = torch.full((1,), P, dtype=torch.int32, device=dev)
             self.seq_t = torch.full((A,), TL, dtype=torch.int32, device=dev)
         stream.synchronize()
@@ -383,11 +385,12 @@ class FanoutWork:
         c, (kt, vt) = self.caches[i % self.n_rot], self.tails[i % self.n_rot]
         # The agents' queries as 15 query tokens of one sequence over the prefix,
         # and as 15 sequences of one query token over their own tails.
-        ckv.attn_decode(c, self.seq_p, self.P, qa[None], self.scale, self.o_pre, self.l_pre, self.ws, stream=s)
+        ckv.attn_decode(c, self.seq_p, self.P, qa[None], self.scale, self.o_pre, self.l_pre, self.ws,
+                        n_split=self.ps, stream=s)
         A, Hq, D = self.A, self.Hq, self.D
         ckv.attn_decode_f16_merge(kt, vt, self.seq_t, self.TL, qa[:, None], self.scale, self.o_pre.view(A, 1, Hq, D),
                                   self.l_pre.view(A, 1, Hq), self.out.view(A, 1, Hq, D), self.lse.view(A, 1, Hq),
-                                  self.ws_t, stream=s)
+                                  self.ws_t, n_split=self.ts, stream=s)
 
     def step(self, i):
         self._run(i, self.qa)
@@ -414,6 +417,7 @@ class FanoutWork:
         return {"workload": "fanout_decode", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
                 "agents": self.A, "prefix_tokens": self.P, "tail_tokens": self.TL,
                 "step": "attn_decode(prefix, 15 agents) + attn_decode_f16_merge(tails, merged with the prefix)",
+                "splits": {"prefix": self.ps, "tails": self.ts, "from": "ckv_fanout_plan"},
                 "l2": f"rotating {self.n_rot} copies ({self.n_rot * self.per_copy / 1e6:.0f} MB > 4x L2)"}
 
     def roofline(self, kernel_ms, peaks):

@@ -10,5 +10,6 @@ from ._binding import (CkvError, PackedCache, attn_decode, attn_decode_append, a
                        attn_decode_dca, attn_decode_dca_workspace, attn_decode_noalloc, attn_decode_verify,
                        attn_decode_f16_workspace, attn_decode_workspace, attn_prefill, attn_prefill_f16,
                        attn_prefill_prefix, attn_prefill_shared, attn_prefill_shared_workspace,
-                       attn_prefill_workspace, cache_bytes, calibrate_stream, f16_append, kv_pack, load, lse_merge,
-                       read_device_flag, read_noalloc_flag, set_concurrent_kernels, selftest_bounded_waits, version)
+                       attn_prefill_workspace, cache_bytes, calibrate_stream, f16_append, fanout_plan, kv_pack, load,
+                       lse_merge, read_device_flag, read_noalloc_flag, set_concurrent_kernels, selftest_bounded_waits,
+                       version)

@@ -61,6 +61,8 @@ SIGNATURES = {
     "ckv_attn_decode_f16_merge_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode_f16_merge": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
                                            _c_int, _c_f, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "ckv_fanout_plan": (_c_int, [_c_int, _c_int, _c_int, ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_int32)]),
     "ckv_attn_decode_f16": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
                                      _c_int, _c_f, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_lse_merge": (_c_int, [_c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _c_i64, _c_int, _vp, _vp,
@@ -256,6 +258,13 @@ def attn_decode_f16_merge(k, v, seq_len, max_seq_len: int, q, scale: float, prio
                                             max_seq_len, _ptr(q), n_q, n_q_heads, scale, n_split, _ptr(prior_o),
                                             _ptr(prior_lse), _ptr(out), _ptr(lse), _ptr(workspace),
                                             workspace.numel(), _stream(stream)))
+
+
+def fanout_plan(n_agents: int, n_kv_heads: int, n_q_heads: int):
+    """(prefix_splits, tail_splits) for the fan-out step on the current device (0, 0: automatic)."""
+    ps, ts = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load().ckv_fanout_plan(n_agents, n_kv_heads, n_q_heads, ctypes.byref(ps), ctypes.byref(ts)))
+    return ps.value, ts.value
 
 
 def attn_decode_f16(k, v, seq_len, max_seq_len: int, q, scale: float, out, lse, workspace,

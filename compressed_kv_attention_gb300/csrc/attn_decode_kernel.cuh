@@ -258,7 +258,6 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
   // the consumers fill the centroid table, one copy per lane. B <= 3: entry f
   // (2B bits) = fp16x2(c[f % 2^B], c[f / 2^B]); B = 4: entry f = c[f] in
   // both halves. Values are c / centroid_scale(B).
-  griddep_launch_dependents();
   if (warp == C::NCW) {
     if (lane == 0) {
       for (int s = 0; s < C::NSTAGE; ++s) {
@@ -280,6 +279,10 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
     }
   }
   griddep_wait();
+  // The next grid may begin only now: a grid that reads its inputs before its
+  // own wait (the fp16 decode with a prior partial) then runs beside this one
+  // alone, never beside the grids before it, which may still write them.
+  griddep_launch_dependents();
 
   // Query fragments first: issued before the producer starts its bulk copies,
   // these small loads do not queue behind them. The sequence length is read by

@@ -145,7 +145,7 @@ int set_last_error(int status, const char* fmt, ...) {
 
 extern "C" {
 
-int32_t ckv_version(void) { return 103; }
+int32_t ckv_version(void) { return 104; }
 
 void ckv_set_concurrent_kernels(int32_t on) { ckv::g_concurrent.store(on ? 1 : 0, std::memory_order_relaxed); }
 
@@ -590,6 +590,29 @@ ckv_status ckv_attn_decode_f16_merge(const void* k_f16, const void* v_f16, int32
   return run_decode(false, nullptr, k_f16, v_f16, head_dim, n_kv_heads, batch, capacity, seq_len, max_seq_len,
                     q_f16, n_q, n_q_heads, scale, n_split, out, lse, workspace, ws_bytes, stream, nullptr, 0, 0, 0,
                     0, prior_o, prior_lse);
+}
+
+ckv_status ckv_fanout_plan(int32_t n_agents, int32_t n_kv_heads, int32_t n_q_heads, int32_t* prefix_splits,
+                           int32_t* tail_splits) {
+  if (!prefix_splits || !tail_splits) return fail(CKV_ERR_INVALID_ARG, "null output");
+  if (n_agents <= 0 || n_kv_heads <= 0 || n_q_heads <= 0) return fail(CKV_ERR_INVALID_ARG, "counts must be positive");
+  if (n_q_heads % n_kv_heads)
+    return fail(CKV_ERR_UNSUPPORTED, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, n_kv_heads);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return fail(CKV_ERR_CUDA, "cannot query the device");
+  const int64_t group_q = n_q_heads / n_kv_heads;
+  // Tail pass: batch n_agents, one query token; prefix pass: batch 1, n_agents query tokens.
+  const int64_t tail_groups = static_cast<int64_t>(n_agents) * n_kv_heads * ((group_q + 7) / 8);
+  const int64_t prefix_groups = static_cast<int64_t>(n_kv_heads) * ((group_q * n_agents + 7) / 8);
+  *prefix_splits = 0;
+  *tail_splits = 0;
+  if (2 * tail_groups >= sms) return CKV_OK;
+  const int64_t ps = (sms - tail_groups) / prefix_groups;
+  if (ps < 1) return CKV_OK;
+  *prefix_splits = static_cast<int32_t>(ps < ckv::kMaxSplits ? ps : ckv::kMaxSplits);
+  *tail_splits = 1;
+  return CKV_OK;
 }
 
 ckv_status ckv_f16_append(void* k_f16, void* v_f16, int32_t head_dim, int32_t n_kv_heads, int32_t batch,

@@ -51,7 +51,6 @@ __global__ void __launch_bounds__((kNCW + 1) * 32, 1) stream_floor_kernel(FloorA
   const uint8_t* base = a.src + (s_id * a.n_tiles + t0) * a.rec;
   const int stage_bytes = kNP * a.rec;
 
-  ckv::griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNStage; ++s) {
       ckv::mbar_init(&full[s], 1);
@@ -62,6 +61,7 @@ __global__ void __launch_bounds__((kNCW + 1) * 32, 1) stream_floor_kernel(FloorA
   }
   __syncthreads();
   ckv::griddep_wait();
+  ckv::griddep_launch_dependents();
 
   if (warp == kNCW) {
     if (lane == 0) {

@@ -391,6 +391,14 @@ CKV_API ckv_status ckv_attn_decode_f16(const void* k_f16, const void* v_f16, int
  * may alias out or lse. Workspace: ckv_attn_decode_f16_merge_workspace (one
  * more merge slot per row group than attn_decode_f16). Other arguments and
  * errors as attn_decode_f16.
+ * Ordering: the kernel streams K, V and Q (and reads seq_len) before it waits
+ * for the previous kernel on the stream, and waits only before it merges, so
+ * that a prefix decode launched just before it (which writes prior_o and
+ * prior_lse) overlaps its tail pass. So K, V, Q and seq_len must not be
+ * written by the kernel just before it on the stream; kernels that write them
+ * (ckv_f16_append, kv_pack, the caller's own) are fully ordered before it as
+ * usual, because only this library's decode kernels let a following kernel
+ * start early, and only after their own wait.
  */
 CKV_API size_t ckv_attn_decode_f16_merge_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
                                                    int64_t max_seq_len, int32_t n_q, int32_t n_q_heads,
@@ -401,6 +409,25 @@ CKV_API ckv_status ckv_attn_decode_f16_merge(const void* k_f16, const void* v_f1
                                              int32_t n_q, int32_t n_q_heads, float scale, int32_t n_split,
                                              const float* prior_o, const float* prior_lse, float* out, float* lse,
                                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * fanout_plan — split counts for the shared-pool fan-out step (PolyKV page,
+ * section "S1 — SharedKVPool"): the prefix decode (ckv_attn_decode over the
+ * shared cache, batch 1, the n_agents agents' single query tokens as n_q =
+ * n_agents) followed on the same stream by ckv_attn_decode_f16_merge over the
+ * agents' private fp16 tails (batch n_agents, n_q 1). The tail grid streams
+ * its tails on the SMs that the prefix grid leaves free and waits for it only
+ * to merge, so the two run side by side: the plan gives the tail pass one
+ * split per (agent, kv head) row group and the prefix pass as many splits per
+ * row group as fit on the remaining SMs of the current device. When the tail
+ * grid alone would take half of the SMs or more, both counts are 0 (each
+ * call's own automatic choice). This is a host computation: it launches
+ * nothing. Errors: CKV_ERR_INVALID_ARG for non-positive counts or null
+ * outputs, CKV_ERR_UNSUPPORTED if n_q_heads is not a multiple of n_kv_heads,
+ * CKV_ERR_CUDA if the device cannot be queried.
+ */
+CKV_API ckv_status ckv_fanout_plan(int32_t n_agents, int32_t n_kv_heads, int32_t n_q_heads,
+                                   int32_t* prefix_splits, int32_t* tail_splits);
 
 /*
  * lse_merge — exact merge of n_parts normalised partials computed over

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_cache_bytes(lib):
-    assert lib.ckv_version() == 103
+    assert lib.ckv_version() == 104
     assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * (32768 // 16) * (23 * 512 + 32)
     assert lib.ckv_cache_bytes(512, 2, 1, 32768) == 2 * 32768 * 738
     assert lib.ckv_cache_bytes(128, 1, 1, 256) == 256 * 186
@@ -145,6 +145,14 @@ def test_decode_f16_and_merge_argument_checks(lib):
     nul = (ctypes.c_void_p * 2)(fake, None)
     assert lib.ckv_lse_merge(2, ptrs, nul, 10, 512, fake, fake, None) == -1
     assert lib.ckv_lse_merge(2, ptrs, ptrs, 10, 0, fake, fake, None) == -1
+
+
+def test_fanout_plan_argument_checks(lib):
+    ps, ts = ctypes.c_int32(7), ctypes.c_int32(7)
+    assert lib.ckv_fanout_plan(15, 2, 16, None, ctypes.byref(ts)) == -1
+    assert lib.ckv_fanout_plan(0, 2, 16, ctypes.byref(ps), ctypes.byref(ts)) == -1
+    assert lib.ckv_fanout_plan(15, 0, 16, ctypes.byref(ps), ctypes.byref(ts)) == -1
+    assert lib.ckv_fanout_plan(15, 3, 16, ctypes.byref(ps), ctypes.byref(ts)) == -2  # 16 heads over 3 kv heads
 
 
 def test_read_device_flag_checks(lib):

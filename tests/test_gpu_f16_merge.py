@@ -103,6 +103,53 @@ def test_f16_merge_matches_oracle_and_separate_merge(D, A, P, TL, tails, n_split
     H.check_attention(o_gpu, l_gpu, o_ref, l_ref, "f16_merge vs oracle")
 
 
+def test_fanout_back_to_back_matches_each_step_alone():
+    """The fan-out step as the benchmark runs it: the prefix decode and the tail
+    decode with the merge, with the fan-out plan's split counts, launched back
+    to back for several steps with different queries and no synchronisation.
+    The tail pass reads its tails and queries while the prefix pass runs and
+    waits for it only to merge, so each step must still merge its own prefix
+    partial (the prior buffers are reused by every step): every step's output
+    equals, bit for bit, the same two calls run alone."""
+    _need_gpu()
+    D, Hkv, Hq, A, P, TL, N = 512, 2, 16, 15, 4096, 512, 6
+    ps, ts = ckv.fanout_plan(A, Hkv, Hq)
+    seed = 71
+    outl = inputs.outlier_channels(D, 5, seed)
+    kp = torch.from_numpy(inputs.normal_tensor((1, P, Hkv, D), seed, "b2b/kp", outl)).to(DEV)
+    vp = torch.from_numpy(inputs.normal_tensor((1, P, Hkv, D), seed, "b2b/vp", outl)).to(DEV)
+    cache = ckv.PackedCache(D, Hkv, 1, P, inputs.tbq_signs(D), device=DEV)
+    ckv.kv_pack(cache, 0, kp, vp)
+    kt = torch.from_numpy(inputs.normal_tensor((A, Hkv, TL, D), seed, "b2b/kt", outl)).to(DEV)
+    vt = torch.from_numpy(inputs.normal_tensor((A, Hkv, TL, D), seed, "b2b/vt", outl)).to(DEV)
+    qs = [torch.from_numpy(inputs.normal_tensor((A, Hq, D), seed + i, "b2b/q", outl)).to(DEV) for i in range(N)]
+    seq_p = torch.full((1,), P, dtype=torch.int32, device=DEV)
+    seq_t = torch.full((A,), TL, dtype=torch.int32, device=DEV)
+    o_p = torch.empty((1, A, Hq, D), dtype=torch.float32, device=DEV)
+    l_p = torch.empty((1, A, Hq), dtype=torch.float32, device=DEV)
+    ws_p = torch.zeros(ckv.attn_decode_workspace(cache, P, A, Hq, ps), dtype=torch.uint8, device=DEV)
+    ws_m = torch.zeros(ckv.attn_decode_f16_merge_workspace(D, Hkv, A, TL, 1, Hq, ts), dtype=torch.uint8, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+
+    def step(q, out, lse):
+        ckv.attn_decode(cache, seq_p, P, q[None], scale, o_p, l_p, ws_p, n_split=ps)
+        ckv.attn_decode_f16_merge(kt, vt, seq_t, TL, q[:, None], scale, o_p.view(A, 1, Hq, D), l_p.view(A, 1, Hq),
+                                  out, lse, ws_m, n_split=ts)
+
+    outs = [torch.empty((A, 1, Hq, D), dtype=torch.float32, device=DEV) for _ in range(N)]
+    lses = [torch.empty((A, 1, Hq), dtype=torch.float32, device=DEV) for _ in range(N)]
+    for i in range(N):
+        step(qs[i], outs[i], lses[i])
+    torch.cuda.synchronize()
+    assert ckv.read_device_flag(ws_p) == 0 and ckv.read_device_flag(ws_m) == 0
+    out1 = torch.empty((A, 1, Hq, D), dtype=torch.float32, device=DEV)
+    lse1 = torch.empty((A, 1, Hq), dtype=torch.float32, device=DEV)
+    for i in range(N):
+        step(qs[i], out1, lse1)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], out1) and torch.equal(lses[i], lse1), f"step {i}"
+
+
 def test_f16_merge_rejects_missing_or_aliased_prior():
     _need_gpu()
     D, Hkv, Hq, A, TL = 128, 1, 4, 2, 32
