@@ -331,8 +331,8 @@ class DecodeWork:
 
 
 class FanoutWork:
-    """Shared-prefix fan-out: prefix decode (15 agents as 15 query tokens), then the fp16 tails' decode whose
-    split merge takes in the prefix partial (attn_decode_f16_merge)."""
+    """Shared-prefix fan-out: attn_decode_fanout, the prefix decode (15 agents as 15 query tokens) writing its
+    split partials and the fp16 tails' decode, beside it, whose split merge takes them in."""
 
     graph = True
 
@@ -363,34 +363,24 @@ class FanoutWork:
                 kt = inputs.normal_tensor((A, Hkv, TL, D), w.seed, "tail/k", outl, device=str(dev))
                 vt = inputs.normal_tensor((A, Hkv, TL, D), w.seed, "tail/v", outl, device=str(dev))
                 self.tails.append((kt, vt))
-            self.o_pre = torch.empty((1, A, Hq, D), dtype=torch.float32, device=dev)
-            self.l_pre = torch.empty((1, A, Hq), dtype=torch.float32, device=dev)
-            self.out = torch.empty((A * Hq, D), dtype=torch.float32, device=dev)
-            self.lse = torch.empty(A * Hq, dtype=torch.float32, device=dev)
-            # Split counts that let the tail pass run beside the prefix pass (it waits for it only to merge).
+            self.out = torch.empty((A, Hq, D), dtype=torch.float32, device=dev)
+            self.lse = torch.empty((A, Hq), dtype=torch.float32, device=dev)
+            # The split counts the step uses: the tail pass runs beside the prefix pass and merges its partials.
             self.ps, self.ts = ckv.fanout_plan(A, Hkv, Hq)
-            self.ws = torch.zeros(ckv.attn_decode_workspace(self.caches[0], P, A, Hq, self.ps), dtype=torch.uint8,
+            self.ws = torch.zeros(ckv.attn_decode_fanout_workspace(self.caches[0], P, A, TL, Hq), dtype=torch.uint8,
                                   device=dev)
-            self.ws_t = torch.zeros(ckv.attn_decode_f16_merge_workspace(D, Hkv, A, TL, 1, Hq, self.ts),
-                                    dtype=torch.uint8, device=dev)
             self.seq_p = torch.full((1,), P, dtype=torch.int32, device=dev)
             self.seq_t = torch.full((A,), TL, dtype=torch.int32, device=dev)
         stream.synchronize()
         self.tokens_per_step = A
-        self.launches_per_step = 2  # prefix decode, tail decode with the merge
+        self.launches_per_step = 2  # prefix decode (split partials), tail decode merging them
         self.algo_bytes = Hkv * P * inputs.compressed_bytes_per_token(D) + 2 * A * Hkv * TL * D * 2
 
     def _run(self, i, qa):
         ckv, s = self.ckv, self.stream
         c, (kt, vt) = self.caches[i % self.n_rot], self.tails[i % self.n_rot]
-        # The agents' queries as 15 query tokens of one sequence over the prefix,
-        # and as 15 sequences of one query token over their own tails.
-        ckv.attn_decode(c, self.seq_p, self.P, qa[None], self.scale, self.o_pre, self.l_pre, self.ws,
-                        n_split=self.ps, stream=s)
-        A, Hq, D = self.A, self.Hq, self.D
-        ckv.attn_decode_f16_merge(kt, vt, self.seq_t, self.TL, qa[:, None], self.scale, self.o_pre.view(A, 1, Hq, D),
-                                  self.l_pre.view(A, 1, Hq), self.out.view(A, 1, Hq, D), self.lse.view(A, 1, Hq),
-                                  self.ws_t, n_split=self.ts, stream=s)
+        ckv.attn_decode_fanout(c, self.seq_p, self.P, kt, vt, self.seq_t, self.TL, qa, self.scale, self.out, self.lse,
+                               self.ws, stream=s)
 
     def step(self, i):
         self._run(i, self.qa)
@@ -398,7 +388,6 @@ class FanoutWork:
 
     def check(self):
         assert self.ckv.read_device_flag(self.ws, stream=self.stream) == 0
-        assert self.ckv.read_device_flag(self.ws_t, stream=self.stream) == 0
 
     def e2e_setup(self):
         t = self.torch
@@ -416,14 +405,16 @@ class FanoutWork:
     def describe(self):
         return {"workload": "fanout_decode", "head_dim": self.D, "n_kv_heads": self.Hkv, "n_q_heads": self.Hq,
                 "agents": self.A, "prefix_tokens": self.P, "tail_tokens": self.TL,
-                "step": "attn_decode(prefix, 15 agents) + attn_decode_f16_merge(tails, merged with the prefix)",
+                "step": "attn_decode_fanout (prefix decode of the 15 agents writing split partials; fp16 tail "
+                        "decode beside it, merging them)",
                 "splits": {"prefix": self.ps, "tails": self.ts, "from": "ckv_fanout_plan"},
                 "l2": f"rotating {self.n_rot} copies ({self.n_rot * self.per_copy / 1e6:.0f} MB > 4x L2)"}
 
     def roofline(self, kernel_ms, peaks):
         hbm, _, kind = peaks
         achieved = self.algo_bytes / (kernel_ms / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "prefix decode + fp16 tail decode with the merge (whole step)",
+        return {"bound": "hbm", "kernel": "attn_decode_fanout: prefix decode (split partials) + fp16 tail decode "
+                "merging them (whole step)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_kind": kind, "traffic": ncu_traffic("fanout_decode", "fanout"), "algorithmic_bytes": self.algo_bytes,
                 "launch_ms": round(kernel_ms, 6)}

@@ -7,7 +7,8 @@ the library; the first call does, and fails loudly if it was not built.
 """
 from ._binding import (CkvError, PackedCache, attn_decode, attn_decode_append, attn_decode_f16,  # noqa: F401
                        attn_decode_f16_merge, attn_decode_f16_merge_workspace, attn_decode_append_host,
-                       attn_decode_dca, attn_decode_dca_workspace, attn_decode_noalloc, attn_decode_verify,
+                       attn_decode_dca, attn_decode_dca_workspace, attn_decode_fanout, attn_decode_fanout_workspace,
+                       attn_decode_noalloc, attn_decode_verify,
                        attn_decode_f16_workspace, attn_decode_workspace, attn_prefill, attn_prefill_f16,
                        attn_prefill_prefix, attn_prefill_shared, attn_prefill_shared_workspace,
                        attn_prefill_workspace, cache_bytes, calibrate_stream, f16_append, fanout_plan, kv_pack, load,

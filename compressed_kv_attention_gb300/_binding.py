@@ -61,6 +61,9 @@ SIGNATURES = {
     "ckv_attn_decode_f16_merge_workspace": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
     "ckv_attn_decode_f16_merge": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
                                            _c_int, _c_f, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "ckv_attn_decode_fanout_workspace": (_c_size, [_cache_p, _c_i64, _c_int, _c_i64, _c_int]),
+    "ckv_attn_decode_fanout": (_c_int, [_cache_p, _vp, _c_i64, _vp, _vp, _c_i64, _vp, _c_i64, _c_int, _vp, _c_int,
+                                        _c_f, _vp, _vp, _vp, _c_size, _vp]),
     "ckv_fanout_plan": (_c_int, [_c_int, _c_int, _c_int, ctypes.POINTER(ctypes.c_int32),
                                  ctypes.POINTER(ctypes.c_int32)]),
     "ckv_attn_decode_f16": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_i64, _vp, _c_i64, _vp, _c_int,
@@ -258,6 +261,23 @@ def attn_decode_f16_merge(k, v, seq_len, max_seq_len: int, q, scale: float, prio
                                             max_seq_len, _ptr(q), n_q, n_q_heads, scale, n_split, _ptr(prior_o),
                                             _ptr(prior_lse), _ptr(out), _ptr(lse), _ptr(workspace),
                                             workspace.numel(), _stream(stream)))
+
+
+def attn_decode_fanout_workspace(prefix: PackedCache, max_prefix_len: int, n_agents: int, max_tail_len: int,
+                                 n_q_heads: int) -> int:
+    return int(load().ckv_attn_decode_fanout_workspace(prefix.ref(), max_prefix_len, n_agents,
+                                                       max_tail_len, n_q_heads))
+
+
+def attn_decode_fanout(prefix: PackedCache, prefix_len, max_prefix_len: int, k_tail, v_tail, tail_len,
+                       max_tail_len: int, q, scale: float, out, lse, workspace, stream=None):
+    """One fan-out decode step: q fp16 [n_agents, n_q_heads, D] over the shared prefix and each agent's
+    fp16 tail (k_tail, v_tail [n_agents, n_kv_heads, capacity, D]); out [n_agents, n_q_heads, D]."""
+    n_agents, n_kv_heads, capacity, D = k_tail.shape
+    _check(load().ckv_attn_decode_fanout(prefix.ref(), _ptr(prefix_len), max_prefix_len,
+                                         _ptr(k_tail), _ptr(v_tail), capacity, _ptr(tail_len), max_tail_len,
+                                         n_agents, _ptr(q), q.shape[1], scale, _ptr(out), _ptr(lse),
+                                         _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def fanout_plan(n_agents: int, n_kv_heads: int, n_q_heads: int):

@@ -115,14 +115,15 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   float4* xbuf = reinterpret_cast<float4*>(smem + C::OFF_XCHG);
   float* mlbuf = reinterpret_cast<float*>(smem + C::OFF_ML);
 
-  // With a prior partial (written by the previous grid: the shared prefix's
-  // decode) the wait moves to just before the epilogue, so the tails stream
-  // while that grid finishes. Until then the kernel only reads K, V, Q and
+  // With a prior partial or another decode's slots to merge (written by the
+  // previous grid: the shared prefix's decode) the wait moves to just before
+  // the epilogue, so the tails stream while that grid finishes. Until then the kernel only reads K, V, Q and
   // seq_len, which no grid that can still be running writes: the decode
   // kernels start their dependents only after their own wait, and the kernels
   // that write caches or tails do not start them early at all.
+  const bool late_wait = a.prior_o || a.ext_part;
   griddep_launch_dependents();
-  if (!a.prior_o) griddep_wait();
+  if (!late_wait) griddep_wait();
   int seqlen = a.seq_len[b];
   const int64_t lim = a.capacity < a.max_seq_len ? a.capacity : a.max_seq_len;
   if (seqlen < 0 || seqlen > lim) {
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     }
   }
 
-  if (a.prior_o) griddep_wait();  // the prior partial is complete
+  if (late_wait) griddep_wait();  // the prior partial (or the prefix's slots) is complete
   if constexpr (ROWS) {
     rows_epilogue<C>(a, st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane, b, kvh,
                      blockIdx.y * C::NP);

@@ -538,6 +538,7 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
   decode_epilogue<typename C::Sh, C::MT_W, ROT>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp,
                                                 lane, a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
                                                 centroid_scale(B), a.signs2);
+  if (a.slots_only) return;  // the fan-out's tail decode merges these slots
   decode_split_tail<D, C::RING, 256>(a, split, gid, b, kvh, rg, tid, smem);
 }
 

@@ -269,6 +269,16 @@ struct AppendRows {
   int64_t token_stride, batch_stride;
 };
 
+// The fan-out's link between its two decodes (see ckv_attn_decode_fanout):
+// the prefix decode writes slots only; the tail decode merges ext_n of them
+// per row group and raises its errors in the prefix decode's flag word.
+struct FanoutLink {
+  int slots_only;
+  const float* ext_part;
+  int ext_n, ext_nrg;
+  int32_t* flag;
+};
+
 static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void* k16, const void* v16,
                              int D, int Hkv, int B, int64_t capacity, const int32_t* seq_len,
                              int64_t max_seq_len, const void* q, int n_q, int n_q_heads, float scale,
@@ -276,7 +286,8 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              void* stream, const AppendRows* app = nullptr, int causal_q = 0,
                              int dca_chunk = 0, int q_bf16 = 0, int dca_parts = 0,
                              const float* prior_o = nullptr, const float* prior_lse = nullptr,
-                             float* fold_out = nullptr, float* fold_lse = nullptr, int* host_folded = nullptr) {
+                             float* fold_out = nullptr, float* fold_lse = nullptr, int* host_folded = nullptr,
+                             const FanoutLink* link = nullptr) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p, prior_o ? 1 : 0);
   if (s != CKV_OK) return s;
@@ -341,6 +352,13 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
   a.host_folded = host_folded;
   a.ctr_stride = ctr_stride(p.n_split);
   a.flag = reinterpret_cast<int32_t*>(base);
+  if (link) {
+    a.slots_only = link->slots_only;
+    a.ext_part = link->ext_part;
+    a.ext_n = link->ext_n;
+    a.ext_nrg = link->ext_nrg;
+    if (link->flag) a.flag = link->flag;
+  }
   a.counters = reinterpret_cast<uint32_t*>(base + 64);
   a.out = out;
   a.lse = lse;
@@ -592,6 +610,21 @@ ckv_status ckv_attn_decode_f16_merge(const void* k_f16, const void* v_f16, int32
                     0, prior_o, prior_lse);
 }
 
+// Split counts that let the fan-out's tail decode run beside its prefix decode
+// on `sms` SMs (0, 0: each decode's automatic count).
+static void fanout_splits(int64_t n_agents, int64_t n_kv_heads, int64_t group_q, int sms, int* ps_out, int* ts_out) {
+  // Tail pass: batch n_agents, one query token; prefix pass: batch 1, n_agents query tokens.
+  const int64_t tail_groups = n_agents * n_kv_heads * ((group_q + 7) / 8);
+  const int64_t prefix_groups = n_kv_heads * ((group_q * n_agents + 7) / 8);
+  *ps_out = 0;
+  *ts_out = 0;
+  if (2 * tail_groups >= sms) return;
+  const int64_t ps = (sms - tail_groups) / prefix_groups;
+  if (ps < 1) return;
+  *ps_out = static_cast<int>(ps < ckv::kMaxSplits ? ps : ckv::kMaxSplits);
+  *ts_out = 1;
+}
+
 ckv_status ckv_fanout_plan(int32_t n_agents, int32_t n_kv_heads, int32_t n_q_heads, int32_t* prefix_splits,
                            int32_t* tail_splits) {
   if (!prefix_splits || !tail_splits) return fail(CKV_ERR_INVALID_ARG, "null output");
@@ -601,18 +634,114 @@ ckv_status ckv_fanout_plan(int32_t n_agents, int32_t n_kv_heads, int32_t n_q_hea
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return fail(CKV_ERR_CUDA, "cannot query the device");
-  const int64_t group_q = n_q_heads / n_kv_heads;
-  // Tail pass: batch n_agents, one query token; prefix pass: batch 1, n_agents query tokens.
-  const int64_t tail_groups = static_cast<int64_t>(n_agents) * n_kv_heads * ((group_q + 7) / 8);
-  const int64_t prefix_groups = static_cast<int64_t>(n_kv_heads) * ((group_q * n_agents + 7) / 8);
-  *prefix_splits = 0;
-  *tail_splits = 0;
-  if (2 * tail_groups >= sms) return CKV_OK;
-  const int64_t ps = (sms - tail_groups) / prefix_groups;
-  if (ps < 1) return CKV_OK;
-  *prefix_splits = static_cast<int32_t>(ps < ckv::kMaxSplits ? ps : ckv::kMaxSplits);
-  *tail_splits = 1;
+  int ps, ts;
+  fanout_splits(n_agents, n_kv_heads, n_q_heads / n_kv_heads, sms, &ps, &ts);
+  *prefix_splits = ps;
+  *tail_splits = ts;
   return CKV_OK;
+}
+
+// Fan-out workspace: [prefix decode][tail decode][prefix partial O, lse (composed form)].
+struct FanoutWs {
+  size_t pre, tail, o_pre, l_pre, total;
+  int ps, ts;       // split counts (0: automatic)
+  bool fused;       // the tail decode merges the prefix decode's slots
+};
+static bool fanout_ws(const ckv_cache* prefix, int64_t max_prefix_len, int32_t n_agents, int64_t max_tail_len,
+                      int32_t n_q_heads, FanoutWs* w) {
+  if (!prefix || check_cache(prefix) != CKV_OK || prefix->batch != 1 || n_agents <= 0 || n_q_heads <= 0 ||
+      max_prefix_len < 0 || max_tail_len < 0 || n_q_heads != 8 * prefix->n_kv_heads)
+    return false;
+  const int D = prefix->head_dim, Hkv = prefix->n_kv_heads;
+  int ps = 0, ts = 0;
+  fanout_splits(n_agents, Hkv, 8, num_sms(), &ps, &ts);
+  // The fused form needs the prefix on the mma.sync decode (the tile path's
+  // cost model may prefer 128-row tiles for a long prefix) and the tail grid
+  // resident at once (its merge is the rendezvous).
+  const int64_t tail_grid = static_cast<int64_t>(n_agents) * Hkv * (ts ? ts : 1);
+  w->fused = !ckv::concurrent_kernels() && ts > 0 && tail_grid <= num_sms() &&
+             !ckv::rows_decode_applies(1, Hkv, n_q_heads, n_agents, 0, max_prefix_len);
+  w->ps = w->fused ? ps : 0;
+  w->ts = w->fused ? ts : 0;
+  // Regions sized for both forms, so that the size does not depend on which
+  // one a call takes.
+  const size_t pre_f = ts > 0 ? mma_decode_ws(prefix, max_prefix_len, n_agents, n_q_heads, ps) : 0;
+  const size_t pre_c = ckv_attn_decode_workspace(prefix, max_prefix_len, n_agents, n_q_heads, 0);
+  const size_t tail_f = ts > 0 ? ckv_attn_decode_f16_workspace(D, Hkv, n_agents, max_tail_len, 1, n_q_heads, ts) : 0;
+  const size_t tail_c = ckv_attn_decode_f16_merge_workspace(D, Hkv, n_agents, max_tail_len, 1, n_q_heads, 0);
+  if (pre_c == 0 || tail_c == 0 || (ts > 0 && (pre_f == 0 || tail_f == 0))) return false;
+  const size_t pre = pre_f > pre_c ? pre_f : pre_c;
+  const size_t tail = tail_f > tail_c ? tail_f : tail_c;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(n_agents) * n_q_heads;
+  w->pre = 0;
+  w->tail = up(pre);
+  w->o_pre = w->tail + up(tail);
+  w->l_pre = w->o_pre + up(rows * D * sizeof(float));
+  w->total = w->l_pre + up(rows * sizeof(float));
+  return true;
+}
+
+size_t ckv_attn_decode_fanout_workspace(const ckv_cache* prefix, int64_t max_prefix_len, int32_t n_agents,
+                                        int64_t max_tail_len, int32_t n_q_heads) {
+  FanoutWs w;
+  return fanout_ws(prefix, max_prefix_len, n_agents, max_tail_len, n_q_heads, &w) ? w.total : 0;
+}
+
+ckv_status ckv_attn_decode_fanout(const ckv_cache* prefix, const int32_t* prefix_len, int64_t max_prefix_len,
+                                  const void* k_tail, const void* v_tail, int64_t tail_capacity,
+                                  const int32_t* tail_len, int64_t max_tail_len, int32_t n_agents, const void* q_f16,
+                                  int32_t n_q_heads, float scale, float* out, float* lse, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  ckv_status s = check_cache(prefix);
+  if (s != CKV_OK) return s;
+  if (prefix->batch != 1) return fail(CKV_ERR_INVALID_ARG, "the shared prefix cache holds one sequence (batch 1)");
+  if (n_agents <= 0 || n_q_heads <= 0) return fail(CKV_ERR_INVALID_ARG, "n_agents and n_q_heads must be positive");
+  if (n_q_heads != 8 * prefix->n_kv_heads)
+    return fail(CKV_ERR_UNSUPPORTED, "the fan-out step needs 8 query heads per kv head (%d over %d)", n_q_heads,
+                prefix->n_kv_heads);
+  if (max_prefix_len < 0 || max_prefix_len > prefix->capacity) return fail(CKV_ERR_INVALID_ARG, "max_prefix_len outside the cache");
+  if (max_tail_len < 0 || max_tail_len > tail_capacity) return fail(CKV_ERR_INVALID_ARG, "max_tail_len outside the tails");
+  if (tail_capacity <= 0 || tail_capacity % 16) return fail(CKV_ERR_INVALID_ARG, "tail capacity must be a positive multiple of 16");
+  if (!k_tail || !v_tail || !aligned(k_tail, 16) || !aligned(v_tail, 16))
+    return fail(CKV_ERR_INVALID_ARG, "tail k/v null or not 16-byte aligned");
+  if (!prefix_len || !aligned(prefix_len, 4)) return fail(CKV_ERR_INVALID_ARG, "prefix_len null or misaligned");
+  FanoutWs w;
+  if (!fanout_ws(prefix, max_prefix_len, n_agents, max_tail_len, n_q_heads, &w))
+    return fail(CKV_ERR_INVALID_ARG, "invalid fan-out geometry");
+  s = check_ws(workspace, ws_bytes, w.total);
+  if (s != CKV_OK) return s;
+  const int D = prefix->head_dim, Hkv = prefix->n_kv_heads;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  if (!w.fused) {
+    // Composed form: the prefix partial goes through the workspace and the
+    // tail decode merges it as its prior.
+    float* o_pre = reinterpret_cast<float*>(base + w.o_pre);
+    float* l_pre = reinterpret_cast<float*>(base + w.l_pre);
+    s = ckv_attn_decode(prefix, prefix_len, max_prefix_len, q_f16, n_agents, n_q_heads, scale, 0, o_pre, l_pre,
+                        base + w.pre, w.tail - w.pre, stream);
+    if (s != CKV_OK) return s;
+    FanoutLink fl{0, nullptr, 0, 0, reinterpret_cast<int32_t*>(base + w.pre)};  // one flag word for the step
+    return run_decode(false, nullptr, k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, max_tail_len, q_f16,
+                      1, n_q_heads, scale, 0, out, lse, base + w.tail, w.o_pre - w.tail, stream, nullptr, 0, 0, 0, 0,
+                      o_pre, l_pre, nullptr, nullptr, nullptr, &fl);
+  }
+  // Fused form: the prefix decode writes its split slots and leaves; the tail
+  // decode, beside it on the SMs it leaves free, merges its own split with the
+  // prefix's slots of the same rows.
+  DecodePlan pp;
+  s = plan_decode(D, Hkv, 1, max_prefix_len, n_agents, n_q_heads, w.ps, &pp);
+  if (s != CKV_OK) return s;
+  FanoutLink pl{1, nullptr, 0, 0, nullptr};
+  s = run_decode(true, prefix, nullptr, nullptr, D, Hkv, 1, prefix->capacity, prefix_len, max_prefix_len, q_f16,
+                 n_agents, n_q_heads, scale, w.ps, out, lse, base + w.pre, w.tail - w.pre, stream, nullptr, 0, 0, 0,
+                 0, nullptr, nullptr, nullptr, nullptr, nullptr, &pl);
+  if (s != CKV_OK) return s;
+  FanoutLink tl{0, reinterpret_cast<const float*>(base + w.pre + ws_header_bytes(pp.groups, pp.n_split)),
+                pp.n_split, pp.n_row_groups, reinterpret_cast<int32_t*>(base + w.pre)};
+  return run_decode(false, nullptr, k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, max_tail_len, q_f16,
+                    1, n_q_heads, scale, w.ts, out, lse, base + w.tail, w.o_pre - w.tail, stream, nullptr, 0, 0, 0, 0,
+                    nullptr, nullptr, nullptr, nullptr, nullptr, &tl);
 }
 
 ckv_status ckv_f16_append(void* k_f16, void* v_f16, int32_t head_dim, int32_t n_kv_heads, int32_t batch,

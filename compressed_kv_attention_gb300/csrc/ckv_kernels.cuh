@@ -74,6 +74,15 @@ struct DecodeArgs {
   float* fold_out;
   float* fold_lse;
   int* host_folded;
+  // Fan-out, prefix side (compressed decode): the CTAs write their split slots
+  // and leave; another decode merges them.
+  int slots_only;
+  // Fan-out, tail side (fp16 decode, one query token, 8 query heads per kv
+  // head): the split merge of row group (b, kvh) also takes in ext_n slots of
+  // a slots_only decode of one sequence whose row group b of kv head kvh holds
+  // the same 8 rows: ext_part + ((kvh * ext_nrg + b) * ext_n + s) * slot.
+  const float* ext_part;
+  int ext_n, ext_nrg;
   int rendezvous;            // 1: every CTA resident at once, merge by rendezvous
   int32_t* flag;
   uint32_t* counters;        // ctr_stride words per group, zero between calls

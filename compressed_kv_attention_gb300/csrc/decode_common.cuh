@@ -639,7 +639,7 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 // of the 8 x D rows (unit u: row u / (D/4), dims 4 (u % (D/4)) .. +4), from the
 // n_split slots at `slots`. Threads tid < nthr (a multiple of 32, >= 256) take
 // part and synchronise on named barrier `bar_id`; `sm` holds
-// 8 n_split + 16 nthr / 32 floats. The partials sit in L2, so the cost is
+// 8 (n_split + n_extra) + 16 nthr / 32 floats. The partials sit in L2, so the cost is
 // dependent round trips: every thread issues its (m, l) loads and its first
 // batch of partial loads before it waits on any; row maxima and sums are
 // reduced by all threads at once (the (m, l) entries a thread holds all belong
@@ -648,19 +648,23 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 template <int D>
 __device__ __forceinline__ void merge_slice(const float* slots, int n_split, int u0, int u1, int tid, int nthr,
                                             float* sm, float* const* out_rows, float* const* lse_rows,
-                                            bool write_lse, int bar_id, const float* extra = nullptr) {
+                                            bool write_lse, int bar_id, const float* extra = nullptr,
+                                            int n_extra = 1) {
   constexpr int U = D / 4;                               // float4 units per row
   constexpr int64_t SLOT = merge_slot_floats(D);
   constexpr int MLR = 4;                                 // (m, l) pairs per thread in registers
   constexpr int PB = 8;                                  // partial loads per thread per batch
+  // Slot s < n_split at slots + s SLOT; with `extra`, slots n_split ..
+  // n_split + n_extra - 1 follow at extra, extra + SLOT, ...
+  const int n_real = n_split;
+  if (extra) n_split += n_extra;
   const int nw = nthr >> 5;
-  float* w = sm;                   // [n_split][8] weights
+  float* w = sm;                   // [n_split][8] weights (every slot, the extra ones included)
   float* wmax = w + n_split * 8;   // [nw][8] per-warp row maxima
   float* wsum = wmax + nw * 8;     // [nw][8] per-warp row sums
-  // Slot s < n_split at slots + s SLOT; with `extra`, slot n_split is there.
-  if (extra) ++n_split;
-  const int n_real = extra ? n_split - 1 : n_split;
-  auto slot_at = [&](int sidx) { return sidx < n_real ? slots + (int64_t)sidx * SLOT : extra; };
+  auto slot_at = [&](int sidx) {
+    return sidx < n_real ? slots + (int64_t)sidx * SLOT : extra + (int64_t)(sidx - n_real) * SLOT;
+  };
   const int n_ml = n_split * 8;
   const int nu = u1 - u0;
   const int lane = tid & 31, warp = tid >> 5;
@@ -840,8 +844,16 @@ __device__ __forceinline__ void rendezvous_merge_tail(const DecodeArgs& a, int s
   if (!s_ok) return;
   const int u0 = (int)((int64_t)cm * 2 * D / nm);
   const int u1 = (int)((int64_t)(cm + 1) * 2 * D / nm);
+  const float* extra = nullptr;
+  int n_extra = 1;
+  if (a.prior_o) {
+    extra = a.sub + (gid * a.sub_stride + a.merge_nl) * merge_slot_floats(D);
+  } else if (a.ext_part) {
+    extra = a.ext_part + ((int64_t)kvh * a.ext_nrg + b) * a.ext_n * merge_slot_floats(D);
+    n_extra = a.ext_n;
+  }
   merge_slice<D>(a.part + mg * nm * merge_slot_floats(D), nm, u0, u1, tid, NT, scratch, s_out, s_lse, cm == 0, 1,
-                 a.prior_o ? a.sub + (gid * a.sub_stride + a.merge_nl) * merge_slot_floats(D) : nullptr);
+                 extra, n_extra);
   if (tid == 0 && dep + 1 == n) {  // the last CTA to leave: nobody reads the counters any more
     *arrive = 0u;
     *depart = 0u;
@@ -899,6 +911,9 @@ static inline cudaError_t launch_split_decode(K kernel, DecodeArgs a, int thread
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
   if (cache->blocks[dev] == 0) cache->blocks[dev] = coresident_blocks(kernel, threads, smem);
   a.rendezvous = (!concurrent_kernels() && grid_total <= cache->blocks[dev]) ? 1 : 0;
+  // Another decode's slots (ext_part) are merged only by the rendezvous; the
+  // caller checks residency before it asks for them.
+  if (a.ext_part && !a.rendezvous) return cudaErrorNotSupported;
   if (!a.rendezvous) a.dca_fold = 0;
   if (a.host_folded) *a.host_folded = a.dca_fold;
   cudaLaunchConfig_t cfg = {};

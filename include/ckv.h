@@ -430,6 +430,46 @@ CKV_API ckv_status ckv_fanout_plan(int32_t n_agents, int32_t n_kv_heads, int32_t
                                    int32_t* prefix_splits, int32_t* tail_splits);
 
 /*
+ * attn_decode_fanout — one decode step of the shared-pool fan-out (PolyKV
+ * page, section "S1 — SharedKVPool": one compressed prefix counted once, a
+ * private fp16 suffix per agent; DCA page, "Implementation progress +
+ * Section-D simplification": partials over disjoint key sets combined by the
+ * LSE merge). Agent a's query token (n_q_heads heads) attends the prefix
+ * positions [0, prefix_len[0]) of `prefix` (a packed cache of one sequence)
+ * and its own tail positions [0, tail_len[a]). Two launches: the prefix
+ * decode (the agents as n_agents query tokens of one sequence) writes its
+ * split partials and no output; the fp16 tail decode, with the split counts
+ * of ckv_fanout_plan so that it runs beside the prefix decode on the SMs it
+ * leaves free, merges its own partial with the prefix decode's partials of
+ * the same 8 rows in its split merge. When that form does not apply (the
+ * tile path's cost model picks 128-row tiles for a long prefix, the tail grid
+ * does not fit on the device at once, or ckv_set_concurrent_kernels is on)
+ * the step runs as ckv_attn_decode into the workspace followed by
+ * ckv_attn_decode_f16_merge; the result is the same attention.
+ * n_q_heads must be 8 * prefix->n_kv_heads (one row group of 8 query heads
+ * per agent and kv head), else CKV_ERR_UNSUPPORTED: compose ckv_attn_decode
+ * and ckv_attn_decode_f16_merge instead.
+ * prefix_len: device int32 [1], <= max_prefix_len <= prefix capacity.
+ * k_tail, v_tail: device fp16 [n_agents][n_kv_heads][tail_capacity][D]
+ * (tail_capacity a multiple of 16); tail_len: device int32 [n_agents], each
+ * <= max_tail_len <= tail_capacity. q_f16: device fp16 [n_agents][n_q_heads][D].
+ * out: float32 [n_agents][n_q_heads][D]; lse: float32 [n_agents][n_q_heads].
+ * workspace: ckv_attn_decode_fanout_workspace bytes (0: invalid geometry),
+ * 256-byte aligned, zero-filled before first use and left reusable by each
+ * call; ckv_read_device_flag on it reports both launches' device errors.
+ * Ordering as ckv_attn_decode_f16_merge: K, V, Q and tail_len must not be
+ * written by the kernel just before this call on the stream.
+ */
+CKV_API size_t ckv_attn_decode_fanout_workspace(const ckv_cache* prefix, int64_t max_prefix_len,
+                                                int32_t n_agents, int64_t max_tail_len, int32_t n_q_heads);
+CKV_API ckv_status ckv_attn_decode_fanout(const ckv_cache* prefix, const int32_t* prefix_len,
+                                          int64_t max_prefix_len, const void* k_tail, const void* v_tail,
+                                          int64_t tail_capacity, const int32_t* tail_len, int64_t max_tail_len,
+                                          int32_t n_agents, const void* q_f16, int32_t n_q_heads, float scale,
+                                          float* out, float* lse, void* workspace, size_t ws_bytes,
+                                          void* stream);
+
+/*
  * lse_merge — exact merge of n_parts normalised partials computed over
  * disjoint key sets (DCA page, "Implementation progress + Section-D
  * simplification": M = max lse_r, w_r = exp(lse_r - M), O = sum w_r O_r / sum w_r,

@@ -147,6 +147,29 @@ def test_decode_f16_and_merge_argument_checks(lib):
     assert lib.ckv_lse_merge(2, ptrs, ptrs, 10, 0, fake, fake, None) == -1
 
 
+def test_fanout_step_argument_checks(lib):
+    fake = 0x7f0000000000
+    pre = _fake_cache(D=512, Hkv=2, batch=1, cap=4096)
+    need = lib.ckv_attn_decode_fanout_workspace(ctypes.byref(pre), 4096, 15, 512, 16)
+    assert need > 15 * 16 * 512 * 4  # holds at least the prefix partial of the composed form
+    assert need % 256 == 0
+    assert lib.ckv_attn_decode_fanout_workspace(ctypes.byref(pre), 4096, 15, 512, 8) == 0   # 4 heads per kv head
+    assert lib.ckv_attn_decode_fanout_workspace(ctypes.byref(pre), 4096, 0, 512, 16) == 0
+    two = _fake_cache(D=512, Hkv=2, batch=2, cap=4096)
+    assert lib.ckv_attn_decode_fanout_workspace(ctypes.byref(two), 4096, 15, 512, 16) == 0  # prefix of 2 sequences
+
+    def call(cache, n_q_heads=16, max_prefix=4096, cap=512, max_tail=512, k=fake, ws_bytes=need):
+        return lib.ckv_attn_decode_fanout(ctypes.byref(cache), fake, max_prefix, k, fake, cap, fake, max_tail, 15,
+                                          fake, n_q_heads, 0.04, fake, fake, fake, ws_bytes, None)
+    assert call(pre, n_q_heads=8) == -2
+    assert call(two) == -1
+    assert call(pre, max_prefix=5000) == -1       # beyond the prefix capacity
+    assert call(pre, max_tail=600) == -1          # beyond the tail capacity
+    assert call(pre, cap=500, max_tail=400) == -1  # tail capacity not a multiple of 16
+    assert call(pre, k=fake + 8) == -1
+    assert call(pre, ws_bytes=need - 256) == -3
+
+
 def test_fanout_plan_argument_checks(lib):
     ps, ts = ctypes.c_int32(7), ctypes.c_int32(7)
     assert lib.ckv_fanout_plan(15, 2, 16, None, ctypes.byref(ts)) == -1

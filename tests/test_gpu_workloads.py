@@ -82,21 +82,16 @@ def test_fanout_decode_full():
     lse = torch.empty(A * Hq, dtype=torch.float32, device=DEV)
     ckv.lse_merge([to_dev(o_pre.reshape(A * Hq, D)), o_t.view(A * Hq, D)],
                   [to_dev(l_pre.reshape(A * Hq)), l_t.view(A * Hq)], out, lse)
-    # The benchmark's path: the prefix decode, then the tail decode with the prefix partial merged in,
-    # back to back with the fan-out plan's split counts (the tail pass streams while the prefix runs).
-    ps, ts = ckv.fanout_plan(A, Hkv, Hq)
-    o_p = torch.empty((1, A, Hq, D), dtype=torch.float32, device=DEV)
-    l_p = torch.empty((1, A, Hq), dtype=torch.float32, device=DEV)
-    ws_p = torch.zeros(ckv.attn_decode_workspace(cache, P, A, Hq, ps), dtype=torch.uint8, device=DEV)
-    ws_m = torch.zeros(ckv.attn_decode_f16_merge_workspace(D, Hkv, A, TL, 1, Hq, ts), dtype=torch.uint8, device=DEV)
-    out2 = torch.empty((A, 1, Hq, D), dtype=torch.float32, device=DEV)
-    lse2 = torch.empty((A, 1, Hq), dtype=torch.float32, device=DEV)
-    ckv.attn_decode(cache, torch.full((1,), P, dtype=torch.int32, device=DEV), P, to_dev(qa[None]), scale, o_p, l_p,
-                    ws_p, n_split=ps)
-    ckv.attn_decode_f16_merge(to_dev(kt), to_dev(vt), torch.full((A,), TL, dtype=torch.int32, device=DEV), TL, qd,
-                              scale, o_p.view(A, 1, Hq, D), l_p.view(A, 1, Hq), out2, lse2, ws_m, n_split=ts)
+    # The benchmark's path: the fan-out step (prefix decode writing split partials, fp16 tail decode
+    # beside it merging them).
+    ws_f = torch.zeros(ckv.attn_decode_fanout_workspace(cache, P, A, TL, Hq), dtype=torch.uint8, device=DEV)
+    out2 = torch.empty((A, Hq, D), dtype=torch.float32, device=DEV)
+    lse2 = torch.empty((A, Hq), dtype=torch.float32, device=DEV)
+    ckv.attn_decode_fanout(cache, torch.full((1,), P, dtype=torch.int32, device=DEV), P, to_dev(kt), to_dev(vt),
+                           torch.full((A,), TL, dtype=torch.int32, device=DEV), TL, to_dev(qa), scale, out2, lse2,
+                           ws_f)
     torch.cuda.synchronize()
-    assert ckv.read_device_flag(ws_p) == 0 and ckv.read_device_flag(ws_m) == 0
+    assert ckv.read_device_flag(ws_f) == 0
     # Oracle: per agent, merge(prefix attention over the dequantised pool, tail attention).
     qs, d16, codes, n16, _ = oracle_cache(k, v, signs)
     kh = O.q8_0_dequantize(qs[0], d16[0])
@@ -109,7 +104,7 @@ def test_fanout_decode_full():
                                     scale)
         o_ref[a], l_ref[a] = O.lse_merge([op[0], ot[0]], [lp[0], lt[0]])
     H.check_attention(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "fan-out")
-    H.check_attention(out2.cpu().numpy()[:, 0], lse2.cpu().numpy()[:, 0], o_ref, l_ref, "fan-out, planned splits")
+    H.check_attention(out2.cpu().numpy(), lse2.cpu().numpy(), o_ref, l_ref, "fan-out step")
 
 
 @pytest.mark.parametrize("name,checks", [("long_decode", ((0, 0), (1, 1), (2, 0), (2, 1), (3, 1))),
