@@ -117,10 +117,11 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
 
   // With a prior partial or another decode's slots to merge (written by the
   // previous grid: the shared prefix's decode) the wait moves to just before
-  // the epilogue, so the tails stream while that grid finishes. Until then the kernel only reads K, V, Q and
-  // seq_len, which no grid that can still be running writes: the decode
-  // kernels start their dependents only after their own wait, and the kernels
-  // that write caches or tails do not start them early at all.
+  // the epilogue, so the tails stream while that grid finishes. Until then
+  // the kernel only reads K, V, Q and seq_len, which no grid that can still be
+  // running writes: the decode kernels start their dependents only after their
+  // own wait, and the kernels that write caches or tails do not start them
+  // early at all.
   const bool late_wait = a.prior_o || a.ext_part;
   griddep_launch_dependents();
   if (!late_wait) griddep_wait();
@@ -176,52 +177,126 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   SoftmaxState st{-INFINITY, -INFINITY, 0.0f, 0.0f};
   const int dbase = C::GD * g + 2 * wh * C::MT_W;  // first output dim of this lane's m-tiles
 
-  for (int it = 0; it < n_iters; ++it) {
-    const int64_t tile = ROWS ? (int64_t)it : tile_begin + (int64_t)it * C::NP + group;
-    if (tile >= tile_end) break;  // uniform across the warps of a group
-    const int64_t tpos = tile * kTile;
-    // ---- S^T = K Q^T ----
-    float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const __half* k0p = kb + (tpos + g) * D + 8 * t;
-    const __half* k1p = kb + (tpos + g + 8) * D + 8 * t;
+  // ROWS at D = 512: the NP groups walk the same tiles, so the whole CTA
+  // stages each tile in shared memory with cp.async, double-buffered, and the
+  // groups read their fragments from there (one L2 round trip per tile, under
+  // the previous tile's work, instead of one per fragment load). The 16-byte
+  // chunk c of tile row r sits at chunk c ^ ((r & 7) << 2) of its 1 KB row for
+  // K and c ^ (((c >> 3) + 2 ((r >> 1) & 3)) & 7) for V: the 8 lanes of each
+  // phase of a fragment load then fall on 8 different bank groups. The loop
+  // runs to the last tile of any group, so that every thread meets the
+  // barriers; a group past its own last tile only helps to stage.
+  constexpr bool STG = ROWS && D == 512;
+  static_assert(!STG || (C::THREADS == 256 && C::MT_W == 16 && C::RED_BYTES >= 65536), "staging layout");
+  const uint32_t stg0 = smem_u32(smem);
+  int cta_iters = n_iters;
+  if constexpr (STG) {
+    __shared__ int s_iters;
+    if (tid == 0) s_iters = 0;
+    __syncthreads();
+    if (lane == 0) atomicMax(&s_iters, n_iters);
+    __syncthreads();
+    cta_iters = s_iters;
+  }
+  auto stage = [&](int64_t tile, int buf) {
+    const __half* ks = kb + tile * kTile * D;
+    const __half* vs = vb + tile * kTile * D;
+    const uint32_t sk = stg0 + buf * 32768, sv = sk + 16384;
 #pragma unroll
-    for (int i = 0; i < C::NB_W; ++i) {
-      const int blk = wh * C::NB_W + i;
-      const uint4 k0 = __ldg(reinterpret_cast<const uint4*>(k0p + blk * 32));
-      const uint4 k1 = __ldg(reinterpret_cast<const uint4*>(k1p + blk * 32));
-      mma16816(S, k0.x, k1.x, k0.y, k1.y, qf[i][0], qf[i][1]);
-      mma16816(S, k0.z, k1.z, k0.w, k1.w, qf[i][2], qf[i][3]);
+    for (int k = 0; k < 4; ++k) {
+      const int idx = tid + 256 * k;
+      const int r = idx >> 6, c = idx & 63;
+      const uint32_t dk = sk + r * 1024 + ((c ^ ((r & 7) << 2)) << 4);
+      const uint32_t dv = sv + r * 1024 + ((c ^ (((c >> 3) + 2 * ((r >> 1) & 3)) & 7)) << 4);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dk), "l"(ks + r * D + c * 8) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dv), "l"(vs + r * D + c * 8) : "memory");
     }
-    if constexpr (C::WT >= 2) exchange_S<C::WT>(S, xbuf, group, wh, it & 1, lane);
-    uint32_t pb0, pb1, pl[2] = {0u, 0u};
-    softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lo0, lim0, lo1, lim1, a.scale_log2, 1.0f, 1.0f, st, acc, pb0,
-                                     pb1, pl);
-    // ---- O^T += V^T P^T: lane reads positions 2t, 2t+1, 2t+8, 2t+9 ----
-    const __half* vp = vb + tpos * D + dbase;
-    // Rows at or past seq_len may hold any bytes (a NaN there would reach O
-    // through P = 0): they enter as zero.
-    const int64_t vrem = seqlen - tpos;
-    const bool ve0 = 2 * t < vrem, vo0 = 2 * t + 1 < vrem, ve1 = 2 * t + 8 < vrem, vo1 = 2 * t + 9 < vrem;
-    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int c4 = 0; c4 < C::MT_W / 4; ++c4) {
-      const uint4 e0 = ve0 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t) * D + c4 * 8)) : z4;
-      const uint4 o0 = vo0 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 1) * D + c4 * 8)) : z4;
-      const uint4 e1 = ve1 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 8) * D + c4 * 8)) : z4;
-      const uint4 o1 = vo1 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 9) * D + c4 * 8)) : z4;
-      const uint32_t we[4] = {e0.x, e0.y, e0.z, e0.w}, wo[4] = {o0.x, o0.y, o0.z, o0.w};
-      const uint32_t xe[4] = {e1.x, e1.y, e1.z, e1.w}, xo[4] = {o1.x, o1.y, o1.z, o1.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t a0, a1, a2, a3;
-        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a0) : "r"(we[j]), "r"(wo[j]));
-        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a1) : "r"(we[j]), "r"(wo[j]));
-        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a2) : "r"(xe[j]), "r"(xo[j]));
-        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a3) : "r"(xe[j]), "r"(xo[j]));
-        mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pb0, pb1);
-        if constexpr (C::PSPLIT) mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pl[0], pl[1]);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  if constexpr (STG) {
+    if (cta_iters > 0) stage(0, 0);
+  }
+
+  for (int it = 0; it < cta_iters; ++it) {
+    if constexpr (STG) {
+      if (it + 1 < cta_iters) {
+        stage(it + 1, (it + 1) & 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
       }
+      __syncthreads();  // tile it has landed for every thread's copies
     }
+    const int64_t tile = ROWS ? (int64_t)it : tile_begin + (int64_t)it * C::NP + group;
+    const bool active = tile < tile_end;  // uniform across the warps of a group
+    if constexpr (!STG) {
+      if (!active) break;
+    }
+    if (active) {
+      const int64_t tpos = tile * kTile;
+      // ---- S^T = K Q^T ----
+      float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const __half* k0p = kb + (tpos + g) * D + 8 * t;
+      const __half* k1p = kb + (tpos + g + 8) * D + 8 * t;
+#pragma unroll
+      for (int i = 0; i < C::NB_W; ++i) {
+        const int blk = wh * C::NB_W + i;
+        uint4 k0, k1;
+        if constexpr (STG) {
+          // rows g and g + 8 share the swizzle (r & 7 = g)
+          const uint32_t off = (((blk * 4 + t) ^ (g << 2)) << 4) + stg0 + (it & 1) * 32768;
+          k0 = lds128(off + g * 1024);
+          k1 = lds128(off + (g + 8) * 1024);
+        } else {
+          k0 = __ldg(reinterpret_cast<const uint4*>(k0p + blk * 32));
+          k1 = __ldg(reinterpret_cast<const uint4*>(k1p + blk * 32));
+        }
+        mma16816(S, k0.x, k1.x, k0.y, k1.y, qf[i][0], qf[i][1]);
+        mma16816(S, k0.z, k1.z, k0.w, k1.w, qf[i][2], qf[i][3]);
+      }
+      if constexpr (C::WT >= 2) exchange_S<C::WT>(S, xbuf, group, wh, it & 1, lane);
+      uint32_t pb0, pb1, pl[2] = {0u, 0u};
+      softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lo0, lim0, lo1, lim1, a.scale_log2, 1.0f, 1.0f, st, acc, pb0,
+                                       pb1, pl);
+      // ---- O^T += V^T P^T: lane reads positions 2t, 2t+1, 2t+8, 2t+9 ----
+      const __half* vp = vb + tpos * D + dbase;
+      // Rows at or past seq_len may hold any bytes (a NaN there would reach O
+      // through P = 0): they enter as zero.
+      const int64_t vrem = seqlen - tpos;
+      const bool ve0 = 2 * t < vrem, vo0 = 2 * t + 1 < vrem, ve1 = 2 * t + 8 < vrem, vo1 = 2 * t + 9 < vrem;
+      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c4 = 0; c4 < C::MT_W / 4; ++c4) {
+        uint4 e0, o0, e1, o1;
+        if constexpr (STG) {
+          // chunk 8 g + 4 wh + c4 of rows 2t, 2t+1, 2t+8, 2t+9: ((r >> 1) & 3) = t for all four
+          const uint32_t sv = stg0 + (it & 1) * 32768 + 16384 +
+                              (((8 * g + 4 * wh + c4) ^ ((g + 2 * t) & 7)) << 4);
+          e0 = ve0 ? lds128(sv + (2 * t) * 1024) : z4;
+          o0 = vo0 ? lds128(sv + (2 * t + 1) * 1024) : z4;
+          e1 = ve1 ? lds128(sv + (2 * t + 8) * 1024) : z4;
+          o1 = vo1 ? lds128(sv + (2 * t + 9) * 1024) : z4;
+        } else {
+          e0 = ve0 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t) * D + c4 * 8)) : z4;
+          o0 = vo0 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 1) * D + c4 * 8)) : z4;
+          e1 = ve1 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 8) * D + c4 * 8)) : z4;
+          o1 = vo1 ? __ldg(reinterpret_cast<const uint4*>(vp + (2 * t + 9) * D + c4 * 8)) : z4;
+        }
+        const uint32_t we[4] = {e0.x, e0.y, e0.z, e0.w}, wo[4] = {o0.x, o0.y, o0.z, o0.w};
+        const uint32_t xe[4] = {e1.x, e1.y, e1.z, e1.w}, xo[4] = {o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t a0, a1, a2, a3;
+          asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a0) : "r"(we[j]), "r"(wo[j]));
+          asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a1) : "r"(we[j]), "r"(wo[j]));
+          asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a2) : "r"(xe[j]), "r"(xo[j]));
+          asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a3) : "r"(xe[j]), "r"(xo[j]));
+          mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pb0, pb1);
+          if constexpr (C::PSPLIT) mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pl[0], pl[1]);
+        }
+      }
+    }  // active
+    if constexpr (STG) __syncthreads();  // the buffer of tile it is staged again at it + 2
   }
 
   if (late_wait) griddep_wait();  // the prior partial (or the prefix's slots) is complete
