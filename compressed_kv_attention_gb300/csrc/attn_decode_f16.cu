@@ -21,7 +21,9 @@ struct FDec : DecodeShape<D> {
   static constexpr int RED_BYTES = Sh::NP * Sh::RED_FLOATS * 4;
   static constexpr int OFF_XCHG = (RED_BYTES + 127) / 128 * 128;
   static constexpr int OFF_ML = OFF_XCHG + Sh::XCHG_BYTES;
-  static constexpr int SMEM = OFF_ML + Sh::NP * 16 * 4;
+  // D = 512, split form: each tile group's K and V tile (32 KB) staged here.
+  static constexpr int OFF_STG = (OFF_ML + Sh::NP * 16 * 4 + 1023) / 1024 * 1024;
+  static constexpr int SMEM = D == 512 ? OFF_STG + Sh::NP * 32768 : OFF_ML + Sh::NP * 16 * 4;
 };
 
 // Epilogue of the row-parallel form: group q holds the 8 rows of row group
@@ -189,6 +191,33 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
   constexpr bool STG = ROWS && D == 512;
   static_assert(!STG || (C::THREADS == 256 && C::MT_W == 16 && C::RED_BYTES >= 65536), "staging layout");
   const uint32_t stg0 = smem_u32(smem);
+  // Split form at D = 512: the NP groups walk different tiles, so each group
+  // stages its own: K of its next tile is copied (cp.async, by the group's 64
+  // threads, same swizzles) as soon as both warps have read the current K (at
+  // the S exchange), and V of its next tile once both have read the current V,
+  // so the copies overlap the softmax and P.V of this tile and the S of the
+  // next. Group barriers only: a group that has run out of tiles leaves the
+  // loop on its own.
+  constexpr bool STS = !ROWS && D == 512;
+  const uint32_t sgk = smem_u32(smem) + C::OFF_STG + group * 32768, sgv = sgk + 16384;
+  const int gtid = wh * 32 + lane;
+  auto stage_rows = [&](const __half* src, uint32_t dst, bool is_v) {
+#pragma unroll 4
+    for (int r = 0; r < kTile; ++r) {
+      const int c = gtid;  // chunk: 64 threads x 16 bytes = one 1 KB row
+      const int cs = is_v ? (c ^ (((c >> 3) + 2 * ((r >> 1) & 3)) & 7)) : (c ^ ((r & 7) << 2));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + r * 1024 + (cs << 4)),
+                   "l"(src + r * D + c * 8) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  if constexpr (STS) {
+    const int64_t t0 = tile_begin + group;
+    if (n_iters > 0 && t0 < tile_end) {
+      stage_rows(kb + t0 * kTile * D, sgk, false);
+      stage_rows(vb + t0 * kTile * D, sgv, true);
+    }
+  }
   int cta_iters = n_iters;
   if constexpr (STG) {
     __shared__ int s_iters;
@@ -232,6 +261,13 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
     if constexpr (!STG) {
       if (!active) break;
     }
+    // STS: this tile's K and V are the group's two newest copy groups or older
+    const int64_t next_tile = tile + C::NP;
+    const bool next_active = STS && it + 1 < n_iters && next_tile < tile_end;
+    if constexpr (STS) {
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // K landed (V may still be in flight)
+      named_bar(2 + group, 64);
+    }
     if (active) {
       const int64_t tpos = tile * kTile;
       // ---- S^T = K Q^T ----
@@ -242,9 +278,9 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
       for (int i = 0; i < C::NB_W; ++i) {
         const int blk = wh * C::NB_W + i;
         uint4 k0, k1;
-        if constexpr (STG) {
+        if constexpr (STG || STS) {
           // rows g and g + 8 share the swizzle (r & 7 = g)
-          const uint32_t off = (((blk * 4 + t) ^ (g << 2)) << 4) + stg0 + (it & 1) * 32768;
+          const uint32_t off = (((blk * 4 + t) ^ (g << 2)) << 4) + (STG ? stg0 + (it & 1) * 32768 : sgk);
           k0 = lds128(off + g * 1024);
           k1 = lds128(off + (g + 8) * 1024);
         } else {
@@ -255,6 +291,11 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
         mma16816(S, k0.z, k1.z, k0.w, k1.w, qf[i][2], qf[i][3]);
       }
       if constexpr (C::WT >= 2) exchange_S<C::WT>(S, xbuf, group, wh, it & 1, lane);
+      if constexpr (STS) {
+        // both warps are past their K reads (the exchange's barrier): stage the next K
+        if (next_active) stage_rows(kb + next_tile * kTile * D, sgk, false);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
+      }
       uint32_t pb0, pb1, pl[2] = {0u, 0u};
       softmax_tile<C::MT_W, C::PSPLIT>(S, tpos, g, lo0, lim0, lo1, lim1, a.scale_log2, 1.0f, 1.0f, st, acc, pb0,
                                        pb1, pl);
@@ -265,12 +306,16 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
       const int64_t vrem = seqlen - tpos;
       const bool ve0 = 2 * t < vrem, vo0 = 2 * t + 1 < vrem, ve1 = 2 * t + 8 < vrem, vo1 = 2 * t + 9 < vrem;
       const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (STS) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // V landed (the next K may still be in flight)
+        named_bar(2 + group, 64);
+      }
 #pragma unroll
       for (int c4 = 0; c4 < C::MT_W / 4; ++c4) {
         uint4 e0, o0, e1, o1;
-        if constexpr (STG) {
+        if constexpr (STG || STS) {
           // chunk 8 g + 4 wh + c4 of rows 2t, 2t+1, 2t+8, 2t+9: ((r >> 1) & 3) = t for all four
-          const uint32_t sv = stg0 + (it & 1) * 32768 + 16384 +
+          const uint32_t sv = (STG ? stg0 + (it & 1) * 32768 + 16384 : sgv) +
                               (((8 * g + 4 * wh + c4) ^ ((g + 2 * t) & 7)) << 4);
           e0 = ve0 ? lds128(sv + (2 * t) * 1024) : z4;
           o0 = vo0 ? lds128(sv + (2 * t + 1) * 1024) : z4;
@@ -295,9 +340,15 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
           if constexpr (C::PSPLIT) mma16816(acc[c4 * 4 + j], a0, a1, a2, a3, pl[0], pl[1]);
         }
       }
+      if constexpr (STS) {
+        named_bar(2 + group, 64);  // both warps are past their V reads: stage the next V
+        if (next_active) stage_rows(vb + next_tile * kTile * D, sgv, true);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
+      }
     }  // active
     if constexpr (STG) __syncthreads();  // the buffer of tile it is staged again at it + 2
   }
+  if constexpr (STS) asm volatile("cp.async.wait_group 0;" ::: "memory");
 
   if (late_wait) griddep_wait();  // the prior partial (or the prefix's slots) is complete
   if constexpr (ROWS) {
