@@ -87,6 +87,7 @@ class _Fanout:
     (256, 2, 4, 0, 0, 96, [96, 50, 96, 3]),                  # no prefix
     (64, 1, 40, 1000, 1000, 64, None),                       # many agents: two prefix splits
     (512, 1, 3, 48, 33, 32, [32, 1, 0]),                     # prefix and tails shorter than one record
+    (64, 1, 80, 512, 512, 32, None),                         # too many tails to run beside: the composed form
 ])
 def test_fanout_matches_oracle(D, Hkv, A, P_max, P, TL, tails):
     _need_gpu()

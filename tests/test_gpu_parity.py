@@ -163,6 +163,24 @@ def test_decode_shapes_ragged(D, Hkv, Hq, n_q, n_split):
     H.check_attention(o, l, o_ref, lse_ref, f"D={D} Hq={Hq} n_q={n_q} split={n_split}")
 
 
+def test_decode_at_the_split_limit():
+    """The largest split count (1024): one 16-token tile per CTA, the merge
+    tree over 1024 slots (32 leaves of 32), a grid that does not fit at once;
+    and one more split than that is refused."""
+    _need_gpu()
+    D, Hkv, Hq, B, T = 128, 1, 4, 2, 1024 * 16
+    seq_lens = [T, 1000]
+    k, v, outl = make_kv(D, Hkv, B, T, seed=77, n_out=2)
+    q = inputs.normal_tensor((B, 1, Hq, D), 77, "q", outl)
+    signs = inputs.tbq_signs(D)
+    qs, d16, codes, n16, _ = oracle_cache(k, v, signs)
+    o_ref, lse_ref = oracle_decode_all(q, qs, d16, codes, n16, signs, seq_lens)
+    cache = gpu_pack(k, v, signs, T)
+    o, l = run_decode(cache, q, seq_lens, T, n_split=1024)
+    H.check_attention(o, l, o_ref, lse_ref, "n_split 1024")
+    assert ckv.attn_decode_workspace(cache, T, 1, Hq, 1025) == 0
+
+
 @pytest.mark.parametrize("D,Hkv,Hq,n_q,n_split", [(128, 2, 16, 4, 0), (512, 2, 16, 2, 0), (512, 2, 16, 8, 0),
                                                   (512, 1, 4, 5, 3), (128, 2, 2, 16, 0), (64, 1, 1, 3, 200)])
 def test_verify_decode_is_causal_among_the_batch(D, Hkv, Hq, n_q, n_split):
