@@ -278,17 +278,23 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
       s_lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
   }
-  griddep_wait();
-  // The next grid may begin only now: a grid that reads its inputs before its
-  // own wait (the fp16 decode with a prior partial) then runs beside this one
-  // alone, never beside the grids before it, which may still write them.
-  griddep_launch_dependents();
+  // Inputs that no kernel writes (early_inputs: the page-locked host Q and
+  // new rows of a host-buffer step) are loaded before the wait, so their
+  // trips across the host link overlap the previous grid's last work.
+  if (!a.early_inputs) {
+    griddep_wait();
+    // The next grid may begin only now: a grid that reads its inputs before
+    // its own wait (the fp16 decode with a prior partial) then runs beside
+    // this one alone, never beside the grids before it, which may still
+    // write them.
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) s_seq = a.seq_len[b];
+  }
 
   // Query fragments first: issued before the producer starts its bulk copies,
   // these small loads do not queue behind them. The sequence length is read by
   // one thread per CTA (every CTA of the grid reads the same few words) and
   // shared; for an append the producer warp also fetches the newest row now.
-  if (threadIdx.x == 0) s_seq = a.seq_len[b];
   pack::PositionInput<D> new_row;
   if (warp == C::NCW && a.n_new > 0) {
     const int64_t j = a.n_new - 1;
@@ -308,6 +314,11 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
     const int q_src = (DCA && qi > 2) ? 2 : qi;
     const __half* qrow = a.q + ((int64_t)(b * q_tokens + q_src) * a.n_q_heads + h) * D;
     load_q_frags<C::NB_W>(qf, qrow, ok, wh * C::NB_W, t);
+  }
+  if (a.early_inputs) {
+    griddep_wait();
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) s_seq = a.seq_len[b];
   }
 
   // For a plain decode the producer lane issues the first stages before the

@@ -269,14 +269,17 @@ struct AppendRows {
   int64_t token_stride, batch_stride;
 };
 
-// The fan-out's link between its two decodes (see ckv_attn_decode_fanout):
-// the prefix decode writes slots only; the tail decode merges ext_n of them
-// per row group and raises its errors in the prefix decode's flag word.
-struct FanoutLink {
+// Launch options beyond the common arguments. The fan-out's link between its
+// two decodes (see ckv_attn_decode_fanout): the prefix decode writes slots
+// only; the tail decode merges ext_n of them per row group and raises its
+// errors in the prefix decode's flag word. early_inputs: Q and the new rows
+// are page-locked host buffers, read before the wait for the previous grid.
+struct DecodeExtras {
   int slots_only;
   const float* ext_part;
   int ext_n, ext_nrg;
   int32_t* flag;
+  int early_inputs;
 };
 
 static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void* k16, const void* v16,
@@ -287,7 +290,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
                              int dca_chunk = 0, int q_bf16 = 0, int dca_parts = 0,
                              const float* prior_o = nullptr, const float* prior_lse = nullptr,
                              float* fold_out = nullptr, float* fold_lse = nullptr, int* host_folded = nullptr,
-                             const FanoutLink* link = nullptr) {
+                             const DecodeExtras* link = nullptr) {
   DecodePlan p;
   ckv_status s = plan_decode(D, Hkv, B, max_seq_len, n_q, n_q_heads, n_split, &p, prior_o ? 1 : 0);
   if (s != CKV_OK) return s;
@@ -358,6 +361,7 @@ static ckv_status run_decode(bool compressed, const ckv_cache* cache, const void
     a.ext_n = link->ext_n;
     a.ext_nrg = link->ext_nrg;
     if (link->flag) a.flag = link->flag;
+    a.early_inputs = link->early_inputs;
   }
   a.counters = reinterpret_cast<uint32_t*>(base + 64);
   a.out = out;
@@ -555,9 +559,12 @@ ckv_status ckv_attn_decode_append_host(const ckv_cache* cache, const int32_t* se
   if (!k || !v || !q || !o || !l)
     return fail(CKV_ERR_INVALID_ARG, "host buffers must be page-locked and mapped (cudaHostAlloc / pinned)");
   const int64_t tok = static_cast<int64_t>(cache->n_kv_heads) * cache->head_dim;
-  return ckv_attn_decode_append(cache, seq_len, max_seq_len, k, v, n_new, tok, tok * n_new, q, n_q, n_q_heads,
-                                scale, n_split, static_cast<float*>(o), static_cast<float*>(l), workspace, ws_bytes,
-                                stream);
+  const AppendRows app{k, v, n_new, tok, tok * n_new};
+  const DecodeExtras ex{0, nullptr, 0, 0, nullptr, 1};
+  return run_decode(true, cache, nullptr, nullptr, cache->head_dim, cache->n_kv_heads, cache->batch,
+                    cache->capacity, seq_len, max_seq_len, q, n_q, n_q_heads, scale, n_split, static_cast<float*>(o),
+                    static_cast<float*>(l), workspace, ws_bytes, stream, &app, 0, 0, 0, 0, nullptr, nullptr, nullptr,
+                    nullptr, nullptr, &ex);
 }
 
 size_t ckv_attn_decode_f16_workspace(int32_t head_dim, int32_t n_kv_heads, int32_t batch,
@@ -721,7 +728,7 @@ ckv_status ckv_attn_decode_fanout(const ckv_cache* prefix, const int32_t* prefix
     s = ckv_attn_decode(prefix, prefix_len, max_prefix_len, q_f16, n_agents, n_q_heads, scale, 0, o_pre, l_pre,
                         base + w.pre, w.tail - w.pre, stream);
     if (s != CKV_OK) return s;
-    FanoutLink fl{0, nullptr, 0, 0, reinterpret_cast<int32_t*>(base + w.pre)};  // one flag word for the step
+    DecodeExtras fl{0, nullptr, 0, 0, reinterpret_cast<int32_t*>(base + w.pre), 0};  // one flag word for the step
     return run_decode(false, nullptr, k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, max_tail_len, q_f16,
                       1, n_q_heads, scale, 0, out, lse, base + w.tail, w.o_pre - w.tail, stream, nullptr, 0, 0, 0, 0,
                       o_pre, l_pre, nullptr, nullptr, nullptr, &fl);
@@ -732,13 +739,13 @@ ckv_status ckv_attn_decode_fanout(const ckv_cache* prefix, const int32_t* prefix
   DecodePlan pp;
   s = plan_decode(D, Hkv, 1, max_prefix_len, n_agents, n_q_heads, w.ps, &pp);
   if (s != CKV_OK) return s;
-  FanoutLink pl{1, nullptr, 0, 0, nullptr};
+  DecodeExtras pl{1, nullptr, 0, 0, nullptr, 0};
   s = run_decode(true, prefix, nullptr, nullptr, D, Hkv, 1, prefix->capacity, prefix_len, max_prefix_len, q_f16,
                  n_agents, n_q_heads, scale, w.ps, out, lse, base + w.pre, w.tail - w.pre, stream, nullptr, 0, 0, 0,
                  0, nullptr, nullptr, nullptr, nullptr, nullptr, &pl);
   if (s != CKV_OK) return s;
-  FanoutLink tl{0, reinterpret_cast<const float*>(base + w.pre + ws_header_bytes(pp.groups, pp.n_split)),
-                pp.n_split, pp.n_row_groups, reinterpret_cast<int32_t*>(base + w.pre)};
+  DecodeExtras tl{0, reinterpret_cast<const float*>(base + w.pre + ws_header_bytes(pp.groups, pp.n_split)),
+                  pp.n_split, pp.n_row_groups, reinterpret_cast<int32_t*>(base + w.pre), 0};
   return run_decode(false, nullptr, k_tail, v_tail, D, Hkv, n_agents, tail_capacity, tail_len, max_tail_len, q_f16,
                     1, n_q_heads, scale, w.ts, out, lse, base + w.tail, w.o_pre - w.tail, stream, nullptr, 0, 0, 0, 0,
                     nullptr, nullptr, nullptr, nullptr, nullptr, &tl);

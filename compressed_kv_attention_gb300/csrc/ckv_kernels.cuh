@@ -83,6 +83,9 @@ struct DecodeArgs {
   // the same 8 rows: ext_part + ((kvh * ext_nrg + b) * ext_n + s) * slot.
   const float* ext_part;
   int ext_n, ext_nrg;
+  // Compressed decode: q, k_new and v_new are written by no kernel (page-locked
+  // host buffers), so they are loaded before the wait for the previous grid.
+  int early_inputs;
   int rendezvous;            // 1: every CTA resident at once, merge by rendezvous
   int32_t* flag;
   uint32_t* counters;        // ctr_stride words per group, zero between calls

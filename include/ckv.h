@@ -313,9 +313,12 @@ CKV_API ckv_status ckv_attn_decode_append(const ckv_cache* cache, const int32_t*
  * address space (cudaHostAlloc or cudaHostRegister; with unified addressing
  * their device address is the host address): anything else is refused with
  * CKV_ERR_INVALID_ARG before any launch. The results are in host memory once
- * `stream` has completed. seq_len stays a device array. Other arguments and
- * errors as attn_decode_append. No counterpart in the pages: it is the host
- * side of a serving loop.
+ * `stream` has completed. seq_len stays a device array. The kernel reads q,
+ * k_new and v_new before it waits for the previous kernel on the stream (no
+ * kernel writes them), so their trips across the interconnect overlap that
+ * kernel's last work; the host must have written them before this call, as
+ * for any launch. Other arguments and errors as attn_decode_append. No
+ * counterpart in the pages: it is the host side of a serving loop.
  */
 CKV_API ckv_status ckv_attn_decode_append_host(const ckv_cache* cache, const int32_t* seq_len, int64_t max_seq_len,
                                                const void* k_new_host, const void* v_new_host, int32_t n_new,
