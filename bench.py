@@ -56,12 +56,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel sources whose hash is recorded beside it (null once they change).
 # Fan-out and prefill: the sum over the step's kernels (their rooflines time the whole step).
 NCU_TRAFFIC = {
-    "gemma4_decode": {"bytes": 48516864 + 256, "source_sha": "02a419c12d3fd9b7"},
-    "tiny_decode": {"bytes": 123392, "source_sha": "02a419c12d3fd9b7"},
-    "long_decode": {"bytes": 1548166912 + 3258880, "source_sha": "02a419c12d3fd9b7"},
-    "fanout_decode": {"bytes": 6402816 + 33744384, "source_sha": "795bc95941ed29b4"},
-    "chunked_prefill": {"bytes": 8454912 + (122628096 + 62078464) + (106606080 + 23781888),
-                        "source_sha": "2b0a5b078e13c7bc"},
+    "gemma4_decode": {"bytes": 48518400 + 512, "source_sha": "32e9d0e931b98782"},
+    "tiny_decode": {"bytes": 126208, "source_sha": "32e9d0e931b98782"},
+    "long_decode": {"bytes": 1547973376 + 3558144, "source_sha": "32e9d0e931b98782"},
+    "fanout_decode": {"bytes": 6411008 + 33744384, "source_sha": "d12984d39ccabf29"},
+    "chunked_prefill": {"bytes": 8451072 + (123420928 + 67802880) + (106605568 + 23612160),
+                        "source_sha": "cdade01ace9bef23"},
 }
 
 _DECODE_SOURCES = ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh",
