@@ -356,8 +356,12 @@ __global__ void __launch_bounds__(FDec<D>::THREADS, 1) attn_decode_f16_kernel(De
                      blockIdx.y * C::NP);
   } else {
     const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
+    // One split and nothing to merge in: the rows go out directly.
+    const bool direct = a.n_split == 1 && !a.prior_o && !a.ext_part;
     decode_epilogue<typename C::Sh, C::MT_W>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp, lane,
-                                             nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D));
+                                             nullptr, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
+                                             kCentroidScale, nullptr, direct ? &a : nullptr, b, kvh, rg);
+    if (direct) return;
     if (a.prior_o && split == 0) write_prior_slot<D>(a, gid, b, kvh, rg, tid, C::THREADS);
     decode_split_tail<D, C::RED_BYTES, C::THREADS>(a, split, gid, b, kvh, rg, tid, smem);
   }

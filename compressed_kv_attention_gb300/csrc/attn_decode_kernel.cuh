@@ -546,10 +546,12 @@ __global__ void __launch_bounds__(CDec<D, B, ROT>::THREADS, 1) attn_decode_kerne
   }
 
   const int64_t gid = (int64_t)(b * a.n_kv_heads + kvh) * a.n_row_groups + rg;
+  // One split and nothing to merge across row groups: the rows go out directly.
+  const bool direct = a.n_split == 1 && !a.dca_fold && !a.slots_only;
   decode_epilogue<typename C::Sh, C::MT_W, ROT>(st, acc, reinterpret_cast<float*>(smem), mlbuf, group, wh, warp,
                                                 lane, a.signs, a.part + (gid * a.n_split + split) * merge_slot_floats(D),
-                                                centroid_scale(B), a.signs2);
-  if (a.slots_only) return;  // the fan-out's tail decode merges these slots
+                                                centroid_scale(B), a.signs2, direct ? &a : nullptr, b, kvh, rg);
+  if (direct || a.slots_only) return;  // slots_only: the fan-out's tail decode merges these slots
   decode_split_tail<D, C::RING, 256>(a, split, gid, b, kvh, rg, tid, smem);
 }
 

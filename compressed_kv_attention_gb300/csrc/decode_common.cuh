@@ -237,11 +237,19 @@ __device__ __forceinline__ void derotate_store_row(float2 (&v)[D / 64], int lane
 // Each group stores its unscaled accumulators with its own (m, l); warp r < 8
 // owns row r and rescales the groups while summing them (other warps are done
 // after the second barrier).
+__device__ __forceinline__ void row_outputs(const DecodeArgs& a, int b, int kvh, int rg, int r, float** o,
+                                            float** l);
+
+// With `direct` (a launch of one split and nothing to merge) the rows go
+// straight to the outputs of row group (b, kvh, rg), normalised, with their
+// lse, instead of to the slot.
 template <typename Sh, int MTW, int ROT = 0>
 __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MTW][4], float* red,
                                                 float* mlbuf, int group, int wh, int warp, int lane,
                                                 const int8_t* signs, float* slot,
-                                                float vscale = kCentroidScale, const int8_t* signs2 = nullptr) {
+                                                float vscale = kCentroidScale, const int8_t* signs2 = nullptr,
+                                                const DecodeArgs* direct = nullptr, int b = 0, int kvh = 0,
+                                                int rg = 0) {
   constexpr int D = Sh::DIM;
   const int g = lane >> 2, t = lane & 3;
   // Reduce the row sums over the 8 lanes that share rows (2t, 2t+1).
@@ -295,6 +303,18 @@ __device__ __forceinline__ void decode_epilogue(SoftmaxState st, float (&acc)[MT
       x.y = fmaf(fq[q], y.y, x.y);
     }
     v[e] = x;
+  }
+  if (direct) {
+    float* orow;
+    float* lrow;
+    row_outputs(*direct, b, kvh, rg, r, &orow, &lrow);
+    if (!orow) return;
+    const float inv = lc > 0.0f ? 1.0f / lc : 0.0f;
+#pragma unroll
+    for (int e = 0; e < E2; ++e) v[e] = make_float2(v[e].x * inv, v[e].y * inv);
+    derotate_store_row<D, ROT>(v, lane, signs, orow, vscale, signs2);
+    if (lane == 0) *lrow = lc > 0.0f ? (mc + log2f(lc)) * 0.6931471805599453f : -INFINITY;
+    return;
   }
   derotate_store_row<D, ROT>(v, lane, signs, slot + r * D, vscale, signs2);
   if (lane == 0) {
