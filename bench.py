@@ -56,12 +56,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel sources whose hash is recorded beside it (null once they change).
 # Fan-out and prefill: the sum over the step's kernels (their rooflines time the whole step).
 NCU_TRAFFIC = {
-    "gemma4_decode": {"bytes": 48518400 + 512, "source_sha": "32e9d0e931b98782"},
-    "tiny_decode": {"bytes": 126208, "source_sha": "32e9d0e931b98782"},
-    "long_decode": {"bytes": 1547973376 + 3558144, "source_sha": "32e9d0e931b98782"},
-    "fanout_decode": {"bytes": 6411008 + 33744384, "source_sha": "d12984d39ccabf29"},
-    "chunked_prefill": {"bytes": 8451072 + (123420928 + 67802880) + (106605568 + 23612160),
-                        "source_sha": "cdade01ace9bef23"},
+    "gemma4_decode": {"bytes": 48518912, "source_sha": "13626d8ac99541f9"},
+    "tiny_decode": {"bytes": 116736, "source_sha": "13626d8ac99541f9"},
+    "long_decode": {"bytes": 1547972096 + 3602432, "source_sha": "13626d8ac99541f9"},
+    "fanout_decode": {"bytes": 6405120 + 33743616, "source_sha": "c19b11ad11052ba4"},
+    "chunked_prefill": {"bytes": 8451328 + (121211392 + 61330688) + (106605824 + 23828736),
+                        "source_sha": "ae568074c9611238"},
 }
 
 _DECODE_SOURCES = ("attn_decode.cu", "attn_decode_kernel.cuh", "decode_common.cuh", "ckv_device.cuh",
